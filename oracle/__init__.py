@@ -1,0 +1,387 @@
+"""CPU oracle for the S3R / S3R-EC INT8 backward -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  The CUDA library never calls it and shares no code
+with it.  The arithmetic lives in ``s3r_oracle.c`` (plain single-threaded C);
+this module builds it with gcc, loads it with ctypes, and composes its pieces
+into the linear-layer and SwiGLU-FFN backward passes step by step, in the order
+of the S3R paper ("Efficient Quantization Training with Stochastic Rounding via
+Structured Subspace Randomness", §III-A to §III-D).
+
+Parity pins: every function here is pinned by a ``-m "not gpu"`` test in
+``tests/test_oracle_*.py`` (worked example, closed forms, invariants, library
+routines, brute force).  Whole-pipeline training quality (the paper's Tables I
+and II) is *parity unpinned*: it needs the C4 data set and trained checkpoints.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "s3r_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liborc_s3r.so")
+_lock = threading.Lock()
+_lib = None
+
+RTNE, S3R, INDEP = 0, 1, 2
+EC_NONE, EC_DX_ONLY, EC_TWO_WAY, EC_DX_TOKEN_ONLY = 0, 1, 2, 3
+TILE = 128
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fused multiply-add contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                               "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = C.CDLL(build())
+            L = _lib
+            L.orc_word_to_unit.restype = C.c_float
+            L.orc_word_to_unit.argtypes = [C.c_uint32]
+            L.orc_token_threshold.restype = C.c_float
+            L.orc_token_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
+            L.orc_element_threshold.restype = C.c_float
+            L.orc_element_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
+            L.orc_sr_step.restype = C.c_float
+            L.orc_sr_step.argtypes = [C.c_float, C.c_float]
+            L.orc_expf.restype = C.c_float
+            L.orc_expf.argtypes = [C.c_float]
+            L.orc_sigmoidf.restype = C.c_float
+            L.orc_sigmoidf.argtypes = [C.c_float]
+            L.orc_quantize.restype = C.c_int
+            L.orc_rtne_operand.restype = C.c_int
+            L.orc_error_stats.restype = C.c_int
+        return _lib
+
+
+def _p(a):
+    return None if a is None else C.c_void_p(a.ctypes.data)
+
+
+def _f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _i64(x):
+    return C.c_int64(int(x))
+
+
+# --------------------------------------------------------------------------
+# primitives
+# --------------------------------------------------------------------------
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
+
+
+def word_to_unit(w: int) -> float:
+    return lib().orc_word_to_unit(int(w) & 0xFFFFFFFF)
+
+
+def token_threshold(t: int, seed: int, tensor_id: int) -> float:
+    return lib().orc_token_threshold(int(t), int(seed), int(tensor_id))
+
+
+def element_threshold(e: int, seed: int, tensor_id: int) -> float:
+    return lib().orc_element_threshold(int(e), int(seed), int(tensor_id))
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32, exactly."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float32)
+    lib().orc_bf16_array_to_float(_p(b), _i64(b.size), _p(out))
+    return out
+
+
+def from_torch_bf16(t) -> np.ndarray:
+    """A torch bf16 CPU tensor -> float32 numpy, via the oracle's own widening."""
+    import torch
+    return bf16_to_f32(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def sr_step(y: float, u: float) -> float:
+    """One stochastic rounding of y to the unit grid with threshold u."""
+    return lib().orc_sr_step(float(y), float(u))
+
+
+def expf(x: float) -> float:
+    return lib().orc_expf(float(x))
+
+
+def sigmoidf(x: float) -> float:
+    return lib().orc_sigmoidf(float(x))
+
+
+def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, TILE)):
+    """Fold, tile-scale and round G (float32 [T, N]).
+
+    Returns (Q int8 [T,N], delta f32 [ceil(T/tr), ceil(N/tc)], E f32 [T,N], status)."""
+    G = _f32(G)
+    T, N = G.shape
+    tr, tc = tile
+    ntr, ntc = -(-T // tr), -(-N // tc)
+    Q = np.zeros((T, N), dtype=np.int8)
+    delta = np.zeros((ntr, ntc), dtype=np.float32)
+    E = np.zeros((T, N), dtype=np.float32)
+    st = lib().orc_quantize(_p(G), _i64(T), _i64(N), _i64(N), _p(_f32(s_x)), _p(_f32(s_w)), C.c_int(mode),
+                            C.c_uint64(seed), C.c_uint32(tensor_id), _i64(tr), _i64(tc), _p(Q), _p(delta), _p(E))
+    return Q, delta, E, st
+
+
+def rtne_operand(A, axis: int):
+    """Forward RTNE operand with a per-row (axis 0) or per-column (axis 1) scale."""
+    A = _f32(A)
+    R, Cc = A.shape
+    Q = np.zeros((R, Cc), dtype=np.int8)
+    scale = np.zeros(R if axis == 0 else Cc, dtype=np.float32)
+    st = lib().orc_rtne_operand(_p(A), _i64(R), _i64(Cc), _i64(Cc), C.c_int(axis), _p(Q), _p(scale))
+    if st != 0:
+        raise ValueError(f"orc_rtne_operand status {st}")
+    return Q, scale
+
+
+def error_partials(E, tile=(TILE, TILE)):
+    E = _f32(E)
+    T, N = E.shape
+    tr, tc = tile
+    tok = np.zeros((T, -(-N // tc)), dtype=np.float64)
+    col = np.zeros((-(-T // tr), N), dtype=np.float64)
+    lib().orc_error_partials(_p(E), _i64(T), _i64(N), _i64(tr), _i64(tc), _p(tok), _p(col))
+    return tok, col
+
+
+def error_stats(E, S: int):
+    E = _f32(E)
+    T, N = E.shape
+    B = T // S
+    eps = np.zeros(T, dtype=np.float64)
+    colmean = np.zeros((B, N), dtype=np.float64)
+    mu = np.zeros(B, dtype=np.float64)
+    st = lib().orc_error_stats(_p(E), _i64(T), _i64(N), _i64(S), _p(eps), _p(colmean), _p(mu))
+    if st != 0:
+        raise ValueError("T must be a multiple of S")
+    return eps, colmean, mu
+
+
+def ec_factors(eps, colmean, mu, S: int, W8, X8=None):
+    W8 = np.ascontiguousarray(W8, dtype=np.int8)
+    K, N = W8.shape
+    T = eps.shape[0]
+    B = T // S
+    rowsum = np.zeros(K, dtype=np.int64)
+    v = np.zeros((B, K), dtype=np.float64)
+    xsum = np.zeros((B, K), dtype=np.int64)
+    p = np.zeros(K, dtype=np.float64)
+    X8c = None if X8 is None else np.ascontiguousarray(X8, dtype=np.int8)
+    lib().orc_ec_factors(_p(np.ascontiguousarray(eps, dtype=np.float64)),
+                         _p(np.ascontiguousarray(colmean, dtype=np.float64)),
+                         _p(np.ascontiguousarray(mu, dtype=np.float64)),
+                         _i64(T), _i64(N), _i64(S), _p(W8), _p(X8c), _i64(K), _p(rowsum), _p(v), _p(xsum), _p(p))
+    return rowsum, v, xsum, p
+
+
+def dx_blocks(Q, W8, rows, blk=TILE):
+    Q = np.ascontiguousarray(Q, dtype=np.int8)
+    W8 = np.ascontiguousarray(W8, dtype=np.int8)
+    T, N = Q.shape
+    K = W8.shape[0]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    nkb = -(-N // blk)
+    out = np.zeros((rows.size, K, nkb), dtype=np.int32)
+    lib().orc_dx_blocks(_p(Q), _p(W8), _i64(T), _i64(N), _i64(K), _i64(blk), _p(rows), _i64(rows.size), _p(out))
+    return out
+
+
+def dw_blocks(X8, Q, krows, blk=TILE):
+    X8 = np.ascontiguousarray(X8, dtype=np.int8)
+    Q = np.ascontiguousarray(Q, dtype=np.int8)
+    T, K = X8.shape
+    N = Q.shape[1]
+    krows = np.ascontiguousarray(krows, dtype=np.int64)
+    ntb = -(-T // blk)
+    out = np.zeros((krows.size, N, ntb), dtype=np.int32)
+    lib().orc_dw_blocks(_p(X8), _p(Q), _i64(T), _i64(K), _i64(N), _i64(blk), _p(krows), _i64(krows.size), _p(out))
+    return out
+
+
+def dx(Q, delta, W8, s_x, ec_mode, eps, rowsum, v, S, rows, tile=(TILE, TILE)):
+    Q = np.ascontiguousarray(Q, dtype=np.int8)
+    W8 = np.ascontiguousarray(W8, dtype=np.int8)
+    T, N = Q.shape
+    K = W8.shape[0]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.zeros((rows.size, K), dtype=np.float64)
+    f64 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+    i64 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.int64)
+    lib().orc_dx(_p(Q), _p(_f32(delta)), _p(W8), _i64(T), _i64(N), _i64(K), _i64(tile[0]), _i64(tile[1]),
+                 _p(_f32(s_x)), C.c_int(ec_mode), _p(f64(eps)), _p(i64(rowsum)), _p(f64(v)), _i64(S),
+                 _p(rows), _i64(rows.size), _p(out))
+    return out
+
+
+def dw(X8, Q, delta, s_w, ec_mode, colmean, mu, xsum, p, S, krows, tile=(TILE, TILE)):
+    X8 = np.ascontiguousarray(X8, dtype=np.int8)
+    Q = np.ascontiguousarray(Q, dtype=np.int8)
+    T, K = X8.shape
+    N = Q.shape[1]
+    krows = np.ascontiguousarray(krows, dtype=np.int64)
+    out = np.zeros((krows.size, N), dtype=np.float64)
+    f64 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+    i64 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.int64)
+    lib().orc_dw(_p(X8), _p(Q), _p(_f32(delta)), _i64(T), _i64(K), _i64(N), _i64(tile[0]), _i64(tile[1]),
+                 _p(_f32(s_w)), C.c_int(ec_mode), _p(f64(colmean)), _p(f64(mu)), _p(i64(xsum)), _p(f64(p)), _i64(S),
+                 _p(krows), _i64(krows.size), _p(out))
+    return out
+
+
+def swiglu_bwd(dA, h1, h3):
+    dA, h1, h3 = _f32(dA), _f32(h1), _f32(h3)
+    dh1 = np.empty_like(dA)
+    dh3 = np.empty_like(dA)
+    lib().orc_swiglu_bwd(_p(dA), _p(h1), _p(h3), _i64(dA.size), _p(dh1), _p(dh3))
+    return dh1, dh3
+
+
+# --------------------------------------------------------------------------
+# composition: one linear layer's backward ([S3R] §III-A .. §III-D)
+# --------------------------------------------------------------------------
+@dataclass
+class LinearBackward:
+    Q: np.ndarray              # codes used by dX (and dW unless independent SR)
+    delta: np.ndarray
+    E: np.ndarray
+    Q_rhs: np.ndarray | None = None     # independent SR: codes used by dW
+    delta_rhs: np.ndarray | None = None
+    eps: np.ndarray | None = None
+    colmean: np.ndarray | None = None
+    mu: np.ndarray | None = None
+    rowsum: np.ndarray | None = None
+    v: np.ndarray | None = None
+    xsum: np.ndarray | None = None
+    p: np.ndarray | None = None
+    dX: np.ndarray | None = None        # [len(rows), K] float64
+    dW: np.ndarray | None = None        # [len(krows), N] float64
+    status: int = 0
+    extra: dict = field(default_factory=dict)
+
+
+RHS_ID_OFFSET = 0x100   # tensor-id offset of the second (dW) copy under independent SR
+
+
+def linear_backward(G, X8, s_x, W8, s_w, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0, tensor_id=0,
+                    rows=None, krows=None, tile=(TILE, TILE)) -> LinearBackward:
+    """Backward of Y = X W given the saved forward operands.
+
+    G: float32 [T, N] upstream gradient (exact widening of bf16).
+    X8 [T, K] int8 with s_x [T]; W8 [K, N] int8 with s_w [N].
+    rows / krows: which rows of dX / dW to produce (default: all).
+    """
+    G = _f32(G)
+    T, N = G.shape
+    K = W8.shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    krows = np.arange(K) if krows is None else np.asarray(krows)
+    Q, delta, E, st = quantize(G, s_x, s_w, mode, seed, tensor_id, tile)
+    out = LinearBackward(Q=Q, delta=delta, E=E, status=st)
+    use_ec = mode == S3R and ec_mode != EC_NONE
+    if mode == INDEP:
+        Qr, dr, _, st2 = quantize(G, s_x, s_w, INDEP, seed, tensor_id + RHS_ID_OFFSET, tile)
+        out.Q_rhs, out.delta_rhs, out.status = Qr, dr, st or st2
+    if use_ec:
+        out.eps, out.colmean, out.mu = error_stats(E, S)
+        out.rowsum, out.v, out.xsum, out.p = ec_factors(out.eps, out.colmean, out.mu, S, W8,
+                                                        X8 if ec_mode == EC_TWO_WAY else None)
+    em = ec_mode if use_ec else EC_NONE
+    out.dX = dx(Q, delta, W8, s_x, em, out.eps, out.rowsum, out.v, S, rows, tile)
+    Qw = out.Q_rhs if mode == INDEP else Q
+    dw_delta = out.delta_rhs if mode == INDEP else delta
+    out.dW = dw(X8, Qw, dw_delta, s_w, em, out.colmean, out.mu, out.xsum, out.p, S, krows, tile)
+    return out
+
+
+# --------------------------------------------------------------------------
+# composition: SwiGLU FFN block backward
+# --------------------------------------------------------------------------
+# Tensor ids of the three linears of one FFN block.
+TID_W2, TID_W1, TID_W3 = 0, 1, 2
+
+
+@dataclass
+class FFNForwardOperands:
+    X8: np.ndarray
+    s_x: np.ndarray
+    A8: np.ndarray
+    s_a: np.ndarray
+    W1_8: np.ndarray
+    s_w1: np.ndarray
+    W3_8: np.ndarray
+    s_w3: np.ndarray
+    W2_8: np.ndarray
+    s_w2: np.ndarray
+
+
+def ffn_forward_operands(X, W1, W3, W2, a) -> FFNForwardOperands:
+    """RTNE forward operands: per-token scales for X and a, per-output-channel
+    scales for the weights ([S3R] §III-A)."""
+    X8, s_x = rtne_operand(X, 0)
+    A8, s_a = rtne_operand(a, 0)
+    W1_8, s_w1 = rtne_operand(W1, 1)
+    W3_8, s_w3 = rtne_operand(W3, 1)
+    W2_8, s_w2 = rtne_operand(W2, 1)
+    return FFNForwardOperands(X8, s_x, A8, s_a, W1_8, s_w1, W3_8, s_w3, W2_8, s_w2)
+
+
+@dataclass
+class FFNBackward:
+    w2: LinearBackward
+    w1: LinearBackward
+    w3: LinearBackward
+    dA: np.ndarray          # [T, F] float32 as fed to the glue (all rows)
+    dh1: np.ndarray
+    dh3: np.ndarray
+    dX: np.ndarray          # [len(rows), d] float64
+    dW1: np.ndarray
+    dW2: np.ndarray
+    dW3: np.ndarray
+
+
+def ffn_backward(ops: FFNForwardOperands, h1, h3, dY, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0,
+                 rows=None, krows_d=None, krows_f=None) -> FFNBackward:
+    """SwiGLU FFN block backward: W2 linear, then the SwiGLU glue, then W1 and
+    W3 (dX = dX1 + dX3).  dA is needed for every token (the glue feeds the
+    second quantization), so the W2 activation gradient is computed in full
+    and rounded to fp32 before the glue, the precision the kernels hand on."""
+    T = dY.shape[0]
+    F = ops.A8.shape[1]
+    d = ops.X8.shape[1]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    krows_d = np.arange(d) if krows_d is None else np.asarray(krows_d)
+    krows_f = np.arange(F) if krows_f is None else np.asarray(krows_f)
+    w2 = linear_backward(dY, ops.A8, ops.s_a, ops.W2_8, ops.s_w2, S, mode, ec_mode, seed, TID_W2,
+                         rows=np.arange(T), krows=krows_f)
+    dA = w2.dX.astype(np.float32)
+    dh1, dh3 = swiglu_bwd(dA, h1, h3)
+    w1 = linear_backward(dh1, ops.X8, ops.s_x, ops.W1_8, ops.s_w1, S, mode, ec_mode, seed, TID_W1,
+                         rows=rows, krows=krows_d)
+    w3 = linear_backward(dh3, ops.X8, ops.s_x, ops.W3_8, ops.s_w3, S, mode, ec_mode, seed, TID_W3,
+                         rows=rows, krows=krows_d)
+    return FFNBackward(w2=w2, w1=w1, w3=w3, dA=dA, dh1=dh1, dh3=dh3,
+                       dX=w1.dX + w3.dX, dW1=w1.dW, dW2=w2.dW, dW3=w3.dW)

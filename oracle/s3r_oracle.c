@@ -1,0 +1,452 @@
+/*
+ * s3r_oracle.c -- plain, single-threaded CPU oracle for the S3R / S3R-EC INT8
+ * backward.  TEST INFRASTRUCTURE ONLY: the product path never links, loads or
+ * calls this file; only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or constant generator
+ * with the CUDA library.
+ *
+ * Sources (cited by page title and section):
+ *   [S3R]  "Efficient Quantization Training with Stochastic Rounding via
+ *          Structured Subspace Randomness" (sections rebuilt from the text:
+ *          §III-A quantized backprop with SR, §III-B structured subspace
+ *          randomness, §III-C why sharing hurts, §III-D S3R-EC, §IV-B compared
+ *          configurations).
+ *   [SRB]  "Stochastic Rounding" (transformer-math blog): sections "Stochastic
+ *          rounding, defined", "The probability formula".
+ *   [PHX]  Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ *          1, 2, 3", SC'11: the Philox4x32-10 bijection (cited by [S3R] §II).
+ *
+ * Precision.  Where floating point decides an integer code (fold, tile scale,
+ * normalised value, residual, threshold compare) this file uses exactly the
+ * fp32 operations the kernels use, in the order stated below, so codes can be
+ * compared bit for bit.  Reductions, error statistics, correction factors and
+ * the GEMM rescale are computed in fp64.  Compile with -ffp-contract=off so no
+ * multiply-add is fused behind our back.
+ *
+ * Nothing here is blocked, fused or reordered beyond the definitions: every
+ * function is a direct loop over the formula it cites.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG (-1)
+#define ORC_ERR_NONFINITE (-4)
+
+/* rounding modes */
+#define ORC_RTNE 0
+#define ORC_S3R 1   /* one threshold per token, shared by its channels (Phi_2D) */
+#define ORC_INDEP 2 /* one threshold per element */
+
+/* error-correction modes */
+#define ORC_EC_NONE 0
+#define ORC_EC_DX_ONLY 1     /* full activation-gradient term of the projection */
+#define ORC_EC_TWO_WAY 2     /* both products */
+#define ORC_EC_DX_TOKEN_ONLY 3 /* alternative reading: token-mean term eps*r only */
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 [PHX]: 10 rounds of the Philox S-box on a 4x32-bit counter   */
+/* with a 2x32-bit key bumped by the Weyl constants between rounds.           */
+/* ------------------------------------------------------------------------- */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u; /* golden ratio */
+            k1 += 0xBB67AE85u; /* sqrt(3) - 1 */
+        }
+        uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+        uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n1 = lo1;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        uint32_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* A 32-bit word to a threshold on the 24-bit grid in [0, 1): (w >> 8) * 2^-24. */
+float orc_word_to_unit(uint32_t w) {
+    return (float)(w >> 8) * 0x1.0p-24f;
+}
+
+/* [S3R] §III-B "Threshold broadcasting", Phi_2D: one uniform threshold u_t per
+ * token, shared by all channels of that token.  Counter = token index t,
+ * key = (low 32 bits of seed, tensor id); the threshold is output word 0. */
+float orc_token_threshold(uint64_t t, uint64_t seed, uint32_t tensor_id) {
+    uint32_t ctr[4] = {(uint32_t)t, (uint32_t)(t >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, tensor_id};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return orc_word_to_unit(out[0]);
+}
+
+/* [S3R] §III-A, conventional QT: an independent threshold for every element.
+ * Element e = t*N + n uses word (e mod 4) of Philox(counter = e / 4). */
+float orc_element_threshold(uint64_t e, uint64_t seed, uint32_t tensor_id) {
+    uint64_t c = e >> 2;
+    uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, tensor_id};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return orc_word_to_unit(out[e & 3]);
+}
+
+/* bf16 bit pattern to fp32 (exact). */
+float orc_bf16_to_float(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+void orc_bf16_array_to_float(const uint16_t* src, int64_t n, float* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = orc_bf16_to_float(src[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Quantization of the backward gradient ([S3R] §III-A).                      */
+/*                                                                            */
+/* For each element, in fp32:                                                 */
+/*   fold      g  = (s_x[t] * G[t,n]) * s_w[n]      (null scale pointer = 1)  */
+/*   scale     amax = max |g| over the tile; delta = amax / 127;              */
+/*             inv = 127 / amax   (delta = inv = 0 when amax == 0)            */
+/*   normalise y  = g * inv                                                   */
+/*   SR        f = floor(y); p = y - f; q = f + [u < p]   ([SRB] "u < p")     */
+/*   RTNE      q = nearbyint(y)  (round half to even)                         */
+/*   clamp     q in [-127, 127]                                               */
+/*   error     e = fma(delta, q, -g)     (E = delta*Q - G', [S3R] §III-A)     */
+/* Tiles are tr x tc and start at row 0 / column 0; the last ones may be      */
+/* partial.  delta is [ceil(T/tr), ceil(N/tc)] row-major.  E may be NULL.     */
+/* ------------------------------------------------------------------------- */
+/* The scalar SR step on a grid of unit spacing ([SRB] "Stochastic rounding,
+ * defined" / "The probability formula"; [S3R] §III-A): with f = floor(y) and
+ * residual p = y - f, round up to f + 1 when the threshold u lies below p,
+ * otherwise down to f.  A value on the grid (p = 0) never moves. */
+float orc_sr_step(float y, float u) {
+    float f = floorf(y);
+    float p = y - f;
+    return (u < p) ? f + 1.0f : f;
+}
+
+static float fold_one(const float* G, int64_t ldg, const float* s_x, const float* s_w, int64_t t, int64_t n) {
+    float g = G[t * ldg + n];
+    if (s_x) g = s_x[t] * g;
+    if (s_w) g = g * s_w[n];
+    return g;
+}
+
+int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
+                 const float* s_x, const float* s_w, int mode, uint64_t seed, uint32_t tensor_id,
+                 int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E) {
+    if (T < 0 || N < 0 || tr <= 0 || tc <= 0 || ldg < N) return ORC_ERR_ARG;
+    if (mode != ORC_RTNE && mode != ORC_S3R && mode != ORC_INDEP) return ORC_ERR_ARG;
+    int status = ORC_OK;
+    int64_t ntr = (T + tr - 1) / tr, ntc = (N + tc - 1) / tc;
+    for (int64_t i = 0; i < ntr; ++i) {
+        for (int64_t j = 0; j < ntc; ++j) {
+            int64_t t0 = i * tr, t1 = (t0 + tr < T) ? t0 + tr : T;
+            int64_t n0 = j * tc, n1 = (n0 + tc < N) ? n0 + tc : N;
+            /* tile absmax of the folded gradient */
+            float amax = 0.0f;
+            int finite = 1;
+            for (int64_t t = t0; t < t1; ++t)
+                for (int64_t n = n0; n < n1; ++n) {
+                    float g = fold_one(G, ldg, s_x, s_w, t, n);
+                    if (!isfinite(g)) finite = 0;
+                    else if (fabsf(g) > amax) amax = fabsf(g);
+                }
+            if (!finite) {
+                status = ORC_ERR_NONFINITE;
+                delta[i * ntc + j] = NAN;
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int64_t n = n0; n < n1; ++n) {
+                        Q[t * N + n] = 0;
+                        if (E) E[t * N + n] = 0.0f;
+                    }
+                continue;
+            }
+            float d = amax / 127.0f;
+            float inv = (amax > 0.0f) ? 127.0f / amax : 0.0f;
+            delta[i * ntc + j] = d;
+            for (int64_t t = t0; t < t1; ++t) {
+                float u_tok = (mode == ORC_S3R) ? orc_token_threshold((uint64_t)t, seed, tensor_id) : 0.0f;
+                for (int64_t n = n0; n < n1; ++n) {
+                    float g = fold_one(G, ldg, s_x, s_w, t, n);
+                    float y = g * inv;
+                    float qf;
+                    if (mode == ORC_RTNE) {
+                        qf = nearbyintf(y);
+                    } else {
+                        float u = (mode == ORC_S3R) ? u_tok
+                                                    : orc_element_threshold((uint64_t)(t * N + n), seed, tensor_id);
+                        qf = orc_sr_step(y, u);
+                    }
+                    if (qf > 127.0f) qf = 127.0f;
+                    if (qf < -127.0f) qf = -127.0f;
+                    Q[t * N + n] = (int8_t)qf;
+                    if (E) E[t * N + n] = fmaf(d, qf, -g);
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/* Forward operands ([S3R] §III-A): RTNE with a per-row (axis 0) or per-column
+ * (axis 1) absmax scale s = amax/127, so that A ~= diag(s) A_hat (rows) or
+ * A ~= A_hat diag(s) (columns).  An all-zero row/column gets s = 1: any scale
+ * reproduces zero, and 1 keeps the backward fold and rescale finite. */
+int orc_rtne_operand(const float* A, int64_t R, int64_t C, int64_t lda, int axis, int8_t* Q, float* scale) {
+    if (R < 0 || C < 0 || lda < C || (axis != 0 && axis != 1)) return ORC_ERR_ARG;
+    int64_t nvec = axis == 0 ? R : C, len = axis == 0 ? C : R;
+    for (int64_t v = 0; v < nvec; ++v) {
+        float amax = 0.0f;
+        for (int64_t l = 0; l < len; ++l) {
+            float a = axis == 0 ? A[v * lda + l] : A[l * lda + v];
+            if (!isfinite(a)) return ORC_ERR_NONFINITE;
+            if (fabsf(a) > amax) amax = fabsf(a);
+        }
+        float s = amax > 0.0f ? amax / 127.0f : 1.0f;
+        float inv = amax > 0.0f ? 127.0f / amax : 1.0f;
+        scale[v] = s;
+        for (int64_t l = 0; l < len; ++l) {
+            int64_t r = axis == 0 ? v : l, c = axis == 0 ? l : v;
+            float qf = nearbyintf(A[r * lda + c] * inv);
+            if (qf > 127.0f) qf = 127.0f;
+            if (qf < -127.0f) qf = -127.0f;
+            Q[r * C + c] = (int8_t)qf;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Per-tile partial sums of the rounding error, the quantities the quantizer
+ * hands to the correction: tok[t, j] = sum over tile column j of e[t, n];
+ * col[i, n] = sum over tile row i of e[t, n]. */
+void orc_error_partials(const float* E, int64_t T, int64_t N, int64_t tr, int64_t tc, double* tok, double* col) {
+    int64_t ntr = (T + tr - 1) / tr, ntc = (N + tc - 1) / tc;
+    for (int64_t i = 0; i < T * ntc; ++i) tok[i] = 0.0;
+    for (int64_t i = 0; i < ntr * N; ++i) col[i] = 0.0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            tok[t * ntc + n / tc] += (double)E[t * N + n];
+            col[(t / tr) * N + n] += (double)E[t * N + n];
+        }
+}
+
+/* [S3R] §III-D "Two-way correction": the averages of the rounding error of
+ * example b (S consecutive tokens, T = B*S): token means eps[t] over the N
+ * channels, channel means colmean[b, n] over the S tokens, and the grand
+ * mean mu[b].  Together they give the orthogonal projection of E_b onto
+ * {1_S a^T + c 1_D^T}: P(E_b) = 1_S colmean_b^T + eps_b 1_D^T - mu_b 1 1^T. */
+int orc_error_stats(const float* E, int64_t T, int64_t N, int64_t S, double* eps, double* colmean, double* mu) {
+    if (S <= 0 || T % S != 0) return ORC_ERR_ARG;
+    int64_t B = T / S;
+    for (int64_t t = 0; t < T; ++t) {
+        double s = 0.0;
+        for (int64_t n = 0; n < N; ++n) s += (double)E[t * N + n];
+        eps[t] = s / (double)N;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        double total = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int64_t t = b * S; t < (b + 1) * S; ++t) s += (double)E[t * N + n];
+            colmean[b * N + n] = s / (double)S;
+            total += s;
+        }
+        mu[b] = total / ((double)S * (double)N);
+    }
+    return ORC_OK;
+}
+
+/* [S3R] §III-D: the factors through which P(E) enters the two products.
+ *   rowsum[k]  = sum_n W8[k, n]                (W 1_D, "precomputed row sums")
+ *   v[b, k]    = sum_n (colmean[b,n] - mu[b]) W8[k, n]
+ *   xsum[b, k] = sum_{t in b} X8[t, k]          (= S * xbar_b)
+ *   p[k]       = sum_t X8[t, k] eps[t]
+ * so that  P(E_b) W8^T [t, k] = eps[t] rowsum[k] + v[b, k]  and
+ *          X8^T P(E) [k, n]   = sum_b xsum[b,k] (colmean[b,n] - mu[b]) + p[k].
+ * W8 is [K, N] (the weight of Y = X W with K = H_in, N = H_out), X8 is [T, K].
+ * X8 may be NULL (then xsum and p are not written). */
+void orc_ec_factors(const double* eps, const double* colmean, const double* mu,
+                    int64_t T, int64_t N, int64_t S, const int8_t* W8, const int8_t* X8, int64_t K,
+                    int64_t* rowsum, double* v, int64_t* xsum, double* p) {
+    int64_t B = T / S;
+    for (int64_t k = 0; k < K; ++k) {
+        int64_t r = 0;
+        for (int64_t n = 0; n < N; ++n) r += W8[k * N + n];
+        rowsum[k] = r;
+        for (int64_t b = 0; b < B; ++b) {
+            double s = 0.0;
+            for (int64_t n = 0; n < N; ++n) s += (colmean[b * N + n] - mu[b]) * (double)W8[k * N + n];
+            v[b * K + k] = s;
+        }
+    }
+    if (!X8) return;
+    for (int64_t k = 0; k < K; ++k) {
+        double pk = 0.0;
+        for (int64_t b = 0; b < B; ++b) {
+            int64_t s = 0;
+            for (int64_t t = b * S; t < (b + 1) * S; ++t) s += X8[t * K + k];
+            xsum[b * K + k] = s;
+        }
+        for (int64_t t = 0; t < T; ++t) pk += (double)X8[t * K + k] * eps[t];
+        p[k] = pk;
+    }
+}
+
+/* Exact integer partial products per 128-wide contraction block (the S8 GEMM
+ * with S32 accumulation of [S3R] §III-A), straight from the definition.
+ *   dX block kb: I[r, k, kb] = sum_{n in block kb} Q[t_r, n] W8[k, n]
+ *   dW block tb: J[r, n, tb] = sum_{t in block tb} X8[t, k_r] Q[t, n]
+ * Only the requested rows (t_r for dX, k_r for dW) are produced. */
+void orc_dx_blocks(const int8_t* Q, const int8_t* W8, int64_t T, int64_t N, int64_t K, int64_t blk,
+                   const int64_t* rows, int64_t nrows, int32_t* I) {
+    int64_t nkb = (N + blk - 1) / blk;
+    (void)T;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t t = rows[r];
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t kb = 0; kb < nkb; ++kb) {
+                int64_t s = 0;
+                for (int64_t n = kb * blk; n < N && n < (kb + 1) * blk; ++n) s += (int64_t)Q[t * N + n] * W8[k * N + n];
+                I[(r * K + k) * nkb + kb] = (int32_t)s;
+            }
+    }
+}
+
+void orc_dw_blocks(const int8_t* X8, const int8_t* Q, int64_t T, int64_t K, int64_t N, int64_t blk,
+                   const int64_t* krows, int64_t nk, int32_t* J) {
+    int64_t ntb = (T + blk - 1) / blk;
+    for (int64_t r = 0; r < nk; ++r) {
+        int64_t k = krows[r];
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t tb = 0; tb < ntb; ++tb) {
+                int64_t s = 0;
+                for (int64_t t = tb * blk; t < T && t < (tb + 1) * blk; ++t) s += (int64_t)X8[t * K + k] * Q[t * N + n];
+                J[(r * N + n) * ntb + tb] = (int32_t)s;
+            }
+    }
+}
+
+/* Activation gradient ([S3R] §III-A, §III-D), for the requested token rows:
+ *   acc[t,k] = sum_kb delta[t/tr, kb] * I[t, k, kb]          (rescale, fp64)
+ *   corr     = eps[t] rowsum[k] + v[b(t), k]    (EC_DX_ONLY, EC_TWO_WAY)
+ *            = eps[t] rowsum[k]                 (EC_DX_TOKEN_ONLY)
+ *   dX[t,k]  = (acc - corr) / s_x[t]            (s_x NULL = 1)
+ * The contraction blocks are the tile columns of Q (blk = tc). */
+void orc_dx(const int8_t* Q, const float* delta, const int8_t* W8, int64_t T, int64_t N, int64_t K,
+            int64_t tr, int64_t tc, const float* s_x, int ec_mode, const double* eps, const int64_t* rowsum,
+            const double* v, int64_t S, const int64_t* rows, int64_t nrows, double* dX) {
+    int64_t nkb = (N + tc - 1) / tc;
+    int32_t* I = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K * nkb > 0 ? K * nkb : 1));
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t t = rows[r];
+        orc_dx_blocks(Q, W8, T, N, K, tc, &t, 1, I);
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t kb = 0; kb < nkb; ++kb) acc += (double)delta[(t / tr) * nkb + kb] * (double)I[k * nkb + kb];
+            double corr = 0.0;
+            if (ec_mode == ORC_EC_DX_ONLY || ec_mode == ORC_EC_TWO_WAY)
+                corr = eps[t] * (double)rowsum[k] + v[(t / S) * K + k];
+            else if (ec_mode == ORC_EC_DX_TOKEN_ONLY)
+                corr = eps[t] * (double)rowsum[k];
+            double sx = s_x ? (double)s_x[t] : 1.0;
+            dX[r * K + k] = (acc - corr) / sx;
+        }
+    }
+    free(I);
+}
+
+/* Weight gradient ([S3R] §III-A, §III-D), for the requested rows k of dW [K, N]:
+ *   acc[k,n] = sum_tb delta[tb, n/tc] * J[k, n, tb]
+ *   corr     = sum_b xsum[b,k] (colmean[b,n] - mu[b]) + p[k]   (EC_TWO_WAY only)
+ *   dW[k,n]  = (acc - corr) / s_w[n]                            (s_w NULL = 1)
+ * The contraction blocks are the tile rows of Q (blk = tr).  dW is the sum
+ * X^T G, not divided by the token count ([S3R] §III-A leaves 1/(BS) to the
+ * caller). */
+void orc_dw(const int8_t* X8, const int8_t* Q, const float* delta, int64_t T, int64_t K, int64_t N,
+            int64_t tr, int64_t tc, const float* s_w, int ec_mode, const double* colmean, const double* mu,
+            const int64_t* xsum, const double* p, int64_t S, const int64_t* krows, int64_t nk, double* dW) {
+    int64_t ntb = (T + tr - 1) / tr, ntc = (N + tc - 1) / tc, B = T / S;
+    int32_t* J = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N * ntb > 0 ? N * ntb : 1));
+    for (int64_t r = 0; r < nk; ++r) {
+        int64_t k = krows[r];
+        orc_dw_blocks(X8, Q, T, K, N, tr, &k, 1, J);
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t tb = 0; tb < ntb; ++tb) acc += (double)delta[tb * ntc + n / tc] * (double)J[n * ntb + tb];
+            double corr = 0.0;
+            if (ec_mode == ORC_EC_TWO_WAY) {
+                for (int64_t b = 0; b < B; ++b) corr += (double)xsum[b * K + k] * (colmean[b * N + n] - mu[b]);
+                corr += p[k];
+            }
+            double sw = s_w ? (double)s_w[n] : 1.0;
+            dW[r * N + n] = (acc - corr) / sw;
+        }
+    }
+    free(J);
+}
+
+/* ------------------------------------------------------------------------- */
+/* SwiGLU backward glue (the FFN block of [S3R] §IV-A / Table III).           */
+/* exp: Cody-Waite argument reduction x = n ln2 + r with ln2 split in a       */
+/* 16-bit head and a tail, |r| <= ln2/2, e^r by its degree-7 Taylor series in */
+/* Horner form, then scaling by 2^n.  The argument is clamped to [-87, 88] so */
+/* 2^n stays a normal number.                                                 */
+/* ------------------------------------------------------------------------- */
+float orc_expf(float x) {
+    if (x > 88.0f) x = 88.0f;
+    if (x < -87.0f) x = -87.0f;
+    const float log2e = 0x1.715476p+0f;     /* log2(e) rounded to fp32 */
+    const float ln2_hi = 0x1.62e4p-1f;      /* 45426 / 2^16 */
+    const float ln2_lo = 0x1.7f7d1cp-20f;   /* ln2 - ln2_hi rounded to fp32 */
+    float n = nearbyintf(x * log2e);
+    float r = fmaf(-n, ln2_hi, x);
+    r = fmaf(-n, ln2_lo, r);
+    float poly = 0x1.a01a02p-13f;           /* 1/7! */
+    poly = fmaf(poly, r, 0x1.6c16c2p-10f);  /* 1/6! */
+    poly = fmaf(poly, r, 0x1.111112p-7f);   /* 1/5! */
+    poly = fmaf(poly, r, 0x1.555556p-5f);   /* 1/4! */
+    poly = fmaf(poly, r, 0x1.555556p-3f);   /* 1/3! */
+    poly = fmaf(poly, r, 0.5f);             /* 1/2! */
+    poly = fmaf(poly, r, 1.0f);
+    poly = fmaf(poly, r, 1.0f);
+    int32_t ni = (int32_t)n;
+    uint32_t bits = (uint32_t)(ni + 127) << 23;
+    float scale;
+    memcpy(&scale, &bits, 4);
+    return poly * scale;
+}
+
+float orc_sigmoidf(float x) {
+    float e = orc_expf(-x);
+    return 1.0f / (1.0f + e);
+}
+
+/* With a = silu(h1) * h3 and dA = dL/da (fp32), in fp32 and in this order:
+ *   s    = sigmoid(h1)
+ *   silu = h1 * s
+ *   dsilu = s * (1 + h1 * (1 - s))        (d silu / d h1)
+ *   dh1  = (dA * h3) * dsilu
+ *   dh3  = dA * silu                                                          */
+void orc_swiglu_bwd(const float* dA, const float* h1, const float* h3, int64_t n, float* dh1, float* dh3) {
+    for (int64_t i = 0; i < n; ++i) {
+        float s = orc_sigmoidf(h1[i]);
+        float silu = h1[i] * s;
+        float one_minus = 1.0f - s;
+        float inner = h1[i] * one_minus;
+        float dsilu = s * (1.0f + inner);
+        float g = dA[i] * h3[i];
+        dh1[i] = g * dsilu;
+        dh3[i] = dA[i] * silu;
+    }
+}
