@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark: SwiGLU FFN block backward with S3R-EC INT8 on one GB300.
+
+One step = one pass of the whole backward hot path (quantize dY, correction
+factors, both INT8 GEMMs of W2, SwiGLU glue fused into the quantization of the
+gate/up gradients, their correction factors, both GEMMs of W1 and W3) over one
+batch: the d=2048, F=5632, T=8192 (4 x 2048 tokens) Llama-style block, inputs
+resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling; the path
+needs no exchange inside one backward); the time is the max over ranks.
+--impl reference times the plain CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "FFN backward tokens/s, S3R-EC INT8 vs BF16, 1 GB300; quantize GB/s vs HBM peak"
+WORKLOAD = "swiglu_ffn_d2048_F5632_T8192"
+CFG = workloads.WORKLOADS[WORKLOAD]
+T, D, F, S = CFG["T"], CFG["d"], CFG["F"], CFG["S"]
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only: no collective touches the data path)
+# ---------------------------------------------------------------------------
+def dist_setup(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def device_setup(s3r, rank):
+    inp = workloads.ffn_inputs(T, D, F, S, seed=workloads.DATA_SEED + 1 + 1000 * rank)
+    c = lambda t: t.cuda()
+    ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
+    torch.cuda.synchronize()
+    return inp, ops
+
+
+def time_ffn(s3r, ops, dY, steps, warmup, rm, ec, world, events=False):
+    """Device time of `steps` ffn_backward calls on resident inputs."""
+    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S, rm, ec), dtype=torch.uint8, device="cuda")
+    grads = s3r.alloc_ffn_grads(T, D, F)
+    st = s3r.new_status()
+    for i in range(warmup):
+        s3r.ffn_backward(ops, dY, S, rm, ec, seed=i, grads=grads, workspace=ws, status=st)
+    step_ev = None
+    if events:
+        step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(s3r.FFN_NUM_EVENTS)] for _ in range(steps)]
+        for evs in step_ev:
+            for e in evs:
+                e.record()   # materialize the handles
+    torch.cuda.synchronize()
+    barrier(world)
+    n0 = s3r.kernel_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        s3r.ffn_backward(ops, dY, S, rm, ec, seed=1000 + i, grads=grads, workspace=ws, status=st,
+                         step_events=step_ev[i] if events else None)
+    t1.record()
+    torch.cuda.synchronize()
+    launches = s3r.kernel_launch_count() - n0
+    ms = t0.elapsed_time(t1)
+    barrier(world)
+    s3r.check_status(st)
+    seg = None
+    if events:
+        seg = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(s3r.FFN_NUM_EVENTS - 1)] for evs in step_ev])
+    return max_over_ranks(ms, world), launches, seg, grads
+
+
+def time_e2e(s3r, inp, ops, steps, warmup, world):
+    """Same step through the C ABI with HOST buffers: pinned host -> device
+    copies of every input of the step, the backward, device -> host copies of
+    all four gradients, inside the timed region."""
+    host_in = {k: getattr(ops, k).cpu().pin_memory() for k in
+               ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2", "h1", "h3")}
+    host_in["dY"] = inp.dY.pin_memory()
+    dev_in = {k: torch.empty_like(v, device="cuda") for k, v in host_in.items()}
+    dops = s3r.FFNOperands(**{k: dev_in[k] for k in host_in if k != "dY"})
+    grads = s3r.alloc_ffn_grads(T, D, F)
+    host_out = {k: torch.empty(getattr(grads, k).shape, dtype=torch.float32).pin_memory()
+                for k in ("dX", "dW1", "dW3", "dW2")}
+    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S), dtype=torch.uint8, device="cuda")
+    bi = sum(v.numel() * v.element_size() for v in host_in.values())
+    bo = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def step(i):
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        s3r.ffn_backward(dops, dev_in["dY"], S, seed=i, grads=grads, workspace=ws)
+        for k, v in host_out.items():
+            v.copy_(getattr(grads, k), non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        step(i)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    barrier(world)
+    return ms, bi, bo
+
+
+def time_bf16_backward(inp, steps, warmup):
+    """Context: the same block's backward in BF16 with cuBLAS via torch."""
+    X, W1, W3, W2, h1, h3, a, dY = (t.cuda() for t in (inp.X, inp.W1, inp.W3, inp.W2, inp.h1, inp.h3, inp.a, inp.dY))
+
+    def step():
+        dA = dY @ W2.t()
+        dW2 = a.t() @ dY
+        s = torch.sigmoid(h1.float())
+        dAf = dA.float()
+        dh1 = (dAf * h3.float() * s * (1 + h1.float() * (1 - s))).to(torch.bfloat16)
+        dh3 = (dAf * h1.float() * s).to(torch.bfloat16)
+        dX = dh1 @ W1.t() + dh3 @ W3.t()
+        dW1 = X.t() @ dh1
+        dW3 = X.t() @ dh3
+        return dX, dW1, dW2, dW3
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
+def time_quantize_sweep(s3r, steps=20):
+    """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100 outliers."""
+    Tq, Nq = 16384, 8192
+    G = workloads.quantize_sweep_input(Tq, Nq, seed=workloads.DATA_SEED + 3).cuda()
+    out = {}
+    q = s3r.s3r_quantize(G)
+    qi = s3r.indep_sr_quantize(G)
+    Qr, sr = s3r.rtne_quantize(G)
+    runs = {
+        "s3r": (lambda i: s3r.s3r_quantize(G, seed=i, out=q), 2 + 1 + 8 / 128),
+        "indep_sr_one_copy": (lambda i: s3r.indep_sr_quantize(G, seed=i, out=qi), 3.0),
+        "rtne": (lambda i: s3r.rtne_quantize(G, Q=Qr, scale=sr), 3.0),
+    }
+    for name, (fn, bpe) in runs.items():
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(steps):
+            fn(i)
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(bpe * Tq * Nq / (ms * 1e-3) / 1e9, 1),
+                     "alg_bytes_per_elem": round(bpe, 4)}
+    out["shape"] = [Tq, Nq]
+    return out
+
+
+def cpu_baseline(tokens=128):
+    """The plain CPU oracle (single thread) on a bounded sample of the same
+    block: `tokens` tokens (one example) of the d=2048, F=5632 FFN."""
+    import oracle as orc
+    inp = workloads.ffn_inputs(tokens, D, F, tokens, seed=workloads.DATA_SEED + 1)
+    f = orc.from_torch_bf16
+    ops = orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
+    h1, h3, dY = f(inp.h1), f(inp.h3), f(inp.dY)
+    t0 = time.perf_counter()
+    orc.ffn_backward(ops, h1, h3, dY, tokens, mode=orc.S3R, ec_mode=orc.EC_TWO_WAY, seed=0)
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{tokens} tokens (one example) of the d=2048, F=5632 SwiGLU block, S3R-EC two-way, "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_ours(args, world, rank, local):
+    import stochastic_rounding_int8_gb300 as s3r
+    s3r.lib()
+    pk, pk_kind = peaks()
+    inp, ops = device_setup(s3r, rank)
+    dY = inp.dY.cuda()
+    clocks = Clocks(local)
+    # main timed region: S3R-EC two-way, step events for the per-kernel roofline
+    clocks.start()
+    ms, launches, seg, _ = time_ffn(s3r, ops, dY, args.steps, args.warmup, s3r.ROUND_S3R, s3r.EC_TWO_WAY, world,
+                                    events=True)
+    clk = clocks.stop()
+    ms_step = ms / args.steps
+    value = world * T * args.steps / (ms * 1e-3)
+    # per-step segments -> dominant kernel class
+    segm = seg.mean(0)
+    names = s3r.FFN_STEPS
+    classes = {"int8_gemm_dx": (segm[2] + segm[6], 3), "int8_gemm_dw (incl. operand transposes)": (segm[3] + segm[7], 3),
+               "quantize (dY + SwiGLU-fused)": (segm[0] + segm[4], 2), "s3r_ec_correct": (segm[1] + segm[5], 3)}
+    dom = max(classes, key=lambda k: classes[k][0])
+    dom_ms, dom_n = classes[dom]
+    flops_per_launch = 2.0 * T * D * F
+    if dom.startswith("int8_gemm"):
+        achieved = flops_per_launch / (dom_ms / dom_n * 1e-3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_note": f"dense bf16 sustained ({pk_kind}); the s8 codes run on the tensor cores at the "
+                             f"16-bit rate or below on sm_103a",
+                "flops_per_launch": flops_per_launch, "launches_per_step": dom_n,
+                "avg_launch_us": round(dom_ms / dom_n * 1e3, 1)}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": None, "traffic": None}
+    steps_ms = {n: round(float(v), 4) for n, v in zip(names, segm)}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8", "data": "synthetic (seeded; shapes/distributions of the paper's FFN "
+                                                  "block workload)",
+        "config": {"workload": WORKLOAD, "T": T, "d": D, "F": F, "examples": T // S, "seq": S,
+                   "rounding": "S3R Phi_2D", "ec": "two-way", "tile": 128,
+                   "l2": "working set ~1 GB > 129 MB L2 (no flush needed)", "parallelism": f"replica x{world}"},
+        "clocks": clk,
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "step_breakdown_ms": steps_ms,
+    }
+    # e2e through the C ABI with host buffers
+    e2e_steps = max(3, min(args.steps, 20))
+    ems, bi, bo = time_e2e(s3r, inp, ops, e2e_steps, min(args.warmup, 3), world)
+    line["e2e"] = {"value": round(world * T * e2e_steps / (ems * 1e-3), 1), "unit": "tokens/s",
+                   "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
+    if not args.no_context and rank == 0:
+        ctx = {}
+        for name, rm, ec in (("s3r_ec_dx_only", s3r.ROUND_S3R, s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE),
+                             ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE)):
+            m, _, _, _ = time_ffn(s3r, ops, dY, 10, 2, rm, ec, 1)
+            ctx[name] = {"tokens_s": round(T * 10 / (m * 1e-3), 1), "ms": round(m / 10, 4)}
+        bms = time_bf16_backward(inp, 10, 3)
+        ctx["bf16_cublas_backward"] = {"tokens_s": round(T / (bms * 1e-3), 1), "ms": round(bms, 4)}
+        ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / ms_step, 3)
+        ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / ms_step, 3)
+        qs = time_quantize_sweep(s3r)
+        for k in ("s3r", "indep_sr_one_copy", "rtne"):
+            qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
+        ctx["quantize_sweep"] = qs
+        line["context"] = ctx
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    return line
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step a bounded sample (8 tokens of
+    the d=2048, F=5632 block, ~1-3 s) on the host cores."""
+    if rank != 0:
+        return None
+    import oracle as orc
+    tok = 8
+    inp = workloads.ffn_inputs(tok, D, F, tok, seed=workloads.DATA_SEED + 1)
+    f = orc.from_torch_bf16
+    ops = orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
+    h1, h3, dY = f(inp.h1), f(inp.h3), f(inp.dY)
+    run = lambda: orc.ffn_backward(ops, h1, h3, dY, tok, mode=orc.S3R, ec_mode=orc.EC_TWO_WAY, seed=0)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = tok * args.steps / dt
+    sample = f"{tok} tokens (one example) of the d=2048, F=5632 SwiGLU block per step, single-threaded C oracle"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T, "d": D, "F": F, "rounding": "S3R Phi_2D", "ec": "two-way"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

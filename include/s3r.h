@@ -1,0 +1,294 @@
+/*
+ * s3r.h -- C ABI of libs3r, a GB300 (sm_103a) implementation of the S3R /
+ * S3R-EC INT8 backward pass of a linear or SwiGLU FFN layer.
+ *
+ * Method: "Efficient Quantization Training with Stochastic Rounding via
+ * Structured Subspace Randomness" (cited below as [S3R] with its sections:
+ * §III-A quantized backprop with SR, §III-B structured subspace randomness,
+ * §III-C why sharing hurts, §III-D S3R-EC, §IV-B compared configurations).
+ * SR definition: "Stochastic Rounding" (transformer-math blog), sections
+ * "Stochastic rounding, defined" and "The probability formula".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Notation: a linear layer Y = X W with X [T, K] (T = B*S tokens, B
+ *    examples of S tokens), W [K, N], upstream gradient G = dY [T, N].
+ *  - All tensors are row-major.  "ld*" arguments are row strides in elements.
+ *    bf16 tensors are passed as `const void*` holding IEEE bfloat16.
+ *  - Every pointer except those documented as host pointers is a DEVICE
+ *    pointer owned by the caller.  The library never allocates device memory
+ *    and never synchronizes; where scratch is needed the caller passes a
+ *    workspace whose size a *_workspace_size() call returns.
+ *  - Every call is asynchronous on `stream` and returns an int status
+ *    (S3R_OK = 0, negative on error) for what the host can check: null or
+ *    misaligned pointers, bad sizes, launch failures.  Nothing is launched
+ *    when the host check fails.  Conditions only the device can see (a
+ *    non-finite gradient value, a bounded wait that ran out) are written to
+ *    `d_status` (a device int, may be NULL), which the caller reads after
+ *    synchronizing; the call itself then still returns S3R_OK.  The caller
+ *    zeroes *d_status before the first call; calls only ever write error
+ *    codes into it.
+ *  - Tiles are S3R_TILE x S3R_TILE = 128 x 128 and start at row 0 and column 0;
+ *    the last tile row / column may be partial (ragged T and N are allowed).
+ *  - Base pointers of int8 and bf16 tensors must be 16-byte aligned and their
+ *    row strides multiples of 16 bytes (S3R_ERR_ALIGN otherwise).
+ *  - No exception crosses the ABI.
+ */
+#ifndef S3R_H
+#define S3R_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same definition as the CUDA runtime's. */
+typedef struct CUstream_st* cudaStream_t;
+
+#define S3R_TILE 128
+
+enum s3r_status {
+    S3R_OK = 0,
+    S3R_ERR_ARG = -1,        /* null pointer, negative size, unknown enum */
+    S3R_ERR_ALIGN = -2,      /* base pointer or row stride not 16-byte aligned */
+    S3R_ERR_SHAPE = -3,      /* inconsistent sizes (e.g. T not a multiple of S) */
+    S3R_ERR_NONFINITE = -4,  /* (device) NaN or Inf in the folded gradient */
+    S3R_ERR_TIMEOUT = -5,    /* (device) a bounded wait gave up */
+    S3R_ERR_CUDA = -6,       /* a CUDA launch or attribute call failed */
+    S3R_ERR_WORKSPACE = -7,  /* workspace null or smaller than required */
+    S3R_ERR_UNSUPPORTED = -8 /* size outside what the kernels support */
+};
+
+/* Error correction ([S3R] §III-D). */
+enum s3r_ec_mode {
+    S3R_EC_NONE = 0,     /* plain S3R (or a baseline rounding) */
+    S3R_EC_DX_ONLY = 1,  /* subtract P(E) W^T from the activation gradient only */
+    S3R_EC_TWO_WAY = 2   /* also subtract X^T P(E) from the weight gradient */
+};
+
+/* How the upstream gradient is rounded ([S3R] §IV-B). */
+enum s3r_round_mode {
+    S3R_ROUND_RTNE = 0,  /* deterministic round to nearest even */
+    S3R_ROUND_S3R = 1,   /* one threshold per token shared by its channels (Phi_2D) */
+    S3R_ROUND_INDEP = 2  /* one threshold per element (conventional SR) */
+};
+
+/* Scale granularity of rtne_quantize. */
+enum s3r_scale_axis {
+    S3R_AXIS_ROW = 0,  /* one scale per row:    A ~= diag(s) A_hat (per-token s_x) */
+    S3R_AXIS_COL = 1,  /* one scale per column: A ~= A_hat diag(s) (per-channel s_w) */
+    S3R_AXIS_TILE = 2  /* one scale per 128x128 tile (RTNE baseline for dY) */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* s3r_status_string(int status);
+
+/* ABI version of this header (major*100 + minor). */
+int s3r_abi_version(void);
+
+/* Number of kernels this library has launched in this process (a host-side
+ * count, for measurement). */
+uint64_t s3r_kernel_launch_count(void);
+
+/*
+ * s3r_quantize -- S3R quantization of the upstream gradient, written once for
+ * both backward products ([S3R] §III-A eq. (2) "fold and quantize once",
+ * §III-B inter-operand sharing and per-token threshold broadcast Phi_2D).
+ *
+ * For every element, in fp32 and in this order:
+ *   g    = (s_x[t] * G[t,n]) * s_w[n]     fold; a NULL scale pointer means 1
+ *   amax = max |g| over its 128x128 tile;  tile_scale = amax / 127
+ *   y    = g * (127 / amax)               (y = 0 when amax = 0)
+ *   u_t  = (w >> 8) * 2^-24, w = word 0 of Philox4x32-10 with
+ *          counter (t mod 2^32, t >> 32, 0, 0), key (seed mod 2^32, tensor_id)
+ *   q    = clamp(floor(y) + [u_t < y - floor(y)], -127, 127)
+ *   e    = fma(tile_scale, q, -g)         the rounding error E = Delta Q - G'
+ *
+ * In : G [T, N] bf16 (row stride ldg >= N); s_x [T] or NULL; s_w [N] or NULL.
+ * Out: Q [T, N] int8 (row stride N); tile_scale [ceil(T/128), ceil(N/128)];
+ *      tok_err_part [T, ceil(N/128)]  sum of e over each tile's columns, per token;
+ *      col_err_part [ceil(T/128), N]  sum of e over each tile's rows, per channel.
+ *      Both partial arrays may be NULL (then they are not written).
+ * A tile holding a non-finite g gets tile_scale = NaN, Q = 0, zero partials and
+ * sets *d_status = S3R_ERR_NONFINITE.
+ */
+int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
+                 uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale, float* tok_err_part,
+                 float* col_err_part, int* d_status, cudaStream_t stream);
+
+/*
+ * indep_sr_quantize -- conventional stochastic rounding with an independent
+ * threshold per element ([S3R] §III-A, "Conventional QT implementations draw
+ * independent full-size thresholds"; §IV-B "Independent SR").  Same fold, tile
+ * scale, clamp and layout as s3r_quantize; the threshold of element
+ * e = t*N + n is word (e mod 4) of Philox4x32-10 with counter
+ * (floor(e/4) mod 2^32, floor(e/4) >> 32, 0, 0) and key (seed mod 2^32,
+ * tensor_id).  Call it twice with two tensor ids for the two products.
+ */
+int indep_sr_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
+                      uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale, int* d_status,
+                      cudaStream_t stream);
+
+/*
+ * rtne_quantize -- round to nearest even ([S3R] §III-A forward operands;
+ * §IV-B "INT8 RTNE").  q = clamp(rint(a * (127 / amax)), -127, 127) with
+ * amax taken per row, per column or per 128x128 tile of the folded input
+ * a = (s_x[r] * A[r,c]) * s_w[c] (NULL scale = 1).
+ * Out: Q [R, C] int8 (row stride C); scale = amax / 127 per row [R], per
+ * column [C] or per tile [ceil(R/128), ceil(C/128)].  For ROW and COL an
+ * all-zero row/column gets scale 1 (any scale reproduces zero; 1 keeps the
+ * backward fold finite); for TILE an all-zero tile gets scale 0.
+ */
+int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, const float* s_x, const float* s_w,
+                  int scale_axis, int8_t* Q, float* scale, int* d_status, cudaStream_t stream);
+
+/*
+ * swiglu_quantize -- the SwiGLU backward glue fused into the quantization of
+ * the two gate/up gradients (FFN block of [S3R] §IV-A).  With a = silu(h1)*h3
+ * and dA = dL/da, in fp32 and in this order:
+ *   s = sigmoid(h1) = 1 / (1 + exp(-h1)),  silu = h1*s,
+ *   dsilu = s * (1 + h1*(1 - s)),  dh1 = (dA*h3) * dsilu,  dh3 = dA * silu,
+ * where exp is Cody-Waite reduction (ln 2 split in a 16-bit head and a tail)
+ * with a degree-7 Taylor polynomial and the argument clamped to [-87, 88].
+ * dh1 and dh3 are then quantized exactly as s3r_quantize would quantize them
+ * (fold with s_x [T] and s_w1 / s_w3 [F]), with `round_mode` choosing S3R,
+ * independent SR or RTNE and tensor ids tid1 / tid3.
+ * In : dA [T, F] fp32 (row stride ldd); h1, h3 [T, F] bf16 (row stride ldh).
+ * Out: Q1, Q3 [T, F] int8; scale1, scale3 tile scales; tok1/col1/tok3/col3
+ *      error partials as in s3r_quantize (NULL allowed).
+ */
+int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh, int64_t T,
+                    int64_t F, const float* s_x, const float* s_w1, const float* s_w3, int round_mode,
+                    uint64_t seed, uint32_t tid1, uint32_t tid3, int8_t* Q1, float* scale1, float* tok1,
+                    float* col1, int8_t* Q3, float* scale3, float* tok3, float* col3, int* d_status,
+                    cudaStream_t stream);
+
+/*
+ * s3r_ec_correct -- the error statistics and correction factors of S3R-EC
+ * ([S3R] §III-D, "Two-way correction").  With e the rounding error of
+ * s3r_quantize and example b the S consecutive tokens [b*S, (b+1)*S):
+ *   eps[t]        = (1/N) sum_n e[t,n]                 token mean
+ *   colmean[b,n]  = (1/S) sum_{t in b} e[t,n]          channel mean of example b
+ *   mu[b]         = (1/(S*N)) sum_{t in b, n} e[t,n]   grand mean
+ * so that P(E_b) = 1 colmean_b^T + eps_b 1^T - mu_b 1 1^T is the orthogonal
+ * projection onto row- and column-constant matrices, and
+ *   rowsum[k]     = sum_n W8[k,n]                      (W 1_D)
+ *   v[b,k]        = sum_n (colmean[b,n] - mu[b]) W8[k,n]
+ * and for S3R_EC_TWO_WAY also
+ *   xsum[b,k]     = sum_{t in b} X8[t,k]
+ *   p[k]          = sum_t X8[t,k] eps[t].
+ * In : the partial sums from s3r_quantize; W8 [K, N] int8; X8 [T, K] int8
+ *      (two-way only, else may be NULL).  Requires T % S == 0 and either
+ *      S % 128 == 0 or S == T.
+ * Out: eps [T], mu [B], colmean [B, N], rowsum [K] int32, v [B, K];
+ *      two-way: xsum [B, K] int32, p [K].
+ * workspace: s3r_ec_workspace_size(T, K) bytes (two-way only; else may be NULL).
+ */
+size_t s3r_ec_workspace_size(int64_t T, int64_t K);
+int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
+                   const int8_t* W8, int64_t K, const int8_t* X8, int ec_mode, float* eps, float* mu,
+                   float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p, void* workspace,
+                   size_t workspace_bytes, int* d_status, cudaStream_t stream);
+
+/*
+ * int8_gemm_dx -- activation gradient from the S8 codes ([S3R] §III-A "S8 GEMM
+ * with S32 accumulation, and rescaled"; §III-D activation-gradient term):
+ *   acc[t,k] = sum_kb tile_scale[t/128, kb] * (int32) sum_{n in block kb} Q[t,n] W8[k,n]
+ *   dX[t,k]  = (acc - eps[t]*rowsum[k] - v[t/S, k]) / s_x[t]     (EC modes 1, 2)
+ *   dX[t,k]  = acc / s_x[t]                                      (EC mode 0)
+ * (plus the old dX[t,k] when accumulate != 0).  Each 128-wide block is an
+ * exact integer; blocks are combined in fp32.
+ * In : Q [T, N] int8; tile_scale from the quantizer; W8 [K, N] int8 (the
+ *      forward weight's codes, W [K, N] ~= W8 diag(s_w)); s_x [T] or NULL;
+ *      eps, rowsum, v from s3r_ec_correct (unused when ec_mode = 0).
+ * Out: dX [T, K] fp32 (row stride K).
+ */
+int int8_gemm_dx(const int8_t* Q, const float* tile_scale, const int8_t* W8, int64_t T, int64_t N, int64_t K,
+                 const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum, const float* v,
+                 int64_t S, float* dX, int accumulate, int* d_status, cudaStream_t stream);
+
+/*
+ * int8_gemm_dw -- weight gradient from the same S8 codes ([S3R] §III-A;
+ * §III-D weight-gradient term):
+ *   acc[k,n] = sum_tb tile_scale[tb, n/128] * (int32) sum_{t in block tb} X8[t,k] Q[t,n]
+ *   dW[k,n]  = (acc - sum_b xsum[b,k]*(colmean[b,n] - mu[b]) - p[k]) / s_w[n]  (EC mode 2)
+ *   dW[k,n]  = acc / s_w[n]                                                   (EC modes 0, 1)
+ * dW is the sum X^T G (not divided by the token count).
+ * In : X8 [T, K] int8 (the forward input's codes); Q [T, N] int8; tile_scale;
+ *      s_w [N] or NULL; colmean, mu, xsum, p from s3r_ec_correct (mode 2).
+ * Out: dW [K, N] fp32 (row stride N).
+ * workspace: int8_gemm_dw_workspace_size(T, K, N) bytes (0 allowed when it
+ * returns 0).
+ */
+size_t int8_gemm_dw_workspace_size(int64_t T, int64_t K, int64_t N);
+int int8_gemm_dw(const int8_t* X8, const int8_t* Q, const float* tile_scale, int64_t T, int64_t K, int64_t N,
+                 const float* s_w, int ec_mode, const float* colmean, const float* mu, const int32_t* xsum,
+                 const float* p, int64_t S, float* dW, void* workspace, size_t workspace_bytes, int* d_status,
+                 cudaStream_t stream);
+
+/*
+ * ffn_backward -- the whole SwiGLU FFN block backward (FFN block of [S3R]
+ * §IV-A, Table III), y = (silu(X W1) * (X W3)) W2:
+ *   1. quantize dY (fold s_a, s_w2) -> Q2          [tensor id 0]
+ *   2. EC factors for W2 (if ec_mode != 0 and round_mode == S3R)
+ *   3. dA  = int8_gemm_dx(Q2, W2_8)                [T, F] fp32, in workspace
+ *   4. dW2 = int8_gemm_dw(A8, Q2)
+ *   5. swiglu_quantize(dA, h1, h3) -> Q1, Q3       [tensor ids 1 (W1), 2 (W3)]
+ *   6. EC factors for W1 and W3
+ *   7. dX  = int8_gemm_dx(Q1, W1_8) + int8_gemm_dx(Q3, W3_8)
+ *   8. dW1 = int8_gemm_dw(X8, Q1), dW3 = int8_gemm_dw(X8, Q3)
+ * Independent SR quantizes each gradient twice (tensor ids + 0x100 for the
+ * dW copy) and applies no correction; RTNE applies no correction either.
+ * All buffers are device pointers owned by the caller; `args` itself is a
+ * HOST pointer read during the call only.
+ */
+struct s3r_ffn_args {
+    int64_t T, d, F, S;          /* tokens, model width, FFN width, tokens per example */
+    const void* dY;              /* bf16 [T, d] upstream gradient */
+    const void* h1;              /* bf16 [T, F] gate pre-activation X W1 */
+    const void* h3;              /* bf16 [T, F] up pre-activation X W3 */
+    const int8_t* X8;            /* [T, d] RTNE codes of X, per-token scale s_x [T] */
+    const float* s_x;
+    const int8_t* A8;            /* [T, F] RTNE codes of a = silu(h1)*h3, per-token scale s_a [T] */
+    const float* s_a;
+    const int8_t* W1_8;          /* [d, F] codes of W1, per-column scale s_w1 [F] */
+    const float* s_w1;
+    const int8_t* W3_8;          /* [d, F] codes of W3, per-column scale s_w3 [F] */
+    const float* s_w3;
+    const int8_t* W2_8;          /* [F, d] codes of W2, per-column scale s_w2 [d] */
+    const float* s_w2;
+    int round_mode;              /* enum s3r_round_mode */
+    int ec_mode;                 /* enum s3r_ec_mode (S3R only) */
+    uint64_t seed;
+    float* dX;                   /* out [T, d] fp32 */
+    float* dW1;                  /* out [d, F] fp32 */
+    float* dW3;                  /* out [d, F] fp32 */
+    float* dW2;                  /* out [F, d] fp32 */
+    void* workspace;
+    size_t workspace_bytes;      /* >= s3r_ffn_workspace_size(...) */
+    int* d_status;               /* device int or NULL */
+    void** step_events;          /* NULL, or S3R_FFN_NUM_EVENTS cudaEvent_t (a HOST array of handles)
+                                    recorded on `stream` at the step boundaries: before step 1 and
+                                    after steps 1, 2, 3, 4, 5, 6, 7, 8 above (for timing) */
+};
+#define S3R_FFN_NUM_EVENTS 9
+size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode);
+int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
+
+/*
+ * Test hooks: the exact int32 per-block partial products computed by the
+ * same tensor-core main loops as int8_gemm_dx / int8_gemm_dw, before any
+ * rescale.  out_dx [T, K, ceil(N/128)]: block kb of sum_n Q[t,n] W8[k,n];
+ * out_dw [K, N, ceil(T/128)]: block tb of sum_t X8[t,k] Q[t,n].  int32.
+ */
+int s3r_debug_dx_blocks(const int8_t* Q, const int8_t* W8, int64_t T, int64_t N, int64_t K, int32_t* out_dx,
+                        cudaStream_t stream);
+int s3r_debug_dw_blocks(const int8_t* X8, const int8_t* Q, int64_t T, int64_t K, int64_t N, int32_t* out_dw,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* S3R_H */

@@ -63,6 +63,7 @@ def lib():
             L.orc_sigmoidf.restype = C.c_float
             L.orc_sigmoidf.argtypes = [C.c_float]
             L.orc_quantize.restype = C.c_int
+            L.orc_quantize_window.restype = C.c_int
             L.orc_rtne_operand.restype = C.c_int
             L.orc_error_stats.restype = C.c_int
         return _lib
@@ -130,9 +131,11 @@ def sigmoidf(x: float) -> float:
     return lib().orc_sigmoidf(float(x))
 
 
-def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, TILE)):
+def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, TILE), window=None):
     """Fold, tile-scale and round G (float32 [T, N]).
 
+    window = (row_base, col_base, n_global) treats G as a tile-aligned window
+    of a larger tensor (thresholds use global indices).
     Returns (Q int8 [T,N], delta f32 [ceil(T/tr), ceil(N/tc)], E f32 [T,N], status)."""
     G = _f32(G)
     T, N = G.shape
@@ -141,8 +144,10 @@ def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, T
     Q = np.zeros((T, N), dtype=np.int8)
     delta = np.zeros((ntr, ntc), dtype=np.float32)
     E = np.zeros((T, N), dtype=np.float32)
-    st = lib().orc_quantize(_p(G), _i64(T), _i64(N), _i64(N), _p(_f32(s_x)), _p(_f32(s_w)), C.c_int(mode),
-                            C.c_uint64(seed), C.c_uint32(tensor_id), _i64(tr), _i64(tc), _p(Q), _p(delta), _p(E))
+    rb, cb, ng = window if window is not None else (0, 0, N)
+    st = lib().orc_quantize_window(_p(G), _i64(T), _i64(N), _i64(N), _p(_f32(s_x)), _p(_f32(s_w)), C.c_int(mode),
+                                   C.c_uint64(seed), C.c_uint32(tensor_id), _i64(tr), _i64(tc), _p(Q), _p(delta),
+                                   _p(E), _i64(rb), _i64(cb), _i64(ng))
     return Q, delta, E, st
 
 

@@ -142,9 +142,14 @@ static float fold_one(const float* G, int64_t ldg, const float* s_x, const float
     return g;
 }
 
-int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
-                 const float* s_x, const float* s_w, int mode, uint64_t seed, uint32_t tensor_id,
-                 int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E) {
+/* orc_quantize_window: the same on a tile-aligned window of a larger tensor
+ * whose first row is global token row_base and first column is col_base, in a
+ * tensor of n_global columns; only the threshold indices use these (token
+ * t + row_base; element (t + row_base) * n_global + col_base + n). */
+int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
+                        const float* s_x, const float* s_w, int mode, uint64_t seed, uint32_t tensor_id,
+                        int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E,
+                        int64_t row_base, int64_t col_base, int64_t n_global) {
     if (T < 0 || N < 0 || tr <= 0 || tc <= 0 || ldg < N) return ORC_ERR_ARG;
     if (mode != ORC_RTNE && mode != ORC_S3R && mode != ORC_INDEP) return ORC_ERR_ARG;
     int status = ORC_OK;
@@ -176,7 +181,7 @@ int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
             float inv = (amax > 0.0f) ? 127.0f / amax : 0.0f;
             delta[i * ntc + j] = d;
             for (int64_t t = t0; t < t1; ++t) {
-                float u_tok = (mode == ORC_S3R) ? orc_token_threshold((uint64_t)t, seed, tensor_id) : 0.0f;
+                float u_tok = (mode == ORC_S3R) ? orc_token_threshold((uint64_t)(t + row_base), seed, tensor_id) : 0.0f;
                 for (int64_t n = n0; n < n1; ++n) {
                     float g = fold_one(G, ldg, s_x, s_w, t, n);
                     float y = g * inv;
@@ -184,8 +189,10 @@ int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
                     if (mode == ORC_RTNE) {
                         qf = nearbyintf(y);
                     } else {
-                        float u = (mode == ORC_S3R) ? u_tok
-                                                    : orc_element_threshold((uint64_t)(t * N + n), seed, tensor_id);
+                        float u = (mode == ORC_S3R)
+                                      ? u_tok
+                                      : orc_element_threshold((uint64_t)((t + row_base) * n_global + col_base + n),
+                                                              seed, tensor_id);
                         qf = orc_sr_step(y, u);
                     }
                     if (qf > 127.0f) qf = 127.0f;
@@ -197,6 +204,12 @@ int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
         }
     }
     return status;
+}
+
+int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
+                 const float* s_x, const float* s_w, int mode, uint64_t seed, uint32_t tensor_id,
+                 int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E) {
+    return orc_quantize_window(G, T, N, ldg, s_x, s_w, mode, seed, tensor_id, tr, tc, Q, delta, E, 0, 0, N);
 }
 
 /* Forward operands ([S3R] §III-A): RTNE with a per-row (axis 0) or per-column
@@ -326,15 +339,20 @@ void orc_dx_blocks(const int8_t* Q, const int8_t* W8, int64_t T, int64_t N, int6
 void orc_dw_blocks(const int8_t* X8, const int8_t* Q, int64_t T, int64_t K, int64_t N, int64_t blk,
                    const int64_t* krows, int64_t nk, int32_t* J) {
     int64_t ntb = (T + blk - 1) / blk;
+    int64_t* acc = (int64_t*)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     for (int64_t r = 0; r < nk; ++r) {
         int64_t k = krows[r];
-        for (int64_t n = 0; n < N; ++n)
-            for (int64_t tb = 0; tb < ntb; ++tb) {
-                int64_t s = 0;
-                for (int64_t t = tb * blk; t < T && t < (tb + 1) * blk; ++t) s += (int64_t)X8[t * K + k] * Q[t * N + n];
-                J[(r * N + n) * ntb + tb] = (int32_t)s;
+        for (int64_t tb = 0; tb < ntb; ++tb) {
+            /* integer sums: the order of the t loop does not change them */
+            for (int64_t n = 0; n < N; ++n) acc[n] = 0;
+            for (int64_t t = tb * blk; t < T && t < (tb + 1) * blk; ++t) {
+                int64_t x = X8[t * K + k];
+                for (int64_t n = 0; n < N; ++n) acc[n] += x * Q[t * N + n];
             }
+            for (int64_t n = 0; n < N; ++n) J[(r * N + n) * ntb + tb] = (int32_t)acc[n];
+        }
     }
+    free(acc);
 }
 
 /* Activation gradient ([S3R] §III-A, §III-D), for the requested token rows:

@@ -1,0 +1,381 @@
+"""Python binding of libs3r: the S3R / S3R-EC INT8 backward on GB300 (sm_103a).
+
+Argument marshalling only: every step of the backward runs in the CUDA kernels
+of ``libs3r.so`` (built in-tree by ``build.py``).  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library is
+missing or no GPU is present, calls raise.
+
+The functions carry the C ABI's names (see ``include/s3r.h`` for the exact
+semantics, layouts and citations):
+
+    s3r_quantize, indep_sr_quantize, rtne_quantize, swiglu_quantize,
+    s3r_ec_correct, int8_gemm_dx, int8_gemm_dw, ffn_backward
+
+Outputs may be passed in (then they are written in place) or are allocated
+with torch on the inputs' device.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libs3r.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "s3r.h")
+TILE = 128
+
+S3R_OK = 0
+ROUND_RTNE, ROUND_S3R, ROUND_INDEP = 0, 1, 2
+EC_NONE, EC_DX_ONLY, EC_TWO_WAY = 0, 1, 2
+AXIS_ROW, AXIS_COL, AXIS_TILE = 0, 1, 2
+TID_W2, TID_W1, TID_W3, RHS_ID_OFFSET = 0, 1, 2, 0x100
+
+_lib = None
+
+_VP, _I64, _U64, _U32, _INT, _SZ = C.c_void_p, C.c_int64, C.c_uint64, C.c_uint32, C.c_int, C.c_size_t
+
+_SIGS = {
+    "s3r_status_string": (C.c_char_p, [_INT]),
+    "s3r_abi_version": (_INT, []),
+    "s3r_kernel_launch_count": (C.c_uint64, []),
+    "s3r_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "indep_sr_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _VP, _VP, _VP]),
+    "rtne_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _VP, _VP, _VP]),
+    "swiglu_quantize": (_INT, [_VP, _I64, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _INT, _U64, _U32, _U32,
+                               _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "s3r_ec_workspace_size": (_SZ, [_I64, _I64]),
+    "s3r_ec_correct": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                              _VP, _SZ, _VP, _VP]),
+    "int8_gemm_dx": (_INT, [_VP, _VP, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _I64, _VP, _INT, _VP, _VP]),
+    "int8_gemm_dw_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "int8_gemm_dw": (_INT, [_VP, _VP, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP, _VP, _SZ,
+                            _VP, _VP]),
+    "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT]),
+    "ffn_backward": (_INT, [_VP, _VP]),
+    "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP]),
+    "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
+}
+
+
+class S3RError(RuntimeError):
+    pass
+
+
+def header_functions() -> list[str]:
+    """Names of every function the C header declares."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?(?:int|size_t|uint64_t|char\s*\*|const\s+char\s*\*)\s*\**\s*(\w+)\s*\(",
+                      txt, re.M)
+
+
+def kernel_launch_count() -> int:
+    """Kernels launched by libs3r so far in this process."""
+    return int(lib().s3r_kernel_launch_count())
+
+
+def lib():
+    """Load libs3r.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise S3RError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().s3r_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != S3R_OK:
+        raise S3RError(f"{what}: {status_string(code)}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise S3RError("libs3r takes device tensors only")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_status(status: torch.Tensor):
+    """Synchronize-free read is not possible: this copies the device status to the host."""
+    code = int(status.item())
+    _check(code, "device status")
+
+
+def _bits(t):
+    assert t.dtype == torch.bfloat16, t.dtype
+    return t
+
+
+# ---------------------------------------------------------------------------
+# quantizers
+# ---------------------------------------------------------------------------
+@dataclass
+class Quantized:
+    Q: torch.Tensor
+    tile_scale: torch.Tensor
+    tok_err_part: torch.Tensor | None = None
+    col_err_part: torch.Tensor | None = None
+
+
+def s3r_quantize(G, s_x=None, s_w=None, seed=0, tensor_id=0, out: Quantized | None = None, partials=True,
+                 status=None, stream=None) -> Quantized:
+    T, N = G.shape
+    dev = G.device
+    if out is None:
+        out = Quantized(torch.empty((T, N), dtype=torch.int8, device=dev),
+                        torch.empty((_cdiv(T, TILE), _cdiv(N, TILE)), dtype=torch.float32, device=dev),
+                        torch.empty((T, _cdiv(N, TILE)), dtype=torch.float32, device=dev) if partials else None,
+                        torch.empty((_cdiv(T, TILE), N), dtype=torch.float32, device=dev) if partials else None)
+    _check(lib().s3r_quantize(_ptr(_bits(G)), T, N, G.stride(0), _ptr(s_x), _ptr(s_w), seed, tensor_id, _ptr(out.Q),
+                              _ptr(out.tile_scale), _ptr(out.tok_err_part), _ptr(out.col_err_part), _ptr(status),
+                              _stream(stream)), "s3r_quantize")
+    return out
+
+
+def indep_sr_quantize(G, s_x=None, s_w=None, seed=0, tensor_id=0, out: Quantized | None = None, status=None,
+                      stream=None) -> Quantized:
+    T, N = G.shape
+    dev = G.device
+    if out is None:
+        out = Quantized(torch.empty((T, N), dtype=torch.int8, device=dev),
+                        torch.empty((_cdiv(T, TILE), _cdiv(N, TILE)), dtype=torch.float32, device=dev))
+    _check(lib().indep_sr_quantize(_ptr(_bits(G)), T, N, G.stride(0), _ptr(s_x), _ptr(s_w), seed, tensor_id,
+                                   _ptr(out.Q), _ptr(out.tile_scale), _ptr(status), _stream(stream)),
+           "indep_sr_quantize")
+    return out
+
+
+def rtne_quantize(A, scale_axis=AXIS_TILE, s_x=None, s_w=None, Q=None, scale=None, status=None, stream=None):
+    R, Cc = A.shape
+    dev = A.device
+    if Q is None:
+        Q = torch.empty((R, Cc), dtype=torch.int8, device=dev)
+    if scale is None:
+        shape = {AXIS_ROW: (R,), AXIS_COL: (Cc,), AXIS_TILE: (_cdiv(R, TILE), _cdiv(Cc, TILE))}[scale_axis]
+        scale = torch.empty(shape, dtype=torch.float32, device=dev)
+    _check(lib().rtne_quantize(_ptr(_bits(A)), R, Cc, A.stride(0), _ptr(s_x), _ptr(s_w), scale_axis, _ptr(Q),
+                               _ptr(scale), _ptr(status), _stream(stream)), "rtne_quantize")
+    return Q, scale
+
+
+def swiglu_quantize(dA, h1, h3, s_x=None, s_w1=None, s_w3=None, round_mode=ROUND_S3R, seed=0, tid1=TID_W1,
+                    tid3=TID_W3, partials=True, status=None, stream=None):
+    T, F = dA.shape
+    dev = dA.device
+
+    def mk():
+        return Quantized(torch.empty((T, F), dtype=torch.int8, device=dev),
+                         torch.empty((_cdiv(T, TILE), _cdiv(F, TILE)), dtype=torch.float32, device=dev),
+                         torch.empty((T, _cdiv(F, TILE)), dtype=torch.float32, device=dev) if partials else None,
+                         torch.empty((_cdiv(T, TILE), F), dtype=torch.float32, device=dev) if partials else None)
+
+    o1, o3 = mk(), mk()
+    assert dA.dtype == torch.float32 and h1.stride(0) == h3.stride(0)
+    _check(lib().swiglu_quantize(_ptr(dA), dA.stride(0), _ptr(_bits(h1)), _ptr(_bits(h3)), h1.stride(0), T, F,
+                                 _ptr(s_x), _ptr(s_w1), _ptr(s_w3), round_mode, seed, tid1, tid3,
+                                 _ptr(o1.Q), _ptr(o1.tile_scale), _ptr(o1.tok_err_part), _ptr(o1.col_err_part),
+                                 _ptr(o3.Q), _ptr(o3.tile_scale), _ptr(o3.tok_err_part), _ptr(o3.col_err_part),
+                                 _ptr(status), _stream(stream)), "swiglu_quantize")
+    return o1, o3
+
+
+# ---------------------------------------------------------------------------
+# error correction
+# ---------------------------------------------------------------------------
+@dataclass
+class ECFactors:
+    eps: torch.Tensor
+    mu: torch.Tensor
+    colmean: torch.Tensor
+    rowsum: torch.Tensor | None
+    v: torch.Tensor | None
+    xsum: torch.Tensor | None
+    p: torch.Tensor | None
+
+
+def s3r_ec_correct(q: Quantized, T, N, S, W8=None, X8=None, ec_mode=EC_TWO_WAY, status=None, stream=None) -> ECFactors:
+    dev = q.Q.device
+    B = T // S
+    K = W8.shape[0] if W8 is not None else 0
+    f = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)
+    i = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)
+    ec = ECFactors(f(T), f(B), f(B, N), i(K) if K else None, f(B, K) if K else None,
+                   i(B, K) if ec_mode == EC_TWO_WAY else None, f(K) if ec_mode == EC_TWO_WAY else None)
+    ws_bytes = lib().s3r_ec_workspace_size(T, K) if ec_mode == EC_TWO_WAY else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check(lib().s3r_ec_correct(_ptr(q.tok_err_part), _ptr(q.col_err_part), T, N, S, _ptr(W8), K, _ptr(X8), ec_mode,
+                                _ptr(ec.eps), _ptr(ec.mu), _ptr(ec.colmean), _ptr(ec.rowsum), _ptr(ec.v),
+                                _ptr(ec.xsum), _ptr(ec.p), _ptr(ws), ws_bytes, _ptr(status), _stream(stream)),
+           "s3r_ec_correct")
+    return ec
+
+
+# ---------------------------------------------------------------------------
+# GEMMs
+# ---------------------------------------------------------------------------
+def int8_gemm_dx(Q, tile_scale, W8, s_x=None, ec_mode=EC_NONE, ec: ECFactors | None = None, S=None, dX=None,
+                 accumulate=False, status=None, stream=None):
+    T, N = Q.shape
+    K = W8.shape[0]
+    if dX is None:
+        dX = torch.empty((T, K), dtype=torch.float32, device=Q.device)
+    S = T if S is None else S
+    _check(lib().int8_gemm_dx(_ptr(Q), _ptr(tile_scale), _ptr(W8), T, N, K, _ptr(s_x), ec_mode,
+                              _ptr(ec.eps if ec else None), _ptr(ec.rowsum if ec else None),
+                              _ptr(ec.v if ec else None), S, _ptr(dX), int(accumulate), _ptr(status),
+                              _stream(stream)), "int8_gemm_dx")
+    return dX
+
+
+def int8_gemm_dw(X8, Q, tile_scale, s_w=None, ec_mode=EC_NONE, ec: ECFactors | None = None, S=None, dW=None,
+                 workspace=None, status=None, stream=None):
+    T, K = X8.shape
+    N = Q.shape[1]
+    if dW is None:
+        dW = torch.empty((K, N), dtype=torch.float32, device=Q.device)
+    ws_bytes = lib().int8_gemm_dw_workspace_size(T, K, N)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
+    S = T if S is None else S
+    two = ec_mode == EC_TWO_WAY and ec is not None
+    _check(lib().int8_gemm_dw(_ptr(X8), _ptr(Q), _ptr(tile_scale), T, K, N, _ptr(s_w), ec_mode,
+                              _ptr(ec.colmean if two else None), _ptr(ec.mu if two else None),
+                              _ptr(ec.xsum if two else None), _ptr(ec.p if two else None), S, _ptr(dW),
+                              _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)), "int8_gemm_dw")
+    return dW
+
+
+def debug_dx_blocks(Q, W8, stream=None):
+    T, N = Q.shape
+    K = W8.shape[0]
+    out = torch.empty((T, K, _cdiv(N, TILE)), dtype=torch.int32, device=Q.device)
+    _check(lib().s3r_debug_dx_blocks(_ptr(Q), _ptr(W8), T, N, K, _ptr(out), _stream(stream)), "s3r_debug_dx_blocks")
+    return out
+
+
+def debug_dw_blocks(X8, Q, stream=None):
+    T, K = X8.shape
+    N = Q.shape[1]
+    out = torch.empty((K, N, _cdiv(T, TILE)), dtype=torch.int32, device=Q.device)
+    ws_bytes = lib().int8_gemm_dw_workspace_size(T, K, N)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
+    _check(lib().s3r_debug_dw_blocks(_ptr(X8), _ptr(Q), T, K, N, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "s3r_debug_dw_blocks")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# whole FFN block
+# ---------------------------------------------------------------------------
+class _FfnArgs(C.Structure):
+    _fields_ = [("T", C.c_int64), ("d", C.c_int64), ("F", C.c_int64), ("S", C.c_int64),
+                ("dY", _VP), ("h1", _VP), ("h3", _VP),
+                ("X8", _VP), ("s_x", _VP), ("A8", _VP), ("s_a", _VP),
+                ("W1_8", _VP), ("s_w1", _VP), ("W3_8", _VP), ("s_w3", _VP), ("W2_8", _VP), ("s_w2", _VP),
+                ("round_mode", C.c_int), ("ec_mode", C.c_int), ("seed", C.c_uint64),
+                ("dX", _VP), ("dW1", _VP), ("dW3", _VP), ("dW2", _VP),
+                ("workspace", _VP), ("workspace_bytes", C.c_size_t), ("d_status", _VP),
+                ("step_events", C.POINTER(C.c_void_p))]
+
+
+FFN_NUM_EVENTS = 9
+FFN_STEPS = ["quantize dY", "EC W2", "GEMM dA (dX of W2)", "GEMM dW2", "SwiGLU + quantize dh1/dh3", "EC W1/W3",
+             "GEMM dX (W1 + W3)", "GEMM dW1 + dW3"]
+
+
+@dataclass
+class FFNOperands:
+    """Saved forward state of a SwiGLU FFN block, on the device."""
+    X8: torch.Tensor
+    s_x: torch.Tensor
+    A8: torch.Tensor
+    s_a: torch.Tensor
+    W1_8: torch.Tensor
+    s_w1: torch.Tensor
+    W3_8: torch.Tensor
+    s_w3: torch.Tensor
+    W2_8: torch.Tensor
+    s_w2: torch.Tensor
+    h1: torch.Tensor
+    h3: torch.Tensor
+
+
+def ffn_forward_operands(X, W1, W3, W2, a, h1, h3, stream=None) -> FFNOperands:
+    """RTNE forward operands (per-token scales for X and a, per-output-channel
+    scales for the weights) computed with rtne_quantize."""
+    X8, s_x = rtne_quantize(X, AXIS_ROW, stream=stream)
+    A8, s_a = rtne_quantize(a, AXIS_ROW, stream=stream)
+    W1_8, s_w1 = rtne_quantize(W1, AXIS_COL, stream=stream)
+    W3_8, s_w3 = rtne_quantize(W3, AXIS_COL, stream=stream)
+    W2_8, s_w2 = rtne_quantize(W2, AXIS_COL, stream=stream)
+    return FFNOperands(X8, s_x, A8, s_a, W1_8, s_w1, W3_8, s_w3, W2_8, s_w2, h1, h3)
+
+
+def ffn_workspace_size(T, d, F, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY) -> int:
+    return int(lib().s3r_ffn_workspace_size(T, d, F, S, round_mode, ec_mode))
+
+
+@dataclass
+class FFNGrads:
+    dX: torch.Tensor
+    dW1: torch.Tensor
+    dW3: torch.Tensor
+    dW2: torch.Tensor
+
+
+def alloc_ffn_grads(T, d, F, device="cuda") -> FFNGrads:
+    f = lambda *s: torch.empty(s, dtype=torch.float32, device=device)
+    return FFNGrads(f(T, d), f(d, F), f(d, F), f(F, d))
+
+
+def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, seed=0,
+                 grads: FFNGrads | None = None, workspace=None, status=None, stream=None,
+                 step_events=None) -> FFNGrads:
+    """step_events: optional list of FFN_NUM_EVENTS torch.cuda.Event (timing)."""
+    T, d = dY.shape
+    F = ops.A8.shape[1]
+    dev = dY.device
+    if grads is None:
+        grads = alloc_ffn_grads(T, d, F, dev)
+    need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    p = lambda t: None if t is None else t.data_ptr()
+    args = _FfnArgs(T, d, F, S, p(_bits(dY)), p(_bits(ops.h1)), p(_bits(ops.h3)), p(ops.X8), p(ops.s_x), p(ops.A8),
+                    p(ops.s_a), p(ops.W1_8), p(ops.s_w1), p(ops.W3_8), p(ops.s_w3), p(ops.W2_8), p(ops.s_w2),
+                    round_mode, ec_mode, seed, p(grads.dX), p(grads.dW1), p(grads.dW3), p(grads.dW2),
+                    p(workspace), workspace.numel(), p(status), None)
+    if step_events is not None:
+        assert len(step_events) == FFN_NUM_EVENTS
+        handles = (C.c_void_p * FFN_NUM_EVENTS)(*[C.c_void_p(e.cuda_event) for e in step_events])
+        args.step_events = C.cast(handles, C.POINTER(C.c_void_p))
+    _check(lib().ffn_backward(C.byref(args), _stream(stream)), "ffn_backward")
+    return grads

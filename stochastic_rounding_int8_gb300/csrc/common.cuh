@@ -1,0 +1,106 @@
+// common.cuh -- device helpers shared by the libs3r kernels (sm_103a).
+//
+// The library is compiled with -fmad=false: no multiply-add is contracted
+// unless written as fmaf(), so every fp32 operation that decides an int8 code
+// happens exactly as the header documents it.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/s3r.h"
+
+namespace s3r {
+
+constexpr int kTile = S3R_TILE;
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies whose high
+// halves are xored with the other two counter words and the key; the key is
+// bumped by the Weyl increments between rounds.
+// ---------------------------------------------------------------------------
+struct Philox4 {
+    uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                                 uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo_a = 0xD2511F53u * c0, hi_a = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo_b = 0xCD9E8D57u * c2, hi_b = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi_b ^ c1 ^ k0;
+        const uint32_t n2 = hi_a ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo_b;
+        c2 = n2;
+        c3 = lo_a;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return Philox4{c0, c1, c2, c3};
+}
+
+// Top 24 bits of a word as a threshold on the grid {0, 2^-24, ..., 1 - 2^-24}.
+__device__ __forceinline__ float unit24(uint32_t w) { return (float)(w >> 8) * 5.9604644775390625e-8f; }
+
+// S3R per-token threshold (Phi_2D): word 0 of Philox(counter = t, key = (seed, id)).
+__device__ __forceinline__ float token_threshold(uint64_t t, uint32_t seed_lo, uint32_t tensor_id) {
+    return unit24(philox4x32_10((uint32_t)t, (uint32_t)(t >> 32), 0u, 0u, seed_lo, tensor_id).x);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_at(const uint16_t* p) { return __uint_as_float((uint32_t)(*p) << 16); }
+
+// ---------------------------------------------------------------------------
+// exp by Cody-Waite reduction x = n ln2 + r (ln2 = head + tail, the head with
+// 16 significant bits so n*head is exact), e^r by the degree-7 Taylor series
+// in Horner form, times 2^n built in the exponent field.  The argument is
+// clamped to [-87, 88] so 2^n is a normal number.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float exp_cw(float x) {
+    x = fminf(fmaxf(x, -87.0f), 88.0f);
+    const float n = rintf(x * 1.44269502162933349609375f);     // log2(e) in fp32
+    float r = fmaf(-n, 0.693145751953125f, x);                   // 45426 / 2^16
+    r = fmaf(-n, 1.42860682028622683e-06f, r);                   // ln2 - head
+    float poly = 1.98412701138295233e-04f;                       // 1/5040
+    poly = fmaf(poly, r, 1.38888892251998186e-03f);              // 1/720
+    poly = fmaf(poly, r, 8.33333376795053482e-03f);              // 1/120
+    poly = fmaf(poly, r, 4.16666679084300995e-02f);              // 1/24
+    poly = fmaf(poly, r, 1.66666671633720398e-01f);              // 1/6
+    poly = fmaf(poly, r, 0.5f);
+    poly = fmaf(poly, r, 1.0f);
+    poly = fmaf(poly, r, 1.0f);
+    const float two_n = __int_as_float(((int)n + 127) << 23);
+    return poly * two_n;
+}
+
+__device__ __forceinline__ float sigmoid_cw(float x) { return 1.0f / (1.0f + exp_cw(-x)); }
+
+// Record a device-side error (first writer wins is not needed: any error code
+// tells the caller to look; all writers write a negative constant).
+__device__ __forceinline__ void set_status(int* d_status, int code) {
+    if (d_status) *(volatile int*)d_status = code;
+}
+
+}  // namespace s3r
+
+// Host-side helpers.  Every kernel launch is followed by S3R_CHECK_LAUNCH(),
+// which also counts it (s3r_kernel_launch_count()).
+void s3r_count_launch();
+#define S3R_CHECK_LAUNCH()                                 \
+    do {                                                   \
+        s3r_count_launch();                                \
+        if (cudaPeekAtLastError() != cudaSuccess) {        \
+            (void)cudaGetLastError();                      \
+            return S3R_ERR_CUDA;                           \
+        }                                                  \
+    } while (0)
+
+static inline bool s3r_aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }
+__host__ __device__ static inline int64_t s3r_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -1,0 +1,464 @@
+// quantize.cu -- tile quantizers of the backward gradient (S3R, independent SR,
+// RTNE), the SwiGLU-fused variant and the forward-operand RTNE kernels.
+//
+// Paper: "Efficient Quantization Training with Stochastic Rounding via
+// Structured Subspace Randomness" §III-A (fold, per-tensor/tile step, SR
+// operator), §III-B (one threshold per token broadcast over the hidden
+// dimension; one quantized tensor for both products), §IV-B (baselines).
+//
+// Design (HBM-bound): one CTA owns one 128x128 tile.  Every thread holds a
+// 16-byte chunk (8 columns) of RPT rows in registers, loaded once with 128-bit
+// coalesced loads; the tile absmax is a warp redux.sync on the IEEE bit
+// patterns (which also flags NaN/Inf) then a CTA reduction; the per-token
+// Philox threshold is computed by one lane per row and broadcast with
+// __shfl_sync; codes are written once as 8-byte stores; the error partials are
+// reduced with shuffles and a small shared-memory pass, in a fixed order.
+#include "common.cuh"
+
+namespace s3r {
+
+enum QMode { kRTNE = 0, kS3R = 1, kINDEP = 2 };
+
+// Per-thread geometry of a 128x128 tile: chunk c (8 columns), rows r0 + j*RSTRIDE.
+template <int RPT>
+struct TileGeom {
+    static constexpr int kThreads = 16 * (128 / RPT);
+    static constexpr int kRowStride = 128 / RPT;
+    static constexpr int kWarps = kThreads / 32;
+};
+
+struct QuantOut {
+    int8_t* Q;
+    float* scale;
+    float* tok;
+    float* col;
+    uint32_t tensor_id;
+};
+
+struct QuantCommon {
+    int64_t T, N;
+    int64_t ntc;
+    uint32_t seed_lo;
+    int* d_status;
+    bool vec_store;  // Q rows 8-byte aligned for every chunk
+};
+
+// Block-wide max of non-negative float bit patterns (NaN/Inf compare largest).
+template <int WARPS>
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) m = max(m, smem[w]);
+    __syncthreads();
+    return m;
+}
+
+// Round the folded values g[RPT][8] of one thread to codes, write them, and
+// accumulate the tile's error partials.  amax_bits is the tile absmax.
+template <int MODE, int RPT>
+__device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32_t amax_bits, int64_t t0, int64_t n0,
+                                                int r0, int c, const QuantCommon& C, const QuantOut& O,
+                                                float* col_smem /* [WARPS][128] */) {
+    using Geo = TileGeom<RPT>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t nc0 = n0 + 8 * c;
+    const bool nonfinite = amax_bits >= 0x7F800000u;
+    const float amax = __uint_as_float(amax_bits);
+    const float d = nonfinite ? __uint_as_float(0x7FC00000u) : amax / 127.0f;
+    const float inv = (amax_bits == 0u || nonfinite) ? 0.0f : 127.0f / amax;
+    if (threadIdx.x == 0) {
+        O.scale[(t0 / kTile) * C.ntc + (n0 / kTile)] = d;
+        if (nonfinite) set_status(C.d_status, S3R_ERR_NONFINITE);
+    }
+
+    // thresholds of my rows: lane (half*16 + j) draws the one of row r0 + j*RSTRIDE
+    float u_row[RPT];
+    if (MODE == kS3R) {
+        float mine = 0.0f;
+        if (c < RPT) mine = token_threshold((uint64_t)(t0 + r0 + c * Geo::kRowStride), C.seed_lo, O.tensor_id);
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) u_row[j] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) + j);
+    }
+
+    float colsum[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) colsum[i] = 0.0f;
+
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int64_t t = t0 + r0 + j * Geo::kRowStride;
+        float u8[8];
+        if (MODE == kINDEP) {
+            if ((C.N & 3) == 0) {
+                const uint64_t e0 = (uint64_t)t * (uint64_t)C.N + (uint64_t)nc0;  // multiple of 4
+                const uint64_t ctr = e0 >> 2;
+                const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, C.seed_lo, O.tensor_id);
+                const Philox4 b =
+                    philox4x32_10((uint32_t)(ctr + 1), (uint32_t)((ctr + 1) >> 32), 0u, 0u, C.seed_lo, O.tensor_id);
+                u8[0] = unit24(a.x); u8[1] = unit24(a.y); u8[2] = unit24(a.z); u8[3] = unit24(a.w);
+                u8[4] = unit24(b.x); u8[5] = unit24(b.y); u8[6] = unit24(b.z); u8[7] = unit24(b.w);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint64_t e = (uint64_t)t * (uint64_t)C.N + (uint64_t)(nc0 + i);
+                    const uint64_t ctr = e >> 2;
+                    const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, C.seed_lo, O.tensor_id);
+                    const uint32_t w = (e & 3) == 0 ? a.x : (e & 3) == 1 ? a.y : (e & 3) == 2 ? a.z : a.w;
+                    u8[i] = unit24(w);
+                }
+            }
+        }
+        float rowsum = 0.0f;
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float y = g[j][i] * inv;
+            float qf;
+            if (MODE == kRTNE) {
+                qf = rintf(y);
+            } else {
+                const float u = (MODE == kS3R) ? u_row[j] : u8[i];
+                const float f = floorf(y);
+                const float p = y - f;
+                qf = (u < p) ? f + 1.0f : f;
+            }
+            qf = fminf(fmaxf(qf, -127.0f), 127.0f);
+            const int q = (int)qf;
+            packed[i >> 2] |= ((uint32_t)(q & 0xFF)) << (8 * (i & 3));
+            const float e = nonfinite ? 0.0f : fmaf(d, qf, -g[j][i]);
+            rowsum += e;
+            colsum[i] += e;
+        }
+        if (nonfinite) packed[0] = packed[1] = 0u;
+        if (t < C.T) {
+            int8_t* dst = O.Q + t * C.N + nc0;
+            if (C.vec_store && nc0 + 8 <= C.N) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (nc0 + i < C.N) dst[i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFF);
+            }
+        }
+        if (O.tok) {
+            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 8);
+            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 4);
+            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 2);
+            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 1);
+            if (c == 0 && t < C.T) O.tok[t * C.ntc + n0 / kTile] = rowsum;
+        }
+    }
+    if (O.col) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) colsum[i] += __shfl_xor_sync(0xFFFFFFFFu, colsum[i], 16);
+        if (lane < 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) col_smem[warp * 128 + 8 * c + i] = colsum[i];
+        }
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            float s = 0.0f;
+#pragma unroll
+            for (int w = 0; w < Geo::kWarps; ++w) s += col_smem[w * 128 + threadIdx.x];
+            if (n0 + threadIdx.x < C.N) O.col[(t0 / kTile) * C.N + n0 + threadIdx.x] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward-gradient tile quantizer: bf16 G -> fold -> tile scale -> codes.
+// ---------------------------------------------------------------------------
+struct TileQuantArgs {
+    const uint16_t* G;
+    int64_t ldg;
+    const float* s_x;
+    const float* s_w;
+    bool vec_load;  // rows 16-byte aligned
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(256) quantize_tile_kernel(TileQuantArgs A, QuantCommon C, QuantOut O) {
+    constexpr int RPT = 8;
+    using Geo = TileGeom<RPT>;
+    __shared__ uint32_t red[Geo::kWarps];
+    __shared__ float col_smem[Geo::kWarps * 128];
+    const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
+    const int64_t t0 = (int64_t)blockIdx.y * kTile, n0 = (int64_t)blockIdx.x * kTile;
+    const int64_t nc0 = n0 + 8 * c;
+
+    uint4 raw[RPT];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int64_t t = t0 + r0 + j * Geo::kRowStride;
+        raw[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (t < C.T) {
+            const uint16_t* src = A.G + t * A.ldg + nc0;
+            if (A.vec_load && nc0 + 8 <= C.N) {
+                raw[j] = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (nc0 + i < C.N) w[i >> 1] |= (uint32_t)src[i] << (16 * (i & 1));
+                raw[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+    float sw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sw[i] = (A.s_w && nc0 + i < C.N) ? __ldg(A.s_w + nc0 + i) : 1.0f;
+
+    float g[RPT][8];
+    uint32_t amax_bits = 0u;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int64_t t = t0 + r0 + j * Geo::kRowStride;
+        const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+        const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float v = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+            if (A.s_x) v = sx * v;
+            if (A.s_w) v = v * sw[i];
+            g[j][i] = v;
+            amax_bits = max(amax_bits, __float_as_uint(v) & 0x7FFFFFFFu);
+        }
+    }
+    amax_bits = block_max_u32<Geo::kWarps>(amax_bits, red);
+    round_and_store<MODE, RPT>(g, amax_bits, t0, n0, r0, c, C, O, col_smem);
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU glue fused into the two quantizations (dh1 -> Q1, dh3 -> Q3).
+// ---------------------------------------------------------------------------
+struct SwigluArgs {
+    const float* dA;
+    int64_t ldd;
+    const uint16_t* h1;
+    const uint16_t* h3;
+    int64_t ldh;
+    const float* s_x;
+    const float* s_w1;
+    const float* s_w3;
+    bool vec_load;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, QuantCommon C, QuantOut O1, QuantOut O3) {
+    constexpr int RPT = 4;
+    using Geo = TileGeom<RPT>;
+    __shared__ uint32_t red[Geo::kWarps];
+    __shared__ float col_smem[Geo::kWarps * 128];
+    const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
+    const int64_t t0 = (int64_t)blockIdx.y * kTile, n0 = (int64_t)blockIdx.x * kTile;
+    const int64_t nc0 = n0 + 8 * c;
+
+    float g1[RPT][8], g3[RPT][8];
+    float sw1[8], sw3[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool ok = nc0 + i < C.N;
+        sw1[i] = (A.s_w1 && ok) ? __ldg(A.s_w1 + nc0 + i) : 1.0f;
+        sw3[i] = (A.s_w3 && ok) ? __ldg(A.s_w3 + nc0 + i) : 1.0f;
+    }
+    uint32_t amax1 = 0u, amax3 = 0u;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int64_t t = t0 + r0 + j * Geo::kRowStride;
+        float da[8], x1[8], x3[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) da[i] = x1[i] = x3[i] = 0.0f;
+        if (t < C.T) {
+            const float* pd = A.dA + t * A.ldd + nc0;
+            const uint16_t* p1 = A.h1 + t * A.ldh + nc0;
+            const uint16_t* p3 = A.h3 + t * A.ldh + nc0;
+            if (A.vec_load && nc0 + 8 <= C.N) {
+                const float4 d0 = __ldg(reinterpret_cast<const float4*>(pd));
+                const float4 d1 = __ldg(reinterpret_cast<const float4*>(pd) + 1);
+                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(p1));
+                const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(p3));
+                da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
+                da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
+                const uint32_t w1[4] = {a1.x, a1.y, a1.z, a1.w}, w3[4] = {a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    x1[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+                    x3[i] = (i & 1) ? bf16_hi(w3[i >> 1]) : bf16_lo(w3[i >> 1]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (nc0 + i < C.N) {
+                        da[i] = pd[i];
+                        x1[i] = bf16_at(p1 + i);
+                        x3[i] = bf16_at(p3 + i);
+                    }
+            }
+        }
+        const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // glue, in the documented order (no contraction: built with -fmad=false)
+            const float s = sigmoid_cw(x1[i]);
+            const float silu = x1[i] * s;
+            const float dsilu = s * (1.0f + x1[i] * (1.0f - s));
+            const float dh1 = (da[i] * x3[i]) * dsilu;
+            const float dh3 = da[i] * silu;
+            float v1 = dh1, v3 = dh3;
+            if (A.s_x) { v1 = sx * v1; v3 = sx * v3; }
+            if (A.s_w1) v1 = v1 * sw1[i];
+            if (A.s_w3) v3 = v3 * sw3[i];
+            g1[j][i] = v1;
+            g3[j][i] = v3;
+            amax1 = max(amax1, __float_as_uint(v1) & 0x7FFFFFFFu);
+            amax3 = max(amax3, __float_as_uint(v3) & 0x7FFFFFFFu);
+        }
+    }
+    amax1 = block_max_u32<Geo::kWarps>(amax1, red);
+    amax3 = block_max_u32<Geo::kWarps>(amax3, red);
+    round_and_store<MODE, RPT>(g1, amax1, t0, n0, r0, c, C, O1, col_smem);
+    round_and_store<MODE, RPT>(g3, amax3, t0, n0, r0, c, C, O3, col_smem);
+}
+
+// ---------------------------------------------------------------------------
+// Forward operands: RTNE with one scale per row or per column (scale 1 for an
+// all-zero row/column).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rtne_rows_kernel(const uint16_t* A, int64_t R, int64_t C, int64_t lda,
+                                                        int8_t* Q, float* scale, int* d_status) {
+    const int64_t r = (int64_t)blockIdx.x;
+    __shared__ uint32_t red[8];
+    uint32_t m = 0u;
+    for (int64_t c = threadIdx.x; c < C; c += blockDim.x)
+        m = max(m, __float_as_uint(bf16_at(A + r * lda + c)) & 0x7FFFFFFFu);
+    m = block_max_u32<8>(m, red);
+    if (m >= 0x7F800000u) {
+        if (threadIdx.x == 0) { set_status(d_status, S3R_ERR_NONFINITE); scale[r] = __uint_as_float(0x7FC00000u); }
+        for (int64_t c = threadIdx.x; c < C; c += blockDim.x) Q[r * C + c] = 0;
+        return;
+    }
+    const float amax = __uint_as_float(m);
+    const float s = m ? amax / 127.0f : 1.0f;
+    const float inv = m ? 127.0f / amax : 1.0f;
+    if (threadIdx.x == 0) scale[r] = s;
+    for (int64_t c = threadIdx.x; c < C; c += blockDim.x) {
+        const float q = fminf(fmaxf(rintf(bf16_at(A + r * lda + c) * inv), -127.0f), 127.0f);
+        Q[r * C + c] = (int8_t)(int)q;
+    }
+}
+
+__global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64_t R, int64_t C, int64_t lda,
+                                                        int8_t* Q, float* scale, int* d_status) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    uint32_t m = 0u;
+    for (int64_t r = 0; r < R; ++r) m = max(m, __float_as_uint(bf16_at(A + r * lda + c)) & 0x7FFFFFFFu);
+    if (m >= 0x7F800000u) {
+        set_status(d_status, S3R_ERR_NONFINITE);
+        scale[c] = __uint_as_float(0x7FC00000u);
+        for (int64_t r = 0; r < R; ++r) Q[r * C + c] = 0;
+        return;
+    }
+    const float amax = __uint_as_float(m);
+    const float s = m ? amax / 127.0f : 1.0f;
+    const float inv = m ? 127.0f / amax : 1.0f;
+    scale[c] = s;
+    for (int64_t r = 0; r < R; ++r) {
+        const float q = fminf(fmaxf(rintf(bf16_at(A + r * lda + c) * inv), -127.0f), 127.0f);
+        Q[r * C + c] = (int8_t)(int)q;
+    }
+}
+
+}  // namespace s3r
+
+using namespace s3r;
+
+static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
+                             const float* s_w, uint64_t seed, uint32_t tensor_id, int8_t* Q, float* scale, float* tok,
+                             float* col, int* d_status, cudaStream_t stream) {
+    if (T < 0 || N < 0) return S3R_ERR_ARG;
+    if (T == 0 || N == 0) return S3R_OK;
+    if (!G || !Q || !scale) return S3R_ERR_ARG;
+    if (ldg < N) return S3R_ERR_SHAPE;
+    if (s3r_cdiv(T, kTile) > 65535) return S3R_ERR_UNSUPPORTED;
+    TileQuantArgs A{static_cast<const uint16_t*>(G), ldg, s_x, s_w, s3r_aligned16(G) && (ldg % 8) == 0};
+    QuantCommon C{T, N, s3r_cdiv(N, kTile), (uint32_t)seed, d_status,
+                  s3r_aligned16(Q) && (N % 8) == 0};
+    QuantOut O{Q, scale, tok, col, tensor_id};
+    dim3 grid((unsigned)s3r_cdiv(N, kTile), (unsigned)s3r_cdiv(T, kTile));
+    switch (mode) {
+        case kRTNE: quantize_tile_kernel<kRTNE><<<grid, 256, 0, stream>>>(A, C, O); break;
+        case kS3R: quantize_tile_kernel<kS3R><<<grid, 256, 0, stream>>>(A, C, O); break;
+        case kINDEP: quantize_tile_kernel<kINDEP><<<grid, 256, 0, stream>>>(A, C, O); break;
+        default: return S3R_ERR_ARG;
+    }
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+extern "C" int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
+                            uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale, float* tok_err_part,
+                            float* col_err_part, int* d_status, cudaStream_t stream) {
+    return launch_tile_quant(kS3R, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, tile_scale, tok_err_part,
+                             col_err_part, d_status, stream);
+}
+
+extern "C" int indep_sr_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
+                                 const float* s_w, uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale,
+                                 int* d_status, cudaStream_t stream) {
+    return launch_tile_quant(kINDEP, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, tile_scale, nullptr, nullptr,
+                             d_status, stream);
+}
+
+extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, const float* s_x, const float* s_w,
+                             int scale_axis, int8_t* Q, float* scale, int* d_status, cudaStream_t stream) {
+    if (scale_axis == S3R_AXIS_TILE)
+        return launch_tile_quant(kRTNE, A, R, C, lda, s_x, s_w, 0, 0, Q, scale, nullptr, nullptr, d_status, stream);
+    if (R < 0 || C < 0) return S3R_ERR_ARG;
+    if (R == 0 || C == 0) return S3R_OK;
+    if (!A || !Q || !scale) return S3R_ERR_ARG;
+    if (lda < C) return S3R_ERR_SHAPE;
+    if (s_x || s_w) return S3R_ERR_ARG;  // forward operands are not folded
+    const uint16_t* a = static_cast<const uint16_t*>(A);
+    if (scale_axis == S3R_AXIS_ROW) {
+        if (R > 0x7FFFFFFF) return S3R_ERR_UNSUPPORTED;
+        rtne_rows_kernel<<<(unsigned)R, 256, 0, stream>>>(a, R, C, lda, Q, scale, d_status);
+    } else if (scale_axis == S3R_AXIS_COL) {
+        rtne_cols_kernel<<<(unsigned)s3r_cdiv(C, 256), 256, 0, stream>>>(a, R, C, lda, Q, scale, d_status);
+    } else {
+        return S3R_ERR_ARG;
+    }
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh, int64_t T,
+                               int64_t F, const float* s_x, const float* s_w1, const float* s_w3, int round_mode,
+                               uint64_t seed, uint32_t tid1, uint32_t tid3, int8_t* Q1, float* scale1, float* tok1,
+                               float* col1, int8_t* Q3, float* scale3, float* tok3, float* col3, int* d_status,
+                               cudaStream_t stream) {
+    if (T < 0 || F < 0) return S3R_ERR_ARG;
+    if (T == 0 || F == 0) return S3R_OK;
+    if (!dA || !h1 || !h3 || !Q1 || !Q3 || !scale1 || !scale3) return S3R_ERR_ARG;
+    if (ldd < F || ldh < F) return S3R_ERR_SHAPE;
+    if (s3r_cdiv(T, kTile) > 65535) return S3R_ERR_UNSUPPORTED;
+    SwigluArgs A{dA, ldd, static_cast<const uint16_t*>(h1), static_cast<const uint16_t*>(h3), ldh, s_x, s_w1, s_w3,
+                 s3r_aligned16(dA) && s3r_aligned16(h1) && s3r_aligned16(h3) && (ldd % 4) == 0 && (ldh % 8) == 0};
+    QuantCommon C{T, F, s3r_cdiv(F, kTile), (uint32_t)seed, d_status,
+                  s3r_aligned16(Q1) && s3r_aligned16(Q3) && (F % 8) == 0};
+    QuantOut O1{Q1, scale1, tok1, col1, tid1}, O3{Q3, scale3, tok3, col3, tid3};
+    dim3 grid((unsigned)s3r_cdiv(F, kTile), (unsigned)s3r_cdiv(T, kTile));
+    switch (round_mode) {
+        case S3R_ROUND_RTNE: swiglu_quantize_kernel<kRTNE><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
+        case S3R_ROUND_S3R: swiglu_quantize_kernel<kS3R><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
+        case S3R_ROUND_INDEP: swiglu_quantize_kernel<kINDEP><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
+        default: return S3R_ERR_ARG;
+    }
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}

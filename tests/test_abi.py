@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side argument checks work without a GPU (nothing is launched
+when they fail)."""
+import ctypes as C
+
+import pytest
+
+import stochastic_rounding_int8_gb300 as s3r
+from stochastic_rounding_int8_gb300 import build as s3r_build
+
+
+@pytest.fixture(scope="module")
+def L():
+    s3r_build.build()
+    return s3r.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(s3r.header_functions())
+    for want in ["s3r_quantize", "indep_sr_quantize", "rtne_quantize", "s3r_ec_correct", "int8_gemm_dx",
+                 "int8_gemm_dw", "ffn_backward", "swiglu_quantize", "s3r_status_string"]:
+        assert want in names
+
+
+def test_library_exports_every_header_symbol(L):
+    for name in s3r.header_functions():
+        assert hasattr(L, name), name
+        assert name in s3r._SIGS, f"binding has no signature for {name}"
+
+
+def test_status_strings(L):
+    assert s3r.status_string(0) == "S3R_OK"
+    for code in range(-1, -9, -1):
+        assert s3r.status_string(code).startswith("S3R_ERR_")
+    assert s3r.status_string(-99) == "S3R_ERR_UNKNOWN"
+    assert L.s3r_abi_version() == 100
+
+
+def test_host_argument_checks_need_no_gpu(L):
+    null = None
+    # null outputs -> S3R_ERR_ARG before any launch
+    assert L.s3r_quantize(C.c_void_p(16), 4, 4, 4, null, null, 0, 0, null, null, null, null, null, null) == -1
+    # empty tensors are a no-op
+    assert L.s3r_quantize(null, 0, 0, 0, null, null, 0, 0, null, null, null, null, null, null) == 0
+    # ldg < N
+    assert L.s3r_quantize(C.c_void_p(16), 4, 8, 4, null, null, 0, 0, C.c_void_p(16), C.c_void_p(16), null, null,
+                          null, null) == -3
+    # unknown enum values
+    assert L.rtne_quantize(C.c_void_p(16), 4, 4, 4, null, null, 7, C.c_void_p(16), C.c_void_p(16), null, null) == -1
+    # T not a multiple of S in the correction
+    assert L.s3r_ec_correct(C.c_void_p(16), C.c_void_p(16), 10, 4, 3, null, 0, null, 0, C.c_void_p(16),
+                            C.c_void_p(16), C.c_void_p(16), null, null, null, null, null, 0, null, null) == -3
+    # dW workspace too small
+    assert L.int8_gemm_dw(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 256, 64, 64, null, 0, null, null, null,
+                          null, 256, C.c_void_p(16), C.c_void_p(16), 8, null, null) == -7
+
+
+def test_workspace_sizes_are_host_only(L):
+    assert L.s3r_ffn_workspace_size(256, 128, 384, 128, 1, 2) > 0
+    assert L.s3r_ffn_workspace_size(256, 128, 384, 100, 1, 2) == 0   # T % S != 0
+    assert L.s3r_ffn_workspace_size(8192, 2048, 5632, 2048, 2, 0) > L.s3r_ffn_workspace_size(8192, 2048, 5632, 2048,
+                                                                                             1, 2) - 10 ** 9
+    assert L.int8_gemm_dw_workspace_size(300, 5, 7) >= (5 + 7) * 304
+    assert L.s3r_ec_workspace_size(0, 5) == 0
+
+
+def test_ffn_args_struct_layout_matches_header():
+    """The ctypes mirror of struct s3r_ffn_args has one field per header field."""
+    import re
+    txt = open(s3r.HEADER).read()
+    body = re.search(r"struct s3r_ffn_args \{(.*?)\};", txt, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        names = decl.split()[-1] if "," not in decl else decl
+        for part in re.split(r",", decl):
+            fields.append(re.findall(r"\w+", part)[-1])
+    assert fields == [f for f, _ in s3r._FfnArgs._fields_]

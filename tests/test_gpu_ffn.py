@@ -1,0 +1,213 @@
+"""GPU parity: the SwiGLU FFN block backward.
+
+1. ffn_backward equals the same steps called one by one (bit for bit).
+2. The steps match the oracle's chain.  The first stage (W2) is compared
+   directly.  In the second stage the gate/up gradients come from the fp32
+   dA, whose last bits depend on the summation order, so a code may differ by
+   one step where the oracle's decision was a near tie; the test checks that
+   every such difference is a near tie and adds its exact linear effect
+   (through the correction and both products) before comparing dX, dW1, dW3.
+3. At the full d=2048 / F=5632 / T=8192 size the block's outputs are finite,
+   stage 1 matches the oracle on sampled rows, and every gradient lies within
+   quantization noise of fp64 autograd through the dequantized operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity_util import assert_close_mag, dw_magnitude, dx_magnitude, expand_tiles, near_tie_flips, projection
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def s3r():
+    import stochastic_rounding_int8_gb300 as m
+    m.lib()
+    return m
+
+
+def _staged(s3r, ops, dY, S, rm, ec, seed):
+    """The block backward as separate library calls (same order as ffn_backward)."""
+    T, d = dY.shape
+    F = ops.A8.shape[1]
+    out = {}
+    indep = rm == s3r.ROUND_INDEP
+    ecm = ec if rm == s3r.ROUND_S3R else s3r.EC_NONE
+    if rm == s3r.ROUND_S3R:
+        q2 = s3r.s3r_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2)
+    elif indep:
+        q2 = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2)
+        out["q2r"] = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2 + s3r.RHS_ID_OFFSET)
+    else:
+        Q, sc = s3r.rtne_quantize(dY, s3r.AXIS_TILE, s_x=ops.s_a, s_w=ops.s_w2)
+        q2 = s3r.Quantized(Q, sc)
+    ec2 = s3r.s3r_ec_correct(q2, T, d, S, ops.W2_8, ops.A8, ecm) if ecm else None
+    dA = s3r.int8_gemm_dx(q2.Q, q2.tile_scale, ops.W2_8, ops.s_a, ecm, ec2, S)
+    q2w = out.get("q2r", q2)
+    dW2 = s3r.int8_gemm_dw(ops.A8, q2w.Q, q2w.tile_scale, ops.s_w2, ecm, ec2, S)
+    q1, q3 = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed, s3r.TID_W1, s3r.TID_W3)
+    if indep:
+        out["q1r"], out["q3r"] = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed,
+                                                     s3r.TID_W1 + s3r.RHS_ID_OFFSET, s3r.TID_W3 + s3r.RHS_ID_OFFSET)
+    ec1 = s3r.s3r_ec_correct(q1, T, F, S, ops.W1_8, ops.X8, ecm) if ecm else None
+    ec3 = s3r.s3r_ec_correct(q3, T, F, S, ops.W3_8, ops.X8, ecm) if ecm else None
+    dX = s3r.int8_gemm_dx(q1.Q, q1.tile_scale, ops.W1_8, ops.s_x, ecm, ec1, S)
+    s3r.int8_gemm_dx(q3.Q, q3.tile_scale, ops.W3_8, ops.s_x, ecm, ec3, S, dX=dX, accumulate=True)
+    q1w, q3w = out.get("q1r", q1), out.get("q3r", q3)
+    dW1 = s3r.int8_gemm_dw(ops.X8, q1w.Q, q1w.tile_scale, ops.s_w1, ecm, ec1, S)
+    dW3 = s3r.int8_gemm_dw(ops.X8, q3w.Q, q3w.tile_scale, ops.s_w3, ecm, ec3, S)
+    out.update(q2=q2, dA=dA, dW2=dW2, q1=q1, q3=q3, dX=dX, dW1=dW1, dW3=dW3)
+    return out
+
+
+def _device_ops(s3r, inp):
+    c = lambda t: t.cuda()
+    return s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
+
+
+def _oracle_ops(orc, inp):
+    f = orc.from_torch_bf16
+    return orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
+
+
+MODES = [("S3R", "EC_TWO_WAY"), ("S3R", "EC_DX_ONLY"), ("S3R", "EC_NONE"), ("INDEP", "EC_NONE"), ("RTNE", "EC_NONE")]
+
+
+@pytest.mark.parametrize("mode,ec", MODES)
+def test_ffn_backward_equals_staged_calls(s3r, mode, ec):
+    inp = workloads.ffn_inputs(512, 256, 384, 256, seed=7)
+    ops = _device_ops(s3r, inp)
+    rm, ecm = getattr(s3r, "ROUND_" + mode), getattr(s3r, ec)
+    st = s3r.new_status()
+    g = s3r.ffn_backward(ops, inp.dY.cuda(), 256, rm, ecm, seed=9, status=st)
+    ref = _staged(s3r, ops, inp.dY.cuda(), 256, rm, ecm, seed=9)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for k in ("dX", "dW1", "dW3", "dW2"):
+        assert torch.equal(getattr(g, k), ref[k]), k
+
+
+def _forward_ops_bit_exact(ops_g, ops_o):
+    for name in ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2"):
+        assert np.array_equal(getattr(ops_g, name).cpu().numpy(), getattr(ops_o, name)), name
+
+
+def _flip_effect(D, W8, X8, s_x, s_w, S, ecm, orc):
+    """Exact change of (dX, dW) when the dequantized operand changes by D."""
+    Dx = D - projection(D, S) if ecm in (orc.EC_DX_ONLY, orc.EC_TWO_WAY) else D
+    Dw = D - projection(D, S) if ecm == orc.EC_TWO_WAY else D
+    ddx = (Dx @ W8.astype(np.float64).T) / s_x[:, None].astype(np.float64)
+    ddw = (X8.astype(np.float64).T @ Dw) / s_w[None, :].astype(np.float64)
+    return ddx, ddw
+
+
+def _thresholds(orc, mode, T, N, seed, tid):
+    if mode == "S3R":
+        return np.array([orc.token_threshold(t, seed, tid) for t in range(T)])[:, None]
+    if mode == "INDEP":
+        return np.array([[orc.element_threshold(t * N + n, seed, tid) for n in range(N)] for t in range(T)])
+    return 0.5
+
+
+@pytest.mark.parametrize("mode,ec", MODES)
+def test_ffn_staged_matches_oracle(s3r, orc, mode, ec):
+    T, d, F, S = 256, 128, 384, 128
+    inp = workloads.ffn_inputs(T, d, F, S, seed=11)
+    ops_g = _device_ops(s3r, inp)
+    ops_o = _oracle_ops(orc, inp)
+    _forward_ops_bit_exact(ops_g, ops_o)
+    rm, ecm = getattr(s3r, "ROUND_" + mode), getattr(s3r, ec)
+    seed = 5
+    gpu = _staged(s3r, ops_g, inp.dY.cuda(), S, rm, ecm, seed)
+    torch.cuda.synchronize()
+    h1, h3, dY = (orc.from_torch_bf16(t) for t in (inp.h1, inp.h3, inp.dY))
+    omode, oec = getattr(orc, mode), getattr(orc, ec)
+    ref = orc.ffn_backward(ops_o, h1, h3, dY, S, mode=omode, ec_mode=oec, seed=seed)
+    ecx = oec if omode == orc.S3R else orc.EC_NONE
+    # stage 1: codes exact, dA and dW2 within the fp32 bound
+    assert np.array_equal(gpu["q2"].Q.cpu().numpy(), ref.w2.Q)
+    w2 = ref.w2
+    mdx = dx_magnitude(w2.Q, w2.delta, ops_o.W2_8, ops_o.s_a,
+                       *( (w2.eps, w2.rowsum, w2.v, S) if ecx else (None, None, None, None)))
+    assert_close_mag(gpu["dA"].cpu().numpy(), w2.dX, mdx, "dA")
+    Qw2 = w2.Q_rhs if omode == orc.INDEP else w2.Q
+    dw2 = w2.delta_rhs if omode == orc.INDEP else w2.delta
+    mdw = dw_magnitude(ops_o.A8, Qw2, dw2, ops_o.s_w2,
+                       *((w2.colmean, w2.mu, w2.xsum, w2.p) if ecx == orc.EC_TWO_WAY else (None,) * 4))
+    assert_close_mag(gpu["dW2"].cpu().numpy(), w2.dW, mdw, "dW2")
+    # stage 2: near-tie flips only; their exact effect added to the oracle
+    exp_dX = ref.dX.copy()
+    exp = {"dW1": ref.dW1.copy(), "dW3": ref.dW3.copy()}
+    mags_dx = np.zeros_like(ref.dX)
+    mags = {}
+    for name, lb, dh, W8, s_w, tid in (("dW1", ref.w1, ref.dh1, ops_o.W1_8, ops_o.s_w1, orc.TID_W1),
+                                       ("dW3", ref.w3, ref.dh3, ops_o.W3_8, ops_o.s_w3, orc.TID_W3)):
+        q = gpu["q1" if name == "dW1" else "q3"]
+        Qg, dg = q.Q.cpu().numpy(), q.tile_scale.cpu().numpy()
+        g = (ops_o.s_x[:, None] * dh) * s_w[None, :]
+        amax = np.abs(g).reshape(T // 128, 128, -1, 128).max(axis=(1, 3)) if F % 128 == 0 else None
+        y = g * expand_tiles(np.float32(127.0) / amax, T, F).astype(np.float32)
+        near_tie_flips(Qg, lb.Q, y, _thresholds(orc, mode, T, F, seed, tid))
+        D = expand_tiles(dg, T, F) * Qg - expand_tiles(lb.delta, T, F) * lb.Q
+        ddx, ddw = _flip_effect(D, W8, ops_o.X8, ops_o.s_x, s_w, S, ecx, orc)
+        exp_dX += ddx
+        if omode == orc.INDEP:
+            qr = gpu["q1r" if name == "dW1" else "q3r"]
+            Qr, dr = qr.Q.cpu().numpy(), qr.tile_scale.cpu().numpy()
+            near_tie_flips(Qr, lb.Q_rhs, y, _thresholds(orc, mode, T, F, seed, tid + orc.RHS_ID_OFFSET))
+            Dr = expand_tiles(dr, T, F) * Qr - expand_tiles(lb.delta_rhs, T, F) * lb.Q_rhs
+            _, ddw = _flip_effect(Dr, W8, ops_o.X8, ops_o.s_x, s_w, S, ecx, orc)
+        exp[name] += ddw
+        if ecx:
+            mags_dx += dx_magnitude(lb.Q, lb.delta, W8, ops_o.s_x, lb.eps, lb.rowsum, lb.v, S)
+        else:
+            mags_dx += dx_magnitude(lb.Q, lb.delta, W8, ops_o.s_x)
+        Qw = lb.Q_rhs if omode == orc.INDEP else lb.Q
+        dw_ = lb.delta_rhs if omode == orc.INDEP else lb.delta
+        mags[name] = dw_magnitude(ops_o.X8, Qw, dw_, s_w,
+                                  *((lb.colmean, lb.mu, lb.xsum, lb.p) if ecx == orc.EC_TWO_WAY else (None,) * 4))
+    assert_close_mag(gpu["dX"].cpu().numpy(), exp_dX, mags_dx, "dX")
+    assert_close_mag(gpu["dW1"].cpu().numpy(), exp["dW1"], mags["dW1"], "dW1")
+    assert_close_mag(gpu["dW3"].cpu().numpy(), exp["dW3"], mags["dW3"], "dW3")
+
+
+def test_ffn_full_size_block(s3r, orc):
+    """d=2048, F=5632, T=8192 (4 x 2048), S3R-EC two-way, as the benchmark runs it."""
+    T, d, F, S = 8192, 2048, 5632, 2048
+    inp = workloads.ffn_inputs(T, d, F, S, seed=workloads.DATA_SEED + 1)
+    ops = _device_ops(s3r, inp)
+    st = s3r.new_status()
+    g = s3r.ffn_backward(ops, inp.dY.cuda(), S, s3r.ROUND_S3R, s3r.EC_TWO_WAY, seed=0, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for k in ("dX", "dW1", "dW3", "dW2"):
+        assert torch.isfinite(getattr(g, k)).all(), k
+    # stage 1 exact on sampled rows of dW2 (oracle)
+    A8, s_a = ops.A8.cpu().numpy(), ops.s_a.cpu().numpy()
+    W8, s_w2 = ops.W2_8.cpu().numpy(), ops.s_w2.cpu().numpy()
+    krows = np.array([0, 17, 2900, F - 1])
+    ref = orc.linear_backward(orc.from_torch_bf16(inp.dY), A8, s_a, W8, s_w2, S, mode=orc.S3R,
+                              ec_mode=orc.EC_TWO_WAY, seed=0, tensor_id=orc.TID_W2, rows=np.array([0, T - 1]),
+                              krows=krows)
+    mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w2, ref.colmean, ref.mu, ref.xsum, ref.p, krows=krows)
+    assert_close_mag(g.dW2.cpu().numpy()[krows], ref.dW, mdw, "dW2 rows")
+    # every gradient within quantization noise of fp64 autograd (sampled rows)
+    f64 = lambda q, s, ax: q.double() * s.double().unsqueeze(1 - ax)
+    Xd, Ad = f64(ops.X8.cpu(), ops.s_x.cpu(), 0), f64(ops.A8.cpu(), ops.s_a.cpu(), 0)
+    W1d, W3d = f64(ops.W1_8.cpu(), ops.s_w1.cpu(), 1), f64(ops.W3_8.cpu(), ops.s_w3.cpu(), 1)
+    W2d = f64(ops.W2_8.cpu(), ops.s_w2.cpu(), 1)
+    G = inp.dY.double()
+    dA = G @ W2d.T
+    t1 = inp.h1.double().requires_grad_(True)
+    t3 = inp.h3.double().requires_grad_(True)
+    (torch.nn.functional.silu(t1) * t3).backward(dA)
+    dh1, dh3 = t1.grad, t3.grad
+    rows = torch.arange(0, T, 97)
+    cols = torch.arange(0, F, 89)
+    rel = lambda a, b: float((a - b).norm() / b.norm())
+    assert rel(g.dX.cpu().double()[rows], (dh1[rows] @ W1d.T + dh3[rows] @ W3d.T)) < 0.15
+    assert rel(g.dW2.cpu().double()[cols], (Ad[:, cols].T @ G)) < 0.15
+    assert rel(g.dW1.cpu().double()[:, cols], (Xd.T @ dh1[:, cols])) < 0.15
+    assert rel(g.dW3.cpu().double()[:, cols], (Xd.T @ dh3[:, cols])) < 0.15

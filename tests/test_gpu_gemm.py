@@ -1,0 +1,127 @@
+"""GPU parity: the INT8 backward GEMMs.
+
+The int32 partial of every 128-wide contraction block is bit-exact against
+brute force; the rescaled and corrected fp32 outputs match the fp64 oracle
+within the fp32 bound.  Includes the full-size activation- and weight-gradient
+GEMMs of the d=2048 / F=5632 / T=8192 FFN block on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity_util import assert_close_mag, dw_magnitude, dx_magnitude
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def s3r():
+    import stochastic_rounding_int8_gb300 as m
+    m.lib()
+    return m
+
+
+def _i8(rng, *shape):
+    return rng.integers(-127, 128, size=shape).astype(np.int8)
+
+
+@pytest.mark.parametrize("T,N,K", [(256, 1024, 512), (130, 136, 70), (1, 16, 1), (300, 384, 257), (64, 1000, 33)])
+def test_dx_blocks_bit_exact(s3r, orc, T, N, K):
+    rng = np.random.default_rng(T * N + K)
+    Q, W8 = _i8(rng, T, N), _i8(rng, K, N)
+    got = s3r.debug_dx_blocks(torch.from_numpy(Q).cuda(), torch.from_numpy(W8).cuda()).cpu().numpy()
+    ref = orc.dx_blocks(Q, W8, np.arange(T))
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("T,K,N", [(256, 512, 1024), (130, 70, 136), (1, 1, 16), (300, 257, 384), (1000, 33, 64)])
+def test_dw_blocks_bit_exact(s3r, orc, T, K, N):
+    rng = np.random.default_rng(T + 3 * N + K)
+    X8, Q = _i8(rng, T, K), _i8(rng, T, N)
+    got = s3r.debug_dw_blocks(torch.from_numpy(X8).cuda(), torch.from_numpy(Q).cuda()).cpu().numpy()
+    ref = orc.dw_blocks(X8, Q, np.arange(K))
+    assert np.array_equal(got, ref)
+
+
+def _linear(orc, T, K, N, S, seed):
+    inp = workloads.linear_inputs(T, K, N, S, seed=seed)
+    X, W, G = (orc.from_torch_bf16(t) for t in (inp.X, inp.W, inp.dY))
+    X8, s_x = orc.rtne_operand(X, 0)
+    W8, s_w = orc.rtne_operand(W, 1)
+    return inp, G, X8, s_x, W8, s_w
+
+
+@pytest.mark.parametrize("ec_name", ["EC_NONE", "EC_DX_ONLY", "EC_TWO_WAY"])
+@pytest.mark.parametrize("T,K,N,S", [(256, 512, 1024, 256), (512, 200, 384, 128), (300, 136, 260, 300)])
+def test_linear_backward_parity(s3r, orc, ec_name, T, K, N, S):
+    """dX and dW of one linear layer (the tiny-linear workload and ragged
+    variants) through quantize -> correction -> both GEMMs."""
+    inp, G, X8, s_x, W8, s_w = _linear(orc, T, K, N, S, seed=T + K + N)
+    ec_mode = getattr(orc, ec_name)
+    ref = orc.linear_backward(G, X8, s_x, W8, s_w, S, mode=orc.S3R, ec_mode=ec_mode, seed=11, tensor_id=0)
+    c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q = s3r.s3r_quantize(inp.dY.cuda(), c(s_x), c(s_w), seed=11, tensor_id=0)
+    ec = s3r.s3r_ec_correct(q, T, N, S, c(W8), c(X8), ec_mode=ec_mode) if ec_mode else None
+    dX = s3r.int8_gemm_dx(q.Q, q.tile_scale, c(W8), c(s_x), ec_mode, ec, S)
+    dW = s3r.int8_gemm_dw(c(X8), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.Q.cpu().numpy(), ref.Q)
+    if ec_mode:
+        mdx = dx_magnitude(ref.Q, ref.delta, W8, s_x, ref.eps, ref.rowsum, ref.v, S)
+    else:
+        mdx = dx_magnitude(ref.Q, ref.delta, W8, s_x)
+    assert_close_mag(dX.cpu().numpy(), ref.dX, mdx, "dX")
+    if ec_mode == orc.EC_TWO_WAY:
+        mdw = dw_magnitude(X8, ref.Q, ref.delta, s_w, ref.colmean, ref.mu, ref.xsum, ref.p)
+    else:
+        mdw = dw_magnitude(X8, ref.Q, ref.delta, s_w)
+    assert_close_mag(dW.cpu().numpy(), ref.dW, mdw, "dW")
+
+
+def test_dx_accumulate(s3r, orc):
+    rng = np.random.default_rng(1)
+    T, N, K = 256, 256, 128
+    Q, W8 = _i8(rng, T, N), _i8(rng, K, N)
+    sc = (rng.random((2, 2)) + 0.5).astype(np.float32)
+    c = lambda a: torch.from_numpy(a).cuda()
+    base = torch.randn(T, K, device="cuda")
+    out = base.clone()
+    s3r.int8_gemm_dx(c(Q), c(sc), c(W8), dX=out, accumulate=True)
+    fresh = s3r.int8_gemm_dx(c(Q), c(sc), c(W8))
+    torch.cuda.synchronize()
+    assert torch.allclose(out, base + fresh, rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("ec_name", ["EC_DX_ONLY", "EC_TWO_WAY"])
+def test_ffn_w2_gemms_full_size_sampled(s3r, orc, ec_name):
+    """The W2 linear of the d=2048, F=5632, T=8192 (4 x 2048) SwiGLU block at
+    full size: dA = dX of W2 [8192, 5632] and dW2 [5632, 2048] in the launch
+    configuration the benchmark times, checked on 48 sampled rows each."""
+    T, d, F, S = 8192, 2048, 5632, 2048
+    inp = workloads.ffn_inputs(T, d, F, S, seed=workloads.DATA_SEED + 1)
+    A = orc.from_torch_bf16(inp.a)
+    W2 = orc.from_torch_bf16(inp.W2)
+    G = orc.from_torch_bf16(inp.dY)
+    A8, s_a = orc.rtne_operand(A, 0)
+    W8, s_w = orc.rtne_operand(W2, 1)
+    ec_mode = getattr(orc, ec_name)
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([[0, T - 1], rng.choice(T, 46, replace=False)]))
+    krows = np.sort(np.concatenate([[0, F - 1], rng.choice(F, 46, replace=False)]))
+    ref = orc.linear_backward(G, A8, s_a, W8, s_w, S, mode=orc.S3R, ec_mode=ec_mode, seed=0, tensor_id=0,
+                              rows=rows, krows=krows)
+    c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q = s3r.s3r_quantize(inp.dY.cuda(), c(s_a), c(s_w), seed=0, tensor_id=0)
+    ec = s3r.s3r_ec_correct(q, T, d, S, c(W8), c(A8), ec_mode=ec_mode)
+    dA = s3r.int8_gemm_dx(q.Q, q.tile_scale, c(W8), c(s_a), ec_mode, ec, S)
+    dW = s3r.int8_gemm_dw(c(A8), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.Q.cpu().numpy(), ref.Q)
+    mdx = dx_magnitude(ref.Q, ref.delta, W8, s_a, ref.eps, ref.rowsum, ref.v, S, rows=rows)
+    assert_close_mag(dA.cpu().numpy()[rows], ref.dX, mdx, "dA rows")
+    if ec_mode == orc.EC_TWO_WAY:
+        mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w, ref.colmean, ref.mu, ref.xsum, ref.p, krows=krows)
+    else:
+        mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w, krows=krows)
+    assert_close_mag(dW.cpu().numpy()[krows], ref.dW, mdw, "dW2 rows")

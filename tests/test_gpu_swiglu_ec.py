@@ -1,0 +1,81 @@
+"""GPU parity: the SwiGLU-fused quantizer and the S3R-EC correction factors."""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import assert_close_mag
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def s3r():
+    import stochastic_rounding_int8_gb300 as m
+    m.lib()
+    return m
+
+
+def _swiglu_case(T, F, seed):
+    rng = np.random.default_rng(seed)
+    dA = (rng.standard_normal((T, F)) * 3e-4).astype(np.float32)
+    h1 = torch.from_numpy((rng.standard_normal((T, F)) * 0.9).astype(np.float32)).to(torch.bfloat16)
+    h3 = torch.from_numpy((rng.standard_normal((T, F)) * 0.9).astype(np.float32)).to(torch.bfloat16)
+    s_x = (rng.random(T) * 0.03 + 0.02).astype(np.float32)
+    s_w1 = (rng.random(F) * 5e-4 + 1e-4).astype(np.float32)
+    s_w3 = (rng.random(F) * 5e-4 + 1e-4).astype(np.float32)
+    return dA, h1, h3, s_x, s_w1, s_w3
+
+
+@pytest.mark.parametrize("mode", ["S3R", "INDEP", "RTNE"])
+@pytest.mark.parametrize("T,F", [(256, 384), (300, 200), (129, 1000), (64, 8)])
+def test_swiglu_quantize_parity(s3r, orc, mode, T, F):
+    dA, h1, h3, s_x, s_w1, s_w3 = _swiglu_case(T, F, T + F)
+    c = lambda a: torch.from_numpy(a).cuda()
+    o1, o3 = s3r.swiglu_quantize(c(dA), h1.cuda(), h3.cuda(), c(s_x), c(s_w1), c(s_w3),
+                                 round_mode=getattr(s3r, "ROUND_" + mode), seed=42, tid1=1, tid3=2)
+    torch.cuda.synchronize()
+    dh1, dh3 = orc.swiglu_bwd(dA, orc.from_torch_bf16(h1), orc.from_torch_bf16(h3))
+    for o, g, s_w, tid in ((o1, dh1, s_w1, 1), (o3, dh3, s_w3, 2)):
+        Qo, do, Eo, st = orc.quantize(g, s_x, s_w, mode=getattr(orc, mode), seed=42, tensor_id=tid)
+        assert st == 0
+        Qg = o.Q.cpu().numpy()
+        assert np.array_equal(Qg, Qo), f"{mode} tid {tid}: {(Qg != Qo).sum()} codes differ"
+        assert np.array_equal(o.tile_scale.cpu().numpy(), do)
+        if mode == "S3R":
+            t_o, c_o = orc.error_partials(Eo)
+            t_m, c_m = orc.error_partials(np.abs(Eo))
+            assert_close_mag(o.tok_err_part.cpu().numpy(), t_o, t_m, "tok")
+            assert_close_mag(o.col_err_part.cpu().numpy(), c_o, c_m, "col")
+
+
+@pytest.mark.parametrize("ec_mode", ["EC_DX_ONLY", "EC_TWO_WAY"])
+@pytest.mark.parametrize("T,N,K,S", [(256, 1024, 512, 256), (512, 384, 200, 128), (300, 260, 72, 300),
+                                     (1024, 256, 130, 256)])
+def test_ec_factors_parity(s3r, orc, ec_mode, T, N, K, S):
+    rng = np.random.default_rng(T + N + K)
+    G = (rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)
+    Gb = torch.from_numpy(G).to(torch.bfloat16)
+    W8 = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
+    X8 = rng.integers(-127, 128, size=(T, K)).astype(np.int8)
+    q = s3r.s3r_quantize(Gb.cuda(), seed=3, tensor_id=9)
+    ec = s3r.s3r_ec_correct(q, T, N, S, torch.from_numpy(W8).cuda(), torch.from_numpy(X8).cuda(),
+                            ec_mode=getattr(s3r, ec_mode))
+    torch.cuda.synchronize()
+    Qo, do, Eo, _ = orc.quantize(orc.from_torch_bf16(Gb), seed=3, tensor_id=9)
+    eps, colmean, mu = orc.error_stats(Eo, S)
+    rowsum, v, xsum, p = orc.ec_factors(eps, colmean, mu, S, W8, X8)
+    B = T // S
+    absE = np.abs(Eo).astype(np.float64)
+    eps_m = absE.sum(1) / N
+    cm_m = absE.reshape(B, S, N).sum(1) / S
+    mu_m = absE.reshape(B, -1).sum(1) / (S * N)
+    assert_close_mag(ec.eps.cpu().numpy(), eps, eps_m, "eps")
+    assert_close_mag(ec.colmean.cpu().numpy(), colmean, cm_m, "colmean")
+    assert_close_mag(ec.mu.cpu().numpy(), mu, mu_m, "mu")
+    assert np.array_equal(ec.rowsum.cpu().numpy(), rowsum)
+    v_m = (np.abs(colmean) + np.abs(mu)[:, None]) @ np.abs(W8.astype(np.float64)).T
+    assert_close_mag(ec.v.cpu().numpy(), v, v_m + cm_m @ np.abs(W8.astype(np.float64)).T, "v")
+    if ec_mode == "EC_TWO_WAY":
+        assert np.array_equal(ec.xsum.cpu().numpy(), xsum)
+        p_m = np.abs(X8.astype(np.float64)).T @ (np.abs(eps) + eps_m)
+        assert_close_mag(ec.p.cpu().numpy(), p, p_m, "p")

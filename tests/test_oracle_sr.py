@@ -254,3 +254,18 @@ def test_rtne_operand_scales(orc):
     B = np.array([[127.0, 2.5, -3.5, 0.5]], dtype=np.float32)
     Qb, sb = orc.rtne_operand(B, 0)
     assert sb[0] == 1.0 and Qb.tolist() == [[127, 2, -4, 0]]
+
+
+def test_window_equals_slice_of_full(orc):
+    """Quantizing a tile-aligned window with global indices reproduces the
+    corresponding slice of the whole tensor's quantization (used by the
+    sampled full-size parity tests)."""
+    rng = np.random.default_rng(13)
+    T, N = 384, 300
+    G = (rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)
+    for mode in (orc.S3R, orc.INDEP, orc.RTNE):
+        Q, delta, E, _ = orc.quantize(G, mode=mode, seed=21, tensor_id=4)
+        Qw, dw, Ew, _ = orc.quantize(G[128:256, 128:300], mode=mode, seed=21, tensor_id=4, window=(128, 128, N))
+        assert np.array_equal(Qw, Q[128:256, 128:300])
+        assert np.array_equal(dw, delta[1:2, 1:3])
+        assert np.array_equal(Ew, E[128:256, 128:300])
