@@ -131,4 +131,9 @@ def test_zero_tile(s3r):
     sc = o.tile_scale.cpu()
     assert sc[0, 0] == 0 and sc[1, 2] == np.float32(1.0) / np.float32(127.0)
     assert int(o.Q[150, 290]) == 127 and int(o.Q.abs().sum()) == 127
-    assert float(o.tok_err_part.abs().sum()) == 0.0
+    tok = o.tok_err_part.cpu().numpy()
+    # all-zero tiles carry no error; the lone element's error is Delta*127 - 1 (Delta is rounded)
+    want = np.float32(np.float32(1.0) / np.float32(127.0)) * np.float64(127.0) - 1.0
+    assert tok[150, 2] == np.float32(want)
+    tok[150, 2] = 0.0
+    assert not tok.any() and float(o.col_err_part.cpu()[0].abs().sum()) == 0.0
