@@ -148,17 +148,20 @@ def peaks():
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def device_setup(s3r, rank):
+def device_setup(s3r, rank, code_format=None):
     inp = workloads.ffn_inputs(T, D, F, S, seed=workloads.DATA_SEED + 1 + 1000 * rank)
     c = lambda t: t.cuda()
-    ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
+    cf = s3r.DEFAULT_CODES if code_format is None else code_format
+    ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3),
+                                   code_format=cf)
     torch.cuda.synchronize()
     return inp, ops
 
 
 def time_ffn(s3r, ops, dY, steps, warmup, rm, ec, world, events=False):
     """Device time of `steps` ffn_backward calls on resident inputs."""
-    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S, rm, ec), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S, rm, ec, s3r.code_format_of(ops.X8)), dtype=torch.uint8,
+                     device="cuda")
     grads = s3r.alloc_ffn_grads(T, D, F)
     st = s3r.new_status()
     for i in range(warmup):
@@ -201,7 +204,8 @@ def time_e2e(s3r, inp, ops, steps, warmup, world):
     grads = s3r.alloc_ffn_grads(T, D, F)
     host_out = {k: torch.empty(getattr(grads, k).shape, dtype=torch.float32).pin_memory()
                 for k in ("dX", "dW1", "dW3", "dW2")}
-    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S, code_format=s3r.code_format_of(ops.X8)), dtype=torch.uint8,
+                     device="cuda")
     bi = sum(v.numel() * v.element_size() for v in host_in.values())
     bo = sum(v.numel() * v.element_size() for v in host_out.values())
 
@@ -256,15 +260,20 @@ def time_bf16_backward(inp, steps, warmup):
 
 
 def time_quantize_sweep(s3r, steps=20):
-    """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100 outliers."""
+    """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100
+    outliers; int8 codes (1 B) and fp16-carried codes (2 B)."""
     Tq, Nq = 16384, 8192
     G = workloads.quantize_sweep_input(Tq, Nq, seed=workloads.DATA_SEED + 3).cuda()
     out = {}
-    q = s3r.s3r_quantize(G)
-    qi = s3r.indep_sr_quantize(G)
-    Qr, sr = s3r.rtne_quantize(G)
+    S8, F16 = s3r.CODES_S8, s3r.CODES_F16
+    q8 = s3r.s3r_quantize(G, code_format=S8)
+    q16 = s3r.s3r_quantize(G, code_format=F16)
+    qi = s3r.indep_sr_quantize(G, code_format=S8)
+    Qr, sr = s3r.rtne_quantize(G, code_format=S8)
+    part = 8 / 128   # the two fp32 error partials per 128 elements
     runs = {
-        "s3r": (lambda i: s3r.s3r_quantize(G, seed=i, out=q), 2 + 1 + 8 / 128),
+        "s3r": (lambda i: s3r.s3r_quantize(G, seed=i, out=q8), 2 + 1 + part),
+        "s3r_f16_codes": (lambda i: s3r.s3r_quantize(G, seed=i, out=q16), 2 + 2 + part),
         "indep_sr_one_copy": (lambda i: s3r.indep_sr_quantize(G, seed=i, out=qi), 3.0),
         "rtne": (lambda i: s3r.rtne_quantize(G, Q=Qr, scale=sr), 3.0),
     }
@@ -343,6 +352,7 @@ def run_ours(args, world, rank, local):
                                                   "block workload)",
         "config": {"workload": WORKLOAD, "T": T, "d": D, "F": F, "examples": T // S, "seq": S,
                    "rounding": "S3R Phi_2D", "ec": "two-way", "tile": 128,
+                   "codes": "int8 values carried in fp16 (tcgen05 kind::f16, fp32 accumulate per 128-K block)",
                    "l2": "working set ~1 GB > 129 MB L2 (no flush needed)", "parallelism": f"replica x{world}"},
         "clocks": clk,
         "gpu_launches": int(launches),
@@ -360,12 +370,16 @@ def run_ours(args, world, rank, local):
                              ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE)):
             m, _, _, _ = time_ffn(s3r, ops, dY, 10, 2, rm, ec, 1)
             ctx[name] = {"tokens_s": round(T * 10 / (m * 1e-3), 1), "ms": round(m / 10, 4)}
+        _, ops8 = device_setup(s3r, rank, s3r.CODES_S8)
+        m, _, _, _ = time_ffn(s3r, ops8, dY, 5, 1, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1)
+        ctx["s3r_ec_two_way_int8_storage_mma_sync"] = {"tokens_s": round(T * 5 / (m * 1e-3), 1), "ms": round(m / 5, 4)}
+        del ops8
         bms = time_bf16_backward(inp, 10, 3)
         ctx["bf16_cublas_backward"] = {"tokens_s": round(T / (bms * 1e-3), 1), "ms": round(bms, 4)}
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / ms_step, 3)
         ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / ms_step, 3)
         qs = time_quantize_sweep(s3r)
-        for k in ("s3r", "indep_sr_one_copy", "rtne"):
+        for k in ("s3r", "s3r_f16_codes", "indep_sr_one_copy", "rtne"):
             qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
         ctx["quantize_sweep"] = qs
         line["context"] = ctx

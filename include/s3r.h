@@ -75,6 +75,17 @@ enum s3r_round_mode {
     S3R_ROUND_INDEP = 2  /* one threshold per element (conventional SR) */
 };
 
+/* Storage of the integer codes (values in [-127, 127]).  S8 is one byte per
+ * code.  F16 stores the same integer exactly in an IEEE half: sm_103a has no
+ * integer tcgen05 MMA and its warp-level s8 MMA runs far below the 16-bit
+ * tensor rate, so F16 is the operand format of the tensor-core GEMMs here
+ * (TMA straight into the MMA's shared-memory layout, no conversion pass).
+ * Both products of one layer must use the same format. */
+enum s3r_code_format {
+    S3R_CODES_S8 = 0,   /* int8_t [rows, cols] */
+    S3R_CODES_F16 = 1   /* IEEE fp16 [rows, cols], integer valued; cols % 8 == 0 for the GEMMs */
+};
+
 /* Scale granularity of rtne_quantize. */
 enum s3r_scale_axis {
     S3R_AXIS_ROW = 0,  /* one scale per row:    A ~= diag(s) A_hat (per-token s_x) */
@@ -107,7 +118,7 @@ uint64_t s3r_kernel_launch_count(void);
  *   e    = fma(tile_scale, q, -g)         the rounding error E = Delta Q - G'
  *
  * In : G [T, N] bf16 (row stride ldg >= N); s_x [T] or NULL; s_w [N] or NULL.
- * Out: Q [T, N] int8 (row stride N); tile_scale [ceil(T/128), ceil(N/128)];
+ * Out: Q [T, N] codes in `code_format` (row stride N); tile_scale [ceil(T/128), ceil(N/128)];
  *      tok_err_part [T, ceil(N/128)]  sum of e over each tile's columns, per token;
  *      col_err_part [ceil(T/128), N]  sum of e over each tile's rows, per channel.
  *      Both partial arrays may be NULL (then they are not written).
@@ -115,8 +126,8 @@ uint64_t s3r_kernel_launch_count(void);
  * sets *d_status = S3R_ERR_NONFINITE.
  */
 int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
-                 uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale, float* tok_err_part,
-                 float* col_err_part, int* d_status, cudaStream_t stream);
+                 uint64_t seed, uint32_t tensor_id, void* Q, int code_format, float* tile_scale,
+                 float* tok_err_part, float* col_err_part, int* d_status, cudaStream_t stream);
 
 /*
  * indep_sr_quantize -- conventional stochastic rounding with an independent
@@ -128,21 +139,21 @@ int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* 
  * tensor_id).  Call it twice with two tensor ids for the two products.
  */
 int indep_sr_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
-                      uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale, int* d_status,
-                      cudaStream_t stream);
+                      uint64_t seed, uint32_t tensor_id, void* Q, int code_format, float* tile_scale,
+                      int* d_status, cudaStream_t stream);
 
 /*
  * rtne_quantize -- round to nearest even ([S3R] §III-A forward operands;
  * §IV-B "INT8 RTNE").  q = clamp(rint(a * (127 / amax)), -127, 127) with
  * amax taken per row, per column or per 128x128 tile of the folded input
  * a = (s_x[r] * A[r,c]) * s_w[c] (NULL scale = 1).
- * Out: Q [R, C] int8 (row stride C); scale = amax / 127 per row [R], per
+ * Out: Q [R, C] codes in `code_format` (row stride C); scale = amax / 127 per row [R], per
  * column [C] or per tile [ceil(R/128), ceil(C/128)].  For ROW and COL an
  * all-zero row/column gets scale 1 (any scale reproduces zero; 1 keeps the
  * backward fold finite); for TILE an all-zero tile gets scale 0.
  */
 int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, const float* s_x, const float* s_w,
-                  int scale_axis, int8_t* Q, float* scale, int* d_status, cudaStream_t stream);
+                  int scale_axis, void* Q, int code_format, float* scale, int* d_status, cudaStream_t stream);
 
 /*
  * swiglu_quantize -- the SwiGLU backward glue fused into the quantization of
@@ -156,13 +167,13 @@ int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, const float*
  * (fold with s_x [T] and s_w1 / s_w3 [F]), with `round_mode` choosing S3R,
  * independent SR or RTNE and tensor ids tid1 / tid3.
  * In : dA [T, F] fp32 (row stride ldd); h1, h3 [T, F] bf16 (row stride ldh).
- * Out: Q1, Q3 [T, F] int8; scale1, scale3 tile scales; tok1/col1/tok3/col3
+ * Out: Q1, Q3 [T, F] codes in `code_format`; scale1, scale3 tile scales; tok1/col1/tok3/col3
  *      error partials as in s3r_quantize (NULL allowed).
  */
 int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh, int64_t T,
                     int64_t F, const float* s_x, const float* s_w1, const float* s_w3, int round_mode,
-                    uint64_t seed, uint32_t tid1, uint32_t tid3, int8_t* Q1, float* scale1, float* tok1,
-                    float* col1, int8_t* Q3, float* scale3, float* tok3, float* col3, int* d_status,
+                    int code_format, uint64_t seed, uint32_t tid1, uint32_t tid3, void* Q1, float* scale1,
+                    float* tok1, float* col1, void* Q3, float* scale3, float* tok3, float* col3, int* d_status,
                     cudaStream_t stream);
 
 /*
@@ -179,8 +190,8 @@ int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3
  * and for S3R_EC_TWO_WAY also
  *   xsum[b,k]     = sum_{t in b} X8[t,k]
  *   p[k]          = sum_t X8[t,k] eps[t].
- * In : the partial sums from s3r_quantize; W8 [K, N] int8; X8 [T, K] int8
- *      (two-way only, else may be NULL).  Requires T % S == 0 and either
+ * In : the partial sums from s3r_quantize; W8 [K, N] and X8 [T, K] codes in
+ *      `code_format` (X8 two-way only, else may be NULL).  Requires T % S == 0 and either
  *      S % 128 == 0 or S == T.
  * Out: eps [T], mu [B], colmean [B, N], rowsum [K] int32, v [B, K];
  *      two-way: xsum [B, K] int32, p [K].
@@ -188,7 +199,7 @@ int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3
  */
 size_t s3r_ec_workspace_size(int64_t T, int64_t K);
 int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
-                   const int8_t* W8, int64_t K, const int8_t* X8, int ec_mode, float* eps, float* mu,
+                   const void* W8, int64_t K, const void* X8, int code_format, int ec_mode, float* eps, float* mu,
                    float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p, void* workspace,
                    size_t workspace_bytes, int* d_status, cudaStream_t stream);
 
@@ -199,14 +210,16 @@ int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t
  *   dX[t,k]  = (acc - eps[t]*rowsum[k] - v[t/S, k]) / s_x[t]     (EC modes 1, 2)
  *   dX[t,k]  = acc / s_x[t]                                      (EC mode 0)
  * (plus the old dX[t,k] when accumulate != 0).  Each 128-wide block is an
- * exact integer; blocks are combined in fp32.
- * In : Q [T, N] int8; tile_scale from the quantizer; W8 [K, N] int8 (the
+ * exact integer; blocks are combined in fp32.  S3R_CODES_F16 runs on tcgen05
+ * (kind::f16, fp32 accumulator drained per block; needs N % 8 == 0);
+ * S3R_CODES_S8 runs on the warp-level s8 mma.sync path.
+ * In : Q [T, N] codes; tile_scale from the quantizer; W8 [K, N] codes (the
  *      forward weight's codes, W [K, N] ~= W8 diag(s_w)); s_x [T] or NULL;
  *      eps, rowsum, v from s3r_ec_correct (unused when ec_mode = 0).
  * Out: dX [T, K] fp32 (row stride K).
  */
-int int8_gemm_dx(const int8_t* Q, const float* tile_scale, const int8_t* W8, int64_t T, int64_t N, int64_t K,
-                 const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum, const float* v,
+int int8_gemm_dx(const void* Q, const float* tile_scale, const void* W8, int code_format, int64_t T, int64_t N,
+                 int64_t K, const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum, const float* v,
                  int64_t S, float* dX, int accumulate, int* d_status, cudaStream_t stream);
 
 /*
@@ -215,18 +228,20 @@ int int8_gemm_dx(const int8_t* Q, const float* tile_scale, const int8_t* W8, int
  *   acc[k,n] = sum_tb tile_scale[tb, n/128] * (int32) sum_{t in block tb} X8[t,k] Q[t,n]
  *   dW[k,n]  = (acc - sum_b xsum[b,k]*(colmean[b,n] - mu[b]) - p[k]) / s_w[n]  (EC mode 2)
  *   dW[k,n]  = acc / s_w[n]                                                   (EC modes 0, 1)
- * dW is the sum X^T G (not divided by the token count).
- * In : X8 [T, K] int8 (the forward input's codes); Q [T, N] int8; tile_scale;
+ * dW is the sum X^T G (not divided by the token count).  S3R_CODES_F16 runs
+ * on tcgen05 reading both operands MN-major (needs K % 8 == 0, N % 8 == 0);
+ * S3R_CODES_S8 transposes both operands into the workspace first.
+ * In : X8 [T, K] codes (the forward input's); Q [T, N] codes; tile_scale;
  *      s_w [N] or NULL; colmean, mu, xsum, p from s3r_ec_correct (mode 2).
  * Out: dW [K, N] fp32 (row stride N).
- * workspace: int8_gemm_dw_workspace_size(T, K, N) bytes (0 allowed when it
- * returns 0).
+ * workspace: int8_gemm_dw_workspace_size(T, K, N, code_format) bytes (may be
+ * NULL when that is 0).
  */
-size_t int8_gemm_dw_workspace_size(int64_t T, int64_t K, int64_t N);
-int int8_gemm_dw(const int8_t* X8, const int8_t* Q, const float* tile_scale, int64_t T, int64_t K, int64_t N,
-                 const float* s_w, int ec_mode, const float* colmean, const float* mu, const int32_t* xsum,
-                 const float* p, int64_t S, float* dW, void* workspace, size_t workspace_bytes, int* d_status,
-                 cudaStream_t stream);
+size_t int8_gemm_dw_workspace_size(int64_t T, int64_t K, int64_t N, int code_format);
+int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int code_format, int64_t T, int64_t K,
+                 int64_t N, const float* s_w, int ec_mode, const float* colmean, const float* mu,
+                 const int32_t* xsum, const float* p, int64_t S, float* dW, void* workspace, size_t workspace_bytes,
+                 int* d_status, cudaStream_t stream);
 
 /*
  * ffn_backward -- the whole SwiGLU FFN block backward (FFN block of [S3R]
@@ -249,18 +264,19 @@ struct s3r_ffn_args {
     const void* dY;              /* bf16 [T, d] upstream gradient */
     const void* h1;              /* bf16 [T, F] gate pre-activation X W1 */
     const void* h3;              /* bf16 [T, F] up pre-activation X W3 */
-    const int8_t* X8;            /* [T, d] RTNE codes of X, per-token scale s_x [T] */
+    const void* X8;              /* [T, d] RTNE codes of X, per-token scale s_x [T] */
     const float* s_x;
-    const int8_t* A8;            /* [T, F] RTNE codes of a = silu(h1)*h3, per-token scale s_a [T] */
+    const void* A8;              /* [T, F] RTNE codes of a = silu(h1)*h3, per-token scale s_a [T] */
     const float* s_a;
-    const int8_t* W1_8;          /* [d, F] codes of W1, per-column scale s_w1 [F] */
+    const void* W1_8;            /* [d, F] codes of W1, per-column scale s_w1 [F] */
     const float* s_w1;
-    const int8_t* W3_8;          /* [d, F] codes of W3, per-column scale s_w3 [F] */
+    const void* W3_8;            /* [d, F] codes of W3, per-column scale s_w3 [F] */
     const float* s_w3;
-    const int8_t* W2_8;          /* [F, d] codes of W2, per-column scale s_w2 [d] */
+    const void* W2_8;            /* [F, d] codes of W2, per-column scale s_w2 [d] */
     const float* s_w2;
     int round_mode;              /* enum s3r_round_mode */
     int ec_mode;                 /* enum s3r_ec_mode (S3R only) */
+    int code_format;             /* enum s3r_code_format of the forward codes and of Q1, Q2, Q3 */
     uint64_t seed;
     float* dX;                   /* out [T, d] fp32 */
     float* dW1;                  /* out [d, F] fp32 */
@@ -274,7 +290,8 @@ struct s3r_ffn_args {
                                     after steps 1, 2, 3, 4, 5, 6, 7, 8 above (for timing) */
 };
 #define S3R_FFN_NUM_EVENTS 9
-size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode);
+size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
+                              int code_format);
 int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
 
 /*
@@ -283,10 +300,10 @@ int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
  * rescale.  out_dx [T, K, ceil(N/128)]: block kb of sum_n Q[t,n] W8[k,n];
  * out_dw [K, N, ceil(T/128)]: block tb of sum_t X8[t,k] Q[t,n].  int32.
  */
-int s3r_debug_dx_blocks(const int8_t* Q, const int8_t* W8, int64_t T, int64_t N, int64_t K, int32_t* out_dx,
-                        cudaStream_t stream);
-int s3r_debug_dw_blocks(const int8_t* X8, const int8_t* Q, int64_t T, int64_t K, int64_t N, int32_t* out_dw,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int s3r_debug_dx_blocks(const void* Q, const void* W8, int code_format, int64_t T, int64_t N, int64_t K,
+                        int32_t* out_dx, cudaStream_t stream);
+int s3r_debug_dw_blocks(const void* X8, const void* Q, int code_format, int64_t T, int64_t K, int64_t N,
+                        int32_t* out_dw, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -12,7 +12,9 @@ semantics, layouts and citations):
     s3r_ec_correct, int8_gemm_dx, int8_gemm_dw, ffn_backward
 
 Outputs may be passed in (then they are written in place) or are allocated
-with torch on the inputs' device.
+with torch on the inputs' device.  Codes are int8 tensors (S3R_CODES_S8) or
+float16 tensors holding the same integers (S3R_CODES_F16, the operand format
+of the tcgen05 GEMMs); the format follows the tensors' dtype.
 """
 from __future__ import annotations
 
@@ -33,6 +35,9 @@ ROUND_RTNE, ROUND_S3R, ROUND_INDEP = 0, 1, 2
 EC_NONE, EC_DX_ONLY, EC_TWO_WAY = 0, 1, 2
 AXIS_ROW, AXIS_COL, AXIS_TILE = 0, 1, 2
 TID_W2, TID_W1, TID_W3, RHS_ID_OFFSET = 0, 1, 2, 0x100
+CODES_S8, CODES_F16 = 0, 1
+DEFAULT_CODES = CODES_F16
+_CODE_DTYPE = {CODES_S8: torch.int8, CODES_F16: torch.float16}
 
 _lib = None
 
@@ -42,22 +47,23 @@ _SIGS = {
     "s3r_status_string": (C.c_char_p, [_INT]),
     "s3r_abi_version": (_INT, []),
     "s3r_kernel_launch_count": (C.c_uint64, []),
-    "s3r_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "indep_sr_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _VP, _VP, _VP]),
-    "rtne_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _VP, _VP, _VP]),
-    "swiglu_quantize": (_INT, [_VP, _I64, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _INT, _U64, _U32, _U32,
+    "s3r_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _INT, _VP, _VP, _VP, _VP, _VP]),
+    "indep_sr_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _INT, _VP, _VP, _VP]),
+    "rtne_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _INT, _VP, _VP, _VP]),
+    "swiglu_quantize": (_INT, [_VP, _I64, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _INT, _INT, _U64, _U32, _U32,
                                _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "s3r_ec_workspace_size": (_SZ, [_I64, _I64]),
-    "s3r_ec_correct": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
-                              _VP, _SZ, _VP, _VP]),
-    "int8_gemm_dx": (_INT, [_VP, _VP, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _I64, _VP, _INT, _VP, _VP]),
-    "int8_gemm_dw_workspace_size": (_SZ, [_I64, _I64, _I64]),
-    "int8_gemm_dw": (_INT, [_VP, _VP, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP, _VP, _SZ,
-                            _VP, _VP]),
-    "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT]),
+    "s3r_ec_correct": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _I64, _VP, _INT, _INT, _VP, _VP, _VP, _VP, _VP, _VP,
+                              _VP, _VP, _SZ, _VP, _VP]),
+    "int8_gemm_dx": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _I64, _VP, _INT, _VP,
+                            _VP]),
+    "int8_gemm_dw_workspace_size": (_SZ, [_I64, _I64, _I64, _INT]),
+    "int8_gemm_dw": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP, _VP,
+                            _SZ, _VP, _VP]),
+    "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
-    "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP]),
-    "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
+    "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP]),
+    "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
 }
 
 
@@ -134,6 +140,22 @@ def _bits(t):
     return t
 
 
+def code_format_of(t) -> int:
+    """S3R_CODES_* of a code tensor, from its dtype."""
+    if t.dtype == torch.int8:
+        return CODES_S8
+    if t.dtype == torch.float16:
+        return CODES_F16
+    raise S3RError(f"codes must be int8 or float16, got {t.dtype}")
+
+
+def _fmt2(a, b) -> int:
+    fa, fb = code_format_of(a), code_format_of(b)
+    if fa != fb:
+        raise S3RError("both operands of a product must use the same code format")
+    return fa
+
+
 # ---------------------------------------------------------------------------
 # quantizers
 # ---------------------------------------------------------------------------
@@ -146,53 +168,55 @@ class Quantized:
 
 
 def s3r_quantize(G, s_x=None, s_w=None, seed=0, tensor_id=0, out: Quantized | None = None, partials=True,
-                 status=None, stream=None) -> Quantized:
+                 status=None, stream=None, code_format=DEFAULT_CODES) -> Quantized:
     T, N = G.shape
     dev = G.device
     if out is None:
-        out = Quantized(torch.empty((T, N), dtype=torch.int8, device=dev),
+        out = Quantized(torch.empty((T, N), dtype=_CODE_DTYPE[code_format], device=dev),
                         torch.empty((_cdiv(T, TILE), _cdiv(N, TILE)), dtype=torch.float32, device=dev),
                         torch.empty((T, _cdiv(N, TILE)), dtype=torch.float32, device=dev) if partials else None,
                         torch.empty((_cdiv(T, TILE), N), dtype=torch.float32, device=dev) if partials else None)
     _check(lib().s3r_quantize(_ptr(_bits(G)), T, N, G.stride(0), _ptr(s_x), _ptr(s_w), seed, tensor_id, _ptr(out.Q),
-                              _ptr(out.tile_scale), _ptr(out.tok_err_part), _ptr(out.col_err_part), _ptr(status),
-                              _stream(stream)), "s3r_quantize")
+                              code_format_of(out.Q), _ptr(out.tile_scale), _ptr(out.tok_err_part),
+                              _ptr(out.col_err_part), _ptr(status), _stream(stream)), "s3r_quantize")
     return out
 
 
 def indep_sr_quantize(G, s_x=None, s_w=None, seed=0, tensor_id=0, out: Quantized | None = None, status=None,
-                      stream=None) -> Quantized:
+                      stream=None, code_format=DEFAULT_CODES) -> Quantized:
     T, N = G.shape
     dev = G.device
     if out is None:
-        out = Quantized(torch.empty((T, N), dtype=torch.int8, device=dev),
+        out = Quantized(torch.empty((T, N), dtype=_CODE_DTYPE[code_format], device=dev),
                         torch.empty((_cdiv(T, TILE), _cdiv(N, TILE)), dtype=torch.float32, device=dev))
     _check(lib().indep_sr_quantize(_ptr(_bits(G)), T, N, G.stride(0), _ptr(s_x), _ptr(s_w), seed, tensor_id,
-                                   _ptr(out.Q), _ptr(out.tile_scale), _ptr(status), _stream(stream)),
+                                   _ptr(out.Q), code_format_of(out.Q), _ptr(out.tile_scale), _ptr(status),
+                                   _stream(stream)),
            "indep_sr_quantize")
     return out
 
 
-def rtne_quantize(A, scale_axis=AXIS_TILE, s_x=None, s_w=None, Q=None, scale=None, status=None, stream=None):
+def rtne_quantize(A, scale_axis=AXIS_TILE, s_x=None, s_w=None, Q=None, scale=None, status=None, stream=None,
+                  code_format=DEFAULT_CODES):
     R, Cc = A.shape
     dev = A.device
     if Q is None:
-        Q = torch.empty((R, Cc), dtype=torch.int8, device=dev)
+        Q = torch.empty((R, Cc), dtype=_CODE_DTYPE[code_format], device=dev)
     if scale is None:
         shape = {AXIS_ROW: (R,), AXIS_COL: (Cc,), AXIS_TILE: (_cdiv(R, TILE), _cdiv(Cc, TILE))}[scale_axis]
         scale = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(lib().rtne_quantize(_ptr(_bits(A)), R, Cc, A.stride(0), _ptr(s_x), _ptr(s_w), scale_axis, _ptr(Q),
-                               _ptr(scale), _ptr(status), _stream(stream)), "rtne_quantize")
+                               code_format_of(Q), _ptr(scale), _ptr(status), _stream(stream)), "rtne_quantize")
     return Q, scale
 
 
 def swiglu_quantize(dA, h1, h3, s_x=None, s_w1=None, s_w3=None, round_mode=ROUND_S3R, seed=0, tid1=TID_W1,
-                    tid3=TID_W3, partials=True, status=None, stream=None):
+                    tid3=TID_W3, partials=True, status=None, stream=None, code_format=DEFAULT_CODES):
     T, F = dA.shape
     dev = dA.device
 
     def mk():
-        return Quantized(torch.empty((T, F), dtype=torch.int8, device=dev),
+        return Quantized(torch.empty((T, F), dtype=_CODE_DTYPE[code_format], device=dev),
                          torch.empty((_cdiv(T, TILE), _cdiv(F, TILE)), dtype=torch.float32, device=dev),
                          torch.empty((T, _cdiv(F, TILE)), dtype=torch.float32, device=dev) if partials else None,
                          torch.empty((_cdiv(T, TILE), F), dtype=torch.float32, device=dev) if partials else None)
@@ -200,7 +224,7 @@ def swiglu_quantize(dA, h1, h3, s_x=None, s_w1=None, s_w3=None, round_mode=ROUND
     o1, o3 = mk(), mk()
     assert dA.dtype == torch.float32 and h1.stride(0) == h3.stride(0)
     _check(lib().swiglu_quantize(_ptr(dA), dA.stride(0), _ptr(_bits(h1)), _ptr(_bits(h3)), h1.stride(0), T, F,
-                                 _ptr(s_x), _ptr(s_w1), _ptr(s_w3), round_mode, seed, tid1, tid3,
+                                 _ptr(s_x), _ptr(s_w1), _ptr(s_w3), round_mode, code_format, seed, tid1, tid3,
                                  _ptr(o1.Q), _ptr(o1.tile_scale), _ptr(o1.tok_err_part), _ptr(o1.col_err_part),
                                  _ptr(o3.Q), _ptr(o3.tile_scale), _ptr(o3.tok_err_part), _ptr(o3.col_err_part),
                                  _ptr(status), _stream(stream)), "swiglu_quantize")
@@ -231,7 +255,8 @@ def s3r_ec_correct(q: Quantized, T, N, S, W8=None, X8=None, ec_mode=EC_TWO_WAY, 
                    i(B, K) if ec_mode == EC_TWO_WAY else None, f(K) if ec_mode == EC_TWO_WAY else None)
     ws_bytes = lib().s3r_ec_workspace_size(T, K) if ec_mode == EC_TWO_WAY else 0
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    _check(lib().s3r_ec_correct(_ptr(q.tok_err_part), _ptr(q.col_err_part), T, N, S, _ptr(W8), K, _ptr(X8), ec_mode,
+    fmt = code_format_of(W8 if W8 is not None else q.Q)
+    _check(lib().s3r_ec_correct(_ptr(q.tok_err_part), _ptr(q.col_err_part), T, N, S, _ptr(W8), K, _ptr(X8), fmt, ec_mode,
                                 _ptr(ec.eps), _ptr(ec.mu), _ptr(ec.colmean), _ptr(ec.rowsum), _ptr(ec.v),
                                 _ptr(ec.xsum), _ptr(ec.p), _ptr(ws), ws_bytes, _ptr(status), _stream(stream)),
            "s3r_ec_correct")
@@ -248,7 +273,7 @@ def int8_gemm_dx(Q, tile_scale, W8, s_x=None, ec_mode=EC_NONE, ec: ECFactors | N
     if dX is None:
         dX = torch.empty((T, K), dtype=torch.float32, device=Q.device)
     S = T if S is None else S
-    _check(lib().int8_gemm_dx(_ptr(Q), _ptr(tile_scale), _ptr(W8), T, N, K, _ptr(s_x), ec_mode,
+    _check(lib().int8_gemm_dx(_ptr(Q), _ptr(tile_scale), _ptr(W8), _fmt2(Q, W8), T, N, K, _ptr(s_x), ec_mode,
                               _ptr(ec.eps if ec else None), _ptr(ec.rowsum if ec else None),
                               _ptr(ec.v if ec else None), S, _ptr(dX), int(accumulate), _ptr(status),
                               _stream(stream)), "int8_gemm_dx")
@@ -261,12 +286,13 @@ def int8_gemm_dw(X8, Q, tile_scale, s_w=None, ec_mode=EC_NONE, ec: ECFactors | N
     N = Q.shape[1]
     if dW is None:
         dW = torch.empty((K, N), dtype=torch.float32, device=Q.device)
-    ws_bytes = lib().int8_gemm_dw_workspace_size(T, K, N)
+    fmt = _fmt2(X8, Q)
+    ws_bytes = lib().int8_gemm_dw_workspace_size(T, K, N, fmt)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
     S = T if S is None else S
     two = ec_mode == EC_TWO_WAY and ec is not None
-    _check(lib().int8_gemm_dw(_ptr(X8), _ptr(Q), _ptr(tile_scale), T, K, N, _ptr(s_w), ec_mode,
+    _check(lib().int8_gemm_dw(_ptr(X8), _ptr(Q), _ptr(tile_scale), fmt, T, K, N, _ptr(s_w), ec_mode,
                               _ptr(ec.colmean if two else None), _ptr(ec.mu if two else None),
                               _ptr(ec.xsum if two else None), _ptr(ec.p if two else None), S, _ptr(dW),
                               _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)), "int8_gemm_dw")
@@ -277,7 +303,8 @@ def debug_dx_blocks(Q, W8, stream=None):
     T, N = Q.shape
     K = W8.shape[0]
     out = torch.empty((T, K, _cdiv(N, TILE)), dtype=torch.int32, device=Q.device)
-    _check(lib().s3r_debug_dx_blocks(_ptr(Q), _ptr(W8), T, N, K, _ptr(out), _stream(stream)), "s3r_debug_dx_blocks")
+    _check(lib().s3r_debug_dx_blocks(_ptr(Q), _ptr(W8), _fmt2(Q, W8), T, N, K, _ptr(out), _stream(stream)),
+           "s3r_debug_dx_blocks")
     return out
 
 
@@ -285,10 +312,11 @@ def debug_dw_blocks(X8, Q, stream=None):
     T, K = X8.shape
     N = Q.shape[1]
     out = torch.empty((K, N, _cdiv(T, TILE)), dtype=torch.int32, device=Q.device)
-    ws_bytes = lib().int8_gemm_dw_workspace_size(T, K, N)
+    fmt = _fmt2(X8, Q)
+    ws_bytes = lib().int8_gemm_dw_workspace_size(T, K, N, fmt)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
-    _check(lib().s3r_debug_dw_blocks(_ptr(X8), _ptr(Q), T, K, N, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
-           "s3r_debug_dw_blocks")
+    _check(lib().s3r_debug_dw_blocks(_ptr(X8), _ptr(Q), fmt, T, K, N, _ptr(out), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "s3r_debug_dw_blocks")
     return out
 
 
@@ -300,7 +328,7 @@ class _FfnArgs(C.Structure):
                 ("dY", _VP), ("h1", _VP), ("h3", _VP),
                 ("X8", _VP), ("s_x", _VP), ("A8", _VP), ("s_a", _VP),
                 ("W1_8", _VP), ("s_w1", _VP), ("W3_8", _VP), ("s_w3", _VP), ("W2_8", _VP), ("s_w2", _VP),
-                ("round_mode", C.c_int), ("ec_mode", C.c_int), ("seed", C.c_uint64),
+                ("round_mode", C.c_int), ("ec_mode", C.c_int), ("code_format", C.c_int), ("seed", C.c_uint64),
                 ("dX", _VP), ("dW1", _VP), ("dW3", _VP), ("dW2", _VP),
                 ("workspace", _VP), ("workspace_bytes", C.c_size_t), ("d_status", _VP),
                 ("step_events", C.POINTER(C.c_void_p))]
@@ -328,19 +356,20 @@ class FFNOperands:
     h3: torch.Tensor
 
 
-def ffn_forward_operands(X, W1, W3, W2, a, h1, h3, stream=None) -> FFNOperands:
+def ffn_forward_operands(X, W1, W3, W2, a, h1, h3, stream=None, code_format=DEFAULT_CODES) -> FFNOperands:
     """RTNE forward operands (per-token scales for X and a, per-output-channel
     scales for the weights) computed with rtne_quantize."""
-    X8, s_x = rtne_quantize(X, AXIS_ROW, stream=stream)
-    A8, s_a = rtne_quantize(a, AXIS_ROW, stream=stream)
-    W1_8, s_w1 = rtne_quantize(W1, AXIS_COL, stream=stream)
-    W3_8, s_w3 = rtne_quantize(W3, AXIS_COL, stream=stream)
-    W2_8, s_w2 = rtne_quantize(W2, AXIS_COL, stream=stream)
+    cf = code_format
+    X8, s_x = rtne_quantize(X, AXIS_ROW, stream=stream, code_format=cf)
+    A8, s_a = rtne_quantize(a, AXIS_ROW, stream=stream, code_format=cf)
+    W1_8, s_w1 = rtne_quantize(W1, AXIS_COL, stream=stream, code_format=cf)
+    W3_8, s_w3 = rtne_quantize(W3, AXIS_COL, stream=stream, code_format=cf)
+    W2_8, s_w2 = rtne_quantize(W2, AXIS_COL, stream=stream, code_format=cf)
     return FFNOperands(X8, s_x, A8, s_a, W1_8, s_w1, W3_8, s_w3, W2_8, s_w2, h1, h3)
 
 
-def ffn_workspace_size(T, d, F, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY) -> int:
-    return int(lib().s3r_ffn_workspace_size(T, d, F, S, round_mode, ec_mode))
+def ffn_workspace_size(T, d, F, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, code_format=DEFAULT_CODES) -> int:
+    return int(lib().s3r_ffn_workspace_size(T, d, F, S, round_mode, ec_mode, code_format))
 
 
 @dataclass
@@ -365,13 +394,14 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
     dev = dY.device
     if grads is None:
         grads = alloc_ffn_grads(T, d, F, dev)
-    need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode)
+    fmt = code_format_of(ops.X8)
+    need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode, fmt)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     p = lambda t: None if t is None else t.data_ptr()
     args = _FfnArgs(T, d, F, S, p(_bits(dY)), p(_bits(ops.h1)), p(_bits(ops.h3)), p(ops.X8), p(ops.s_x), p(ops.A8),
                     p(ops.s_a), p(ops.W1_8), p(ops.s_w1), p(ops.W3_8), p(ops.s_w3), p(ops.W2_8), p(ops.s_w2),
-                    round_mode, ec_mode, seed, p(grads.dX), p(grads.dW1), p(grads.dW3), p(grads.dW2),
+                    round_mode, ec_mode, fmt, seed, p(grads.dX), p(grads.dW1), p(grads.dW3), p(grads.dW2),
                     p(workspace), workspace.numel(), p(status), None)
     if step_events is not None:
         assert len(step_events) == FFN_NUM_EVENTS

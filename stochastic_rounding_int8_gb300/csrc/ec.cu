@@ -10,9 +10,14 @@
 //
 // Every reduction runs in a fixed order (no float atomics), so results are
 // deterministic run to run.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace s3r {
+
+__device__ __forceinline__ int code_value(int8_t c) { return c; }
+__device__ __forceinline__ int code_value(__half c) { return __half2int_rn(c); }
 
 // eps[t] = (sum_j tok[t, j]) / N ;  colmean[b, n] = (sum_{tile rows i of b} col[i, n]) / S
 __global__ void ec_means_kernel(const float* tok, const float* col, int64_t T, int64_t N, int64_t S, int64_t ntc,
@@ -50,15 +55,16 @@ __global__ void __launch_bounds__(256) ec_mu_kernel(const float* eps, int64_t S,
 }
 
 // One warp per weight row k: rowsum[k] = sum_n W8[k,n]; v[b,k] = sum_n (colmean[b,n]-mu[b]) W8[k,n].
-__global__ void __launch_bounds__(256) ec_gemv_kernel(const int8_t* W8, int64_t K, int64_t N, int64_t B,
+template <typename CodeT>
+__global__ void __launch_bounds__(256) ec_gemv_kernel(const CodeT* W8, int64_t K, int64_t N, int64_t B,
                                                       const float* colmean, const float* mu, int32_t* rowsum,
                                                       float* v) {
     const int64_t k = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (k >= K) return;
-    const int8_t* w = W8 + k * N;
+    const CodeT* w = W8 + k * N;
     int32_t rs = 0;
-    for (int64_t n = lane; n < N; n += 32) rs += w[n];
+    for (int64_t n = lane; n < N; n += 32) rs += code_value(w[n]);
     for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xFFFFFFFFu, rs, o);
     if (lane == 0) rowsum[k] = rs;
     if (!v) return;
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(256) ec_gemv_kernel(const int8_t* W8, int64_t 
             m[q] = (b0 + q < B) ? mu[b0 + q] : 0.0f;
         }
         for (int64_t n = lane; n < N; n += 32) {
-            const float wv = (float)w[n];
+            const float wv = (float)code_value(w[n]);
 #pragma unroll
             for (int q = 0; q < BCH; ++q)
                 if (b0 + q < B) acc[q] = fmaf(colmean[(b0 + q) * N + n] - m[q], wv, acc[q]);
@@ -88,7 +94,8 @@ __global__ void __launch_bounds__(256) ec_gemv_kernel(const int8_t* W8, int64_t 
 
 // Two-way factors, first pass: per 128-row tile i and column k,
 //   xs[i, k] = sum_{t in tile i} X8[t,k],   ps[i, k] = sum_{t in tile i} X8[t,k] eps[t].
-__global__ void __launch_bounds__(128) ec_xsum_partial_kernel(const int8_t* X8, int64_t T, int64_t K,
+template <typename CodeT>
+__global__ void __launch_bounds__(128) ec_xsum_partial_kernel(const CodeT* X8, int64_t T, int64_t K,
                                                               const float* eps, int32_t* xs, float* ps) {
     const int64_t k = (int64_t)blockIdx.x * 128 + threadIdx.x;
     const int64_t i = blockIdx.y;
@@ -97,7 +104,7 @@ __global__ void __launch_bounds__(128) ec_xsum_partial_kernel(const int8_t* X8, 
     int32_t sx = 0;
     float sp = 0.0f;
     for (int64_t t = i * kTile; t < t_end; ++t) {
-        const int x = X8[t * K + k];
+        const int x = code_value(X8[t * K + k]);
         sx += x;
         sp = fmaf((float)x, eps[t], sp);
     }
@@ -134,11 +141,13 @@ extern "C" size_t s3r_ec_workspace_size(int64_t T, int64_t K) {
 }
 
 extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
-                              const int8_t* W8, int64_t K, const int8_t* X8, int ec_mode, float* eps, float* mu,
-                              float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p, void* workspace,
-                              size_t workspace_bytes, int* d_status, cudaStream_t stream) {
+                              const void* W8, int64_t K, const void* X8, int code_format, int ec_mode, float* eps,
+                              float* mu, float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p,
+                              void* workspace, size_t workspace_bytes, int* d_status, cudaStream_t stream) {
     (void)d_status;
     if (T < 0 || N < 0 || K < 0 || S <= 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    const bool f16 = code_format == S3R_CODES_F16;
     if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
     if (T == 0 || N == 0) return S3R_OK;
     if (T % S != 0) return S3R_ERR_SHAPE;
@@ -155,7 +164,12 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
     }
     if (ec_mode == S3R_EC_NONE || K == 0) return S3R_OK;
     if (!W8 || !rowsum || !v) return S3R_ERR_ARG;
-    ec_gemv_kernel<<<(unsigned)s3r_cdiv(K, 8), 256, 0, stream>>>(W8, K, N, B, colmean, mu, rowsum, v);
+    if (f16)
+        ec_gemv_kernel<<<(unsigned)s3r_cdiv(K, 8), 256, 0, stream>>>(static_cast<const __half*>(W8), K, N, B, colmean,
+                                                                     mu, rowsum, v);
+    else
+        ec_gemv_kernel<<<(unsigned)s3r_cdiv(K, 8), 256, 0, stream>>>(static_cast<const int8_t*>(W8), K, N, B, colmean,
+                                                                     mu, rowsum, v);
     S3R_CHECK_LAUNCH();
     if (ec_mode != S3R_EC_TWO_WAY) return S3R_OK;
     if (!X8 || !xsum || !p) return S3R_ERR_ARG;
@@ -163,7 +177,10 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
     int32_t* xs = static_cast<int32_t*>(workspace);
     float* ps = reinterpret_cast<float*>(xs + ntr * K);
     dim3 grid((unsigned)s3r_cdiv(K, 128), (unsigned)ntr);
-    ec_xsum_partial_kernel<<<grid, 128, 0, stream>>>(X8, T, K, eps, xs, ps);
+    if (f16)
+        ec_xsum_partial_kernel<<<grid, 128, 0, stream>>>(static_cast<const __half*>(X8), T, K, eps, xs, ps);
+    else
+        ec_xsum_partial_kernel<<<grid, 128, 0, stream>>>(static_cast<const int8_t*>(X8), T, K, eps, xs, ps);
     S3R_CHECK_LAUNCH();
     ec_xsum_reduce_kernel<<<(unsigned)s3r_cdiv(K, 256), 256, 0, stream>>>(xs, ps, ntr, K, B, S / kTile, xsum, p);
     S3R_CHECK_LAUNCH();

@@ -33,9 +33,9 @@ struct Carver {
 
 // Buffers of one linear's quantization + correction.
 struct LinearWs {
-    int8_t* Q;       // codes for dX (and dW unless independent SR)
+    void* Q;         // codes for dX (and dW unless independent SR)
     float* scale;
-    int8_t* Qr;      // independent SR: codes for dW
+    void* Qr;        // independent SR: codes for dW
     float* scale_r;
     float* tok;
     float* col;
@@ -55,11 +55,12 @@ struct FfnLayout {
     bool ok;
 };
 
-void carve_linear(Carver& c, LinearWs& L, int64_t T, int64_t N, int64_t K, int64_t S, int round_mode) {
+void carve_linear(Carver& c, LinearWs& L, int64_t T, int64_t N, int64_t K, int64_t S, int round_mode, int fmt) {
     const int64_t ntr = s3r_cdiv(T, S3R_TILE), ntc = s3r_cdiv(N, S3R_TILE), B = T / S;
-    L.Q = c.take<int8_t>(T * N);
+    const int64_t qbytes = T * N * (fmt == S3R_CODES_F16 ? 2 : 1);
+    L.Q = c.take<uint8_t>(qbytes);
     L.scale = c.take<float>(ntr * ntc);
-    L.Qr = round_mode == S3R_ROUND_INDEP ? c.take<int8_t>(T * N) : nullptr;
+    L.Qr = round_mode == S3R_ROUND_INDEP ? c.take<uint8_t>(qbytes) : nullptr;
     L.scale_r = round_mode == S3R_ROUND_INDEP ? c.take<float>(ntr * ntc) : nullptr;
     L.tok = c.take<float>(T * ntc);
     L.col = c.take<float>(ntr * N);
@@ -72,16 +73,16 @@ void carve_linear(Carver& c, LinearWs& L, int64_t T, int64_t N, int64_t K, int64
     L.xsum = c.take<int32_t>(B * K);
 }
 
-FfnLayout layout(void* base, size_t bytes, int64_t T, int64_t d, int64_t F, int64_t S, int round_mode) {
+FfnLayout layout(void* base, size_t bytes, int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int fmt) {
     FfnLayout Lo{};
     Carver c(base, base ? bytes : ~(size_t)0 >> 1);
-    carve_linear(c, Lo.w2, T, d, F, S, round_mode);   // W2: G = dY [T, d], W2 [F, d]
-    carve_linear(c, Lo.w1, T, F, d, S, round_mode);   // W1: G = dh1 [T, F], W1 [d, F]
-    carve_linear(c, Lo.w3, T, F, d, S, round_mode);
+    carve_linear(c, Lo.w2, T, d, F, S, round_mode, fmt);   // W2: G = dY [T, d], W2 [F, d]
+    carve_linear(c, Lo.w1, T, F, d, S, round_mode, fmt);   // W1: G = dh1 [T, F], W1 [d, F]
+    carve_linear(c, Lo.w3, T, F, d, S, round_mode, fmt);
     Lo.dA = c.take<float>(T * F);
     Lo.ec_ws_bytes = s3r_ec_workspace_size(T, F > d ? F : d);
     Lo.ec_ws = c.take<uint8_t>((int64_t)Lo.ec_ws_bytes);
-    const size_t a = int8_gemm_dw_workspace_size(T, F, d), b = int8_gemm_dw_workspace_size(T, d, F);
+    const size_t a = int8_gemm_dw_workspace_size(T, F, d, fmt), b = int8_gemm_dw_workspace_size(T, d, F, fmt);
     Lo.dw_ws_bytes = a > b ? a : b;
     Lo.dw_ws = c.take<uint8_t>((int64_t)Lo.dw_ws_bytes);
     Lo.total = (size_t)(c.cur - (uintptr_t)base) + 256;
@@ -97,10 +98,11 @@ FfnLayout layout(void* base, size_t bytes, int64_t T, int64_t d, int64_t F, int6
 
 }  // namespace
 
-extern "C" size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode) {
+extern "C" size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
+                                         int code_format) {
     (void)ec_mode;
     if (T <= 0 || d <= 0 || F <= 0 || S <= 0 || T % S != 0) return 0;
-    return layout(nullptr, 0, T, d, F, S, round_mode).total;
+    return layout(nullptr, 0, T, d, F, S, round_mode, code_format).total;
 }
 
 extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
@@ -110,12 +112,14 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     if (T % S != 0 || (S % S3R_TILE != 0 && S != T)) return S3R_ERR_SHAPE;
     if (a->round_mode < S3R_ROUND_RTNE || a->round_mode > S3R_ROUND_INDEP) return S3R_ERR_ARG;
     if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    const int fmt = a->code_format;
     if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->A8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 ||
         !a->dW2 || !a->dW3)
         return S3R_ERR_ARG;
-    if (!a->workspace || a->workspace_bytes < s3r_ffn_workspace_size(T, d, F, S, a->round_mode, a->ec_mode))
+    if (!a->workspace || a->workspace_bytes < s3r_ffn_workspace_size(T, d, F, S, a->round_mode, a->ec_mode, fmt))
         return S3R_ERR_WORKSPACE;
-    FfnLayout Lo = layout(a->workspace, a->workspace_bytes, T, d, F, S, a->round_mode);
+    FfnLayout Lo = layout(a->workspace, a->workspace_bytes, T, d, F, S, a->round_mode, fmt);
     if (!Lo.ok) return S3R_ERR_WORKSPACE;
     const int rm = a->round_mode;
     const int ec = rm == S3R_ROUND_S3R ? a->ec_mode : S3R_EC_NONE;
@@ -133,58 +137,58 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     // 1. quantize dY with the W2 fold (s_a per token, s_w2 per output channel)
     LinearWs& L2 = Lo.w2;
     if (rm == S3R_ROUND_S3R) {
-        S3R_TRY(s3r_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2, L2.Q, L2.scale, L2.tok, L2.col, st,
-                             stream));
+        S3R_TRY(s3r_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2, L2.Q, fmt, L2.scale, L2.tok, L2.col,
+                             st, stream));
     } else if (indep) {
-        S3R_TRY(indep_sr_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2, L2.Q, L2.scale, st, stream));
-        S3R_TRY(indep_sr_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2 + kRhsOffset, L2.Qr, L2.scale_r,
-                                  st, stream));
+        S3R_TRY(indep_sr_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2, L2.Q, fmt, L2.scale, st, stream));
+        S3R_TRY(indep_sr_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2 + kRhsOffset, L2.Qr, fmt,
+                                  L2.scale_r, st, stream));
     } else {
-        S3R_TRY(rtne_quantize(a->dY, T, d, d, a->s_a, a->s_w2, S3R_AXIS_TILE, L2.Q, L2.scale, st, stream));
+        S3R_TRY(rtne_quantize(a->dY, T, d, d, a->s_a, a->s_w2, S3R_AXIS_TILE, L2.Q, fmt, L2.scale, st, stream));
     }
     S3R_TRY(mark(1));
     // 2. correction factors of W2 (W8 = W2_8 [F, d], X8 = A8 [T, F])
     if (ec != S3R_EC_NONE)
-        S3R_TRY(s3r_ec_correct(L2.tok, L2.col, T, d, S, a->W2_8, F, a->A8, ec, L2.eps, L2.mu, L2.colmean, L2.rowsum,
-                               L2.v, L2.xsum, L2.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
+        S3R_TRY(s3r_ec_correct(L2.tok, L2.col, T, d, S, a->W2_8, F, a->A8, fmt, ec, L2.eps, L2.mu, L2.colmean,
+                               L2.rowsum, L2.v, L2.xsum, L2.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
     S3R_TRY(mark(2));
     // 3. dA = Q2 W2_8^T (rescaled, corrected, / s_a)  [T, F]
-    S3R_TRY(int8_gemm_dx(L2.Q, L2.scale, a->W2_8, T, d, F, a->s_a, ec, L2.eps, L2.rowsum, L2.v, S, Lo.dA, 0, st,
-                         stream));
+    S3R_TRY(int8_gemm_dx(L2.Q, L2.scale, a->W2_8, fmt, T, d, F, a->s_a, ec, L2.eps, L2.rowsum, L2.v, S, Lo.dA, 0,
+                         st, stream));
     S3R_TRY(mark(3));
     // 4. dW2 = A8^T Q2 / s_w2  [F, d]
-    S3R_TRY(int8_gemm_dw(a->A8, indep ? L2.Qr : L2.Q, indep ? L2.scale_r : L2.scale, T, F, d, a->s_w2, ec,
+    S3R_TRY(int8_gemm_dw(a->A8, indep ? L2.Qr : L2.Q, indep ? L2.scale_r : L2.scale, fmt, T, F, d, a->s_w2, ec,
                          L2.colmean, L2.mu, L2.xsum, L2.p, S, a->dW2, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
     S3R_TRY(mark(4));
     // 5. SwiGLU glue fused into the quantization of dh1 (W1 fold) and dh3 (W3 fold)
     LinearWs &L1 = Lo.w1, &L3 = Lo.w3;
     const bool keep_err = ec != S3R_EC_NONE;
-    S3R_TRY(swiglu_quantize(Lo.dA, F, a->h1, a->h3, F, T, F, a->s_x, a->s_w1, a->s_w3, rm, a->seed, kTidW1, kTidW3,
-                            L1.Q, L1.scale, keep_err ? L1.tok : nullptr, keep_err ? L1.col : nullptr, L3.Q, L3.scale,
-                            keep_err ? L3.tok : nullptr, keep_err ? L3.col : nullptr, st, stream));
+    S3R_TRY(swiglu_quantize(Lo.dA, F, a->h1, a->h3, F, T, F, a->s_x, a->s_w1, a->s_w3, rm, fmt, a->seed, kTidW1,
+                            kTidW3, L1.Q, L1.scale, keep_err ? L1.tok : nullptr, keep_err ? L1.col : nullptr, L3.Q,
+                            L3.scale, keep_err ? L3.tok : nullptr, keep_err ? L3.col : nullptr, st, stream));
     if (indep)
-        S3R_TRY(swiglu_quantize(Lo.dA, F, a->h1, a->h3, F, T, F, a->s_x, a->s_w1, a->s_w3, rm, a->seed,
+        S3R_TRY(swiglu_quantize(Lo.dA, F, a->h1, a->h3, F, T, F, a->s_x, a->s_w1, a->s_w3, rm, fmt, a->seed,
                                 kTidW1 + kRhsOffset, kTidW3 + kRhsOffset, L1.Qr, L1.scale_r, nullptr, nullptr, L3.Qr,
                                 L3.scale_r, nullptr, nullptr, st, stream));
     S3R_TRY(mark(5));
     // 6. correction factors of W1 and W3 (W8 [d, F], X8 [T, d])
     if (ec != S3R_EC_NONE) {
-        S3R_TRY(s3r_ec_correct(L1.tok, L1.col, T, F, S, a->W1_8, d, a->X8, ec, L1.eps, L1.mu, L1.colmean, L1.rowsum,
-                               L1.v, L1.xsum, L1.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
-        S3R_TRY(s3r_ec_correct(L3.tok, L3.col, T, F, S, a->W3_8, d, a->X8, ec, L3.eps, L3.mu, L3.colmean, L3.rowsum,
-                               L3.v, L3.xsum, L3.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
+        S3R_TRY(s3r_ec_correct(L1.tok, L1.col, T, F, S, a->W1_8, d, a->X8, fmt, ec, L1.eps, L1.mu, L1.colmean,
+                               L1.rowsum, L1.v, L1.xsum, L1.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
+        S3R_TRY(s3r_ec_correct(L3.tok, L3.col, T, F, S, a->W3_8, d, a->X8, fmt, ec, L3.eps, L3.mu, L3.colmean,
+                               L3.rowsum, L3.v, L3.xsum, L3.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
     }
     S3R_TRY(mark(6));
     // 7. dX = dX1 + dX3
-    S3R_TRY(int8_gemm_dx(L1.Q, L1.scale, a->W1_8, T, F, d, a->s_x, ec, L1.eps, L1.rowsum, L1.v, S, a->dX, 0, st,
-                         stream));
-    S3R_TRY(int8_gemm_dx(L3.Q, L3.scale, a->W3_8, T, F, d, a->s_x, ec, L3.eps, L3.rowsum, L3.v, S, a->dX, 1, st,
-                         stream));
+    S3R_TRY(int8_gemm_dx(L1.Q, L1.scale, a->W1_8, fmt, T, F, d, a->s_x, ec, L1.eps, L1.rowsum, L1.v, S, a->dX, 0,
+                         st, stream));
+    S3R_TRY(int8_gemm_dx(L3.Q, L3.scale, a->W3_8, fmt, T, F, d, a->s_x, ec, L3.eps, L3.rowsum, L3.v, S, a->dX, 1,
+                         st, stream));
     S3R_TRY(mark(7));
     // 8. dW1, dW3
-    S3R_TRY(int8_gemm_dw(a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, T, d, F, a->s_w1, ec,
+    S3R_TRY(int8_gemm_dw(a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, fmt, T, d, F, a->s_w1, ec,
                          L1.colmean, L1.mu, L1.xsum, L1.p, S, a->dW1, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
-    S3R_TRY(int8_gemm_dw(a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, T, d, F, a->s_w3, ec,
+    S3R_TRY(int8_gemm_dw(a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, fmt, T, d, F, a->s_w3, ec,
                          L3.colmean, L3.mu, L3.xsum, L3.p, S, a->dW3, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
     S3R_TRY(mark(8));
     return S3R_OK;

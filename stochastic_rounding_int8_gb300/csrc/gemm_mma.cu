@@ -233,6 +233,14 @@ __global__ void __launch_bounds__(256) transpose_s8_kernel(const int8_t* src, in
 
 using namespace s3r;
 
+// tcgen05 path for fp16-carried codes (gemm_umma.cu)
+int umma_gemm_dx(const void* Q, const float* tile_scale, const void* W, int64_t T, int64_t N, int64_t K,
+                 const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum, const float* v, int64_t S,
+                 float* dX, int accumulate, int32_t* dump, int* d_status, cudaStream_t stream);
+int umma_gemm_dw(const void* X, const void* Q, const float* tile_scale, int64_t T, int64_t K, int64_t N,
+                 const float* s_w, int ec_mode, const float* colmean, const float* mu, const int32_t* xsum,
+                 const float* p, int64_t S, float* dW, int32_t* dump, int* d_status, cudaStream_t stream);
+
 static bool gemm_smem_ready = false;
 
 static int ensure_gemm_smem() {
@@ -263,14 +271,14 @@ static int launch_gemm(const GemmOperands& P, const GemmEpilogue& E, cudaStream_
 
 static int64_t pad16(int64_t x) { return (x + 15) / 16 * 16; }
 
-extern "C" size_t int8_gemm_dw_workspace_size(int64_t T, int64_t K, int64_t N) {
-    if (T <= 0 || K <= 0 || N <= 0) return 0;
+extern "C" size_t int8_gemm_dw_workspace_size(int64_t T, int64_t K, int64_t N, int code_format) {
+    if (T <= 0 || K <= 0 || N <= 0 || code_format != S3R_CODES_S8) return 0;
     return (size_t)(K + N) * (size_t)pad16(T) + 512;
 }
 
 static int transpose_pair(const int8_t* X8, const int8_t* Q, int64_t T, int64_t K, int64_t N, void* ws,
                           size_t ws_bytes, int8_t** Xt, int8_t** Qt, cudaStream_t stream) {
-    if (!ws || ws_bytes < int8_gemm_dw_workspace_size(T, K, N)) return S3R_ERR_WORKSPACE;
+    if (!ws || ws_bytes < int8_gemm_dw_workspace_size(T, K, N, S3R_CODES_S8)) return S3R_ERR_WORKSPACE;
     const int64_t ldt = pad16(T);
     uintptr_t base = ((uintptr_t)ws + 255) & ~(uintptr_t)255;
     *Xt = reinterpret_cast<int8_t*>(base);
@@ -284,36 +292,46 @@ static int transpose_pair(const int8_t* X8, const int8_t* Q, int64_t T, int64_t 
     return S3R_OK;
 }
 
-extern "C" int int8_gemm_dx(const int8_t* Q, const float* tile_scale, const int8_t* W8, int64_t T, int64_t N,
-                            int64_t K, const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum,
-                            const float* v, int64_t S, float* dX, int accumulate, int* d_status,
+extern "C" int int8_gemm_dx(const void* Qv, const float* tile_scale, const void* W8v, int code_format, int64_t T,
+                            int64_t N, int64_t K, const float* s_x, int ec_mode, const float* eps,
+                            const int32_t* rowsum, const float* v, int64_t S, float* dX, int accumulate, int* d_status,
                             cudaStream_t stream) {
-    (void)d_status;
     if (T < 0 || N < 0 || K < 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (T == 0 || K == 0) return S3R_OK;
-    if (!Q || !tile_scale || !W8 || !dX) return S3R_ERR_ARG;
+    if (!Qv || !tile_scale || !W8v || !dX) return S3R_ERR_ARG;
     if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
     if (ec_mode != S3R_EC_NONE && (!eps || !rowsum || !v || S <= 0 || T % S != 0)) return S3R_ERR_ARG;
+    if (N == 0) return S3R_ERR_SHAPE;
+    if (code_format == S3R_CODES_F16)
+        return umma_gemm_dx(Qv, tile_scale, W8v, T, N, K, s_x, ec_mode, eps, rowsum, v, S > 0 ? S : T, dX,
+                            accumulate, nullptr, d_status, stream);
+    const int8_t* Q = static_cast<const int8_t*>(Qv);
+    const int8_t* W8 = static_cast<const int8_t*>(W8v);
     const bool aligned = s3r_aligned16(Q) && s3r_aligned16(W8) && N % 16 == 0;
     GemmOperands P{Q, N, W8, N, T, K, N, tile_scale, s3r_cdiv(N, kTile), 0, 1, aligned};
     GemmEpilogue E{};
     E.C = dX; E.ldc = K; E.s_x = s_x; E.eps = eps; E.rowsum = rowsum; E.v = v; E.accumulate = accumulate;
     E.ec_mode = ec_mode; E.S = S > 0 ? S : T;
-    if (N == 0) return S3R_ERR_SHAPE;
     return launch_gemm<kEpiDX>(P, E, stream);
 }
 
-extern "C" int int8_gemm_dw(const int8_t* X8, const int8_t* Q, const float* tile_scale, int64_t T, int64_t K,
-                            int64_t N, const float* s_w, int ec_mode, const float* colmean, const float* mu,
+extern "C" int int8_gemm_dw(const void* X8v, const void* Qv, const float* tile_scale, int code_format, int64_t T,
+                            int64_t K, int64_t N, const float* s_w, int ec_mode, const float* colmean, const float* mu,
                             const int32_t* xsum, const float* p, int64_t S, float* dW, void* workspace,
                             size_t workspace_bytes, int* d_status, cudaStream_t stream) {
-    (void)d_status;
     if (T < 0 || N < 0 || K < 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (K == 0 || N == 0) return S3R_OK;
-    if (!X8 || !Q || !tile_scale || !dW) return S3R_ERR_ARG;
+    if (!X8v || !Qv || !tile_scale || !dW) return S3R_ERR_ARG;
     if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
     if (ec_mode == S3R_EC_TWO_WAY && (!colmean || !mu || !xsum || !p || S <= 0 || T % S != 0)) return S3R_ERR_ARG;
     if (T == 0) return S3R_ERR_SHAPE;
+    if (code_format == S3R_CODES_F16)
+        return umma_gemm_dw(X8v, Qv, tile_scale, T, K, N, s_w, ec_mode, colmean, mu, xsum, p, S > 0 ? S : T, dW,
+                            nullptr, d_status, stream);
+    const int8_t* X8 = static_cast<const int8_t*>(X8v);
+    const int8_t* Q = static_cast<const int8_t*>(Qv);
     int8_t *Xt, *Qt;
     int st = transpose_pair(X8, Q, T, K, N, workspace, workspace_bytes, &Xt, &Qt, stream);
     if (st) return st;
@@ -325,9 +343,15 @@ extern "C" int int8_gemm_dw(const int8_t* X8, const int8_t* Q, const float* tile
     return launch_gemm<kEpiDW>(P, E, stream);
 }
 
-extern "C" int s3r_debug_dx_blocks(const int8_t* Q, const int8_t* W8, int64_t T, int64_t N, int64_t K,
-                                   int32_t* out_dx, cudaStream_t stream) {
-    if (T <= 0 || N <= 0 || K <= 0 || !Q || !W8 || !out_dx) return S3R_ERR_ARG;
+extern "C" int s3r_debug_dx_blocks(const void* Qv, const void* W8v, int code_format, int64_t T, int64_t N,
+                                   int64_t K, int32_t* out_dx, cudaStream_t stream) {
+    if (T <= 0 || N <= 0 || K <= 0 || !Qv || !W8v || !out_dx) return S3R_ERR_ARG;
+    if (code_format == S3R_CODES_F16)
+        return umma_gemm_dx(Qv, nullptr, W8v, T, N, K, nullptr, 0, nullptr, nullptr, nullptr, T, nullptr, 0, out_dx,
+                            nullptr, stream);
+    if (code_format != S3R_CODES_S8) return S3R_ERR_ARG;
+    const int8_t* Q = static_cast<const int8_t*>(Qv);
+    const int8_t* W8 = static_cast<const int8_t*>(W8v);
     const bool aligned = s3r_aligned16(Q) && s3r_aligned16(W8) && N % 16 == 0;
     GemmOperands P{Q, N, W8, N, T, K, N, nullptr, 0, 0, 0, aligned};
     GemmEpilogue E{};
@@ -335,9 +359,15 @@ extern "C" int s3r_debug_dx_blocks(const int8_t* Q, const int8_t* W8, int64_t T,
     return launch_gemm<kEpiDump>(P, E, stream);
 }
 
-extern "C" int s3r_debug_dw_blocks(const int8_t* X8, const int8_t* Q, int64_t T, int64_t K, int64_t N,
+extern "C" int s3r_debug_dw_blocks(const void* X8v, const void* Qv, int code_format, int64_t T, int64_t K, int64_t N,
                                    int32_t* out_dw, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (T <= 0 || N <= 0 || K <= 0 || !X8 || !Q || !out_dw) return S3R_ERR_ARG;
+    if (T <= 0 || N <= 0 || K <= 0 || !X8v || !Qv || !out_dw) return S3R_ERR_ARG;
+    if (code_format == S3R_CODES_F16)
+        return umma_gemm_dw(X8v, Qv, nullptr, T, K, N, nullptr, 0, nullptr, nullptr, nullptr, nullptr, T, nullptr,
+                            out_dw, nullptr, stream);
+    if (code_format != S3R_CODES_S8) return S3R_ERR_ARG;
+    const int8_t* X8 = static_cast<const int8_t*>(X8v);
+    const int8_t* Q = static_cast<const int8_t*>(Qv);
     int8_t *Xt, *Qt;
     int st = transpose_pair(X8, Q, T, K, N, workspace, workspace_bytes, &Xt, &Qt, stream);
     if (st) return st;

@@ -13,6 +13,8 @@
 // Philox threshold is computed by one lane per row and broadcast with
 // __shfl_sync; codes are written once as 8-byte stores; the error partials are
 // reduced with shuffles and a small shared-memory pass, in a fixed order.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace s3r {
@@ -28,7 +30,8 @@ struct TileGeom {
 };
 
 struct QuantOut {
-    int8_t* Q;
+    void* Q;
+    int fmt;  // S3R_CODES_S8 or S3R_CODES_F16
     float* scale;
     float* tok;
     float* col;
@@ -40,7 +43,7 @@ struct QuantCommon {
     int64_t ntc;
     uint32_t seed_lo;
     int* d_status;
-    bool vec_store;  // Q rows 8-byte aligned for every chunk
+    bool vec_store;  // Q rows aligned for one vector store per 8-code chunk
 };
 
 // Block-wide max of non-negative float bit patterns (NaN/Inf compare largest).
@@ -135,13 +138,33 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
         }
         if (nonfinite) packed[0] = packed[1] = 0u;
         if (t < C.T) {
-            int8_t* dst = O.Q + t * C.N + nc0;
-            if (C.vec_store && nc0 + 8 <= C.N) {
-                *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-            } else {
+            if (O.fmt == S3R_CODES_S8) {
+                int8_t* dst = static_cast<int8_t*>(O.Q) + t * C.N + nc0;
+                if (C.vec_store && nc0 + 8 <= C.N) {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (nc0 + i < C.N) dst[i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFF);
+                    for (int i = 0; i < 8; ++i)
+                        if (nc0 + i < C.N) dst[i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFF);
+                }
+            } else {
+                // the same integer in an IEEE half (exact for |q| <= 2048)
+                uint32_t hw[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int qa = (int)(int8_t)((packed[(2 * k) >> 2] >> (8 * ((2 * k) & 3))) & 0xFF);
+                    const int qb = (int)(int8_t)((packed[(2 * k + 1) >> 2] >> (8 * ((2 * k + 1) & 3))) & 0xFF);
+                    hw[k] = (uint32_t)__half_as_ushort(__int2half_rn(qa)) |
+                            ((uint32_t)__half_as_ushort(__int2half_rn(qb)) << 16);
+                }
+                __half* dst = static_cast<__half*>(O.Q) + t * C.N + nc0;
+                if (C.vec_store && nc0 + 8 <= C.N) {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (nc0 + i < C.N) dst[i] = __ushort_as_half((unsigned short)(hw[i >> 1] >> (16 * (i & 1))));
+                }
             }
         }
         if (O.tok) {
@@ -329,8 +352,13 @@ __global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, Quan
 // Forward operands: RTNE with one scale per row or per column (scale 1 for an
 // all-zero row/column).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_code(void* Q, int fmt, int64_t idx, float q) {
+    if (fmt == S3R_CODES_S8) static_cast<int8_t*>(Q)[idx] = (int8_t)(int)q;
+    else static_cast<__half*>(Q)[idx] = __int2half_rn((int)q);
+}
+
 __global__ void __launch_bounds__(256) rtne_rows_kernel(const uint16_t* A, int64_t R, int64_t C, int64_t lda,
-                                                        int8_t* Q, float* scale, int* d_status) {
+                                                        void* Q, int fmt, float* scale, int* d_status) {
     const int64_t r = (int64_t)blockIdx.x;
     __shared__ uint32_t red[8];
     uint32_t m = 0u;
@@ -339,7 +367,7 @@ __global__ void __launch_bounds__(256) rtne_rows_kernel(const uint16_t* A, int64
     m = block_max_u32<8>(m, red);
     if (m >= 0x7F800000u) {
         if (threadIdx.x == 0) { set_status(d_status, S3R_ERR_NONFINITE); scale[r] = __uint_as_float(0x7FC00000u); }
-        for (int64_t c = threadIdx.x; c < C; c += blockDim.x) Q[r * C + c] = 0;
+        for (int64_t c = threadIdx.x; c < C; c += blockDim.x) store_code(Q, fmt, r * C + c, 0.0f);
         return;
     }
     const float amax = __uint_as_float(m);
@@ -348,12 +376,12 @@ __global__ void __launch_bounds__(256) rtne_rows_kernel(const uint16_t* A, int64
     if (threadIdx.x == 0) scale[r] = s;
     for (int64_t c = threadIdx.x; c < C; c += blockDim.x) {
         const float q = fminf(fmaxf(rintf(bf16_at(A + r * lda + c) * inv), -127.0f), 127.0f);
-        Q[r * C + c] = (int8_t)(int)q;
+        store_code(Q, fmt, r * C + c, q);
     }
 }
 
 __global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64_t R, int64_t C, int64_t lda,
-                                                        int8_t* Q, float* scale, int* d_status) {
+                                                        void* Q, int fmt, float* scale, int* d_status) {
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= C) return;
     uint32_t m = 0u;
@@ -361,7 +389,7 @@ __global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64
     if (m >= 0x7F800000u) {
         set_status(d_status, S3R_ERR_NONFINITE);
         scale[c] = __uint_as_float(0x7FC00000u);
-        for (int64_t r = 0; r < R; ++r) Q[r * C + c] = 0;
+        for (int64_t r = 0; r < R; ++r) store_code(Q, fmt, r * C + c, 0.0f);
         return;
     }
     const float amax = __uint_as_float(m);
@@ -370,7 +398,7 @@ __global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64
     scale[c] = s;
     for (int64_t r = 0; r < R; ++r) {
         const float q = fminf(fmaxf(rintf(bf16_at(A + r * lda + c) * inv), -127.0f), 127.0f);
-        Q[r * C + c] = (int8_t)(int)q;
+        store_code(Q, fmt, r * C + c, q);
     }
 }
 
@@ -378,18 +406,19 @@ __global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64
 
 using namespace s3r;
 
+static bool valid_fmt(int fmt) { return fmt == S3R_CODES_S8 || fmt == S3R_CODES_F16; }
+
 static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
-                             const float* s_w, uint64_t seed, uint32_t tensor_id, int8_t* Q, float* scale, float* tok,
-                             float* col, int* d_status, cudaStream_t stream) {
-    if (T < 0 || N < 0) return S3R_ERR_ARG;
+                             const float* s_w, uint64_t seed, uint32_t tensor_id, void* Q, int fmt, float* scale,
+                             float* tok, float* col, int* d_status, cudaStream_t stream) {
+    if (T < 0 || N < 0 || !valid_fmt(fmt)) return S3R_ERR_ARG;
     if (T == 0 || N == 0) return S3R_OK;
     if (!G || !Q || !scale) return S3R_ERR_ARG;
     if (ldg < N) return S3R_ERR_SHAPE;
     if (s3r_cdiv(T, kTile) > 65535) return S3R_ERR_UNSUPPORTED;
     TileQuantArgs A{static_cast<const uint16_t*>(G), ldg, s_x, s_w, s3r_aligned16(G) && (ldg % 8) == 0};
-    QuantCommon C{T, N, s3r_cdiv(N, kTile), (uint32_t)seed, d_status,
-                  s3r_aligned16(Q) && (N % 8) == 0};
-    QuantOut O{Q, scale, tok, col, tensor_id};
+    QuantCommon C{T, N, s3r_cdiv(N, kTile), (uint32_t)seed, d_status, s3r_aligned16(Q) && (N % 8) == 0};
+    QuantOut O{Q, fmt, scale, tok, col, tensor_id};
     dim3 grid((unsigned)s3r_cdiv(N, kTile), (unsigned)s3r_cdiv(T, kTile));
     switch (mode) {
         case kRTNE: quantize_tile_kernel<kRTNE><<<grid, 256, 0, stream>>>(A, C, O); break;
@@ -402,24 +431,26 @@ static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int6
 }
 
 extern "C" int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
-                            uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale, float* tok_err_part,
-                            float* col_err_part, int* d_status, cudaStream_t stream) {
-    return launch_tile_quant(kS3R, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, tile_scale, tok_err_part,
+                            uint64_t seed, uint32_t tensor_id, void* Q, int code_format, float* tile_scale,
+                            float* tok_err_part, float* col_err_part, int* d_status, cudaStream_t stream) {
+    return launch_tile_quant(kS3R, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, code_format, tile_scale, tok_err_part,
                              col_err_part, d_status, stream);
 }
 
 extern "C" int indep_sr_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
-                                 const float* s_w, uint64_t seed, uint32_t tensor_id, int8_t* Q, float* tile_scale,
-                                 int* d_status, cudaStream_t stream) {
-    return launch_tile_quant(kINDEP, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, tile_scale, nullptr, nullptr,
-                             d_status, stream);
+                                 const float* s_w, uint64_t seed, uint32_t tensor_id, void* Q, int code_format,
+                                 float* tile_scale, int* d_status, cudaStream_t stream) {
+    return launch_tile_quant(kINDEP, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, code_format, tile_scale, nullptr,
+                             nullptr, d_status, stream);
 }
 
 extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, const float* s_x, const float* s_w,
-                             int scale_axis, int8_t* Q, float* scale, int* d_status, cudaStream_t stream) {
+                             int scale_axis, void* Q, int code_format, float* scale, int* d_status,
+                             cudaStream_t stream) {
     if (scale_axis == S3R_AXIS_TILE)
-        return launch_tile_quant(kRTNE, A, R, C, lda, s_x, s_w, 0, 0, Q, scale, nullptr, nullptr, d_status, stream);
-    if (R < 0 || C < 0) return S3R_ERR_ARG;
+        return launch_tile_quant(kRTNE, A, R, C, lda, s_x, s_w, 0, 0, Q, code_format, scale, nullptr, nullptr,
+                                 d_status, stream);
+    if (R < 0 || C < 0 || !valid_fmt(code_format)) return S3R_ERR_ARG;
     if (R == 0 || C == 0) return S3R_OK;
     if (!A || !Q || !scale) return S3R_ERR_ARG;
     if (lda < C) return S3R_ERR_SHAPE;
@@ -427,9 +458,10 @@ extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, c
     const uint16_t* a = static_cast<const uint16_t*>(A);
     if (scale_axis == S3R_AXIS_ROW) {
         if (R > 0x7FFFFFFF) return S3R_ERR_UNSUPPORTED;
-        rtne_rows_kernel<<<(unsigned)R, 256, 0, stream>>>(a, R, C, lda, Q, scale, d_status);
+        rtne_rows_kernel<<<(unsigned)R, 256, 0, stream>>>(a, R, C, lda, Q, code_format, scale, d_status);
     } else if (scale_axis == S3R_AXIS_COL) {
-        rtne_cols_kernel<<<(unsigned)s3r_cdiv(C, 256), 256, 0, stream>>>(a, R, C, lda, Q, scale, d_status);
+        rtne_cols_kernel<<<(unsigned)s3r_cdiv(C, 256), 256, 0, stream>>>(a, R, C, lda, Q, code_format, scale,
+                                                                          d_status);
     } else {
         return S3R_ERR_ARG;
     }
@@ -439,10 +471,10 @@ extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, c
 
 extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh, int64_t T,
                                int64_t F, const float* s_x, const float* s_w1, const float* s_w3, int round_mode,
-                               uint64_t seed, uint32_t tid1, uint32_t tid3, int8_t* Q1, float* scale1, float* tok1,
-                               float* col1, int8_t* Q3, float* scale3, float* tok3, float* col3, int* d_status,
-                               cudaStream_t stream) {
-    if (T < 0 || F < 0) return S3R_ERR_ARG;
+                               int code_format, uint64_t seed, uint32_t tid1, uint32_t tid3, void* Q1, float* scale1,
+                               float* tok1, float* col1, void* Q3, float* scale3, float* tok3, float* col3,
+                               int* d_status, cudaStream_t stream) {
+    if (T < 0 || F < 0 || !valid_fmt(code_format)) return S3R_ERR_ARG;
     if (T == 0 || F == 0) return S3R_OK;
     if (!dA || !h1 || !h3 || !Q1 || !Q3 || !scale1 || !scale3) return S3R_ERR_ARG;
     if (ldd < F || ldh < F) return S3R_ERR_SHAPE;
@@ -451,7 +483,7 @@ extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, con
                  s3r_aligned16(dA) && s3r_aligned16(h1) && s3r_aligned16(h3) && (ldd % 4) == 0 && (ldh % 8) == 0};
     QuantCommon C{T, F, s3r_cdiv(F, kTile), (uint32_t)seed, d_status,
                   s3r_aligned16(Q1) && s3r_aligned16(Q3) && (F % 8) == 0};
-    QuantOut O1{Q1, scale1, tok1, col1, tid1}, O3{Q3, scale3, tok3, col3, tid3};
+    QuantOut O1{Q1, code_format, scale1, tok1, col1, tid1}, O3{Q3, code_format, scale3, tok3, col3, tid3};
     dim3 grid((unsigned)s3r_cdiv(F, kTile), (unsigned)s3r_cdiv(T, kTile));
     switch (round_mode) {
         case S3R_ROUND_RTNE: swiglu_quantize_kernel<kRTNE><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;

@@ -18,6 +18,17 @@ ATOL_REL = 1e-6
 TILE = 128
 
 
+def codes(Q):
+    """Device code tensor (int8 or float16 holding integers) -> int8 numpy."""
+    import torch
+    q = Q.detach().cpu()
+    if q.dtype == torch.float16:
+        f = q.float()
+        assert torch.equal(f, f.round()) and float(f.abs().max()) <= 127, "fp16 codes must be integers in [-127, 127]"
+        q = f.to(torch.int8)
+    return q.numpy()
+
+
 def assert_close_mag(got, ref, mag, what, rtol=RTOL, atol_rel=ATOL_REL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

@@ -38,29 +38,36 @@ def test_status_strings(L):
 
 def test_host_argument_checks_need_no_gpu(L):
     null = None
+    P = C.c_void_p(16)
     # null outputs -> S3R_ERR_ARG before any launch
-    assert L.s3r_quantize(C.c_void_p(16), 4, 4, 4, null, null, 0, 0, null, null, null, null, null, null) == -1
+    assert L.s3r_quantize(P, 4, 4, 4, null, null, 0, 0, null, 0, null, null, null, null, null) == -1
     # empty tensors are a no-op
-    assert L.s3r_quantize(null, 0, 0, 0, null, null, 0, 0, null, null, null, null, null, null) == 0
+    assert L.s3r_quantize(null, 0, 0, 0, null, null, 0, 0, null, 0, null, null, null, null, null) == 0
     # ldg < N
-    assert L.s3r_quantize(C.c_void_p(16), 4, 8, 4, null, null, 0, 0, C.c_void_p(16), C.c_void_p(16), null, null,
-                          null, null) == -3
+    assert L.s3r_quantize(P, 4, 8, 4, null, null, 0, 0, P, 0, P, null, null, null, null) == -3
+    # unknown code format
+    assert L.s3r_quantize(P, 4, 8, 8, null, null, 0, 0, P, 7, P, null, null, null, null) == -1
     # unknown enum values
-    assert L.rtne_quantize(C.c_void_p(16), 4, 4, 4, null, null, 7, C.c_void_p(16), C.c_void_p(16), null, null) == -1
+    assert L.rtne_quantize(P, 4, 4, 4, null, null, 7, P, 0, P, null, null) == -1
     # T not a multiple of S in the correction
-    assert L.s3r_ec_correct(C.c_void_p(16), C.c_void_p(16), 10, 4, 3, null, 0, null, 0, C.c_void_p(16),
-                            C.c_void_p(16), C.c_void_p(16), null, null, null, null, null, 0, null, null) == -3
-    # dW workspace too small
-    assert L.int8_gemm_dw(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 256, 64, 64, null, 0, null, null, null,
-                          null, 256, C.c_void_p(16), C.c_void_p(16), 8, null, null) == -7
+    assert L.s3r_ec_correct(P, P, 10, 4, 3, null, 0, null, 0, 0, P, P, P, null, null, null, null, null, 0, null,
+                            null) == -3
+    # S8 dW workspace too small
+    assert L.int8_gemm_dw(P, P, P, 0, 256, 64, 64, null, 0, null, null, null, null, 256, P, P, 8, null, null) == -7
+    # mixed or unknown formats in the GEMMs
+    assert L.int8_gemm_dx(P, P, P, 5, 4, 16, 4, null, 0, null, null, null, 4, P, 0, null, null) == -1
+    # fp16-carried codes need rows of a multiple of 8 codes (TMA strides)
+    assert L.int8_gemm_dx(P, P, P, 1, 4, 12, 4, null, 0, null, null, null, 4, P, 0, null, null) == -2
 
 
 def test_workspace_sizes_are_host_only(L):
-    assert L.s3r_ffn_workspace_size(256, 128, 384, 128, 1, 2) > 0
-    assert L.s3r_ffn_workspace_size(256, 128, 384, 100, 1, 2) == 0   # T % S != 0
-    assert L.s3r_ffn_workspace_size(8192, 2048, 5632, 2048, 2, 0) > L.s3r_ffn_workspace_size(8192, 2048, 5632, 2048,
-                                                                                             1, 2) - 10 ** 9
-    assert L.int8_gemm_dw_workspace_size(300, 5, 7) >= (5 + 7) * 304
+    assert L.s3r_ffn_workspace_size(256, 128, 384, 128, 1, 2, 1) > 0
+    assert L.s3r_ffn_workspace_size(256, 128, 384, 100, 1, 2, 1) == 0   # T % S != 0
+    big_f16 = L.s3r_ffn_workspace_size(8192, 2048, 5632, 2048, 1, 2, 1)
+    big_s8 = L.s3r_ffn_workspace_size(8192, 2048, 5632, 2048, 1, 2, 0)
+    assert big_f16 > big_s8 - 200 * 2 ** 20   # fp16 codes double Q; S8 adds the dW transposes
+    assert L.int8_gemm_dw_workspace_size(300, 5, 7, 0) >= (5 + 7) * 304
+    assert L.int8_gemm_dw_workspace_size(300, 5, 7, 1) == 0
     assert L.s3r_ec_workspace_size(0, 5) == 0
 
 

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import workloads
-from parity_util import assert_close_mag, dw_magnitude, dx_magnitude, expand_tiles, near_tie_flips, projection
+from parity_util import assert_close_mag, codes, dw_magnitude, dx_magnitude, expand_tiles, near_tie_flips, projection
 
 pytestmark = pytest.mark.gpu
 
@@ -35,22 +35,26 @@ def _staged(s3r, ops, dY, S, rm, ec, seed):
     out = {}
     indep = rm == s3r.ROUND_INDEP
     ecm = ec if rm == s3r.ROUND_S3R else s3r.EC_NONE
+    cf = s3r.code_format_of(ops.X8)
     if rm == s3r.ROUND_S3R:
-        q2 = s3r.s3r_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2)
+        q2 = s3r.s3r_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2, code_format=cf)
     elif indep:
-        q2 = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2)
-        out["q2r"] = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2 + s3r.RHS_ID_OFFSET)
+        q2 = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2, code_format=cf)
+        out["q2r"] = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, s3r.TID_W2 + s3r.RHS_ID_OFFSET,
+                                           code_format=cf)
     else:
-        Q, sc = s3r.rtne_quantize(dY, s3r.AXIS_TILE, s_x=ops.s_a, s_w=ops.s_w2)
+        Q, sc = s3r.rtne_quantize(dY, s3r.AXIS_TILE, s_x=ops.s_a, s_w=ops.s_w2, code_format=cf)
         q2 = s3r.Quantized(Q, sc)
     ec2 = s3r.s3r_ec_correct(q2, T, d, S, ops.W2_8, ops.A8, ecm) if ecm else None
     dA = s3r.int8_gemm_dx(q2.Q, q2.tile_scale, ops.W2_8, ops.s_a, ecm, ec2, S)
     q2w = out.get("q2r", q2)
     dW2 = s3r.int8_gemm_dw(ops.A8, q2w.Q, q2w.tile_scale, ops.s_w2, ecm, ec2, S)
-    q1, q3 = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed, s3r.TID_W1, s3r.TID_W3)
+    q1, q3 = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed, s3r.TID_W1, s3r.TID_W3,
+                                 code_format=cf)
     if indep:
         out["q1r"], out["q3r"] = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed,
-                                                     s3r.TID_W1 + s3r.RHS_ID_OFFSET, s3r.TID_W3 + s3r.RHS_ID_OFFSET)
+                                                     s3r.TID_W1 + s3r.RHS_ID_OFFSET, s3r.TID_W3 + s3r.RHS_ID_OFFSET,
+                                                     code_format=cf)
     ec1 = s3r.s3r_ec_correct(q1, T, F, S, ops.W1_8, ops.X8, ecm) if ecm else None
     ec3 = s3r.s3r_ec_correct(q3, T, F, S, ops.W3_8, ops.X8, ecm) if ecm else None
     dX = s3r.int8_gemm_dx(q1.Q, q1.tile_scale, ops.W1_8, ops.s_x, ecm, ec1, S)
@@ -62,9 +66,10 @@ def _staged(s3r, ops, dY, S, rm, ec, seed):
     return out
 
 
-def _device_ops(s3r, inp):
+def _device_ops(s3r, inp, fmt=1):
     c = lambda t: t.cuda()
-    return s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
+    return s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3),
+                                    code_format=fmt)
 
 
 def _oracle_ops(orc, inp):
@@ -75,10 +80,11 @@ def _oracle_ops(orc, inp):
 MODES = [("S3R", "EC_TWO_WAY"), ("S3R", "EC_DX_ONLY"), ("S3R", "EC_NONE"), ("INDEP", "EC_NONE"), ("RTNE", "EC_NONE")]
 
 
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("mode,ec", MODES)
-def test_ffn_backward_equals_staged_calls(s3r, mode, ec):
+def test_ffn_backward_equals_staged_calls(s3r, fmt, mode, ec):
     inp = workloads.ffn_inputs(512, 256, 384, 256, seed=7)
-    ops = _device_ops(s3r, inp)
+    ops = _device_ops(s3r, inp, fmt)
     rm, ecm = getattr(s3r, "ROUND_" + mode), getattr(s3r, ec)
     st = s3r.new_status()
     g = s3r.ffn_backward(ops, inp.dY.cuda(), 256, rm, ecm, seed=9, status=st)
@@ -90,7 +96,9 @@ def test_ffn_backward_equals_staged_calls(s3r, mode, ec):
 
 
 def _forward_ops_bit_exact(ops_g, ops_o):
-    for name in ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2"):
+    for name in ("X8", "A8", "W1_8", "W3_8", "W2_8"):
+        assert np.array_equal(codes(getattr(ops_g, name)), getattr(ops_o, name)), name
+    for name in ("s_x", "s_a", "s_w1", "s_w3", "s_w2"):
         assert np.array_equal(getattr(ops_g, name).cpu().numpy(), getattr(ops_o, name)), name
 
 
@@ -111,11 +119,12 @@ def _thresholds(orc, mode, T, N, seed, tid):
     return 0.5
 
 
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("mode,ec", MODES)
-def test_ffn_staged_matches_oracle(s3r, orc, mode, ec):
+def test_ffn_staged_matches_oracle(s3r, orc, fmt, mode, ec):
     T, d, F, S = 256, 128, 384, 128
     inp = workloads.ffn_inputs(T, d, F, S, seed=11)
-    ops_g = _device_ops(s3r, inp)
+    ops_g = _device_ops(s3r, inp, fmt)
     ops_o = _oracle_ops(orc, inp)
     _forward_ops_bit_exact(ops_g, ops_o)
     rm, ecm = getattr(s3r, "ROUND_" + mode), getattr(s3r, ec)
@@ -127,7 +136,7 @@ def test_ffn_staged_matches_oracle(s3r, orc, mode, ec):
     ref = orc.ffn_backward(ops_o, h1, h3, dY, S, mode=omode, ec_mode=oec, seed=seed)
     ecx = oec if omode == orc.S3R else orc.EC_NONE
     # stage 1: codes exact, dA and dW2 within the fp32 bound
-    assert np.array_equal(gpu["q2"].Q.cpu().numpy(), ref.w2.Q)
+    assert np.array_equal(codes(gpu["q2"].Q), ref.w2.Q)
     w2 = ref.w2
     mdx = dx_magnitude(w2.Q, w2.delta, ops_o.W2_8, ops_o.s_a,
                        *( (w2.eps, w2.rowsum, w2.v, S) if ecx else (None, None, None, None)))
@@ -145,7 +154,7 @@ def test_ffn_staged_matches_oracle(s3r, orc, mode, ec):
     for name, lb, dh, W8, s_w, tid in (("dW1", ref.w1, ref.dh1, ops_o.W1_8, ops_o.s_w1, orc.TID_W1),
                                        ("dW3", ref.w3, ref.dh3, ops_o.W3_8, ops_o.s_w3, orc.TID_W3)):
         q = gpu["q1" if name == "dW1" else "q3"]
-        Qg, dg = q.Q.cpu().numpy(), q.tile_scale.cpu().numpy()
+        Qg, dg = codes(q.Q), q.tile_scale.cpu().numpy()
         g = (ops_o.s_x[:, None] * dh) * s_w[None, :]
         amax = np.abs(g).reshape(T // 128, 128, -1, 128).max(axis=(1, 3)) if F % 128 == 0 else None
         y = g * expand_tiles(np.float32(127.0) / amax, T, F).astype(np.float32)
@@ -155,7 +164,7 @@ def test_ffn_staged_matches_oracle(s3r, orc, mode, ec):
         exp_dX += ddx
         if omode == orc.INDEP:
             qr = gpu["q1r" if name == "dW1" else "q3r"]
-            Qr, dr = qr.Q.cpu().numpy(), qr.tile_scale.cpu().numpy()
+            Qr, dr = codes(qr.Q), qr.tile_scale.cpu().numpy()
             near_tie_flips(Qr, lb.Q_rhs, y, _thresholds(orc, mode, T, F, seed, tid + orc.RHS_ID_OFFSET))
             Dr = expand_tiles(dr, T, F) * Qr - expand_tiles(lb.delta_rhs, T, F) * lb.Q_rhs
             _, ddw = _flip_effect(Dr, W8, ops_o.X8, ops_o.s_x, s_w, S, ecx, orc)
@@ -185,8 +194,8 @@ def test_ffn_full_size_block(s3r, orc):
     for k in ("dX", "dW1", "dW3", "dW2"):
         assert torch.isfinite(getattr(g, k)).all(), k
     # stage 1 exact on sampled rows of dW2 (oracle)
-    A8, s_a = ops.A8.cpu().numpy(), ops.s_a.cpu().numpy()
-    W8, s_w2 = ops.W2_8.cpu().numpy(), ops.s_w2.cpu().numpy()
+    A8, s_a = codes(ops.A8), ops.s_a.cpu().numpy()
+    W8, s_w2 = codes(ops.W2_8), ops.s_w2.cpu().numpy()
     krows = np.array([0, 17, 2900, F - 1])
     ref = orc.linear_backward(orc.from_torch_bf16(inp.dY), A8, s_a, W8, s_w2, S, mode=orc.S3R,
                               ec_mode=orc.EC_TWO_WAY, seed=0, tensor_id=orc.TID_W2, rows=np.array([0, T - 1]),
@@ -194,7 +203,7 @@ def test_ffn_full_size_block(s3r, orc):
     mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w2, ref.colmean, ref.mu, ref.xsum, ref.p, krows=krows)
     assert_close_mag(g.dW2.cpu().numpy()[krows], ref.dW, mdw, "dW2 rows")
     # every gradient within quantization noise of fp64 autograd (sampled rows)
-    f64 = lambda q, s, ax: q.double() * s.double().unsqueeze(1 - ax)
+    f64 = lambda q, s, ax: q.double() * s.double().unsqueeze(1 - ax)   # fp16/int8 codes are exact in fp64
     Xd, Ad = f64(ops.X8.cpu(), ops.s_x.cpu(), 0), f64(ops.A8.cpu(), ops.s_a.cpu(), 0)
     W1d, W3d = f64(ops.W1_8.cpu(), ops.s_w1.cpu(), 1), f64(ops.W3_8.cpu(), ops.s_w3.cpu(), 1)
     W2d = f64(ops.W2_8.cpu(), ops.s_w2.cpu(), 1)

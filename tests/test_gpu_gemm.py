@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import workloads
-from parity_util import assert_close_mag, dw_magnitude, dx_magnitude
+from parity_util import assert_close_mag, codes, dw_magnitude, dx_magnitude
 
 pytestmark = pytest.mark.gpu
 
@@ -22,24 +22,41 @@ def s3r():
     return m
 
 
+FMTS = pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
+
+
 def _i8(rng, *shape):
     return rng.integers(-127, 128, size=shape).astype(np.int8)
 
 
-@pytest.mark.parametrize("T,N,K", [(256, 1024, 512), (130, 136, 70), (1, 16, 1), (300, 384, 257), (64, 1000, 33)])
-def test_dx_blocks_bit_exact(s3r, orc, T, N, K):
+def _dev(a, fmt):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return (t.to(torch.float16) if fmt else t).cuda()
+
+
+@FMTS
+@pytest.mark.parametrize("T,N,K", [(256, 1024, 512), (130, 136, 70), (1, 16, 1), (300, 384, 257), (64, 1000, 33),
+                                   (129, 4096, 300)])
+def test_dx_blocks_bit_exact(s3r, orc, fmt, T, N, K):
     rng = np.random.default_rng(T * N + K)
     Q, W8 = _i8(rng, T, N), _i8(rng, K, N)
-    got = s3r.debug_dx_blocks(torch.from_numpy(Q).cuda(), torch.from_numpy(W8).cuda()).cpu().numpy()
+    Q[0, :] = 127
+    W8[0, :] = 127          # the largest block sum, 128 * 127^2
+    W8[-1, :] = -127
+    got = s3r.debug_dx_blocks(_dev(Q, fmt), _dev(W8, fmt)).cpu().numpy()
     ref = orc.dx_blocks(Q, W8, np.arange(T))
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("T,K,N", [(256, 512, 1024), (130, 70, 136), (1, 1, 16), (300, 257, 384), (1000, 33, 64)])
-def test_dw_blocks_bit_exact(s3r, orc, T, K, N):
+@FMTS
+@pytest.mark.parametrize("T,K,N", [(256, 512, 1024), (130, 72, 136), (1, 8, 16), (300, 256, 384), (1000, 40, 64),
+                                   (4096, 136, 200)])
+def test_dw_blocks_bit_exact(s3r, orc, fmt, T, K, N):
     rng = np.random.default_rng(T + 3 * N + K)
     X8, Q = _i8(rng, T, K), _i8(rng, T, N)
-    got = s3r.debug_dw_blocks(torch.from_numpy(X8).cuda(), torch.from_numpy(Q).cuda()).cpu().numpy()
+    X8[:, 0] = -127
+    Q[:, 0] = 127
+    got = s3r.debug_dw_blocks(_dev(X8, fmt), _dev(Q, fmt)).cpu().numpy()
     ref = orc.dw_blocks(X8, Q, np.arange(K))
     assert np.array_equal(got, ref)
 
@@ -52,21 +69,22 @@ def _linear(orc, T, K, N, S, seed):
     return inp, G, X8, s_x, W8, s_w
 
 
+@FMTS
 @pytest.mark.parametrize("ec_name", ["EC_NONE", "EC_DX_ONLY", "EC_TWO_WAY"])
-@pytest.mark.parametrize("T,K,N,S", [(256, 512, 1024, 256), (512, 200, 384, 128), (300, 136, 260, 300)])
-def test_linear_backward_parity(s3r, orc, ec_name, T, K, N, S):
+@pytest.mark.parametrize("T,K,N,S", [(256, 512, 1024, 256), (512, 200, 384, 128), (300, 136, 264, 300)])
+def test_linear_backward_parity(s3r, orc, fmt, ec_name, T, K, N, S):
     """dX and dW of one linear layer (the tiny-linear workload and ragged
     variants) through quantize -> correction -> both GEMMs."""
     inp, G, X8, s_x, W8, s_w = _linear(orc, T, K, N, S, seed=T + K + N)
     ec_mode = getattr(orc, ec_name)
     ref = orc.linear_backward(G, X8, s_x, W8, s_w, S, mode=orc.S3R, ec_mode=ec_mode, seed=11, tensor_id=0)
     c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    q = s3r.s3r_quantize(inp.dY.cuda(), c(s_x), c(s_w), seed=11, tensor_id=0)
-    ec = s3r.s3r_ec_correct(q, T, N, S, c(W8), c(X8), ec_mode=ec_mode) if ec_mode else None
-    dX = s3r.int8_gemm_dx(q.Q, q.tile_scale, c(W8), c(s_x), ec_mode, ec, S)
-    dW = s3r.int8_gemm_dw(c(X8), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
+    q = s3r.s3r_quantize(inp.dY.cuda(), c(s_x), c(s_w), seed=11, tensor_id=0, code_format=fmt)
+    ec = s3r.s3r_ec_correct(q, T, N, S, _dev(W8, fmt), _dev(X8, fmt), ec_mode=ec_mode) if ec_mode else None
+    dX = s3r.int8_gemm_dx(q.Q, q.tile_scale, _dev(W8, fmt), c(s_x), ec_mode, ec, S)
+    dW = s3r.int8_gemm_dw(_dev(X8, fmt), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
     torch.cuda.synchronize()
-    assert np.array_equal(q.Q.cpu().numpy(), ref.Q)
+    assert np.array_equal(codes(q.Q), ref.Q)
     if ec_mode:
         mdx = dx_magnitude(ref.Q, ref.delta, W8, s_x, ref.eps, ref.rowsum, ref.v, S)
     else:
@@ -79,7 +97,8 @@ def test_linear_backward_parity(s3r, orc, ec_name, T, K, N, S):
     assert_close_mag(dW.cpu().numpy(), ref.dW, mdw, "dW")
 
 
-def test_dx_accumulate(s3r, orc):
+@FMTS
+def test_dx_accumulate(s3r, orc, fmt):
     rng = np.random.default_rng(1)
     T, N, K = 256, 256, 128
     Q, W8 = _i8(rng, T, N), _i8(rng, K, N)
@@ -87,14 +106,14 @@ def test_dx_accumulate(s3r, orc):
     c = lambda a: torch.from_numpy(a).cuda()
     base = torch.randn(T, K, device="cuda")
     out = base.clone()
-    s3r.int8_gemm_dx(c(Q), c(sc), c(W8), dX=out, accumulate=True)
-    fresh = s3r.int8_gemm_dx(c(Q), c(sc), c(W8))
+    s3r.int8_gemm_dx(_dev(Q, fmt), c(sc), _dev(W8, fmt), dX=out, accumulate=True)
+    fresh = s3r.int8_gemm_dx(_dev(Q, fmt), c(sc), _dev(W8, fmt))
     torch.cuda.synchronize()
     assert torch.allclose(out, base + fresh, rtol=1e-6, atol=1e-6)
 
 
-@pytest.mark.parametrize("ec_name", ["EC_DX_ONLY", "EC_TWO_WAY"])
-def test_ffn_w2_gemms_full_size_sampled(s3r, orc, ec_name):
+@pytest.mark.parametrize("fmt,ec_name", [(1, "EC_DX_ONLY"), (1, "EC_TWO_WAY"), (0, "EC_TWO_WAY")])
+def test_ffn_w2_gemms_full_size_sampled(s3r, orc, fmt, ec_name):
     """The W2 linear of the d=2048, F=5632, T=8192 (4 x 2048) SwiGLU block at
     full size: dA = dX of W2 [8192, 5632] and dW2 [5632, 2048] in the launch
     configuration the benchmark times, checked on 48 sampled rows each."""
@@ -112,12 +131,12 @@ def test_ffn_w2_gemms_full_size_sampled(s3r, orc, ec_name):
     ref = orc.linear_backward(G, A8, s_a, W8, s_w, S, mode=orc.S3R, ec_mode=ec_mode, seed=0, tensor_id=0,
                               rows=rows, krows=krows)
     c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    q = s3r.s3r_quantize(inp.dY.cuda(), c(s_a), c(s_w), seed=0, tensor_id=0)
-    ec = s3r.s3r_ec_correct(q, T, d, S, c(W8), c(A8), ec_mode=ec_mode)
-    dA = s3r.int8_gemm_dx(q.Q, q.tile_scale, c(W8), c(s_a), ec_mode, ec, S)
-    dW = s3r.int8_gemm_dw(c(A8), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
+    q = s3r.s3r_quantize(inp.dY.cuda(), c(s_a), c(s_w), seed=0, tensor_id=0, code_format=fmt)
+    ec = s3r.s3r_ec_correct(q, T, d, S, _dev(W8, fmt), _dev(A8, fmt), ec_mode=ec_mode)
+    dA = s3r.int8_gemm_dx(q.Q, q.tile_scale, _dev(W8, fmt), c(s_a), ec_mode, ec, S)
+    dW = s3r.int8_gemm_dw(_dev(A8, fmt), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
     torch.cuda.synchronize()
-    assert np.array_equal(q.Q.cpu().numpy(), ref.Q)
+    assert np.array_equal(codes(q.Q), ref.Q)
     mdx = dx_magnitude(ref.Q, ref.delta, W8, s_a, ref.eps, ref.rowsum, ref.v, S, rows=rows)
     assert_close_mag(dA.cpu().numpy()[rows], ref.dX, mdx, "dA rows")
     if ec_mode == orc.EC_TWO_WAY:

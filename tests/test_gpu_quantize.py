@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads
-from parity_util import assert_close_mag
+from parity_util import assert_close_mag, codes
 
 pytestmark = pytest.mark.gpu
 
@@ -23,14 +23,14 @@ def s3r():
     return m
 
 
-def _gpu_quant(s3r, mode, G, s_x, s_w, seed, tid):
+def _gpu_quant(s3r, mode, G, s_x, s_w, seed, tid, fmt=1):
     if mode == "S3R":
-        o = s3r.s3r_quantize(G, s_x, s_w, seed, tid)
+        o = s3r.s3r_quantize(G, s_x, s_w, seed, tid, code_format=fmt)
         return o.Q, o.tile_scale, o.tok_err_part, o.col_err_part
     if mode == "INDEP":
-        o = s3r.indep_sr_quantize(G, s_x, s_w, seed, tid)
+        o = s3r.indep_sr_quantize(G, s_x, s_w, seed, tid, code_format=fmt)
         return o.Q, o.tile_scale, None, None
-    Q, sc = s3r.rtne_quantize(G, s3r.AXIS_TILE, s_x=s_x, s_w=s_w)
+    Q, sc = s3r.rtne_quantize(G, s3r.AXIS_TILE, s_x=s_x, s_w=s_w, code_format=fmt)
     return Q, sc, None, None
 
 
@@ -49,23 +49,25 @@ def _case(T, N, seed, ld=None, outliers=False):
     return Gb, s_x, s_w
 
 
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("T,N,ld,fold", [(256, 1024, None, True), (300, 260, None, True), (1, 8, None, False),
                                          (129, 136, None, True), (200, 1001, 1001, True), (130, 96, 128, False),
                                          (513, 384, None, True)])
-def test_quantize_parity(s3r, orc, mode, T, N, ld, fold):
+def test_quantize_parity(s3r, orc, fmt, mode, T, N, ld, fold):
     Gb, s_x, s_w = _case(T, N, T * 7 + N, ld)
     dev = "cuda"
     Gd = Gb.to(dev) if ld is None else torch.zeros((T, ld), dtype=torch.bfloat16, device=dev)[:, :N].copy_(Gb.to(dev))
     sxd, swd = (s_x.to(dev), s_w.to(dev)) if fold else (None, None)
     seed, tid = 1234567, 5
-    Q, sc, tok, col = _gpu_quant(s3r, mode, Gd, sxd, swd, seed, tid)
+    Q, sc, tok, col = _gpu_quant(s3r, mode, Gd, sxd, swd, seed, tid, fmt)
     torch.cuda.synchronize()
     G = orc.from_torch_bf16(Gb.contiguous())
     Qo, do, Eo, st = orc.quantize(G, s_x.numpy() if fold else None, s_w.numpy() if fold else None,
                                   mode=getattr(orc, mode), seed=seed, tensor_id=tid)
     assert st == 0
-    assert np.array_equal(Q.cpu().numpy(), Qo), f"codes differ in {(Q.cpu().numpy() != Qo).sum()} elements"
+    Qg = codes(Q)
+    assert np.array_equal(Qg, Qo), f"codes differ in {(Qg != Qo).sum()} elements"
     assert np.array_equal(sc.cpu().numpy(), do)
     if tok is not None:
         tok_o, col_o = orc.error_partials(Eo)
@@ -85,8 +87,8 @@ def test_quantize_sweep_full_size_sampled(s3r, orc, T):
     windows = [(0, 0), ((T // 128 - 1) * 128, N - 512)]
     windows += [(int(rng.integers(0, T // 128)) * 128, int(rng.integers(0, N // 128 - 4)) * 128) for _ in range(2)]
     for mode in MODES:
-        Q, sc, tok, col = _gpu_quant(s3r, mode, Gd, None, None, 77, 3)
-        Q, sc = Q.cpu().numpy(), sc.cpu().numpy()
+        Q, sc, tok, col = _gpu_quant(s3r, mode, Gd, None, None, 77, 3, fmt=(T // 4096) % 2)
+        Q, sc = codes(Q), sc.cpu().numpy()
         tok = tok.cpu().numpy() if tok is not None else None
         for (r0, c0) in windows:
             Gw = orc.from_torch_bf16(Gb[r0:r0 + 128, c0:c0 + 512].contiguous())
@@ -103,6 +105,8 @@ def test_quantize_deterministic_and_seed_sensitive(s3r):
     Gb, s_x, s_w = _case(384, 512, 9)
     G = Gb.cuda()
     a = s3r.s3r_quantize(G, seed=1, tensor_id=0).Q.clone()
+    a8 = s3r.s3r_quantize(G, seed=1, tensor_id=0, code_format=s3r.CODES_S8).Q
+    assert np.array_equal(codes(a), codes(a8))
     b = s3r.s3r_quantize(G, seed=1, tensor_id=0).Q
     c = s3r.s3r_quantize(G, seed=2, tensor_id=0).Q
     d = s3r.s3r_quantize(G, seed=1, tensor_id=1).Q
@@ -119,7 +123,7 @@ def test_nonfinite_sets_device_status(s3r):
     assert int(st.item()) == -4
     sc = o.tile_scale.cpu()
     assert torch.isnan(sc[0, 1]) and torch.isfinite(sc[0, 0]) and torch.isfinite(sc[1]).all()
-    assert not o.Q[:128, 128:].any()
+    assert not codes(o.Q)[:128, 128:].any()
     with pytest.raises(s3r.S3RError):
         s3r.check_status(st)
 
@@ -130,7 +134,8 @@ def test_zero_tile(s3r):
     o = s3r.s3r_quantize(G)
     sc = o.tile_scale.cpu()
     assert sc[0, 0] == 0 and sc[1, 2] == np.float32(1.0) / np.float32(127.0)
-    assert int(o.Q[150, 290]) == 127 and int(o.Q.abs().sum()) == 127
+    q = codes(o.Q).astype(np.int64)
+    assert q[150, 290] == 127 and np.abs(q).sum() == 127
     tok = o.tok_err_part.cpu().numpy()
     # all-zero tiles carry no error; the lone element's error is Delta*127 - 1 (Delta is rounded)
     want = np.float32(np.float32(1.0) / np.float32(127.0)) * np.float64(127.0) - 1.0

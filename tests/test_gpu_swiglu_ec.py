@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import assert_close_mag
+from parity_util import assert_close_mag, codes
 
 pytestmark = pytest.mark.gpu
 
@@ -26,19 +26,20 @@ def _swiglu_case(T, F, seed):
     return dA, h1, h3, s_x, s_w1, s_w3
 
 
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("mode", ["S3R", "INDEP", "RTNE"])
 @pytest.mark.parametrize("T,F", [(256, 384), (300, 200), (129, 1000), (64, 8)])
-def test_swiglu_quantize_parity(s3r, orc, mode, T, F):
+def test_swiglu_quantize_parity(s3r, orc, fmt, mode, T, F):
     dA, h1, h3, s_x, s_w1, s_w3 = _swiglu_case(T, F, T + F)
     c = lambda a: torch.from_numpy(a).cuda()
     o1, o3 = s3r.swiglu_quantize(c(dA), h1.cuda(), h3.cuda(), c(s_x), c(s_w1), c(s_w3),
-                                 round_mode=getattr(s3r, "ROUND_" + mode), seed=42, tid1=1, tid3=2)
+                                 round_mode=getattr(s3r, "ROUND_" + mode), seed=42, tid1=1, tid3=2, code_format=fmt)
     torch.cuda.synchronize()
     dh1, dh3 = orc.swiglu_bwd(dA, orc.from_torch_bf16(h1), orc.from_torch_bf16(h3))
     for o, g, s_w, tid in ((o1, dh1, s_w1, 1), (o3, dh3, s_w3, 2)):
         Qo, do, Eo, st = orc.quantize(g, s_x, s_w, mode=getattr(orc, mode), seed=42, tensor_id=tid)
         assert st == 0
-        Qg = o.Q.cpu().numpy()
+        Qg = codes(o.Q)
         assert np.array_equal(Qg, Qo), f"{mode} tid {tid}: {(Qg != Qo).sum()} codes differ"
         assert np.array_equal(o.tile_scale.cpu().numpy(), do)
         if mode == "S3R":
@@ -48,17 +49,19 @@ def test_swiglu_quantize_parity(s3r, orc, mode, T, F):
             assert_close_mag(o.col_err_part.cpu().numpy(), c_o, c_m, "col")
 
 
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("ec_mode", ["EC_DX_ONLY", "EC_TWO_WAY"])
 @pytest.mark.parametrize("T,N,K,S", [(256, 1024, 512, 256), (512, 384, 200, 128), (300, 260, 72, 300),
                                      (1024, 256, 130, 256)])
-def test_ec_factors_parity(s3r, orc, ec_mode, T, N, K, S):
+def test_ec_factors_parity(s3r, orc, fmt, ec_mode, T, N, K, S):
     rng = np.random.default_rng(T + N + K)
     G = (rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)
     Gb = torch.from_numpy(G).to(torch.bfloat16)
     W8 = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
     X8 = rng.integers(-127, 128, size=(T, K)).astype(np.int8)
-    q = s3r.s3r_quantize(Gb.cuda(), seed=3, tensor_id=9)
-    ec = s3r.s3r_ec_correct(q, T, N, S, torch.from_numpy(W8).cuda(), torch.from_numpy(X8).cuda(),
+    dt = torch.float16 if fmt else torch.int8
+    q = s3r.s3r_quantize(Gb.cuda(), seed=3, tensor_id=9, code_format=fmt)
+    ec = s3r.s3r_ec_correct(q, T, N, S, torch.from_numpy(W8).to(dt).cuda(), torch.from_numpy(X8).to(dt).cuda(),
                             ec_mode=getattr(s3r, ec_mode))
     torch.cuda.synchronize()
     Qo, do, Eo, _ = orc.quantize(orc.from_torch_bf16(Gb), seed=3, tensor_id=9)
