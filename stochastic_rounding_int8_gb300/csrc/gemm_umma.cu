@@ -288,7 +288,9 @@ __global__ void __maxnreg__(200)
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
             const int buf = kb & 1;
-            if (!mbar_wait(tfull0 + 8 * buf, (uint32_t)(kb >> 1) & 1u, abrt)) {
+            // warp-uniform outcome: the tcgen05.ld below needs the whole warp
+            const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * buf, (uint32_t)(kb >> 1) & 1u, abrt));
+            if (!got) {
                 ok = false;
                 *abrt = 1;
                 break;
