@@ -103,6 +103,11 @@ int s3r_abi_version(void);
  * count, for measurement). */
 uint64_t s3r_kernel_launch_count(void);
 
+/* Description of the last failure this thread saw (which call, and the CUDA
+ * error or the tensor-map encoder's result); "" when none.  Static per-thread
+ * storage, valid until the thread's next failing call. */
+const char* s3r_last_error(void);
+
 /*
  * s3r_quantize -- S3R quantization of the upstream gradient, written once for
  * both backward products ([S3R] §III-A eq. (2) "fold and quantize once",

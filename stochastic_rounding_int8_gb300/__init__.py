@@ -47,6 +47,7 @@ _SIGS = {
     "s3r_status_string": (C.c_char_p, [_INT]),
     "s3r_abi_version": (_INT, []),
     "s3r_kernel_launch_count": (C.c_uint64, []),
+    "s3r_last_error": (C.c_char_p, []),
     "s3r_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _INT, _VP, _VP, _VP, _VP, _VP]),
     "indep_sr_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _INT, _VP, _VP, _VP]),
     "rtne_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _INT, _VP, _VP, _VP]),
@@ -105,7 +106,8 @@ def status_string(code: int) -> str:
 
 def _check(code: int, what: str):
     if code != S3R_OK:
-        raise S3RError(f"{what}: {status_string(code)}")
+        detail = lib().s3r_last_error().decode()
+        raise S3RError(f"{what}: {status_string(code)}" + (f" [{detail}]" if detail else ""))
 
 
 def _ptr(t):

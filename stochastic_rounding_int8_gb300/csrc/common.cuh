@@ -91,16 +91,22 @@ __device__ __forceinline__ void set_status(int* d_status, int code) {
 }  // namespace s3r
 
 // Host-side helpers.  Every kernel launch is followed by S3R_CHECK_LAUNCH(),
-// which also counts it (s3r_kernel_launch_count()).
+// which also counts it (s3r_kernel_launch_count()).  Failures are described
+// in a thread-local message (s3r_last_error()).
 void s3r_count_launch();
-#define S3R_CHECK_LAUNCH()                                 \
-    do {                                                   \
-        s3r_count_launch();                                \
-        if (cudaPeekAtLastError() != cudaSuccess) {        \
-            (void)cudaGetLastError();                      \
-            return S3R_ERR_CUDA;                           \
-        }                                                  \
+void s3r_record_error(const char* where, const char* what);
+int s3r_cuda_fail(const char* where, cudaError_t err);
+#define S3R_CHECK_LAUNCH()                                               \
+    do {                                                                 \
+        s3r_count_launch();                                              \
+        cudaError_t _e = cudaPeekAtLastError();                          \
+        if (_e != cudaSuccess) {                                         \
+            (void)cudaGetLastError();                                    \
+            return s3r_cuda_fail(__FILE__ ":" S3R_STR(__LINE__), _e);    \
+        }                                                                \
     } while (0)
+#define S3R_STR2(x) #x
+#define S3R_STR(x) S3R_STR2(x)
 
 static inline bool s3r_aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }
 __host__ __device__ static inline int64_t s3r_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }

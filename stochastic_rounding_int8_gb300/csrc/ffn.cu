@@ -9,9 +9,23 @@
 
 #include "common.cuh"
 
+#include <cstdio>
+
 static std::atomic<uint64_t> g_launches{0};
 void s3r_count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 extern "C" uint64_t s3r_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+static thread_local char g_last_error[512] = "";
+void s3r_record_error(const char* where, const char* what) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, what);
+}
+int s3r_cuda_fail(const char* where, cudaError_t err) {
+    char buf[400];
+    std::snprintf(buf, sizeof(buf), "%s (%s)", cudaGetErrorName(err), cudaGetErrorString(err));
+    s3r_record_error(where, buf);
+    return S3R_ERR_CUDA;
+}
+extern "C" const char* s3r_last_error(void) { return g_last_error; }
 
 namespace {
 
@@ -126,9 +140,12 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     const bool indep = rm == S3R_ROUND_INDEP;
     int* st = a->d_status;
     auto mark = [&](int i) -> int {
-        if (a->step_events && cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return S3R_ERR_CUDA;
+        if (a->step_events) {
+            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream);
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                return s3r_cuda_fail("ffn_backward step event", e);
+            }
         }
         return S3R_OK;
     };

@@ -251,8 +251,8 @@ static int ensure_gemm_smem() {
             cudaSuccess ||
         cudaFuncSetAttribute(gemm_tn_s8_kernel<kEpiDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
             cudaSuccess) {
-        (void)cudaGetLastError();
-        return S3R_ERR_CUDA;
+        cudaError_t e = cudaGetLastError();
+        return s3r_cuda_fail("mma.sync gemm: cudaFuncSetAttribute", e);
     }
     gemm_smem_ready = true;
     return S3R_OK;

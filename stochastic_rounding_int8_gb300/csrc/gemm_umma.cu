@@ -26,6 +26,8 @@
 // W [K,N] contract over N); dW reads MN-major operands (X [T,K] and Q [T,N]
 // contract over T), which the UMMA descriptors address directly.
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
+#include <cstdio>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -146,20 +148,20 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 TMEM lanes x 16 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 10 warps: one SM sub-partition hosts three of them, so 16384 / (3 * 32) caps
+// the kernel at 168 registers per thread.
 template <int EPI, bool MN>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Args P) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
@@ -299,22 +301,22 @@ __global__ void __maxnreg__(200)
             float sc = 0.0f;
             if (EPI != kDump && nt < P.nt_limit) sc = __ldg(P.scale + mt * P.sm + nt * P.sn + (int64_t)kb * P.sk);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + (uint32_t)(buf * BN + 32 * c), r);
+            for (int c = 0; c < 8; ++c) {
+                uint32_t r[16];
+                tmem_ld16(lane_addr + (uint32_t)(buf * BN + 16 * c), r);
                 tmem_wait_ld();
                 if (EPI == kDump) {
                     if (row < P.M) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int64_t col = c0 + 32 * c + j;
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t col = c0 + 16 * c + j;
                             if (col < P.N)
                                 P.dump[(row * P.N + col) * nkb + kb] = __float2int_rn(__uint_as_float(r[j]));
                         }
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(sc, __uint_as_float(r[j]), acc[32 * c + j]);
+                    for (int j = 0; j < 16; ++j) acc[16 * c + j] = fmaf(sc, __uint_as_float(r[j]), acc[16 * c + j]);
                 }
             }
             tc_before();
@@ -376,13 +378,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && p) {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
+        } else {
             (void)cudaGetLastError();
+            char buf[160];
+            snprintf(buf, sizeof(buf), "cudaGetDriverEntryPointByVersion: %s, query result %d", cudaGetErrorName(e),
+                     (int)q);
+            s3r_record_error("tensor map encoder", buf);
+        }
     }
     return fn;
 }
@@ -399,17 +405,25 @@ static int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t out
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? S3R_OK : S3R_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        char buf[200];
+        snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled returned %d (dims %lld x %lld, box 64 x %u)", (int)r,
+                 (long long)inner, (long long)outer, box_outer);
+        s3r_record_error("tensor map", buf);
+        return S3R_ERR_CUDA;
+    }
+    return S3R_OK;
 }
 
 template <int EPI, bool MN>
 static int launch(const CUtensorMap& a, const CUtensorMap& b, const Args& P, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(umma_gemm_kernel<EPI, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess) {
+        cudaError_t e =
+            cudaFuncSetAttribute(umma_gemm_kernel<EPI, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) {
             (void)cudaGetLastError();
-            return S3R_ERR_CUDA;
+            return s3r_cuda_fail("umma gemm: cudaFuncSetAttribute", e);
         }
         attr = true;
     }
