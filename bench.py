@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "swiglu", "ec", "ffn"],
+                    help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
     return ap.parse_args()
 
 
@@ -327,7 +329,7 @@ def run_ours(args, world, rank, local):
     # per-step segments -> dominant kernel class
     segm = seg.mean(0)
     names = s3r.FFN_STEPS
-    classes = {"int8_gemm_dx": (segm[2] + segm[6], 3), "int8_gemm_dw (incl. operand transposes)": (segm[3] + segm[7], 3),
+    classes = {"int8_gemm_dx": (segm[2] + segm[6], 3), "int8_gemm_dw": (segm[3] + segm[7], 3),
                "quantize (dY + SwiGLU-fused)": (segm[0] + segm[4], 2), "s3r_ec_correct": (segm[1] + segm[5], 3)}
     dom = max(classes, key=lambda k: classes[k][0])
     dom_ms, dom_n = classes[dom]
@@ -388,6 +390,37 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def run_kernel_case(args):
+    """Launch one kernel class of the benchmark's FFN block (the W2 / W1 linear
+    shapes) --steps times after --warmup, for ncu captures; prints its time."""
+    import stochastic_rounding_int8_gb300 as s3r
+    s3r.lib()
+    inp, ops = device_setup(s3r, 0)
+    dY = inp.dY.cuda()
+    q2 = s3r.s3r_quantize(dY, ops.s_a, ops.s_w2)
+    ec2 = s3r.s3r_ec_correct(q2, T, D, S, ops.W2_8, ops.A8, s3r.EC_TWO_WAY)
+    dA = s3r.int8_gemm_dx(q2.Q, q2.tile_scale, ops.W2_8, ops.s_a, s3r.EC_TWO_WAY, ec2, S)
+    fns = {
+        "gemm_dx": lambda: s3r.int8_gemm_dx(q2.Q, q2.tile_scale, ops.W2_8, ops.s_a, s3r.EC_TWO_WAY, ec2, S, dX=dA),
+        "gemm_dw": lambda: s3r.int8_gemm_dw(ops.A8, q2.Q, q2.tile_scale, ops.s_w2, s3r.EC_TWO_WAY, ec2, S),
+        "quantize": lambda: s3r.s3r_quantize(dY, ops.s_a, ops.s_w2, out=q2),
+        "swiglu": lambda: s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3),
+        "ec": lambda: s3r.s3r_ec_correct(q2, T, D, S, ops.W2_8, ops.A8, s3r.EC_TWO_WAY),
+        "ffn": lambda: s3r.ffn_backward(ops, dY, S),
+    }
+    fn = fns[args.kernel_case]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        fn()
+    t1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel_case": args.kernel_case, "ms_per_call": round(t0.elapsed_time(t1) / args.steps, 4)}))
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: each step a bounded sample (8 tokens of
     the d=2048, F=5632 block, ~1-3 s) on the host cores."""
@@ -420,6 +453,9 @@ def run_reference(args, world, rank):
 def main():
     args = parse()
     world, rank, local = dist_setup(args.gpus)
+    if args.kernel_case:
+        run_kernel_case(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, world, rank)
     else:
