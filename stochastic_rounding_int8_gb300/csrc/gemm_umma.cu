@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------
-        const int q = warp & 3, half = (warp - 2) >> 2;
+        const int q = warp & 3, half = (warp - 2) >> 2, ew = warp - 2;
         const int64_t row = m0 + 32 * q + lane;
         const int64_t c0 = n0 + 128 * half;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * half);
@@ -287,9 +287,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
         const int64_t mt = m0 / 128, nt = n0 / 128 + half;
+        const bool has_scale = EPI != kDump && nt < P.nt_limit;
+        const float* scale_ptr = has_scale ? P.scale + mt * P.sm + nt * P.sn : nullptr;
+        float sc_next = (has_scale && nkb > 0) ? __ldg(scale_ptr) : 0.0f;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
             const int buf = kb & 1;
+            const float sc = sc_next;   // loaded one block ahead
+            if (has_scale && kb + 1 < nkb) sc_next = __ldg(scale_ptr + (int64_t)(kb + 1) * P.sk);
             // warp-uniform outcome: the tcgen05.ld below needs the whole warp
             const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * buf, (uint32_t)(kb >> 1) & 1u, abrt));
             if (!got) {
@@ -298,8 +303,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_after();
-            float sc = 0.0f;
-            if (EPI != kDump && nt < P.nt_limit) sc = __ldg(P.scale + mt * P.sm + nt * P.sn + (int64_t)kb * P.sk);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t r[16];
@@ -323,42 +326,91 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
         }
-        if (EPI != kDump && ok && row < P.M) {
-            if (EPI == kDX) {
-                const float ep = P.ec_mode ? P.eps[row] : 0.0f;
-                const float* vrow = P.ec_mode ? P.v + (row / P.S) * P.N : nullptr;
-                const float sr = P.s_row ? P.s_row[row] : 1.0f;
-                float* dst = P.C + row * P.ldc;
+        if (EPI != kDump && ok) {
+            // The last accumulator commit retired every MMA, so the operand ring is
+            // free: stage this warp's 32 x 128 fp32 block there (row pitch 132
+            // floats keeps both the row writes and the column reads conflict-free),
+            // then finish row by row with 16-byte coalesced accesses.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            float* stage = reinterpret_cast<float*>(smem) + ew * (32 * 132);
+            float* mine = stage + lane * 132;
 #pragma unroll
-                for (int j = 0; j < 128; ++j) {
-                    const int64_t col = c0 + j;
-                    if (col < P.N) {
-                        float out = acc[j];
-                        if (P.ec_mode) out = out - fmaf(ep, (float)__ldg(P.rowsum + col), __ldg(vrow + col));
-                        if (P.s_row) out = out / sr;
-                        if (P.accumulate) out = out + dst[col];
-                        dst[col] = out;
-                    }
+            for (int c = 0; c < 32; ++c)
+                *reinterpret_cast<float4*>(mine + 4 * c) =
+                    make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+            __syncwarp();
+            const int64_t col = c0 + 4 * lane;   // this thread's 4 columns
+            const bool vec = (P.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(P.C) & 15u) == 0) && col + 4 <= P.N;
+            float cterm[4] = {0.f, 0.f, 0.f, 0.f}, cscale[4] = {1.f, 1.f, 1.f, 1.f};
+            if (EPI == kDX) {
+                // every row of this tile lies in one example (S % 128 == 0 or one example)
+                if (P.ec_mode) {
+                    const int64_t b = m0 / P.S;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col + j < P.N) {
+                            cterm[j] = __ldg(P.v + b * P.N + col + j);   // v[b, col]
+                            cscale[j] = (float)__ldg(P.rowsum + col + j);
+                        }
                 }
             } else {
-                float* dst = P.C + row * P.ldc;
-                const bool two = P.ec_mode == S3R_EC_TWO_WAY;
-                const float pr = two ? P.p[row] : 0.0f;
 #pragma unroll
-                for (int j = 0; j < 128; ++j) {
-                    const int64_t col = c0 + j;
-                    if (col < P.N) {
-                        float out = acc[j];
-                        if (two) {
-                            float corr = pr;
-                            for (int64_t b = 0; b < P.B; ++b)
-                                corr = fmaf((float)P.xsum[b * P.M + row],
-                                            __ldg(P.colmean + b * P.N + col) - __ldg(P.mu + b), corr);
-                            out = out - corr;
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < P.N && P.s_col) cscale[j] = __ldg(P.s_col + col + j);
+            }
+            for (int r = 0; r < 32; ++r) {
+                const int64_t grow = m0 + 32 * q + r;
+                if (grow >= P.M) break;
+                const float4 a4 = *reinterpret_cast<const float4*>(stage + r * 132 + 4 * lane);
+                float o[4] = {a4.x, a4.y, a4.z, a4.w};
+                float* dst = P.C + grow * P.ldc + col;
+                if (EPI == kDX) {
+                    const float ep = P.ec_mode ? __ldg(P.eps + grow) : 0.0f;
+                    const float sr = P.s_row ? __ldg(P.s_row + grow) : 1.0f;
+                    float old[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (P.accumulate) {
+                        if (vec) {
+                            const float4 t = *reinterpret_cast<const float4*>(dst);
+                            old[0] = t.x; old[1] = t.y; old[2] = t.z; old[3] = t.w;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (col + j < P.N) old[j] = dst[j];
                         }
-                        if (P.s_col) out = out / __ldg(P.s_col + col);
-                        dst[col] = out;
                     }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (P.ec_mode) o[j] = o[j] - fmaf(ep, cscale[j], cterm[j]);
+                        if (P.s_row) o[j] = o[j] / sr;
+                        if (P.accumulate) o[j] = o[j] + old[j];
+                    }
+                } else {
+                    if (P.ec_mode == S3R_EC_TWO_WAY) {
+                        float corr[4];
+                        const float pr = __ldg(P.p + grow);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) corr[j] = pr;
+                        for (int64_t b = 0; b < P.B; ++b) {
+                            const float xs = (float)__ldg(P.xsum + b * P.M + grow);
+                            const float m = __ldg(P.mu + b);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (col + j < P.N) corr[j] = fmaf(xs, __ldg(P.colmean + b * P.N + col + j) - m, corr[j]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) o[j] = o[j] - corr[j];
+                    }
+                    if (P.s_col) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) o[j] = o[j] / cscale[j];
+                    }
+                }
+                if (vec) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col + j < P.N) dst[j] = o[j];
                 }
             }
         }
