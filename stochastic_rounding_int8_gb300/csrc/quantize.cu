@@ -13,7 +13,11 @@
 // Philox threshold is computed by one lane per row and broadcast with
 // __shfl_sync; codes are written once as 8-byte stores; the error partials are
 // reduced with shuffles and a small shared-memory pass, in a fixed order.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
+
+#include <cstdio>
 
 #include "common.cuh"
 
@@ -62,10 +66,11 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
 
 // Round the folded values g[RPT][8] of one thread to codes, write them, and
 // accumulate the tile's error partials.  amax_bits is the tile absmax.
-template <int MODE, int RPT>
+template <int MODE, int RPT, int FMT = -1>
 __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32_t amax_bits, int64_t t0, int64_t n0,
                                                 int r0, int c, const QuantCommon& C, const QuantOut& O,
                                                 float* col_smem /* [WARPS][128] */) {
+    const int fmt = FMT >= 0 ? FMT : O.fmt;
     using Geo = TileGeom<RPT>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t nc0 = n0 + 8 * c;
@@ -116,7 +121,7 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
             }
         }
         float rowsum = 0.0f;
-        uint32_t packed[2] = {0u, 0u};
+        float qv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float y = g[j][i] * inv;
@@ -130,32 +135,35 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
                 qf = (u < p) ? f + 1.0f : f;
             }
             qf = fminf(fmaxf(qf, -127.0f), 127.0f);
-            const int q = (int)qf;
-            packed[i >> 2] |= ((uint32_t)(q & 0xFF)) << (8 * (i & 3));
+            if (nonfinite) qf = 0.0f;
+            qv[i] = qf;
             const float e = nonfinite ? 0.0f : fmaf(d, qf, -g[j][i]);
             rowsum += e;
             colsum[i] += e;
         }
-        if (nonfinite) packed[0] = packed[1] = 0u;
         if (t < C.T) {
-            if (O.fmt == S3R_CODES_S8) {
+            if (fmt == S3R_CODES_S8) {
+                uint32_t w[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int a = (int)qv[4 * k], b = (int)qv[4 * k + 1], cc = (int)qv[4 * k + 2], dd = (int)qv[4 * k + 3];
+                    w[k] = __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(cc, dd, 0x0040), 0x5410);
+                }
                 int8_t* dst = static_cast<int8_t*>(O.Q) + t * C.N + nc0;
                 if (C.vec_store && nc0 + 8 <= C.N) {
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (nc0 + i < C.N) dst[i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFF);
+                        if (nc0 + i < C.N) dst[i] = (int8_t)(int)qv[i];
                 }
             } else {
                 // the same integer in an IEEE half (exact for |q| <= 2048)
                 uint32_t hw[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int qa = (int)(int8_t)((packed[(2 * k) >> 2] >> (8 * ((2 * k) & 3))) & 0xFF);
-                    const int qb = (int)(int8_t)((packed[(2 * k + 1) >> 2] >> (8 * ((2 * k + 1) & 3))) & 0xFF);
-                    hw[k] = (uint32_t)__half_as_ushort(__int2half_rn(qa)) |
-                            ((uint32_t)__half_as_ushort(__int2half_rn(qb)) << 16);
+                    const __half2 h2 = __floats2half2_rn(qv[2 * k], qv[2 * k + 1]);
+                    hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 __half* dst = static_cast<__half*>(O.Q) + t * C.N + nc0;
                 if (C.vec_store && nc0 + 8 <= C.N) {
@@ -163,7 +171,7 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (nc0 + i < C.N) dst[i] = __ushort_as_half((unsigned short)(hw[i >> 1] >> (16 * (i & 1))));
+                        if (nc0 + i < C.N) dst[i] = __float2half_rn(qv[i]);
                 }
             }
         }
@@ -254,6 +262,127 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(TileQuantArgs A, Qua
     }
     amax_bits = block_max_u32<Geo::kWarps>(amax_bits, red);
     round_and_store<MODE, RPT>(g, amax_bits, t0, n0, r0, c, C, O, col_smem);
+}
+
+// ---------------------------------------------------------------------------
+// Persistent variant: each CTA walks tiles tile = blockIdx.x + i * gridDim.x;
+// a TMA engine copies the next 128x128 bf16 tile into the other half of a
+// two-buffer shared-memory ring while the current one is rounded, so the HBM
+// stream never waits for the arithmetic.  The folded values stay in registers
+// after the absmax pass, which frees the buffer for the next copy early.
+// ---------------------------------------------------------------------------
+constexpr uint64_t kQuantWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t q_gtime() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool q_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok = 0;
+    const uint64_t t0 = q_gtime();
+    while (true) {
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (q_gtime() - t0 > kQuantWaitNs) return false;
+    }
+}
+__device__ __forceinline__ void q_issue_tile(uint32_t dst, const CUtensorMap* map, int32_t col, int32_t row,
+                                             uint32_t bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTile * kTile * 2)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(col), "r"(row), "r"(bar)
+        : "memory");
+}
+
+template <int MODE, int FMT>
+__global__ void __launch_bounds__(256, 2)
+    quantize_tma_kernel(const __grid_constant__ CUtensorMap tmG, TileQuantArgs A, QuantCommon C, QuantOut O,
+                        int64_t ntiles) {
+    constexpr int RPT = 8;
+    using Geo = TileGeom<RPT>;
+    extern __shared__ __align__(128) uint8_t qsmem[];
+    uint16_t* buf[2] = {reinterpret_cast<uint16_t*>(qsmem), reinterpret_cast<uint16_t*>(qsmem + kTile * kTile * 2)};
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + 2 * kTile * kTile * 2);
+    __shared__ uint32_t red[Geo::kWarps];
+    __shared__ float col_smem[Geo::kWarps * 128];
+    const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars), bar1 = bar0 + 8;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar1) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    int issued = 0;
+    if (threadIdx.x == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmG) : "memory");
+        for (int k = 0; k < 2 && first + k * stride < ntiles; ++k) {
+            const int64_t tile = first + k * stride;
+            q_issue_tile((uint32_t)__cvta_generic_to_shared(buf[k]), &tmG, (int32_t)((tile % C.ntc) * kTile),
+                         (int32_t)((tile / C.ntc) * kTile), k ? bar1 : bar0);
+            ++issued;
+        }
+    }
+    int i = 0;
+    for (int64_t tile = first; tile < ntiles; tile += stride, ++i) {
+        const int b = i & 1;
+        const int64_t t0 = (tile / C.ntc) * kTile, n0 = (tile % C.ntc) * kTile;
+        const int64_t nc0 = n0 + 8 * c;
+        if (!q_wait(b ? bar1 : bar0, (uint32_t)(i >> 1) & 1u)) {
+            set_status(C.d_status, S3R_ERR_TIMEOUT);
+            break;
+        }
+        float sw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sw[k] = (A.s_w && nc0 + k < C.N) ? __ldg(A.s_w + nc0 + k) : 1.0f;
+        float g[RPT][8];
+        uint32_t amax_bits = 0u;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int rr = r0 + j * Geo::kRowStride;
+            const int64_t t = t0 + rr;
+            const uint4 raw = *reinterpret_cast<const uint4*>(buf[b] + rr * kTile + 8 * c);
+            const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float v = (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
+                if (A.s_x) v = sx * v;
+                if (A.s_w) v = v * sw[k];
+                g[j][k] = v;
+                amax_bits = max(amax_bits, __float_as_uint(v) & 0x7FFFFFFFu);
+            }
+        }
+        // block absmax; the first barrier also means every thread is done with buf[b]
+        amax_bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax_bits;
+        __syncthreads();
+        if (threadIdx.x == 0 && tile + 2 * stride < ntiles) {
+            const int64_t nt = tile + 2 * stride;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            q_issue_tile((uint32_t)__cvta_generic_to_shared(buf[b]), &tmG, (int32_t)((nt % C.ntc) * kTile),
+                         (int32_t)((nt / C.ntc) * kTile), b ? bar1 : bar0);
+            ++issued;
+        }
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < Geo::kWarps; ++w) m = max(m, red[w]);
+        __syncthreads();
+        round_and_store<MODE, RPT, FMT>(g, m, t0, n0, r0, c, C, O, col_smem);
+    }
+    // an early exit may leave copies in flight: wait for them before leaving
+    if (threadIdx.x == 0) {
+        for (int k = i; k < issued; ++k) q_wait((k & 1) ? bar1 : bar0, (uint32_t)(k >> 1) & 1u);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -408,6 +537,82 @@ using namespace s3r;
 
 static bool valid_fmt(int fmt) { return fmt == S3R_CODES_S8 || fmt == S3R_CODES_F16; }
 
+static PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess && p)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+
+static int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 148;
+        }
+    }
+    return n;
+}
+
+constexpr int kQuantTmaSmem = 2 * kTile * kTile * 2 + 16;
+
+template <int MODE, int FMT>
+static int launch_quant_tma(const CUtensorMap& map, const TileQuantArgs& A, const QuantCommon& C, const QuantOut& O,
+                            int64_t ntiles, cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(quantize_tma_kernel<MODE, FMT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantTmaSmem);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return s3r_cuda_fail("quantize: cudaFuncSetAttribute", e);
+        }
+        attr = true;
+    }
+    const int64_t grid = ntiles < 2LL * sm_count() ? ntiles : 2LL * sm_count();
+    quantize_tma_kernel<MODE, FMT><<<(unsigned)grid, 256, kQuantTmaSmem, stream>>>(map, A, C, O, ntiles);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+// The TMA path needs 16-byte aligned rows; returns 1 when it does not apply.
+static int try_quant_tma(int mode, const TileQuantArgs& A, const QuantCommon& C, const QuantOut& O,
+                         cudaStream_t stream) {
+    if (!A.vec_load || !C.vec_store) return 1;
+    auto fn = q_encode_fn();
+    if (!fn) return 1;
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)C.N, (cuuint64_t)C.T};
+    cuuint64_t strides[1] = {(cuuint64_t)A.ldg * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+    cuuint32_t estr[2] = {1u, 1u};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(A.G), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return 1;
+    const int64_t ntiles = s3r_cdiv(C.T, kTile) * C.ntc;
+    const bool f16 = O.fmt == S3R_CODES_F16;
+    switch (mode) {
+        case kRTNE: return f16 ? launch_quant_tma<kRTNE, 1>(map, A, C, O, ntiles, stream)
+                               : launch_quant_tma<kRTNE, 0>(map, A, C, O, ntiles, stream);
+        case kS3R: return f16 ? launch_quant_tma<kS3R, 1>(map, A, C, O, ntiles, stream)
+                              : launch_quant_tma<kS3R, 0>(map, A, C, O, ntiles, stream);
+        default: return f16 ? launch_quant_tma<kINDEP, 1>(map, A, C, O, ntiles, stream)
+                            : launch_quant_tma<kINDEP, 0>(map, A, C, O, ntiles, stream);
+    }
+}
+
 static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
                              const float* s_w, uint64_t seed, uint32_t tensor_id, void* Q, int fmt, float* scale,
                              float* tok, float* col, int* d_status, cudaStream_t stream) {
@@ -419,6 +624,8 @@ static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int6
     TileQuantArgs A{static_cast<const uint16_t*>(G), ldg, s_x, s_w, s3r_aligned16(G) && (ldg % 8) == 0};
     QuantCommon C{T, N, s3r_cdiv(N, kTile), (uint32_t)seed, d_status, s3r_aligned16(Q) && (N % 8) == 0};
     QuantOut O{Q, fmt, scale, tok, col, tensor_id};
+    const int tma = try_quant_tma(mode, A, C, O, stream);
+    if (tma <= 0) return tma;   // launched (0) or failed (< 0)
     dim3 grid((unsigned)s3r_cdiv(N, kTile), (unsigned)s3r_cdiv(T, kTile));
     switch (mode) {
         case kRTNE: quantize_tile_kernel<kRTNE><<<grid, 256, 0, stream>>>(A, C, O); break;
