@@ -209,6 +209,26 @@ int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t
                    size_t workspace_bytes, int* d_status, cudaStream_t stream);
 
 /*
+ * s3r_ec_correct_static -- s3r_ec_correct without a caller workspace, for
+ * callers that cannot allocate device memory when they run it (inside a
+ * stream capture that must not allocate, from a host callback or a real-time
+ * loop, or under a device memory budget fixed before the first step).  The
+ * paper has no counterpart: this is a deployment convenience of this library.
+ * Arguments and results are those of s3r_ec_correct.  The two-way column sums
+ * use a scratch array of 8 MiB that lives in the library (every GPU that loads
+ * the library keeps it until the process exits); sizes whose scratch
+ * (s3r_ec_workspace_size(T, K)) exceeds 8 MiB are rejected with
+ * S3R_ERR_UNSUPPORTED and an explanation in s3r_last_error().  The first call
+ * on a device looks up the array's device address; make that first call before
+ * any stream capture.  Every call shares the array, so calls that overlap on
+ * the GPU (other streams or threads) race on it.  Allocates nothing.
+ */
+int s3r_ec_correct_static(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
+                          const void* W8, int64_t K, const void* X8, int code_format, int ec_mode, float* eps,
+                          float* mu, float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p,
+                          int* d_status, cudaStream_t stream);
+
+/*
  * int8_gemm_dx -- activation gradient from the S8 codes ([S3R] §III-A "S8 GEMM
  * with S32 accumulation, and rescaled"; §III-D activation-gradient term):
  *   acc[t,k] = sum_kb tile_scale[t/128, kb] * (int32) sum_{n in block kb} Q[t,n] W8[k,n]

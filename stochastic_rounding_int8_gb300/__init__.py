@@ -56,6 +56,8 @@ _SIGS = {
     "s3r_ec_workspace_size": (_SZ, [_I64, _I64]),
     "s3r_ec_correct": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _I64, _VP, _INT, _INT, _VP, _VP, _VP, _VP, _VP, _VP,
                               _VP, _VP, _SZ, _VP, _VP]),
+    "s3r_ec_correct_static": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _I64, _VP, _INT, _INT, _VP, _VP, _VP, _VP, _VP,
+                                     _VP, _VP, _VP, _VP]),
     "int8_gemm_dx": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _I64, _VP, _INT, _VP,
                             _VP]),
     "int8_gemm_dw_workspace_size": (_SZ, [_I64, _I64, _I64, _INT]),

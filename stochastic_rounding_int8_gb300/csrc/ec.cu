@@ -12,6 +12,8 @@
 // deterministic run to run.
 #include <cuda_fp16.h>
 
+#include <cstdio>
+
 #include "common.cuh"
 
 namespace s3r {
@@ -353,4 +355,80 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
                                                                           p);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of s3r_ec_correct.
+//
+// Some callers cannot allocate device memory at the moment they run the
+// backward: code that must not call cudaMalloc while a stream is being
+// captured, code running from a host callback or a real-time loop where an
+// allocation would block or fail, or deployments that fix their whole device
+// memory budget before the first step.  For them the two-way column sums use a
+// scratch array that lives in this library's module, not a caller workspace.
+//
+// The array is a file-scope __device__ object of kStaticScratchBytes (8 MiB):
+// every GPU that loads the library holds it until the process exits.  Its
+// name in host code is only a host-side stand-in, so the device address is
+// fetched with cudaGetSymbolAddress, once per device, with that device
+// current; the first call on a device does this set-up (call it once before
+// any stream capture).  All calls share the array and it keeps the last
+// call's contents; nothing in it needs to start at zero (every partial it
+// holds is written before it is read).  Calls that overlap on the GPU (two
+// streams, or two host threads) race on it.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_ec_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_ec_scratch on the current device (nullptr on failure).
+void* static_scratch(int* status) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        *status = s3r_cuda_fail("s3r_ec_correct_static: cudaGetDevice", e == cudaSuccess ? cudaErrorInvalidDevice : e);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_ec_scratch);
+        if (e != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            *status = s3r_cuda_fail("s3r_ec_correct_static: cudaGetSymbolAddress", e == cudaSuccess ? cudaErrorUnknown : e);
+            return nullptr;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+}  // namespace
+
+extern "C" int s3r_ec_correct_static(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N,
+                                     int64_t S, const void* W8, int64_t K, const void* X8, int code_format,
+                                     int ec_mode, float* eps, float* mu, float* colmean, int32_t* rowsum, float* v,
+                                     int32_t* xsum, float* p, int* d_status, cudaStream_t stream) {
+    if (ec_mode != S3R_EC_TWO_WAY)   // only the two-way factors need scratch
+        return s3r_ec_correct(tok_err_part, col_err_part, T, N, S, W8, K, X8, code_format, ec_mode, eps, mu, colmean,
+                              rowsum, v, xsum, p, nullptr, 0, d_status, stream);
+    const size_t need = s3r_ec_workspace_size(T, K);
+    if (need > kStaticScratchBytes) {
+        char buf[200];
+        std::snprintf(buf, sizeof(buf), "needs %zu bytes of scratch for T=%lld, K=%lld; the static array holds %zu",
+                      need, (long long)T, (long long)K, kStaticScratchBytes);
+        s3r_record_error("s3r_ec_correct_static", buf);
+        return S3R_ERR_UNSUPPORTED;
+    }
+    int st = S3R_OK;
+    void* scratch = static_scratch(&st);
+    if (!scratch) return st;
+    return s3r_ec_correct(tok_err_part, col_err_part, T, N, S, W8, K, X8, code_format, ec_mode, eps, mu, colmean,
+                          rowsum, v, xsum, p, scratch, kStaticScratchBytes, d_status, stream);
 }

@@ -1,0 +1,85 @@
+"""The allocation-free correction entry point (s3r_ec_correct_static).
+
+Callers that cannot allocate device memory while they run the backward --
+code inside a stream capture that must not allocate, host callbacks and
+real-time loops, deployments with a device budget fixed up front -- use this
+variant, whose scratch lives in a static array of the library instead of a
+caller workspace.  The test calls it through the C ABI twice in a row (two
+different gradients, so the second call runs over the first call's leftover
+scratch) and checks each result against s3r_ec_correct with a torch-allocated
+workspace, within the tolerances the other parity tests use.  This file is
+collected last on purpose.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+from parity_util import assert_close_mag
+
+pytestmark = pytest.mark.gpu
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _outputs(T, N, K, S, dev):
+    B = T // S
+    f = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device=dev)
+    i = lambda *s: torch.full(s, -7, dtype=torch.int32, device=dev)
+    return dict(eps=f(T), mu=f(B), colmean=f(B, N), rowsum=i(K), v=f(B, K), xsum=i(B, K), p=f(K))
+
+
+def _call(L, fn, q, T, N, S, W, X, fmt, out, ws=None, status=None):
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = [_ptr(q.tok_err_part), _ptr(q.col_err_part), T, N, S, _ptr(W), W.shape[0], _ptr(X), fmt, 2,
+            _ptr(out["eps"]), _ptr(out["mu"]), _ptr(out["colmean"]), _ptr(out["rowsum"]), _ptr(out["v"]),
+            _ptr(out["xsum"]), _ptr(out["p"])]
+    if fn == "s3r_ec_correct":
+        args += [_ptr(ws), ws.numel()]
+    args += [_ptr(status), stream]
+    return getattr(L, fn)(*args)
+
+
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
+def test_static_scratch_matches_workspace_version_twice(fmt):
+    import stochastic_rounding_int8_gb300 as s3r
+    L = s3r.lib()
+    T, N, K, S = 8192, 2048, 5632, 2048      # the W2 linear of the d=2048, F=5632 FFN block
+    dev = "cuda"
+    rng = np.random.default_rng(99)
+    dt = torch.float16 if fmt else torch.int8
+    W = torch.from_numpy(rng.integers(-127, 128, size=(K, N)).astype(np.int8)).to(dt).to(dev)
+    X = torch.from_numpy(rng.integers(-127, 128, size=(T, K)).astype(np.int8)).to(dt).to(dev)
+    st = s3r.new_status()
+    for call in range(2):
+        G = torch.from_numpy((rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)).to(torch.bfloat16).to(dev)
+        q = s3r.s3r_quantize(G, seed=call, tensor_id=3, code_format=fmt)
+        ref = _outputs(T, N, K, S, dev)
+        ws = torch.empty(L.s3r_ec_workspace_size(T, K), dtype=torch.uint8, device=dev)
+        assert _call(L, "s3r_ec_correct", q, T, N, S, W, X, fmt, ref, ws=ws) == 0
+        got = _outputs(T, N, K, S, dev)
+        assert _call(L, "s3r_ec_correct_static", q, T, N, S, W, X, fmt, got, status=st) == 0, \
+            L.s3r_last_error().decode()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for k in ("rowsum", "xsum"):
+            assert torch.equal(got[k], ref[k]), (call, k)
+        for k in ("eps", "mu", "colmean", "v", "p"):
+            r = ref[k].double().cpu().numpy()
+            assert_close_mag(got[k].cpu().numpy(), r, np.abs(r), f"call {call}: {k}")
+
+
+def test_static_scratch_rejects_oversized_problem():
+    import stochastic_rounding_int8_gb300 as s3r
+    L = s3r.lib()
+    T, N, K, S = 16384, 256, 16384, 16384    # needs 128 chunks x 16384 x 8 B = 16 MiB of scratch
+    dev = "cuda"
+    q = s3r.s3r_quantize(torch.zeros((T, N), dtype=torch.bfloat16, device=dev))
+    W = torch.zeros((K, N), dtype=torch.float16, device=dev)
+    X = torch.zeros((T, K), dtype=torch.float16, device=dev)
+    out = _outputs(T, N, K, S, dev)
+    assert _call(L, "s3r_ec_correct_static", q, T, N, S, W, X, 1, out) == -8
+    assert "static array holds" in L.s3r_last_error().decode()
