@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "swiglu", "ec", "ffn"],
+    ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn"],
                     help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
     return ap.parse_args()
 
@@ -408,6 +408,10 @@ def run_kernel_case(args):
         "ec": lambda: s3r.s3r_ec_correct(q2, T, D, S, ops.W2_8, ops.A8, s3r.EC_TWO_WAY),
         "ffn": lambda: s3r.ffn_backward(ops, dY, S),
     }
+    if args.kernel_case == "quantize_sweep":
+        Gs = workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).cuda()
+        qs = s3r.s3r_quantize(Gs, code_format=s3r.CODES_S8)
+        fns["quantize_sweep"] = lambda: s3r.s3r_quantize(Gs, out=qs)
     fn = fns[args.kernel_case]
     for _ in range(args.warmup):
         fn()
