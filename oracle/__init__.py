@@ -56,6 +56,8 @@ def lib():
             L.orc_token_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
             L.orc_element_threshold.restype = C.c_float
             L.orc_element_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
+            L.orc_inv127_rz.restype = C.c_float
+            L.orc_inv127_rz.argtypes = [C.c_float]
             L.orc_sr_step.restype = C.c_float
             L.orc_sr_step.argtypes = [C.c_float, C.c_float]
             L.orc_expf.restype = C.c_float
@@ -116,6 +118,11 @@ def from_torch_bf16(t) -> np.ndarray:
     """A torch bf16 CPU tensor -> float32 numpy, via the oracle's own widening."""
     import torch
     return bf16_to_f32(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def inv127_rz(a: float) -> float:
+    """127 / a rounded toward zero (the quantizer's normalizing factor)."""
+    return lib().orc_inv127_rz(float(a))
 
 
 def sr_step(y: float, u: float) -> float:

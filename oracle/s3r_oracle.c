@@ -115,8 +115,9 @@ void orc_bf16_array_to_float(const uint16_t* src, int64_t n, float* dst) {
 /*                                                                            */
 /* For each element, in fp32:                                                 */
 /*   fold      g  = (s_x[t] * G[t,n]) * s_w[n]      (null scale pointer = 1)  */
-/*   scale     amax = max |g| over the tile; delta = amax / 127;              */
-/*             inv = 127 / amax   (delta = inv = 0 when amax == 0)            */
+/*   scale     amax = max |g| over the tile; delta = amax / 127 (nearest);    */
+/*             inv = 127 / amax rounded toward zero, so |g * inv| <= 127     */
+/*             and no code leaves [-127, 127] (delta = inv = 0 if amax == 0) */
 /*   normalise y  = g * inv                                                   */
 /*   SR        f = floor(y); p = y - f; q = f + [u < p]   ([SRB] "u < p")     */
 /*   RTNE      q = nearbyint(y)  (round half to even)                         */
@@ -133,6 +134,14 @@ float orc_sr_step(float y, float u) {
     float f = floorf(y);
     float p = y - f;
     return (u < p) ? f + 1.0f : f;
+}
+
+/* 127 / a rounded toward zero (a > 0): the nearest quotient, stepped down
+ * one ulp when it overshoots (the fma residual 127 - q*a is exact in sign). */
+float orc_inv127_rz(float a) {
+    float q = 127.0f / a;
+    if (fmaf(-q, a, 127.0f) < 0.0f) q = nextafterf(q, 0.0f);
+    return q;
 }
 
 static float fold_one(const float* G, int64_t ldg, const float* s_x, const float* s_w, int64_t t, int64_t n) {
@@ -178,7 +187,7 @@ int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
                 continue;
             }
             float d = amax / 127.0f;
-            float inv = (amax > 0.0f) ? 127.0f / amax : 0.0f;
+            float inv = (amax > 0.0f) ? orc_inv127_rz(amax) : 0.0f;
             delta[i * ntc + j] = d;
             for (int64_t t = t0; t < t1; ++t) {
                 float u_tok = (mode == ORC_S3R) ? orc_token_threshold((uint64_t)(t + row_base), seed, tensor_id) : 0.0f;
@@ -227,7 +236,7 @@ int orc_rtne_operand(const float* A, int64_t R, int64_t C, int64_t lda, int axis
             if (fabsf(a) > amax) amax = fabsf(a);
         }
         float s = amax > 0.0f ? amax / 127.0f : 1.0f;
-        float inv = amax > 0.0f ? 127.0f / amax : 1.0f;
+        float inv = amax > 0.0f ? orc_inv127_rz(amax) : 1.0f;
         scale[v] = s;
         for (int64_t l = 0; l < len; ++l) {
             int64_t r = axis == 0 ? v : l, c = axis == 0 ? l : v;

@@ -157,7 +157,8 @@ def test_ffn_staged_matches_oracle(s3r, orc, fmt, mode, ec):
         Qg, dg = codes(q.Q), q.tile_scale.cpu().numpy()
         g = (ops_o.s_x[:, None] * dh) * s_w[None, :]
         amax = np.abs(g).reshape(T // 128, 128, -1, 128).max(axis=(1, 3)) if F % 128 == 0 else None
-        y = g * expand_tiles(np.float32(127.0) / amax, T, F).astype(np.float32)
+        inv = np.vectorize(lambda a: np.float32(orc.inv127_rz(float(a))))(amax).astype(np.float32)
+        y = g * expand_tiles(inv, T, F).astype(np.float32)
         near_tie_flips(Qg, lb.Q, y, _thresholds(orc, mode, T, F, seed, tid))
         D = expand_tiles(dg, T, F) * Qg - expand_tiles(lb.delta, T, F) * lb.Q
         ddx, ddw = _flip_effect(D, W8, ops_o.X8, ops_o.s_x, s_w, S, ecx, orc)

@@ -92,19 +92,30 @@ def test_unbiased_and_variance(orc, mode):
     G = (rng.standard_normal((8, 24)) * 0.01).astype(np.float32)
     codes, delta = _mc(orc, G, getattr(orc, mode), n=4000)
     d = float(delta[0, 0])
-    y = G * np.float32(127.0 / np.abs(G).max())
+    inv = np.float32(orc.inv127_rz(float(np.abs(G).max())))
+    y = (G * inv).astype(np.float64)            # the value SR sees, in grid units
     p = y - np.floor(y)
-    mean = codes.astype(np.float64).mean(0) * d
-    var_theory = p * (1 - p) * d * d
+    mean = codes.astype(np.float64).mean(0)
+    var_theory = p * (1 - p)
     se = np.sqrt(np.maximum(var_theory, 1e-30) / codes.shape[0])
-    z = (mean - G) / se
-    ok = var_theory > 0
+    z = (mean - y) / se                         # E[SR(y)] = y
+    n = codes.shape[0]
+    ok = n * var_theory >= 5                    # where the normal approximation holds
     assert np.abs(z[ok]).max() < 5.0
     assert (np.abs(z[ok]) > 3).mean() < 0.02
-    var_emp = codes.astype(np.float64).var(0) * d * d
+    # near-certain elements: the count of the rare outcome stays within a Poisson tail
+    rare = (var_theory > 0) & ~ok
+    lam = n * np.minimum(p, 1 - p)[rare]
+    f = np.floor(y)[rare]
+    ups = (codes[:, rare] > f).sum(0)
+    minority = np.where(p[rare] < 0.5, ups, n - ups)
+    assert (minority <= lam + 6 * np.sqrt(lam) + 4).all()
+    var_emp = codes.astype(np.float64).var(0)
     rel = np.abs(var_emp[ok] - var_theory[ok]) / var_theory[ok]
     assert np.median(rel) < 0.05
-    assert (var_theory <= d * d / 4 + 1e-18).all()
+    assert (var_theory <= 0.25 + 1e-12).all()
+    # dequantizing by delta returns G' up to fp32 rounding: |delta * inv - 1| <= 2^-22
+    assert abs(np.float64(delta[0, 0]) * np.float64(inv) - 1.0) <= 2.0 ** -22
 
 
 def test_on_grid_values_unchanged(orc):
@@ -132,7 +143,7 @@ def test_same_direction_per_token(orc):
     rng = np.random.default_rng(4)
     G = (rng.standard_normal((256, 384)) * 1e-3).astype(np.float32)
     Q, delta, E, _ = orc.quantize(G, mode=orc.S3R, seed=7)
-    inv = np.float32(127.0) / np.abs(G[:128, :128]).max()
+    inv = np.float32(orc.inv127_rz(float(np.abs(G[:128, :128]).max())))
     y = G[:128, :128] * inv
     f = np.floor(y)
     p = y - f
@@ -269,3 +280,28 @@ def test_window_equals_slice_of_full(orc):
         assert np.array_equal(Qw, Q[128:256, 128:300])
         assert np.array_equal(dw, delta[1:2, 1:3])
         assert np.array_equal(Ew, E[128:256, 128:300])
+
+
+def test_inverse_rounds_toward_zero_and_bounds_y(orc):
+    """inv = 127/amax rounded toward zero: never above the exact quotient, at
+    most one ulp below it (checked against exact rational arithmetic), so
+    |g * inv| <= 127 for every |g| <= amax and codes never need clamping."""
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    amaxes = np.concatenate([rng.random(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000),
+                             np.float32([1.0, 127.0, 3.0, 1e-38, 3e38, 0.1])]).astype(np.float32)
+    for a in amaxes[:4000]:
+        a = np.float32(a)
+        if not np.isfinite(a) or a <= 0:
+            continue
+        inv = np.float32(orc.inv127_rz(float(a)))
+        exact = Fraction(127) / Fraction(float(a))
+        assert Fraction(float(inv)) <= exact
+        assert Fraction(float(np.nextafter(inv, np.float32(np.inf)))) > exact
+    for a in amaxes:
+        a = np.float32(a)
+        if not np.isfinite(a) or a <= 0:
+            continue
+        inv = np.float32(orc.inv127_rz(float(a)))
+        assert abs(np.float32(a) * inv) <= np.float32(127.0)
+        assert abs(np.float32(-a) * inv) <= np.float32(127.0)
