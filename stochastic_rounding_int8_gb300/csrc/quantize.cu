@@ -64,20 +64,23 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
     return m;
 }
 
-// Round the folded values g[RPT][8] of one thread to codes, write them, and
-// accumulate the tile's error partials.  amax_bits is the tile absmax.
+// Round one thread's folded values to codes, write them, and accumulate the
+// tile's error partials.  ng holds the folded gradient NEGATED (-g), so the
+// error e = delta*q - g is a single fma(delta, q, ng).  amax_bits is the tile
+// absmax.  inv = 127/amax rounded toward zero keeps |y| <= 127, so no code can
+// leave [-127, 127] and no clamp is needed.
 template <int MODE, int RPT, int FMT = -1>
-__device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32_t amax_bits, int64_t t0, int64_t n0,
+__device__ __forceinline__ void round_and_store(const float (&ng)[RPT][8], uint32_t amax_bits, int64_t t0, int64_t n0,
                                                 int r0, int c, const QuantCommon& C, const QuantOut& O,
                                                 float* col_smem /* [WARPS][128] */) {
-    const int fmt = FMT >= 0 ? FMT : O.fmt;
     using Geo = TileGeom<RPT>;
+    const int fmt = FMT >= 0 ? FMT : O.fmt;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t nc0 = n0 + 8 * c;
-    const bool nonfinite = amax_bits >= 0x7F800000u;
+    const bool nonfinite = amax_bits >= 0x7F800000u;   // uniform across the CTA
     const float amax = __uint_as_float(amax_bits);
     const float d = nonfinite ? __uint_as_float(0x7FC00000u) : amax / 127.0f;
-    const float inv = (amax_bits == 0u || nonfinite) ? 0.0f : 127.0f / amax;
+    const float inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amax);
     if (threadIdx.x == 0) {
         O.scale[(t0 / kTile) * C.ntc + (n0 / kTile)] = d;
         if (nonfinite) set_status(C.d_status, S3R_ERR_NONFINITE);
@@ -92,9 +95,10 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
         for (int j = 0; j < RPT; ++j) u_row[j] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) + j);
     }
 
-    float colsum[8];
+    const float2 ninv2 = make_float2(-inv, -inv), d2 = make_float2(d, d);
+    float2 colsum[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) colsum[i] = 0.0f;
+    for (int k = 0; k < 4; ++k) colsum[k] = make_float2(0.0f, 0.0f);
 
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
@@ -120,33 +124,41 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
                 }
             }
         }
-        float rowsum = 0.0f;
         float qv[8];
+        float2 rs = make_float2(0.0f, 0.0f);
+        if (!nonfinite) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float y = g[j][i] * inv;
-            float qf;
-            if (MODE == kRTNE) {
-                qf = rintf(y);
-            } else {
-                const float u = (MODE == kS3R) ? u_row[j] : u8[i];
-                const float f = floorf(y);
-                const float p = y - f;
-                qf = (u < p) ? f + 1.0f : f;
+            for (int k = 0; k < 4; ++k) {
+                const float2 g2 = make_float2(ng[j][2 * k], ng[j][2 * k + 1]);
+                const float2 y = f2_mul(g2, ninv2);                  // = g * inv, exactly
+                float2 q;
+                if (MODE == kRTNE) {
+                    q = make_float2(rintf(y.x), rintf(y.y));
+                } else {
+                    const float2 f = make_float2(floorf(y.x), floorf(y.y));
+                    const float2 p = f2_sub(y, f);
+                    const float ua = (MODE == kS3R) ? u_row[j] : u8[2 * k];
+                    const float ub = (MODE == kS3R) ? u_row[j] : u8[2 * k + 1];
+                    q = f2_add(f, make_float2(ua < p.x ? 1.0f : 0.0f, ub < p.y ? 1.0f : 0.0f));
+                }
+                qv[2 * k] = q.x;
+                qv[2 * k + 1] = q.y;
+                const float2 e = f2_fma(d2, q, g2);                  // delta*q - g
+                rs = f2_add(rs, e);
+                colsum[k] = f2_add(colsum[k], e);
             }
-            qf = fminf(fmaxf(qf, -127.0f), 127.0f);
-            if (nonfinite) qf = 0.0f;
-            qv[i] = qf;
-            const float e = nonfinite ? 0.0f : fmaf(d, qf, -g[j][i]);
-            rowsum += e;
-            colsum[i] += e;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qv[i] = 0.0f;
         }
+        const float rowsum = rs.x + rs.y;
         if (t < C.T) {
             if (fmt == S3R_CODES_S8) {
                 uint32_t w[2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const int a = (int)qv[4 * k], b = (int)qv[4 * k + 1], cc = (int)qv[4 * k + 2], dd = (int)qv[4 * k + 3];
+                    const int a = __float2int_rn(qv[4 * k]), b = __float2int_rn(qv[4 * k + 1]);
+                    const int cc = __float2int_rn(qv[4 * k + 2]), dd = __float2int_rn(qv[4 * k + 3]);
                     w[k] = __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(cc, dd, 0x0040), 0x5410);
                 }
                 int8_t* dst = static_cast<int8_t*>(O.Q) + t * C.N + nc0;
@@ -155,7 +167,7 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (nc0 + i < C.N) dst[i] = (int8_t)(int)qv[i];
+                        if (nc0 + i < C.N) dst[i] = (int8_t)__float2int_rn(qv[i]);
                 }
             } else {
                 // the same integer in an IEEE half (exact for |q| <= 2048)
@@ -176,26 +188,31 @@ __device__ __forceinline__ void round_and_store(const float (&g)[RPT][8], uint32
             }
         }
         if (O.tok) {
-            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 8);
-            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 4);
-            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 2);
-            rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 1);
-            if (c == 0 && t < C.T) O.tok[t * C.ntc + n0 / kTile] = rowsum;
+            float r = rowsum;
+            r += __shfl_xor_sync(0xFFFFFFFFu, r, 8);
+            r += __shfl_xor_sync(0xFFFFFFFFu, r, 4);
+            r += __shfl_xor_sync(0xFFFFFFFFu, r, 2);
+            r += __shfl_xor_sync(0xFFFFFFFFu, r, 1);
+            if (c == 0 && t < C.T) O.tok[t * C.ntc + n0 / kTile] = r;
         }
     }
     if (O.col) {
+        float cs[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) colsum[i] += __shfl_xor_sync(0xFFFFFFFFu, colsum[i], 16);
+        for (int k = 0; k < 4; ++k) {
+            cs[2 * k] = colsum[k].x + __shfl_xor_sync(0xFFFFFFFFu, colsum[k].x, 16);
+            cs[2 * k + 1] = colsum[k].y + __shfl_xor_sync(0xFFFFFFFFu, colsum[k].y, 16);
+        }
         if (lane < 16) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) col_smem[warp * 128 + 8 * c + i] = colsum[i];
+            for (int i = 0; i < 8; ++i) col_smem[warp * 128 + 8 * c + i] = cs[i];
         }
         __syncthreads();
         if (threadIdx.x < 128) {
-            float s = 0.0f;
+            float sum = 0.0f;
 #pragma unroll
-            for (int w = 0; w < Geo::kWarps; ++w) s += col_smem[w * 128 + threadIdx.x];
-            if (n0 + threadIdx.x < C.N) O.col[(t0 / kTile) * C.N + n0 + threadIdx.x] = s;
+            for (int w = 0; w < Geo::kWarps; ++w) sum += col_smem[w * 128 + threadIdx.x];
+            if (n0 + threadIdx.x < C.N) O.col[(t0 / kTile) * C.N + n0 + threadIdx.x] = sum;
         }
         __syncthreads();
     }
@@ -249,12 +266,13 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(TileQuantArgs A, Qua
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
         const int64_t t = t0 + r0 + j * Geo::kRowStride;
-        const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+        // negated fold: (-s_x) * G * s_w == -((s_x * G) * s_w) exactly
+        const float nsx = (A.s_x && t < C.T) ? -__ldg(A.s_x + t) : -1.0f;
         const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float v = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-            if (A.s_x) v = sx * v;
+            v = nsx * v;
             if (A.s_w) v = v * sw[i];
             g[j][i] = v;
             amax_bits = max(amax_bits, __float_as_uint(v) & 0x7FFFFFFFu);
@@ -351,15 +369,17 @@ __global__ void __launch_bounds__(256, 2)
             const int rr = r0 + j * Geo::kRowStride;
             const int64_t t = t0 + rr;
             const uint4 raw = *reinterpret_cast<const uint4*>(buf[b] + rr * kTile + 8 * c);
-            const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+            // negated fold: (-s_x) * G * s_w == -((s_x * G) * s_w) exactly; a missing scale is 1
+            const float nsx = (A.s_x && t < C.T) ? -__ldg(A.s_x + t) : -1.0f;
+            const float2 nsx2 = make_float2(nsx, nsx);
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float v = (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
-                if (A.s_x) v = sx * v;
-                if (A.s_w) v = v * sw[k];
-                g[j][k] = v;
-                amax_bits = max(amax_bits, __float_as_uint(v) & 0x7FFFFFFFu);
+            for (int k = 0; k < 4; ++k) {
+                float2 v = f2_mul(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), nsx2);
+                v = f2_mul(v, make_float2(sw[2 * k], sw[2 * k + 1]));
+                g[j][2 * k] = v.x;
+                g[j][2 * k + 1] = v.y;
+                amax_bits = max(amax_bits, max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu));
             }
         }
         // block absmax; the first barrier also means every thread is done with buf[b]
@@ -461,8 +481,9 @@ __global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, Quan
             const float dsilu = s * (1.0f + x1[i] * (1.0f - s));
             const float dh1 = (da[i] * x3[i]) * dsilu;
             const float dh3 = da[i] * silu;
-            float v1 = dh1, v3 = dh3;
-            if (A.s_x) { v1 = sx * v1; v3 = sx * v3; }
+            // negated folds: (-s_x) * dh * s_w == -((s_x * dh) * s_w) exactly
+            const float nsx = A.s_x ? -sx : -1.0f;
+            float v1 = nsx * dh1, v3 = nsx * dh3;
             if (A.s_w1) v1 = v1 * sw1[i];
             if (A.s_w3) v3 = v3 * sw3[i];
             g1[j][i] = v1;
@@ -501,7 +522,7 @@ __global__ void __launch_bounds__(256) rtne_rows_kernel(const uint16_t* A, int64
     }
     const float amax = __uint_as_float(m);
     const float s = m ? amax / 127.0f : 1.0f;
-    const float inv = m ? 127.0f / amax : 1.0f;
+    const float inv = m ? __fdiv_rz(127.0f, amax) : 1.0f;   // |a * inv| <= 127
     if (threadIdx.x == 0) scale[r] = s;
     for (int64_t c = threadIdx.x; c < C; c += blockDim.x) {
         const float q = fminf(fmaxf(rintf(bf16_at(A + r * lda + c) * inv), -127.0f), 127.0f);
@@ -523,7 +544,7 @@ __global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64
     }
     const float amax = __uint_as_float(m);
     const float s = m ? amax / 127.0f : 1.0f;
-    const float inv = m ? 127.0f / amax : 1.0f;
+    const float inv = m ? __fdiv_rz(127.0f, amax) : 1.0f;   // |a * inv| <= 127
     scale[c] = s;
     for (int64_t r = 0; r < R; ++r) {
         const float q = fminf(fmaxf(rintf(bf16_at(A + r * lda + c) * inv), -127.0f), 127.0f);
