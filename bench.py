@@ -329,6 +329,7 @@ def run_ours(args, world, rank, local):
     # per-step segments -> dominant kernel class
     segm = seg.mean(0)
     names = s3r.FFN_STEPS
+    # second field: GEMM products of 2*T*d*F flops per step (the fused dX1 + dX3 launch holds two)
     classes = {"int8_gemm_dx": (segm[2] + segm[6], 3), "int8_gemm_dw": (segm[3] + segm[7], 3),
                "quantize (dY + SwiGLU-fused)": (segm[0] + segm[4], 2), "s3r_ec_correct": (segm[1] + segm[5], 3)}
     dom = max(classes, key=lambda k: classes[k][0])
@@ -341,8 +342,8 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_note": f"dense bf16 sustained ({pk_kind}); the s8 codes run on the tensor cores at the "
                              f"16-bit rate or below on sm_103a",
-                "flops_per_launch": flops_per_launch, "launches_per_step": dom_n,
-                "avg_launch_us": round(dom_ms / dom_n * 1e3, 1)}
+                "flops_per_product": flops_per_launch, "products_per_step": dom_n,
+                "avg_us_per_product": round(dom_ms / dom_n * 1e3, 1)}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "traffic": None}

@@ -248,6 +248,35 @@ int int8_gemm_dx(const void* Q, const float* tile_scale, const void* W8, int cod
                  int64_t S, float* dX, int accumulate, int* d_status, cudaStream_t stream);
 
 /*
+ * int8_gemm_dx_sum -- activation gradient of a layer whose input feeds several
+ * linears, dX = sum_i (corrected, rescaled) Q_i W8_i^T.  The SwiGLU FFN block
+ * of [S3R] §IV-A (Table III) feeds X to both W1 and W3, so its input gradient
+ * is dX1 + dX3; each term follows the int8_gemm_dx formula with its own codes,
+ * tile scales and correction, and all terms share T, N, K, s_x and ec_mode:
+ *   dX[t,k] = (sum_i (acc_i - eps_i[t]*rowsum_i[k] - v_i[t/S, k])) / s_x[t]
+ * (plus the old dX when accumulate != 0).  S3R_CODES_F16 contracts every term
+ * into one fp32 accumulator in a single tcgen05 launch (one rescale, one store
+ * of dX); S3R_CODES_S8 runs one int8_gemm_dx per term, the later ones
+ * accumulating, so the two formats round the sum in a different order.
+ * terms: HOST array of n_terms (1 .. S3R_DX_MAX_TERMS) entries, read during
+ *        the call only; every pointer in it is a device pointer as in
+ *        int8_gemm_dx (eps, rowsum, v may be NULL when ec_mode = 0).
+ * Out: dX [T, K] fp32 (row stride K).
+ */
+#define S3R_DX_MAX_TERMS 2
+struct s3r_dx_term {
+    const void* Q;               /* [T, N] codes of this term's gradient */
+    const float* tile_scale;     /* its per-tile steps from the quantizer */
+    const void* W8;              /* [K, N] codes of this term's forward weight */
+    const float* eps;            /* [T]    from s3r_ec_correct (EC modes 1, 2) */
+    const int32_t* rowsum;       /* [K] */
+    const float* v;              /* [T/S, K] */
+};
+int int8_gemm_dx_sum(const struct s3r_dx_term* terms, int n_terms, int code_format, int64_t T, int64_t N, int64_t K,
+                     const float* s_x, int ec_mode, int64_t S, float* dX, int accumulate, int* d_status,
+                     cudaStream_t stream);
+
+/*
  * int8_gemm_dw -- weight gradient from the same S8 codes ([S3R] §III-A;
  * §III-D weight-gradient term):
  *   acc[k,n] = sum_tb tile_scale[tb, n/128] * (int32) sum_{t in block tb} X8[t,k] Q[t,n]
@@ -277,7 +306,7 @@ int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int cod
  *   4. dW2 = int8_gemm_dw(A8, Q2)
  *   5. swiglu_quantize(dA, h1, h3) -> Q1, Q3       [tensor ids 1 (W1), 2 (W3)]
  *   6. EC factors for W1 and W3
- *   7. dX  = int8_gemm_dx(Q1, W1_8) + int8_gemm_dx(Q3, W3_8)
+ *   7. dX  = int8_gemm_dx_sum({Q1, W1_8}, {Q3, W3_8})
  *   8. dW1 = int8_gemm_dw(X8, Q1), dW3 = int8_gemm_dw(X8, Q3)
  * Independent SR quantizes each gradient twice (tensor ids + 0x100 for the
  * dW copy) and applies no correction; RTNE applies no correction either.

@@ -9,7 +9,7 @@ The functions carry the C ABI's names (see ``include/s3r.h`` for the exact
 semantics, layouts and citations):
 
     s3r_quantize, indep_sr_quantize, rtne_quantize, swiglu_quantize,
-    s3r_ec_correct, int8_gemm_dx, int8_gemm_dw, ffn_backward
+    s3r_ec_correct, int8_gemm_dx, int8_gemm_dx_sum, int8_gemm_dw, ffn_backward
 
 Outputs may be passed in (then they are written in place) or are allocated
 with torch on the inputs' device.  Codes are int8 tensors (S3R_CODES_S8) or
@@ -60,6 +60,7 @@ _SIGS = {
                                      _VP, _VP, _VP, _VP]),
     "int8_gemm_dx": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _I64, _VP, _INT, _VP,
                             _VP]),
+    "int8_gemm_dx_sum": (_INT, [_VP, _INT, _INT, _I64, _I64, _I64, _VP, _INT, _I64, _VP, _INT, _VP, _VP]),
     "int8_gemm_dw_workspace_size": (_SZ, [_I64, _I64, _I64, _INT]),
     "int8_gemm_dw": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP, _VP,
                             _SZ, _VP, _VP]),
@@ -281,6 +282,41 @@ def int8_gemm_dx(Q, tile_scale, W8, s_x=None, ec_mode=EC_NONE, ec: ECFactors | N
                               _ptr(ec.eps if ec else None), _ptr(ec.rowsum if ec else None),
                               _ptr(ec.v if ec else None), S, _ptr(dX), int(accumulate), _ptr(status),
                               _stream(stream)), "int8_gemm_dx")
+    return dX
+
+
+class _DxTerm(C.Structure):
+    """struct s3r_dx_term"""
+    _fields_ = [("Q", _VP), ("tile_scale", _VP), ("W8", _VP), ("eps", _VP), ("rowsum", _VP), ("v", _VP)]
+
+
+DX_MAX_TERMS = 2
+
+
+def int8_gemm_dx_sum(terms, s_x=None, ec_mode=EC_NONE, S=None, dX=None, accumulate=False, status=None,
+                     stream=None):
+    """dX = sum over terms of the corrected, rescaled Q_i W8_i^T; `terms` is a
+    list of (Q, tile_scale, W8, ec) with ec an ECFactors or None."""
+    if not 1 <= len(terms) <= DX_MAX_TERMS:
+        raise S3RError(f"int8_gemm_dx_sum takes 1..{DX_MAX_TERMS} terms")
+    Q0, _, W0, _ = terms[0]
+    T, N = Q0.shape
+    K = W0.shape[0]
+    for Q, _, W8, _ in terms:
+        if tuple(Q.shape) != (T, N) or tuple(W8.shape) != (K, N):
+            raise S3RError("int8_gemm_dx_sum: every term needs Q [T, N] and W8 [K, N] of the same sizes")
+    fmt = _fmt2(Q0, W0)
+    if dX is None:
+        dX = torch.empty((T, K), dtype=torch.float32, device=Q0.device)
+    S = T if S is None else S
+    arr = (_DxTerm * len(terms))()
+    for i, (Q, sc, W8, ec) in enumerate(terms):
+        if _fmt2(Q, W8) != fmt:
+            raise S3RError("int8_gemm_dx_sum: every term needs the same code format")
+        arr[i] = _DxTerm(_ptr(Q), _ptr(sc), _ptr(W8), _ptr(ec.eps if ec else None),
+                         _ptr(ec.rowsum if ec else None), _ptr(ec.v if ec else None))
+    _check(lib().int8_gemm_dx_sum(C.cast(arr, _VP), len(terms), fmt, T, N, K, _ptr(s_x), ec_mode, S, _ptr(dX),
+                                  int(accumulate), _ptr(status), _stream(stream)), "int8_gemm_dx_sum")
     return dX
 
 

@@ -197,10 +197,9 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     }
     S3R_TRY(mark(6));
     // 7. dX = dX1 + dX3
-    S3R_TRY(int8_gemm_dx(L1.Q, L1.scale, a->W1_8, fmt, T, F, d, a->s_x, ec, L1.eps, L1.rowsum, L1.v, S, a->dX, 0,
-                         st, stream));
-    S3R_TRY(int8_gemm_dx(L3.Q, L3.scale, a->W3_8, fmt, T, F, d, a->s_x, ec, L3.eps, L3.rowsum, L3.v, S, a->dX, 1,
-                         st, stream));
+    const s3r_dx_term terms[2] = {{L1.Q, L1.scale, a->W1_8, L1.eps, L1.rowsum, L1.v},
+                                  {L3.Q, L3.scale, a->W3_8, L3.eps, L3.rowsum, L3.v}};
+    S3R_TRY(int8_gemm_dx_sum(terms, 2, fmt, T, F, d, a->s_x, ec, S, a->dX, 0, st, stream));
     S3R_TRY(mark(7));
     // 8. dW1, dW3
     S3R_TRY(int8_gemm_dw(a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, fmt, T, d, F, a->s_w1, ec,

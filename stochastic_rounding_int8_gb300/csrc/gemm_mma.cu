@@ -237,6 +237,11 @@ using namespace s3r;
 int umma_gemm_dx(const void* Q, const float* tile_scale, const void* W, int64_t T, int64_t N, int64_t K,
                  const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum, const float* v, int64_t S,
                  float* dX, int accumulate, int32_t* dump, int* d_status, cudaStream_t stream);
+int umma_gemm_dx2(const void* Q, const float* tile_scale, const void* W, const float* eps, const int32_t* rowsum,
+                  const float* v, const void* Q3, const float* tile_scale3, const void* W3, const float* eps3,
+                  const int32_t* rowsum3, const float* v3, int64_t T, int64_t N, int64_t K, const float* s_x,
+                  int ec_mode, int64_t S, float* dX, int accumulate, int32_t* dump, int* d_status,
+                  cudaStream_t stream);
 int umma_gemm_dw(const void* X, const void* Q, const float* tile_scale, int64_t T, int64_t K, int64_t N,
                  const float* s_w, int ec_mode, const float* colmean, const float* mu, const int32_t* xsum,
                  const float* p, int64_t S, float* dW, int32_t* dump, int* d_status, cudaStream_t stream);
@@ -314,6 +319,39 @@ extern "C" int int8_gemm_dx(const void* Qv, const float* tile_scale, const void*
     E.C = dX; E.ldc = K; E.s_x = s_x; E.eps = eps; E.rowsum = rowsum; E.v = v; E.accumulate = accumulate;
     E.ec_mode = ec_mode; E.S = S > 0 ? S : T;
     return launch_gemm<kEpiDX>(P, E, stream);
+}
+
+extern "C" int int8_gemm_dx_sum(const struct s3r_dx_term* terms, int n_terms, int code_format, int64_t T,
+                                int64_t N, int64_t K, const float* s_x, int ec_mode, int64_t S, float* dX,
+                                int accumulate, int* d_status, cudaStream_t stream) {
+    if (!terms || n_terms < 1 || n_terms > S3R_DX_MAX_TERMS) return S3R_ERR_ARG;
+    if (T < 0 || N < 0 || K < 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    if (T == 0 || K == 0) return S3R_OK;
+    if (!dX) return S3R_ERR_ARG;
+    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    for (int i = 0; i < n_terms; ++i) {
+        const s3r_dx_term& t = terms[i];
+        if (!t.Q || !t.tile_scale || !t.W8) return S3R_ERR_ARG;
+        if (ec_mode != S3R_EC_NONE && (!t.eps || !t.rowsum || !t.v || S <= 0 || T % S != 0)) return S3R_ERR_ARG;
+    }
+    if (N == 0) return S3R_ERR_SHAPE;
+    if (code_format == S3R_CODES_F16) {
+        const s3r_dx_term& a = terms[0];
+        const s3r_dx_term* b = n_terms > 1 ? &terms[1] : nullptr;
+        return umma_gemm_dx2(a.Q, a.tile_scale, a.W8, a.eps, a.rowsum, a.v, b ? b->Q : nullptr,
+                             b ? b->tile_scale : nullptr, b ? b->W8 : nullptr, b ? b->eps : nullptr,
+                             b ? b->rowsum : nullptr, b ? b->v : nullptr, T, N, K, s_x, ec_mode, S > 0 ? S : T, dX,
+                             accumulate, nullptr, d_status, stream);
+    }
+    // the warp-level path runs one launch per term, the later ones accumulating
+    for (int i = 0; i < n_terms; ++i) {
+        const s3r_dx_term& t = terms[i];
+        int st = int8_gemm_dx(t.Q, t.tile_scale, t.W8, code_format, T, N, K, s_x, ec_mode, t.eps, t.rowsum, t.v, S,
+                              dX, i > 0 ? 1 : accumulate, d_status, stream);
+        if (st) return st;
+    }
+    return S3R_OK;
 }
 
 extern "C" int int8_gemm_dw(const void* X8v, const void* Qv, const float* tile_scale, int code_format, int64_t T,

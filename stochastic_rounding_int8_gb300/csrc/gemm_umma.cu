@@ -13,18 +13,23 @@
 // contraction block and promoted with that block's scale, as the per-tile
 // quantization requires.
 //
-// Kernel layout (one CTA per 128 x 256 output tile, 320 threads):
+// Kernel layout: persistent, one CTA per SM looping over 128 x 256 output
+// tiles (N fastest); 384 threads in three warpgroups:
 //   warp 0      TMA producer: 4-stage ring of 64-deep K slices in smem
 //               (128-byte swizzle), one mbarrier pair per stage;
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (M=128, N=256, K=16) into one of two 256-column fp32
 //               accumulators (double buffer) and commits to mbarriers;
-//   warps 2..9  epilogue: per 128-K block, tcgen05.ld their 32 TMEM lanes x
-//               128 columns, acc = fma(scale, block, acc) in registers; at the
-//               end apply the correction and the 1/s rescale and store fp32.
-// Both products use the same kernel: dX reads K-major operands (Q [T,N] and
-// W [K,N] contract over N); dW reads MN-major operands (X [T,K] and Q [T,N]
-// contract over T), which the UMMA descriptors address directly.
+//   warps 2, 3  idle (they complete warpgroup 0 for the register split);
+//   warps 4..11 epilogue: per 128-K block, tcgen05.ld their 32 TMEM lanes x
+//               128 columns, acc = fma(scale, block, acc) in registers (acc
+//               seeded with minus the correction); at the end of the tile the
+//               1/s rescale and coalesced fp32 stores, while the producer and
+//               the MMA issuer already run the next tile.
+// Warpgroup 0 gives registers to the epilogue warpgroups (setmaxnreg), so a
+// drain keeps four TMEM loads in flight next to the 128 accumulators.
+// The activation gradient may contract two operand pairs into one
+// accumulator (dX = Q1 W1^T + Q3 W3^T), each with its own scales.
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
 #include <cstdio>
 
@@ -42,18 +47,47 @@ constexpr int A_STAGE = BM * BKS * 2;       // 16 KiB
 constexpr int B_STAGE = BN * BKS * 2;       // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int MN_ATOM_BYTES = BKS * 128;    // one 64-wide MN atom column over a 64-deep K slice: 8 KiB
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;               // three warpgroups
+constexpr int EPI_WARP0 = 4;                // epilogue warps 4..11 (warpgroups 1 and 2)
+// Register split (setmaxnreg): warpgroup 0 (producer, MMA issuer, two idle
+// warps) drops to kRegsLow, the epilogue warpgroups rise to kRegsHigh.  The
+// launch holds regs_per_thread * 384 registers; the split needs
+// kRegsLow * 128 + kRegsHigh * 256 of them, so the host refuses to launch a
+// build whose per-thread count is below kMinLaunchRegs (an increase that the
+// pool cannot satisfy would wait forever).
+constexpr int kRegsLow = 40, kRegsHigh = 216;
+constexpr int kMinLaunchRegs = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
+constexpr int EPI_WARPS = 8;
+constexpr int CHUNK = 16;                   // columns per epilogue staging round
+constexpr int STAGE_PITCH = 20;             // floats per staged row: conflict-free 16-byte writes
+constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * STAGE_PITCH * 4;   // 20 KiB
+constexpr int kNbX = 4;                     // dX: examples one 128-row tile may span (S >= 43)
+constexpr int kBch = 8;                     // dW: examples staged per pass
+constexpr int CV_FLOATS = 256 + 2 * kNbX * 128;   // per half; the dW layout (128 + kBch * 128) fits too
+static_assert(128 + kBch * 128 <= CV_FLOATS, "dW column staging fits the dX layout's size");
+constexpr int CV_BYTES = 2 * CV_FLOATS * 4;        // 10 KiB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NUM_BARS * 8 + 16;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + CV_BYTES + 1024 + NUM_BARS * 8 + 16;
+static_assert(SMEM_BYTES + 64 <= 232448, "shared memory budget of one sm_103a CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 enum Epi { kDX = 0, kDW = 1, kDump = 2 };
 
-struct Args {
-    int64_t M, N, K;             // C[M, N] = sum_k A[m, k] B[n, k]
-    const float* scale;          // scale(mt, nt, kb) = scale[mt*sm + nt*sn + kb*sk] (128-granular tiles)
+// One contraction segment: scale(mt, nt, kb) = scale[mt*sm + nt*sn + kb*sk],
+// and for the activation gradient its correction terms.
+struct Segment {
+    const float* scale;
     int64_t sm, sn, sk, nt_limit;
+    int64_t K;                   // contraction length of this segment
+    const float* eps;
+    const int32_t* rowsum;
+    const float* v;
+};
+
+struct Args {
+    int64_t M, N;                // C[M, N] = sum over segments of sum_k A[m, k] B[n, k]
+    Segment seg[2];              // seg[1].K == 0 when there is one segment
     float* C;
     int64_t ldc;
     int32_t* dump;
@@ -61,9 +95,6 @@ struct Args {
     const float* s_col;          // dW: 1/s_w[col] rescale
     int ec_mode;
     int64_t S, B;
-    const float* eps;
-    const int32_t* rowsum;
-    const float* v;
     const float* colmean;
     const float* mu;
     const int32_t* xsum;
@@ -107,6 +138,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if (*abort_flag) return false;
         if (gtime() - t0 > kWaitNs) return false;
     }
+    return true;
+}
+// Bounded wait that ignores the abort flag: used before teardown, where the
+// copies or MMAs still in flight must land whatever the other roles did.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = gtime();
+    while (!mbar_try(bar, parity))
+        if (gtime() - t0 > kWaitNs) return false;
     return true;
 }
 
@@ -158,25 +197,188 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 10 warps: one SM sub-partition hosts three of them, so 16384 / (3 * 32) caps
-// the kernel at 168 registers per thread.
+// Per-tile column vectors, staged in shared memory by the four epilogue warps
+// of each 128-column half (one column per thread, coalesced), so that the
+// per-thread seed and rescale below are branch-free broadcast smem reads:
+//   dX: rowsum_g[128] for g < 2, then v_g[b_lo + i][128] for i < kNbX;
+//   dW: 1/s_w[128], then colmean[b][128] - mu[b] for a chunk of kBch examples.
+// Columns past N are staged as 0.
+__device__ __forceinline__ void half_bar(int half) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + half), "r"(128) : "memory");
+}
+
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Seeds the thread's 128 accumulators (row `row`, columns c0..c0+127) with
+// minus the correction, which does not depend on the contraction:
+//   dX: -(eps_g[t] rowsum_g[k] + v_g[t/S, k]) summed over the terms g;
+//   dW: -(p[k] + sum_b xsum[b, k] (colmean[b, n] - mu[b])).
+// The dW pass also stages 1/s_w for the final rescale.
+template <int EPI>
+__device__ __forceinline__ void seed_tile(const Args& P, float (&acc)[128], float* cv, int64_t row, int64_t m0,
+                                          int64_t c0, int half, int ht) {
+    const bool in = row < P.M;
+    const int64_t cc = c0 + ht;   // the column this thread stages
+    const bool cin = cc < P.N;
+    if (EPI == kDX) {
+        if (!P.ec_mode) {
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            return;
+        }
+        const int64_t b_lo = m0 / P.S;
+        const int64_t b_hi = ((m0 + BM - 1 < P.M ? m0 + BM - 1 : P.M - 1)) / P.S;
+        half_bar(half);   // every thread of the half is past its previous use of cv
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const bool on = g == 0 || P.seg[1].K > 0;
+            cv[g * 128 + ht] = (on && cin) ? (float)__ldg(P.seg[g].rowsum + cc) : 0.0f;
+            for (int i = 0; i < kNbX; ++i)
+                cv[256 + (g * kNbX + i) * 128 + ht] =
+                    (on && cin && b_lo + i <= b_hi) ? __ldg(P.seg[g].v + (b_lo + i) * P.N + cc) : 0.0f;
+        }
+        half_bar(half);
+        const float ep0 = in ? __ldg(P.seg[0].eps + row) : 0.0f;
+        const float ep1 = (in && P.seg[1].K > 0) ? __ldg(P.seg[1].eps + row) : 0.0f;
+        const int i_row = in ? (int)(row / P.S - b_lo) : 0;
+        const float* rs0 = cv;
+        const float* v0 = cv + 256 + i_row * 128;
+#pragma unroll
+        for (int j4 = 0; j4 < 128; j4 += 4) {
+            const float4 r = lds4(rs0 + j4), w = lds4(v0 + j4);
+            acc[j4 + 0] = -fmaf(ep0, r.x, w.x);
+            acc[j4 + 1] = -fmaf(ep0, r.y, w.y);
+            acc[j4 + 2] = -fmaf(ep0, r.z, w.z);
+            acc[j4 + 3] = -fmaf(ep0, r.w, w.w);
+        }
+        if (P.seg[1].K > 0) {
+            const float* rs1 = cv + 128;
+            const float* v1 = cv + 256 + (kNbX + i_row) * 128;
+#pragma unroll
+            for (int j4 = 0; j4 < 128; j4 += 4) {
+                const float4 r = lds4(rs1 + j4), w = lds4(v1 + j4);
+                acc[j4 + 0] = acc[j4 + 0] - fmaf(ep1, r.x, w.x);
+                acc[j4 + 1] = acc[j4 + 1] - fmaf(ep1, r.y, w.y);
+                acc[j4 + 2] = acc[j4 + 2] - fmaf(ep1, r.z, w.z);
+                acc[j4 + 3] = acc[j4 + 3] - fmaf(ep1, r.w, w.w);
+            }
+        }
+    } else {
+        const bool two = P.ec_mode == S3R_EC_TWO_WAY;
+        const float pr = (two && in) ? __ldg(P.p + row) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = pr;
+        const int64_t nb = two ? P.B : 0;
+        for (int64_t b0 = 0; b0 == 0 || b0 < nb; b0 += kBch) {
+            half_bar(half);   // every thread of the half is past its previous use of cv
+            if (b0 == 0) cv[ht] = (P.s_col && cin) ? __frcp_rn(__ldg(P.s_col + cc)) : 1.0f;
+            for (int i = 0; i < kBch; ++i)
+                cv[128 + i * 128 + ht] =
+                    (cin && b0 + i < nb) ? __ldg(P.colmean + (b0 + i) * P.N + cc) - __ldg(P.mu + b0 + i) : 0.0f;
+            half_bar(half);
+            const int64_t nbi = nb - b0 < kBch ? nb - b0 : kBch;
+            for (int64_t i = 0; i < nbi; ++i) {
+                const float xs = in ? (float)__ldg(P.xsum + (b0 + i) * P.M + row) : 0.0f;
+                const float* cm = cv + 128 + i * 128;
+#pragma unroll
+                for (int j4 = 0; j4 < 128; j4 += 4) {
+                    const float4 c4 = lds4(cm + j4);
+                    acc[j4 + 0] = fmaf(xs, c4.x, acc[j4 + 0]);
+                    acc[j4 + 1] = fmaf(xs, c4.y, acc[j4 + 1]);
+                    acc[j4 + 2] = fmaf(xs, c4.z, acc[j4 + 2]);
+                    acc[j4 + 3] = fmaf(xs, c4.w, acc[j4 + 3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = -acc[j];
+    }
+}
+
+// Final epilogue of one warp's 32 x 128 block (thread = row, acc = its 128
+// columns from c0, already corrected): the rescale (times 1/s_x[t] or the
+// staged 1/s_w[n]), then 16-column rounds through the warp's staging buffer
+// so that every global access is a 64-byte row segment (accumulate reads
+// included).
+template <int EPI>
+__device__ __forceinline__ void finish_tile(const Args& P, float (&acc)[128], const float* cv, float* stage,
+                                            int64_t row, int64_t c0, int lane) {
+    if (EPI == kDX && P.s_row) {
+        const float rinv = row < P.M ? __frcp_rn(__ldg(P.s_row + row)) : 1.0f;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = acc[j] * rinv;
+    }
+    if (EPI == kDW && P.s_col) {
+#pragma unroll
+        for (int j4 = 0; j4 < 128; j4 += 4) {
+            const float4 r = lds4(cv + j4);
+            acc[j4 + 0] *= r.x;
+            acc[j4 + 1] *= r.y;
+            acc[j4 + 2] *= r.z;
+            acc[j4 + 3] *= r.w;
+        }
+    }
+    const bool cvec = (P.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(P.C) & 15u) == 0);
+    const bool accum = EPI == kDX && P.accumulate;
+    const int srow = lane >> 2, scol = 4 * (lane & 3);   // store mapping: 8 rows x 4 float4 per instruction
+    const int64_t row0 = row - lane;
+    float* mine = stage + lane * STAGE_PITCH;
+#pragma unroll
+    for (int c = 0; c < 128 / CHUNK; ++c) {
+#pragma unroll
+        for (int j4 = 0; j4 < CHUNK; j4 += 4)
+            *reinterpret_cast<float4*>(mine + j4) = make_float4(acc[CHUNK * c + j4], acc[CHUNK * c + j4 + 1],
+                                                                acc[CHUNK * c + j4 + 2], acc[CHUNK * c + j4 + 3]);
+        __syncwarp();
+        const int64_t col = c0 + CHUNK * c + scol;
+#pragma unroll 1
+        for (int r8 = 0; r8 < 4; ++r8) {
+            const int lr = 8 * r8 + srow;
+            const int64_t grow = row0 + lr;
+            if (grow < P.M && col < P.N) {
+                const float4 v4 = lds4(stage + lr * STAGE_PITCH + scol);
+                float w[4] = {v4.x, v4.y, v4.z, v4.w};
+                float* dst = P.C + grow * P.ldc + col;
+                if (cvec && col + 4 <= P.N) {
+                    if (accum) {
+                        const float4 t = *reinterpret_cast<const float4*>(dst);
+                        w[0] += t.x; w[1] += t.y; w[2] += t.z; w[3] += t.w;
+                    }
+                    *reinterpret_cast<float4*>(dst) = make_float4(w[0], w[1], w[2], w[3]);
+                } else {
+                    for (int j = 0; j < 4; ++j)
+                        if (col + j < P.N) dst[j] = accum ? w[j] + dst[j] : w[j];
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// 12 warps: one SM sub-partition hosts three of them, one per warpgroup, so the
+// launch is capped at 168 registers per thread; after the split a
+// sub-partition holds (40 + 216 + 216) * 32 = 15104 of its 16384.
 template <int EPI, bool MN>
 __global__ void __launch_bounds__(THREADS, 1)
-    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Args P) {
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1, Args P) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+    float* sEpi = reinterpret_cast<float*>(sB + STAGES * B_STAGE);
+    float* sCv = sEpi + EPI_STAGE_BYTES / 4;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sCv) + CV_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     const uint32_t full0 = su32(bars), empty0 = su32(bars + STAGES), tfull0 = su32(bars + 2 * STAGES),
                    tempty0 = su32(bars + 2 * STAGES + 2), done_bar = su32(bars + 2 * STAGES + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
-    const int nkb = (int)s3r_cdiv(P.K, 128);
-    const int nslices = 2 * nkb;
+    const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
+    const int nkb = nkb0 + nkb1;                 // 128-wide blocks per tile
+    // tile counts fit 32 bits: the host caps M and N far below 2^31 * 128
+    const int ntn = (int)s3r_cdiv(P.N, BN), ntiles = (int)s3r_cdiv(P.M, BM) * ntn;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -185,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, 8);
+            mbar_init(tempty0 + 8 * b, EPI_WARPS);
         }
         mbar_init(done_bar, 1);
         abort_flag = 0;
@@ -203,216 +405,176 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     volatile int* abrt = &abort_flag;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
-            int issued = 0;
-            for (int it = 0; it < nslices; ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abrt)) {
-                    *abrt = 1;
-                    break;
+    // Persistent: this CTA owns tiles blockIdx.x, blockIdx.x + gridDim.x, ...;
+    // tiles run along N first.  The smem ring and the TMEM double buffer keep
+    // their phases across tiles, so the next tile's copies and MMAs start while
+    // the epilogue still stores the previous tile.
+    if (warp < EPI_WARP0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp == 0) {
+            if (lane == 0) {
+                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA0) : "memory");
+                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB0) : "memory");
+                if (nkb1) {
+                    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA1) : "memory");
+                    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB1) : "memory");
                 }
-                const uint32_t fb = full0 + 8 * s;
-                mbar_expect_tx(fb, STAGE_BYTES);
-                const int32_t k0 = it * BKS;
-                const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
-                if (!MN) {
-                    tma_load(a_dst, &tmA, k0, (int32_t)m0, fb);
-                    tma_load(b_dst, &tmB, k0, (int32_t)n0, fb);
-                } else {
-                    tma_load(a_dst, &tmA, (int32_t)m0, k0, fb);
-                    tma_load(a_dst + MN_ATOM_BYTES, &tmA, (int32_t)m0 + 64, k0, fb);
+                int it = 0;   // slice counter over the whole persistent run
+                bool ok = true;
+                for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                    const int32_t m0 = (tile / ntn) * BM, n0 = (tile % ntn) * BN;
+                    for (int sl = 0; sl < 2 * nkb; ++sl, ++it) {
+                        const int s = it % STAGES;
+                        if (!mbar_wait(empty0 + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abrt)) {
+                            *abrt = 1;
+                            ok = false;
+                            ++it;
+                            break;
+                        }
+                        const uint32_t fb = full0 + 8 * s;
+                        mbar_expect_tx(fb, STAGE_BYTES);
+                        const bool second = sl >= 2 * nkb0;
+                        const CUtensorMap* mA = second ? &tmA1 : &tmA0;
+                        const CUtensorMap* mB = second ? &tmB1 : &tmB0;
+                        const int32_t k0 = (second ? sl - 2 * nkb0 : sl) * BKS;
+                        const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
+                        if (!MN) {
+                            tma_load(a_dst, mA, k0, m0, fb);
+                            tma_load(b_dst, mB, k0, n0, fb);
+                        } else {
+                            tma_load(a_dst, mA, m0, k0, fb);
+                            tma_load(a_dst + MN_ATOM_BYTES, mA, m0 + 64, k0, fb);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_load(b_dst + j * MN_ATOM_BYTES, &tmB, (int32_t)n0 + 64 * j, k0, fb);
+                            for (int j = 0; j < 4; ++j) tma_load(b_dst + j * MN_ATOM_BYTES, mB, n0 + 64 * j, k0, fb);
+                        }
+                    }
                 }
-                issued = it + 1;
+                // no copy may still be landing in shared memory when the CTA exits
+                const int issued = ok ? it : it - 1;
+                for (int k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+                    mbar_wait_drain(full0 + 8 * (k % STAGES), (uint32_t)(k / STAGES) & 1u);
             }
-            // no copy may still be landing in shared memory when the CTA exits
-            for (int it = issued > STAGES ? issued - STAGES : 0; it < issued; ++it)
-                mbar_wait(full0 + 8 * (it % STAGES), (uint32_t)(it / STAGES) & 1u, abrt);
+        } else if (warp == 1) {
+            if (lane == 0) {
+                constexpr uint32_t idesc = idesc_f16(BM, BN, MN, MN);
+                int it = 0, gkb = 0;   // slice and block counters over the whole run
+                bool ok = true;
+                for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                    for (int kb = 0; kb < nkb; ++kb, ++gkb) {
+                        const int buf = gkb & 1;
+                        if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(gkb >> 1) & 1u) ^ 1u, abrt)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_after();
+                        const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+                        for (int h = 0; h < 2 && ok; ++h, ++it) {
+                            const int s = it % STAGES;
+                            if (!mbar_wait(full0 + 8 * s, (uint32_t)(it / STAGES) & 1u, abrt)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_after();
+                            const uint32_t a0 = su32(sA + s * A_STAGE), b0 = su32(sB + s * B_STAGE);
+#pragma unroll
+                            for (int k16 = 0; k16 < BKS / 16; ++k16) {
+                                uint64_t ad, bd;
+                                if (!MN) {
+                                    ad = sdesc(a0 + 32 * k16, 16, 1024);
+                                    bd = sdesc(b0 + 32 * k16, 16, 1024);
+                                } else {
+                                    ad = sdesc(a0 + 2048 * k16, MN_ATOM_BYTES, 1024);
+                                    bd = sdesc(b0 + 2048 * k16, MN_ATOM_BYTES, 1024);
+                                }
+                                umma_f16(d_tmem, ad, bd, idesc, (h | k16) != 0);
+                            }
+                            umma_commit(empty0 + 8 * s);
+                        }
+                        if (!ok) break;
+                        umma_commit(tfull0 + 8 * buf);
+                    }
+                }
+                if (!ok) *abrt = 1;
+                umma_commit(done_bar);
+                mbar_wait_drain(done_bar, 0);
+            }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN, MN, MN);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int buf = kb & 1;
-                if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(kb >> 1) & 1u) ^ 1u, abrt)) {
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ------------------------------ epilogue ------------------------------
+        // warp w reads TMEM lanes 32 * (w % 4) ..; two warps per lane quarter
+        // split the 256 accumulator columns into halves
+        const int q = warp & 3, ew = warp - EPI_WARP0, half = ew >> 2;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * half);
+        float* stage = sEpi + ew * (32 * STAGE_PITCH);
+        float* cv = sCv + half * CV_FLOATS;
+        const int ht = 32 * q + lane;   // thread index within the half
+        int gkb = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const int mt = tile / ntn, nt = (tile % ntn) * 2 + half;   // 128-wide tile indices
+            const int64_t row = (int64_t)mt * BM + 32 * q + lane;
+            const int64_t c0 = (int64_t)nt * 128;
+            float acc[128];
+            if (EPI != kDump) seed_tile<EPI>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
+            // scale of block kb, loaded one block ahead
+            auto scale_of = [&](int kb) -> float {
+                if (EPI == kDump) return 0.0f;
+                const bool first = kb < nkb0;
+                const int64_t k = first ? kb : kb - nkb0;
+                const float* base = first ? P.seg[0].scale : P.seg[1].scale;
+                const int64_t off = first ? mt * P.seg[0].sm + nt * P.seg[0].sn + k * P.seg[0].sk
+                                          : mt * P.seg[1].sm + nt * P.seg[1].sn + k * P.seg[1].sk;
+                const int64_t lim = first ? P.seg[0].nt_limit : P.seg[1].nt_limit;
+                return nt < lim ? __ldg(base + off) : 0.0f;
+            };
+            float sc_next = nkb > 0 ? scale_of(0) : 0.0f;
+            for (int kb = 0; kb < nkb; ++kb, ++gkb) {
+                const int buf = gkb & 1;
+                const float sc = sc_next;
+                if (kb + 1 < nkb) sc_next = scale_of(kb + 1);
+                // warp-uniform outcome: the tcgen05.ld below needs the whole warp
+                const bool got =
+                    __all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * buf, (uint32_t)(gkb >> 1) & 1u, abrt));
+                if (!got) {
+                    ok = false;
                     *abrt = 1;
                     break;
                 }
                 tc_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
-                bool ok = true;
-                for (int h = 0; h < 2; ++h) {
-                    const int it = 2 * kb + h, s = it % STAGES;
-                    if (!mbar_wait(full0 + 8 * s, (uint32_t)(it / STAGES) & 1u, abrt)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_after();
-                    const uint32_t a0 = su32(sA + s * A_STAGE), b0 = su32(sB + s * B_STAGE);
+                // four 16-column loads in flight per wait (64 registers next to acc[128])
 #pragma unroll
-                    for (int k16 = 0; k16 < BKS / 16; ++k16) {
-                        uint64_t ad, bd;
-                        if (!MN) {
-                            ad = sdesc(a0 + 32 * k16, 16, 1024);
-                            bd = sdesc(b0 + 32 * k16, 16, 1024);
-                        } else {
-                            ad = sdesc(a0 + 2048 * k16, MN_ATOM_BYTES, 1024);
-                            bd = sdesc(b0 + 2048 * k16, MN_ATOM_BYTES, 1024);
+                for (int c = 0; c < 8; c += 4) {
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) tmem_ld16(lane_addr + (uint32_t)(buf * BN + 16 * (c + u)), r[u]);
+                    tmem_wait_ld();
+                    if (EPI == kDump) {
+                        if (row < P.M) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const int64_t col = c0 + 16 * (c + u) + j;
+                                    if (col < P.N)
+                                        P.dump[(row * P.N + col) * nkb + kb] =
+                                            __float2int_rn(__uint_as_float(r[u][j]));
+                                }
                         }
-                        umma_f16(d_tmem, ad, bd, idesc, (h | k16) != 0);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                acc[16 * (c + u) + j] = fmaf(sc, __uint_as_float(r[u][j]), acc[16 * (c + u) + j]);
                     }
-                    umma_commit(empty0 + 8 * s);
                 }
-                if (!ok) {
-                    *abrt = 1;
-                    break;
-                }
-                umma_commit(tfull0 + 8 * buf);
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
             }
-            umma_commit(done_bar);
-            mbar_wait(done_bar, 0, abrt);
-        }
-    } else {
-        // ------------------------------ epilogue ------------------------------
-        const int q = warp & 3, half = (warp - 2) >> 2, ew = warp - 2;
-        const int64_t row = m0 + 32 * q + lane;
-        const int64_t c0 = n0 + 128 * half;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * half);
-        float acc[128];
-#pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-        const int64_t mt = m0 / 128, nt = n0 / 128 + half;
-        const bool has_scale = EPI != kDump && nt < P.nt_limit;
-        const float* scale_ptr = has_scale ? P.scale + mt * P.sm + nt * P.sn : nullptr;
-        float sc_next = (has_scale && nkb > 0) ? __ldg(scale_ptr) : 0.0f;
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int buf = kb & 1;
-            const float sc = sc_next;   // loaded one block ahead
-            if (has_scale && kb + 1 < nkb) sc_next = __ldg(scale_ptr + (int64_t)(kb + 1) * P.sk);
-            // warp-uniform outcome: the tcgen05.ld below needs the whole warp
-            const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * buf, (uint32_t)(kb >> 1) & 1u, abrt));
-            if (!got) {
-                ok = false;
-                *abrt = 1;
-                break;
-            }
-            tc_after();
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t r[16];
-                tmem_ld16(lane_addr + (uint32_t)(buf * BN + 16 * c), r);
-                tmem_wait_ld();
-                if (EPI == kDump) {
-                    if (row < P.M) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int64_t col = c0 + 16 * c + j;
-                            if (col < P.N)
-                                P.dump[(row * P.N + col) * nkb + kb] = __float2int_rn(__uint_as_float(r[j]));
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[16 * c + j] = fmaf(sc, __uint_as_float(r[j]), acc[16 * c + j]);
-                }
-            }
-            tc_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-        }
-        if (EPI != kDump && ok) {
-            // The last accumulator commit retired every MMA, so the operand ring is
-            // free: stage this warp's 32 x 128 fp32 block there (row pitch 132
-            // floats keeps both the row writes and the column reads conflict-free),
-            // then finish row by row with 16-byte coalesced accesses.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            float* stage = reinterpret_cast<float*>(smem) + ew * (32 * 132);
-            float* mine = stage + lane * 132;
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                *reinterpret_cast<float4*>(mine + 4 * c) =
-                    make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
-            __syncwarp();
-            const int64_t col = c0 + 4 * lane;   // this thread's 4 columns
-            const bool vec = (P.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(P.C) & 15u) == 0) && col + 4 <= P.N;
-            float cterm[4] = {0.f, 0.f, 0.f, 0.f}, cscale[4] = {1.f, 1.f, 1.f, 1.f};
-            if (EPI == kDX) {
-                // every row of this tile lies in one example (S % 128 == 0 or one example)
-                if (P.ec_mode) {
-                    const int64_t b = m0 / P.S;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (col + j < P.N) {
-                            cterm[j] = __ldg(P.v + b * P.N + col + j);   // v[b, col]
-                            cscale[j] = (float)__ldg(P.rowsum + col + j);
-                        }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (col + j < P.N && P.s_col) cscale[j] = __ldg(P.s_col + col + j);
-            }
-            for (int r = 0; r < 32; ++r) {
-                const int64_t grow = m0 + 32 * q + r;
-                if (grow >= P.M) break;
-                const float4 a4 = *reinterpret_cast<const float4*>(stage + r * 132 + 4 * lane);
-                float o[4] = {a4.x, a4.y, a4.z, a4.w};
-                float* dst = P.C + grow * P.ldc + col;
-                if (EPI == kDX) {
-                    const float ep = P.ec_mode ? __ldg(P.eps + grow) : 0.0f;
-                    const float sr = P.s_row ? __ldg(P.s_row + grow) : 1.0f;
-                    float old[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (P.accumulate) {
-                        if (vec) {
-                            const float4 t = *reinterpret_cast<const float4*>(dst);
-                            old[0] = t.x; old[1] = t.y; old[2] = t.z; old[3] = t.w;
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                if (col + j < P.N) old[j] = dst[j];
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (P.ec_mode) o[j] = o[j] - fmaf(ep, cscale[j], cterm[j]);
-                        if (P.s_row) o[j] = o[j] / sr;
-                        if (P.accumulate) o[j] = o[j] + old[j];
-                    }
-                } else {
-                    if (P.ec_mode == S3R_EC_TWO_WAY) {
-                        float corr[4];
-                        const float pr = __ldg(P.p + grow);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) corr[j] = pr;
-                        for (int64_t b = 0; b < P.B; ++b) {
-                            const float xs = (float)__ldg(P.xsum + b * P.M + grow);
-                            const float m = __ldg(P.mu + b);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                if (col + j < P.N) corr[j] = fmaf(xs, __ldg(P.colmean + b * P.N + col + j) - m, corr[j]);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) o[j] = o[j] - corr[j];
-                    }
-                    if (P.s_col) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) o[j] = o[j] / cscale[j];
-                    }
-                }
-                if (vec) {
-                    *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (col + j < P.N) dst[j] = o[j];
-                }
-            }
+            if (EPI == kDump || !ok) continue;
+            finish_tile<EPI>(P, acc, cv, stage, row, c0, lane);
         }
     }
     __syncthreads();
@@ -467,8 +629,19 @@ static int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t out
     return S3R_OK;
 }
 
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    return n;
+}
+
 template <int EPI, bool MN>
-static int launch(const CUtensorMap& a, const CUtensorMap& b, const Args& P, cudaStream_t stream) {
+static int launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
+                  const Args& P, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e =
@@ -477,11 +650,25 @@ static int launch(const CUtensorMap& a, const CUtensorMap& b, const Args& P, cud
             (void)cudaGetLastError();
             return s3r_cuda_fail("umma gemm: cudaFuncSetAttribute", e);
         }
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, umma_gemm_kernel<EPI, MN>);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return s3r_cuda_fail("umma gemm: cudaFuncGetAttributes", e);
+        }
+        if (fa.numRegs < kMinLaunchRegs || fa.numRegs > kRegsHigh) {
+            char buf[160];
+            snprintf(buf, sizeof(buf), "kernel built with %d registers per thread; the register split needs %d..%d",
+                     fa.numRegs, kMinLaunchRegs, kRegsHigh);
+            s3r_record_error("umma gemm", buf);
+            return S3R_ERR_UNSUPPORTED;
+        }
         attr = true;
     }
-    if (s3r_cdiv(P.M, BM) > 65535) return S3R_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)s3r_cdiv(P.N, BN), (unsigned)s3r_cdiv(P.M, BM));
-    umma_gemm_kernel<EPI, MN><<<grid, THREADS, SMEM_BYTES, stream>>>(a, b, P);
+    const int64_t ntiles = s3r_cdiv(P.M, BM) * s3r_cdiv(P.N, BN);
+    if (ntiles == 0) return S3R_OK;
+    const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();   // persistent: one CTA per SM
+    umma_gemm_kernel<EPI, MN><<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(a0, b0, a1, b1, P);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
 }
@@ -491,23 +678,62 @@ static int launch(const CUtensorMap& a, const CUtensorMap& b, const Args& P, cud
 
 using namespace s3r;
 
-// dX [T, K] from fp16-carried codes: A = Q [T, N], B = W [K, N] (both K-major).
+static void dx_segment(umma::Segment& g, const float* tile_scale, int64_t N, const float* eps, const int32_t* rowsum,
+                       const float* v) {
+    g.scale = tile_scale; g.sm = s3r_cdiv(N, kTile); g.sn = 0; g.sk = 1; g.nt_limit = INT64_MAX; g.K = N;
+    g.eps = eps; g.rowsum = rowsum; g.v = v;
+}
+
+// dX [T, K] from fp16-carried codes: A = Q [T, N], B = W [K, N] (both K-major);
+// with a second term (Q3, W3) the kernel contracts both into one accumulator:
+// dX = Q W^T + Q3 W3^T, each term with its own tile scales and correction.
+int umma_gemm_dx2(const void* Q, const float* tile_scale, const void* W, const float* eps, const int32_t* rowsum,
+                  const float* v, const void* Q3, const float* tile_scale3, const void* W3, const float* eps3,
+                  const int32_t* rowsum3, const float* v3, int64_t T, int64_t N, int64_t K, const float* s_x,
+                  int ec_mode, int64_t S, float* dX, int accumulate, int32_t* dump, int* d_status,
+                  cudaStream_t stream) {
+    if (!s3r_aligned16(Q) || !s3r_aligned16(W) || N % 8 != 0) return S3R_ERR_ALIGN;
+    if (Q3 && (!s3r_aligned16(Q3) || !s3r_aligned16(W3))) return S3R_ERR_ALIGN;
+    CUtensorMap ma, mb, ma3, mb3;
+    int st = umma::make_map(&ma, Q, N, T, N, umma::BM);
+    if (!st) st = umma::make_map(&mb, W, N, K, N, umma::BN);
+    if (!st && Q3) st = umma::make_map(&ma3, Q3, N, T, N, umma::BM);
+    if (!st && Q3) st = umma::make_map(&mb3, W3, N, K, N, umma::BN);
+    if (st) return st;
+    if (!Q3) {
+        ma3 = ma;
+        mb3 = mb;
+    }
+    if (ec_mode && S > 0 && S < T && S % kTile != 0) {
+        // the epilogue stages v for at most kNbX examples per 128-row tile
+        int64_t nb = 0;
+        for (int64_t m0 = 0; m0 < T; m0 += umma::BM) {
+            const int64_t hi = (m0 + umma::BM - 1 < T ? m0 + umma::BM - 1 : T - 1) / S;
+            if (hi - m0 / S + 1 > nb) nb = hi - m0 / S + 1;
+        }
+        if (nb > umma::kNbX) {
+            char buf[160];
+            snprintf(buf, sizeof(buf), "S = %lld lets a 128-token tile span %lld examples; the fp16-code path takes %d",
+                     (long long)S, (long long)nb, umma::kNbX);
+            s3r_record_error("int8_gemm_dx", buf);
+            return S3R_ERR_UNSUPPORTED;
+        }
+    }
+    umma::Args P{};
+    P.M = T; P.N = K;
+    dx_segment(P.seg[0], tile_scale, N, eps, rowsum, v);
+    if (Q3) dx_segment(P.seg[1], tile_scale3, N, eps3, rowsum3, v3);
+    P.C = dX; P.ldc = K; P.dump = dump; P.s_row = s_x; P.ec_mode = ec_mode; P.S = S > 0 ? S : T;
+    P.accumulate = accumulate; P.d_status = d_status;
+    if (dump) return umma::launch<umma::kDump, false>(ma, mb, ma3, mb3, P, stream);
+    return umma::launch<umma::kDX, false>(ma, mb, ma3, mb3, P, stream);
+}
+
 int umma_gemm_dx(const void* Q, const float* tile_scale, const void* W, int64_t T, int64_t N, int64_t K,
                  const float* s_x, int ec_mode, const float* eps, const int32_t* rowsum, const float* v, int64_t S,
                  float* dX, int accumulate, int32_t* dump, int* d_status, cudaStream_t stream) {
-    if (!s3r_aligned16(Q) || !s3r_aligned16(W) || N % 8 != 0) return S3R_ERR_ALIGN;
-    CUtensorMap ma, mb;
-    int st = umma::make_map(&ma, Q, N, T, N, umma::BM);
-    if (st) return st;
-    st = umma::make_map(&mb, W, N, K, N, umma::BN);
-    if (st) return st;
-    umma::Args P{};
-    P.M = T; P.N = K; P.K = N;
-    P.scale = tile_scale; P.sm = s3r_cdiv(N, kTile); P.sn = 0; P.sk = 1; P.nt_limit = INT64_MAX;
-    P.C = dX; P.ldc = K; P.dump = dump; P.s_row = s_x; P.ec_mode = ec_mode; P.S = S > 0 ? S : T;
-    P.eps = eps; P.rowsum = rowsum; P.v = v; P.accumulate = accumulate; P.d_status = d_status;
-    if (dump) return umma::launch<umma::kDump, false>(ma, mb, P, stream);
-    return umma::launch<umma::kDX, false>(ma, mb, P, stream);
+    return umma_gemm_dx2(Q, tile_scale, W, eps, rowsum, v, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, T, N,
+                         K, s_x, ec_mode, S, dX, accumulate, dump, d_status, stream);
 }
 
 // dW [K, N] from fp16-carried codes: A = X [T, K], B = Q [T, N] (both MN-major, contracted over T).
@@ -521,10 +747,11 @@ int umma_gemm_dw(const void* X, const void* Q, const float* tile_scale, int64_t 
     st = umma::make_map(&mb, Q, N, T, N, 64);
     if (st) return st;
     umma::Args P{};
-    P.M = K; P.N = N; P.K = T;
-    P.scale = tile_scale; P.sm = 0; P.sn = 1; P.sk = s3r_cdiv(N, kTile); P.nt_limit = s3r_cdiv(N, kTile);
+    P.M = K; P.N = N;
+    umma::Segment& g = P.seg[0];
+    g.scale = tile_scale; g.sm = 0; g.sn = 1; g.sk = s3r_cdiv(N, kTile); g.nt_limit = s3r_cdiv(N, kTile); g.K = T;
     P.C = dW; P.ldc = N; P.dump = dump; P.s_col = s_w; P.ec_mode = ec_mode; P.S = S > 0 ? S : T;
     P.B = S > 0 ? T / S : 1; P.colmean = colmean; P.mu = mu; P.xsum = xsum; P.p = p; P.d_status = d_status;
-    if (dump) return umma::launch<umma::kDump, true>(ma, mb, P, stream);
-    return umma::launch<umma::kDW, true>(ma, mb, P, stream);
+    if (dump) return umma::launch<umma::kDump, true>(ma, mb, ma, mb, P, stream);
+    return umma::launch<umma::kDW, true>(ma, mb, ma, mb, P, stream);
 }

@@ -57,8 +57,8 @@ def _staged(s3r, ops, dY, S, rm, ec, seed):
                                                      code_format=cf)
     ec1 = s3r.s3r_ec_correct(q1, T, F, S, ops.W1_8, ops.X8, ecm) if ecm else None
     ec3 = s3r.s3r_ec_correct(q3, T, F, S, ops.W3_8, ops.X8, ecm) if ecm else None
-    dX = s3r.int8_gemm_dx(q1.Q, q1.tile_scale, ops.W1_8, ops.s_x, ecm, ec1, S)
-    s3r.int8_gemm_dx(q3.Q, q3.tile_scale, ops.W3_8, ops.s_x, ecm, ec3, S, dX=dX, accumulate=True)
+    dX = s3r.int8_gemm_dx_sum([(q1.Q, q1.tile_scale, ops.W1_8, ec1), (q3.Q, q3.tile_scale, ops.W3_8, ec3)],
+                              ops.s_x, ecm, S)
     q1w, q3w = out.get("q1r", q1), out.get("q3r", q3)
     dW1 = s3r.int8_gemm_dw(ops.X8, q1w.Q, q1w.tile_scale, ops.s_w1, ecm, ec1, S)
     dW3 = s3r.int8_gemm_dw(ops.X8, q3w.Q, q3w.tile_scale, ops.s_w3, ecm, ec3, S)

@@ -112,6 +112,52 @@ def test_dx_accumulate(s3r, orc, fmt):
     assert torch.allclose(out, base + fresh, rtol=1e-6, atol=1e-6)
 
 
+@FMTS
+@pytest.mark.parametrize("ec_name", ["EC_NONE", "EC_DX_ONLY"])
+@pytest.mark.parametrize("T,K,N,S", [(256, 512, 1024, 256), (384, 200, 264, 128), (300, 136, 384, 300)])
+def test_dx_sum_parity(s3r, orc, fmt, ec_name, T, K, N, S):
+    """Input gradient of a layer that feeds two linears (X -> W1 and X -> W3 of
+    the SwiGLU block): dX = dX1 + dX3, against the sum of the oracle's terms,
+    and against two accumulating int8_gemm_dx calls."""
+    inp1, G1, X8, s_x, W1_8, s_w1 = _linear(orc, T, K, N, S, seed=T + 1)
+    inp3, G3, _, _, W3_8, s_w3 = _linear(orc, T, K, N, S, seed=T + 3)
+    ec_mode = getattr(orc, ec_name)
+    r1 = orc.linear_backward(G1, X8, s_x, W1_8, s_w1, S, mode=orc.S3R, ec_mode=ec_mode, seed=4, tensor_id=1)
+    r3 = orc.linear_backward(G3, X8, s_x, W3_8, s_w3, S, mode=orc.S3R, ec_mode=ec_mode, seed=4, tensor_id=2)
+    c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    terms, qs = [], []
+    for inp, W8, s_w, tid in ((inp1, W1_8, s_w1, 1), (inp3, W3_8, s_w3, 2)):
+        q = s3r.s3r_quantize(inp.dY.cuda(), c(s_x), c(s_w), seed=4, tensor_id=tid, code_format=fmt)
+        ec = s3r.s3r_ec_correct(q, T, N, S, _dev(W8, fmt), _dev(X8, fmt), ec_mode=ec_mode) if ec_mode else None
+        terms.append((q.Q, q.tile_scale, _dev(W8, fmt), ec))
+        qs.append(q)
+    dX = s3r.int8_gemm_dx_sum(terms, c(s_x), ec_mode, S)
+    two = s3r.int8_gemm_dx(*terms[0][:3], c(s_x), ec_mode, terms[0][3], S)
+    s3r.int8_gemm_dx(*terms[1][:3], c(s_x), ec_mode, terms[1][3], S, dX=two, accumulate=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes(qs[0].Q), r1.Q) and np.array_equal(codes(qs[1].Q), r3.Q)
+    args = lambda r, W8: (r.Q, r.delta, W8, s_x) + ((r.eps, r.rowsum, r.v, S) if ec_mode else ())
+    mag = dx_magnitude(*args(r1, W1_8)) + dx_magnitude(*args(r3, W3_8))
+    assert_close_mag(dX.cpu().numpy(), r1.dX + r3.dX, mag, "dX1 + dX3")
+    assert_close_mag(dX.cpu().numpy(), two.cpu().numpy().astype(np.float64), mag, "fused vs two calls")
+
+
+def test_dx_sum_accumulate_and_single_term(s3r):
+    rng = np.random.default_rng(2)
+    T, N, K = 256, 256, 384
+    Q, W8 = _i8(rng, T, N), _i8(rng, K, N)
+    sc = (rng.random((2, 2)) + 0.5).astype(np.float32)
+    c = lambda a: torch.from_numpy(a).cuda()
+    one = s3r.int8_gemm_dx_sum([(_dev(Q, 1), c(sc), _dev(W8, 1), None)])
+    ref = s3r.int8_gemm_dx(_dev(Q, 1), c(sc), _dev(W8, 1))
+    base = torch.randn(T, K, device="cuda")
+    out = base.clone()
+    s3r.int8_gemm_dx_sum([(_dev(Q, 1), c(sc), _dev(W8, 1), None)], dX=out, accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.equal(one, ref)
+    assert torch.allclose(out, base + ref, rtol=1e-6, atol=1e-6)
+
+
 @pytest.mark.parametrize("fmt,ec_name", [(1, "EC_DX_ONLY"), (1, "EC_TWO_WAY"), (0, "EC_TWO_WAY")])
 def test_ffn_w2_gemms_full_size_sampled(s3r, orc, fmt, ec_name):
     """The W2 linear of the d=2048, F=5632, T=8192 (4 x 2048) SwiGLU block at
