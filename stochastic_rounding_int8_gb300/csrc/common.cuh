@@ -134,6 +134,17 @@ __device__ __forceinline__ void set_status(int* d_status, int code) {
 void s3r_count_launch();
 void s3r_record_error(const char* where, const char* what);
 int s3r_cuda_fail(const char* where, cudaError_t err);
+
+// S3R-EC factors of the two linears that read the same input X (W1 and W3 of
+// the SwiGLU block) in one pass; bit-identical to two s3r_ec_correct calls
+// (ec.cu).
+size_t s3r_ec_pair_workspace_size(int64_t T, int64_t K);
+int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, float* eps1, float* mu1,
+                        float* colmean1, int32_t* rowsum1, float* v1, int32_t* xsum1, float* p1, const float* tok3,
+                        const float* col3, const void* W3_8, float* eps3, float* mu3, float* colmean3,
+                        int32_t* rowsum3, float* v3, int32_t* xsum3, float* p3, int64_t T, int64_t N, int64_t S,
+                        int64_t K, const void* X8, int code_format, int ec_mode, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
 #define S3R_CHECK_LAUNCH()                                               \
     do {                                                                 \
         s3r_count_launch();                                              \

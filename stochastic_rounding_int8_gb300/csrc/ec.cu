@@ -9,7 +9,9 @@
 // sum_b xsum_b (colmean_b - mu_b)^T + X8^T eps.
 //
 // Every reduction runs in a fixed order (no float atomics), so results are
-// deterministic run to run.
+// deterministic run to run.  Up to two linears that share the input X (W1
+// and W3 of the SwiGLU block) are handled by the same launches: their weight
+// rows share one grid and the column sums of X are read once for both.
 #include <cuda_fp16.h>
 
 #include <cstdio>
@@ -21,19 +23,52 @@ namespace s3r {
 __device__ __forceinline__ int code_value(int8_t c) { return c; }
 __device__ __forceinline__ int code_value(__half c) { return __half2int_rn(c); }
 
+constexpr int kMaxJobs = 2;
+
+// One linear's statistics and factors (device pointers).
+struct EcJob {
+    const float* tok;      // [T, ntc] token error partials
+    const float* col;      // [ntr, N] channel error partials
+    const void* W8;        // [K, N] weight codes
+    float* eps;            // [T]
+    float* mu;             // [B]
+    float* colmean;        // [B, N]
+    int32_t* rowsum;       // [K]
+    float* v;              // [B, K]
+    int32_t* xsum;         // [B, K]
+    float* p;              // [K]
+};
+
+struct EcMeansArgs {
+    const float* tok[kMaxJobs];
+    const float* col[kMaxJobs];
+    float* eps[kMaxJobs];
+    float* colmean[kMaxJobs];
+    int64_t T, N, S, ntc, ntr;
+    int* counter;          // column-block counters of the column-sum pass, zeroed here (or null)
+    int ncounter;
+};
+
 // eps[t] = (sum_j tok[t, j]) / N ;  colmean[b, n] = (sum_{tile rows i of b} col[i, n]) / S
-__global__ void ec_means_kernel(const float* tok, const float* col, int64_t T, int64_t N, int64_t S, int64_t ntc,
-                                int64_t ntr, float* eps, float* colmean) {
+// (blockIdx.y selects the linear).
+__global__ void ec_means_kernel(EcMeansArgs A) {
+    const int j = blockIdx.y;
+    const float* tok = j ? A.tok[1] : A.tok[0];
+    const float* col = j ? A.col[1] : A.col[0];
+    float* eps = j ? A.eps[1] : A.eps[0];
+    float* colmean = j ? A.colmean[1] : A.colmean[0];
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t B = T / S;
+    const int64_t T = A.T, N = A.N, S = A.S, B = T / S;
+    if (A.counter && blockIdx.x == 0 && j == 0)
+        for (int c = threadIdx.x; c < A.ncounter; c += blockDim.x) A.counter[c] = 0;
     if (i < T) {
         float s = 0.0f;
-        for (int64_t j = 0; j < ntc; ++j) s += tok[i * ntc + j];
+        for (int64_t c = 0; c < A.ntc; ++c) s += tok[i * A.ntc + c];
         eps[i] = s / (float)N;
     } else if (i < T + B * N) {
         const int64_t k = i - T, b = k / N, n = k % N;
         int64_t r_begin, r_end;
-        if (B == 1) { r_begin = 0; r_end = ntr; }
+        if (B == 1) { r_begin = 0; r_end = A.ntr; }
         else { r_begin = b * (S / kTile); r_end = (b + 1) * (S / kTile); }
         float s = 0.0f;
         for (int64_t r = r_begin; r < r_end; ++r) s += col[r * N + n];
@@ -41,23 +76,33 @@ __global__ void ec_means_kernel(const float* tok, const float* col, int64_t T, i
     }
 }
 
-// mu[b] = (1/S) sum_{t in b} eps[t]
-__global__ void __launch_bounds__(256) ec_mu_kernel(const float* eps, int64_t S, float* mu) {
-    const int64_t b = blockIdx.x;
-    __shared__ float red[256];
+// (sum_{t < S} e[t]) / S over a 256-thread CTA in a fixed order (strided
+// per-thread sums, then a tree); red holds 256 floats.  Every caller gets the
+// same bits.
+__device__ float cta_mean(const float* e, int64_t S, float* red) {
     float s = 0.0f;
-    for (int64_t t = threadIdx.x; t < S; t += 256) s += eps[b * S + t];
+    for (int64_t t = threadIdx.x; t < S; t += 256) s += e[t];
     red[threadIdx.x] = s;
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
         if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) mu[b] = red[0] / (float)S;
+    const float r = red[0] / (float)S;
+    __syncthreads();
+    return r;
 }
 
+// mu[b] = (1/S) sum_{t in b} eps[t]  (used where the factor kernels do not run)
+__global__ void __launch_bounds__(256) ec_mu_kernel(const float* eps, int64_t S, float* mu) {
+    __shared__ float red[256];
+    const float m = cta_mean(eps + (int64_t)blockIdx.x * S, S, red);
+    if (threadIdx.x == 0) mu[blockIdx.x] = m;
+}
+
+// ---------------------------------------------------------------------------
 // Generic (any row length) versions, one warp per weight row / one thread per
-// column: used when rows are not a multiple of 8 codes.
+// column: used when rows are not a multiple of 8 codes or not 16-byte aligned.
 template <typename CodeT>
 __global__ void __launch_bounds__(256) ec_gemv_generic_kernel(const CodeT* W8, int64_t K, int64_t N, int64_t B,
                                                               const float* colmean, const float* mu, int32_t* rowsum,
@@ -79,17 +124,18 @@ __global__ void __launch_bounds__(256) ec_gemv_generic_kernel(const CodeT* W8, i
     }
 }
 
+constexpr int kXsumChunk = 128;   // rows per column-sum chunk (inside one example)
+
 template <typename CodeT>
 __global__ void __launch_bounds__(128) ec_xsum_partial_generic_kernel(const CodeT* X8, int64_t T, int64_t K,
-                                                                      const float* eps, int32_t* xs, float* ps,
-                                                                      int64_t chunk) {
+                                                                      const float* eps, int32_t* xs, float* ps) {
     const int64_t k = (int64_t)blockIdx.x * 128 + threadIdx.x;
     const int64_t c = blockIdx.y;
     if (k >= K) return;
-    const int64_t t_end = min(T, (c + 1) * chunk);
+    const int64_t t_end = min(T, (c + 1) * kXsumChunk);
     int32_t sx = 0;
     float sp = 0.0f;
-    for (int64_t t = c * chunk; t < t_end; ++t) {
+    for (int64_t t = c * kXsumChunk; t < t_end; ++t) {
         const int x = code_value(X8[t * K + k]);
         sx += x;
         sp = fmaf((float)x, eps[t], sp);
@@ -98,7 +144,28 @@ __global__ void __launch_bounds__(128) ec_xsum_partial_generic_kernel(const Code
     ps[c * K + k] = sp;
 }
 
-// 8 consecutive codes starting at p (16-byte aligned rows, 8-code chunks).
+// xsum[b, k] = sum over the chunks of example b; p[k] = sum over all chunks.
+__global__ void ec_xsum_reduce_generic_kernel(const int32_t* xs, const float* ps, int64_t nch, int64_t K, int64_t B,
+                                              int64_t chunks_per_example, int32_t* xsum, float* p) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= K) return;
+    float pk = 0.0f;
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t r0 = b * chunks_per_example, r1 = (B == 1) ? nch : (b + 1) * chunks_per_example;
+        int32_t s = 0;
+        for (int64_t r = r0; r < r1; ++r) {
+            s += xs[r * K + k];
+            pk += ps[r * K + k];
+        }
+        xsum[b * K + k] = s;
+    }
+    p[k] = pk;
+}
+
+// ---------------------------------------------------------------------------
+// Vector path (rows of 8-code multiples, 16-byte aligned).
+
+// 8 consecutive codes starting at p.
 __device__ __forceinline__ void load8(const int8_t* p, float (&f)[8], int& isum) {
     const uint2 w = *reinterpret_cast<const uint2*>(p);
     isum = 0;
@@ -121,166 +188,399 @@ __device__ __forceinline__ void load8(const __half* p, float (&f)[8], int& isum)
 }
 
 // rowsum[k] = sum_n W8[k,n] and v[b,k] = sum_n (colmean[b,n] - mu[b]) W8[k,n].
-// One CTA per 8 weight rows; its 8 warps split the N range, each lane takes 8
-// consecutive channels at a time (one 16-byte load per row), so the centered
-// channel means are read once per CTA and reused for 8 rows.  Partial sums
-// meet in shared memory in a fixed order.  Needs N % 8 == 0 and 16-byte rows;
-// bmax examples per pass.
+// Each CTA first computes every mu[b] (fixed order, the same bits in every
+// CTA; the first CTA of a linear stores them), then stages the centered means
+// of kGemvBch examples in shared memory.  A warp owns kGemvRows weight rows;
+// its lanes stride the row 8 codes (one 16-byte load) at a time and the row
+// sums meet in a butterfly.  CTAs [0, ctas0) serve linear 0, the rest linear 1.
+constexpr int kGemvRows = 2, kGemvBch = 4, kGemvCtaRows = 8 * kGemvRows;
+
+struct EcGemvArgs {
+    const void* W8[kMaxJobs];
+    const float* colmean[kMaxJobs];
+    const float* eps[kMaxJobs];
+    float* mu[kMaxJobs];
+    int32_t* rowsum[kMaxJobs];
+    float* v[kMaxJobs];
+    int64_t K, N, S, B;
+    int ctas0;
+};
+
+// dynamic shared memory: 256 floats (reduction) + B rounded to 4 + kGemvBch * N
+static size_t gemv_smem_bytes(int64_t N, int64_t B) {
+    return (size_t)(256 + ((B + 3) & ~(int64_t)3) + kGemvBch * N) * sizeof(float);
+}
+
 template <typename CodeT>
-__global__ void __launch_bounds__(256) ec_gemv_kernel(const CodeT* W8, int64_t K, int64_t N, int64_t B,
-                                                      const float* colmean, const float* mu, int32_t* rowsum,
-                                                      float* v) {
-    constexpr int ROWS = 8, BCH = 4;
-    __shared__ float red_v[8][ROWS][BCH];
-    __shared__ int red_r[8][ROWS];
+__global__ void __launch_bounds__(256) ec_gemv_kernel(EcGemvArgs A) {
+    extern __shared__ __align__(16) float sm[];
+    const int64_t K = A.K, N = A.N, S = A.S, B = A.B;
+    float* red = sm;
+    float* mu_s = sm + 256;
+    float* cm = mu_s + ((B + 3) & ~(int64_t)3);
+    const int j = (int)blockIdx.x < A.ctas0 ? 0 : 1;
+    const CodeT* W8 = static_cast<const CodeT*>(j ? A.W8[1] : A.W8[0]);
+    const float* colmean = j ? A.colmean[1] : A.colmean[0];
+    const float* eps = j ? A.eps[1] : A.eps[0];
+    int32_t* rowsum = j ? A.rowsum[1] : A.rowsum[0];
+    float* v = j ? A.v[1] : A.v[0];
+    const int64_t cta = j ? blockIdx.x - A.ctas0 : blockIdx.x;
+    for (int64_t b = 0; b < B; ++b) {
+        const float m = cta_mean(eps + b * S, S, red);
+        if (threadIdx.x == 0) mu_s[b] = m;
+    }
+    __syncthreads();
+    if (cta == 0) {
+        float* mu = j ? A.mu[1] : A.mu[0];
+        for (int64_t b = threadIdx.x; b < B; b += 256) mu[b] = mu_s[b];
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t k0 = (int64_t)blockIdx.x * ROWS;
-    const int64_t nchunks = N / 8;                         // 8-channel chunks
-    const int64_t per_warp = (nchunks + 7) / 8;
-    const int64_t ch0 = warp * per_warp, ch1 = min(nchunks, ch0 + per_warp);
-    for (int64_t b0 = 0; b0 < (B > 0 ? B : 1); b0 += BCH) {
-        float acc[ROWS][BCH];
-        int rs[ROWS];
+    const int64_t k0 = cta * kGemvCtaRows + warp * kGemvRows;
+    const int64_t nch = N / 8, n4 = N / 4;
+    for (int64_t b0 = 0; b0 < B; b0 += kGemvBch) {
+        __syncthreads();   // the previous pass is done with cm
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) {
+        for (int q = 0; q < kGemvBch; ++q) {
+            const bool on = b0 + q < B;
+            const float m = on ? mu_s[b0 + q] : 0.0f;
+            for (int64_t i = threadIdx.x; i < n4; i += 256) {
+                float4 c = on ? __ldg(reinterpret_cast<const float4*>(colmean + (b0 + q) * N) + i)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                c.x -= m; c.y -= m; c.z -= m; c.w -= m;
+                reinterpret_cast<float4*>(cm + q * N)[i] = on ? c : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        __syncthreads();
+        float acc[kGemvRows][kGemvBch];
+        int rs[kGemvRows];
+#pragma unroll
+        for (int r = 0; r < kGemvRows; ++r) {
             rs[r] = 0;
 #pragma unroll
-            for (int q = 0; q < BCH; ++q) acc[r][q] = 0.0f;
+            for (int q = 0; q < kGemvBch; ++q) acc[r][q] = 0.0f;
         }
-        float m[BCH];
+        for (int64_t ch = lane; ch < nch; ch += 32) {
+            float w[kGemvRows][8];
 #pragma unroll
-        for (int q = 0; q < BCH; ++q) m[q] = (v && b0 + q < B) ? mu[b0 + q] : 0.0f;
-        for (int64_t ch = ch0 + lane; ch < ch1; ch += 32) {
-            const int64_t n = ch * 8;
-            float cm[BCH][8];
-#pragma unroll
-            for (int q = 0; q < BCH; ++q) {
-                if (v && b0 + q < B) {
-                    const float4 x0 = __ldg(reinterpret_cast<const float4*>(colmean + (b0 + q) * N + n));
-                    const float4 x1 = __ldg(reinterpret_cast<const float4*>(colmean + (b0 + q) * N + n + 4));
-                    cm[q][0] = x0.x - m[q]; cm[q][1] = x0.y - m[q]; cm[q][2] = x0.z - m[q]; cm[q][3] = x0.w - m[q];
-                    cm[q][4] = x1.x - m[q]; cm[q][5] = x1.y - m[q]; cm[q][6] = x1.z - m[q]; cm[q][7] = x1.w - m[q];
+            for (int r = 0; r < kGemvRows; ++r) {
+                int isum = 0;
+                if (k0 + r < K) {
+                    load8(W8 + (k0 + r) * N + 8 * ch, w[r], isum);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) cm[q][i] = 0.0f;
+                    for (int i = 0; i < 8; ++i) w[r][i] = 0.0f;
                 }
+                rs[r] += isum;
             }
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                if (k0 + r >= K) continue;
-                float w[8];
-                int isum;
-                load8(W8 + (k0 + r) * N + n, w, isum);
-                rs[r] += isum;
+            for (int q = 0; q < kGemvBch; ++q) {
+                const float4 c0 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch);
+                const float4 c1 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch + 4);
+                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int q = 0; q < BCH; ++q)
+                for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[r][q] = fmaf(cm[q][i], w[i], acc[r][q]);
+                    for (int i = 0; i < 8; ++i) acc[r][q] = fmaf(c[i], w[r][i], acc[r][q]);
             }
         }
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) {
+        for (int r = 0; r < kGemvRows; ++r) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) rs[r] += __shfl_xor_sync(0xFFFFFFFFu, rs[r], o);
 #pragma unroll
-            for (int q = 0; q < BCH; ++q)
+            for (int q = 0; q < kGemvBch; ++q)
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc[r][q] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][q], o);
         }
         if (lane == 0) {
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                red_r[warp][r] = rs[r];
+            for (int r = 0; r < kGemvRows; ++r) {
+                if (k0 + r >= K) continue;
+                if (b0 == 0) rowsum[k0 + r] = rs[r];
 #pragma unroll
-                for (int q = 0; q < BCH; ++q) red_v[warp][r][q] = acc[r][q];
+                for (int q = 0; q < kGemvBch; ++q)
+                    if (b0 + q < B) v[(b0 + q) * K + k0 + r] = acc[r][q];
             }
         }
-        __syncthreads();
-        if (threadIdx.x < ROWS * BCH) {
-            const int r = threadIdx.x / BCH, q = threadIdx.x % BCH;
-            float sv = 0.0f;
-            int sr = 0;
-            for (int w = 0; w < 8; ++w) {
-                sv += red_v[w][r][q];
-                sr += red_r[w][r];
-            }
-            if (k0 + r < K) {
-                if (b0 == 0 && q == 0) rowsum[k0 + r] = sr;
-                if (v && b0 + q < B) v[(b0 + q) * K + k0 + r] = sv;
-            }
-        }
-        __syncthreads();
-        if (!v) break;
     }
 }
 
-// Two-way factors, first pass over row chunks of CH rows (each inside one
-// example): per chunk c and column k, xs[c, k] = sum_t X8[t,k] and
-// ps[c, k] = sum_t X8[t,k] eps[t].  A CTA covers 256 columns (8 per lane, one
-// 16-byte load per row) and its 8 warps take every 8th row of the chunk.
-constexpr int kXsumChunk = 128;
-template <typename CodeT>
-__global__ void __launch_bounds__(256) ec_xsum_partial_kernel(const CodeT* X8, int64_t T, int64_t K,
-                                                              const float* eps, int32_t* xs, float* ps) {
-    __shared__ float red_p[8][256];
+// Two-way factors over X8 [T, K]: xsum[b, k] = sum_{t in b} X8[t,k] and, per
+// linear j, p_j[k] = sum_t X8[t,k] eps_j[t].  CTA (cb, c) sums the 128-row
+// chunk c over 256 columns (8 per lane, one 16-byte load per row; its 8 warps
+// take every 8th row) into workspace partials; the last CTA of each column
+// block (a counter, no waiting) adds the chunks up in a fixed order.
+struct EcXsumArgs {
+    const void* X8;
+    int64_t T, K, S, B;
+    const float* eps[kMaxJobs];
+    int32_t* xsum[kMaxJobs];   // xsum is the same for every linear; each gets its copy
+    float* p[kMaxJobs];
+    int32_t* xs;               // [nch, K]
+    float* ps;                 // [NJ, nch, K]
+    int* counter;              // [K / 256]
+};
+
+template <typename CodeT, int NJ>
+__global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
+    __shared__ float red_p[NJ][8][256];
     __shared__ int red_x[8][256];
+    __shared__ int last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t T = A.T, K = A.K;
+    const int64_t nch = gridDim.y, c = blockIdx.y;
     const int64_t kc = (int64_t)blockIdx.x * 256 + 8 * lane;
-    const int64_t c = blockIdx.y;
     const int64_t t0 = c * kXsumChunk, t1 = min(T, t0 + kXsumChunk);
-    float sp[8];
-    int sx[8];
+    const CodeT* X8 = static_cast<const CodeT*>(A.X8);
+    {
+        float sp[NJ][8];
+        int sx[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { sp[i] = 0.0f; sx[i] = 0; }
-    if (kc < K) {
-        for (int64_t t = t0 + warp; t < t1; t += 8) {
-            float x[8];
-            int isum;
-            load8(X8 + t * K + kc, x, isum);
-            const float e = __ldg(eps + t);
+        for (int i = 0; i < 8; ++i) {
+            sx[i] = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                sx[i] += (int)x[i];
-                sp[i] = fmaf(x[i], e, sp[i]);
+            for (int jj = 0; jj < NJ; ++jj) sp[jj][i] = 0.0f;
+        }
+        if (kc < K) {
+            for (int64_t t = t0 + warp; t < t1; t += 8) {
+                float x[8];
+                int isum;
+                load8(X8 + t * K + kc, x, isum);
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const float e = __ldg(A.eps[jj] + t);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) sp[jj][i] = fmaf(x[i], e, sp[jj][i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sx[i] += (int)x[i];
             }
         }
-    }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        red_p[warp][8 * lane + i] = sp[i];
-        red_x[warp][8 * lane + i] = sx[i];
+        for (int i = 0; i < 8; ++i) {
+            red_x[warp][8 * lane + i] = sx[i];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) red_p[jj][warp][8 * lane + i] = sp[jj][i];
+        }
     }
     __syncthreads();
     const int64_t k = (int64_t)blockIdx.x * 256 + threadIdx.x;
     if (k < K) {
-        float a = 0.0f;
         int b = 0;
+        float a[NJ];
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) a[jj] = 0.0f;
         for (int w = 0; w < 8; ++w) {
-            a += red_p[w][threadIdx.x];
             b += red_x[w][threadIdx.x];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][threadIdx.x];
         }
-        xs[c * K + k] = b;
-        ps[c * K + k] = a;
+        A.xs[c * K + k] = b;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) A.ps[(jj * nch + c) * K + k] = a[jj];
     }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(A.counter + blockIdx.x, 1) == (int)nch - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // Last CTA of this column block: per example, warp w adds the chunks
+    // c = w, w + 8, ... of that example (8 columns per lane), then the warps'
+    // sums meet in shared memory in warp order; p adds the examples in order.
+    const int64_t B = A.B, cpe = B == 1 ? nch : A.S / kXsumChunk;
+    float pk[NJ];
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
+    for (int64_t b = 0; b < B; ++b) {
+        int sx[8];
+        float sp[NJ][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            sx[i] = 0;
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) sp[jj][i] = 0.0f;
+        }
+        if (kc < K) {
+            for (int64_t cc = b * cpe + warp; cc < (b + 1) * cpe; cc += 8) {
+                const int4 x0 = __ldcg(reinterpret_cast<const int4*>(A.xs + cc * K + kc));
+                const int4 x1 = __ldcg(reinterpret_cast<const int4*>(A.xs + cc * K + kc + 4));
+                sx[0] += x0.x; sx[1] += x0.y; sx[2] += x0.z; sx[3] += x0.w;
+                sx[4] += x1.x; sx[5] += x1.y; sx[6] += x1.z; sx[7] += x1.w;
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const float4 p0 = __ldcg(reinterpret_cast<const float4*>(A.ps + (jj * nch + cc) * K + kc));
+                    const float4 p1 = __ldcg(reinterpret_cast<const float4*>(A.ps + (jj * nch + cc) * K + kc + 4));
+                    sp[jj][0] += p0.x; sp[jj][1] += p0.y; sp[jj][2] += p0.z; sp[jj][3] += p0.w;
+                    sp[jj][4] += p1.x; sp[jj][5] += p1.y; sp[jj][6] += p1.z; sp[jj][7] += p1.w;
+                }
+            }
+        }
+        __syncthreads();   // red_* free again
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            red_x[warp][8 * lane + i] = sx[i];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) red_p[jj][warp][8 * lane + i] = sp[jj][i];
+        }
+        __syncthreads();
+        if (k < K) {
+            int xb = 0;
+            float pb[NJ];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
+            for (int w = 0; w < 8; ++w) {
+                xb += red_x[w][threadIdx.x];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) pb[jj] += red_p[jj][w][threadIdx.x];
+            }
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
+                A.xsum[jj][b * K + k] = xb;
+                pk[jj] += pb[jj];
+            }
+        }
+    }
+    if (k < K) {
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) A.p[jj][k] = pk[jj];
+    }
+    if (threadIdx.x == 0) A.counter[blockIdx.x] = 0;
 }
 
-// Second pass: xsum[b, k] = sum over the chunks of example b; p[k] = sum over all chunks.
-__global__ void ec_xsum_reduce_kernel(const int32_t* xs, const float* ps, int64_t nch, int64_t K, int64_t B,
-                                      int64_t chunks_per_example, int32_t* xsum, float* p) {
-    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= K) return;
-    float pk = 0.0f;
-    for (int64_t b = 0; b < B; ++b) {
-        const int64_t r0 = b * chunks_per_example, r1 = (B == 1) ? nch : (b + 1) * chunks_per_example;
-        int32_t s = 0;
-#pragma unroll 8
-        for (int64_t r = r0; r < r1; ++r) {
-            s += xs[r * K + k];
-            pk += ps[r * K + k];
-        }
-        xsum[b * K + k] = s;
+// Workspace of the column-sum pass for `njobs` linears sharing X8 [T, K].
+static size_t xsum_workspace_bytes(int64_t T, int64_t K, int njobs) {
+    const size_t nch = (size_t)s3r_cdiv(T, kXsumChunk);
+    return nch * (size_t)K * (sizeof(int32_t) + njobs * sizeof(float)) + (size_t)s3r_cdiv(K, 256) * sizeof(int) +
+           512;
+}
+
+template <typename CodeT>
+static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
+                          int ec_mode, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const int64_t B = T / S, ntc = s3r_cdiv(N, kTile), ntr = s3r_cdiv(T, kTile);
+    const bool two = ec_mode == S3R_EC_TWO_WAY;
+    bool vec_w = N % 8 == 0;
+    for (int j = 0; j < nj; ++j) vec_w = vec_w && s3r_aligned16(jobs[j].W8) && s3r_aligned16(jobs[j].colmean);
+    const size_t gsm = gemv_smem_bytes(N, B);
+    vec_w = vec_w && gsm <= 200 * 1024;
+    const bool vec_x = K % 8 == 0 && s3r_aligned16(X8);
+    // workspace: xs [nch, K] | ps [nj, nch, K] | counters
+    const int64_t nch = s3r_cdiv(T, kXsumChunk), ncb = s3r_cdiv(K, 256);
+    int32_t* xs = nullptr;
+    float* ps = nullptr;
+    int* counter = nullptr;
+    if (two) {
+        if (!workspace || workspace_bytes < xsum_workspace_bytes(T, K, nj)) return S3R_ERR_WORKSPACE;
+        uintptr_t base = ((uintptr_t)workspace + 255) & ~(uintptr_t)255;
+        xs = reinterpret_cast<int32_t*>(base);
+        ps = reinterpret_cast<float*>(xs + nch * K);
+        counter = reinterpret_cast<int*>(ps + nj * nch * K);
     }
-    p[k] = pk;
+    {
+        EcMeansArgs M{};
+        for (int j = 0; j < nj; ++j) {
+            M.tok[j] = jobs[j].tok;
+            M.col[j] = jobs[j].col;
+            M.eps[j] = jobs[j].eps;
+            M.colmean[j] = jobs[j].colmean;
+        }
+        M.T = T; M.N = N; M.S = S; M.ntc = ntc; M.ntr = ntr;
+        M.counter = (two && vec_x) ? counter : nullptr;
+        M.ncounter = (int)ncb;
+        dim3 grid((unsigned)s3r_cdiv(T + B * N, 256), (unsigned)nj);
+        ec_means_kernel<<<grid, 256, 0, stream>>>(M);
+        S3R_CHECK_LAUNCH();
+    }
+    if (ec_mode == S3R_EC_NONE || K == 0 || !vec_w) {
+        for (int j = 0; j < nj; ++j) {
+            ec_mu_kernel<<<(unsigned)B, 256, 0, stream>>>(jobs[j].eps, S, jobs[j].mu);
+            S3R_CHECK_LAUNCH();
+        }
+    }
+    if (ec_mode == S3R_EC_NONE || K == 0) return S3R_OK;
+    if (vec_w) {
+        EcGemvArgs G{};
+        for (int j = 0; j < nj; ++j) {
+            G.W8[j] = jobs[j].W8;
+            G.colmean[j] = jobs[j].colmean;
+            G.eps[j] = jobs[j].eps;
+            G.mu[j] = jobs[j].mu;
+            G.rowsum[j] = jobs[j].rowsum;
+            G.v[j] = jobs[j].v;
+        }
+        G.K = K; G.N = N; G.S = S; G.B = B;
+        const int64_t per = s3r_cdiv(K, kGemvCtaRows);
+        G.ctas0 = (int)per;
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(ec_gemv_kernel<CodeT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 200 * 1024);
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                return s3r_cuda_fail("ec gemv: cudaFuncSetAttribute", e);
+            }
+            attr = true;
+        }
+        ec_gemv_kernel<CodeT><<<(unsigned)(per * nj), 256, gsm, stream>>>(G);
+        S3R_CHECK_LAUNCH();
+    } else {
+        for (int j = 0; j < nj; ++j) {
+            ec_gemv_generic_kernel<<<(unsigned)s3r_cdiv(K, 8), 256, 0, stream>>>(
+                static_cast<const CodeT*>(jobs[j].W8), K, N, B, jobs[j].colmean, jobs[j].mu, jobs[j].rowsum,
+                jobs[j].v);
+            S3R_CHECK_LAUNCH();
+        }
+    }
+    if (!two) return S3R_OK;
+    if (vec_x) {
+        EcXsumArgs X{};
+        X.X8 = X8; X.T = T; X.K = K; X.S = S; X.B = B;
+        for (int j = 0; j < nj; ++j) {
+            X.eps[j] = jobs[j].eps;
+            X.xsum[j] = jobs[j].xsum;
+            X.p[j] = jobs[j].p;
+        }
+        X.xs = xs; X.ps = ps; X.counter = counter;
+        dim3 grid((unsigned)ncb, (unsigned)nch);
+        if (nj == 2) ec_xsum_kernel<CodeT, 2><<<grid, 256, 0, stream>>>(X);
+        else ec_xsum_kernel<CodeT, 1><<<grid, 256, 0, stream>>>(X);
+        S3R_CHECK_LAUNCH();
+    } else {
+        for (int j = 0; j < nj; ++j) {
+            dim3 grid((unsigned)s3r_cdiv(K, 128), (unsigned)nch);
+            ec_xsum_partial_generic_kernel<<<grid, 128, 0, stream>>>(static_cast<const CodeT*>(X8), T, K,
+                                                                    jobs[j].eps, xs, ps);
+            S3R_CHECK_LAUNCH();
+            ec_xsum_reduce_generic_kernel<<<(unsigned)s3r_cdiv(K, 256), 256, 0, stream>>>(
+                xs, ps, nch, K, B, S / kXsumChunk, jobs[j].xsum, jobs[j].p);
+            S3R_CHECK_LAUNCH();
+        }
+    }
+    return S3R_OK;
+}
+
+// Checks and dispatch shared by the single-linear C entry point and the
+// two-linear path of the FFN block.
+static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
+                           int code_format, int ec_mode, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    if (T < 0 || N < 0 || K < 0 || S <= 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (T == 0 || N == 0) return S3R_OK;
+    if (T % S != 0) return S3R_ERR_SHAPE;
+    if (S % kTile != 0 && S != T) return S3R_ERR_SHAPE;
+    for (int j = 0; j < nj; ++j) {
+        const EcJob& J = jobs[j];
+        if (!J.tok || !J.col || !J.eps || !J.mu || !J.colmean) return S3R_ERR_ARG;
+        if (ec_mode != S3R_EC_NONE && K > 0 && (!J.W8 || !J.rowsum || !J.v)) return S3R_ERR_ARG;
+        if (ec_mode == S3R_EC_TWO_WAY && K > 0 && (!J.xsum || !J.p)) return S3R_ERR_ARG;
+    }
+    if (ec_mode == S3R_EC_TWO_WAY && K > 0 && !X8) return S3R_ERR_ARG;
+    if (code_format == S3R_CODES_F16)
+        return launch_factors<__half>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, stream);
+    return launch_factors<int8_t>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, stream);
 }
 
 }  // namespace s3r
@@ -289,8 +589,7 @@ using namespace s3r;
 
 extern "C" size_t s3r_ec_workspace_size(int64_t T, int64_t K) {
     if (T <= 0 || K <= 0) return 0;
-    const size_t nch = (size_t)s3r_cdiv(T, kXsumChunk);
-    return nch * (size_t)K * (sizeof(int32_t) + sizeof(float)) + 256;
+    return xsum_workspace_bytes(T, K, 1);
 }
 
 extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
@@ -298,63 +597,26 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
                               float* mu, float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p,
                               void* workspace, size_t workspace_bytes, int* d_status, cudaStream_t stream) {
     (void)d_status;
-    if (T < 0 || N < 0 || K < 0 || S <= 0) return S3R_ERR_ARG;
-    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
-    const bool f16 = code_format == S3R_CODES_F16;
-    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
-    if (T == 0 || N == 0) return S3R_OK;
-    if (T % S != 0) return S3R_ERR_SHAPE;
-    if (S % kTile != 0 && S != T) return S3R_ERR_SHAPE;
-    if (!tok_err_part || !col_err_part || !eps || !mu || !colmean) return S3R_ERR_ARG;
-    const int64_t B = T / S, ntc = s3r_cdiv(N, kTile), ntr = s3r_cdiv(T, kTile);
-    {
-        const int64_t total = T + B * N;
-        ec_means_kernel<<<(unsigned)s3r_cdiv(total, 256), 256, 0, stream>>>(tok_err_part, col_err_part, T, N, S, ntc,
-                                                                          ntr, eps, colmean);
-        S3R_CHECK_LAUNCH();
-        ec_mu_kernel<<<(unsigned)B, 256, 0, stream>>>(eps, S, mu);
-        S3R_CHECK_LAUNCH();
-    }
-    if (ec_mode == S3R_EC_NONE || K == 0) return S3R_OK;
-    if (!W8 || !rowsum || !v) return S3R_ERR_ARG;
-    // vector path: 8 codes per load, so rows (and colmean rows) must start on 16 bytes
-    const bool vec_w = N % 8 == 0 && s3r_aligned16(W8) && s3r_aligned16(colmean);
-    const unsigned gk = (unsigned)s3r_cdiv(K, 8);
-    if (f16) {
-        const __half* w = static_cast<const __half*>(W8);
-        if (vec_w) ec_gemv_kernel<<<gk, 256, 0, stream>>>(w, K, N, B, colmean, mu, rowsum, v);
-        else ec_gemv_generic_kernel<<<gk, 256, 0, stream>>>(w, K, N, B, colmean, mu, rowsum, v);
-    } else {
-        const int8_t* w = static_cast<const int8_t*>(W8);
-        if (vec_w) ec_gemv_kernel<<<gk, 256, 0, stream>>>(w, K, N, B, colmean, mu, rowsum, v);
-        else ec_gemv_generic_kernel<<<gk, 256, 0, stream>>>(w, K, N, B, colmean, mu, rowsum, v);
-    }
-    S3R_CHECK_LAUNCH();
-    if (ec_mode != S3R_EC_TWO_WAY) return S3R_OK;
-    if (!X8 || !xsum || !p) return S3R_ERR_ARG;
-    if (!workspace || workspace_bytes < s3r_ec_workspace_size(T, K)) return S3R_ERR_WORKSPACE;
-    const bool vec_x = K % 8 == 0 && s3r_aligned16(X8);
-    const int64_t nch = s3r_cdiv(T, kXsumChunk);
-    int32_t* xs = static_cast<int32_t*>(workspace);
-    float* ps = reinterpret_cast<float*>(xs + nch * K);
-    if (vec_x) {
-        dim3 grid((unsigned)s3r_cdiv(K, 256), (unsigned)nch);
-        if (f16) ec_xsum_partial_kernel<<<grid, 256, 0, stream>>>(static_cast<const __half*>(X8), T, K, eps, xs, ps);
-        else ec_xsum_partial_kernel<<<grid, 256, 0, stream>>>(static_cast<const int8_t*>(X8), T, K, eps, xs, ps);
-    } else {
-        dim3 grid((unsigned)s3r_cdiv(K, 128), (unsigned)nch);
-        if (f16)
-            ec_xsum_partial_generic_kernel<<<grid, 128, 0, stream>>>(static_cast<const __half*>(X8), T, K, eps, xs, ps,
-                                                                    kXsumChunk);
-        else
-            ec_xsum_partial_generic_kernel<<<grid, 128, 0, stream>>>(static_cast<const int8_t*>(X8), T, K, eps, xs, ps,
-                                                                    kXsumChunk);
-    }
-    S3R_CHECK_LAUNCH();
-    ec_xsum_reduce_kernel<<<(unsigned)s3r_cdiv(K, 256), 256, 0, stream>>>(xs, ps, nch, K, B, S / kXsumChunk, xsum,
-                                                                          p);
-    S3R_CHECK_LAUNCH();
-    return S3R_OK;
+    const EcJob job{tok_err_part, col_err_part, W8, eps, mu, colmean, rowsum, v, xsum, p};
+    return ec_correct_jobs(&job, 1, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, stream);
+}
+
+// The two linears of the SwiGLU block that read the same input X (W1 and W3):
+// the same factors as two s3r_ec_correct calls, bit for bit, in one pass.
+size_t s3r_ec_pair_workspace_size(int64_t T, int64_t K) {
+    if (T <= 0 || K <= 0) return 0;
+    return xsum_workspace_bytes(T, K, 2);
+}
+
+int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, float* eps1, float* mu1,
+                        float* colmean1, int32_t* rowsum1, float* v1, int32_t* xsum1, float* p1, const float* tok3,
+                        const float* col3, const void* W3_8, float* eps3, float* mu3, float* colmean3,
+                        int32_t* rowsum3, float* v3, int32_t* xsum3, float* p3, int64_t T, int64_t N, int64_t S,
+                        int64_t K, const void* X8, int code_format, int ec_mode, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    const EcJob jobs[2] = {{tok1, col1, W1_8, eps1, mu1, colmean1, rowsum1, v1, xsum1, p1},
+                           {tok3, col3, W3_8, eps3, mu3, colmean3, rowsum3, v3, xsum3, p3}};
+    return ec_correct_jobs(jobs, 2, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -374,7 +636,8 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
 // current; the first call on a device does this set-up (call it once before
 // any stream capture).  All calls share the array and it keeps the last
 // call's contents; nothing in it needs to start at zero (every partial it
-// holds is written before it is read).  Calls that overlap on the GPU (two
+// holds is written before it is read, and the column-block counters are
+// zeroed by the first kernel of each call).  Calls that overlap on the GPU (two
 // streams, or two host threads) race on it.
 // ---------------------------------------------------------------------------
 #include <mutex>

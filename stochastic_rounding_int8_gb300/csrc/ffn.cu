@@ -94,7 +94,10 @@ FfnLayout layout(void* base, size_t bytes, int64_t T, int64_t d, int64_t F, int6
     carve_linear(c, Lo.w1, T, F, d, S, round_mode, fmt);   // W1: G = dh1 [T, F], W1 [d, F]
     carve_linear(c, Lo.w3, T, F, d, S, round_mode, fmt);
     Lo.dA = c.take<float>(T * F);
-    Lo.ec_ws_bytes = s3r_ec_workspace_size(T, F > d ? F : d);
+    {   // W2's factors read A8 [T, F]; W1 and W3 share one pass over X8 [T, d]
+        const size_t a = s3r_ec_workspace_size(T, F), b = s3r_ec_pair_workspace_size(T, d);
+        Lo.ec_ws_bytes = a > b ? a : b;
+    }
     Lo.ec_ws = c.take<uint8_t>((int64_t)Lo.ec_ws_bytes);
     const size_t a = int8_gemm_dw_workspace_size(T, F, d, fmt), b = int8_gemm_dw_workspace_size(T, d, F, fmt);
     Lo.dw_ws_bytes = a > b ? a : b;
@@ -190,10 +193,9 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     S3R_TRY(mark(5));
     // 6. correction factors of W1 and W3 (W8 [d, F], X8 [T, d])
     if (ec != S3R_EC_NONE) {
-        S3R_TRY(s3r_ec_correct(L1.tok, L1.col, T, F, S, a->W1_8, d, a->X8, fmt, ec, L1.eps, L1.mu, L1.colmean,
-                               L1.rowsum, L1.v, L1.xsum, L1.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
-        S3R_TRY(s3r_ec_correct(L3.tok, L3.col, T, F, S, a->W3_8, d, a->X8, fmt, ec, L3.eps, L3.mu, L3.colmean,
-                               L3.rowsum, L3.v, L3.xsum, L3.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
+        S3R_TRY(s3r_ec_correct_pair(L1.tok, L1.col, a->W1_8, L1.eps, L1.mu, L1.colmean, L1.rowsum, L1.v, L1.xsum,
+                                    L1.p, L3.tok, L3.col, a->W3_8, L3.eps, L3.mu, L3.colmean, L3.rowsum, L3.v,
+                                    L3.xsum, L3.p, T, F, S, d, a->X8, fmt, ec, Lo.ec_ws, Lo.ec_ws_bytes, stream));
     }
     S3R_TRY(mark(6));
     // 7. dX = dX1 + dX3

@@ -52,7 +52,7 @@ def test_swiglu_quantize_parity(s3r, orc, fmt, mode, T, F):
 @pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("ec_mode", ["EC_DX_ONLY", "EC_TWO_WAY"])
 @pytest.mark.parametrize("T,N,K,S", [(256, 1024, 512, 256), (512, 384, 200, 128), (300, 260, 72, 300),
-                                     (1024, 256, 130, 256)])
+                                     (1024, 256, 130, 256), (1280, 256, 136, 128), (384, 5632, 264, 128)])
 def test_ec_factors_parity(s3r, orc, fmt, ec_mode, T, N, K, S):
     rng = np.random.default_rng(T + N + K)
     G = (rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)
@@ -82,3 +82,21 @@ def test_ec_factors_parity(s3r, orc, fmt, ec_mode, T, N, K, S):
         assert np.array_equal(ec.xsum.cpu().numpy(), xsum)
         p_m = np.abs(X8.astype(np.float64)).T @ (np.abs(eps) + eps_m)
         assert_close_mag(ec.p.cpu().numpy(), p, p_m, "p")
+
+
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
+def test_ec_factors_repeat_bit_identical(s3r, fmt):
+    """Two calls in a row (the column-sum pass keeps per-column-block counters
+    in the workspace) give the same bits, and so does a fresh workspace."""
+    rng = np.random.default_rng(5)
+    T, N, K, S = 1024, 512, 264, 256
+    G = torch.from_numpy((rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)).to(torch.bfloat16).cuda()
+    dt = torch.float16 if fmt else torch.int8
+    W8 = torch.from_numpy(rng.integers(-127, 128, size=(K, N)).astype(np.int8)).to(dt).cuda()
+    X8 = torch.from_numpy(rng.integers(-127, 128, size=(T, K)).astype(np.int8)).to(dt).cuda()
+    q = s3r.s3r_quantize(G, seed=1, tensor_id=3, code_format=fmt)
+    runs = [s3r.s3r_ec_correct(q, T, N, S, W8, X8, ec_mode=s3r.EC_TWO_WAY) for _ in range(3)]
+    torch.cuda.synchronize()
+    for r in runs[1:]:
+        for f in ("eps", "mu", "colmean", "rowsum", "v", "xsum", "p"):
+            assert torch.equal(getattr(r, f), getattr(runs[0], f)), f
