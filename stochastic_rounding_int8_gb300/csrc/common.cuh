@@ -84,7 +84,10 @@ __device__ __forceinline__ float sigmoid_cw(float x) { return 1.0f / (1.0f + exp
 
 // ---------------------------------------------------------------------------
 // Packed fp32 pair arithmetic (sm_100 family): one instruction per two lanes,
-// each rounded to nearest exactly like the scalar operation.
+// each rounded to nearest exactly like the scalar operation.  Caution: ptxas
+// fuses f2_mul followed by an f2_add / f2_sub that is the product's only use
+// into one packed fma despite the .rn qualifiers (measured on sm_103a); where
+// the separate rounding matters, do that add with the scalar __fadd_rn.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
     float2 d;
@@ -118,6 +121,40 @@ __device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
+}
+
+// The SwiGLU derivative terms of two lanes at once, per lane bit-identical to
+//   s = sigmoid_cw(x); silu = x * s; dsilu = s * (1 + x * (1 - s))
+// (exp_cw of -x with the negation folded into the reduction constants, the
+// correctly rounded reciprocal standing for the IEEE quotient 1 / (1 + e)).
+__device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& dsilu) {
+    // exp_cw(-x): clamp, n = rint(-x log2 e), r = -x - n ln2 (two parts), Taylor
+    const float a0 = fminf(fmaxf(-x.x, -87.0f), 88.0f), a1 = fminf(fmaxf(-x.y, -87.0f), 88.0f);
+    const float2 a = make_float2(a0, a1);
+    const float2 t = f2_mul(a, make_float2(1.44269502162933349609375f, 1.44269502162933349609375f));
+    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    float2 r = f2_fma(n, make_float2(-0.693145751953125f, -0.693145751953125f), a);
+    r = f2_fma(n, make_float2(-1.42860682028622683e-06f, -1.42860682028622683e-06f), r);
+    float2 poly = make_float2(1.98412701138295233e-04f, 1.98412701138295233e-04f);
+    poly = f2_fma(poly, r, make_float2(1.38888892251998186e-03f, 1.38888892251998186e-03f));
+    poly = f2_fma(poly, r, make_float2(8.33333376795053482e-03f, 8.33333376795053482e-03f));
+    poly = f2_fma(poly, r, make_float2(4.16666679084300995e-02f, 4.16666679084300995e-02f));
+    poly = f2_fma(poly, r, make_float2(1.66666671633720398e-01f, 1.66666671633720398e-01f));
+    poly = f2_fma(poly, r, make_float2(0.5f, 0.5f));
+    poly = f2_fma(poly, r, make_float2(1.0f, 1.0f));
+    poly = f2_fma(poly, r, make_float2(1.0f, 1.0f));
+    const float2 two_n = make_float2(__int_as_float(((int)n.x + 127) << 23), __int_as_float(((int)n.y + 127) << 23));
+    const float2 e = f2_mul(poly, two_n);
+    const float2 den = f2_add(make_float2(1.0f, 1.0f), e);
+    const float2 s = make_float2(__frcp_rn(den.x), __frcp_rn(den.y));
+    silu = f2_mul(x, s);
+    const float2 one = make_float2(1.0f, 1.0f);
+    // ptxas contracts a packed multiply whose only use is a packed add into a
+    // packed fma, .rn or not; the scalar __fadd_rn is never contracted, so the
+    // product x (1 - s) is rounded on its own as the documented order requires.
+    // (1 + poly 2^n above may fuse: a product with a power of two is exact.)
+    const float2 xt = f2_mul(x, f2_sub(one, s));
+    dsilu = f2_mul(s, make_float2(__fadd_rn(1.0f, xt.x), __fadd_rn(1.0f, xt.y)));
 }
 
 // Record a device-side error (first writer wins is not needed: any error code

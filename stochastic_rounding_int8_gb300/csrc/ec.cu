@@ -14,6 +14,7 @@
 // rows share one grid and the column sums of X are read once for both.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdio>
 
 #include "common.cuh"
@@ -76,28 +77,41 @@ __global__ void ec_means_kernel(EcMeansArgs A) {
     }
 }
 
-// (sum_{t < S} e[t]) / S over a 256-thread CTA in a fixed order (strided
-// per-thread sums, then a tree); red holds 256 floats.  Every caller gets the
-// same bits.
-__device__ float cta_mean(const float* e, int64_t S, float* red) {
-    float s = 0.0f;
-    for (int64_t t = threadIdx.x; t < S; t += 256) s += e[t];
-    red[threadIdx.x] = s;
+// mu[b] = (sum_{t < S} e[b S + t]) / S for b0 <= b < b0 + 8 (and b < B) over a
+// CTA of NT threads in a fixed order: per-thread strided sums, then a tree
+// over the NT partials.  The loads of all eight examples are in flight
+// together.  red holds 8 x NT floats; the results land in out[b].  Every
+// caller with the same NT gets the same bits.
+template <int NT>
+__device__ void cta_means8(const float* e, int64_t S, int64_t B, int64_t b0, float* red, float* out) {
+    float s[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s[q] = 0.0f;
+#pragma unroll 4
+    for (int64_t t = threadIdx.x; t < S; t += NT) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (b0 + q < B) s[q] += e[(b0 + q) * S + t];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) red[q * NT + threadIdx.x] = s[q];
     __syncthreads();
-    for (int w = 128; w > 0; w >>= 1) {
-        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    for (int w = NT / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) red[q * NT + threadIdx.x] += red[q * NT + threadIdx.x + w];
         __syncthreads();
     }
-    const float r = red[0] / (float)S;
+    if (threadIdx.x < 8 && b0 + threadIdx.x < B) out[b0 + threadIdx.x] = red[threadIdx.x * NT] / (float)S;
     __syncthreads();
-    return r;
 }
 
+constexpr int kGemvThreads = 512;
+
 // mu[b] = (1/S) sum_{t in b} eps[t]  (used where the factor kernels do not run)
-__global__ void __launch_bounds__(256) ec_mu_kernel(const float* eps, int64_t S, float* mu) {
-    __shared__ float red[256];
-    const float m = cta_mean(eps + (int64_t)blockIdx.x * S, S, red);
-    if (threadIdx.x == 0) mu[blockIdx.x] = m;
+__global__ void __launch_bounds__(kGemvThreads) ec_mu_kernel(const float* eps, int64_t S, int64_t B, float* mu) {
+    __shared__ float red[8 * kGemvThreads];
+    cta_means8<kGemvThreads>(eps, S, B, (int64_t)blockIdx.x * 8, red, mu);
 }
 
 // ---------------------------------------------------------------------------
@@ -165,35 +179,17 @@ __global__ void ec_xsum_reduce_generic_kernel(const int32_t* xs, const float* ps
 // ---------------------------------------------------------------------------
 // Vector path (rows of 8-code multiples, 16-byte aligned).
 
-// 8 consecutive codes starting at p.
-__device__ __forceinline__ void load8(const int8_t* p, float (&f)[8], int& isum) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    isum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int c = (int)(int8_t)(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFF);
-        f[i] = (float)c;
-        isum += c;
-    }
-}
-__device__ __forceinline__ void load8(const __half* p, float (&f)[8], int& isum) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    isum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[i] = __half2float(__ushort_as_half((unsigned short)(u[i >> 1] >> (16 * (i & 1)))));
-        isum += (int)f[i];
-    }
-}
-
 // rowsum[k] = sum_n W8[k,n] and v[b,k] = sum_n (colmean[b,n] - mu[b]) W8[k,n].
-// Each CTA first computes every mu[b] (fixed order, the same bits in every
-// CTA; the first CTA of a linear stores them), then stages the centered means
-// of kGemvBch examples in shared memory.  A warp owns kGemvRows weight rows;
-// its lanes stride the row 8 codes (one 16-byte load) at a time and the row
-// sums meet in a butterfly.  CTAs [0, ctas0) serve linear 0, the rest linear 1.
-constexpr int kGemvRows = 2, kGemvBch = 4, kGemvCtaRows = 8 * kGemvRows;
+// One 512-thread CTA per SM.  Each CTA first computes every mu[b] (fixed
+// order, the same bits in every CTA; the first CTA of a linear stores them),
+// then stages the centered means of kGemvBch examples in shared memory and
+// streams weight rows: a warp takes kGemvRows rows at a time (rows strided
+// over all warps of the linear); its lanes stride each row 8 codes (one
+// 16-byte load) at a time, issuing the loads of kGemvUnroll chunks of every
+// row before the arithmetic; the row sums meet in a butterfly.  CTAs
+// [0, ctas0) serve linear 0, the rest linear 1.
+constexpr int kGemvRows = 2, kGemvBch = 4, kGemvUnroll = 8;
+constexpr int kGemvWarps = kGemvThreads / 32;
 
 struct EcGemvArgs {
     const void* W8[kMaxJobs];
@@ -203,20 +199,37 @@ struct EcGemvArgs {
     int32_t* rowsum[kMaxJobs];
     float* v[kMaxJobs];
     int64_t K, N, S, B;
-    int ctas0;
+    int ctas0, ctas1;
 };
 
-// dynamic shared memory: 256 floats (reduction) + B rounded to 4 + kGemvBch * N
+// dynamic shared memory: 8 x 512 floats (reductions) + B rounded to 4 + kGemvBch * N
 static size_t gemv_smem_bytes(int64_t N, int64_t B) {
-    return (size_t)(256 + ((B + 3) & ~(int64_t)3) + kGemvBch * N) * sizeof(float);
+    return (size_t)(8 * kGemvThreads + ((B + 3) & ~(int64_t)3) + kGemvBch * N) * sizeof(float);
 }
 
 template <typename CodeT>
-__global__ void __launch_bounds__(256) ec_gemv_kernel(EcGemvArgs A) {
+__device__ __forceinline__ uint4 raw8(const CodeT* p) {
+    if (sizeof(CodeT) == 2) return __ldg(reinterpret_cast<const uint4*>(p));
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+    return make_uint4(w.x, w.y, 0u, 0u);
+}
+// the 8 codes of a raw 16-byte (fp16) or 8-byte (int8) load as floats
+__device__ __forceinline__ void codes8(const uint4& w, float (&f)[8], __half) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __half2float(__ushort_as_half((unsigned short)(u[i >> 1] >> (16 * (i & 1)))));
+}
+__device__ __forceinline__ void codes8(const uint4& w, float (&f)[8], int8_t) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = (float)(int)(int8_t)(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFF);
+}
+
+template <typename CodeT>
+__global__ void __launch_bounds__(kGemvThreads) ec_gemv_kernel(EcGemvArgs A) {
     extern __shared__ __align__(16) float sm[];
     const int64_t K = A.K, N = A.N, S = A.S, B = A.B;
     float* red = sm;
-    float* mu_s = sm + 256;
+    float* mu_s = sm + 8 * kGemvThreads;
     float* cm = mu_s + ((B + 3) & ~(int64_t)3);
     const int j = (int)blockIdx.x < A.ctas0 ? 0 : 1;
     const CodeT* W8 = static_cast<const CodeT*>(j ? A.W8[1] : A.W8[0]);
@@ -225,17 +238,14 @@ __global__ void __launch_bounds__(256) ec_gemv_kernel(EcGemvArgs A) {
     int32_t* rowsum = j ? A.rowsum[1] : A.rowsum[0];
     float* v = j ? A.v[1] : A.v[0];
     const int64_t cta = j ? blockIdx.x - A.ctas0 : blockIdx.x;
-    for (int64_t b = 0; b < B; ++b) {
-        const float m = cta_mean(eps + b * S, S, red);
-        if (threadIdx.x == 0) mu_s[b] = m;
-    }
-    __syncthreads();
+    const int64_t nctas = j ? A.ctas1 : A.ctas0;
+    for (int64_t b0 = 0; b0 < B; b0 += 8) cta_means8<kGemvThreads>(eps, S, B, b0, red, mu_s);
     if (cta == 0) {
         float* mu = j ? A.mu[1] : A.mu[0];
-        for (int64_t b = threadIdx.x; b < B; b += 256) mu[b] = mu_s[b];
+        for (int64_t b = threadIdx.x; b < B; b += kGemvThreads) mu[b] = mu_s[b];
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t k0 = cta * kGemvCtaRows + warp * kGemvRows;
+    const int64_t gw = cta * kGemvWarps + warp, nw = nctas * kGemvWarps;
     const int64_t nch = N / 8, n4 = N / 4;
     for (int64_t b0 = 0; b0 < B; b0 += kGemvBch) {
         __syncthreads();   // the previous pass is done with cm
@@ -243,7 +253,7 @@ __global__ void __launch_bounds__(256) ec_gemv_kernel(EcGemvArgs A) {
         for (int q = 0; q < kGemvBch; ++q) {
             const bool on = b0 + q < B;
             const float m = on ? mu_s[b0 + q] : 0.0f;
-            for (int64_t i = threadIdx.x; i < n4; i += 256) {
+            for (int64_t i = threadIdx.x; i < n4; i += kGemvThreads) {
                 float4 c = on ? __ldg(reinterpret_cast<const float4*>(colmean + (b0 + q) * N) + i)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
                 c.x -= m; c.y -= m; c.z -= m; c.w -= m;
@@ -251,65 +261,81 @@ __global__ void __launch_bounds__(256) ec_gemv_kernel(EcGemvArgs A) {
             }
         }
         __syncthreads();
-        float acc[kGemvRows][kGemvBch];
-        int rs[kGemvRows];
+        for (int64_t k0 = gw * kGemvRows; k0 < K; k0 += nw * kGemvRows) {
+            const CodeT* wrow[kGemvRows];
 #pragma unroll
-        for (int r = 0; r < kGemvRows; ++r) {
-            rs[r] = 0;
-#pragma unroll
-            for (int q = 0; q < kGemvBch; ++q) acc[r][q] = 0.0f;
-        }
-        for (int64_t ch = lane; ch < nch; ch += 32) {
-            float w[kGemvRows][8];
+            for (int r = 0; r < kGemvRows; ++r) wrow[r] = W8 + (k0 + r < K ? k0 + r : K - 1) * N;   // clamped
+            float acc[kGemvRows][kGemvBch];
+            int rs[kGemvRows];
 #pragma unroll
             for (int r = 0; r < kGemvRows; ++r) {
-                int isum = 0;
-                if (k0 + r < K) {
-                    load8(W8 + (k0 + r) * N + 8 * ch, w[r], isum);
-                } else {
+                rs[r] = 0;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) w[r][i] = 0.0f;
+                for (int q = 0; q < kGemvBch; ++q) acc[r][q] = 0.0f;
+            }
+            for (int64_t c0 = 0; c0 < nch; c0 += 32 * kGemvUnroll) {
+                uint4 raw[kGemvUnroll][kGemvRows];
+#pragma unroll
+                for (int u = 0; u < kGemvUnroll; ++u) {
+                    const int64_t ch = c0 + 32 * u + lane;
+                    const int64_t chc = ch < nch ? ch : nch - 1;   // clamped: always a valid load
+#pragma unroll
+                    for (int r = 0; r < kGemvRows; ++r) raw[u][r] = raw8(wrow[r] + 8 * chc);
                 }
-                rs[r] += isum;
+#pragma unroll
+                for (int u = 0; u < kGemvUnroll; ++u) {
+                    const int64_t ch = c0 + 32 * u + lane;
+                    if (ch >= nch) break;
+                    float w[kGemvRows][8];
+#pragma unroll
+                    for (int r = 0; r < kGemvRows; ++r) {
+                        codes8(raw[u][r], w[r], CodeT{});
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) rs[r] += (int)w[r][i];
+                    }
+#pragma unroll
+                    for (int q = 0; q < kGemvBch; ++q) {
+                        const float4 x0 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch);
+                        const float4 x1 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch + 4);
+                        const float c[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                        for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) acc[r][q] = fmaf(c[i], w[r][i], acc[r][q]);
+                    }
+                }
             }
-#pragma unroll
-            for (int q = 0; q < kGemvBch; ++q) {
-                const float4 c0 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch);
-                const float4 c1 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch + 4);
-                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int r = 0; r < kGemvRows; ++r)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[r][q] = fmaf(c[i], w[r][i], acc[r][q]);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kGemvRows; ++r) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) rs[r] += __shfl_xor_sync(0xFFFFFFFFu, rs[r], o);
-#pragma unroll
-            for (int q = 0; q < kGemvBch; ++q)
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[r][q] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][q], o);
-        }
-        if (lane == 0) {
 #pragma unroll
             for (int r = 0; r < kGemvRows; ++r) {
-                if (k0 + r >= K) continue;
-                if (b0 == 0) rowsum[k0 + r] = rs[r];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) rs[r] += __shfl_xor_sync(0xFFFFFFFFu, rs[r], o);
 #pragma unroll
                 for (int q = 0; q < kGemvBch; ++q)
-                    if (b0 + q < B) v[(b0 + q) * K + k0 + r] = acc[r][q];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc[r][q] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][q], o);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < kGemvRows; ++r) {
+                    if (k0 + r >= K) continue;
+                    if (b0 == 0) rowsum[k0 + r] = rs[r];
+#pragma unroll
+                    for (int q = 0; q < kGemvBch; ++q)
+                        if (b0 + q < B) v[(b0 + q) * K + k0 + r] = acc[r][q];
+                }
             }
         }
     }
 }
 
 // Two-way factors over X8 [T, K]: xsum[b, k] = sum_{t in b} X8[t,k] and, per
-// linear j, p_j[k] = sum_t X8[t,k] eps_j[t].  CTA (cb, c) sums the 128-row
-// chunk c over 256 columns (8 per lane, one 16-byte load per row; its 8 warps
-// take every 8th row) into workspace partials; the last CTA of each column
-// block (a counter, no waiting) adds the chunks up in a fixed order.
+// linear j, p_j[k] = sum_t X8[t,k] eps_j[t].  CTA (cb, c) sums the
+// ROWS-row chunk c over 256 columns (8 per lane, one 16-byte load per
+// row; warp w takes rows w, w + 8, ..., all of its loads in flight together)
+// into workspace partials; the last CTA of each column block (a counter, no
+// waiting) adds the chunks up in a fixed order, one column per thread.
+constexpr int kXsumGroup = 16;   // rows whose loads are issued together
+
 struct EcXsumArgs {
     const void* X8;
     int64_t T, K, S, B;
@@ -321,17 +347,20 @@ struct EcXsumArgs {
     int* counter;              // [K / 256]
 };
 
-template <typename CodeT, int NJ>
+template <typename CodeT, int NJ, int ROWS>
 __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
-    __shared__ float red_p[NJ][8][256];
-    __shared__ int red_x[8][256];
+    constexpr int kXsumRowsPerWarp = ROWS / 8;
+    constexpr int P = 33;   // padded pitch: conflict-free writes (lane-major) and reads (column-major)
+    __shared__ float red_p[NJ][8][8 * P];
+    __shared__ int red_x[8][8 * P];
     __shared__ int last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = A.T, K = A.K;
     const int64_t nch = gridDim.y, c = blockIdx.y;
     const int64_t kc = (int64_t)blockIdx.x * 256 + 8 * lane;
-    const int64_t t0 = c * kXsumChunk, t1 = min(T, t0 + kXsumChunk);
+    const int64_t t0 = c * ROWS;
     const CodeT* X8 = static_cast<const CodeT*>(A.X8);
+    const int64_t kcl = kc < K ? kc : K - 8;   // clamped column: always a valid load
     {
         float sp[NJ][8];
         int sx[8];
@@ -341,41 +370,56 @@ __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
 #pragma unroll
             for (int jj = 0; jj < NJ; ++jj) sp[jj][i] = 0.0f;
         }
-        if (kc < K) {
-            for (int64_t t = t0 + warp; t < t1; t += 8) {
+#pragma unroll
+        for (int g = 0; g < kXsumRowsPerWarp; g += kXsumGroup) {
+            uint4 raw[kXsumGroup];
+            float e[NJ][kXsumGroup];
+#pragma unroll
+            for (int u = 0; u < kXsumGroup; ++u) {
+                const int64_t t = t0 + warp + 8 * (g + u);
+                const int64_t tc = t < T ? t : T - 1;   // clamped row
+                raw[u] = raw8(X8 + tc * K + kcl);
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) e[jj][u] = t < T ? __ldg(A.eps[jj] + tc) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kXsumGroup; ++u) {
+                const int64_t t = t0 + warp + 8 * (g + u);
                 float x[8];
-                int isum;
-                load8(X8 + t * K + kc, x, isum);
+                codes8(raw[u], x, CodeT{});
+                if (t < T && kc < K) {
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) {
-                    const float e = __ldg(A.eps[jj] + t);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) sp[jj][i] = fmaf(x[i], e, sp[jj][i]);
+                    for (int i = 0; i < 8; ++i) sx[i] += (int)x[i];
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) sx[i] += (int)x[i];
+                for (int jj = 0; jj < NJ; ++jj)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) sp[jj][i] = fmaf(x[i], e[jj][u], sp[jj][i]);
             }
         }
+        // column 8 * lane + i of this block sits at [i * P + lane]
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            red_x[warp][8 * lane + i] = sx[i];
+            red_x[warp][i * P + lane] = sx[i];
 #pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) red_p[jj][warp][8 * lane + i] = sp[jj][i];
+            for (int jj = 0; jj < NJ; ++jj) red_p[jj][warp][i * P + lane] = sp[jj][i];
         }
     }
     __syncthreads();
     const int64_t k = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const int slot = (threadIdx.x & 7) * P + (threadIdx.x >> 3);
     if (k < K) {
-        int b = 0;
+        int xb = 0;
         float a[NJ];
 #pragma unroll
         for (int jj = 0; jj < NJ; ++jj) a[jj] = 0.0f;
-        for (int w = 0; w < 8; ++w) {
-            b += red_x[w][threadIdx.x];
 #pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][threadIdx.x];
+        for (int w = 0; w < 8; ++w) {
+            xb += red_x[w][slot];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][slot];
         }
-        A.xs[c * K + k] = b;
+        A.xs[c * K + k] = xb;
 #pragma unroll
         for (int jj = 0; jj < NJ; ++jj) A.ps[(jj * nch + c) * K + k] = a[jj];
     }
@@ -385,54 +429,23 @@ __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
     __syncthreads();
     if (!last) return;
     __threadfence();
-    // Last CTA of this column block: per example, warp w adds the chunks
-    // c = w, w + 8, ... of that example (8 columns per lane), then the warps'
-    // sums meet in shared memory in warp order; p adds the examples in order.
-    const int64_t B = A.B, cpe = B == 1 ? nch : A.S / kXsumChunk;
-    float pk[NJ];
+    // Last CTA of this column block: thread = column; per example the chunks
+    // are added in order, then p adds the examples in order.
+    if (k < K) {
+        const int64_t B = A.B, cpe = B == 1 ? nch : A.S / ROWS;
+        float pk[NJ];
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
-    for (int64_t b = 0; b < B; ++b) {
-        int sx[8];
-        float sp[NJ][8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            sx[i] = 0;
-#pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) sp[jj][i] = 0.0f;
-        }
-        if (kc < K) {
-            for (int64_t cc = b * cpe + warp; cc < (b + 1) * cpe; cc += 8) {
-                const int4 x0 = __ldcg(reinterpret_cast<const int4*>(A.xs + cc * K + kc));
-                const int4 x1 = __ldcg(reinterpret_cast<const int4*>(A.xs + cc * K + kc + 4));
-                sx[0] += x0.x; sx[1] += x0.y; sx[2] += x0.z; sx[3] += x0.w;
-                sx[4] += x1.x; sx[5] += x1.y; sx[6] += x1.z; sx[7] += x1.w;
-#pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) {
-                    const float4 p0 = __ldcg(reinterpret_cast<const float4*>(A.ps + (jj * nch + cc) * K + kc));
-                    const float4 p1 = __ldcg(reinterpret_cast<const float4*>(A.ps + (jj * nch + cc) * K + kc + 4));
-                    sp[jj][0] += p0.x; sp[jj][1] += p0.y; sp[jj][2] += p0.z; sp[jj][3] += p0.w;
-                    sp[jj][4] += p1.x; sp[jj][5] += p1.y; sp[jj][6] += p1.z; sp[jj][7] += p1.w;
-                }
-            }
-        }
-        __syncthreads();   // red_* free again
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            red_x[warp][8 * lane + i] = sx[i];
-#pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) red_p[jj][warp][8 * lane + i] = sp[jj][i];
-        }
-        __syncthreads();
-        if (k < K) {
+        for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
+        for (int64_t b = 0; b < B; ++b) {
             int xb = 0;
             float pb[NJ];
 #pragma unroll
             for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
-            for (int w = 0; w < 8; ++w) {
-                xb += red_x[w][threadIdx.x];
+#pragma unroll 8
+            for (int64_t cc = b * cpe; cc < (b + 1) * cpe; ++cc) {
+                xb += __ldcg(A.xs + cc * K + k);
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) pb[jj] += red_p[jj][w][threadIdx.x];
+                for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * nch + cc) * K + k);
             }
 #pragma unroll
             for (int jj = 0; jj < NJ; ++jj) {
@@ -440,8 +453,6 @@ __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
                 pk[jj] += pb[jj];
             }
         }
-    }
-    if (k < K) {
 #pragma unroll
         for (int jj = 0; jj < NJ; ++jj) A.p[jj][k] = pk[jj];
     }
@@ -450,7 +461,7 @@ __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
 
 // Workspace of the column-sum pass for `njobs` linears sharing X8 [T, K].
 static size_t xsum_workspace_bytes(int64_t T, int64_t K, int njobs) {
-    const size_t nch = (size_t)s3r_cdiv(T, kXsumChunk);
+    const size_t nch = (size_t)s3r_cdiv(T, kXsumChunk);   // the generic path's chunks, the finer of the two
     return nch * (size_t)K * (sizeof(int32_t) + njobs * sizeof(float)) + (size_t)s3r_cdiv(K, 256) * sizeof(int) +
            512;
 }
@@ -494,7 +505,7 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
     }
     if (ec_mode == S3R_EC_NONE || K == 0 || !vec_w) {
         for (int j = 0; j < nj; ++j) {
-            ec_mu_kernel<<<(unsigned)B, 256, 0, stream>>>(jobs[j].eps, S, jobs[j].mu);
+            ec_mu_kernel<<<(unsigned)s3r_cdiv(B, 8), kGemvThreads, 0, stream>>>(jobs[j].eps, S, B, jobs[j].mu);
             S3R_CHECK_LAUNCH();
         }
     }
@@ -510,8 +521,17 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
             G.v[j] = jobs[j].v;
         }
         G.K = K; G.N = N; G.S = S; G.B = B;
-        const int64_t per = s3r_cdiv(K, kGemvCtaRows);
+        // persistent: one CTA per SM in all, split evenly between the linears
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess) {
+            (void)cudaGetLastError();
+            sms = 148;
+        }
+        const int64_t need = s3r_cdiv(K, kGemvWarps * kGemvRows);   // CTAs that give every warp a row block
+        const int64_t per = std::min<int64_t>(need, std::max<int64_t>(1, sms / nj));
         G.ctas0 = (int)per;
+        G.ctas1 = nj > 1 ? (int)per : 0;
         static bool attr = false;
         if (!attr) {
             cudaError_t e = cudaFuncSetAttribute(ec_gemv_kernel<CodeT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -522,7 +542,7 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
             }
             attr = true;
         }
-        ec_gemv_kernel<CodeT><<<(unsigned)(per * nj), 256, gsm, stream>>>(G);
+        ec_gemv_kernel<CodeT><<<(unsigned)(per * nj), kGemvThreads, gsm, stream>>>(G);
         S3R_CHECK_LAUNCH();
     } else {
         for (int j = 0; j < nj; ++j) {
@@ -542,9 +562,16 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
             X.p[j] = jobs[j].p;
         }
         X.xs = xs; X.ps = ps; X.counter = counter;
-        dim3 grid((unsigned)ncb, (unsigned)nch);
-        if (nj == 2) ec_xsum_kernel<CodeT, 2><<<grid, 256, 0, stream>>>(X);
-        else ec_xsum_kernel<CodeT, 1><<<grid, 256, 0, stream>>>(X);
+        // 256-row chunks where the examples allow it (chunks never straddle two)
+        const bool wide = B == 1 || S % 256 == 0;
+        dim3 grid((unsigned)ncb, (unsigned)s3r_cdiv(T, wide ? 256 : 128));
+        if (wide) {
+            if (nj == 2) ec_xsum_kernel<CodeT, 2, 256><<<grid, 256, 0, stream>>>(X);
+            else ec_xsum_kernel<CodeT, 1, 256><<<grid, 256, 0, stream>>>(X);
+        } else {
+            if (nj == 2) ec_xsum_kernel<CodeT, 2, 128><<<grid, 256, 0, stream>>>(X);
+            else ec_xsum_kernel<CodeT, 1, 128><<<grid, 256, 0, stream>>>(X);
+        }
         S3R_CHECK_LAUNCH();
     } else {
         for (int j = 0; j < nj; ++j) {

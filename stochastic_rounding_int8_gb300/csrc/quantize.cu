@@ -473,23 +473,28 @@ __global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, Quan
             }
         }
         const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+        // negated folds: (-s_x) * dh * s_w == -((s_x * dh) * s_w) exactly
+        const float nsx = A.s_x ? -sx : -1.0f;
+        const float2 nsx2 = make_float2(nsx, nsx);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            // glue, in the documented order (no contraction: built with -fmad=false)
-            const float s = sigmoid_cw(x1[i]);
-            const float silu = x1[i] * s;
-            const float dsilu = s * (1.0f + x1[i] * (1.0f - s));
-            const float dh1 = (da[i] * x3[i]) * dsilu;
-            const float dh3 = da[i] * silu;
-            // negated folds: (-s_x) * dh * s_w == -((s_x * dh) * s_w) exactly
-            const float nsx = A.s_x ? -sx : -1.0f;
-            float v1 = nsx * dh1, v3 = nsx * dh3;
-            if (A.s_w1) v1 = v1 * sw1[i];
-            if (A.s_w3) v3 = v3 * sw3[i];
-            g1[j][i] = v1;
-            g3[j][i] = v3;
-            amax1 = max(amax1, __float_as_uint(v1) & 0x7FFFFFFFu);
-            amax3 = max(amax3, __float_as_uint(v3) & 0x7FFFFFFFu);
+        for (int i = 0; i < 8; i += 2) {
+            // glue, in the documented order, two lanes per packed instruction
+            // (no contraction: built with -fmad=false)
+            const float2 x = make_float2(x1[i], x1[i + 1]);
+            const float2 d2 = make_float2(da[i], da[i + 1]);
+            float2 silu, dsilu;
+            swiglu_terms2(x, silu, dsilu);
+            const float2 dh1 = f2_mul(f2_mul(d2, make_float2(x3[i], x3[i + 1])), dsilu);
+            const float2 dh3 = f2_mul(d2, silu);
+            float2 v1 = f2_mul(nsx2, dh1), v3 = f2_mul(nsx2, dh3);
+            if (A.s_w1) v1 = f2_mul(v1, make_float2(sw1[i], sw1[i + 1]));
+            if (A.s_w3) v3 = f2_mul(v3, make_float2(sw3[i], sw3[i + 1]));
+            g1[j][i] = v1.x;
+            g1[j][i + 1] = v1.y;
+            g3[j][i] = v3.x;
+            g3[j][i + 1] = v3.y;
+            amax1 = max(amax1, max(__float_as_uint(v1.x) & 0x7FFFFFFFu, __float_as_uint(v1.y) & 0x7FFFFFFFu));
+            amax3 = max(amax3, max(__float_as_uint(v3.x) & 0x7FFFFFFFu, __float_as_uint(v3.y) & 0x7FFFFFFFu));
         }
     }
     amax1 = block_max_u32<Geo::kWarps>(amax1, red);
