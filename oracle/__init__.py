@@ -376,24 +376,96 @@ class FFNBackward:
 
 
 def ffn_backward(ops: FFNForwardOperands, h1, h3, dY, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0,
-                 rows=None, krows_d=None, krows_f=None) -> FFNBackward:
+                 rows=None, krows_d=None, krows_f=None, tid_base=0) -> FFNBackward:
     """SwiGLU FFN block backward: W2 linear, then the SwiGLU glue, then W1 and
     W3 (dX = dX1 + dX3).  dA is needed for every token (the glue feeds the
     second quantization), so the W2 activation gradient is computed in full
-    and rounded to fp32 before the glue, the precision the kernels hand on."""
+    and rounded to fp32 before the glue, the precision the kernels hand on.
+    The three linears use tensor ids tid_base + (0, 1, 2)."""
     T = dY.shape[0]
     F = ops.A8.shape[1]
     d = ops.X8.shape[1]
     rows = np.arange(T) if rows is None else np.asarray(rows)
     krows_d = np.arange(d) if krows_d is None else np.asarray(krows_d)
     krows_f = np.arange(F) if krows_f is None else np.asarray(krows_f)
-    w2 = linear_backward(dY, ops.A8, ops.s_a, ops.W2_8, ops.s_w2, S, mode, ec_mode, seed, TID_W2,
+    w2 = linear_backward(dY, ops.A8, ops.s_a, ops.W2_8, ops.s_w2, S, mode, ec_mode, seed, tid_base + TID_W2,
                          rows=np.arange(T), krows=krows_f)
     dA = w2.dX.astype(np.float32)
     dh1, dh3 = swiglu_bwd(dA, h1, h3)
-    w1 = linear_backward(dh1, ops.X8, ops.s_x, ops.W1_8, ops.s_w1, S, mode, ec_mode, seed, TID_W1,
+    w1 = linear_backward(dh1, ops.X8, ops.s_x, ops.W1_8, ops.s_w1, S, mode, ec_mode, seed, tid_base + TID_W1,
                          rows=rows, krows=krows_d)
-    w3 = linear_backward(dh3, ops.X8, ops.s_x, ops.W3_8, ops.s_w3, S, mode, ec_mode, seed, TID_W3,
+    w3 = linear_backward(dh3, ops.X8, ops.s_x, ops.W3_8, ops.s_w3, S, mode, ec_mode, seed, tid_base + TID_W3,
                          rows=rows, krows=krows_d)
     return FFNBackward(w2=w2, w1=w1, w3=w3, dA=dA, dh1=dh1, dh3=dh3,
                        dX=w1.dX + w3.dX, dW1=w1.dW, dW2=w2.dW, dW3=w3.dW)
+
+
+# --------------------------------------------------------------------------
+# grouped (mixture-of-experts) mode
+# --------------------------------------------------------------------------
+# Expert e's three linears use tensor ids MOE_TID_STRIDE * e + (W2, W1, W3).
+MOE_TID_STRIDE = 16
+
+
+@dataclass
+class MoEForwardOperands:
+    X8: np.ndarray      # [R, d] routed rows, expert-sorted, per-row scales
+    s_x: np.ndarray
+    A8: np.ndarray      # [R, F]
+    s_a: np.ndarray
+    W1_8: np.ndarray    # [E, d, F], per-expert per-output-channel scales [E, F]
+    s_w1: np.ndarray
+    W3_8: np.ndarray
+    s_w3: np.ndarray
+    W2_8: np.ndarray    # [E, F, d], scales [E, d]
+    s_w2: np.ndarray
+
+    def expert(self, e: int, r0: int, r1: int) -> FFNForwardOperands:
+        return FFNForwardOperands(self.X8[r0:r1], self.s_x[r0:r1], self.A8[r0:r1], self.s_a[r0:r1],
+                                  self.W1_8[e], self.s_w1[e], self.W3_8[e], self.s_w3[e], self.W2_8[e],
+                                  self.s_w2[e])
+
+
+def moe_forward_operands(X, W1, W3, W2, a) -> MoEForwardOperands:
+    """RTNE forward operands of the routed rows (per-row scales) and of every
+    expert's weights (per-output-channel scales within the expert)."""
+    X8, s_x = rtne_operand(X, 0)
+    A8, s_a = rtne_operand(a, 0)
+    w = [[rtne_operand(Wk[e], 1) for e in range(Wk.shape[0])] for Wk in (W1, W3, W2)]
+    st = lambda k, i: np.stack([w[k][e][i] for e in range(len(w[k]))])
+    return MoEForwardOperands(X8, s_x, A8, s_a, st(0, 0), st(0, 1), st(1, 0), st(1, 1), st(2, 0), st(2, 1))
+
+
+@dataclass
+class MoEBackward:
+    dX: np.ndarray      # [R, d] float64 (zero-size groups leave no rows)
+    dW1: np.ndarray     # [E, d, F] float64 (an empty expert's gradients are zero)
+    dW3: np.ndarray
+    dW2: np.ndarray     # [E, F, d]
+    experts: list       # FFNBackward per expert (None for an empty group)
+
+
+def moe_ffn_backward(ops: MoEForwardOperands, h1, h3, dY, offsets, mode=S3R, ec_mode=EC_TWO_WAY,
+                     seed=0) -> MoEBackward:
+    """Grouped SwiGLU FFN backward over expert-sorted routed rows ([S3R] §IV,
+    MoE models): expert e owns rows offsets[e] .. offsets[e+1] and runs the
+    whole block backward on them as one example, with its own weights; tiles
+    and token indices restart at the group's first row, and its tensor ids
+    are MOE_TID_STRIDE * e + (0, 1, 2)."""
+    E = ops.W1_8.shape[0]
+    R, d = ops.X8.shape
+    F = ops.A8.shape[1]
+    dX = np.zeros((R, d))
+    dW1, dW3, dW2 = np.zeros((E, d, F)), np.zeros((E, d, F)), np.zeros((E, F, d))
+    per = []
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            per.append(None)
+            continue
+        b = ffn_backward(ops.expert(e, r0, r1), h1[r0:r1], h3[r0:r1], dY[r0:r1], r1 - r0, mode, ec_mode, seed,
+                         tid_base=MOE_TID_STRIDE * e)
+        dX[r0:r1] = b.dX
+        dW1[e], dW3[e], dW2[e] = b.dW1, b.dW3, b.dW2
+        per.append(b)
+    return MoEBackward(dX, dW1, dW3, dW2, per)
