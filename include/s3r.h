@@ -312,7 +312,28 @@ int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int cod
  * dW copy) and applies no correction; RTNE applies no correction either.
  * All buffers are device pointers owned by the caller; `args` itself is a
  * HOST pointer read during the call only.
+ *
+ * Grouped (mixture-of-experts) mode, num_groups = E > 0 (the MoE models of
+ * [S3R] §IV; the pages give no grouping rule, so the plain one): the T rows
+ * of dY, h1, h3, X8/s_x, A8/s_a and dX are routed rows sorted by expert, and
+ * expert e owns rows group_offsets[e] .. group_offsets[e+1] (a HOST array of
+ * E + 1 non-decreasing offsets, group_offsets[0] = 0, group_offsets[E] = T).
+ * The weights are stacked per expert -- W1_8, W3_8 [E, d, F], s_w1, s_w3
+ * [E, F], W2_8 [E, F, d], s_w2 [E, d] -- and so are dW1, dW3 [E, d, F] and
+ * dW2 [E, F, d].  Each expert runs steps 1-8 on its own rows as one example
+ * (S is ignored): tiles and token indices restart at the group's first row
+ * and its tensor ids are S3R_MOE_TID_STRIDE * e + (0, 1, 2).  An expert
+ * without rows gets zero weight gradients.  Row offsets must keep the bases
+ * 16-byte aligned (d and F multiples of 8 for fp16 codes, of 16 for int8).
+ * workspace: s3r_ffn_workspace_size(Tmax, d, F, Tmax, ...) with Tmax the
+ * largest group; step events: event 0 before the first expert, the others
+ * after the last.
  */
+#define S3R_TID_W2 0u
+#define S3R_TID_W1 1u
+#define S3R_TID_W3 2u
+#define S3R_TID_RHS_OFFSET 0x100u   /* independent SR: tensor-id offset of the dW copy */
+#define S3R_MOE_TID_STRIDE 16u      /* grouped mode: expert e uses ids 16 e + (0, 1, 2) */
 struct s3r_ffn_args {
     int64_t T, d, F, S;          /* tokens, model width, FFN width, tokens per example */
     const void* dY;              /* bf16 [T, d] upstream gradient */
@@ -342,6 +363,8 @@ struct s3r_ffn_args {
     void** step_events;          /* NULL, or S3R_FFN_NUM_EVENTS cudaEvent_t (a HOST array of handles)
                                     recorded on `stream` at the step boundaries: before step 1 and
                                     after steps 1, 2, 3, 4, 5, 6, 7, 8 above (for timing) */
+    int64_t num_groups;          /* 0: one dense block; E > 0: grouped mode (above) */
+    const int64_t* group_offsets; /* grouped mode: HOST [E + 1] row offsets */
 };
 #define S3R_FFN_NUM_EVENTS 9
 size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,

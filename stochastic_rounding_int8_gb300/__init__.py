@@ -35,6 +35,7 @@ ROUND_RTNE, ROUND_S3R, ROUND_INDEP = 0, 1, 2
 EC_NONE, EC_DX_ONLY, EC_TWO_WAY = 0, 1, 2
 AXIS_ROW, AXIS_COL, AXIS_TILE = 0, 1, 2
 TID_W2, TID_W1, TID_W3, RHS_ID_OFFSET = 0, 1, 2, 0x100
+MOE_TID_STRIDE = 16   # grouped mode: expert e uses tensor ids 16 e + (0, 1, 2)
 CODES_S8, CODES_F16 = 0, 1
 DEFAULT_CODES = CODES_F16
 _CODE_DTYPE = {CODES_S8: torch.int8, CODES_F16: torch.float16}
@@ -371,7 +372,8 @@ class _FfnArgs(C.Structure):
                 ("round_mode", C.c_int), ("ec_mode", C.c_int), ("code_format", C.c_int), ("seed", C.c_uint64),
                 ("dX", _VP), ("dW1", _VP), ("dW3", _VP), ("dW2", _VP),
                 ("workspace", _VP), ("workspace_bytes", C.c_size_t), ("d_status", _VP),
-                ("step_events", C.POINTER(C.c_void_p))]
+                ("step_events", C.POINTER(C.c_void_p)), ("num_groups", C.c_int64),
+                ("group_offsets", C.POINTER(C.c_int64))]
 
 
 FFN_NUM_EVENTS = 9
@@ -425,17 +427,49 @@ def alloc_ffn_grads(T, d, F, device="cuda") -> FFNGrads:
     return FFNGrads(f(T, d), f(d, F), f(d, F), f(F, d))
 
 
+def moe_forward_operands(X, W1, W3, W2, a, h1, h3, stream=None, code_format=DEFAULT_CODES) -> FFNOperands:
+    """Grouped mode: RTNE operands of the expert-sorted routed rows (per-row
+    scales) and of every expert's stacked weights W1, W3 [E, d, F], W2 [E, F, d]
+    (per-output-channel scales within each expert)."""
+    cf = code_format
+    X8, s_x = rtne_quantize(X, AXIS_ROW, stream=stream, code_format=cf)
+    A8, s_a = rtne_quantize(a, AXIS_ROW, stream=stream, code_format=cf)
+    out = []
+    for Wk in (W1, W3, W2):
+        codes, scales = zip(*[rtne_quantize(Wk[e], AXIS_COL, stream=stream, code_format=cf)
+                              for e in range(Wk.shape[0])])
+        out += [torch.stack(codes), torch.stack(scales)]
+    return FFNOperands(X8, s_x, A8, s_a, *out, h1, h3)
+
+
+def alloc_moe_grads(R, E, d, F, device="cuda") -> FFNGrads:
+    f = lambda *s: torch.empty(s, dtype=torch.float32, device=device)
+    return FFNGrads(f(R, d), f(E, d, F), f(E, d, F), f(E, F, d))
+
+
 def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, seed=0,
                  grads: FFNGrads | None = None, workspace=None, status=None, stream=None,
-                 step_events=None) -> FFNGrads:
-    """step_events: optional list of FFN_NUM_EVENTS torch.cuda.Event (timing)."""
+                 step_events=None, group_offsets=None) -> FFNGrads:
+    """step_events: optional list of FFN_NUM_EVENTS torch.cuda.Event (timing).
+    group_offsets: grouped (mixture-of-experts) mode, a list of E + 1 row
+    offsets of the expert-sorted rows; the weights in `ops` are then stacked
+    per expert and S is ignored."""
     T, d = dY.shape
     F = ops.A8.shape[1]
     dev = dY.device
-    if grads is None:
-        grads = alloc_ffn_grads(T, d, F, dev)
     fmt = code_format_of(ops.X8)
-    need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode, fmt)
+    if group_offsets is not None:
+        offs = [int(o) for o in group_offsets]
+        E = len(offs) - 1
+        tmax = max([b - a for a, b in zip(offs[:-1], offs[1:])] + [1])
+        if grads is None:
+            grads = alloc_moe_grads(T, E, d, F, dev)
+        need = ffn_workspace_size(tmax, d, F, tmax, round_mode, ec_mode, fmt)
+        S = 0
+    else:
+        if grads is None:
+            grads = alloc_ffn_grads(T, d, F, dev)
+        need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode, fmt)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     p = lambda t: None if t is None else t.data_ptr()
@@ -443,6 +477,10 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
                     p(ops.s_a), p(ops.W1_8), p(ops.s_w1), p(ops.W3_8), p(ops.s_w3), p(ops.W2_8), p(ops.s_w2),
                     round_mode, ec_mode, fmt, seed, p(grads.dX), p(grads.dW1), p(grads.dW3), p(grads.dW2),
                     p(workspace), workspace.numel(), p(status), None)
+    if group_offsets is not None:
+        off_arr = (C.c_int64 * len(offs))(*offs)   # kept alive until the call returns
+        args.num_groups = len(offs) - 1
+        args.group_offsets = C.cast(off_arr, C.POINTER(C.c_int64))
     if step_events is not None:
         assert len(step_events) == FFN_NUM_EVENTS
         handles = (C.c_void_p * FFN_NUM_EVENTS)(*[C.c_void_p(e.cuda_event) for e in step_events])

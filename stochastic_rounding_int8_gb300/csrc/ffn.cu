@@ -29,7 +29,7 @@ extern "C" const char* s3r_last_error(void) { return g_last_error; }
 
 namespace {
 
-constexpr uint32_t kTidW2 = 0, kTidW1 = 1, kTidW3 = 2, kRhsOffset = 0x100;
+constexpr uint32_t kRhsOffset = S3R_TID_RHS_OFFSET;
 
 struct Carver {
     uintptr_t cur, end;
@@ -122,28 +122,23 @@ extern "C" size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_
     return layout(nullptr, 0, T, d, F, S, round_mode, code_format).total;
 }
 
-extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
-    if (!a) return S3R_ERR_ARG;
+namespace {
+
+// The block backward of one example group (the whole batch, or one expert's
+// rows): a->T rows, a->S tokens per example, tensor ids tid_base + (0, 1, 2).
+// Step events are recorded only when `events` is set.
+int run_block(const struct s3r_ffn_args* a, uint32_t tid_base, bool events, cudaStream_t stream) {
     const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
-    if (T <= 0 || d <= 0 || F <= 0 || S <= 0) return S3R_ERR_ARG;
-    if (T % S != 0 || (S % S3R_TILE != 0 && S != T)) return S3R_ERR_SHAPE;
-    if (a->round_mode < S3R_ROUND_RTNE || a->round_mode > S3R_ROUND_INDEP) return S3R_ERR_ARG;
-    if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_TWO_WAY) return S3R_ERR_ARG;
-    if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     const int fmt = a->code_format;
-    if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->A8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 ||
-        !a->dW2 || !a->dW3)
-        return S3R_ERR_ARG;
-    if (!a->workspace || a->workspace_bytes < s3r_ffn_workspace_size(T, d, F, S, a->round_mode, a->ec_mode, fmt))
-        return S3R_ERR_WORKSPACE;
     FfnLayout Lo = layout(a->workspace, a->workspace_bytes, T, d, F, S, a->round_mode, fmt);
     if (!Lo.ok) return S3R_ERR_WORKSPACE;
     const int rm = a->round_mode;
     const int ec = rm == S3R_ROUND_S3R ? a->ec_mode : S3R_EC_NONE;
     const bool indep = rm == S3R_ROUND_INDEP;
+    const uint32_t kTidW2 = tid_base + S3R_TID_W2, kTidW1 = tid_base + S3R_TID_W1, kTidW3 = tid_base + S3R_TID_W3;
     int* st = a->d_status;
     auto mark = [&](int i) -> int {
-        if (a->step_events) {
+        if (events && a->step_events) {
             cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream);
             if (e != cudaSuccess) {
                 (void)cudaGetLastError();
@@ -209,6 +204,99 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     S3R_TRY(int8_gemm_dw(a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, fmt, T, d, F, a->s_w3, ec,
                          L3.colmean, L3.mu, L3.xsum, L3.p, S, a->dW3, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
     S3R_TRY(mark(8));
+    return S3R_OK;
+}
+
+}  // namespace
+
+extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
+    if (!a) return S3R_ERR_ARG;
+    const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
+    if (T <= 0 || d <= 0 || F <= 0) return S3R_ERR_ARG;
+    if (a->round_mode < S3R_ROUND_RTNE || a->round_mode > S3R_ROUND_INDEP) return S3R_ERR_ARG;
+    if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    const int fmt = a->code_format;
+    if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->A8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 ||
+        !a->dW2 || !a->dW3)
+        return S3R_ERR_ARG;
+    if (a->num_groups == 0) {
+        if (S <= 0) return S3R_ERR_ARG;
+        if (T % S != 0 || (S % S3R_TILE != 0 && S != T)) return S3R_ERR_SHAPE;
+        if (!a->workspace || a->workspace_bytes < s3r_ffn_workspace_size(T, d, F, S, a->round_mode, a->ec_mode, fmt))
+            return S3R_ERR_WORKSPACE;
+        return run_block(a, 0, true, stream);
+    }
+    // grouped: expert e owns rows offsets[e] .. offsets[e+1] (one example);
+    // weights, their scales and gradients are stacked per expert
+    const int64_t E = a->num_groups;
+    const int64_t* off = a->group_offsets;
+    if (E < 0 || !off || off[0] != 0 || off[E] != T) return S3R_ERR_ARG;
+    int64_t tmax = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        if (off[e + 1] < off[e]) return S3R_ERR_ARG;
+        tmax = off[e + 1] - off[e] > tmax ? off[e + 1] - off[e] : tmax;
+    }
+    if (E > (int64_t)(0xFFFFFFFFu / S3R_MOE_TID_STRIDE)) return S3R_ERR_ARG;
+    if (!a->workspace ||
+        a->workspace_bytes < s3r_ffn_workspace_size(tmax, d, F, tmax, a->round_mode, a->ec_mode, fmt))
+        return S3R_ERR_WORKSPACE;
+    const size_t cs = fmt == S3R_CODES_F16 ? 2 : 1;
+    if (a->step_events) {
+        cudaError_t ev = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[0]), stream);
+        if (ev != cudaSuccess) {
+            (void)cudaGetLastError();
+            return s3r_cuda_fail("ffn_backward step event", ev);
+        }
+    }
+    for (int64_t e = 0; e < E; ++e) {
+        const int64_t r0 = off[e], Tg = off[e + 1] - off[e];
+        float* dW1 = a->dW1 + e * d * F;
+        float* dW3 = a->dW3 + e * d * F;
+        float* dW2 = a->dW2 + e * F * d;
+        if (Tg == 0) {   // an expert without rows has zero weight gradients
+            cudaError_t m = cudaMemsetAsync(dW1, 0, (size_t)(d * F) * sizeof(float), stream);
+            if (m == cudaSuccess) m = cudaMemsetAsync(dW3, 0, (size_t)(d * F) * sizeof(float), stream);
+            if (m == cudaSuccess) m = cudaMemsetAsync(dW2, 0, (size_t)(F * d) * sizeof(float), stream);
+            if (m != cudaSuccess) {
+                (void)cudaGetLastError();
+                return s3r_cuda_fail("ffn_backward: zeroing an empty expert's gradients", m);
+            }
+            continue;
+        }
+        s3r_ffn_args g = *a;
+        g.T = Tg;
+        g.S = Tg;
+        g.num_groups = 0;
+        g.group_offsets = nullptr;
+        g.dY = static_cast<const uint16_t*>(a->dY) + r0 * d;
+        g.h1 = static_cast<const uint16_t*>(a->h1) + r0 * F;
+        g.h3 = static_cast<const uint16_t*>(a->h3) + r0 * F;
+        g.X8 = static_cast<const uint8_t*>(a->X8) + (size_t)(r0 * d) * cs;
+        g.s_x = a->s_x ? a->s_x + r0 : nullptr;
+        g.A8 = static_cast<const uint8_t*>(a->A8) + (size_t)(r0 * F) * cs;
+        g.s_a = a->s_a ? a->s_a + r0 : nullptr;
+        g.W1_8 = static_cast<const uint8_t*>(a->W1_8) + (size_t)(e * d * F) * cs;
+        g.s_w1 = a->s_w1 ? a->s_w1 + e * F : nullptr;
+        g.W3_8 = static_cast<const uint8_t*>(a->W3_8) + (size_t)(e * d * F) * cs;
+        g.s_w3 = a->s_w3 ? a->s_w3 + e * F : nullptr;
+        g.W2_8 = static_cast<const uint8_t*>(a->W2_8) + (size_t)(e * F * d) * cs;
+        g.s_w2 = a->s_w2 ? a->s_w2 + e * d : nullptr;
+        g.dX = a->dX + r0 * d;
+        g.dW1 = dW1;
+        g.dW3 = dW3;
+        g.dW2 = dW2;
+        S3R_TRY(run_block(&g, (uint32_t)(S3R_MOE_TID_STRIDE * e), false, stream));
+    }
+    if (a->step_events) {
+        for (int i = 1; i < S3R_FFN_NUM_EVENTS; ++i) {
+            cudaError_t ev = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream);
+            if (ev != cudaSuccess) {
+                (void)cudaGetLastError();
+                return s3r_cuda_fail("ffn_backward step event", ev);
+            }
+        }
+    }
     return S3R_OK;
 }
 

@@ -86,3 +86,16 @@ def test_ffn_args_struct_layout_matches_header():
         for part in re.split(r",", decl):
             fields.append(re.findall(r"\w+", part)[-1])
     assert fields == [f for f, _ in s3r._FfnArgs._fields_]
+
+
+def test_grouped_args_rejected_on_host():
+    """Grouped-mode offsets are checked before any launch: they must start at
+    0, end at T and never decrease (fake, never-dereferenced pointers)."""
+    import ctypes as C
+    fake = C.c_void_p(0x1000)
+    for offs, T in (([0, 5, 9], 10), ([1, 5, 10], 10), ([0, 6, 4, 10], 10)):
+        arr = (C.c_int64 * len(offs))(*offs)
+        a = s3r._FfnArgs(T, 64, 128, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                         s3r.ROUND_S3R, s3r.EC_TWO_WAY, s3r.CODES_F16, 0, fake, fake, fake, fake, fake, 1 << 30,
+                         None, None, len(offs) - 1, C.cast(arr, C.POINTER(C.c_int64)))
+        assert s3r.lib().ffn_backward(C.byref(a), None) == -1

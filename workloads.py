@@ -130,8 +130,13 @@ class MoEInputs:
 
 
 def moe_inputs(tokens: int, topk: int, experts: int, d: int, F: int, seed: int = DATA_SEED) -> MoEInputs:
+    return moe_inputs_sized(moe_group_sizes(tokens * topk, experts), d, F, seed)
+
+
+def moe_inputs_sized(sizes, d: int, F: int, seed: int = DATA_SEED) -> MoEInputs:
+    """Routed rows for explicit per-expert group sizes (expert-sorted)."""
     rng = _rng(seed)
-    sizes = moe_group_sizes(tokens * topk, experts)
+    experts = len(sizes)
     offsets = [0]
     for n in sizes:
         offsets.append(offsets[-1] + n)
