@@ -172,6 +172,48 @@ void s3r_count_launch();
 void s3r_record_error(const char* where, const char* what);
 int s3r_cuda_fail(const char* where, cudaError_t err);
 
+// Grouped tcgen05 GEMMs on fp16-carried codes (gemm_umma.cu): up to 16
+// problems of one kind in one persistent launch, each computed exactly as a
+// launch of its own would compute it.
+struct UmmaDxProblem {
+    const void* Q;               // [T, N] codes, tile scales, W [K, N], correction terms
+    const float* tile_scale;
+    const void* W;
+    const float* eps;
+    const int32_t* rowsum;
+    const float* v;
+    const void* Q3;              // optional second term (NULL: one term)
+    const float* tile_scale3;
+    const void* W3;
+    const float* eps3;
+    const int32_t* rowsum3;
+    const float* v3;
+    int64_t T, N, K;
+    const float* s_x;
+    int ec_mode;
+    int64_t S;
+    float* dX;
+    int accumulate;
+    int32_t* dump;
+};
+struct UmmaDwProblem {
+    const void* X;               // [T, K] codes
+    const void* Q;               // [T, N] codes and their tile scales
+    const float* tile_scale;
+    int64_t T, K, N;
+    const float* s_w;
+    int ec_mode;
+    const float* colmean;
+    const float* mu;
+    const int32_t* xsum;
+    const float* p;
+    int64_t S;
+    float* dW;
+    int32_t* dump;
+};
+int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream);
+int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t stream);
+
 // S3R-EC factors of the two linears that read the same input X (W1 and W3 of
 // the SwiGLU block) in one pass; bit-identical to two s3r_ec_correct calls
 // (ec.cu).

@@ -199,10 +199,23 @@ int run_block(const struct s3r_ffn_args* a, uint32_t tid_base, bool events, cuda
     S3R_TRY(int8_gemm_dx_sum(terms, 2, fmt, T, F, d, a->s_x, ec, S, a->dX, 0, st, stream));
     S3R_TRY(mark(7));
     // 8. dW1, dW3
-    S3R_TRY(int8_gemm_dw(a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, fmt, T, d, F, a->s_w1, ec,
-                         L1.colmean, L1.mu, L1.xsum, L1.p, S, a->dW1, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
-    S3R_TRY(int8_gemm_dw(a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, fmt, T, d, F, a->s_w3, ec,
-                         L3.colmean, L3.mu, L3.xsum, L3.p, S, a->dW3, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
+    if (fmt == S3R_CODES_F16) {
+        // both weight gradients in one persistent launch (their tiles share the grid)
+        const bool two = ec == S3R_EC_TWO_WAY;
+        const UmmaDwProblem q[2] = {
+            {a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, T, d, F, a->s_w1, ec,
+             two ? L1.colmean : nullptr, two ? L1.mu : nullptr, two ? L1.xsum : nullptr, two ? L1.p : nullptr, S,
+             a->dW1, nullptr},
+            {a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, T, d, F, a->s_w3, ec,
+             two ? L3.colmean : nullptr, two ? L3.mu : nullptr, two ? L3.xsum : nullptr, two ? L3.p : nullptr, S,
+             a->dW3, nullptr}};
+        S3R_TRY(umma_dw_group(q, 2, st, stream));
+    } else {
+        S3R_TRY(int8_gemm_dw(a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, fmt, T, d, F, a->s_w1, ec,
+                             L1.colmean, L1.mu, L1.xsum, L1.p, S, a->dW1, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
+        S3R_TRY(int8_gemm_dw(a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, fmt, T, d, F, a->s_w3, ec,
+                             L3.colmean, L3.mu, L3.xsum, L3.p, S, a->dW3, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
+    }
     S3R_TRY(mark(8));
     return S3R_OK;
 }

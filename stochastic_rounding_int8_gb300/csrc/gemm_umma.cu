@@ -32,6 +32,8 @@
 // accumulator (dX = Q1 W1^T + Q3 W3^T), each with its own scales.
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
 #include <cstdio>
+#include <cstring>
+#include <vector>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -85,8 +87,13 @@ struct Segment {
     const float* v;
 };
 
-struct Args {
-    int64_t M, N;                // C[M, N] = sum over segments of sum_k A[m, k] B[n, k]
+// One GEMM of a launch: C[M, N] = sum over segments of sum_k A[m, k] B[n, k],
+// promoted per 128-wide block, corrected and rescaled in the epilogue.
+struct Problem {
+    int64_t M, N;
+    int ntm, ntn;                // 128 x 256 tiles along M and N
+    int tile_base;               // first tile of this problem in the launch's tile order
+    int band_rows;               // tile order inside the problem (tile_coords)
     Segment seg[2];              // seg[1].K == 0 when there is one segment
     float* C;
     int64_t ldc;
@@ -100,7 +107,21 @@ struct Args {
     const int32_t* xsum;
     const float* p;
     int accumulate;
+};
+
+// A launch: up to kMaxProb problems of one kind, their tiles numbered one
+// after another; each problem has up to four tensor maps (A and B of each
+// segment).  Both live in the constant parameter space (__grid_constant__),
+// so indexing them with a run-time problem number costs no copy.
+constexpr int kMaxProb = 16;
+struct Args {
+    Problem prob[kMaxProb];
+    int nprob;
+    int total_tiles;
     int* d_status;
+};
+struct Maps {
+    CUtensorMap m[kMaxProb][4];
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -215,7 +236,7 @@ __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cas
 //   dW: -(p[k] + sum_b xsum[b, k] (colmean[b, n] - mu[b])).
 // The dW pass also stages 1/s_w for the final rescale.
 template <int EPI>
-__device__ __forceinline__ void seed_tile(const Args& P, float (&acc)[128], float* cv, int64_t row, int64_t m0,
+__device__ __forceinline__ void seed_tile(const Problem& P, float (&acc)[128], float* cv, int64_t row, int64_t m0,
                                           int64_t c0, int half, int ht) {
     const bool in = row < P.M;
     const int64_t cc = c0 + ht;   // the column this thread stages
@@ -301,7 +322,7 @@ __device__ __forceinline__ void seed_tile(const Args& P, float (&acc)[128], floa
 // so that every global access is a 64-byte row segment (accumulate reads
 // included).
 template <int EPI>
-__device__ __forceinline__ void finish_tile(const Args& P, float (&acc)[128], const float* cv, float* stage,
+__device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128], const float* cv, float* stage,
                                             int64_t row, int64_t c0, int lane) {
     if (EPI == kDX && P.s_row) {
         const float rinv = row < P.M ? __frcp_rn(__ldg(P.s_row + row)) : 1.0f;
@@ -355,13 +376,34 @@ __device__ __forceinline__ void finish_tile(const Args& P, float (&acc)[128], co
     }
 }
 
+// Tile order: bands of `band` row tiles; inside a band the row index runs
+// fastest, then the column (band = 1 is plain column-fastest order).  The
+// host picks the band height that makes the first wave of concurrent CTAs
+// touch the fewest operand bytes (row strips of A plus column strips of B),
+// so more of each wave's operands are shared in L2.
+__host__ __device__ __forceinline__ void tile_coords(int tile, int ntm, int ntn, int band_rows, int& tm,
+                                                     int& tn) {
+    const int band = tile / (band_rows * ntn);
+    const int rows = min(band_rows, ntm - band * band_rows);   // the last band may be thinner
+    const int in = tile - band * band_rows * ntn;
+    tm = band * band_rows + in % rows;
+    tn = in / rows;
+}
+
+// The problem that owns launch tile `tile` (tiles of problem i start at
+// prob[i].tile_base, in increasing order).
+__device__ __forceinline__ int problem_of(const Args& A, int tile) {
+    int i = 0;
+    while (i + 1 < A.nprob && tile >= A.prob[i + 1].tile_base) ++i;
+    return i;
+}
+
 // 12 warps: one SM sub-partition hosts three of them, one per warpgroup, so the
 // launch is capped at 168 registers per thread; after the split a
 // sub-partition holds (40 + 216 + 216) * 32 = 15104 of its 16384.
 template <int EPI, bool MN>
 __global__ void __launch_bounds__(THREADS, 1)
-    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1, Args P) {
+    umma_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args A) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -375,10 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    tempty0 = su32(bars + 2 * STAGES + 2), done_bar = su32(bars + 2 * STAGES + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
-    const int nkb = nkb0 + nkb1;                 // 128-wide blocks per tile
-    // tile counts fit 32 bits: the host caps M and N far below 2^31 * 128
-    const int ntn = (int)s3r_cdiv(P.N, BN), ntiles = (int)s3r_cdiv(P.M, BM) * ntn;
+    const int ntiles = A.total_tiles;   // tile counts fit 32 bits (checked by the host)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -413,16 +452,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
         if (warp == 0) {
             if (lane == 0) {
-                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA0) : "memory");
-                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB0) : "memory");
-                if (nkb1) {
-                    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA1) : "memory");
-                    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB1) : "memory");
-                }
                 int it = 0;   // slice counter over the whole persistent run
+                int last_pi = -1;
                 bool ok = true;
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                    const int32_t m0 = (tile / ntn) * BM, n0 = (tile % ntn) * BN;
+                    const int pi = problem_of(A, tile);
+                    const Problem& P = A.prob[pi];
+                    const CUtensorMap* mp = &maps.m[pi][0];
+                    const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
+                    const int nkb = nkb0 + nkb1;   // 128-wide blocks of this tile
+                    if (pi != last_pi) {
+                        for (int j = 0; j < (nkb1 ? 4 : 2); ++j)
+                            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)(mp + j)) : "memory");
+                        last_pi = pi;
+                    }
+                    int tm, tn;
+                    tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
+                    const int32_t m0 = tm * BM, n0 = tn * BN;
                     for (int sl = 0; sl < 2 * nkb; ++sl, ++it) {
                         const int s = it % STAGES;
                         if (!mbar_wait(empty0 + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abrt)) {
@@ -434,8 +480,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint32_t fb = full0 + 8 * s;
                         mbar_expect_tx(fb, STAGE_BYTES);
                         const bool second = sl >= 2 * nkb0;
-                        const CUtensorMap* mA = second ? &tmA1 : &tmA0;
-                        const CUtensorMap* mB = second ? &tmB1 : &tmB0;
+                        const CUtensorMap* mA = mp + (second ? 2 : 0);
+                        const CUtensorMap* mB = mp + (second ? 3 : 1);
                         const int32_t k0 = (second ? sl - 2 * nkb0 : sl) * BKS;
                         const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
                         if (!MN) {
@@ -460,6 +506,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int it = 0, gkb = 0;   // slice and block counters over the whole run
                 bool ok = true;
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                    const Problem& P = A.prob[problem_of(A, tile)];
+                    const int nkb = (int)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128));
                     for (int kb = 0; kb < nkb; ++kb, ++gkb) {
                         const int buf = gkb & 1;
                         if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(gkb >> 1) & 1u) ^ 1u, abrt)) {
@@ -512,7 +560,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         int gkb = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const int mt = tile / ntn, nt = (tile % ntn) * 2 + half;   // 128-wide tile indices
+            const Problem& P = A.prob[problem_of(A, tile)];
+            const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
+            const int nkb = nkb0 + nkb1;
+            int tm, tn;
+            tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
+            const int mt = tm, nt = tn * 2 + half;   // 128-wide tile indices
             const int64_t row = (int64_t)mt * BM + 32 * q + lane;
             const int64_t c0 = (int64_t)nt * 128;
             float acc[128];
@@ -582,7 +635,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
-    if (threadIdx.x == 0 && abort_flag) set_status(P.d_status, S3R_ERR_TIMEOUT);
+    if (threadIdx.x == 0 && abort_flag) set_status(A.d_status, S3R_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
@@ -639,36 +692,80 @@ static int sm_count() {
     return n;
 }
 
-template <int EPI, bool MN>
-static int launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
-                  const Args& P, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e =
-            cudaFuncSetAttribute(umma_gemm_kernel<EPI, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return s3r_cuda_fail("umma gemm: cudaFuncSetAttribute", e);
+// Band height whose first wave of `wave` tiles touches the fewest operand
+// bytes: distinct row strips x a_strip + distinct column strips x b_strip.
+static int pick_band_rows(int ntm, int ntn, int wave, double a_strip, double b_strip) {
+    int best = 1;
+    double best_cost = -1.0;
+    for (int r = 1; r <= ntm; r *= 2) {
+        std::vector<char> rows(ntm, 0), cols(ntn, 0);
+        int nr = 0, nc = 0;
+        for (int t = 0; t < wave && t < ntm * ntn; ++t) {
+            int tm, tn;
+            tile_coords(t, ntm, ntn, r, tm, tn);
+            if (!rows[tm]) { rows[tm] = 1; ++nr; }
+            if (!cols[tn]) { cols[tn] = 1; ++nc; }
         }
-        cudaFuncAttributes fa{};
-        e = cudaFuncGetAttributes(&fa, umma_gemm_kernel<EPI, MN>);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return s3r_cuda_fail("umma gemm: cudaFuncGetAttributes", e);
-        }
-        if (fa.numRegs < kMinLaunchRegs || fa.numRegs > kRegsHigh) {
-            char buf[160];
-            snprintf(buf, sizeof(buf), "kernel built with %d registers per thread; the register split needs %d..%d",
-                     fa.numRegs, kMinLaunchRegs, kRegsHigh);
-            s3r_record_error("umma gemm", buf);
-            return S3R_ERR_UNSUPPORTED;
-        }
-        attr = true;
+        const double cost = nr * a_strip + nc * b_strip;
+        if (best_cost < 0.0 || cost < best_cost) { best_cost = cost; best = r; }
     }
-    const int64_t ntiles = s3r_cdiv(P.M, BM) * s3r_cdiv(P.N, BN);
-    if (ntiles == 0) return S3R_OK;
-    const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();   // persistent: one CTA per SM
-    umma_gemm_kernel<EPI, MN><<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(a0, b0, a1, b1, P);
+    return best;
+}
+
+template <int EPI, bool MN>
+static int ensure_kernel() {
+    static bool attr = false;
+    if (attr) return S3R_OK;
+    cudaError_t e =
+        cudaFuncSetAttribute(umma_gemm_kernel<EPI, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("umma gemm: cudaFuncSetAttribute", e);
+    }
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, umma_gemm_kernel<EPI, MN>);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("umma gemm: cudaFuncGetAttributes", e);
+    }
+    if (fa.numRegs < kMinLaunchRegs || fa.numRegs > kRegsHigh) {
+        char buf[160];
+        snprintf(buf, sizeof(buf), "kernel built with %d registers per thread; the register split needs %d..%d",
+                 fa.numRegs, kMinLaunchRegs, kRegsHigh);
+        s3r_record_error("umma gemm", buf);
+        return S3R_ERR_UNSUPPORTED;
+    }
+    attr = true;
+    return S3R_OK;
+}
+
+// Launches the problems A.prob[0 .. A.nprob) (tile counts, bases and band
+// heights filled in here); strip[i] = {bytes of one A row strip, of one B
+// column strip} of problem i, for the tile order.
+template <int EPI, bool MN>
+static int launch(const Maps& maps, Args& A, const double (*strip)[2], cudaStream_t stream) {
+    int st = ensure_kernel<EPI, MN>();
+    if (st) return st;
+    const int sms = sm_count();
+    int64_t total = 0;
+    for (int i = 0; i < A.nprob; ++i) {
+        Problem& P = A.prob[i];
+        const int64_t ntm = s3r_cdiv(P.M, BM), ntn = s3r_cdiv(P.N, BN);
+        if (ntm * ntn > (int64_t)1 << 30) return S3R_ERR_UNSUPPORTED;
+        P.ntm = (int)ntm;
+        P.ntn = (int)ntn;
+        P.tile_base = (int)total;
+        const int64_t tiles = ntm * ntn;
+        P.band_rows = tiles ? pick_band_rows(P.ntm, P.ntn, (int)std::min<int64_t>(tiles, sms), strip[i][0],
+                                             strip[i][1])
+                            : 1;
+        total += tiles;
+        if (total > (int64_t)1 << 30) return S3R_ERR_UNSUPPORTED;
+    }
+    A.total_tiles = (int)total;
+    if (total == 0) return S3R_OK;
+    const int64_t grid = total < sms ? total : sms;   // persistent: one CTA per SM
+    umma_gemm_kernel<EPI, MN><<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(maps, A);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
 }
@@ -684,49 +781,110 @@ static void dx_segment(umma::Segment& g, const float* tile_scale, int64_t N, con
     g.eps = eps; g.rowsum = rowsum; g.v = v;
 }
 
-// dX [T, K] from fp16-carried codes: A = Q [T, N], B = W [K, N] (both K-major);
-// with a second term (Q3, W3) the kernel contracts both into one accumulator:
+// dX problems (fp16-carried codes): A = Q [T, N], B = W [K, N] (both K-major);
+// a second term (Q3, W3) contracts into the same accumulator:
 // dX = Q W^T + Q3 W3^T, each term with its own tile scales and correction.
+int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream) {
+    if (n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
+    thread_local umma::Maps maps;   // host staging of the launch's parameters (copied at launch)
+    thread_local umma::Args A;
+    std::memset(&A, 0, sizeof(A));
+    double strip[umma::kMaxProb][2];
+    bool dump = false;
+    for (int i = 0; i < n; ++i) {
+        const UmmaDxProblem& q = probs[i];
+        const int64_t T = q.T, N = q.N, K = q.K, S = q.S > 0 ? q.S : q.T;
+        const bool two = q.Q3 != nullptr;
+        if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.W) || N % 8 != 0) return S3R_ERR_ALIGN;
+        if (two && (!s3r_aligned16(q.Q3) || !s3r_aligned16(q.W3))) return S3R_ERR_ALIGN;
+        if (q.ec_mode && S < T && S % kTile != 0) {
+            // the epilogue stages v for at most kNbX examples per 128-row tile
+            int64_t nb = 0;
+            for (int64_t m0 = 0; m0 < T; m0 += umma::BM) {
+                const int64_t hi = (m0 + umma::BM - 1 < T ? m0 + umma::BM - 1 : T - 1) / S;
+                if (hi - m0 / S + 1 > nb) nb = hi - m0 / S + 1;
+            }
+            if (nb > umma::kNbX) {
+                char buf[160];
+                snprintf(buf, sizeof(buf),
+                         "S = %lld lets a 128-token tile span %lld examples; the fp16-code path takes %d",
+                         (long long)S, (long long)nb, umma::kNbX);
+                s3r_record_error("int8_gemm_dx", buf);
+                return S3R_ERR_UNSUPPORTED;
+            }
+        }
+        CUtensorMap* m = maps.m[i];
+        int st = umma::make_map(&m[0], q.Q, N, T, N, umma::BM);
+        if (!st) st = umma::make_map(&m[1], q.W, N, K, N, umma::BN);
+        if (!st && two) st = umma::make_map(&m[2], q.Q3, N, T, N, umma::BM);
+        if (!st && two) st = umma::make_map(&m[3], q.W3, N, K, N, umma::BN);
+        if (st) return st;
+        if (!two) {
+            m[2] = m[0];
+            m[3] = m[1];
+        }
+        umma::Problem& P = A.prob[i];
+        P.M = T; P.N = K;
+        dx_segment(P.seg[0], q.tile_scale, N, q.eps, q.rowsum, q.v);
+        if (two) dx_segment(P.seg[1], q.tile_scale3, N, q.eps3, q.rowsum3, q.v3);
+        P.C = q.dX; P.ldc = K; P.dump = q.dump; P.s_row = q.s_x; P.ec_mode = q.ec_mode; P.S = S;
+        P.accumulate = q.accumulate;
+        // bytes per row strip of A (BM rows of Q over the contraction) and per column strip of B (BN rows of W)
+        const double kbytes = 2.0 * (double)N * (two ? 2 : 1);
+        strip[i][0] = umma::BM * kbytes;
+        strip[i][1] = umma::BN * kbytes;
+        dump = dump || q.dump;
+    }
+    A.nprob = n;
+    A.d_status = d_status;
+    if (dump) return umma::launch<umma::kDump, false>(maps, A, strip, stream);
+    return umma::launch<umma::kDX, false>(maps, A, strip, stream);
+}
+
+// dW problems (fp16-carried codes): A = X [T, K], B = Q [T, N] (both MN-major, contracted over T).
+int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t stream) {
+    if (n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
+    thread_local umma::Maps maps;
+    thread_local umma::Args A;
+    std::memset(&A, 0, sizeof(A));
+    double strip[umma::kMaxProb][2];
+    bool dump = false;
+    for (int i = 0; i < n; ++i) {
+        const UmmaDwProblem& q = probs[i];
+        const int64_t T = q.T, K = q.K, N = q.N, S = q.S > 0 ? q.S : q.T;
+        if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.X) || N % 8 != 0 || K % 8 != 0) return S3R_ERR_ALIGN;
+        CUtensorMap* m = maps.m[i];
+        int st = umma::make_map(&m[0], q.X, K, T, K, 64);
+        if (!st) st = umma::make_map(&m[1], q.Q, N, T, N, 64);
+        if (st) return st;
+        m[2] = m[0];
+        m[3] = m[1];
+        umma::Problem& P = A.prob[i];
+        P.M = K; P.N = N;
+        umma::Segment& g = P.seg[0];
+        g.scale = q.tile_scale; g.sm = 0; g.sn = 1; g.sk = s3r_cdiv(N, kTile); g.nt_limit = s3r_cdiv(N, kTile);
+        g.K = T;
+        P.C = q.dW; P.ldc = N; P.dump = q.dump; P.s_col = q.s_w; P.ec_mode = q.ec_mode; P.S = S;
+        P.B = q.S > 0 ? T / q.S : 1; P.colmean = q.colmean; P.mu = q.mu; P.xsum = q.xsum; P.p = q.p;
+        const double kbytes = 2.0 * (double)T;   // per output row / column over the contraction
+        strip[i][0] = umma::BM * kbytes;
+        strip[i][1] = umma::BN * kbytes;
+        dump = dump || q.dump;
+    }
+    A.nprob = n;
+    A.d_status = d_status;
+    if (dump) return umma::launch<umma::kDump, true>(maps, A, strip, stream);
+    return umma::launch<umma::kDW, true>(maps, A, strip, stream);
+}
+
 int umma_gemm_dx2(const void* Q, const float* tile_scale, const void* W, const float* eps, const int32_t* rowsum,
                   const float* v, const void* Q3, const float* tile_scale3, const void* W3, const float* eps3,
                   const int32_t* rowsum3, const float* v3, int64_t T, int64_t N, int64_t K, const float* s_x,
                   int ec_mode, int64_t S, float* dX, int accumulate, int32_t* dump, int* d_status,
                   cudaStream_t stream) {
-    if (!s3r_aligned16(Q) || !s3r_aligned16(W) || N % 8 != 0) return S3R_ERR_ALIGN;
-    if (Q3 && (!s3r_aligned16(Q3) || !s3r_aligned16(W3))) return S3R_ERR_ALIGN;
-    CUtensorMap ma, mb, ma3, mb3;
-    int st = umma::make_map(&ma, Q, N, T, N, umma::BM);
-    if (!st) st = umma::make_map(&mb, W, N, K, N, umma::BN);
-    if (!st && Q3) st = umma::make_map(&ma3, Q3, N, T, N, umma::BM);
-    if (!st && Q3) st = umma::make_map(&mb3, W3, N, K, N, umma::BN);
-    if (st) return st;
-    if (!Q3) {
-        ma3 = ma;
-        mb3 = mb;
-    }
-    if (ec_mode && S > 0 && S < T && S % kTile != 0) {
-        // the epilogue stages v for at most kNbX examples per 128-row tile
-        int64_t nb = 0;
-        for (int64_t m0 = 0; m0 < T; m0 += umma::BM) {
-            const int64_t hi = (m0 + umma::BM - 1 < T ? m0 + umma::BM - 1 : T - 1) / S;
-            if (hi - m0 / S + 1 > nb) nb = hi - m0 / S + 1;
-        }
-        if (nb > umma::kNbX) {
-            char buf[160];
-            snprintf(buf, sizeof(buf), "S = %lld lets a 128-token tile span %lld examples; the fp16-code path takes %d",
-                     (long long)S, (long long)nb, umma::kNbX);
-            s3r_record_error("int8_gemm_dx", buf);
-            return S3R_ERR_UNSUPPORTED;
-        }
-    }
-    umma::Args P{};
-    P.M = T; P.N = K;
-    dx_segment(P.seg[0], tile_scale, N, eps, rowsum, v);
-    if (Q3) dx_segment(P.seg[1], tile_scale3, N, eps3, rowsum3, v3);
-    P.C = dX; P.ldc = K; P.dump = dump; P.s_row = s_x; P.ec_mode = ec_mode; P.S = S > 0 ? S : T;
-    P.accumulate = accumulate; P.d_status = d_status;
-    if (dump) return umma::launch<umma::kDump, false>(ma, mb, ma3, mb3, P, stream);
-    return umma::launch<umma::kDX, false>(ma, mb, ma3, mb3, P, stream);
+    const UmmaDxProblem q{Q, tile_scale, W, eps, rowsum, v, Q3, tile_scale3, W3, eps3, rowsum3, v3,
+                          T, N, K, s_x, ec_mode, S, dX, accumulate, dump};
+    return umma_dx_group(&q, 1, d_status, stream);
 }
 
 int umma_gemm_dx(const void* Q, const float* tile_scale, const void* W, int64_t T, int64_t N, int64_t K,
@@ -736,22 +894,9 @@ int umma_gemm_dx(const void* Q, const float* tile_scale, const void* W, int64_t 
                          K, s_x, ec_mode, S, dX, accumulate, dump, d_status, stream);
 }
 
-// dW [K, N] from fp16-carried codes: A = X [T, K], B = Q [T, N] (both MN-major, contracted over T).
 int umma_gemm_dw(const void* X, const void* Q, const float* tile_scale, int64_t T, int64_t K, int64_t N,
                  const float* s_w, int ec_mode, const float* colmean, const float* mu, const int32_t* xsum,
                  const float* p, int64_t S, float* dW, int32_t* dump, int* d_status, cudaStream_t stream) {
-    if (!s3r_aligned16(Q) || !s3r_aligned16(X) || N % 8 != 0 || K % 8 != 0) return S3R_ERR_ALIGN;
-    CUtensorMap ma, mb;
-    int st = umma::make_map(&ma, X, K, T, K, 64);
-    if (st) return st;
-    st = umma::make_map(&mb, Q, N, T, N, 64);
-    if (st) return st;
-    umma::Args P{};
-    P.M = K; P.N = N;
-    umma::Segment& g = P.seg[0];
-    g.scale = tile_scale; g.sm = 0; g.sn = 1; g.sk = s3r_cdiv(N, kTile); g.nt_limit = s3r_cdiv(N, kTile); g.K = T;
-    P.C = dW; P.ldc = N; P.dump = dump; P.s_col = s_w; P.ec_mode = ec_mode; P.S = S > 0 ? S : T;
-    P.B = S > 0 ? T / S : 1; P.colmean = colmean; P.mu = mu; P.xsum = xsum; P.p = p; P.d_status = d_status;
-    if (dump) return umma::launch<umma::kDump, true>(ma, mb, ma, mb, P, stream);
-    return umma::launch<umma::kDW, true>(ma, mb, ma, mb, P, stream);
+    const UmmaDwProblem q{X, Q, tile_scale, T, K, N, s_w, ec_mode, colmean, mu, xsum, p, S, dW, dump};
+    return umma_dw_group(&q, 1, d_status, stream);
 }
