@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn"],
+    ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn",
+                                              "moe"],
                     help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
     return ap.parse_args()
 
@@ -261,6 +262,66 @@ def time_bf16_backward(inp, steps, warmup):
     return t0.elapsed_time(t1) / steps
 
 
+def time_moe(s3r, steps=5, warmup=2):
+    """Context: the mixture-of-experts workload (8 experts, d=4096, F=1408,
+    16384 tokens top-2, Zipf(1.1) loads): grouped S3R-EC two-way backward
+    through ffn_backward, and the same per-expert backward in BF16 with cuBLAS."""
+    w = workloads.WORKLOADS["moe_e8_d4096_F1408_tok16384_top2"]
+    inp = workloads.moe_inputs(w["tokens"], w["topk"], w["experts"], w["d"], w["F"], seed=workloads.DATA_SEED + 5)
+    c = lambda t: t.cuda()
+    ops = s3r.moe_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
+    dY = inp.dY.cuda()
+    offs = inp.offsets
+    st = s3r.new_status()
+    grads = s3r.ffn_backward(ops, dY, 0, group_offsets=offs, status=st)
+    ws = torch.empty(s3r.grouped_workspace_size(offs, w["d"], w["F"]), dtype=torch.uint8, device="cuda")
+
+    def ours():
+        s3r.ffn_backward(ops, dY, 0, grads=grads, workspace=ws, status=st, group_offsets=offs)
+
+    X, W1, W3, W2, h1, h3, a = (c(t) for t in (inp.X, inp.W1, inp.W3, inp.W2, inp.h1, inp.h3, inp.a))
+
+    def bf16():
+        for e in range(w["experts"]):
+            r0, r1 = offs[e], offs[e + 1]
+            g, x, hh1, hh3, aa = dY[r0:r1], X[r0:r1], h1[r0:r1], h3[r0:r1], a[r0:r1]
+            dA = g @ W2[e].t()
+            aa.t() @ g
+            s = torch.sigmoid(hh1.float())
+            dAf = dA.float()
+            dh1 = (dAf * hh3.float() * s * (1 + hh1.float() * (1 - s))).to(torch.bfloat16)
+            dh3 = (dAf * hh1.float() * s).to(torch.bfloat16)
+            dh1 @ W1[e].t() + dh3 @ W3[e].t()
+            x.t() @ dh1
+            x.t() @ dh3
+
+    out = {}
+    # per-step split of one grouped call (each step over all experts)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(s3r.FFN_NUM_EVENTS)]
+    for e_ in ev:
+        e_.record()
+    torch.cuda.synchronize()
+    s3r.ffn_backward(ops, dY, 0, grads=grads, workspace=ws, status=st, group_offsets=offs, step_events=ev)
+    torch.cuda.synchronize()
+    out["step_breakdown_ms"] = {n: round(ev[j].elapsed_time(ev[j + 1]), 4) for j, n in enumerate(s3r.FFN_STEPS)}
+    for name, fn in (("s3r_ec_two_way_grouped", ours), ("bf16_cublas_per_expert", bf16)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        out[name] = {"tokens_s": round(w["tokens"] / (ms * 1e-3), 1), "ms": round(ms, 4)}
+    s3r.check_status(st)
+    out["group_rows"] = [b - a for a, b in zip(offs[:-1], offs[1:])]
+    out["speedup_vs_bf16"] = round(out["bf16_cublas_per_expert"]["ms"] / out["s3r_ec_two_way_grouped"]["ms"], 3)
+    return out
+
+
 def time_quantize_sweep(s3r, steps=20):
     """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100
     outliers; int8 codes (1 B) and fp16-carried codes (2 B)."""
@@ -385,6 +446,7 @@ def run_ours(args, world, rank, local):
         for k in ("s3r", "s3r_f16_codes", "indep_sr_one_copy", "rtne"):
             qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
         ctx["quantize_sweep"] = qs
+        ctx["moe_e8_d4096_F1408_tok16384_top2"] = time_moe(s3r)
         line["context"] = ctx
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
@@ -409,6 +471,13 @@ def run_kernel_case(args):
         "ec": lambda: s3r.s3r_ec_correct(q2, T, D, S, ops.W2_8, ops.A8, s3r.EC_TWO_WAY),
         "ffn": lambda: s3r.ffn_backward(ops, dY, S),
     }
+    if args.kernel_case == "moe":
+        w = workloads.WORKLOADS["moe_e8_d4096_F1408_tok16384_top2"]
+        mi = workloads.moe_inputs(w["tokens"], w["topk"], w["experts"], w["d"], w["F"], seed=workloads.DATA_SEED + 5)
+        c = lambda t: t.cuda()
+        mops = s3r.moe_forward_operands(c(mi.X), c(mi.W1), c(mi.W3), c(mi.W2), c(mi.a), c(mi.h1), c(mi.h3))
+        mdY = mi.dY.cuda()
+        fns["moe"] = lambda: s3r.ffn_backward(mops, mdY, 0, group_offsets=mi.offsets)
     if args.kernel_case == "quantize_sweep":
         Gs = workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).cuda()
         qs = s3r.s3r_quantize(Gs, code_format=s3r.CODES_S8)

@@ -325,9 +325,12 @@ int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int cod
  * and its tensor ids are S3R_MOE_TID_STRIDE * e + (0, 1, 2).  An expert
  * without rows gets zero weight gradients.  Row offsets must keep the bases
  * 16-byte aligned (d and F multiples of 8 for fp16 codes, of 16 for int8).
- * workspace: s3r_ffn_workspace_size(Tmax, d, F, Tmax, ...) with Tmax the
- * largest group; step events: event 0 before the first expert, the others
- * after the last.
+ * Every step runs for all experts before the next; with fp16 codes each
+ * GEMM step is one multi-problem launch over the experts (results equal to
+ * per-expert launches bit for bit).  workspace:
+ * s3r_ffn_grouped_workspace_size(group_offsets, E, d, F, ...) bytes (one
+ * block's buffers per non-empty expert); step events mark the same step
+ * boundaries, each over all experts.
  */
 #define S3R_TID_W2 0u
 #define S3R_TID_W1 1u
@@ -369,6 +372,10 @@ struct s3r_ffn_args {
 #define S3R_FFN_NUM_EVENTS 9
 size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
                               int code_format);
+/* grouped mode: group_offsets is the HOST [num_groups + 1] array of the call;
+   0 for invalid offsets */
+size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, int64_t num_groups, int64_t d, int64_t F,
+                                      int round_mode, int ec_mode, int code_format);
 int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
 
 /*

@@ -66,6 +66,7 @@ _SIGS = {
     "int8_gemm_dw": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP, _VP,
                             _SZ, _VP, _VP]),
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
+    "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
     "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP]),
     "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
@@ -414,6 +415,14 @@ def ffn_workspace_size(T, d, F, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, cod
     return int(lib().s3r_ffn_workspace_size(T, d, F, S, round_mode, ec_mode, code_format))
 
 
+def grouped_workspace_size(group_offsets, d, F, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY,
+                           code_format=DEFAULT_CODES) -> int:
+    offs = [int(o) for o in group_offsets]
+    arr = (C.c_int64 * len(offs))(*offs)
+    return int(lib().s3r_ffn_grouped_workspace_size(C.cast(arr, _VP), len(offs) - 1, d, F, round_mode, ec_mode,
+                                                    code_format))
+
+
 @dataclass
 class FFNGrads:
     dX: torch.Tensor
@@ -464,7 +473,7 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
         tmax = max([b - a for a, b in zip(offs[:-1], offs[1:])] + [1])
         if grads is None:
             grads = alloc_moe_grads(T, E, d, F, dev)
-        need = ffn_workspace_size(tmax, d, F, tmax, round_mode, ec_mode, fmt)
+        need = grouped_workspace_size(offs, d, F, round_mode, ec_mode, fmt)
         S = 0
     else:
         if grads is None:

@@ -5,7 +5,9 @@
 // Structured Subspace Randomness" §IV-A (single-block SwiGLU FFN benchmark,
 // Table III shapes), §III-A..§III-D for each linear.  One stream, no host
 // synchronization; every intermediate lives in the caller's workspace.
+#include <algorithm>
 #include <atomic>
+#include <vector>
 
 #include "common.cuh"
 
@@ -30,6 +32,7 @@ extern "C" const char* s3r_last_error(void) { return g_last_error; }
 namespace {
 
 constexpr uint32_t kRhsOffset = S3R_TID_RHS_OFFSET;
+constexpr int MaxGroup = 16;   // problems per multi-problem GEMM launch
 
 struct Carver {
     uintptr_t cur, end;
@@ -124,103 +127,205 @@ extern "C" size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_
 
 namespace {
 
-// The block backward of one example group (the whole batch, or one expert's
-// rows): a->T rows, a->S tokens per example, tensor ids tid_base + (0, 1, 2).
-// Step events are recorded only when `events` is set.
-int run_block(const struct s3r_ffn_args* a, uint32_t tid_base, bool events, cudaStream_t stream) {
-    const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
-    const int fmt = a->code_format;
-    FfnLayout Lo = layout(a->workspace, a->workspace_bytes, T, d, F, S, a->round_mode, fmt);
-    if (!Lo.ok) return S3R_ERR_WORKSPACE;
-    const int rm = a->round_mode;
-    const int ec = rm == S3R_ROUND_S3R ? a->ec_mode : S3R_EC_NONE;
-    const bool indep = rm == S3R_ROUND_INDEP;
-    const uint32_t kTidW2 = tid_base + S3R_TID_W2, kTidW1 = tid_base + S3R_TID_W1, kTidW3 = tid_base + S3R_TID_W3;
-    int* st = a->d_status;
-    auto mark = [&](int i) -> int {
-        if (events && a->step_events) {
-            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream);
-            if (e != cudaSuccess) {
-                (void)cudaGetLastError();
-                return s3r_cuda_fail("ffn_backward step event", e);
-            }
-        }
-        return S3R_OK;
-    };
-    S3R_TRY(mark(0));
+// One example group's backward (the whole batch, or one expert's rows):
+// the argument view, its workspace carve, tensor ids tid_base + (0, 1, 2).
+struct Block {
+    s3r_ffn_args a;
+    FfnLayout Lo;
+    int rm, ec, fmt;
+    bool indep;
+    uint32_t tid2, tid1, tid3;
+};
 
-    // 1. quantize dY with the W2 fold (s_a per token, s_w2 per output channel)
-    LinearWs& L2 = Lo.w2;
-    if (rm == S3R_ROUND_S3R) {
-        S3R_TRY(s3r_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2, L2.Q, fmt, L2.scale, L2.tok, L2.col,
-                             st, stream));
-    } else if (indep) {
-        S3R_TRY(indep_sr_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2, L2.Q, fmt, L2.scale, st, stream));
-        S3R_TRY(indep_sr_quantize(a->dY, T, d, d, a->s_a, a->s_w2, a->seed, kTidW2 + kRhsOffset, L2.Qr, fmt,
-                                  L2.scale_r, st, stream));
-    } else {
-        S3R_TRY(rtne_quantize(a->dY, T, d, d, a->s_a, a->s_w2, S3R_AXIS_TILE, L2.Q, fmt, L2.scale, st, stream));
-    }
-    S3R_TRY(mark(1));
-    // 2. correction factors of W2 (W8 = W2_8 [F, d], X8 = A8 [T, F])
-    if (ec != S3R_EC_NONE)
-        S3R_TRY(s3r_ec_correct(L2.tok, L2.col, T, d, S, a->W2_8, F, a->A8, fmt, ec, L2.eps, L2.mu, L2.colmean,
-                               L2.rowsum, L2.v, L2.xsum, L2.p, Lo.ec_ws, Lo.ec_ws_bytes, st, stream));
-    S3R_TRY(mark(2));
-    // 3. dA = Q2 W2_8^T (rescaled, corrected, / s_a)  [T, F]
-    S3R_TRY(int8_gemm_dx(L2.Q, L2.scale, a->W2_8, fmt, T, d, F, a->s_a, ec, L2.eps, L2.rowsum, L2.v, S, Lo.dA, 0,
-                         st, stream));
-    S3R_TRY(mark(3));
-    // 4. dW2 = A8^T Q2 / s_w2  [F, d]
-    S3R_TRY(int8_gemm_dw(a->A8, indep ? L2.Qr : L2.Q, indep ? L2.scale_r : L2.scale, fmt, T, F, d, a->s_w2, ec,
-                         L2.colmean, L2.mu, L2.xsum, L2.p, S, a->dW2, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
-    S3R_TRY(mark(4));
-    // 5. SwiGLU glue fused into the quantization of dh1 (W1 fold) and dh3 (W3 fold)
-    LinearWs &L1 = Lo.w1, &L3 = Lo.w3;
-    const bool keep_err = ec != S3R_EC_NONE;
-    S3R_TRY(swiglu_quantize(Lo.dA, F, a->h1, a->h3, F, T, F, a->s_x, a->s_w1, a->s_w3, rm, fmt, a->seed, kTidW1,
-                            kTidW3, L1.Q, L1.scale, keep_err ? L1.tok : nullptr, keep_err ? L1.col : nullptr, L3.Q,
-                            L3.scale, keep_err ? L3.tok : nullptr, keep_err ? L3.col : nullptr, st, stream));
-    if (indep)
-        S3R_TRY(swiglu_quantize(Lo.dA, F, a->h1, a->h3, F, T, F, a->s_x, a->s_w1, a->s_w3, rm, fmt, a->seed,
-                                kTidW1 + kRhsOffset, kTidW3 + kRhsOffset, L1.Qr, L1.scale_r, nullptr, nullptr, L3.Qr,
-                                L3.scale_r, nullptr, nullptr, st, stream));
-    S3R_TRY(mark(5));
-    // 6. correction factors of W1 and W3 (W8 [d, F], X8 [T, d])
-    if (ec != S3R_EC_NONE) {
-        S3R_TRY(s3r_ec_correct_pair(L1.tok, L1.col, a->W1_8, L1.eps, L1.mu, L1.colmean, L1.rowsum, L1.v, L1.xsum,
-                                    L1.p, L3.tok, L3.col, a->W3_8, L3.eps, L3.mu, L3.colmean, L3.rowsum, L3.v,
-                                    L3.xsum, L3.p, T, F, S, d, a->X8, fmt, ec, Lo.ec_ws, Lo.ec_ws_bytes, stream));
-    }
-    S3R_TRY(mark(6));
-    // 7. dX = dX1 + dX3
-    const s3r_dx_term terms[2] = {{L1.Q, L1.scale, a->W1_8, L1.eps, L1.rowsum, L1.v},
-                                  {L3.Q, L3.scale, a->W3_8, L3.eps, L3.rowsum, L3.v}};
-    S3R_TRY(int8_gemm_dx_sum(terms, 2, fmt, T, F, d, a->s_x, ec, S, a->dX, 0, st, stream));
-    S3R_TRY(mark(7));
-    // 8. dW1, dW3
-    if (fmt == S3R_CODES_F16) {
-        // both weight gradients in one persistent launch (their tiles share the grid)
-        const bool two = ec == S3R_EC_TWO_WAY;
-        const UmmaDwProblem q[2] = {
-            {a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, T, d, F, a->s_w1, ec,
-             two ? L1.colmean : nullptr, two ? L1.mu : nullptr, two ? L1.xsum : nullptr, two ? L1.p : nullptr, S,
-             a->dW1, nullptr},
-            {a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, T, d, F, a->s_w3, ec,
-             two ? L3.colmean : nullptr, two ? L3.mu : nullptr, two ? L3.xsum : nullptr, two ? L3.p : nullptr, S,
-             a->dW3, nullptr}};
-        S3R_TRY(umma_dw_group(q, 2, st, stream));
-    } else {
-        S3R_TRY(int8_gemm_dw(a->X8, indep ? L1.Qr : L1.Q, indep ? L1.scale_r : L1.scale, fmt, T, d, F, a->s_w1, ec,
-                             L1.colmean, L1.mu, L1.xsum, L1.p, S, a->dW1, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
-        S3R_TRY(int8_gemm_dw(a->X8, indep ? L3.Qr : L3.Q, indep ? L3.scale_r : L3.scale, fmt, T, d, F, a->s_w3, ec,
-                             L3.colmean, L3.mu, L3.xsum, L3.p, S, a->dW3, Lo.dw_ws, Lo.dw_ws_bytes, st, stream));
-    }
-    S3R_TRY(mark(8));
+int make_block(Block& b, const s3r_ffn_args& a, void* ws, size_t ws_bytes, uint32_t tid_base) {
+    b.a = a;
+    b.fmt = a.code_format;
+    b.Lo = layout(ws, ws_bytes, a.T, a.d, a.F, a.S, a.round_mode, b.fmt);
+    if (!b.Lo.ok) return S3R_ERR_WORKSPACE;
+    b.rm = a.round_mode;
+    b.ec = b.rm == S3R_ROUND_S3R ? a.ec_mode : S3R_EC_NONE;
+    b.indep = b.rm == S3R_ROUND_INDEP;
+    b.tid2 = tid_base + S3R_TID_W2;
+    b.tid1 = tid_base + S3R_TID_W1;
+    b.tid3 = tid_base + S3R_TID_W3;
     return S3R_OK;
 }
 
+// 1. quantize dY with the W2 fold (s_a per token, s_w2 per output channel)
+int step_quantize_dy(Block& b, cudaStream_t stream) {
+    const s3r_ffn_args& a = b.a;
+    LinearWs& L2 = b.Lo.w2;
+    const int64_t T = a.T, d = a.d;
+    if (b.rm == S3R_ROUND_S3R)
+        return s3r_quantize(a.dY, T, d, d, a.s_a, a.s_w2, a.seed, b.tid2, L2.Q, b.fmt, L2.scale, L2.tok, L2.col,
+                            a.d_status, stream);
+    if (b.indep) {
+        S3R_TRY(indep_sr_quantize(a.dY, T, d, d, a.s_a, a.s_w2, a.seed, b.tid2, L2.Q, b.fmt, L2.scale, a.d_status,
+                                  stream));
+        return indep_sr_quantize(a.dY, T, d, d, a.s_a, a.s_w2, a.seed, b.tid2 + kRhsOffset, L2.Qr, b.fmt,
+                                 L2.scale_r, a.d_status, stream);
+    }
+    return rtne_quantize(a.dY, T, d, d, a.s_a, a.s_w2, S3R_AXIS_TILE, L2.Q, b.fmt, L2.scale, a.d_status, stream);
+}
+
+// 2. correction factors of W2 (W8 = W2_8 [F, d], X8 = A8 [T, F])
+int step_ec_w2(Block& b, cudaStream_t stream) {
+    if (b.ec == S3R_EC_NONE) return S3R_OK;
+    const s3r_ffn_args& a = b.a;
+    LinearWs& L2 = b.Lo.w2;
+    return s3r_ec_correct(L2.tok, L2.col, a.T, a.d, a.S, a.W2_8, a.F, a.A8, b.fmt, b.ec, L2.eps, L2.mu, L2.colmean,
+                          L2.rowsum, L2.v, L2.xsum, L2.p, b.Lo.ec_ws, b.Lo.ec_ws_bytes, a.d_status, stream);
+}
+
+// 3. dA = Q2 W2_8^T (rescaled, corrected, / s_a)  [T, F]
+UmmaDxProblem dx_problem_da(const Block& b) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs& L2 = b.Lo.w2;
+    return UmmaDxProblem{L2.Q, L2.scale, a.W2_8, L2.eps, L2.rowsum, L2.v, nullptr, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, a.T, a.d, a.F, a.s_a, b.ec, a.S, b.Lo.dA, 0, nullptr};
+}
+int step_da(Block& b, cudaStream_t stream) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs& L2 = b.Lo.w2;
+    return int8_gemm_dx(L2.Q, L2.scale, a.W2_8, b.fmt, a.T, a.d, a.F, a.s_a, b.ec, L2.eps, L2.rowsum, L2.v, a.S,
+                        b.Lo.dA, 0, a.d_status, stream);
+}
+
+// 4. dW2 = A8^T Q2 / s_w2  [F, d]
+UmmaDwProblem dw_problem(const Block& b, const void* X8, const LinearWs& L, int64_t K, int64_t N, const float* s_w,
+                         float* dW) {
+    const bool two = b.ec == S3R_EC_TWO_WAY;
+    return UmmaDwProblem{X8, b.indep ? L.Qr : L.Q, b.indep ? L.scale_r : L.scale, b.a.T, K, N, s_w, b.ec,
+                         two ? L.colmean : nullptr, two ? L.mu : nullptr, two ? L.xsum : nullptr,
+                         two ? L.p : nullptr, b.a.S, dW, nullptr};
+}
+int step_dw2(Block& b, cudaStream_t stream) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs& L2 = b.Lo.w2;
+    return int8_gemm_dw(a.A8, b.indep ? L2.Qr : L2.Q, b.indep ? L2.scale_r : L2.scale, b.fmt, a.T, a.F, a.d, a.s_w2,
+                        b.ec, L2.colmean, L2.mu, L2.xsum, L2.p, a.S, a.dW2, b.Lo.dw_ws, b.Lo.dw_ws_bytes, a.d_status,
+                        stream);
+}
+
+// 5. SwiGLU glue fused into the quantization of dh1 (W1 fold) and dh3 (W3 fold)
+int step_swiglu(Block& b, cudaStream_t stream) {
+    const s3r_ffn_args& a = b.a;
+    LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
+    const int64_t T = a.T, F = a.F;
+    const bool keep_err = b.ec != S3R_EC_NONE;
+    S3R_TRY(swiglu_quantize(b.Lo.dA, F, a.h1, a.h3, F, T, F, a.s_x, a.s_w1, a.s_w3, b.rm, b.fmt, a.seed, b.tid1,
+                            b.tid3, L1.Q, L1.scale, keep_err ? L1.tok : nullptr, keep_err ? L1.col : nullptr, L3.Q,
+                            L3.scale, keep_err ? L3.tok : nullptr, keep_err ? L3.col : nullptr, a.d_status, stream));
+    if (b.indep)
+        S3R_TRY(swiglu_quantize(b.Lo.dA, F, a.h1, a.h3, F, T, F, a.s_x, a.s_w1, a.s_w3, b.rm, b.fmt, a.seed,
+                                b.tid1 + kRhsOffset, b.tid3 + kRhsOffset, L1.Qr, L1.scale_r, nullptr, nullptr, L3.Qr,
+                                L3.scale_r, nullptr, nullptr, a.d_status, stream));
+    return S3R_OK;
+}
+
+// 6. correction factors of W1 and W3 (W8 [d, F], X8 [T, d]), one pass over X8
+int step_ec_w13(Block& b, cudaStream_t stream) {
+    if (b.ec == S3R_EC_NONE) return S3R_OK;
+    const s3r_ffn_args& a = b.a;
+    LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
+    return s3r_ec_correct_pair(L1.tok, L1.col, a.W1_8, L1.eps, L1.mu, L1.colmean, L1.rowsum, L1.v, L1.xsum, L1.p,
+                               L3.tok, L3.col, a.W3_8, L3.eps, L3.mu, L3.colmean, L3.rowsum, L3.v, L3.xsum, L3.p,
+                               a.T, a.F, a.S, a.d, a.X8, b.fmt, b.ec, b.Lo.ec_ws, b.Lo.ec_ws_bytes, stream);
+}
+
+// 7. dX = dX1 + dX3
+UmmaDxProblem dx_problem_dx(const Block& b) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
+    return UmmaDxProblem{L1.Q, L1.scale, a.W1_8, L1.eps, L1.rowsum, L1.v, L3.Q, L3.scale, a.W3_8, L3.eps, L3.rowsum,
+                         L3.v, a.T, a.F, a.d, a.s_x, b.ec, a.S, a.dX, 0, nullptr};
+}
+int step_dx(Block& b, cudaStream_t stream) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
+    const s3r_dx_term terms[2] = {{L1.Q, L1.scale, a.W1_8, L1.eps, L1.rowsum, L1.v},
+                                  {L3.Q, L3.scale, a.W3_8, L3.eps, L3.rowsum, L3.v}};
+    return int8_gemm_dx_sum(terms, 2, b.fmt, a.T, a.F, a.d, a.s_x, b.ec, a.S, a.dX, 0, a.d_status, stream);
+}
+
+// 8. dW1, dW3 (fp16 codes: both in one persistent launch, their tiles share the grid)
+int step_dw13(Block& b, cudaStream_t stream) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
+    if (b.fmt == S3R_CODES_F16) {
+        const UmmaDwProblem q[2] = {dw_problem(b, a.X8, L1, a.d, a.F, a.s_w1, a.dW1),
+                                    dw_problem(b, a.X8, L3, a.d, a.F, a.s_w3, a.dW3)};
+        return umma_dw_group(q, 2, a.d_status, stream);
+    }
+    S3R_TRY(int8_gemm_dw(a.X8, b.indep ? L1.Qr : L1.Q, b.indep ? L1.scale_r : L1.scale, b.fmt, a.T, a.d, a.F, a.s_w1,
+                         b.ec, L1.colmean, L1.mu, L1.xsum, L1.p, a.S, a.dW1, b.Lo.dw_ws, b.Lo.dw_ws_bytes,
+                         a.d_status, stream));
+    return int8_gemm_dw(a.X8, b.indep ? L3.Qr : L3.Q, b.indep ? L3.scale_r : L3.scale, b.fmt, a.T, a.d, a.F, a.s_w3,
+                        b.ec, L3.colmean, L3.mu, L3.xsum, L3.p, a.S, a.dW3, b.Lo.dw_ws, b.Lo.dw_ws_bytes, a.d_status,
+                        stream);
+}
+
+int record(const s3r_ffn_args* a, int i, cudaStream_t stream) {
+    if (!a->step_events) return S3R_OK;
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("ffn_backward step event", e);
+    }
+    return S3R_OK;
+}
+
+// Rows of expert e in grouped mode: the argument view with every per-row
+// pointer moved to the group's first row and every per-expert pointer to
+// the expert's slice.
+s3r_ffn_args expert_view(const s3r_ffn_args& a, int64_t e, int64_t r0, int64_t Tg) {
+    const int64_t d = a.d, F = a.F;
+    const size_t cs = a.code_format == S3R_CODES_F16 ? 2 : 1;
+    s3r_ffn_args g = a;
+    g.T = Tg;
+    g.S = Tg;
+    g.num_groups = 0;
+    g.group_offsets = nullptr;
+    g.dY = static_cast<const uint16_t*>(a.dY) + r0 * d;
+    g.h1 = static_cast<const uint16_t*>(a.h1) + r0 * F;
+    g.h3 = static_cast<const uint16_t*>(a.h3) + r0 * F;
+    g.X8 = static_cast<const uint8_t*>(a.X8) + (size_t)(r0 * d) * cs;
+    g.s_x = a.s_x ? a.s_x + r0 : nullptr;
+    g.A8 = static_cast<const uint8_t*>(a.A8) + (size_t)(r0 * F) * cs;
+    g.s_a = a.s_a ? a.s_a + r0 : nullptr;
+    g.W1_8 = static_cast<const uint8_t*>(a.W1_8) + (size_t)(e * d * F) * cs;
+    g.s_w1 = a.s_w1 ? a.s_w1 + e * F : nullptr;
+    g.W3_8 = static_cast<const uint8_t*>(a.W3_8) + (size_t)(e * d * F) * cs;
+    g.s_w3 = a.s_w3 ? a.s_w3 + e * F : nullptr;
+    g.W2_8 = static_cast<const uint8_t*>(a.W2_8) + (size_t)(e * F * d) * cs;
+    g.s_w2 = a.s_w2 ? a.s_w2 + e * d : nullptr;
+    g.dX = a.dX + r0 * d;
+    g.dW1 = a.dW1 + e * d * F;
+    g.dW3 = a.dW3 + e * d * F;
+    g.dW2 = a.dW2 + e * F * d;
+    return g;
+}
+
+// Workspace of the grouped mode: one block carve per non-empty expert, side by side.
+size_t grouped_bytes(const int64_t* off, int64_t E, int64_t d, int64_t F, int round_mode, int fmt) {
+    size_t total = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        const int64_t Tg = off[e + 1] - off[e];
+        if (Tg > 0) total += layout(nullptr, 0, Tg, d, F, Tg, round_mode, fmt).total + 256;
+    }
+    return total;
+}
+
 }  // namespace
+
+extern "C" size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, int64_t num_groups, int64_t d,
+                                                 int64_t F, int round_mode, int ec_mode, int code_format) {
+    (void)ec_mode;
+    if (!group_offsets || num_groups <= 0 || d <= 0 || F <= 0) return 0;
+    for (int64_t e = 0; e < num_groups; ++e)
+        if (group_offsets[e + 1] < group_offsets[e]) return 0;
+    return grouped_bytes(group_offsets, num_groups, d, F, round_mode, code_format);
+}
 
 extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     if (!a) return S3R_ERR_ARG;
@@ -238,79 +343,124 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
         if (T % S != 0 || (S % S3R_TILE != 0 && S != T)) return S3R_ERR_SHAPE;
         if (!a->workspace || a->workspace_bytes < s3r_ffn_workspace_size(T, d, F, S, a->round_mode, a->ec_mode, fmt))
             return S3R_ERR_WORKSPACE;
-        return run_block(a, 0, true, stream);
+        Block b;
+        S3R_TRY(make_block(b, *a, a->workspace, a->workspace_bytes, 0));
+        S3R_TRY(record(a, 0, stream));
+        S3R_TRY(step_quantize_dy(b, stream));
+        S3R_TRY(record(a, 1, stream));
+        S3R_TRY(step_ec_w2(b, stream));
+        S3R_TRY(record(a, 2, stream));
+        S3R_TRY(step_da(b, stream));
+        S3R_TRY(record(a, 3, stream));
+        S3R_TRY(step_dw2(b, stream));
+        S3R_TRY(record(a, 4, stream));
+        S3R_TRY(step_swiglu(b, stream));
+        S3R_TRY(record(a, 5, stream));
+        S3R_TRY(step_ec_w13(b, stream));
+        S3R_TRY(record(a, 6, stream));
+        S3R_TRY(step_dx(b, stream));
+        S3R_TRY(record(a, 7, stream));
+        S3R_TRY(step_dw13(b, stream));
+        return record(a, 8, stream);
     }
     // grouped: expert e owns rows offsets[e] .. offsets[e+1] (one example);
-    // weights, their scales and gradients are stacked per expert
+    // weights, their scales and gradients are stacked per expert.  Every step
+    // runs for all experts before the next; with fp16 codes each GEMM step is
+    // one multi-problem launch over the experts.
     const int64_t E = a->num_groups;
     const int64_t* off = a->group_offsets;
     if (E < 0 || !off || off[0] != 0 || off[E] != T) return S3R_ERR_ARG;
-    int64_t tmax = 0;
-    for (int64_t e = 0; e < E; ++e) {
+    for (int64_t e = 0; e < E; ++e)
         if (off[e + 1] < off[e]) return S3R_ERR_ARG;
-        tmax = off[e + 1] - off[e] > tmax ? off[e + 1] - off[e] : tmax;
-    }
     if (E > (int64_t)(0xFFFFFFFFu / S3R_MOE_TID_STRIDE)) return S3R_ERR_ARG;
-    if (!a->workspace ||
-        a->workspace_bytes < s3r_ffn_workspace_size(tmax, d, F, tmax, a->round_mode, a->ec_mode, fmt))
+    if (!a->workspace || a->workspace_bytes < grouped_bytes(off, E, d, F, a->round_mode, fmt))
         return S3R_ERR_WORKSPACE;
-    const size_t cs = fmt == S3R_CODES_F16 ? 2 : 1;
-    if (a->step_events) {
-        cudaError_t ev = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[0]), stream);
-        if (ev != cudaSuccess) {
-            (void)cudaGetLastError();
-            return s3r_cuda_fail("ffn_backward step event", ev);
-        }
-    }
+    std::vector<Block> blocks;
+    blocks.reserve((size_t)E);
+    uintptr_t cur = (uintptr_t)a->workspace, end = cur + a->workspace_bytes;
     for (int64_t e = 0; e < E; ++e) {
         const int64_t r0 = off[e], Tg = off[e + 1] - off[e];
-        float* dW1 = a->dW1 + e * d * F;
-        float* dW3 = a->dW3 + e * d * F;
-        float* dW2 = a->dW2 + e * F * d;
         if (Tg == 0) {   // an expert without rows has zero weight gradients
-            cudaError_t m = cudaMemsetAsync(dW1, 0, (size_t)(d * F) * sizeof(float), stream);
-            if (m == cudaSuccess) m = cudaMemsetAsync(dW3, 0, (size_t)(d * F) * sizeof(float), stream);
-            if (m == cudaSuccess) m = cudaMemsetAsync(dW2, 0, (size_t)(F * d) * sizeof(float), stream);
+            cudaError_t m = cudaMemsetAsync(a->dW1 + e * d * F, 0, (size_t)(d * F) * sizeof(float), stream);
+            if (m == cudaSuccess) m = cudaMemsetAsync(a->dW3 + e * d * F, 0, (size_t)(d * F) * sizeof(float), stream);
+            if (m == cudaSuccess) m = cudaMemsetAsync(a->dW2 + e * F * d, 0, (size_t)(F * d) * sizeof(float), stream);
             if (m != cudaSuccess) {
                 (void)cudaGetLastError();
                 return s3r_cuda_fail("ffn_backward: zeroing an empty expert's gradients", m);
             }
             continue;
         }
-        s3r_ffn_args g = *a;
-        g.T = Tg;
-        g.S = Tg;
-        g.num_groups = 0;
-        g.group_offsets = nullptr;
-        g.dY = static_cast<const uint16_t*>(a->dY) + r0 * d;
-        g.h1 = static_cast<const uint16_t*>(a->h1) + r0 * F;
-        g.h3 = static_cast<const uint16_t*>(a->h3) + r0 * F;
-        g.X8 = static_cast<const uint8_t*>(a->X8) + (size_t)(r0 * d) * cs;
-        g.s_x = a->s_x ? a->s_x + r0 : nullptr;
-        g.A8 = static_cast<const uint8_t*>(a->A8) + (size_t)(r0 * F) * cs;
-        g.s_a = a->s_a ? a->s_a + r0 : nullptr;
-        g.W1_8 = static_cast<const uint8_t*>(a->W1_8) + (size_t)(e * d * F) * cs;
-        g.s_w1 = a->s_w1 ? a->s_w1 + e * F : nullptr;
-        g.W3_8 = static_cast<const uint8_t*>(a->W3_8) + (size_t)(e * d * F) * cs;
-        g.s_w3 = a->s_w3 ? a->s_w3 + e * F : nullptr;
-        g.W2_8 = static_cast<const uint8_t*>(a->W2_8) + (size_t)(e * F * d) * cs;
-        g.s_w2 = a->s_w2 ? a->s_w2 + e * d : nullptr;
-        g.dX = a->dX + r0 * d;
-        g.dW1 = dW1;
-        g.dW3 = dW3;
-        g.dW2 = dW2;
-        S3R_TRY(run_block(&g, (uint32_t)(S3R_MOE_TID_STRIDE * e), false, stream));
+        const s3r_ffn_args g = expert_view(*a, e, r0, Tg);
+        cur = (cur + 255) & ~(uintptr_t)255;
+        const size_t need = layout(nullptr, 0, Tg, d, F, Tg, a->round_mode, fmt).total;
+        if (cur + need > end) return S3R_ERR_WORKSPACE;
+        blocks.emplace_back();
+        S3R_TRY(make_block(blocks.back(), g, (void*)cur, need, (uint32_t)(S3R_MOE_TID_STRIDE * e)));
+        cur += need;
     }
-    if (a->step_events) {
-        for (int i = 1; i < S3R_FFN_NUM_EVENTS; ++i) {
-            cudaError_t ev = cudaEventRecord(static_cast<cudaEvent_t>(a->step_events[i]), stream);
-            if (ev != cudaSuccess) {
-                (void)cudaGetLastError();
-                return s3r_cuda_fail("ffn_backward step event", ev);
-            }
+    const bool f16 = fmt == S3R_CODES_F16;
+    const size_t nb = blocks.size();
+    S3R_TRY(record(a, 0, stream));
+    for (Block& b : blocks) S3R_TRY(step_quantize_dy(b, stream));
+    S3R_TRY(record(a, 1, stream));
+    for (Block& b : blocks) S3R_TRY(step_ec_w2(b, stream));
+    S3R_TRY(record(a, 2, stream));
+    if (f16) {
+        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
+            UmmaDxProblem q[MaxGroup];
+            const size_t n = std::min(nb - i0, (size_t)MaxGroup);
+            for (size_t i = 0; i < n; ++i) q[i] = dx_problem_da(blocks[i0 + i]);
+            S3R_TRY(umma_dx_group(q, (int)n, a->d_status, stream));
         }
+    } else {
+        for (Block& b : blocks) S3R_TRY(step_da(b, stream));
     }
-    return S3R_OK;
+    S3R_TRY(record(a, 3, stream));
+    if (f16) {
+        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
+            UmmaDwProblem q[MaxGroup];
+            const size_t n = std::min(nb - i0, (size_t)MaxGroup);
+            for (size_t i = 0; i < n; ++i) {
+                const Block& b = blocks[i0 + i];
+                q[i] = dw_problem(b, b.a.A8, b.Lo.w2, b.a.F, b.a.d, b.a.s_w2, b.a.dW2);
+            }
+            S3R_TRY(umma_dw_group(q, (int)n, a->d_status, stream));
+        }
+    } else {
+        for (Block& b : blocks) S3R_TRY(step_dw2(b, stream));
+    }
+    S3R_TRY(record(a, 4, stream));
+    for (Block& b : blocks) S3R_TRY(step_swiglu(b, stream));
+    S3R_TRY(record(a, 5, stream));
+    for (Block& b : blocks) S3R_TRY(step_ec_w13(b, stream));
+    S3R_TRY(record(a, 6, stream));
+    if (f16) {
+        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
+            UmmaDxProblem q[MaxGroup];
+            const size_t n = std::min(nb - i0, (size_t)MaxGroup);
+            for (size_t i = 0; i < n; ++i) q[i] = dx_problem_dx(blocks[i0 + i]);
+            S3R_TRY(umma_dx_group(q, (int)n, a->d_status, stream));
+        }
+    } else {
+        for (Block& b : blocks) S3R_TRY(step_dx(b, stream));
+    }
+    S3R_TRY(record(a, 7, stream));
+    if (f16) {
+        // two problems (dW1, dW3) per expert
+        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup / 2) {
+            UmmaDwProblem q[MaxGroup];
+            const size_t n = std::min(nb - i0, (size_t)MaxGroup / 2);
+            for (size_t i = 0; i < n; ++i) {
+                const Block& b = blocks[i0 + i];
+                q[2 * i] = dw_problem(b, b.a.X8, b.Lo.w1, b.a.d, b.a.F, b.a.s_w1, b.a.dW1);
+                q[2 * i + 1] = dw_problem(b, b.a.X8, b.Lo.w3, b.a.d, b.a.F, b.a.s_w3, b.a.dW3);
+            }
+            S3R_TRY(umma_dw_group(q, (int)(2 * n), a->d_status, stream));
+        }
+    } else {
+        for (Block& b : blocks) S3R_TRY(step_dw13(b, stream));
+    }
+    return record(a, 8, stream);
 }
 
 extern "C" const char* s3r_status_string(int status) {
