@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -373,6 +374,23 @@ def cpu_baseline(tokens=128):
                       f"{dt:.1f} s single-threaded"}
 
 
+def profiled_traffic(kernel: str):
+    """DRAM bytes per GEMM product of `kernel` from the committed ncu summary
+    of this workload, or None when the GEMM source changed since the capture."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    try:
+        txt = open(os.path.join(root, "profiles", "ffn_d2048_F5632_T8192_launches.md")).read()
+        src = open(os.path.join(root, "stochastic_rounding_int8_gb300", "csrc", "gemm_umma.cu"), "rb").read()
+    except OSError:
+        return None
+    m = re.search(r"gemm_umma\.cu sha256: ([0-9a-f]{64})", txt)
+    t = re.search(rf"{kernel}=(\d+)", txt)
+    if not m or not t or m.group(1) != hashlib.sha256(src).hexdigest():
+        return None
+    return int(t.group(1))
+
+
 def run_ours(args, world, rank, local):
     import stochastic_rounding_int8_gb300 as s3r
     s3r.lib()
@@ -400,7 +418,9 @@ def run_ours(args, world, rank, local):
         achieved = flops_per_launch / (dom_ms / dom_n * 1e-3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom),
+                "traffic_note": "DRAM read + write bytes per GEMM product from the committed ncu capture "
+                                "(profiles/ffn_d2048_F5632_T8192_launches.md); null once the GEMM source changed",
                 "peak_note": f"dense bf16 sustained ({pk_kind}); the s8 codes run on the tensor cores at the "
                              f"16-bit rate or below on sm_103a",
                 "flops_per_product": flops_per_launch, "products_per_step": dom_n,
