@@ -123,6 +123,32 @@ __device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// a + b per lane, rounded toward minus infinity
+__device__ __forceinline__ float2 f2_add_rm(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n add.rm.f32x2 z, x, y;\n"
+        " mov.b64 {%0, %1}, z;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// 1.0f if a < b else 0.0f
+__device__ __forceinline__ float lt_one(float a, float b) {
+    float d;
+    asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+// max(m, |a|, |b|), NaN if any of them is NaN
+__device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+    return d;
+}
+// 1.5 * 2^23: for |x| < 2^22, x + kMagic lands in [2^23, 2^24), where the
+// float spacing is 1, so the add rounds x to an integer (in the add's
+// rounding mode) and the low byte of the sum's bits is that integer mod 256.
+constexpr float kMagic = 12582912.0f;
+
 // The SwiGLU derivative terms of two lanes at once, per lane bit-identical to
 //   s = sigmoid_cw(x); silu = x * s; dsilu = s * (1 + x * (1 - s))
 // (exp_cw of -x with the negation folded into the reduction constants, the

@@ -124,23 +124,31 @@ __device__ __forceinline__ void round_and_store(const float (&ng)[RPT][8], uint3
                 }
             }
         }
-        float qv[8];
+        // qm = kMagic + q (exact): floor and round-to-nearest are adds of kMagic
+        // on the FMA pipe, and the int8 code is the low byte of qm's bits
+        float qv[8], qm[8];
         float2 rs = make_float2(0.0f, 0.0f);
+        const float2 M2 = make_float2(kMagic, kMagic);
         if (!nonfinite) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float2 g2 = make_float2(ng[j][2 * k], ng[j][2 * k + 1]);
-                const float2 y = f2_mul(g2, ninv2);                  // = g * inv, exactly
-                float2 q;
+                const float2 y = f2_mul(g2, ninv2);                  // = g * inv, |y| <= 127
+                float2 m;
                 if (MODE == kRTNE) {
-                    q = make_float2(rintf(y.x), rintf(y.y));
+                    // per lane: a packed add that is the product's only use would be fused into an fma
+                    m = make_float2(__fadd_rn(y.x, kMagic), __fadd_rn(y.y, kMagic));   // kMagic + rint(y)
                 } else {
-                    const float2 f = make_float2(floorf(y.x), floorf(y.y));
-                    const float2 p = f2_sub(y, f);
+                    const float2 fm = f2_add_rm(y, M2);              // kMagic + floor(y)
+                    const float2 f = f2_sub(fm, M2);                 // floor(y), exact
+                    const float2 p = f2_sub(y, f);                   // residual in [0, 1), exact
                     const float ua = (MODE == kS3R) ? u_row[j] : u8[2 * k];
                     const float ub = (MODE == kS3R) ? u_row[j] : u8[2 * k + 1];
-                    q = f2_add(f, make_float2(ua < p.x ? 1.0f : 0.0f, ub < p.y ? 1.0f : 0.0f));
+                    m = f2_add(fm, make_float2(lt_one(ua, p.x), lt_one(ub, p.y)));   // + [u < p]
                 }
+                const float2 q = f2_sub(m, M2);                      // the code, exact
+                qm[2 * k] = m.x;
+                qm[2 * k + 1] = m.y;
                 qv[2 * k] = q.x;
                 qv[2 * k + 1] = q.y;
                 const float2 e = f2_fma(d2, q, g2);                  // delta*q - g
@@ -149,7 +157,10 @@ __device__ __forceinline__ void round_and_store(const float (&ng)[RPT][8], uint3
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) qv[i] = 0.0f;
+            for (int i = 0; i < 8; ++i) {
+                qv[i] = 0.0f;
+                qm[i] = kMagic;
+            }
         }
         const float rowsum = rs.x + rs.y;
         if (t < C.T) {
@@ -157,8 +168,8 @@ __device__ __forceinline__ void round_and_store(const float (&ng)[RPT][8], uint3
                 uint32_t w[2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const int a = __float2int_rn(qv[4 * k]), b = __float2int_rn(qv[4 * k + 1]);
-                    const int cc = __float2int_rn(qv[4 * k + 2]), dd = __float2int_rn(qv[4 * k + 3]);
+                    const uint32_t a = __float_as_uint(qm[4 * k]), b = __float_as_uint(qm[4 * k + 1]);
+                    const uint32_t cc = __float_as_uint(qm[4 * k + 2]), dd = __float_as_uint(qm[4 * k + 3]);
                     w[k] = __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(cc, dd, 0x0040), 0x5410);
                 }
                 int8_t* dst = static_cast<int8_t*>(O.Q) + t * C.N + nc0;
@@ -327,7 +338,6 @@ __global__ void __launch_bounds__(256, 2)
     constexpr int RPT = 8;
     using Geo = TileGeom<RPT>;
     extern __shared__ __align__(128) uint8_t qsmem[];
-    uint16_t* buf[2] = {reinterpret_cast<uint16_t*>(qsmem), reinterpret_cast<uint16_t*>(qsmem + kTile * kTile * 2)};
     uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + 2 * kTile * kTile * 2);
     __shared__ uint32_t red[Geo::kWarps];
     __shared__ float col_smem[Geo::kWarps * 128];
@@ -345,7 +355,8 @@ __global__ void __launch_bounds__(256, 2)
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmG) : "memory");
         for (int k = 0; k < 2 && first + k * stride < ntiles; ++k) {
             const int64_t tile = first + k * stride;
-            q_issue_tile((uint32_t)__cvta_generic_to_shared(buf[k]), &tmG, (int32_t)((tile % C.ntc) * kTile),
+            q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + k * (kTile * kTile * 2)), &tmG,
+                         (int32_t)((tile % C.ntc) * kTile),
                          (int32_t)((tile / C.ntc) * kTile), k ? bar1 : bar0);
             ++issued;
         }
@@ -363,12 +374,13 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int k = 0; k < 8; ++k) sw[k] = (A.s_w && nc0 + k < C.N) ? __ldg(A.s_w + nc0 + k) : 1.0f;
         float g[RPT][8];
-        uint32_t amax_bits = 0u;
+        float amax = 0.0f;   // NaN-propagating absmax
+        const uint16_t* tb = reinterpret_cast<const uint16_t*>(qsmem + b * (kTile * kTile * 2));
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             const int rr = r0 + j * Geo::kRowStride;
             const int64_t t = t0 + rr;
-            const uint4 raw = *reinterpret_cast<const uint4*>(buf[b] + rr * kTile + 8 * c);
+            const uint4 raw = *reinterpret_cast<const uint4*>(tb + rr * kTile + 8 * c);
             // negated fold: (-s_x) * G * s_w == -((s_x * G) * s_w) exactly; a missing scale is 1
             const float nsx = (A.s_x && t < C.T) ? -__ldg(A.s_x + t) : -1.0f;
             const float2 nsx2 = make_float2(nsx, nsx);
@@ -379,17 +391,19 @@ __global__ void __launch_bounds__(256, 2)
                 v = f2_mul(v, make_float2(sw[2 * k], sw[2 * k + 1]));
                 g[j][2 * k] = v.x;
                 g[j][2 * k + 1] = v.y;
-                amax_bits = max(amax_bits, max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu));
+                amax = max3_abs_nan(amax, v.x, v.y);
             }
         }
-        // block absmax; the first barrier also means every thread is done with buf[b]
-        amax_bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+        // block absmax (non-negative floats and NaN order like their bit patterns);
+        // the first barrier also means every thread is done with this buffer
+        uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
         if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax_bits;
         __syncthreads();
         if (threadIdx.x == 0 && tile + 2 * stride < ntiles) {
             const int64_t nt = tile + 2 * stride;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            q_issue_tile((uint32_t)__cvta_generic_to_shared(buf[b]), &tmG, (int32_t)((nt % C.ntc) * kTile),
+            q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + b * (kTile * kTile * 2)), &tmG,
+                         (int32_t)((nt % C.ntc) * kTile),
                          (int32_t)((nt / C.ntc) * kTile), b ? bar1 : bar0);
             ++issued;
         }
