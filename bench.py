@@ -323,6 +323,44 @@ def time_moe(s3r, steps=5, warmup=2):
     return out
 
 
+def time_ffn_large(s3r, steps=5, warmup=2):
+    """Context: the larger SwiGLU block (d=4096, F=14336, T=16384 = 8 x 2048,
+    Table III's W7 shape): S3R-EC two-way, S3R-EC dX-only, S3R, independent SR
+    and the BF16 cuBLAS backward of the same block."""
+    w = workloads.WORKLOADS["swiglu_ffn_d4096_F14336_T16384"]
+    Tl, dl, Fl, Sl = w["T"], w["d"], w["F"], w["S"]
+    inp = workloads.ffn_inputs(Tl, dl, Fl, Sl, seed=workloads.DATA_SEED + 2)
+    c = lambda t: t.cuda()
+    ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
+    dY = inp.dY.cuda()
+    st = s3r.new_status()
+    out = {}
+    for name, rm, ec in (("s3r_ec_two_way", s3r.ROUND_S3R, s3r.EC_TWO_WAY), ("s3r_ec_dx_only", s3r.ROUND_S3R,
+                         s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE), ("indep_sr_int8", s3r.ROUND_INDEP,
+                         s3r.EC_NONE)):
+        ws = torch.empty(s3r.ffn_workspace_size(Tl, dl, Fl, Sl, rm, ec), dtype=torch.uint8, device="cuda")
+        grads = s3r.alloc_ffn_grads(Tl, dl, Fl)
+        for i in range(warmup):
+            s3r.ffn_backward(ops, dY, Sl, rm, ec, seed=i, grads=grads, workspace=ws, status=st)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(steps):
+            s3r.ffn_backward(ops, dY, Sl, rm, ec, seed=100 + i, grads=grads, workspace=ws, status=st)
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        out[name] = {"tokens_s": round(Tl / (ms * 1e-3), 1), "ms": round(ms, 4),
+                     "gemm_tflops_if_all_gemm": round(12.0 * Tl * dl * Fl / (ms * 1e-3) / 1e12, 1)}
+        del ws, grads
+    s3r.check_status(st)
+    bms = time_bf16_backward(inp, steps, warmup)
+    out["bf16_cublas_backward"] = {"tokens_s": round(Tl / (bms * 1e-3), 1), "ms": round(bms, 4)}
+    out["s3r_ec_two_way_vs_bf16"] = round(bms / out["s3r_ec_two_way"]["ms"], 3)
+    out["s3r_ec_two_way_vs_indep_sr"] = round(out["indep_sr_int8"]["ms"] / out["s3r_ec_two_way"]["ms"], 3)
+    return out
+
+
 def time_quantize_sweep(s3r, steps=20):
     """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100
     outliers; int8 codes (1 B) and fp16-carried codes (2 B)."""
@@ -467,6 +505,7 @@ def run_ours(args, world, rank, local):
             qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
         ctx["quantize_sweep"] = qs
         ctx["moe_e8_d4096_F1408_tok16384_top2"] = time_moe(s3r)
+        ctx["swiglu_ffn_d4096_F14336_T16384"] = time_ffn_large(s3r)
         line["context"] = ctx
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -181,15 +181,17 @@ __global__ void ec_xsum_reduce_generic_kernel(const int32_t* xs, const float* ps
 
 // rowsum[k] = sum_n W8[k,n] and v[b,k] = sum_n (colmean[b,n] - mu[b]) W8[k,n].
 // One 512-thread CTA per SM.  Each CTA first computes every mu[b] (fixed
-// order, the same bits in every CTA; the first CTA of a linear stores them),
-// then stages the centered means of kGemvBch examples in shared memory and
-// streams weight rows: a warp takes kGemvRows rows at a time (rows strided
-// over all warps of the linear); its lanes stride each row 8 codes (one
-// 16-byte load) at a time, issuing the loads of kGemvUnroll chunks of every
-// row before the arithmetic; the row sums meet in a butterfly.  CTAs
-// [0, ctas0) serve linear 0, the rest linear 1.
-constexpr int kGemvRows = 2, kGemvBch = 4, kGemvUnroll = 8;
+// order, the same bits in every CTA; the first CTA of a linear stores them).
+// A warp owns up to kGemvPairs pairs of weight rows (pairs strided over all
+// warps of the linear) and keeps their sums in registers while the CTA walks
+// the examples kGemvBch at a time and the channels in slabs of `slab`: the
+// centered means of a slab are staged in shared memory, and the lanes stride
+// each row 8 codes (one 16-byte load) at a time with the loads of
+// kGemvUnroll chunks in flight.  The row sums meet in a butterfly after the
+// last slab.  CTAs [0, ctas0) serve linear 0, the rest linear 1.
+constexpr int kGemvRows = 2, kGemvBch = 4, kGemvUnroll = 8, kGemvPairs = 3;
 constexpr int kGemvWarps = kGemvThreads / 32;
+constexpr int64_t kGemvSlabFloats = 24 * 1024;   // staged means per slab (all kGemvBch examples): 96 KiB
 
 struct EcGemvArgs {
     const void* W8[kMaxJobs];
@@ -199,12 +201,13 @@ struct EcGemvArgs {
     int32_t* rowsum[kMaxJobs];
     float* v[kMaxJobs];
     int64_t K, N, S, B;
+    int64_t slab;                // channels per staged slab (multiple of 8)
     int ctas0, ctas1;
 };
 
-// dynamic shared memory: 8 x 512 floats (reductions) + B rounded to 4 + kGemvBch * N
-static size_t gemv_smem_bytes(int64_t N, int64_t B) {
-    return (size_t)(8 * kGemvThreads + ((B + 3) & ~(int64_t)3) + kGemvBch * N) * sizeof(float);
+// dynamic shared memory: 8 x 512 floats (reductions) + B rounded to 4 + kGemvBch * slab
+static size_t gemv_smem_bytes(int64_t slab, int64_t B) {
+    return (size_t)(8 * kGemvThreads + ((B + 3) & ~(int64_t)3) + kGemvBch * slab) * sizeof(float);
 }
 
 template <typename CodeT>
@@ -227,10 +230,10 @@ __device__ __forceinline__ void codes8(const uint4& w, float (&f)[8], int8_t) {
 template <typename CodeT>
 __global__ void __launch_bounds__(kGemvThreads) ec_gemv_kernel(EcGemvArgs A) {
     extern __shared__ __align__(16) float sm[];
-    const int64_t K = A.K, N = A.N, S = A.S, B = A.B;
+    const int64_t K = A.K, N = A.N, S = A.S, B = A.B, slab = A.slab;
     float* red = sm;
     float* mu_s = sm + 8 * kGemvThreads;
-    float* cm = mu_s + ((B + 3) & ~(int64_t)3);
+    float* cm = mu_s + ((B + 3) & ~(int64_t)3);   // [kGemvBch][slab]
     const int j = (int)blockIdx.x < A.ctas0 ? 0 : 1;
     const CodeT* W8 = static_cast<const CodeT*>(j ? A.W8[1] : A.W8[0]);
     const float* colmean = j ? A.colmean[1] : A.colmean[0];
@@ -246,82 +249,95 @@ __global__ void __launch_bounds__(kGemvThreads) ec_gemv_kernel(EcGemvArgs A) {
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t gw = cta * kGemvWarps + warp, nw = nctas * kGemvWarps;
-    const int64_t nch = N / 8, n4 = N / 4;
     for (int64_t b0 = 0; b0 < B; b0 += kGemvBch) {
-        __syncthreads();   // the previous pass is done with cm
+        float acc[kGemvPairs][kGemvRows][kGemvBch];
+        int rs[kGemvPairs][kGemvRows];
 #pragma unroll
-        for (int q = 0; q < kGemvBch; ++q) {
-            const bool on = b0 + q < B;
-            const float m = on ? mu_s[b0 + q] : 0.0f;
-            for (int64_t i = threadIdx.x; i < n4; i += kGemvThreads) {
-                float4 c = on ? __ldg(reinterpret_cast<const float4*>(colmean + (b0 + q) * N) + i)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                c.x -= m; c.y -= m; c.z -= m; c.w -= m;
-                reinterpret_cast<float4*>(cm + q * N)[i] = on ? c : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int pp = 0; pp < kGemvPairs; ++pp)
+#pragma unroll
+            for (int r = 0; r < kGemvRows; ++r) {
+                rs[pp][r] = 0;
+#pragma unroll
+                for (int q = 0; q < kGemvBch; ++q) acc[pp][r][q] = 0.0f;
+            }
+        for (int64_t n0 = 0; n0 < N; n0 += slab) {
+            const int64_t ns = N - n0 < slab ? N - n0 : slab;   // channels in this slab (multiple of 8)
+            __syncthreads();   // the previous slab is done with cm
+#pragma unroll
+            for (int q = 0; q < kGemvBch; ++q) {
+                const bool on = b0 + q < B;
+                const float m = on ? mu_s[b0 + q] : 0.0f;
+                for (int64_t i = threadIdx.x; i < ns / 4; i += kGemvThreads) {
+                    float4 c = on ? __ldg(reinterpret_cast<const float4*>(colmean + (b0 + q) * N + n0) + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    c.x -= m; c.y -= m; c.z -= m; c.w -= m;
+                    reinterpret_cast<float4*>(cm + q * slab)[i] = on ? c : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            __syncthreads();
+            const int64_t nch = ns / 8;
+#pragma unroll
+            for (int pp = 0; pp < kGemvPairs; ++pp) {
+                const int64_t k0 = (gw + pp * nw) * kGemvRows;
+                if (k0 >= K) break;
+                const CodeT* wrow[kGemvRows];
+#pragma unroll
+                for (int r = 0; r < kGemvRows; ++r) wrow[r] = W8 + (k0 + r < K ? k0 + r : K - 1) * N + n0;   // clamped
+                for (int64_t c0 = 0; c0 < nch; c0 += 32 * kGemvUnroll) {
+                    uint4 raw[kGemvUnroll][kGemvRows];
+#pragma unroll
+                    for (int u = 0; u < kGemvUnroll; ++u) {
+                        const int64_t ch = c0 + 32 * u + lane;
+                        const int64_t chc = ch < nch ? ch : nch - 1;   // clamped: always a valid load
+#pragma unroll
+                        for (int r = 0; r < kGemvRows; ++r) raw[u][r] = raw8(wrow[r] + 8 * chc);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kGemvUnroll; ++u) {
+                        const int64_t ch = c0 + 32 * u + lane;
+                        if (ch >= nch) break;
+                        float w[kGemvRows][8];
+#pragma unroll
+                        for (int r = 0; r < kGemvRows; ++r) {
+                            codes8(raw[u][r], w[r], CodeT{});
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) rs[pp][r] += (int)w[r][i];
+                        }
+#pragma unroll
+                        for (int q = 0; q < kGemvBch; ++q) {
+                            const float4 x0 = *reinterpret_cast<const float4*>(cm + q * slab + 8 * ch);
+                            const float4 x1 = *reinterpret_cast<const float4*>(cm + q * slab + 8 * ch + 4);
+                            const float c[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) acc[pp][r][q] = fmaf(c[i], w[r][i], acc[pp][r][q]);
+                        }
+                    }
+                }
             }
         }
-        __syncthreads();
-        for (int64_t k0 = gw * kGemvRows; k0 < K; k0 += nw * kGemvRows) {
-            const CodeT* wrow[kGemvRows];
 #pragma unroll
-            for (int r = 0; r < kGemvRows; ++r) wrow[r] = W8 + (k0 + r < K ? k0 + r : K - 1) * N;   // clamped
-            float acc[kGemvRows][kGemvBch];
-            int rs[kGemvRows];
-#pragma unroll
-            for (int r = 0; r < kGemvRows; ++r) {
-                rs[r] = 0;
-#pragma unroll
-                for (int q = 0; q < kGemvBch; ++q) acc[r][q] = 0.0f;
-            }
-            for (int64_t c0 = 0; c0 < nch; c0 += 32 * kGemvUnroll) {
-                uint4 raw[kGemvUnroll][kGemvRows];
-#pragma unroll
-                for (int u = 0; u < kGemvUnroll; ++u) {
-                    const int64_t ch = c0 + 32 * u + lane;
-                    const int64_t chc = ch < nch ? ch : nch - 1;   // clamped: always a valid load
-#pragma unroll
-                    for (int r = 0; r < kGemvRows; ++r) raw[u][r] = raw8(wrow[r] + 8 * chc);
-                }
-#pragma unroll
-                for (int u = 0; u < kGemvUnroll; ++u) {
-                    const int64_t ch = c0 + 32 * u + lane;
-                    if (ch >= nch) break;
-                    float w[kGemvRows][8];
-#pragma unroll
-                    for (int r = 0; r < kGemvRows; ++r) {
-                        codes8(raw[u][r], w[r], CodeT{});
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) rs[r] += (int)w[r][i];
-                    }
-#pragma unroll
-                    for (int q = 0; q < kGemvBch; ++q) {
-                        const float4 x0 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch);
-                        const float4 x1 = *reinterpret_cast<const float4*>(cm + q * N + 8 * ch + 4);
-                        const float c[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                        for (int r = 0; r < kGemvRows; ++r)
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) acc[r][q] = fmaf(c[i], w[r][i], acc[r][q]);
-                    }
-                }
-            }
+        for (int pp = 0; pp < kGemvPairs; ++pp) {
+            const int64_t k0 = (gw + pp * nw) * kGemvRows;
+            if (k0 >= K) break;
 #pragma unroll
             for (int r = 0; r < kGemvRows; ++r) {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) rs[r] += __shfl_xor_sync(0xFFFFFFFFu, rs[r], o);
+                for (int o = 16; o > 0; o >>= 1) rs[pp][r] += __shfl_xor_sync(0xFFFFFFFFu, rs[pp][r], o);
 #pragma unroll
                 for (int q = 0; q < kGemvBch; ++q)
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) acc[r][q] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][q], o);
+                    for (int o = 16; o > 0; o >>= 1) acc[pp][r][q] += __shfl_xor_sync(0xFFFFFFFFu, acc[pp][r][q], o);
             }
             if (lane == 0) {
 #pragma unroll
                 for (int r = 0; r < kGemvRows; ++r) {
                     if (k0 + r >= K) continue;
-                    if (b0 == 0) rowsum[k0 + r] = rs[r];
+                    if (b0 == 0) rowsum[k0 + r] = rs[pp][r];
 #pragma unroll
                     for (int q = 0; q < kGemvBch; ++q)
-                        if (b0 + q < B) v[(b0 + q) * K + k0 + r] = acc[r][q];
+                        if (b0 + q < B) v[(b0 + q) * K + k0 + r] = acc[pp][r][q];
                 }
             }
         }
@@ -473,8 +489,21 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
     const bool two = ec_mode == S3R_EC_TWO_WAY;
     bool vec_w = N % 8 == 0;
     for (int j = 0; j < nj; ++j) vec_w = vec_w && s3r_aligned16(jobs[j].W8) && s3r_aligned16(jobs[j].colmean);
-    const size_t gsm = gemv_smem_bytes(N, B);
+    const int64_t slab = std::min<int64_t>(N, kGemvSlabFloats / kGemvBch);   // multiple of 8 when N is
+    const size_t gsm = gemv_smem_bytes(slab, B);
     vec_w = vec_w && gsm <= 200 * 1024;
+    // every warp holds at most kGemvPairs row pairs: one CTA per SM gives sms * kGemvWarps warps per launch
+    int gsms = 148;
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&gsms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            gsms = 148;
+        }
+    }
+    const int64_t per_job = std::max<int64_t>(1, gsms / nj);
+    vec_w = vec_w && s3r_cdiv(K, kGemvRows) <= per_job * kGemvWarps * kGemvPairs;
     const bool vec_x = K % 8 == 0 && s3r_aligned16(X8);
     // workspace: xs [nch, K] | ps [nj, nch, K] | counters
     const int64_t nch = s3r_cdiv(T, kXsumChunk), ncb = s3r_cdiv(K, 256);
@@ -520,16 +549,10 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
             G.rowsum[j] = jobs[j].rowsum;
             G.v[j] = jobs[j].v;
         }
-        G.K = K; G.N = N; G.S = S; G.B = B;
+        G.K = K; G.N = N; G.S = S; G.B = B; G.slab = slab;
         // persistent: one CTA per SM in all, split evenly between the linears
-        int dev = 0, sms = 148;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess) {
-            (void)cudaGetLastError();
-            sms = 148;
-        }
-        const int64_t need = s3r_cdiv(K, kGemvWarps * kGemvRows);   // CTAs that give every warp a row block
-        const int64_t per = std::min<int64_t>(need, std::max<int64_t>(1, sms / nj));
+        const int64_t need = s3r_cdiv(K, kGemvWarps * kGemvRows);   // CTAs that give every warp a row pair
+        const int64_t per = std::min<int64_t>(need, per_job);
         G.ctas0 = (int)per;
         G.ctas1 = nj > 1 ? (int)per : 0;
         static bool attr = false;

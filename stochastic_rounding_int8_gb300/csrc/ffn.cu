@@ -306,6 +306,73 @@ s3r_ffn_args expert_view(const s3r_ffn_args& a, int64_t e, int64_t r0, int64_t T
     return g;
 }
 
+// Side streams for the grouped mode's per-expert memory-bound steps (EC,
+// quantize, SwiGLU): expert e's launches of such a step go to side stream
+// e % kSideStreams, forked from and joined back to the caller's stream with
+// events, so small experts' kernels overlap instead of running one after
+// another.  Created once per device (non-blocking streams and timing-free
+// events); the fork and join are plain event waits, so a stream capture of
+// the caller's stream captures them as graph edges.  The pool is per host
+// thread (two threads' calls never share its events) and lives until exit.
+constexpr int kSideStreams = 4;
+struct SidePool {
+    cudaStream_t s[kSideStreams];
+    cudaEvent_t fork, join[kSideStreams];
+    bool ok = false;
+};
+thread_local SidePool g_side[64];
+
+int side_pool(SidePool** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("ffn_backward: cudaGetDevice", e == cudaSuccess ? cudaErrorInvalidDevice : e);
+    }
+    SidePool& p = g_side[dev];
+    if (!p.ok) {
+        for (int i = 0; i < kSideStreams && e == cudaSuccess; ++i)
+            e = cudaStreamCreateWithFlags(&p.s[i], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.fork, cudaEventDisableTiming);
+        for (int i = 0; i < kSideStreams && e == cudaSuccess; ++i)
+            e = cudaEventCreateWithFlags(&p.join[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return s3r_cuda_fail("ffn_backward: side streams", e);
+        }
+        p.ok = true;
+    }
+    *out = &p;
+    return S3R_OK;
+}
+
+// Runs step(b, stream) for every block, block i on side stream i % kSideStreams,
+// between a fork from and a join back to `main`.
+template <typename Step>
+int run_on_side_streams(std::vector<Block>& blocks, Step step, cudaStream_t main) {
+    SidePool* p = nullptr;
+    S3R_TRY(side_pool(&p));
+    const int used = (int)std::min<size_t>(blocks.size(), (size_t)kSideStreams);
+    cudaError_t e = cudaEventRecord(p->fork, main);
+    for (int i = 0; i < used && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(p->s[i], p->fork, 0);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("ffn_backward: fork", e);
+    }
+    int st = S3R_OK;
+    for (size_t i = 0; i < blocks.size() && st == S3R_OK; ++i) st = step(blocks[i], p->s[i % kSideStreams]);
+    // join every side stream that was forked, also after a failure
+    for (int i = 0; i < used && e == cudaSuccess; ++i) {
+        e = cudaEventRecord(p->join[i], p->s[i]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(main, p->join[i], 0);
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("ffn_backward: join", e);
+    }
+    return st;
+}
+
 // Workspace of the grouped mode: one block carve per non-empty expert, side by side.
 size_t grouped_bytes(const int64_t* off, int64_t E, int64_t d, int64_t F, int round_mode, int fmt) {
     size_t total = 0;
@@ -401,9 +468,9 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     const bool f16 = fmt == S3R_CODES_F16;
     const size_t nb = blocks.size();
     S3R_TRY(record(a, 0, stream));
-    for (Block& b : blocks) S3R_TRY(step_quantize_dy(b, stream));
+    S3R_TRY(run_on_side_streams(blocks, step_quantize_dy, stream));
     S3R_TRY(record(a, 1, stream));
-    for (Block& b : blocks) S3R_TRY(step_ec_w2(b, stream));
+    S3R_TRY(run_on_side_streams(blocks, step_ec_w2, stream));
     S3R_TRY(record(a, 2, stream));
     if (f16) {
         for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
@@ -430,9 +497,9 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
         for (Block& b : blocks) S3R_TRY(step_dw2(b, stream));
     }
     S3R_TRY(record(a, 4, stream));
-    for (Block& b : blocks) S3R_TRY(step_swiglu(b, stream));
+    S3R_TRY(run_on_side_streams(blocks, step_swiglu, stream));
     S3R_TRY(record(a, 5, stream));
-    for (Block& b : blocks) S3R_TRY(step_ec_w13(b, stream));
+    S3R_TRY(run_on_side_streams(blocks, step_ec_w13, stream));
     S3R_TRY(record(a, 6, stream));
     if (f16) {
         for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {

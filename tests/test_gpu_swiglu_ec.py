@@ -52,7 +52,8 @@ def test_swiglu_quantize_parity(s3r, orc, fmt, mode, T, F):
 @pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
 @pytest.mark.parametrize("ec_mode", ["EC_DX_ONLY", "EC_TWO_WAY"])
 @pytest.mark.parametrize("T,N,K,S", [(256, 1024, 512, 256), (512, 384, 200, 128), (300, 260, 72, 300),
-                                     (1024, 256, 130, 256), (1280, 256, 136, 128), (384, 5632, 264, 128)])
+                                     (1024, 256, 130, 256), (1280, 256, 136, 128), (384, 5632, 264, 128),
+                                     (512, 7000, 264, 128), (256, 512, 5008, 128)])
 def test_ec_factors_parity(s3r, orc, fmt, ec_mode, T, N, K, S):
     rng = np.random.default_rng(T + N + K)
     G = (rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)
