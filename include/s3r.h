@@ -308,6 +308,9 @@ int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int cod
  *   6. EC factors for W1 and W3
  *   7. dX  = int8_gemm_dx_sum({Q1, W1_8}, {Q3, W3_8})
  *   8. dW1 = int8_gemm_dw(X8, Q1), dW3 = int8_gemm_dw(X8, Q3)
+ * With fp16 codes, steps 3 and 4 run as one tcgen05 launch and so do steps 7
+ * and 8 (each tile computed exactly as in the separate calls); their step
+ * events 4 and 8 then follow 3 and 7 directly.
  * Independent SR quantizes each gradient twice (tensor ids + 0x100 for the
  * dW copy) and applies no correction; RTNE applies no correction either.
  * All buffers are device pointers owned by the caller; `args` itself is a

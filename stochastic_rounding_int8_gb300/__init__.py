@@ -380,6 +380,7 @@ class _FfnArgs(C.Structure):
 FFN_NUM_EVENTS = 9
 FFN_STEPS = ["quantize dY", "EC W2", "GEMM dA (dX of W2)", "GEMM dW2", "SwiGLU + quantize dh1/dh3", "EC W1/W3",
              "GEMM dX (W1 + W3)", "GEMM dW1 + dW3"]
+# with fp16 codes, steps 3 + 4 and 7 + 8 are one launch each (their time lands on 3 and 7)
 
 
 @dataclass

@@ -198,8 +198,8 @@ void s3r_count_launch();
 void s3r_record_error(const char* where, const char* what);
 int s3r_cuda_fail(const char* where, cudaError_t err);
 
-// Grouped tcgen05 GEMMs on fp16-carried codes (gemm_umma.cu): up to 16
-// problems of one kind in one persistent launch, each computed exactly as a
+// Grouped tcgen05 GEMMs on fp16-carried codes (gemm_umma.cu): up to 24
+// problems in one persistent launch, each computed exactly as a
 // launch of its own would compute it.
 struct UmmaDxProblem {
     const void* Q;               // [T, N] codes, tile scales, W [K, N], correction terms
@@ -239,6 +239,10 @@ struct UmmaDwProblem {
 };
 int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream);
 int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t stream);
+// dX and dW problems together (up to 24 in all): one launch, tiles of the
+// longest problems first
+int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, int* d_status,
+                     cudaStream_t stream);
 
 // S3R-EC factors of the two linears that read the same input X (W1 and W3 of
 // the SwiGLU block) in one pass; bit-identical to two s3r_ec_correct calls

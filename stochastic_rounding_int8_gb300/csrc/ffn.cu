@@ -32,7 +32,7 @@ extern "C" const char* s3r_last_error(void) { return g_last_error; }
 namespace {
 
 constexpr uint32_t kRhsOffset = S3R_TID_RHS_OFFSET;
-constexpr int MaxGroup = 16;   // problems per multi-problem GEMM launch
+constexpr int MaxGroup = 24;   // problems per multi-problem GEMM launch
 
 struct Carver {
     uintptr_t cur, end;
@@ -417,17 +417,34 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
         S3R_TRY(record(a, 1, stream));
         S3R_TRY(step_ec_w2(b, stream));
         S3R_TRY(record(a, 2, stream));
-        S3R_TRY(step_da(b, stream));
-        S3R_TRY(record(a, 3, stream));
-        S3R_TRY(step_dw2(b, stream));
+        if (fmt == S3R_CODES_F16) {
+            // dA and dW2 in one mixed launch (their tiles share the grid); step 4 is then empty
+            const UmmaDxProblem qx = dx_problem_da(b);
+            const UmmaDwProblem qw = dw_problem(b, b.a.A8, b.Lo.w2, b.a.F, b.a.d, b.a.s_w2, b.a.dW2);
+            S3R_TRY(umma_mixed_group(&qx, 1, &qw, 1, a->d_status, stream));
+            S3R_TRY(record(a, 3, stream));
+        } else {
+            S3R_TRY(step_da(b, stream));
+            S3R_TRY(record(a, 3, stream));
+            S3R_TRY(step_dw2(b, stream));
+        }
         S3R_TRY(record(a, 4, stream));
         S3R_TRY(step_swiglu(b, stream));
         S3R_TRY(record(a, 5, stream));
         S3R_TRY(step_ec_w13(b, stream));
         S3R_TRY(record(a, 6, stream));
-        S3R_TRY(step_dx(b, stream));
-        S3R_TRY(record(a, 7, stream));
-        S3R_TRY(step_dw13(b, stream));
+        if (fmt == S3R_CODES_F16) {
+            // dX1 + dX3, dW1 and dW3 in one mixed launch; step 8 is then empty
+            const UmmaDxProblem qx = dx_problem_dx(b);
+            const UmmaDwProblem qw[2] = {dw_problem(b, b.a.X8, b.Lo.w1, b.a.d, b.a.F, b.a.s_w1, b.a.dW1),
+                                         dw_problem(b, b.a.X8, b.Lo.w3, b.a.d, b.a.F, b.a.s_w3, b.a.dW3)};
+            S3R_TRY(umma_mixed_group(&qx, 1, qw, 2, a->d_status, stream));
+            S3R_TRY(record(a, 7, stream));
+        } else {
+            S3R_TRY(step_dx(b, stream));
+            S3R_TRY(record(a, 7, stream));
+            S3R_TRY(step_dw13(b, stream));
+        }
         return record(a, 8, stream);
     }
     // grouped: expert e owns rows offsets[e] .. offsets[e+1] (one example);
@@ -473,27 +490,23 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     S3R_TRY(run_on_side_streams(blocks, step_ec_w2, stream));
     S3R_TRY(record(a, 2, stream));
     if (f16) {
-        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
-            UmmaDxProblem q[MaxGroup];
-            const size_t n = std::min(nb - i0, (size_t)MaxGroup);
-            for (size_t i = 0; i < n; ++i) q[i] = dx_problem_da(blocks[i0 + i]);
-            S3R_TRY(umma_dx_group(q, (int)n, a->d_status, stream));
-        }
-    } else {
-        for (Block& b : blocks) S3R_TRY(step_da(b, stream));
-    }
-    S3R_TRY(record(a, 3, stream));
-    if (f16) {
-        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
-            UmmaDwProblem q[MaxGroup];
-            const size_t n = std::min(nb - i0, (size_t)MaxGroup);
+        // dA and dW2 of every expert: mixed launches of up to MaxGroup / 2 experts
+        const size_t per = MaxGroup / 2;
+        for (size_t i0 = 0; i0 < nb; i0 += per) {
+            UmmaDxProblem qx[MaxGroup / 2];
+            UmmaDwProblem qw[MaxGroup / 2];
+            const size_t n = std::min(nb - i0, per);
             for (size_t i = 0; i < n; ++i) {
                 const Block& b = blocks[i0 + i];
-                q[i] = dw_problem(b, b.a.A8, b.Lo.w2, b.a.F, b.a.d, b.a.s_w2, b.a.dW2);
+                qx[i] = dx_problem_da(b);
+                qw[i] = dw_problem(b, b.a.A8, b.Lo.w2, b.a.F, b.a.d, b.a.s_w2, b.a.dW2);
             }
-            S3R_TRY(umma_dw_group(q, (int)n, a->d_status, stream));
+            S3R_TRY(umma_mixed_group(qx, (int)n, qw, (int)n, a->d_status, stream));
         }
+        S3R_TRY(record(a, 3, stream));
     } else {
+        for (Block& b : blocks) S3R_TRY(step_da(b, stream));
+        S3R_TRY(record(a, 3, stream));
         for (Block& b : blocks) S3R_TRY(step_dw2(b, stream));
     }
     S3R_TRY(record(a, 4, stream));
@@ -502,29 +515,24 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     S3R_TRY(run_on_side_streams(blocks, step_ec_w13, stream));
     S3R_TRY(record(a, 6, stream));
     if (f16) {
-        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup) {
-            UmmaDxProblem q[MaxGroup];
-            const size_t n = std::min(nb - i0, (size_t)MaxGroup);
-            for (size_t i = 0; i < n; ++i) q[i] = dx_problem_dx(blocks[i0 + i]);
-            S3R_TRY(umma_dx_group(q, (int)n, a->d_status, stream));
-        }
-    } else {
-        for (Block& b : blocks) S3R_TRY(step_dx(b, stream));
-    }
-    S3R_TRY(record(a, 7, stream));
-    if (f16) {
-        // two problems (dW1, dW3) per expert
-        for (size_t i0 = 0; i0 < nb; i0 += MaxGroup / 2) {
-            UmmaDwProblem q[MaxGroup];
-            const size_t n = std::min(nb - i0, (size_t)MaxGroup / 2);
+        // dX1 + dX3, dW1 and dW3 of every expert: mixed launches of up to MaxGroup / 3 experts
+        const size_t per = MaxGroup / 3;
+        for (size_t i0 = 0; i0 < nb; i0 += per) {
+            UmmaDxProblem qx[MaxGroup / 3];
+            UmmaDwProblem qw[2 * (MaxGroup / 3)];
+            const size_t n = std::min(nb - i0, per);
             for (size_t i = 0; i < n; ++i) {
                 const Block& b = blocks[i0 + i];
-                q[2 * i] = dw_problem(b, b.a.X8, b.Lo.w1, b.a.d, b.a.F, b.a.s_w1, b.a.dW1);
-                q[2 * i + 1] = dw_problem(b, b.a.X8, b.Lo.w3, b.a.d, b.a.F, b.a.s_w3, b.a.dW3);
+                qx[i] = dx_problem_dx(b);
+                qw[2 * i] = dw_problem(b, b.a.X8, b.Lo.w1, b.a.d, b.a.F, b.a.s_w1, b.a.dW1);
+                qw[2 * i + 1] = dw_problem(b, b.a.X8, b.Lo.w3, b.a.d, b.a.F, b.a.s_w3, b.a.dW3);
             }
-            S3R_TRY(umma_dw_group(q, (int)(2 * n), a->d_status, stream));
+            S3R_TRY(umma_mixed_group(qx, (int)n, qw, (int)(2 * n), a->d_status, stream));
         }
+        S3R_TRY(record(a, 7, stream));
     } else {
+        for (Block& b : blocks) S3R_TRY(step_dx(b, stream));
+        S3R_TRY(record(a, 7, stream));
         for (Block& b : blocks) S3R_TRY(step_dw13(b, stream));
     }
     return record(a, 8, stream);

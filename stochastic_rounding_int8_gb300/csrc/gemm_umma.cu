@@ -32,6 +32,7 @@
 // accumulator (dX = Q1 W1^T + Q3 W3^T), each with its own scales.
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <vector>
 
@@ -74,7 +75,8 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + CV_BYTES + 1
 static_assert(SMEM_BYTES + 64 <= 232448, "shared memory budget of one sm_103a CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
-enum Epi { kDX = 0, kDW = 1, kDump = 2 };
+// Epilogue kinds; a kMixed launch takes each problem's kind from the problem.
+enum Epi { kDX = 0, kDW = 1, kDump = 2, kMixed = 3 };
 
 // One contraction segment: scale(mt, nt, kb) = scale[mt*sm + nt*sn + kb*sk],
 // and for the activation gradient its correction terms.
@@ -91,6 +93,7 @@ struct Segment {
 // promoted per 128-wide block, corrected and rescaled in the epilogue.
 struct Problem {
     int64_t M, N;
+    int kind;                    // kDX (K-major operands) or kDW (MN-major operands)
     int ntm, ntn;                // 128 x 256 tiles along M and N
     int tile_base;               // first tile of this problem in the launch's tile order
     int band_rows;               // tile order inside the problem (tile_coords)
@@ -109,11 +112,11 @@ struct Problem {
     int accumulate;
 };
 
-// A launch: up to kMaxProb problems of one kind, their tiles numbered one
+// A launch: up to kMaxProb problems (of one kind, or mixed), their tiles numbered one
 // after another; each problem has up to four tensor maps (A and B of each
 // segment).  Both live in the constant parameter space (__grid_constant__),
 // so indexing them with a run-time problem number costs no copy.
-constexpr int kMaxProb = 16;
+constexpr int kMaxProb = 24;
 struct Args {
     Problem prob[kMaxProb];
     int nprob;
@@ -484,7 +487,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const CUtensorMap* mB = mp + (second ? 3 : 1);
                         const int32_t k0 = (second ? sl - 2 * nkb0 : sl) * BKS;
                         const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
-                        if (!MN) {
+                        if (!(EPI == kMixed ? P.kind == kDW : MN)) {
                             tma_load(a_dst, mA, k0, m0, fb);
                             tma_load(b_dst, mB, k0, n0, fb);
                         } else {
@@ -502,12 +505,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         } else if (warp == 1) {
             if (lane == 0) {
-                constexpr uint32_t idesc = idesc_f16(BM, BN, MN, MN);
                 int it = 0, gkb = 0;   // slice and block counters over the whole run
                 bool ok = true;
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
                     const Problem& P = A.prob[problem_of(A, tile)];
                     const int nkb = (int)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128));
+                    const bool mn = EPI == kMixed ? P.kind == kDW : MN;
+                    const uint32_t idesc = mn ? idesc_f16(BM, BN, true, true) : idesc_f16(BM, BN, false, false);
                     for (int kb = 0; kb < nkb; ++kb, ++gkb) {
                         const int buf = gkb & 1;
                         if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(gkb >> 1) & 1u) ^ 1u, abrt)) {
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int k16 = 0; k16 < BKS / 16; ++k16) {
                                 uint64_t ad, bd;
-                                if (!MN) {
+                                if (!mn) {
                                     ad = sdesc(a0 + 32 * k16, 16, 1024);
                                     bd = sdesc(b0 + 32 * k16, 16, 1024);
                                 } else {
@@ -569,7 +573,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t row = (int64_t)mt * BM + 32 * q + lane;
             const int64_t c0 = (int64_t)nt * 128;
             float acc[128];
-            if (EPI != kDump) seed_tile<EPI>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
+            if (EPI == kMixed) {
+                if (P.kind == kDX) seed_tile<kDX>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
+                else seed_tile<kDW>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
+            } else if (EPI != kDump) {
+                seed_tile<EPI>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
+            }
             // scale of block kb, loaded one block ahead
             auto scale_of = [&](int kb) -> float {
                 if (EPI == kDump) return 0.0f;
@@ -627,7 +636,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
             }
             if (EPI == kDump || !ok) continue;
-            finish_tile<EPI>(P, acc, cv, stage, row, c0, lane);
+            if (EPI == kMixed) {
+                if (P.kind == kDX) finish_tile<kDX>(P, acc, cv, stage, row, c0, lane);
+                else finish_tile<kDW>(P, acc, cv, stage, row, c0, lane);
+            } else {
+                finish_tile<EPI>(P, acc, cv, stage, row, c0, lane);
+            }
         }
     }
     __syncthreads();
@@ -781,9 +795,77 @@ static void dx_segment(umma::Segment& g, const float* tile_scale, int64_t N, con
     g.eps = eps; g.rowsum = rowsum; g.v = v;
 }
 
-// dX problems (fp16-carried codes): A = Q [T, N], B = W [K, N] (both K-major);
+// dX problem (fp16-carried codes): A = Q [T, N], B = W [K, N] (both K-major);
 // a second term (Q3, W3) contracts into the same accumulator:
 // dX = Q W^T + Q3 W3^T, each term with its own tile scales and correction.
+static int add_dx_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDxProblem& q, double (&strip)[2]) {
+    const int64_t T = q.T, N = q.N, K = q.K, S = q.S > 0 ? q.S : q.T;
+    const bool two = q.Q3 != nullptr;
+    if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.W) || N % 8 != 0) return S3R_ERR_ALIGN;
+    if (two && (!s3r_aligned16(q.Q3) || !s3r_aligned16(q.W3))) return S3R_ERR_ALIGN;
+    if (q.ec_mode && S < T && S % kTile != 0) {
+        // the epilogue stages v for at most kNbX examples per 128-row tile
+        int64_t nb = 0;
+        for (int64_t m0 = 0; m0 < T; m0 += umma::BM) {
+            const int64_t hi = (m0 + umma::BM - 1 < T ? m0 + umma::BM - 1 : T - 1) / S;
+            if (hi - m0 / S + 1 > nb) nb = hi - m0 / S + 1;
+        }
+        if (nb > umma::kNbX) {
+            char buf[160];
+            snprintf(buf, sizeof(buf), "S = %lld lets a 128-token tile span %lld examples; the fp16-code path takes %d",
+                     (long long)S, (long long)nb, umma::kNbX);
+            s3r_record_error("int8_gemm_dx", buf);
+            return S3R_ERR_UNSUPPORTED;
+        }
+    }
+    CUtensorMap* m = maps.m[i];
+    int st = umma::make_map(&m[0], q.Q, N, T, N, umma::BM);
+    if (!st) st = umma::make_map(&m[1], q.W, N, K, N, umma::BN);
+    if (!st && two) st = umma::make_map(&m[2], q.Q3, N, T, N, umma::BM);
+    if (!st && two) st = umma::make_map(&m[3], q.W3, N, K, N, umma::BN);
+    if (st) return st;
+    if (!two) {
+        m[2] = m[0];
+        m[3] = m[1];
+    }
+    umma::Problem& P = A.prob[i];
+    P = umma::Problem{};
+    P.M = T; P.N = K; P.kind = umma::kDX;
+    dx_segment(P.seg[0], q.tile_scale, N, q.eps, q.rowsum, q.v);
+    if (two) dx_segment(P.seg[1], q.tile_scale3, N, q.eps3, q.rowsum3, q.v3);
+    P.C = q.dX; P.ldc = K; P.dump = q.dump; P.s_row = q.s_x; P.ec_mode = q.ec_mode; P.S = S;
+    P.accumulate = q.accumulate;
+    // bytes per row strip of A (BM rows of Q over the contraction) and per column strip of B (BN rows of W)
+    const double kbytes = 2.0 * (double)N * (two ? 2 : 1);
+    strip[0] = umma::BM * kbytes;
+    strip[1] = umma::BN * kbytes;
+    return S3R_OK;
+}
+
+// dW problem (fp16-carried codes): A = X [T, K], B = Q [T, N] (both MN-major, contracted over T).
+static int add_dw_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDwProblem& q, double (&strip)[2]) {
+    const int64_t T = q.T, K = q.K, N = q.N, S = q.S > 0 ? q.S : q.T;
+    if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.X) || N % 8 != 0 || K % 8 != 0) return S3R_ERR_ALIGN;
+    CUtensorMap* m = maps.m[i];
+    int st = umma::make_map(&m[0], q.X, K, T, K, 64);
+    if (!st) st = umma::make_map(&m[1], q.Q, N, T, N, 64);
+    if (st) return st;
+    m[2] = m[0];
+    m[3] = m[1];
+    umma::Problem& P = A.prob[i];
+    P = umma::Problem{};
+    P.M = K; P.N = N; P.kind = umma::kDW;
+    umma::Segment& g = P.seg[0];
+    g.scale = q.tile_scale; g.sm = 0; g.sn = 1; g.sk = s3r_cdiv(N, kTile); g.nt_limit = s3r_cdiv(N, kTile);
+    g.K = T;
+    P.C = q.dW; P.ldc = N; P.dump = q.dump; P.s_col = q.s_w; P.ec_mode = q.ec_mode; P.S = S;
+    P.B = q.S > 0 ? T / q.S : 1; P.colmean = q.colmean; P.mu = q.mu; P.xsum = q.xsum; P.p = q.p;
+    const double kbytes = 2.0 * (double)T;   // per output row / column over the contraction
+    strip[0] = umma::BM * kbytes;
+    strip[1] = umma::BN * kbytes;
+    return S3R_OK;
+}
+
 int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream) {
     if (n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
     thread_local umma::Maps maps;   // host staging of the launch's parameters (copied at launch)
@@ -792,48 +874,9 @@ int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t
     double strip[umma::kMaxProb][2];
     bool dump = false;
     for (int i = 0; i < n; ++i) {
-        const UmmaDxProblem& q = probs[i];
-        const int64_t T = q.T, N = q.N, K = q.K, S = q.S > 0 ? q.S : q.T;
-        const bool two = q.Q3 != nullptr;
-        if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.W) || N % 8 != 0) return S3R_ERR_ALIGN;
-        if (two && (!s3r_aligned16(q.Q3) || !s3r_aligned16(q.W3))) return S3R_ERR_ALIGN;
-        if (q.ec_mode && S < T && S % kTile != 0) {
-            // the epilogue stages v for at most kNbX examples per 128-row tile
-            int64_t nb = 0;
-            for (int64_t m0 = 0; m0 < T; m0 += umma::BM) {
-                const int64_t hi = (m0 + umma::BM - 1 < T ? m0 + umma::BM - 1 : T - 1) / S;
-                if (hi - m0 / S + 1 > nb) nb = hi - m0 / S + 1;
-            }
-            if (nb > umma::kNbX) {
-                char buf[160];
-                snprintf(buf, sizeof(buf),
-                         "S = %lld lets a 128-token tile span %lld examples; the fp16-code path takes %d",
-                         (long long)S, (long long)nb, umma::kNbX);
-                s3r_record_error("int8_gemm_dx", buf);
-                return S3R_ERR_UNSUPPORTED;
-            }
-        }
-        CUtensorMap* m = maps.m[i];
-        int st = umma::make_map(&m[0], q.Q, N, T, N, umma::BM);
-        if (!st) st = umma::make_map(&m[1], q.W, N, K, N, umma::BN);
-        if (!st && two) st = umma::make_map(&m[2], q.Q3, N, T, N, umma::BM);
-        if (!st && two) st = umma::make_map(&m[3], q.W3, N, K, N, umma::BN);
+        const int st = add_dx_problem(maps, A, i, probs[i], strip[i]);
         if (st) return st;
-        if (!two) {
-            m[2] = m[0];
-            m[3] = m[1];
-        }
-        umma::Problem& P = A.prob[i];
-        P.M = T; P.N = K;
-        dx_segment(P.seg[0], q.tile_scale, N, q.eps, q.rowsum, q.v);
-        if (two) dx_segment(P.seg[1], q.tile_scale3, N, q.eps3, q.rowsum3, q.v3);
-        P.C = q.dX; P.ldc = K; P.dump = q.dump; P.s_row = q.s_x; P.ec_mode = q.ec_mode; P.S = S;
-        P.accumulate = q.accumulate;
-        // bytes per row strip of A (BM rows of Q over the contraction) and per column strip of B (BN rows of W)
-        const double kbytes = 2.0 * (double)N * (two ? 2 : 1);
-        strip[i][0] = umma::BM * kbytes;
-        strip[i][1] = umma::BN * kbytes;
-        dump = dump || q.dump;
+        dump = dump || probs[i].dump;
     }
     A.nprob = n;
     A.d_status = d_status;
@@ -841,7 +884,6 @@ int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t
     return umma::launch<umma::kDX, false>(maps, A, strip, stream);
 }
 
-// dW problems (fp16-carried codes): A = X [T, K], B = Q [T, N] (both MN-major, contracted over T).
 int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t stream) {
     if (n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
     thread_local umma::Maps maps;
@@ -850,31 +892,46 @@ int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t
     double strip[umma::kMaxProb][2];
     bool dump = false;
     for (int i = 0; i < n; ++i) {
-        const UmmaDwProblem& q = probs[i];
-        const int64_t T = q.T, K = q.K, N = q.N, S = q.S > 0 ? q.S : q.T;
-        if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.X) || N % 8 != 0 || K % 8 != 0) return S3R_ERR_ALIGN;
-        CUtensorMap* m = maps.m[i];
-        int st = umma::make_map(&m[0], q.X, K, T, K, 64);
-        if (!st) st = umma::make_map(&m[1], q.Q, N, T, N, 64);
+        const int st = add_dw_problem(maps, A, i, probs[i], strip[i]);
         if (st) return st;
-        m[2] = m[0];
-        m[3] = m[1];
-        umma::Problem& P = A.prob[i];
-        P.M = K; P.N = N;
-        umma::Segment& g = P.seg[0];
-        g.scale = q.tile_scale; g.sm = 0; g.sn = 1; g.sk = s3r_cdiv(N, kTile); g.nt_limit = s3r_cdiv(N, kTile);
-        g.K = T;
-        P.C = q.dW; P.ldc = N; P.dump = q.dump; P.s_col = q.s_w; P.ec_mode = q.ec_mode; P.S = S;
-        P.B = q.S > 0 ? T / q.S : 1; P.colmean = q.colmean; P.mu = q.mu; P.xsum = q.xsum; P.p = q.p;
-        const double kbytes = 2.0 * (double)T;   // per output row / column over the contraction
-        strip[i][0] = umma::BM * kbytes;
-        strip[i][1] = umma::BN * kbytes;
-        dump = dump || q.dump;
+        dump = dump || probs[i].dump;
     }
     A.nprob = n;
     A.d_status = d_status;
     if (dump) return umma::launch<umma::kDump, true>(maps, A, strip, stream);
     return umma::launch<umma::kDW, true>(maps, A, strip, stream);
+}
+
+// dX and dW problems in one launch (no dumps).  Problems run in the order of
+// their per-tile contraction length, longest first, so the short tiles at the
+// end of the round-robin fill in behind the long ones.
+int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, int* d_status,
+                     cudaStream_t stream) {
+    const int n = ndx + ndw;
+    if (ndx < 0 || ndw < 0 || n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
+    thread_local umma::Maps maps;
+    thread_local umma::Args A;
+    std::memset(&A, 0, sizeof(A));
+    double strip[umma::kMaxProb][2];
+    // order: per-tile 128-blocks descending (stable)
+    int order[umma::kMaxProb];
+    int64_t blocks[umma::kMaxProb];
+    for (int i = 0; i < n; ++i) {
+        order[i] = i;
+        blocks[i] = i < ndx ? s3r_cdiv(dx[i].N, 128) * (dx[i].Q3 ? 2 : 1) : s3r_cdiv(dw[i - ndx].T, 128);
+    }
+    std::stable_sort(order, order + n, [&](int a, int b) { return blocks[a] > blocks[b]; });
+    for (int k = 0; k < n; ++k) {
+        const int i = order[k];
+        if (i < ndx && dx[i].dump) return S3R_ERR_ARG;
+        if (i >= ndx && dw[i - ndx].dump) return S3R_ERR_ARG;
+        const int st = i < ndx ? add_dx_problem(maps, A, k, dx[i], strip[k])
+                               : add_dw_problem(maps, A, k, dw[i - ndx], strip[k]);
+        if (st) return st;
+    }
+    A.nprob = n;
+    A.d_status = d_status;
+    return umma::launch<umma::kMixed, false>(maps, A, strip, stream);
 }
 
 int umma_gemm_dx2(const void* Q, const float* tile_scale, const void* W, const float* eps, const int32_t* rowsum,
