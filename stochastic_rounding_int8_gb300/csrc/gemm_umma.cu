@@ -624,11 +624,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 }
                         }
                     } else {
+                        // acc = fma(scale, block, acc), two lanes per packed instruction
+                        const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                acc[16 * (c + u) + j] = fmaf(sc, __uint_as_float(r[u][j]), acc[16 * (c + u) + j]);
+                            for (int j = 0; j < 16; j += 2) {
+                                const float2 a2 = f2_fma(sc2, make_float2(__uint_as_float(r[u][j]),
+                                                                          __uint_as_float(r[u][j + 1])),
+                                                         make_float2(acc[16 * (c + u) + j], acc[16 * (c + u) + j + 1]));
+                                acc[16 * (c + u) + j] = a2.x;
+                                acc[16 * (c + u) + j + 1] = a2.y;
+                            }
                     }
                 }
                 tc_before();
