@@ -257,34 +257,43 @@ __device__ __forceinline__ void seed_tile(const Problem& P, float (&acc)[128], f
         for (int g = 0; g < 2; ++g) {
             const bool on = g == 0 || P.seg[1].K > 0;
             cv[g * 128 + ht] = (on && cin) ? (float)__ldg(P.seg[g].rowsum + cc) : 0.0f;
-            for (int i = 0; i < kNbX; ++i)
+            for (int i = 0; i < kNbX; ++i)   // staged negated: the seed below is one fma per pair
                 cv[256 + (g * kNbX + i) * 128 + ht] =
-                    (on && cin && b_lo + i <= b_hi) ? __ldg(P.seg[g].v + (b_lo + i) * P.N + cc) : 0.0f;
+                    (on && cin && b_lo + i <= b_hi) ? -__ldg(P.seg[g].v + (b_lo + i) * P.N + cc) : 0.0f;
         }
         half_bar(half);
         const float ep0 = in ? __ldg(P.seg[0].eps + row) : 0.0f;
         const float ep1 = (in && P.seg[1].K > 0) ? __ldg(P.seg[1].eps + row) : 0.0f;
         const int i_row = in ? (int)(row / P.S - b_lo) : 0;
+        // -(ep rowsum + v) = fma(-ep, rowsum, -v) exactly (v is staged negated)
         const float* rs0 = cv;
-        const float* v0 = cv + 256 + i_row * 128;
+        const float* nv0 = cv + 256 + i_row * 128;
+        const float2 nep0 = make_float2(-ep0, -ep0);
 #pragma unroll
         for (int j4 = 0; j4 < 128; j4 += 4) {
-            const float4 r = lds4(rs0 + j4), w = lds4(v0 + j4);
-            acc[j4 + 0] = -fmaf(ep0, r.x, w.x);
-            acc[j4 + 1] = -fmaf(ep0, r.y, w.y);
-            acc[j4 + 2] = -fmaf(ep0, r.z, w.z);
-            acc[j4 + 3] = -fmaf(ep0, r.w, w.w);
+            const float4 r = lds4(rs0 + j4), w = lds4(nv0 + j4);
+            const float2 a = f2_fma(nep0, make_float2(r.x, r.y), make_float2(w.x, w.y));
+            const float2 b = f2_fma(nep0, make_float2(r.z, r.w), make_float2(w.z, w.w));
+            acc[j4 + 0] = a.x;
+            acc[j4 + 1] = a.y;
+            acc[j4 + 2] = b.x;
+            acc[j4 + 3] = b.y;
         }
         if (P.seg[1].K > 0) {
             const float* rs1 = cv + 128;
-            const float* v1 = cv + 256 + (kNbX + i_row) * 128;
+            const float* nv1 = cv + 256 + (kNbX + i_row) * 128;
+            const float2 nep1 = make_float2(-ep1, -ep1);
 #pragma unroll
             for (int j4 = 0; j4 < 128; j4 += 4) {
-                const float4 r = lds4(rs1 + j4), w = lds4(v1 + j4);
-                acc[j4 + 0] = acc[j4 + 0] - fmaf(ep1, r.x, w.x);
-                acc[j4 + 1] = acc[j4 + 1] - fmaf(ep1, r.y, w.y);
-                acc[j4 + 2] = acc[j4 + 2] - fmaf(ep1, r.z, w.z);
-                acc[j4 + 3] = acc[j4 + 3] - fmaf(ep1, r.w, w.w);
+                const float4 r = lds4(rs1 + j4), w = lds4(nv1 + j4);
+                const float2 a = f2_add(make_float2(acc[j4], acc[j4 + 1]),
+                                        f2_fma(nep1, make_float2(r.x, r.y), make_float2(w.x, w.y)));
+                const float2 b = f2_add(make_float2(acc[j4 + 2], acc[j4 + 3]),
+                                        f2_fma(nep1, make_float2(r.z, r.w), make_float2(w.z, w.w)));
+                acc[j4 + 0] = a.x;
+                acc[j4 + 1] = a.y;
+                acc[j4 + 2] = b.x;
+                acc[j4 + 3] = b.y;
             }
         }
     } else {
@@ -304,13 +313,16 @@ __device__ __forceinline__ void seed_tile(const Problem& P, float (&acc)[128], f
             for (int64_t i = 0; i < nbi; ++i) {
                 const float xs = in ? (float)__ldg(P.xsum + (b0 + i) * P.M + row) : 0.0f;
                 const float* cm = cv + 128 + i * 128;
+                const float2 xs2 = make_float2(xs, xs);
 #pragma unroll
                 for (int j4 = 0; j4 < 128; j4 += 4) {
                     const float4 c4 = lds4(cm + j4);
-                    acc[j4 + 0] = fmaf(xs, c4.x, acc[j4 + 0]);
-                    acc[j4 + 1] = fmaf(xs, c4.y, acc[j4 + 1]);
-                    acc[j4 + 2] = fmaf(xs, c4.z, acc[j4 + 2]);
-                    acc[j4 + 3] = fmaf(xs, c4.w, acc[j4 + 3]);
+                    const float2 a = f2_fma(xs2, make_float2(c4.x, c4.y), make_float2(acc[j4], acc[j4 + 1]));
+                    const float2 b = f2_fma(xs2, make_float2(c4.z, c4.w), make_float2(acc[j4 + 2], acc[j4 + 3]));
+                    acc[j4 + 0] = a.x;
+                    acc[j4 + 1] = a.y;
+                    acc[j4 + 2] = b.x;
+                    acc[j4 + 3] = b.y;
                 }
             }
         }
@@ -329,17 +341,24 @@ __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128],
                                             int64_t row, int64_t c0, int lane) {
     if (EPI == kDX && P.s_row) {
         const float rinv = row < P.M ? __frcp_rn(__ldg(P.s_row + row)) : 1.0f;
+        const float2 r2 = make_float2(rinv, rinv);
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = acc[j] * rinv;
+        for (int j = 0; j < 128; j += 2) {
+            const float2 a = f2_mul(make_float2(acc[j], acc[j + 1]), r2);
+            acc[j] = a.x;
+            acc[j + 1] = a.y;
+        }
     }
     if (EPI == kDW && P.s_col) {
 #pragma unroll
         for (int j4 = 0; j4 < 128; j4 += 4) {
             const float4 r = lds4(cv + j4);
-            acc[j4 + 0] *= r.x;
-            acc[j4 + 1] *= r.y;
-            acc[j4 + 2] *= r.z;
-            acc[j4 + 3] *= r.w;
+            const float2 a = f2_mul(make_float2(acc[j4], acc[j4 + 1]), make_float2(r.x, r.y));
+            const float2 b = f2_mul(make_float2(acc[j4 + 2], acc[j4 + 3]), make_float2(r.z, r.w));
+            acc[j4 + 0] = a.x;
+            acc[j4 + 1] = a.y;
+            acc[j4 + 2] = b.x;
+            acc[j4 + 3] = b.y;
         }
     }
     const bool cvec = (P.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(P.C) & 15u) == 0);
