@@ -158,7 +158,11 @@ __device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& ds
     const float a0 = fminf(fmaxf(-x.x, -87.0f), 88.0f), a1 = fminf(fmaxf(-x.y, -87.0f), 88.0f);
     const float2 a = make_float2(a0, a1);
     const float2 t = f2_mul(a, make_float2(1.44269502162933349609375f, 1.44269502162933349609375f));
-    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    // n = rint(t) as kMagic + t rounded to nearest, minus kMagic (|t| <= 127); the sum's bits are
+    // kMagic's plus n, which gives 2^n without a conversion.  Per-lane adds: a packed add as the
+    // product's only use would be fused into an fma.
+    const float tm0 = __fadd_rn(t.x, kMagic), tm1 = __fadd_rn(t.y, kMagic);
+    const float2 n = f2_sub(make_float2(tm0, tm1), make_float2(kMagic, kMagic));
     float2 r = f2_fma(n, make_float2(-0.693145751953125f, -0.693145751953125f), a);
     r = f2_fma(n, make_float2(-1.42860682028622683e-06f, -1.42860682028622683e-06f), r);
     float2 poly = make_float2(1.98412701138295233e-04f, 1.98412701138295233e-04f);
@@ -169,7 +173,9 @@ __device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& ds
     poly = f2_fma(poly, r, make_float2(0.5f, 0.5f));
     poly = f2_fma(poly, r, make_float2(1.0f, 1.0f));
     poly = f2_fma(poly, r, make_float2(1.0f, 1.0f));
-    const float2 two_n = make_float2(__int_as_float(((int)n.x + 127) << 23), __int_as_float(((int)n.y + 127) << 23));
+    const int bm = (int)__float_as_uint(kMagic) - 127;
+    const float2 two_n = make_float2(__int_as_float(((int)__float_as_uint(tm0) - bm) << 23),
+                                     __int_as_float(((int)__float_as_uint(tm1) - bm) << 23));
     const float2 e = f2_mul(poly, two_n);
     const float2 den = f2_add(make_float2(1.0f, 1.0f), e);
     const float2 s = make_float2(__frcp_rn(den.x), __frcp_rn(den.y));

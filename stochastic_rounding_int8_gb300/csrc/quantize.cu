@@ -366,8 +366,9 @@ __global__ void __launch_bounds__(256, 2)
         const int b = i & 1;
         const int64_t t0 = (tile / C.ntc) * kTile, n0 = (tile % C.ntc) * kTile;
         const int64_t nc0 = n0 + 8 * c;
-        if (!q_wait(b ? bar1 : bar0, (uint32_t)(i >> 1) & 1u)) {
-            set_status(C.d_status, S3R_ERR_TIMEOUT);
+        // every thread waits; the CTA leaves together if any wait ran out
+        if (!__syncthreads_and(q_wait(b ? bar1 : bar0, (uint32_t)(i >> 1) & 1u))) {
+            if (threadIdx.x == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
             break;
         }
         float sw[8];
@@ -434,14 +435,40 @@ struct SwigluArgs {
     bool vec_load;
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, QuantCommon C, QuantOut O1, QuantOut O3) {
+// Block-wide max of two values (non-negative float bit patterns, NaN largest).
+template <int WARPS>
+__device__ __forceinline__ void block_max2_u32(uint32_t& a, uint32_t& b, uint32_t* smem /* [2][WARPS] */) {
+    a = __reduce_max_sync(0xFFFFFFFFu, a);
+    b = __reduce_max_sync(0xFFFFFFFFu, b);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        smem[warp] = a;
+        smem[WARPS + warp] = b;
+    }
+    __syncthreads();
+    uint32_t ma = 0, mb = 0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+        ma = max(ma, smem[w]);
+        mb = max(mb, smem[WARPS + w]);
+    }
+    __syncthreads();
+    a = ma;
+    b = mb;
+}
+
+// One 128x128 tile of the SwiGLU glue and its two quantizations; 512
+// threads, each 4 rows x 8 columns.  SMEM: the tile's dA (fp32) and h1, h3
+// (bf16) rows come from shared memory (pitch 128 elements) instead of global
+// memory; `freed` runs once every thread is done reading them.
+template <int MODE, bool SMEM, typename Freed>
+__device__ __forceinline__ void swiglu_tile(const SwigluArgs& A, const QuantCommon& C, const QuantOut& O1,
+                                            const QuantOut& O3, int64_t t0, int64_t n0, const float* sd,
+                                            const uint16_t* s1, const uint16_t* s3, uint32_t* red, float* col_smem,
+                                            Freed freed) {
     constexpr int RPT = 4;
     using Geo = TileGeom<RPT>;
-    __shared__ uint32_t red[Geo::kWarps];
-    __shared__ float col_smem[Geo::kWarps * 128];
     const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
-    const int64_t t0 = (int64_t)blockIdx.y * kTile, n0 = (int64_t)blockIdx.x * kTile;
     const int64_t nc0 = n0 + 8 * c;
 
     float g1[RPT][8], g3[RPT][8];
@@ -452,38 +479,55 @@ __global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, Quan
         sw1[i] = (A.s_w1 && ok) ? __ldg(A.s_w1 + nc0 + i) : 1.0f;
         sw3[i] = (A.s_w3 && ok) ? __ldg(A.s_w3 + nc0 + i) : 1.0f;
     }
-    uint32_t amax1 = 0u, amax3 = 0u;
+    float am1 = 0.0f, am3 = 0.0f;   // NaN-propagating absmax of each tile
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
-        const int64_t t = t0 + r0 + j * Geo::kRowStride;
+        const int rr = r0 + j * Geo::kRowStride;
+        const int64_t t = t0 + rr;
         float da[8], x1[8], x3[8];
+        if (SMEM) {
+            // the copy zero-fills outside the tensor
+            const float4 d0 = *reinterpret_cast<const float4*>(sd + rr * kTile + 8 * c);
+            const float4 d1 = *reinterpret_cast<const float4*>(sd + rr * kTile + 8 * c + 4);
+            const uint4 a1 = *reinterpret_cast<const uint4*>(s1 + rr * kTile + 8 * c);
+            const uint4 a3 = *reinterpret_cast<const uint4*>(s3 + rr * kTile + 8 * c);
+            da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
+            da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
+            const uint32_t w1[4] = {a1.x, a1.y, a1.z, a1.w}, w3[4] = {a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) da[i] = x1[i] = x3[i] = 0.0f;
-        if (t < C.T) {
-            const float* pd = A.dA + t * A.ldd + nc0;
-            const uint16_t* p1 = A.h1 + t * A.ldh + nc0;
-            const uint16_t* p3 = A.h3 + t * A.ldh + nc0;
-            if (A.vec_load && nc0 + 8 <= C.N) {
-                const float4 d0 = __ldg(reinterpret_cast<const float4*>(pd));
-                const float4 d1 = __ldg(reinterpret_cast<const float4*>(pd) + 1);
-                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(p1));
-                const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(p3));
-                da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
-                da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
-                const uint32_t w1[4] = {a1.x, a1.y, a1.z, a1.w}, w3[4] = {a3.x, a3.y, a3.z, a3.w};
+            for (int i = 0; i < 8; ++i) {
+                x1[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+                x3[i] = (i & 1) ? bf16_hi(w3[i >> 1]) : bf16_lo(w3[i >> 1]);
+            }
+        } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    x1[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
-                    x3[i] = (i & 1) ? bf16_hi(w3[i >> 1]) : bf16_lo(w3[i >> 1]);
-                }
-            } else {
+            for (int i = 0; i < 8; ++i) da[i] = x1[i] = x3[i] = 0.0f;
+            if (t < C.T) {
+                const float* pd = A.dA + t * A.ldd + nc0;
+                const uint16_t* p1 = A.h1 + t * A.ldh + nc0;
+                const uint16_t* p3 = A.h3 + t * A.ldh + nc0;
+                if (A.vec_load && nc0 + 8 <= C.N) {
+                    const float4 d0 = __ldg(reinterpret_cast<const float4*>(pd));
+                    const float4 d1 = __ldg(reinterpret_cast<const float4*>(pd) + 1);
+                    const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(p1));
+                    const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(p3));
+                    da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
+                    da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
+                    const uint32_t w1[4] = {a1.x, a1.y, a1.z, a1.w}, w3[4] = {a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (nc0 + i < C.N) {
-                        da[i] = pd[i];
-                        x1[i] = bf16_at(p1 + i);
-                        x3[i] = bf16_at(p3 + i);
+                    for (int i = 0; i < 8; ++i) {
+                        x1[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+                        x3[i] = (i & 1) ? bf16_hi(w3[i >> 1]) : bf16_lo(w3[i >> 1]);
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (nc0 + i < C.N) {
+                            da[i] = pd[i];
+                            x1[i] = bf16_at(p1 + i);
+                            x3[i] = bf16_at(p3 + i);
+                        }
+                }
             }
         }
         const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
@@ -507,14 +551,96 @@ __global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, Quan
             g1[j][i + 1] = v1.y;
             g3[j][i] = v3.x;
             g3[j][i + 1] = v3.y;
-            amax1 = max(amax1, max(__float_as_uint(v1.x) & 0x7FFFFFFFu, __float_as_uint(v1.y) & 0x7FFFFFFFu));
-            amax3 = max(amax3, max(__float_as_uint(v3.x) & 0x7FFFFFFFu, __float_as_uint(v3.y) & 0x7FFFFFFFu));
+            am1 = max3_abs_nan(am1, v1.x, v1.y);
+            am3 = max3_abs_nan(am3, v3.x, v3.y);
         }
     }
-    amax1 = block_max_u32<Geo::kWarps>(amax1, red);
-    amax3 = block_max_u32<Geo::kWarps>(amax3, red);
+    // non-negative floats and NaN order like their bit patterns; after the
+    // reduction's barriers no thread reads the staged tile any more
+    uint32_t amax1 = __float_as_uint(am1), amax3 = __float_as_uint(am3);
+    block_max2_u32<Geo::kWarps>(amax1, amax3, red);
+    freed();
     round_and_store<MODE, RPT>(g1, amax1, t0, n0, r0, c, C, O1, col_smem);
     round_and_store<MODE, RPT>(g3, amax3, t0, n0, r0, c, C, O3, col_smem);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, QuantCommon C, QuantOut O1, QuantOut O3) {
+    __shared__ uint32_t red[2 * 16];
+    __shared__ float col_smem[16 * 128];
+    swiglu_tile<MODE, false>(A, C, O1, O3, (int64_t)blockIdx.y * kTile, (int64_t)blockIdx.x * kTile, nullptr, nullptr,
+                             nullptr, red, col_smem, [] {});
+}
+
+// Persistent variant: one CTA per SM walks tiles tile = blockIdx.x + i * gridDim.x.
+// TMA copies the next tile's dA (fp32) and h1, h3 (bf16) into shared memory
+// (128 KB) while the current tile is quantized from registers, so the HBM
+// stream is not exposed between tiles.
+constexpr int kSwigluTmaBytes = kTile * kTile * (4 + 2 + 2);
+constexpr int kSwigluTmaSmem = kSwigluTmaBytes + 128 + 16;
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(512, 1)
+    swiglu_tma_kernel(const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmH1,
+                      const __grid_constant__ CUtensorMap tmH3, SwigluArgs A, QuantCommon C, QuantOut O1, QuantOut O3,
+                      int64_t ntiles) {
+    extern __shared__ uint8_t swsm_raw[];
+    uint8_t* swsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(swsm_raw) + 127) & ~(uintptr_t)127);
+    float* sd = reinterpret_cast<float*>(swsm);
+    uint16_t* s1 = reinterpret_cast<uint16_t*>(swsm + kTile * kTile * 4);
+    uint16_t* s3 = s1 + kTile * kTile;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(swsm + kSwigluTmaBytes);
+    __shared__ uint32_t red[2 * 16];
+    __shared__ float col_smem[16 * 128];
+    const uint32_t b0 = (uint32_t)__cvta_generic_to_shared(bar);
+    auto issue = [&](int64_t tile) {
+        const int32_t x = (int32_t)((tile % C.ntc) * kTile), y = (int32_t)((tile / C.ntc) * kTile);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b0), "r"(kSwigluTmaBytes)
+                     : "memory");
+        tma_2d((uint32_t)__cvta_generic_to_shared(sd), &tmD, x, y, b0);
+        tma_2d((uint32_t)__cvta_generic_to_shared(s1), &tmH1, x, y, b0);
+        tma_2d((uint32_t)__cvta_generic_to_shared(s3), &tmH3, x, y, b0);
+    };
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b0) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmD) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmH1) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmH3) : "memory");
+    }
+    __syncthreads();
+    int64_t issued = 0;   // copies issued (thread 0's count)
+    if (threadIdx.x == 0 && (int64_t)blockIdx.x < ntiles) {
+        issue(blockIdx.x);
+        issued = 1;
+    }
+    int64_t i = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+        // every thread waits; the CTA leaves together if any wait ran out
+        if (!__syncthreads_and(q_wait(b0, (uint32_t)(i & 1)))) {
+            if (threadIdx.x == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
+            break;
+        }
+        const int64_t t0 = (tile / C.ntc) * kTile, n0 = (tile % C.ntc) * kTile;
+        const int64_t next = tile + gridDim.x;
+        swiglu_tile<MODE, true>(A, C, O1, O3, t0, n0, sd, s1, s3, red, col_smem, [&] {
+            if (threadIdx.x == 0 && next < ntiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next);
+                ++issued;
+            }
+        });
+    }
+    // an early exit may leave a copy in flight: wait for it before leaving
+    if (threadIdx.x == 0 && issued > i) q_wait(b0, (uint32_t)(i & 1));
 }
 
 // ---------------------------------------------------------------------------
@@ -716,6 +842,56 @@ extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, c
     return S3R_OK;
 }
 
+template <int MODE>
+static int launch_swiglu_tma(const CUtensorMap* maps, const SwigluArgs& A, const QuantCommon& C, const QuantOut& O1,
+                             const QuantOut& O3, int64_t ntiles, cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(swiglu_tma_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSwigluTmaSmem);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return s3r_cuda_fail("swiglu_quantize: cudaFuncSetAttribute", e);
+        }
+        attr = true;
+    }
+    const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
+    swiglu_tma_kernel<MODE><<<(unsigned)grid, 512, kSwigluTmaSmem, stream>>>(maps[0], maps[1], maps[2], A, C, O1, O3,
+                                                                              ntiles);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+// The TMA path needs 16-byte aligned rows (and codes); returns 1 when it does not apply.
+static int try_swiglu_tma(int round_mode, const SwigluArgs& A, const QuantCommon& C, const QuantOut& O1,
+                          const QuantOut& O3, cudaStream_t stream) {
+    if (!A.vec_load || !C.vec_store) return 1;
+    auto fn = q_encode_fn();
+    if (!fn) return 1;
+    CUtensorMap maps[3];
+    cuuint64_t dims[2] = {(cuuint64_t)C.N, (cuuint64_t)C.T};
+    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+    cuuint32_t estr[2] = {1u, 1u};
+    cuuint64_t sd[1] = {(cuuint64_t)A.ldd * 4}, sh[1] = {(cuuint64_t)A.ldh * 2};
+    if (fn(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A.dA), dims, sd, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        fn(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(A.h1), dims, sh, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        fn(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(A.h3), dims, sh, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return 1;
+    const int64_t ntiles = s3r_cdiv(C.T, kTile) * C.ntc;
+    switch (round_mode) {
+        case S3R_ROUND_RTNE: return launch_swiglu_tma<kRTNE>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_S3R: return launch_swiglu_tma<kS3R>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_INDEP: return launch_swiglu_tma<kINDEP>(maps, A, C, O1, O3, ntiles, stream);
+        default: return S3R_ERR_ARG;
+    }
+}
+
 extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh, int64_t T,
                                int64_t F, const float* s_x, const float* s_w1, const float* s_w3, int round_mode,
                                int code_format, uint64_t seed, uint32_t tid1, uint32_t tid3, void* Q1, float* scale1,
@@ -731,6 +907,8 @@ extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, con
     QuantCommon C{T, F, s3r_cdiv(F, kTile), (uint32_t)seed, d_status,
                   s3r_aligned16(Q1) && s3r_aligned16(Q3) && (F % 8) == 0};
     QuantOut O1{Q1, code_format, scale1, tok1, col1, tid1}, O3{Q3, code_format, scale3, tok3, col3, tid3};
+    const int tma = try_swiglu_tma(round_mode, A, C, O1, O3, stream);
+    if (tma <= 0) return tma;   // launched (0) or failed (< 0)
     dim3 grid((unsigned)s3r_cdiv(F, kTile), (unsigned)s3r_cdiv(T, kTile));
     switch (round_mode) {
         case S3R_ROUND_RTNE: swiglu_quantize_kernel<kRTNE><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
