@@ -259,7 +259,7 @@ int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, 
                         const float* col3, const void* W3_8, float* eps3, float* mu3, float* colmean3,
                         int32_t* rowsum3, float* v3, int32_t* xsum3, float* p3, int64_t T, int64_t N, int64_t S,
                         int64_t K, const void* X8, int code_format, int ec_mode, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream);
+                        size_t workspace_bytes, int* d_status, cudaStream_t stream);
 #define S3R_CHECK_LAUNCH()                                               \
     do {                                                                 \
         s3r_count_launch();                                              \

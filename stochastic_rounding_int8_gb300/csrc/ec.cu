@@ -13,6 +13,7 @@
 // and W3 of the SwiGLU block) are handled by the same launches: their weight
 // rows share one grid and the column sums of X are read once for both.
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdio>
@@ -20,6 +21,12 @@
 #include "common.cuh"
 
 namespace s3r {
+
+__device__ __forceinline__ uint64_t ec_gtime() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ int code_value(int8_t c) { return c; }
 __device__ __forceinline__ int code_value(__half c) { return __half2int_rn(c); }
@@ -475,6 +482,258 @@ __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
     if (threadIdx.x == 0) A.counter[blockIdx.x] = 0;
 }
 
+// fp16 codes: the same sums streamed through shared memory.  One CTA per SM
+// walks the (column block, row chunk) items; TMA copies 64-row x 256-column
+// boxes (32 KiB) into a 4-stage ring while the warps accumulate the previous
+// ones (warp w takes rows w, w + 8, ... of a box, lane l columns 8l .. 8l+7;
+// the integer sums are exact in fp32: at most 256 * 127 per chunk).  Partials,
+// counters and the final fixed-order reduction as in ec_xsum_kernel.
+constexpr int kXsStages = 4, kXsBoxRows = 64;
+constexpr int kXsBoxBytes = kXsBoxRows * 256 * 2;
+constexpr int kXsSmem = kXsStages * kXsBoxBytes + 128 + 64;
+
+__device__ __forceinline__ bool xs_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ec_gtime();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (ec_gtime() - t0 > 2000000000ull) return false;
+    }
+}
+
+template <int NJ, int ROWS>
+__global__ void __launch_bounds__(256, 1)
+    ec_xsum_tma_kernel(const __grid_constant__ CUtensorMap tmX, EcXsumArgs A, int64_t ncb, int64_t nch,
+                       int* d_status) {
+    constexpr int P = 33;
+    constexpr int NBOX = ROWS / kXsBoxRows;
+    extern __shared__ uint8_t xsm_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xsm_raw) + 127) & ~(uintptr_t)127);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kXsStages * kXsBoxBytes);
+    __shared__ float red_p[NJ][8][8 * P];
+    __shared__ float red_x[8][8 * P];
+    __shared__ int last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t T = A.T, K = A.K;
+    const int64_t nitems = ncb * nch;
+    const int64_t my_items = (int64_t)blockIdx.x < nitems ? (nitems - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t total = my_items * NBOX;   // boxes this CTA streams
+    auto box_item = [&](int64_t kk) { return (int64_t)blockIdx.x + (kk / NBOX) * gridDim.x; };
+    auto issue = [&](int64_t kk) {
+        const int64_t item = box_item(kk);
+        const int s = (int)(kk % kXsStages);
+        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(full + s);
+        const int32_t x = (int32_t)((item % ncb) * 256), y = (int32_t)((item / ncb) * ROWS + (kk % NBOX) * kXsBoxRows);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kXsBoxBytes) : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"((uint32_t)__cvta_generic_to_shared(ring + s * kXsBoxBytes)), "l"((uint64_t)&tmX), "r"(x), "r"(y),
+            "r"(bar)
+            : "memory");
+    };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kXsStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(full + i))
+                         : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
+    }
+    __syncthreads();
+    int64_t issued = 0;   // thread 0's count
+    if (threadIdx.x == 0)
+        for (; issued < kXsStages && issued < total; ++issued) issue(issued);
+    int64_t kk = 0;
+    bool ok = true;
+    for (int64_t k = 0; k < my_items && ok; ++k) {
+        const int64_t item = (int64_t)blockIdx.x + k * gridDim.x;
+        const int64_t cb = item % ncb, c = item / ncb;
+        float2 sx[4], sp[NJ][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sx[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) sp[jj][i] = make_float2(0.f, 0.f);
+        }
+        for (int box = 0; box < NBOX; ++box, ++kk) {
+            const int s = (int)(kk % kXsStages);
+            // every thread waits; the CTA leaves together if any wait ran out
+            if (!__syncthreads_and(xs_wait((uint32_t)__cvta_generic_to_shared(full + s),
+                                           (uint32_t)((kk / kXsStages) & 1)))) {
+                if (threadIdx.x == 0 && d_status) *(volatile int*)d_status = S3R_ERR_TIMEOUT;
+                ok = false;
+                break;
+            }
+            const uint8_t* st = ring + s * kXsBoxBytes;
+            const int64_t tb = c * ROWS + box * kXsBoxRows;
+#pragma unroll
+            for (int i = 0; i < kXsBoxRows / 8; ++i) {
+                const int r = warp + 8 * i;
+                const int64_t t = tb + r;
+                const uint4 w = *reinterpret_cast<const uint4*>(st + (r * 256 + 8 * lane) * 2);
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                float e[NJ];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) e[jj] = t < T ? __ldg(A.eps[jj] + t) : 0.0f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
+                    sx[q] = f2_add(sx[q], x);
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) sp[jj][q] = f2_fma(x, make_float2(e[jj], e[jj]), sp[jj][q]);
+                }
+            }
+            __syncthreads();   // every thread is done with this stage
+            if (threadIdx.x == 0 && issued < total) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(issued);
+                ++issued;
+            }
+        }
+        if (!ok) break;
+        // the chunk's column sums: warps meet in shared memory in warp order
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            red_x[warp][(2 * q) * P + lane] = sx[q].x;
+            red_x[warp][(2 * q + 1) * P + lane] = sx[q].y;
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
+                red_p[jj][warp][(2 * q) * P + lane] = sp[jj][q].x;
+                red_p[jj][warp][(2 * q + 1) * P + lane] = sp[jj][q].y;
+            }
+        }
+        __syncthreads();
+        const int64_t kcol = cb * 256 + threadIdx.x;
+        const int slot = (threadIdx.x & 7) * P + (threadIdx.x >> 3);
+        if (kcol < K) {
+            float xb = 0.0f;
+            float a[NJ];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) a[jj] = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                xb += red_x[w][slot];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][slot];
+            }
+            A.xs[c * K + kcol] = (int32_t)xb;
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) A.ps[(jj * nch + c) * K + kcol] = a[jj];
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(A.counter + cb, 1) == (int)nch - 1;
+        __syncthreads();
+        if (last && kcol < K) {
+            __threadfence();
+            // last chunk of this column block: thread = column, chunks in order per example
+            const int64_t B = A.B, cpe = B == 1 ? nch : A.S / ROWS;
+            float pk[NJ];
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
+            for (int64_t b = 0; b < B; ++b) {
+                int xbi = 0;
+                float pb[NJ];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
+#pragma unroll 8
+                for (int64_t cc = b * cpe; cc < (b + 1) * cpe; ++cc) {
+                    xbi += __ldcg(A.xs + cc * K + kcol);
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * nch + cc) * K + kcol);
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    A.xsum[jj][b * K + kcol] = xbi;
+                    pk[jj] += pb[jj];
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) A.p[jj][kcol] = pk[jj];
+        }
+        if (last && threadIdx.x == 0) A.counter[cb] = 0;
+        __syncthreads();   // red_* and `last` are reused by the next item
+    }
+    // an early exit may leave copies in flight: wait for them before leaving
+    if (threadIdx.x == 0)
+        for (int64_t q = kk; q < issued; ++q)
+            xs_wait((uint32_t)__cvta_generic_to_shared(full + (q % kXsStages)), (uint32_t)((q / kXsStages) & 1));
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 ec_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess && p)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+
+static int ec_sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 148;
+        }
+    }
+    return n;
+}
+
+template <int NJ, int ROWS>
+static int launch_xsum_tma_t(const CUtensorMap& map, const EcXsumArgs& X, int64_t ncb, int64_t nch, int* d_status,
+                             cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e =
+            cudaFuncSetAttribute(ec_xsum_tma_kernel<NJ, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXsSmem);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return s3r_cuda_fail("ec column sums: cudaFuncSetAttribute", e);
+        }
+        attr = true;
+    }
+    const int64_t items = ncb * nch;
+    const int64_t grid = std::min<int64_t>(items, ec_sm_count());
+    ec_xsum_tma_kernel<NJ, ROWS><<<(unsigned)grid, 256, kXsSmem, stream>>>(map, X, ncb, nch, d_status);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+// fp16 codes X8 [T, K] with 16-byte aligned rows: the TMA column-sum kernel.
+// Returns 1 when it does not apply (the caller falls back to ec_xsum_kernel).
+static int launch_xsum_tma(const EcXsumArgs& X, int nj, bool wide, int64_t ncb, int64_t nch, int* d_status,
+                           cudaStream_t stream) {
+    auto fn = ec_encode_fn();
+    if (!fn || X.T >= (int64_t(1) << 31) || X.K >= (int64_t(1) << 31)) return 1;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)X.K, (cuuint64_t)X.T};
+    const cuuint64_t strides[1] = {(cuuint64_t)X.K * 2};
+    const cuuint32_t box[2] = {256, (cuuint32_t)kXsBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    // rows and columns past the end read as zero
+    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X.X8), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return 1;
+    if (wide) return nj == 2 ? launch_xsum_tma_t<2, 256>(map, X, ncb, nch, d_status, stream)
+                             : launch_xsum_tma_t<1, 256>(map, X, ncb, nch, d_status, stream);
+    return nj == 2 ? launch_xsum_tma_t<2, 128>(map, X, ncb, nch, d_status, stream)
+                   : launch_xsum_tma_t<1, 128>(map, X, ncb, nch, d_status, stream);
+}
+
 // Workspace of the column-sum pass for `njobs` linears sharing X8 [T, K].
 static size_t xsum_workspace_bytes(int64_t T, int64_t K, int njobs) {
     const size_t nch = (size_t)s3r_cdiv(T, kXsumChunk);   // the generic path's chunks, the finer of the two
@@ -484,7 +743,8 @@ static size_t xsum_workspace_bytes(int64_t T, int64_t K, int njobs) {
 
 template <typename CodeT>
 static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
-                          int ec_mode, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                          int ec_mode, void* workspace, size_t workspace_bytes, int* d_status,
+                          cudaStream_t stream) {
     const int64_t B = T / S, ntc = s3r_cdiv(N, kTile), ntr = s3r_cdiv(T, kTile);
     const bool two = ec_mode == S3R_EC_TWO_WAY;
     bool vec_w = N % 8 == 0;
@@ -587,7 +847,12 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
         X.xs = xs; X.ps = ps; X.counter = counter;
         // 256-row chunks where the examples allow it (chunks never straddle two)
         const bool wide = B == 1 || S % 256 == 0;
-        dim3 grid((unsigned)ncb, (unsigned)s3r_cdiv(T, wide ? 256 : 128));
+        const int64_t nchw = s3r_cdiv(T, wide ? 256 : 128);
+        if (sizeof(CodeT) == 2) {
+            int st = launch_xsum_tma(X, nj, wide, ncb, nchw, d_status, stream);
+            if (st <= 0) return st;   // launched (0) or failed (< 0); 1: fall through
+        }
+        dim3 grid((unsigned)ncb, (unsigned)nchw);
         if (wide) {
             if (nj == 2) ec_xsum_kernel<CodeT, 2, 256><<<grid, 256, 0, stream>>>(X);
             else ec_xsum_kernel<CodeT, 1, 256><<<grid, 256, 0, stream>>>(X);
@@ -614,7 +879,7 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
 // two-linear path of the FFN block.
 static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
                            int code_format, int ec_mode, void* workspace, size_t workspace_bytes,
-                           cudaStream_t stream) {
+                           int* d_status, cudaStream_t stream) {
     if (T < 0 || N < 0 || K < 0 || S <= 0) return S3R_ERR_ARG;
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
@@ -629,8 +894,9 @@ static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int6
     }
     if (ec_mode == S3R_EC_TWO_WAY && K > 0 && !X8) return S3R_ERR_ARG;
     if (code_format == S3R_CODES_F16)
-        return launch_factors<__half>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, stream);
-    return launch_factors<int8_t>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, stream);
+        return launch_factors<__half>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, d_status,
+                                      stream);
+    return launch_factors<int8_t>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, d_status, stream);
 }
 
 }  // namespace s3r
@@ -646,9 +912,9 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
                               const void* W8, int64_t K, const void* X8, int code_format, int ec_mode, float* eps,
                               float* mu, float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p,
                               void* workspace, size_t workspace_bytes, int* d_status, cudaStream_t stream) {
-    (void)d_status;
     const EcJob job{tok_err_part, col_err_part, W8, eps, mu, colmean, rowsum, v, xsum, p};
-    return ec_correct_jobs(&job, 1, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, stream);
+    return ec_correct_jobs(&job, 1, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, d_status,
+                           stream);
 }
 
 // The two linears of the SwiGLU block that read the same input X (W1 and W3):
@@ -663,10 +929,11 @@ int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, 
                         const float* col3, const void* W3_8, float* eps3, float* mu3, float* colmean3,
                         int32_t* rowsum3, float* v3, int32_t* xsum3, float* p3, int64_t T, int64_t N, int64_t S,
                         int64_t K, const void* X8, int code_format, int ec_mode, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream) {
+                        size_t workspace_bytes, int* d_status, cudaStream_t stream) {
     const EcJob jobs[2] = {{tok1, col1, W1_8, eps1, mu1, colmean1, rowsum1, v1, xsum1, p1},
                            {tok3, col3, W3_8, eps3, mu3, colmean3, rowsum3, v3, xsum3, p3}};
-    return ec_correct_jobs(jobs, 2, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, stream);
+    return ec_correct_jobs(jobs, 2, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, d_status,
+                           stream);
 }
 
 // ---------------------------------------------------------------------------

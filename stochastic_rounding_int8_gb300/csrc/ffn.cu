@@ -230,7 +230,8 @@ int step_ec_w13(Block& b, cudaStream_t stream) {
     LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
     return s3r_ec_correct_pair(L1.tok, L1.col, a.W1_8, L1.eps, L1.mu, L1.colmean, L1.rowsum, L1.v, L1.xsum, L1.p,
                                L3.tok, L3.col, a.W3_8, L3.eps, L3.mu, L3.colmean, L3.rowsum, L3.v, L3.xsum, L3.p,
-                               a.T, a.F, a.S, a.d, a.X8, b.fmt, b.ec, b.Lo.ec_ws, b.Lo.ec_ws_bytes, stream);
+                               a.T, a.F, a.S, a.d, a.X8, b.fmt, b.ec, b.Lo.ec_ws, b.Lo.ec_ws_bytes,
+                               a.d_status, stream);
 }
 
 // 7. dX = dX1 + dX3
