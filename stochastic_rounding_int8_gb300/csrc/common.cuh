@@ -132,6 +132,24 @@ __device__ __forceinline__ float2 f2_add_rm(float2 a, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
+// a + b per lane, rounded toward plus infinity
+__device__ __forceinline__ float2 f2_add_rp(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n add.rp.f32x2 z, x, y;\n"
+        " mov.b64 {%0, %1}, z;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// a - b per lane, rounded toward plus infinity
+__device__ __forceinline__ float2 f2_sub_rp(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n sub.rp.f32x2 z, x, y;\n"
+        " mov.b64 {%0, %1}, z;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 // 1.0f if a < b else 0.0f
 __device__ __forceinline__ float lt_one(float a, float b) {
     float d;

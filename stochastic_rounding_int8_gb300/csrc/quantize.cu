@@ -331,93 +331,309 @@ __device__ __forceinline__ void q_issue_tile(uint32_t dst, const CUtensorMap* ma
         : "memory");
 }
 
-template <int MODE, int FMT>
+// Persistent quantizer.  CTA b owns the contiguous tile range
+// [b ntiles / grid, (b + 1) ntiles / grid) in row-major tile order, so its
+// consecutive tiles mostly share a row block and reuse that block's
+// thresholds.  A TMA engine keeps up to kQStages 128 x 128 bf16 tiles in
+// flight in a shared-memory ring.  The side data of a tile -- the row scales
+// with the row thresholds, and the column scales -- is fetched one tile
+// ahead (threads 0..127 own a row, 128..255 a column) into a second slot.
+constexpr int kQStages = 3;
+constexpr int kQTileBytes = kTile * kTile * 2;
+constexpr int kQuantTmaSmem = kQStages * kQTileBytes + 8 * kQStages;
+
+// side data of tile `tile` for this thread: (row scale, threshold) or (column scale, 0)
+template <int MODE>
+__device__ __forceinline__ float2 q_side(const TileQuantArgs& A, const QuantCommon& C, uint32_t tensor_id,
+                                         int64_t tile, float& u_mine, int64_t& u_rb) {
+    const int64_t rb = tile / C.ntc;
+    if (threadIdx.x < kTile) {
+        const int64_t t = rb * kTile + threadIdx.x;
+        const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+        if (MODE == kS3R && rb != u_rb) {
+            u_mine = token_threshold((uint64_t)t, C.seed_lo, tensor_id);
+            u_rb = rb;
+        }
+        return make_float2(sx, u_mine);
+    }
+    const int64_t n = (tile % C.ntc) * kTile + (threadIdx.x - kTile);
+    return make_float2((A.s_w && n < C.N) ? __ldg(A.s_w + n) : 1.0f, 0.0f);
+}
+
+// FOLD: at least one of s_x, s_w is given (a missing one multiplies by 1).
+template <int MODE, int FMT, bool FOLD>
 __global__ void __launch_bounds__(256, 2)
     quantize_tma_kernel(const __grid_constant__ CUtensorMap tmG, TileQuantArgs A, QuantCommon C, QuantOut O,
                         int64_t ntiles) {
-    constexpr int RPT = 8;
-    using Geo = TileGeom<RPT>;
+    constexpr int RPT = 8, RS = 16;   // rows r0 + 16 j of the tile, 8 columns from 8 c
+    constexpr bool ERR = MODE == kS3R;   // error partials
     extern __shared__ __align__(128) uint8_t qsmem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + 2 * kTile * kTile * 2);
-    __shared__ uint32_t red[Geo::kWarps];
-    __shared__ float col_smem[Geo::kWarps * 128];
-    const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
-    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars), bar1 = bar0 + 8;
-    const int64_t first = blockIdx.x, stride = gridDim.x;
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar1) : "memory");
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + kQStages * kQTileBytes);
+    __shared__ __align__(16) float2 xu_s[2][kTile];   // (s_x, u) per tile row
+    __shared__ __align__(16) float sw_s[2][kTile];    // s_w per tile column
+    __shared__ uint32_t red[8];
+    __shared__ __align__(16) float col_smem[8 * kTile];
+    const int tid = threadIdx.x, c = tid & 15, r0 = tid >> 4, lane = tid & 31, warp = tid >> 5;
+    const int64_t beg = (int64_t)blockIdx.x * ntiles / gridDim.x;
+    const int64_t count = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x - beg;
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars);
+    const int64_t row_step = (int64_t)RS * C.N;   // elements between my consecutive rows
+    auto issue = [&](int64_t k) {
+        const int64_t tile = beg + k;
+        const int s = (int)(k % kQStages);
+        q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + s * kQTileBytes), &tmG,
+                     (int32_t)((tile % C.ntc) * kTile), (int32_t)((tile / C.ntc) * kTile), bar0 + 8 * s);
+    };
+    float u_mine = 0.0f;
+    int64_t u_rb = -1;
+    if (count > 0) {
+        const float2 sd = q_side<MODE>(A, C, O.tensor_id, beg, u_mine, u_rb);
+        if (tid < kTile) xu_s[0][tid] = sd;
+        else sw_s[0][tid - kTile] = sd.x;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kQStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * i) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmG) : "memory");
     }
     __syncthreads();
-    int issued = 0;
-    if (threadIdx.x == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmG) : "memory");
-        for (int k = 0; k < 2 && first + k * stride < ntiles; ++k) {
-            const int64_t tile = first + k * stride;
-            q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + k * (kTile * kTile * 2)), &tmG,
-                         (int32_t)((tile % C.ntc) * kTile),
-                         (int32_t)((tile / C.ntc) * kTile), k ? bar1 : bar0);
-            ++issued;
-        }
-    }
-    int i = 0;
-    for (int64_t tile = first; tile < ntiles; tile += stride, ++i) {
-        const int b = i & 1;
-        const int64_t t0 = (tile / C.ntc) * kTile, n0 = (tile % C.ntc) * kTile;
-        const int64_t nc0 = n0 + 8 * c;
+    int64_t issued = 0;   // thread 0's count
+    if (tid == 0)
+        for (; issued < kQStages && issued < count; ++issued) issue(issued);
+    const float2 M2 = make_float2(kMagic, kMagic);
+    int64_t k = 0;
+    for (; k < count; ++k) {
+        const int64_t tile = beg + k;
+        const int s = (int)(k % kQStages), sl = (int)(k & 1);
+        const int64_t rb = tile / C.ntc, cb = tile % C.ntc;
+        const int64_t t0 = rb * kTile, n0 = cb * kTile;
+        const int nc0 = (int)n0 + 8 * c;
+        const int64_t rl = C.T - t0 - r0;
+        const int rows_left = rl < kTile ? (int)rl : kTile;   // my row j is valid iff RS j < rows_left
+        // the next tile's side data: loads (and thresholds) in flight during this tile
+        float2 side = make_float2(0.0f, 0.0f);
+        if (k + 1 < count) side = q_side<MODE>(A, C, O.tensor_id, tile + 1, u_mine, u_rb);
         // every thread waits; the CTA leaves together if any wait ran out
-        if (!__syncthreads_and(q_wait(b ? bar1 : bar0, (uint32_t)(i >> 1) & 1u))) {
-            if (threadIdx.x == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
+        if (!__syncthreads_and(q_wait(bar0 + 8 * s, (uint32_t)((k / kQStages) & 1)))) {
+            if (tid == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
             break;
         }
-        float sw[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sw[k] = (A.s_w && nc0 + k < C.N) ? __ldg(A.s_w + nc0 + k) : 1.0f;
+        // pass 1: fold g = (s_x * G) * s_w and absmax
         float g[RPT][8];
-        float amax = 0.0f;   // NaN-propagating absmax
-        const uint16_t* tb = reinterpret_cast<const uint16_t*>(qsmem + b * (kTile * kTile * 2));
+        float amax = 0.0f;   // NaN-propagating
+        {
+            float sw[8];
+            if (FOLD) {
+                const float4 w0 = *reinterpret_cast<const float4*>(&sw_s[sl][8 * c]);
+                const float4 w1 = *reinterpret_cast<const float4*>(&sw_s[sl][8 * c + 4]);
+                sw[0] = w0.x; sw[1] = w0.y; sw[2] = w0.z; sw[3] = w0.w;
+                sw[4] = w1.x; sw[5] = w1.y; sw[6] = w1.z; sw[7] = w1.w;
+            }
+            const uint16_t* tb = reinterpret_cast<const uint16_t*>(qsmem + s * kQTileBytes);
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int rr = r0 + j * Geo::kRowStride;
-            const int64_t t = t0 + rr;
-            const uint4 raw = *reinterpret_cast<const uint4*>(tb + rr * kTile + 8 * c);
-            // negated fold: (-s_x) * G * s_w == -((s_x * G) * s_w) exactly; a missing scale is 1
-            const float nsx = (A.s_x && t < C.T) ? -__ldg(A.s_x + t) : -1.0f;
-            const float2 nsx2 = make_float2(nsx, nsx);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            for (int j = 0; j < RPT; ++j) {
+                const int rr = r0 + RS * j;
+                const uint4 raw = *reinterpret_cast<const uint4*>(tb + rr * kTile + 8 * c);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                float sx = 1.0f;
+                if (FOLD) sx = xu_s[sl][rr].x;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float2 v = f2_mul(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), nsx2);
-                v = f2_mul(v, make_float2(sw[2 * k], sw[2 * k + 1]));
-                g[j][2 * k] = v.x;
-                g[j][2 * k + 1] = v.y;
-                amax = max3_abs_nan(amax, v.x, v.y);
+                for (int q = 0; q < 4; ++q) {
+                    float2 v = make_float2(bf16_lo(w[q]), bf16_hi(w[q]));
+                    if (FOLD) {
+                        v = f2_mul(v, make_float2(sx, sx));
+                        v = f2_mul(v, make_float2(sw[2 * q], sw[2 * q + 1]));
+                    }
+                    g[j][2 * q] = v.x;
+                    g[j][2 * q + 1] = v.y;
+                    amax = max3_abs_nan(amax, v.x, v.y);
+                }
             }
         }
-        // block absmax (non-negative floats and NaN order like their bit patterns);
-        // the first barrier also means every thread is done with this buffer
-        uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax_bits;
+        // block absmax (non-negative floats and NaN order like their bit patterns); after the
+        // barrier every thread is done with this stage, which is refilled at once
+        {
+            const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
+            if (lane == 0) red[warp] = wm;
+        }
         __syncthreads();
-        if (threadIdx.x == 0 && tile + 2 * stride < ntiles) {
-            const int64_t nt = tile + 2 * stride;
+        if (tid == 0 && issued < count) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + b * (kTile * kTile * 2)), &tmG,
-                         (int32_t)((nt % C.ntc) * kTile),
-                         (int32_t)((nt / C.ntc) * kTile), b ? bar1 : bar0);
+            issue(issued);
             ++issued;
         }
-        uint32_t m = 0;
+        const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, red[lane & 7]);
+        const bool nonfinite = amax_bits >= 0x7F800000u;   // uniform across the CTA
+        const float amx = __uint_as_float(amax_bits);
+        const float d = nonfinite ? __uint_as_float(0x7FC00000u) : amx / 127.0f;
+        // inv = 127/amax rounded toward zero keeps |y| <= 127: no code leaves [-127, 127]
+        const float inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amx);
+        if (tid == 0) {
+            O.scale[rb * C.ntc + cb] = d;
+            if (nonfinite) set_status(C.d_status, S3R_ERR_NONFINITE);
+        }
+        // pass 2: codes, stores and error sums.  The sums collect -e = g - delta*q (one
+        // rounding each, the exact negation of delta*q - g) and are negated when stored.
+        const float2 inv2 = make_float2(inv, inv), nd2 = make_float2(-d, -d);
+        float2 colsum[4];
 #pragma unroll
-        for (int w = 0; w < Geo::kWarps; ++w) m = max(m, red[w]);
+        for (int q = 0; q < 4; ++q) colsum[q] = make_float2(0.0f, 0.0f);
+        float rsum[RPT];
+        int8_t* q8 = static_cast<int8_t*>(O.Q) + (t0 + r0) * C.N + nc0;
+        __half* q16 = static_cast<__half*>(O.Q) + (t0 + r0) * C.N + nc0;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int rr = r0 + RS * j;
+            float u8[8];
+            if (MODE == kINDEP) {
+                const int64_t t = t0 + rr;
+                if ((C.N & 3) == 0) {
+                    const uint64_t ctr = ((uint64_t)t * (uint64_t)C.N + (uint64_t)nc0) >> 2;
+                    const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, C.seed_lo,
+                                                    O.tensor_id);
+                    const Philox4 b = philox4x32_10((uint32_t)(ctr + 1), (uint32_t)((ctr + 1) >> 32), 0u, 0u,
+                                                    C.seed_lo, O.tensor_id);
+                    u8[0] = unit24(a.x); u8[1] = unit24(a.y); u8[2] = unit24(a.z); u8[3] = unit24(a.w);
+                    u8[4] = unit24(b.x); u8[5] = unit24(b.y); u8[6] = unit24(b.z); u8[7] = unit24(b.w);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint64_t e = (uint64_t)t * (uint64_t)C.N + (uint64_t)(nc0 + i);
+                        const uint64_t ctr = e >> 2;
+                        const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, C.seed_lo,
+                                                        O.tensor_id);
+                        const uint32_t w = (e & 3) == 0 ? a.x : (e & 3) == 1 ? a.y : (e & 3) == 2 ? a.z : a.w;
+                        u8[i] = unit24(w);
+                    }
+                }
+            }
+            const float ut = MODE == kS3R ? xu_s[sl][rr].y : 0.0f;
+            // m = kMagic + q (exact), and the int8 code is the low byte of m's bits.  SR:
+            // q = floor(y) + [u < frac(y)] = ceil(y - u) (u in [0, 1)); y - u rounded up
+            // never passes an integer, so its ceiling is exact, and adding kMagic rounded
+            // up takes it.  RTNE: kMagic + y rounded to nearest.
+            float qv[8], qm[8];
+            float2 rs = make_float2(0.0f, 0.0f);
+            if (!nonfinite) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 g2 = make_float2(g[j][2 * q], g[j][2 * q + 1]);
+                    const float2 y = f2_mul(g2, inv2);   // |y| <= 127
+                    float2 m;
+                    if (MODE == kRTNE) {
+                        // per lane: a packed add that is the product's only use would be fused into an fma
+                        m = make_float2(__fadd_rn(y.x, kMagic), __fadd_rn(y.y, kMagic));
+                    } else {
+                        const float2 uu = MODE == kS3R ? make_float2(ut, ut) : make_float2(u8[2 * q], u8[2 * q + 1]);
+                        m = f2_add_rp(f2_sub_rp(y, uu), M2);
+                    }
+                    const float2 qq = f2_sub(m, M2);   // the code, exact
+                    qm[2 * q] = m.x;
+                    qm[2 * q + 1] = m.y;
+                    qv[2 * q] = qq.x;
+                    qv[2 * q + 1] = qq.y;
+                    if (ERR) {
+                        const float2 ne = f2_fma(nd2, qq, g2);   // g - delta*q = -e
+                        rs = f2_add(rs, ne);
+                        colsum[q] = f2_add(colsum[q], ne);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    qv[i] = 0.0f;
+                    qm[i] = kMagic;
+                }
+            }
+            rsum[j] = rs.x + rs.y;
+            if (RS * j < rows_left) {
+                if (FMT == 0) {
+                    uint32_t w[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t a = __float_as_uint(qm[4 * h]), b = __float_as_uint(qm[4 * h + 1]);
+                        const uint32_t cc = __float_as_uint(qm[4 * h + 2]), dd = __float_as_uint(qm[4 * h + 3]);
+                        w[h] = __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(cc, dd, 0x0040), 0x5410);
+                    }
+                    if (nc0 + 8 <= C.N) {
+                        *reinterpret_cast<uint2*>(q8) = make_uint2(w[0], w[1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (nc0 + i < C.N) q8[i] = (int8_t)__float2int_rn(qv[i]);
+                    }
+                } else {
+                    // the same integer in an IEEE half (exact for |q| <= 2048)
+                    uint32_t hw[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __half2 h2 = __floats2half2_rn(qv[2 * q], qv[2 * q + 1]);
+                        hw[q] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    if (nc0 + 8 <= C.N) {
+                        *reinterpret_cast<uint4*>(q16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (nc0 + i < C.N) q16[i] = __float2half_rn(qv[i]);
+                    }
+                }
+            }
+            q8 += row_step;
+            q16 += row_step;
+        }
+        if (ERR && O.tok) {
+            // the 16 lanes of a row group hold 8 row sums each: a reduce-scatter in four
+            // exchanges leaves lanes 2i and 2i + 1 with the sum of row r0 + 16 i
+            const bool h8 = c & 8, h4 = c & 4, h2 = c & 2;
+            float a4[4], a2[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float send = h8 ? rsum[i] : rsum[i + 4], keep = h8 ? rsum[i + 4] : rsum[i];
+                a4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float send = h4 ? a4[i] : a4[i + 2], keep = h4 ? a4[i + 2] : a4[i];
+                a2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+            }
+            float a1;
+            {
+                const float send = h2 ? a2[0] : a2[1], keep = h2 ? a2[1] : a2[0];
+                a1 = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+            }
+            a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 1);
+            if ((c & 1) == 0 && RS * (c >> 1) < rows_left) O.tok[(t0 + r0 + RS * (c >> 1)) * C.ntc + cb] = -a1;
+        }
+        if (ERR && O.col) {
+            float cs[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                cs[2 * q] = colsum[q].x + __shfl_xor_sync(0xFFFFFFFFu, colsum[q].x, 16);
+                cs[2 * q + 1] = colsum[q].y + __shfl_xor_sync(0xFFFFFFFFu, colsum[q].y, 16);
+            }
+            if (lane < 16) {
+                *reinterpret_cast<float4*>(&col_smem[warp * kTile + 8 * c]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+                *reinterpret_cast<float4*>(&col_smem[warp * kTile + 8 * c + 4]) =
+                    make_float4(cs[4], cs[5], cs[6], cs[7]);
+            }
+        }
+        if (k + 1 < count) {
+            if (tid < kTile) xu_s[sl ^ 1][tid] = side;
+            else sw_s[sl ^ 1][tid - kTile] = side.x;
+        }
         __syncthreads();
-        round_and_store<MODE, RPT, FMT>(g, m, t0, n0, r0, c, C, O, col_smem);
+        if (ERR && O.col && tid < kTile) {
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) sum += col_smem[w * kTile + tid];
+            if (n0 + tid < C.N) O.col[rb * C.N + n0 + tid] = -sum;
+        }
     }
     // an early exit may leave copies in flight: wait for them before leaving
-    if (threadIdx.x == 0) {
-        for (int k = i; k < issued; ++k) q_wait((k & 1) ? bar1 : bar0, (uint32_t)(k >> 1) & 1u);
-    }
+    if (tid == 0)
+        for (int64_t q = k; q < issued; ++q) q_wait(bar0 + 8 * (int)(q % kQStages), (uint32_t)((q / kQStages) & 1));
 }
 
 // ---------------------------------------------------------------------------
@@ -731,14 +947,13 @@ static int sm_count() {
     return n;
 }
 
-constexpr int kQuantTmaSmem = 2 * kTile * kTile * 2 + 16;
 
-template <int MODE, int FMT>
+template <int MODE, int FMT, bool FOLD>
 static int launch_quant_tma(const CUtensorMap& map, const TileQuantArgs& A, const QuantCommon& C, const QuantOut& O,
                             int64_t ntiles, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(quantize_tma_kernel<MODE, FMT>,
+        cudaError_t e = cudaFuncSetAttribute(quantize_tma_kernel<MODE, FMT, FOLD>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantTmaSmem);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
@@ -747,9 +962,16 @@ static int launch_quant_tma(const CUtensorMap& map, const TileQuantArgs& A, cons
         attr = true;
     }
     const int64_t grid = ntiles < 2LL * sm_count() ? ntiles : 2LL * sm_count();
-    quantize_tma_kernel<MODE, FMT><<<(unsigned)grid, 256, kQuantTmaSmem, stream>>>(map, A, C, O, ntiles);
+    quantize_tma_kernel<MODE, FMT, FOLD><<<(unsigned)grid, 256, kQuantTmaSmem, stream>>>(map, A, C, O, ntiles);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
+}
+
+template <int MODE, int FMT>
+static int launch_quant_tma(const CUtensorMap& map, const TileQuantArgs& A, const QuantCommon& C, const QuantOut& O,
+                            int64_t ntiles, cudaStream_t stream) {
+    return (A.s_x || A.s_w) ? launch_quant_tma<MODE, FMT, true>(map, A, C, O, ntiles, stream)
+                            : launch_quant_tma<MODE, FMT, false>(map, A, C, O, ntiles, stream);
 }
 
 // The TMA path needs 16-byte aligned rows; returns 1 when it does not apply.
