@@ -331,6 +331,156 @@ __device__ __forceinline__ void q_issue_tile(uint32_t dst, const CUtensorMap* ma
         : "memory");
 }
 
+// Tile scale delta = amax / 127 and inv = 127 / amax rounded toward zero (so
+// |g * inv| <= 127 and no code leaves [-127, 127]) from the tile absmax bits.
+__device__ __forceinline__ void tile_scales(uint32_t amax_bits, float& d, float& inv) {
+    const bool nonfinite = amax_bits >= 0x7F800000u;
+    const float amx = __uint_as_float(amax_bits);
+    d = nonfinite ? __uint_as_float(0x7FC00000u) : amx / 127.0f;
+    inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amx);
+}
+
+// Round RPT rows of 8 values (rows RS apart) to codes and store them; with
+// ERR, add -e = g - delta*q (one rounding: the exact negation of delta*q - g)
+// into the row sums and the per-column sums.
+//   SR: q = floor(y) + [u < frac(y)] = ceil(y - u) for u in [0, 1).  y - u
+//   rounded up never passes an integer, so its ceiling is exact, and adding
+//   kMagic rounded up takes it: m = kMagic + q, exact.  RTNE: m = kMagic + y
+//   rounded to nearest.  The int8 code is the low byte of m's bits.
+// q0 points at my first row's 8 codes; rows_left: row j is stored iff RS j < rows_left.
+template <int MODE, int FMT, int RPT, int RS, bool ERR>
+__device__ __forceinline__ void round_rows(const float (&g)[RPT][8], float d, float inv, bool nonfinite,
+                                           const float* u0, int u_step, void* q0, int64_t row_step, int rows_left,
+                                           int64_t t_first, int nc0, int64_t N, uint32_t seed_lo, uint32_t tensor_id,
+                                           float (&rsum)[RPT], float2 (&colsum)[4]) {
+    const float2 M2 = make_float2(kMagic, kMagic), inv2 = make_float2(inv, inv), nd2 = make_float2(-d, -d);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) colsum[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        float u8[8];
+        if (MODE == kINDEP) {
+            const int64_t t = t_first + RS * j;
+            if ((N & 3) == 0) {
+                const uint64_t ctr = ((uint64_t)t * (uint64_t)N + (uint64_t)nc0) >> 2;
+                const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, seed_lo, tensor_id);
+                const Philox4 b =
+                    philox4x32_10((uint32_t)(ctr + 1), (uint32_t)((ctr + 1) >> 32), 0u, 0u, seed_lo, tensor_id);
+                u8[0] = unit24(a.x); u8[1] = unit24(a.y); u8[2] = unit24(a.z); u8[3] = unit24(a.w);
+                u8[4] = unit24(b.x); u8[5] = unit24(b.y); u8[6] = unit24(b.z); u8[7] = unit24(b.w);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint64_t e = (uint64_t)t * (uint64_t)N + (uint64_t)(nc0 + i);
+                    const uint64_t ctr = e >> 2;
+                    const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, seed_lo, tensor_id);
+                    const uint32_t w = (e & 3) == 0 ? a.x : (e & 3) == 1 ? a.y : (e & 3) == 2 ? a.z : a.w;
+                    u8[i] = unit24(w);
+                }
+            }
+        }
+        const float ut = MODE == kS3R ? u0[j * u_step] : 0.0f;
+        float qv[8], qm[8];
+        float2 rs = make_float2(0.0f, 0.0f);
+        if (!nonfinite) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 g2 = make_float2(g[j][2 * q], g[j][2 * q + 1]);
+                const float2 y = f2_mul(g2, inv2);   // |y| <= 127
+                float2 m;
+                if (MODE == kRTNE) {
+                    // per lane: a packed add that is the product's only use would be fused into an fma
+                    m = make_float2(__fadd_rn(y.x, kMagic), __fadd_rn(y.y, kMagic));
+                } else {
+                    const float2 uu = MODE == kS3R ? make_float2(ut, ut) : make_float2(u8[2 * q], u8[2 * q + 1]);
+                    m = f2_add_rp(f2_sub_rp(y, uu), M2);
+                }
+                const float2 qq = f2_sub(m, M2);   // the code, exact
+                qm[2 * q] = m.x;
+                qm[2 * q + 1] = m.y;
+                qv[2 * q] = qq.x;
+                qv[2 * q + 1] = qq.y;
+                if (ERR) {
+                    const float2 ne = f2_fma(nd2, qq, g2);   // g - delta*q = -e
+                    rs = f2_add(rs, ne);
+                    colsum[q] = f2_add(colsum[q], ne);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                qv[i] = 0.0f;
+                qm[i] = kMagic;
+            }
+        }
+        rsum[j] = rs.x + rs.y;
+        if (RS * j < rows_left) {
+            if (FMT == 0) {
+                uint32_t w[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t a = __float_as_uint(qm[4 * h]), b = __float_as_uint(qm[4 * h + 1]);
+                    const uint32_t cc = __float_as_uint(qm[4 * h + 2]), dd = __float_as_uint(qm[4 * h + 3]);
+                    w[h] = __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(cc, dd, 0x0040), 0x5410);
+                }
+                int8_t* dst = static_cast<int8_t*>(q0) + j * row_step;
+                if (nc0 + 8 <= N) {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (nc0 + i < N) dst[i] = (int8_t)__float2int_rn(qv[i]);
+                }
+            } else {
+                // the same integer in an IEEE half (exact for |q| <= 2048)
+                uint32_t hw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __half2 h2 = __floats2half2_rn(qv[2 * q], qv[2 * q + 1]);
+                    hw[q] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                __half* dst = static_cast<__half*>(q0) + j * row_step;
+                if (nc0 + 8 <= N) {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (nc0 + i < N) dst[i] = __float2half_rn(qv[i]);
+                }
+            }
+        }
+    }
+}
+
+// 16 lanes (c = lane & 15) of a row group hold RPT row sums each: a
+// reduce-scatter (halving exchanges, then plain ones) leaves lane c with the
+// full sum of row c / (16 / RPT), in a fixed order.
+template <int RPT>
+__device__ __forceinline__ float scatter_rows16(const float (&v)[RPT], int c) {
+    float a[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) a[i] = v[i];
+    int n = RPT;
+#pragma unroll
+    for (int x = 8; x >= 1; x >>= 1) {
+        if (n > 1) {
+            const int h = n / 2;
+            const bool hi = c & x;
+#pragma unroll
+            for (int i = 0; i < RPT / 2; ++i) {
+                if (i < h) {
+                    const float send = hi ? a[i] : a[i + h], keep = hi ? a[i + h] : a[i];
+                    a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, x);
+                }
+            }
+            n = h;
+        } else {
+            a[0] += __shfl_xor_sync(0xFFFFFFFFu, a[0], x);
+        }
+    }
+    return a[0];
+}
+
 // Persistent quantizer.  CTA b owns the contiguous tile range
 // [b ntiles / grid, (b + 1) ntiles / grid) in row-major tile order, so its
 // consecutive tiles mostly share a row block and reuse that block's
@@ -342,13 +492,13 @@ constexpr int kQStages = 3;
 constexpr int kQTileBytes = kTile * kTile * 2;
 constexpr int kQuantTmaSmem = kQStages * kQTileBytes + 8 * kQStages;
 
-// side data of tile `tile` for this thread: (row scale, threshold) or (column scale, 0)
+// side data of the tile in row block rb, column block cb for this thread:
+// (row scale, threshold) or (column scale, 0)
 template <int MODE>
-__device__ __forceinline__ float2 q_side(const TileQuantArgs& A, const QuantCommon& C, uint32_t tensor_id,
-                                         int64_t tile, float& u_mine, int64_t& u_rb) {
-    const int64_t rb = tile / C.ntc;
+__device__ __forceinline__ float2 q_side(const TileQuantArgs& A, const QuantCommon& C, uint32_t tensor_id, int rb,
+                                         int cb, float& u_mine, int& u_rb) {
     if (threadIdx.x < kTile) {
-        const int64_t t = rb * kTile + threadIdx.x;
+        const int64_t t = (int64_t)rb * kTile + threadIdx.x;
         const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
         if (MODE == kS3R && rb != u_rb) {
             u_mine = token_threshold((uint64_t)t, C.seed_lo, tensor_id);
@@ -356,7 +506,7 @@ __device__ __forceinline__ float2 q_side(const TileQuantArgs& A, const QuantComm
         }
         return make_float2(sx, u_mine);
     }
-    const int64_t n = (tile % C.ntc) * kTile + (threadIdx.x - kTile);
+    const int64_t n = (int64_t)cb * kTile + (threadIdx.x - kTile);
     return make_float2((A.s_w && n < C.N) ? __ldg(A.s_w + n) : 1.0f, 0.0f);
 }
 
@@ -374,20 +524,26 @@ __global__ void __launch_bounds__(256, 2)
     __shared__ uint32_t red[8];
     __shared__ __align__(16) float col_smem[8 * kTile];
     const int tid = threadIdx.x, c = tid & 15, r0 = tid >> 4, lane = tid & 31, warp = tid >> 5;
-    const int64_t beg = (int64_t)blockIdx.x * ntiles / gridDim.x;
-    const int64_t count = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x - beg;
+    // tile indices fit 32 bits (checked on the host) and advance incrementally
+    const int ntc = (int)C.ntc;
+    const int beg = (int)((int64_t)blockIdx.x * ntiles / gridDim.x);
+    const int count = (int)(((int64_t)blockIdx.x + 1) * ntiles / gridDim.x) - beg;
     const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars);
     const int64_t row_step = (int64_t)RS * C.N;   // elements between my consecutive rows
-    auto issue = [&](int64_t k) {
-        const int64_t tile = beg + k;
-        const int s = (int)(k % kQStages);
-        q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + s * kQTileBytes), &tmG,
-                     (int32_t)((tile % C.ntc) * kTile), (int32_t)((tile / C.ntc) * kTile), bar0 + 8 * s);
+    int irb = beg / ntc, icb = beg - (beg / ntc) * ntc;   // next tile to copy (thread 0)
+    auto issue = [&](int k) {
+        const int s = k % kQStages;
+        q_issue_tile((uint32_t)__cvta_generic_to_shared(qsmem + s * kQTileBytes), &tmG, icb * kTile, irb * kTile,
+                     bar0 + 8 * s);
+        if (++icb == ntc) { icb = 0; ++irb; }
     };
+    int rb = beg / ntc, cb = beg - (beg / ntc) * ntc;   // current tile
+    int nrb = rb, ncb = cb;                             // tile after the current one
+    if (++ncb == ntc) { ncb = 0; ++nrb; }
     float u_mine = 0.0f;
-    int64_t u_rb = -1;
+    int u_rb = -1;
     if (count > 0) {
-        const float2 sd = q_side<MODE>(A, C, O.tensor_id, beg, u_mine, u_rb);
+        const float2 sd = q_side<MODE>(A, C, O.tensor_id, rb, cb, u_mine, u_rb);
         if (tid < kTile) xu_s[0][tid] = sd;
         else sw_s[0][tid - kTile] = sd.x;
     }
@@ -398,24 +554,22 @@ __global__ void __launch_bounds__(256, 2)
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmG) : "memory");
     }
     __syncthreads();
-    int64_t issued = 0;   // thread 0's count
+    int issued = 0;   // thread 0's count
     if (tid == 0)
         for (; issued < kQStages && issued < count; ++issued) issue(issued);
-    const float2 M2 = make_float2(kMagic, kMagic);
-    int64_t k = 0;
+    int k = 0, s = 0;
+    uint32_t phase = 0;
     for (; k < count; ++k) {
-        const int64_t tile = beg + k;
-        const int s = (int)(k % kQStages), sl = (int)(k & 1);
-        const int64_t rb = tile / C.ntc, cb = tile % C.ntc;
-        const int64_t t0 = rb * kTile, n0 = cb * kTile;
+        const int sl = k & 1;
+        const int64_t t0 = (int64_t)rb * kTile, n0 = (int64_t)cb * kTile;
         const int nc0 = (int)n0 + 8 * c;
         const int64_t rl = C.T - t0 - r0;
         const int rows_left = rl < kTile ? (int)rl : kTile;   // my row j is valid iff RS j < rows_left
         // the next tile's side data: loads (and thresholds) in flight during this tile
         float2 side = make_float2(0.0f, 0.0f);
-        if (k + 1 < count) side = q_side<MODE>(A, C, O.tensor_id, tile + 1, u_mine, u_rb);
+        if (k + 1 < count) side = q_side<MODE>(A, C, O.tensor_id, nrb, ncb, u_mine, u_rb);
         // every thread waits; the CTA leaves together if any wait ran out
-        if (!__syncthreads_and(q_wait(bar0 + 8 * s, (uint32_t)((k / kQStages) & 1)))) {
+        if (!__syncthreads_and(q_wait(bar0 + 8 * s, phase))) {
             if (tid == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
             break;
         }
@@ -465,146 +619,22 @@ __global__ void __launch_bounds__(256, 2)
         }
         const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, red[lane & 7]);
         const bool nonfinite = amax_bits >= 0x7F800000u;   // uniform across the CTA
-        const float amx = __uint_as_float(amax_bits);
-        const float d = nonfinite ? __uint_as_float(0x7FC00000u) : amx / 127.0f;
-        // inv = 127/amax rounded toward zero keeps |y| <= 127: no code leaves [-127, 127]
-        const float inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amx);
+        float d, inv;
+        tile_scales(amax_bits, d, inv);
         if (tid == 0) {
-            O.scale[rb * C.ntc + cb] = d;
+            O.scale[(int64_t)rb * ntc + cb] = d;
             if (nonfinite) set_status(C.d_status, S3R_ERR_NONFINITE);
         }
-        // pass 2: codes, stores and error sums.  The sums collect -e = g - delta*q (one
-        // rounding each, the exact negation of delta*q - g) and are negated when stored.
-        const float2 inv2 = make_float2(inv, inv), nd2 = make_float2(-d, -d);
+        // pass 2: codes, stores and error sums (of -e, negated when stored)
         float2 colsum[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) colsum[q] = make_float2(0.0f, 0.0f);
         float rsum[RPT];
-        int8_t* q8 = static_cast<int8_t*>(O.Q) + (t0 + r0) * C.N + nc0;
-        __half* q16 = static_cast<__half*>(O.Q) + (t0 + r0) * C.N + nc0;
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int rr = r0 + RS * j;
-            float u8[8];
-            if (MODE == kINDEP) {
-                const int64_t t = t0 + rr;
-                if ((C.N & 3) == 0) {
-                    const uint64_t ctr = ((uint64_t)t * (uint64_t)C.N + (uint64_t)nc0) >> 2;
-                    const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, C.seed_lo,
-                                                    O.tensor_id);
-                    const Philox4 b = philox4x32_10((uint32_t)(ctr + 1), (uint32_t)((ctr + 1) >> 32), 0u, 0u,
-                                                    C.seed_lo, O.tensor_id);
-                    u8[0] = unit24(a.x); u8[1] = unit24(a.y); u8[2] = unit24(a.z); u8[3] = unit24(a.w);
-                    u8[4] = unit24(b.x); u8[5] = unit24(b.y); u8[6] = unit24(b.z); u8[7] = unit24(b.w);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint64_t e = (uint64_t)t * (uint64_t)C.N + (uint64_t)(nc0 + i);
-                        const uint64_t ctr = e >> 2;
-                        const Philox4 a = philox4x32_10((uint32_t)ctr, (uint32_t)(ctr >> 32), 0u, 0u, C.seed_lo,
-                                                        O.tensor_id);
-                        const uint32_t w = (e & 3) == 0 ? a.x : (e & 3) == 1 ? a.y : (e & 3) == 2 ? a.z : a.w;
-                        u8[i] = unit24(w);
-                    }
-                }
-            }
-            const float ut = MODE == kS3R ? xu_s[sl][rr].y : 0.0f;
-            // m = kMagic + q (exact), and the int8 code is the low byte of m's bits.  SR:
-            // q = floor(y) + [u < frac(y)] = ceil(y - u) (u in [0, 1)); y - u rounded up
-            // never passes an integer, so its ceiling is exact, and adding kMagic rounded
-            // up takes it.  RTNE: kMagic + y rounded to nearest.
-            float qv[8], qm[8];
-            float2 rs = make_float2(0.0f, 0.0f);
-            if (!nonfinite) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 g2 = make_float2(g[j][2 * q], g[j][2 * q + 1]);
-                    const float2 y = f2_mul(g2, inv2);   // |y| <= 127
-                    float2 m;
-                    if (MODE == kRTNE) {
-                        // per lane: a packed add that is the product's only use would be fused into an fma
-                        m = make_float2(__fadd_rn(y.x, kMagic), __fadd_rn(y.y, kMagic));
-                    } else {
-                        const float2 uu = MODE == kS3R ? make_float2(ut, ut) : make_float2(u8[2 * q], u8[2 * q + 1]);
-                        m = f2_add_rp(f2_sub_rp(y, uu), M2);
-                    }
-                    const float2 qq = f2_sub(m, M2);   // the code, exact
-                    qm[2 * q] = m.x;
-                    qm[2 * q + 1] = m.y;
-                    qv[2 * q] = qq.x;
-                    qv[2 * q + 1] = qq.y;
-                    if (ERR) {
-                        const float2 ne = f2_fma(nd2, qq, g2);   // g - delta*q = -e
-                        rs = f2_add(rs, ne);
-                        colsum[q] = f2_add(colsum[q], ne);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    qv[i] = 0.0f;
-                    qm[i] = kMagic;
-                }
-            }
-            rsum[j] = rs.x + rs.y;
-            if (RS * j < rows_left) {
-                if (FMT == 0) {
-                    uint32_t w[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t a = __float_as_uint(qm[4 * h]), b = __float_as_uint(qm[4 * h + 1]);
-                        const uint32_t cc = __float_as_uint(qm[4 * h + 2]), dd = __float_as_uint(qm[4 * h + 3]);
-                        w[h] = __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(cc, dd, 0x0040), 0x5410);
-                    }
-                    if (nc0 + 8 <= C.N) {
-                        *reinterpret_cast<uint2*>(q8) = make_uint2(w[0], w[1]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (nc0 + i < C.N) q8[i] = (int8_t)__float2int_rn(qv[i]);
-                    }
-                } else {
-                    // the same integer in an IEEE half (exact for |q| <= 2048)
-                    uint32_t hw[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const __half2 h2 = __floats2half2_rn(qv[2 * q], qv[2 * q + 1]);
-                        hw[q] = *reinterpret_cast<const uint32_t*>(&h2);
-                    }
-                    if (nc0 + 8 <= C.N) {
-                        *reinterpret_cast<uint4*>(q16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (nc0 + i < C.N) q16[i] = __float2half_rn(qv[i]);
-                    }
-                }
-            }
-            q8 += row_step;
-            q16 += row_step;
-        }
+        void* q0 = FMT == 0 ? (void*)(static_cast<int8_t*>(O.Q) + (t0 + r0) * C.N + nc0)
+                            : (void*)(static_cast<__half*>(O.Q) + (t0 + r0) * C.N + nc0);
+        round_rows<MODE, FMT, RPT, RS, ERR>(g, d, inv, nonfinite, &xu_s[sl][r0].y, 2 * RS, q0, row_step, rows_left,
+                                            t0 + r0, nc0, C.N, C.seed_lo, O.tensor_id, rsum, colsum);
         if (ERR && O.tok) {
-            // the 16 lanes of a row group hold 8 row sums each: a reduce-scatter in four
-            // exchanges leaves lanes 2i and 2i + 1 with the sum of row r0 + 16 i
-            const bool h8 = c & 8, h4 = c & 4, h2 = c & 2;
-            float a4[4], a2[2];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float send = h8 ? rsum[i] : rsum[i + 4], keep = h8 ? rsum[i + 4] : rsum[i];
-                a4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float send = h4 ? a4[i] : a4[i + 2], keep = h4 ? a4[i + 2] : a4[i];
-                a2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-            }
-            float a1;
-            {
-                const float send = h2 ? a2[0] : a2[1], keep = h2 ? a2[1] : a2[0];
-                a1 = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
-            }
-            a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 1);
-            if ((c & 1) == 0 && RS * (c >> 1) < rows_left) O.tok[(t0 + r0 + RS * (c >> 1)) * C.ntc + cb] = -a1;
+            const float r = scatter_rows16<RPT>(rsum, c);   // row r0 + 16 (c >> 1)
+            if ((c & 1) == 0 && RS * (c >> 1) < rows_left) O.tok[(t0 + r0 + RS * (c >> 1)) * ntc + cb] = -r;
         }
         if (ERR && O.col) {
             float cs[8];
@@ -628,12 +658,16 @@ __global__ void __launch_bounds__(256, 2)
             float sum = 0.0f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) sum += col_smem[w * kTile + tid];
-            if (n0 + tid < C.N) O.col[rb * C.N + n0 + tid] = -sum;
+            if (n0 + tid < C.N) O.col[(int64_t)rb * C.N + n0 + tid] = -sum;
         }
+        rb = nrb;
+        cb = ncb;
+        if (++ncb == ntc) { ncb = 0; ++nrb; }
+        if (++s == kQStages) { s = 0; phase ^= 1u; }
     }
     // an early exit may leave copies in flight: wait for them before leaving
     if (tid == 0)
-        for (int64_t q = k; q < issued; ++q) q_wait(bar0 + 8 * (int)(q % kQStages), (uint32_t)((q / kQStages) & 1));
+        for (int q = k; q < issued; ++q) q_wait(bar0 + 8 * (q % kQStages), (uint32_t)((q / kQStages) & 1));
 }
 
 // ---------------------------------------------------------------------------
@@ -792,8 +826,6 @@ __global__ void __launch_bounds__(512) swiglu_quantize_kernel(SwigluArgs A, Quan
 // TMA copies the next tile's dA (fp32) and h1, h3 (bf16) into shared memory
 // (128 KB) while the current tile is quantized from registers, so the HBM
 // stream is not exposed between tiles.
-constexpr int kSwigluTmaBytes = kTile * kTile * (4 + 2 + 2);
-constexpr int kSwigluTmaSmem = kSwigluTmaBytes + 128 + 16;
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar) {
     asm volatile(
@@ -803,60 +835,234 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
         : "memory");
 }
 
+// Persistent SwiGLU quantizer: CTA b owns a contiguous range of 128 x 128
+// tiles in row-major order (consecutive tiles share a row block and its two
+// threshold sets).  Each tile arrives as four 32-row quarters (dA fp32, h1 and
+// h3 bf16: 32 KiB) through a six-quarter TMA ring, so one and a half tiles are
+// in flight while one is rounded; thread (c, r0) owns row r0 + 32 j of quarter
+// j and columns 8c .. 8c + 7.  The side data of a tile (row scale and the two
+// row thresholds; the two column scales) is fetched one tile ahead.
+constexpr int kSwQuarterRows = 32;
+constexpr int kSwQuarterBytes = kSwQuarterRows * kTile * (4 + 2 + 2);   // 32 KiB
+constexpr int kSwStages = 6;
+constexpr int kSwigluTmaSmem = kSwStages * kSwQuarterBytes + 8 * kSwStages + 128;
+
 template <int MODE>
+__device__ __forceinline__ void sw_side(const SwigluArgs& A, const QuantCommon& C, const QuantOut& O1,
+                                        const QuantOut& O3, int rb, int cb, float4& xs, float2& ws, float& u1,
+                                        float& u3, int& u_rb) {
+    if (threadIdx.x < kTile) {
+        const int64_t t = (int64_t)rb * kTile + threadIdx.x;
+        const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
+        if (MODE == kS3R && rb != u_rb) {
+            u1 = token_threshold((uint64_t)t, C.seed_lo, O1.tensor_id);
+            u3 = token_threshold((uint64_t)t, C.seed_lo, O3.tensor_id);
+            u_rb = rb;
+        }
+        xs = make_float4(sx, u1, u3, 0.0f);
+    } else if (threadIdx.x < 2 * kTile) {
+        const int64_t n = (int64_t)cb * kTile + (threadIdx.x - kTile);
+        const bool ok = n < C.N;
+        ws = make_float2((A.s_w1 && ok) ? __ldg(A.s_w1 + n) : 1.0f, (A.s_w3 && ok) ? __ldg(A.s_w3 + n) : 1.0f);
+    }
+}
+
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(512, 1)
     swiglu_tma_kernel(const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmH1,
                       const __grid_constant__ CUtensorMap tmH3, SwigluArgs A, QuantCommon C, QuantOut O1, QuantOut O3,
                       int64_t ntiles) {
+    constexpr int RPT = 4, RS = 32;
+    constexpr bool ERR = MODE == kS3R;
     extern __shared__ uint8_t swsm_raw[];
-    uint8_t* swsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(swsm_raw) + 127) & ~(uintptr_t)127);
-    float* sd = reinterpret_cast<float*>(swsm);
-    uint16_t* s1 = reinterpret_cast<uint16_t*>(swsm + kTile * kTile * 4);
-    uint16_t* s3 = s1 + kTile * kTile;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(swsm + kSwigluTmaBytes);
-    __shared__ uint32_t red[2 * 16];
-    __shared__ float col_smem[16 * 128];
-    const uint32_t b0 = (uint32_t)__cvta_generic_to_shared(bar);
-    auto issue = [&](int64_t tile) {
-        const int32_t x = (int32_t)((tile % C.ntc) * kTile), y = (int32_t)((tile / C.ntc) * kTile);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b0), "r"(kSwigluTmaBytes)
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(swsm_raw) + 127) & ~(uintptr_t)127);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kSwStages * kSwQuarterBytes);
+    __shared__ __align__(16) float4 xs_s[2][kTile];   // (s_x, u1, u3, 0) per tile row
+    __shared__ __align__(16) float2 ws_s[2][kTile];   // (s_w1, s_w3) per tile column
+    __shared__ uint32_t red[2][16];
+    __shared__ __align__(16) float col_smem[2][16 * kTile];
+    const int tid = threadIdx.x, c = tid & 15, r0 = tid >> 4, lane = tid & 31, warp = tid >> 5;
+    const int ntc = (int)C.ntc;
+    const int beg = (int)((int64_t)blockIdx.x * ntiles / gridDim.x);
+    const int count = (int)(((int64_t)blockIdx.x + 1) * ntiles / gridDim.x) - beg;
+    const int nq = 4 * count;   // quarters this CTA streams
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars);
+    const int64_t row_step = (int64_t)RS * C.N;
+    int irb = beg / ntc, icb = beg - (beg / ntc) * ntc, iq = 0;   // next quarter to copy (thread 0)
+    auto issue = [&](int q) {
+        const int st = q % kSwStages;
+        const uint32_t bar = bar0 + 8 * st;
+        uint8_t* dst = ring + st * kSwQuarterBytes;
+        const int32_t x = icb * kTile, y = irb * kTile + iq * kSwQuarterRows;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kSwQuarterBytes)
                      : "memory");
-        tma_2d((uint32_t)__cvta_generic_to_shared(sd), &tmD, x, y, b0);
-        tma_2d((uint32_t)__cvta_generic_to_shared(s1), &tmH1, x, y, b0);
-        tma_2d((uint32_t)__cvta_generic_to_shared(s3), &tmH3, x, y, b0);
+        tma_2d((uint32_t)__cvta_generic_to_shared(dst), &tmD, x, y, bar);
+        tma_2d((uint32_t)__cvta_generic_to_shared(dst + kSwQuarterRows * kTile * 4), &tmH1, x, y, bar);
+        tma_2d((uint32_t)__cvta_generic_to_shared(dst + kSwQuarterRows * kTile * 6), &tmH3, x, y, bar);
+        if (++iq == 4) {
+            iq = 0;
+            if (++icb == ntc) { icb = 0; ++irb; }
+        }
     };
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b0) : "memory");
+    int rb = beg / ntc, cb = beg - (beg / ntc) * ntc;
+    int nrb = rb, ncb = cb;
+    if (++ncb == ntc) { ncb = 0; ++nrb; }
+    float u1 = 0.0f, u3 = 0.0f;
+    int u_rb = -1;
+    {
+        float4 xs = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 ws = make_float2(0.f, 0.f);
+        if (count > 0) sw_side<MODE>(A, C, O1, O3, rb, cb, xs, ws, u1, u3, u_rb);
+        if (tid < kTile) xs_s[0][tid] = xs;
+        else if (tid < 2 * kTile) ws_s[0][tid - kTile] = ws;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kSwStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * i) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmD) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmH1) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmH3) : "memory");
     }
     __syncthreads();
-    int64_t issued = 0;   // copies issued (thread 0's count)
-    if (threadIdx.x == 0 && (int64_t)blockIdx.x < ntiles) {
-        issue(blockIdx.x);
-        issued = 1;
-    }
-    int64_t i = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
-        // every thread waits; the CTA leaves together if any wait ran out
-        if (!__syncthreads_and(q_wait(b0, (uint32_t)(i & 1)))) {
-            if (threadIdx.x == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
+    int issued = 0;   // quarters copied (thread 0's count)
+    if (tid == 0)
+        for (; issued < kSwStages && issued < nq; ++issued) issue(issued);
+    int k = 0;
+    for (; k < count; ++k) {
+        const int sl = k & 1;
+        const int64_t t0 = (int64_t)rb * kTile, n0 = (int64_t)cb * kTile;
+        const int nc0 = (int)n0 + 8 * c;
+        const int64_t rl = C.T - t0 - r0;
+        const int rows_left = rl < kTile ? (int)rl : kTile;
+        float4 nxs = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 nws = make_float2(0.f, 0.f);
+        if (k + 1 < count) sw_side<MODE>(A, C, O1, O3, nrb, ncb, nxs, nws, u1, u3, u_rb);
+        // pass 1: glue and folds, quarter by quarter.  Each thread waits for its
+        // quarters itself; a wait that ran out is settled at the next barrier.
+        float g1[RPT][8], g3[RPT][8];
+        float am1 = 0.0f, am3 = 0.0f;   // NaN-propagating absmax of each tile
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int q = 4 * k + j, st = q % kSwStages;
+            ok = ok && q_wait(bar0 + 8 * st, (uint32_t)((q / kSwStages) & 1));
+            const uint8_t* base = ring + st * kSwQuarterBytes;
+            const float* sd = reinterpret_cast<const float*>(base) + r0 * kTile + 8 * c;
+            const uint16_t* s1 = reinterpret_cast<const uint16_t*>(base + kSwQuarterRows * kTile * 4) + r0 * kTile + 8 * c;
+            const uint16_t* s3 = reinterpret_cast<const uint16_t*>(base + kSwQuarterRows * kTile * 6) + r0 * kTile + 8 * c;
+            const float4 d0 = *reinterpret_cast<const float4*>(sd);
+            const float4 d1 = *reinterpret_cast<const float4*>(sd + 4);
+            const uint4 a1 = *reinterpret_cast<const uint4*>(s1);
+            const uint4 a3 = *reinterpret_cast<const uint4*>(s3);
+            const float da[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            const uint32_t h1w[4] = {a1.x, a1.y, a1.z, a1.w}, h3w[4] = {a3.x, a3.y, a3.z, a3.w};
+            const float sx = xs_s[sl][r0 + RS * j].x;
+            const float2 sx2 = make_float2(sx, sx);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                // glue, in the documented order, two lanes per packed instruction
+                // (no contraction: built with -fmad=false)
+                const float2 x = make_float2(bf16_lo(h1w[i >> 1]), bf16_hi(h1w[i >> 1]));
+                const float2 x3 = make_float2(bf16_lo(h3w[i >> 1]), bf16_hi(h3w[i >> 1]));
+                const float2 d2 = make_float2(da[i], da[i + 1]);
+                float2 silu, dsilu;
+                swiglu_terms2(x, silu, dsilu);
+                const float2 dh1 = f2_mul(f2_mul(d2, x3), dsilu);
+                const float2 dh3 = f2_mul(d2, silu);
+                // folds (s_x * dh) * s_w; a missing scale is 1
+                const float4 wp = *reinterpret_cast<const float4*>(&ws_s[sl][8 * c + i]);   // (w1, w3) of i, i + 1
+                const float2 v1 = f2_mul(f2_mul(sx2, dh1), make_float2(wp.x, wp.z));
+                const float2 v3 = f2_mul(f2_mul(sx2, dh3), make_float2(wp.y, wp.w));
+                g1[j][i] = v1.x;
+                g1[j][i + 1] = v1.y;
+                g3[j][i] = v3.x;
+                g3[j][i + 1] = v3.y;
+                am1 = max3_abs_nan(am1, v1.x, v1.y);
+                am3 = max3_abs_nan(am3, v3.x, v3.y);
+            }
+        }
+        {
+            const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am1));
+            const uint32_t m3 = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am3));
+            if (lane == 0) {
+                red[0][warp] = m1;
+                red[1][warp] = m3;
+            }
+        }
+        // every thread is done with this tile's quarters; the CTA leaves together if a wait ran out
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
             break;
         }
-        const int64_t t0 = (tile / C.ntc) * kTile, n0 = (tile % C.ntc) * kTile;
-        const int64_t next = tile + gridDim.x;
-        swiglu_tile<MODE, true>(A, C, O1, O3, t0, n0, sd, s1, s3, red, col_smem, [&] {
-            if (threadIdx.x == 0 && next < ntiles) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(next);
-                ++issued;
+        if (tid == 0 && issued < nq) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            for (int i = 0; i < 4 && issued < nq; ++i, ++issued) issue(issued);
+        }
+        const uint32_t amax1 = __reduce_max_sync(0xFFFFFFFFu, red[0][lane & 15]);
+        const uint32_t amax3 = __reduce_max_sync(0xFFFFFFFFu, red[1][lane & 15]);
+        // lanes 0 and 1 derive the two tiles' scales side by side
+        float dd, ii;
+        tile_scales((lane & 1) ? amax3 : amax1, dd, ii);
+        const float d1s = __shfl_sync(0xFFFFFFFFu, dd, 0), inv1 = __shfl_sync(0xFFFFFFFFu, ii, 0);
+        const float d3s = __shfl_sync(0xFFFFFFFFu, dd, 1), inv3 = __shfl_sync(0xFFFFFFFFu, ii, 1);
+        const bool nf1 = amax1 >= 0x7F800000u, nf3 = amax3 >= 0x7F800000u;   // uniform across the CTA
+        if (tid == 0) {
+            O1.scale[(int64_t)rb * ntc + cb] = d1s;
+            O3.scale[(int64_t)rb * ntc + cb] = d3s;
+            if (nf1 || nf3) set_status(C.d_status, S3R_ERR_NONFINITE);
+        }
+        // pass 2: codes, stores and error sums (of -e, negated when stored)
+        const int64_t off = (t0 + r0) * C.N + nc0;
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const QuantOut& O = o ? O3 : O1;
+            float2 colsum[4];
+            float rsum[RPT];
+            void* q0 = FMT == 0 ? (void*)(static_cast<int8_t*>(O.Q) + off) : (void*)(static_cast<__half*>(O.Q) + off);
+            round_rows<MODE, FMT, RPT, RS, ERR>(o ? g3 : g1, o ? d3s : d1s, o ? inv3 : inv1, o ? nf3 : nf1,
+                                                o ? &xs_s[sl][r0].z : &xs_s[sl][r0].y, 4 * RS, q0, row_step,
+                                                rows_left, t0 + r0, nc0, C.N, C.seed_lo, O.tensor_id, rsum, colsum);
+            if (ERR && O.tok) {
+                const float r = scatter_rows16<RPT>(rsum, c);   // row r0 + 32 (c >> 2)
+                if ((c & 3) == 0 && RS * (c >> 2) < rows_left) O.tok[(t0 + r0 + RS * (c >> 2)) * ntc + cb] = -r;
             }
-        });
+            if (ERR && O.col) {
+                float cs[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    cs[2 * q] = colsum[q].x + __shfl_xor_sync(0xFFFFFFFFu, colsum[q].x, 16);
+                    cs[2 * q + 1] = colsum[q].y + __shfl_xor_sync(0xFFFFFFFFu, colsum[q].y, 16);
+                }
+                if (lane < 16) {
+                    float* dst = &col_smem[o][warp * kTile + 8 * c];
+                    *reinterpret_cast<float4*>(dst) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+                    *reinterpret_cast<float4*>(dst + 4) = make_float4(cs[4], cs[5], cs[6], cs[7]);
+                }
+            }
+        }
+        if (k + 1 < count) {
+            if (tid < kTile) xs_s[sl ^ 1][tid] = nxs;
+            else if (tid < 2 * kTile) ws_s[sl ^ 1][tid - kTile] = nws;
+        }
+        __syncthreads();
+        if (ERR && tid < 2 * kTile) {
+            const int o = tid >> 7, n = tid & (kTile - 1);
+            const QuantOut& O = o ? O3 : O1;
+            if (O.col) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < 16; ++w) sum += col_smem[o][w * kTile + n];
+                if (n0 + n < C.N) O.col[(int64_t)rb * C.N + n0 + n] = -sum;
+            }
+        }
+        rb = nrb;
+        cb = ncb;
+        if (++ncb == ntc) { ncb = 0; ++nrb; }
     }
-    // an early exit may leave a copy in flight: wait for it before leaving
-    if (threadIdx.x == 0 && issued > i) q_wait(b0, (uint32_t)(i & 1));
+    // an early exit may leave copies in flight: wait for them before leaving
+    if (tid == 0)
+        for (int q = 4 * k; q < issued; ++q) q_wait(bar0 + 8 * (q % kSwStages), (uint32_t)((q / kSwStages) & 1));
 }
 
 // ---------------------------------------------------------------------------
@@ -990,6 +1196,7 @@ static int try_quant_tma(int mode, const TileQuantArgs& A, const QuantCommon& C,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return 1;
     const int64_t ntiles = s3r_cdiv(C.T, kTile) * C.ntc;
+    if (ntiles >= (int64_t(1) << 31) / 4) return 1;   // the kernel keeps tile indices in 32 bits
     const bool f16 = O.fmt == S3R_CODES_F16;
     switch (mode) {
         case kRTNE: return f16 ? launch_quant_tma<kRTNE, 1>(map, A, C, O, ntiles, stream)
@@ -1064,13 +1271,13 @@ extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, c
     return S3R_OK;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 static int launch_swiglu_tma(const CUtensorMap* maps, const SwigluArgs& A, const QuantCommon& C, const QuantOut& O1,
                              const QuantOut& O3, int64_t ntiles, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(swiglu_tma_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSwigluTmaSmem);
+        cudaError_t e = cudaFuncSetAttribute(swiglu_tma_kernel<MODE, FMT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSwigluTmaSmem);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return s3r_cuda_fail("swiglu_quantize: cudaFuncSetAttribute", e);
@@ -1078,8 +1285,8 @@ static int launch_swiglu_tma(const CUtensorMap* maps, const SwigluArgs& A, const
         attr = true;
     }
     const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
-    swiglu_tma_kernel<MODE><<<(unsigned)grid, 512, kSwigluTmaSmem, stream>>>(maps[0], maps[1], maps[2], A, C, O1, O3,
-                                                                              ntiles);
+    swiglu_tma_kernel<MODE, FMT><<<(unsigned)grid, 512, kSwigluTmaSmem, stream>>>(maps[0], maps[1], maps[2], A, C,
+                                                                                   O1, O3, ntiles);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
 }
@@ -1092,7 +1299,7 @@ static int try_swiglu_tma(int round_mode, const SwigluArgs& A, const QuantCommon
     if (!fn) return 1;
     CUtensorMap maps[3];
     cuuint64_t dims[2] = {(cuuint64_t)C.N, (cuuint64_t)C.T};
-    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kSwQuarterRows};
     cuuint32_t estr[2] = {1u, 1u};
     cuuint64_t sd[1] = {(cuuint64_t)A.ldd * 4}, sh[1] = {(cuuint64_t)A.ldh * 2};
     if (fn(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A.dA), dims, sd, box, estr,
@@ -1106,10 +1313,16 @@ static int try_swiglu_tma(int round_mode, const SwigluArgs& A, const QuantCommon
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return 1;
     const int64_t ntiles = s3r_cdiv(C.T, kTile) * C.ntc;
+    if (ntiles >= (int64_t(1) << 31) / 4) return 1;   // the kernel keeps quarter indices in 32 bits
+    const bool f16 = O1.fmt == S3R_CODES_F16;
+    if (O3.fmt != O1.fmt) return 1;
     switch (round_mode) {
-        case S3R_ROUND_RTNE: return launch_swiglu_tma<kRTNE>(maps, A, C, O1, O3, ntiles, stream);
-        case S3R_ROUND_S3R: return launch_swiglu_tma<kS3R>(maps, A, C, O1, O3, ntiles, stream);
-        case S3R_ROUND_INDEP: return launch_swiglu_tma<kINDEP>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_RTNE: return f16 ? launch_swiglu_tma<kRTNE, 1>(maps, A, C, O1, O3, ntiles, stream)
+                                        : launch_swiglu_tma<kRTNE, 0>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_S3R: return f16 ? launch_swiglu_tma<kS3R, 1>(maps, A, C, O1, O3, ntiles, stream)
+                                       : launch_swiglu_tma<kS3R, 0>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_INDEP: return f16 ? launch_swiglu_tma<kINDEP, 1>(maps, A, C, O1, O3, ntiles, stream)
+                                         : launch_swiglu_tma<kINDEP, 0>(maps, A, C, O1, O3, ntiles, stream);
         default: return S3R_ERR_ARG;
     }
 }
