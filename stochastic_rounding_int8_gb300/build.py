@@ -55,6 +55,9 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             return None
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0 and (r.returncode < 0 or "Segmentation fault" in r.stderr):
+            # a compiler process that crashed (seen once under parallel builds) gets one more try
+            r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
         return r.stderr if verbose else None

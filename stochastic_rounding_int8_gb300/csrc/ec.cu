@@ -482,16 +482,6 @@ __global__ void __launch_bounds__(256) ec_xsum_kernel(EcXsumArgs A) {
     if (threadIdx.x == 0) A.counter[blockIdx.x] = 0;
 }
 
-// fp16 codes: the same sums streamed through shared memory.  One CTA per SM
-// walks the (column block, row chunk) items; TMA copies 64-row x 256-column
-// boxes (32 KiB) into a 4-stage ring while the warps accumulate the previous
-// ones (warp w takes rows w, w + 8, ... of a box, lane l columns 8l .. 8l+7;
-// the integer sums are exact in fp32: at most 256 * 127 per chunk).  Partials,
-// counters and the final fixed-order reduction as in ec_xsum_kernel.
-constexpr int kXsStages = 4, kXsBoxRows = 64;
-constexpr int kXsBoxBytes = kXsBoxRows * 256 * 2;
-constexpr int kXsSmem = kXsStages * kXsBoxBytes + 128 + 64;
-
 __device__ __forceinline__ bool xs_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = ec_gtime();
     while (true) {
@@ -506,162 +496,502 @@ __device__ __forceinline__ bool xs_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <int NJ, int ROWS>
+// ---------------------------------------------------------------------------
+// fp16 codes: the weight-side factors (rowsum, v) and the input-side factors
+// (xsum, p) of up to two linears in one persistent launch that streams every
+// code matrix through shared memory once.
+//
+// Work items, handed out in order by an atomic queue when the call has a
+// workspace (gemv items first, the larger ones), else strided over the CTAs:
+//   gemv (linear j, examples BCH g .. BCH g + BCH - 1, weight rows 32 rb ..
+//     32 rb + 31): boxes of 32 rows x 256 channels of W8_j, each with the
+//     matching BCH x 256 slab of colmean_j; warp w keeps rows w + 8 i (i < 4), lane l channels
+//     8 l .. 8 l + 7, and after the last box the lanes meet in a butterfly.
+//     The sums of codes are exact in fp32 (|sum| <= 127 N < 2^24).
+//   xsum (256-column block cb, chunk c of XR rows of X8): XR / 64 boxes of
+//     64 rows x 256 columns, each with the matching 64 entries of eps_j; warp
+//     w takes rows w + 8 i, lane l columns 8 l .. 8 l + 7; chunk partials go
+//     to the workspace and the last chunk of a column block (a counter, no
+//     waiting) adds them in a fixed order, one column per thread.
+// A TMA engine keeps kEsStages boxes in flight; a box's stage is refilled
+// once every thread has passed the next box's wait.  mu_b of every linear is
+// computed by each CTA in the same fixed order (the same bits everywhere).
+// ---------------------------------------------------------------------------
+constexpr int kEsStages = 5;
+constexpr int kEsXRowsBox = 64, kEsWRows = 32;
+constexpr int kEsCmOff = kEsWRows * 256 * 2;             // colmean slab after the 16 KiB of weight codes
+constexpr int kEsEpsOff = kEsXRowsBox * 256 * 2;         // eps slices after the 32 KiB of input codes
+constexpr int kEsStageBytes = kEsEpsOff + kMaxJobs * kEsXRowsBox * 4;
+constexpr int kEsQueue = 8;                              // item ids in flight per CTA
+constexpr int kEsMaxB = 1024;                            // examples whose mu a CTA holds
+
+struct EcStreamArgs {
+    int64_t T, K, N, S, B;
+    const float* eps[kMaxJobs];
+    float* mu[kMaxJobs];
+    int32_t* rowsum[kMaxJobs];
+    float* v[kMaxJobs];
+    int32_t* xsum[kMaxJobs];
+    float* p[kMaxJobs];
+    int32_t* xs;       // [nch, K]
+    float* ps;         // [NJ, nch, K]
+    int* counter;      // the work queue (null: static assignment)
+    int* done;         // grid barrier of the column-sum pass (null: no input-side items)
+    int64_t ncb, nch;  // column blocks and chunks of the input-side pass
+    int xr;            // rows per chunk (128, 256 or 512)
+    int64_t ngr;       // weight row blocks per linear
+    int ngroups;       // example groups of kEsBch
+    int64_t nbn;       // channel boxes per weight row block
+    int64_t n_gemv, n_items;
+    int mu_v4;         // eps 16-byte aligned and S % 4 == 0: vector loads for mu
+    int* d_status;
+};
+
+__device__ __forceinline__ void es_tma(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void es_tma1(uint32_t dst, const CUtensorMap* map, int32_t x, uint32_t bar) {
+    es_tma(dst, map, x, 0, bar);
+}
+
+// mu[b] = (1/S) sum_{t < S} e[b S + t] for every b < B over a 256-thread CTA
+// in a fixed order: per-thread strided sums, a butterfly in each warp, then
+// the eight warps in order.  red holds 64 floats.
+__device__ void cta_mu256(const float* e, int64_t S, int64_t B, float* red, float* out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b0 = 0; b0 < B; b0 += 8) {
+        float s[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s[q] = 0.0f;
+#pragma unroll 4
+        for (int64_t t = threadIdx.x; t < S; t += 256) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (b0 + q < B) s[q] += e[(b0 + q) * S + t];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s[q] += __shfl_xor_sync(0xFFFFFFFFu, s[q], o);
+            if (lane == 0) red[q * 8 + warp] = s[q];
+        }
+        __syncthreads();
+        if (threadIdx.x < 8 && b0 + threadIdx.x < B) {
+            float m = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) m += red[threadIdx.x * 8 + w];
+            out[b0 + threadIdx.x] = m / (float)S;
+        }
+        __syncthreads();
+    }
+}
+
+// V = 2^m values per lane (V <= 32) summed over the warp: a reduce-scatter
+// (halving exchanges) then plain exchanges, in a fixed order.  Returns, in
+// every lane, the full sum of value lane / (32 / V).
+template <int V>
+__device__ __forceinline__ float warp_scatter(const float (&v)[V]) {
+    const int lane = threadIdx.x & 31;
+    float a[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) a[i] = v[i];
+    int n = V;
+#pragma unroll
+    for (int x = 16; x >= 1; x >>= 1) {
+        if (n > 1) {
+            const int h = n / 2;
+            const bool hi = lane & x;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < h) {
+                    const float send = hi ? a[i] : a[i + h], keep = hi ? a[i + h] : a[i];
+                    a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, x);
+                }
+            }
+            n = h;
+        } else {
+            a[0] += __shfl_xor_sync(0xFFFFFFFFu, a[0], x);
+        }
+    }
+    return a[0];
+}
+
+// The same means from float4 loads (e 16-byte aligned, S a multiple of 4):
+// every load of eight examples is in flight at once.
+__device__ void cta_mu256_v4(const float* e, int64_t S, int64_t B, float* red, float* out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b0 = 0; b0 < B; b0 += 8) {
+        float s[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s[q] = 0.0f;
+#pragma unroll 2
+        for (int64_t i = 4 * threadIdx.x; i < S; i += 1024) {
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                v[q] = b0 + q < B ? __ldg(reinterpret_cast<const float4*>(e + (b0 + q) * S + i))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) s[q] += (v[q].x + v[q].y) + (v[q].z + v[q].w);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s[q] += __shfl_xor_sync(0xFFFFFFFFu, s[q], o);
+            if (lane == 0) red[q * 8 + warp] = s[q];
+        }
+        __syncthreads();
+        if (threadIdx.x < 8 && b0 + threadIdx.x < B) {
+            float m = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) m += red[threadIdx.x * 8 + w];
+            out[b0 + threadIdx.x] = m / (float)S;
+        }
+        __syncthreads();
+    }
+}
+
+template <int NJ, int BCH>
 __global__ void __launch_bounds__(256, 1)
-    ec_xsum_tma_kernel(const __grid_constant__ CUtensorMap tmX, EcXsumArgs A, int64_t ncb, int64_t nch,
-                       int* d_status) {
+    ec_stream_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmC0,
+                     const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmE0,
+                     const __grid_constant__ CUtensorMap tmE1, EcStreamArgs A) {
     constexpr int P = 33;
-    constexpr int NBOX = ROWS / kXsBoxRows;
-    extern __shared__ uint8_t xsm_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xsm_raw) + 127) & ~(uintptr_t)127);
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kXsStages * kXsBoxBytes);
+    extern __shared__ uint8_t es_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(es_raw) + 127) & ~(uintptr_t)127);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kEsStages * kEsStageBytes);   // copies landed
+    uint64_t* empty = full + kEsStages;                                                // all warps done
+    float* mu_s = reinterpret_cast<float*>(empty + kEsStages);   // [NJ][B]
     __shared__ float red_p[NJ][8][8 * P];
     __shared__ float red_x[8][8 * P];
+    __shared__ float mred[64];
+    __shared__ int q_item[kEsQueue];
     __shared__ int last;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t T = A.T, K = A.K;
-    const int64_t nitems = ncb * nch;
-    const int64_t my_items = (int64_t)blockIdx.x < nitems ? (nitems - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int64_t total = my_items * NBOX;   // boxes this CTA streams
-    auto box_item = [&](int64_t kk) { return (int64_t)blockIdx.x + (kk / NBOX) * gridDim.x; };
-    auto issue = [&](int64_t kk) {
-        const int64_t item = box_item(kk);
-        const int s = (int)(kk % kXsStages);
-        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(full + s);
-        const int32_t x = (int32_t)((item % ncb) * 256), y = (int32_t)((item / ncb) * ROWS + (kk % NBOX) * kXsBoxRows);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kXsBoxBytes) : "memory");
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-            ::"r"((uint32_t)__cvta_generic_to_shared(ring + s * kXsBoxBytes)), "l"((uint64_t)&tmX), "r"(x), "r"(y),
-            "r"(bar)
-            : "memory");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t K = A.K, B = A.B;
+    int* queue = A.counter;
+    const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(full);
+    const uint32_t ebar0 = (uint32_t)__cvta_generic_to_shared(empty);
+    // producer state (thread 0): the next item id (fetched one item ahead, so the
+    // queue's latency hides behind the copies), the current item decoded once,
+    // and the box of the next copy
+    const int n_items = (int)A.n_items, n_gemv = (int)A.n_gemv, ngr = (int)A.ngr, ncb = (int)A.ncb;
+    const int per_j = ngr * A.ngroups;
+    int p_fetched = 0;
+    auto fetch = [&]() -> int {
+        const int it = queue ? atomicAdd(queue, 1) : (int)blockIdx.x + p_fetched * (int)gridDim.x;
+        ++p_fetched;
+        return it < n_items ? it : -1;
     };
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kXsStages; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(full + i))
-                         : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
-    }
-    __syncthreads();
-    int64_t issued = 0;   // thread 0's count
-    if (threadIdx.x == 0)
-        for (; issued < kXsStages && issued < total; ++issued) issue(issued);
-    int64_t kk = 0;
-    bool ok = true;
-    for (int64_t k = 0; k < my_items && ok; ++k) {
-        const int64_t item = (int64_t)blockIdx.x + k * gridDim.x;
-        const int64_t cb = item % ncb, c = item / ncb;
-        float2 sx[4], sp[NJ][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            sx[i] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) sp[jj][i] = make_float2(0.f, 0.f);
-        }
-        for (int box = 0; box < NBOX; ++box, ++kk) {
-            const int s = (int)(kk % kXsStages);
-            // every thread waits; the CTA leaves together if any wait ran out
-            if (!__syncthreads_and(xs_wait((uint32_t)__cvta_generic_to_shared(full + s),
-                                           (uint32_t)((kk / kXsStages) & 1)))) {
-                if (threadIdx.x == 0 && d_status) *(volatile int*)d_status = S3R_ERR_TIMEOUT;
-                ok = false;
-                break;
-            }
-            const uint8_t* st = ring + s * kXsBoxBytes;
-            const int64_t tb = c * ROWS + box * kXsBoxRows;
-#pragma unroll
-            for (int i = 0; i < kXsBoxRows / 8; ++i) {
-                const int r = warp + 8 * i;
-                const int64_t t = tb + r;
-                const uint4 w = *reinterpret_cast<const uint4*>(st + (r * 256 + 8 * lane) * 2);
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-                float e[NJ];
-#pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) e[jj] = t < T ? __ldg(A.eps[jj] + t) : 0.0f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
-                    sx[q] = f2_add(sx[q], x);
-#pragma unroll
-                    for (int jj = 0; jj < NJ; ++jj) sp[jj][q] = f2_fma(x, make_float2(e[jj], e[jj]), sp[jj][q]);
-                }
-            }
-            __syncthreads();   // every thread is done with this stage
-            if (threadIdx.x == 0 && issued < total) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(issued);
+    int p_next = -1, p_box = 0, p_nbox = 0, p_ord = 0;
+    bool p_done = false, p_gemv = false;
+    const CUtensorMap *p_m0 = nullptr, *p_m1 = nullptr;
+    int32_t p_x = 0, p_y = 0, p_y1 = 0;
+    int issued = 0;   // boxes (and end marks) issued
+    auto issue_next = [&]() {
+        const int s = issued % kEsStages;
+        const uint32_t bar = bar0 + 8 * s;
+        uint8_t* dst = ring + s * kEsStageBytes;
+        if (p_box == p_nbox) {   // the next item, or the end mark
+            const int item = p_next;
+            q_item[p_ord % kEsQueue] = item;
+            ++p_ord;
+            p_box = 0;
+            if (item < 0) {
+                p_done = true;
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
                 ++issued;
+                return;
+            }
+            p_next = fetch();
+            p_gemv = item < n_gemv;
+            if (p_gemv) {
+                const int j = item / per_j, rem = item - j * per_j;
+                const int g = rem / ngr, rb = rem - g * ngr;
+                p_m0 = j ? &tmW1 : &tmW0;
+                p_m1 = j ? &tmC1 : &tmC0;
+                p_y = rb * kEsWRows;
+                p_y1 = g * BCH;
+                p_nbox = (int)A.nbn;
+            } else {
+                const int xi = item - n_gemv, c = xi / ncb, cb = xi - c * ncb;
+                p_x = cb * 256;
+                p_y = c * A.xr;
+                p_nbox = A.xr / kEsXRowsBox;
             }
         }
-        if (!ok) break;
-        // the chunk's column sums: warps meet in shared memory in warp order
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            red_x[warp][(2 * q) * P + lane] = sx[q].x;
-            red_x[warp][(2 * q + 1) * P + lane] = sx[q].y;
-#pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) {
-                red_p[jj][warp][(2 * q) * P + lane] = sp[jj][q].x;
-                red_p[jj][warp][(2 * q + 1) * P + lane] = sp[jj][q].y;
+        if (p_gemv) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kEsCmOff + BCH * 256 * 4)
+                         : "memory");
+            es_tma((uint32_t)__cvta_generic_to_shared(dst), p_m0, p_box * 256, p_y, bar);
+            es_tma((uint32_t)__cvta_generic_to_shared(dst + kEsCmOff), p_m1, p_box * 256, p_y1, bar);
+        } else {
+            const int32_t y = p_y + p_box * kEsXRowsBox;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                         "r"(kEsEpsOff + NJ * kEsXRowsBox * 4)
+                         : "memory");
+            es_tma((uint32_t)__cvta_generic_to_shared(dst), &tmX, p_x, y, bar);
+            es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff), &tmE0, y, bar);
+            if (NJ > 1) es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff + kEsXRowsBox * 4), &tmE1, y, bar);
+        }
+        ++p_box;
+        ++issued;
+    };
+    if (tid == 0) {
+        for (int i = 0; i < kEsStages; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * i) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(ebar0 + 8 * i) : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const CUtensorMap* maps[7] = {&tmX, &tmW0, &tmW1, &tmC0, &tmC1, &tmE0, &tmE1};
+        for (int i = 0; i < 7; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)maps[i]) : "memory");
+        p_next = fetch();
+    }
+    // mu_b of every linear (fixed order, the same bits in every CTA) while the first copies land
+    for (int j = 0; j < NJ; ++j) {
+        if (A.mu_v4) cta_mu256_v4(A.eps[j], A.S, B, mred, mu_s + j * B);
+        else cta_mu256(A.eps[j], A.S, B, mred, mu_s + j * B);
+    }
+    if (blockIdx.x == 0)
+        for (int j = 0; j < NJ; ++j)
+            for (int64_t b = tid; b < B; b += 256) A.mu[j][b] = mu_s[j * B + b];
+    // the ring fills once the means' loads are back (they would queue behind the copies)
+    if (tid == 0)
+        for (int i = 0; i < kEsStages && !p_done; ++i) issue_next();
+    __syncthreads();
+    int k = 0;        // boxes consumed
+    int ord = 0;      // items consumed
+    bool ok = true;   // every wait of this thread so far succeeded (after a failure it waits no more)
+    // Thread 0 refills the stage of box k - 1 as soon as every warp has left it
+    // (its empty barrier); then each thread waits for box k itself, so warps
+    // run ahead of each other within an item.  The CTA agrees on success at
+    // every item start (and before the column-sum counters).
+    auto wait_own = [&]() {
+        if (tid == 0 && k > 0 && !p_done && ok) {
+            const int q = k - 1;
+            if (xs_wait(ebar0 + 8 * (q % kEsStages), (uint32_t)((q / kEsStages) & 1))) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_next();
+            } else {
+                ok = false;
             }
         }
-        __syncthreads();
-        const int64_t kcol = cb * 256 + threadIdx.x;
-        const int slot = (threadIdx.x & 7) * P + (threadIdx.x >> 3);
-        if (kcol < K) {
-            float xb = 0.0f;
-            float a[NJ];
+        if (ok) ok = xs_wait(bar0 + 8 * (k % kEsStages), (uint32_t)((k / kEsStages) & 1));
+    };
+    // every warp marks the box it finished
+    auto box_done = [&]() {
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ebar0 + 8 * (k % kEsStages)) : "memory");
+        ++k;
+    };
+    bool failed = false;
+    while (true) {
+        wait_own();
+        if (!__syncthreads_and(ok)) { failed = true; break; }
+        const int item = q_item[ord % kEsQueue];
+        if (item < 0) { ++k; break; }   // the end mark (no copy behind it, no refill after it)
+        ++ord;
+        if (item < n_gemv) {
+            const int j = item / per_j, rem = item - j * per_j;
+            const int g = rem / ngr;
+            const int64_t rb = rem - g * ngr;
+            const float* mu_j = mu_s + j * B;
+            // accumulators over channel pairs (2e, 2e + 1), one per row and example
+            float2 acc[4][BCH], rs[4];
 #pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) a[jj] = 0.0f;
+            for (int i = 0; i < 4; ++i) {
+                rs[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                xb += red_x[w][slot];
-#pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][slot];
+                for (int q = 0; q < BCH; ++q) acc[i][q] = make_float2(0.0f, 0.0f);
             }
-            A.xs[c * K + kcol] = (int32_t)xb;
+            for (int bx = 0; bx < (int)A.nbn; ++bx) {
+                if (bx > 0) wait_own();
+                if (ok) {
+                    const uint8_t* st = ring + (k % kEsStages) * kEsStageBytes;
+                    // centered channel means of my 8 channels (past N and past B the copies read zero)
+                    float2 cm2[BCH][4];
 #pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) A.ps[(jj * nch + c) * K + kcol] = a[jj];
-        }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) last = atomicAdd(A.counter + cb, 1) == (int)nch - 1;
-        __syncthreads();
-        if (last && kcol < K) {
-            __threadfence();
-            // last chunk of this column block: thread = column, chunks in order per example
-            const int64_t B = A.B, cpe = B == 1 ? nch : A.S / ROWS;
-            float pk[NJ];
+                    for (int q = 0; q < BCH; ++q) {
+                        const int64_t b = (int64_t)g * BCH + q;
+                        const float m = b < B ? mu_j[b] : 0.0f;
+                        const float2 m2 = make_float2(m, m);
+                        const float4 c0 = *reinterpret_cast<const float4*>(st + kEsCmOff + (q * 256 + 8 * lane) * 4);
+                        const float4 c1 =
+                            *reinterpret_cast<const float4*>(st + kEsCmOff + (q * 256 + 8 * lane + 4) * 4);
+                        cm2[q][0] = f2_sub(make_float2(c0.x, c0.y), m2);
+                        cm2[q][1] = f2_sub(make_float2(c0.z, c0.w), m2);
+                        cm2[q][2] = f2_sub(make_float2(c1.x, c1.y), m2);
+                        cm2[q][3] = f2_sub(make_float2(c1.z, c1.w), m2);
+                    }
 #pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
-            for (int64_t b = 0; b < B; ++b) {
-                int xbi = 0;
-                float pb[NJ];
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(st + ((warp + 8 * i) * 256 + 8 * lane) * 2);
+                        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
-#pragma unroll 8
-                for (int64_t cc = b * cpe; cc < (b + 1) * cpe; ++cc) {
-                    xbi += __ldcg(A.xs + cc * K + kcol);
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x2 = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
+                            rs[i] = f2_add(rs[i], x2);
 #pragma unroll
-                    for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * nch + cc) * K + kcol);
+                            for (int q = 0; q < BCH; ++q) acc[i][q] = f2_fma(cm2[q][e], x2, acc[i][q]);
+                        }
+                    }
                 }
+                box_done();
+            }
+            // row sums: integers, one reduction each; v: a reduce-scatter of the 4 x BCH values,
+            // after which lane l holds value l / (32 / (4 BCH)) = (row, example) in row-major order
+            {
+                int ri[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ri[i] = __reduce_add_sync(0xFFFFFFFFu, (int)(rs[i].x + rs[i].y));
+                float vv[4 * BCH];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int q = 0; q < BCH; ++q) vv[i * BCH + q] = acc[i][q].x + acc[i][q].y;
+                const float vsum = warp_scatter<4 * BCH>(vv);
+                constexpr int G = 32 / (4 * BCH);   // lanes per value
+                const int vi = lane / G, i = vi / BCH, q = vi - i * BCH;
+                const int64_t kr = rb * kEsWRows + warp + 8 * i;
+                const int64_t b = (int64_t)g * BCH + q;
+                if (ok && lane % G == 0 && kr < K && b < B) A.v[j][b * K + kr] = vsum;
+                if (ok && lane < 4 && g == 0) {
+                    const int64_t kr2 = rb * kEsWRows + warp + 8 * lane;
+                    const int rsel = lane == 0 ? ri[0] : lane == 1 ? ri[1] : lane == 2 ? ri[2] : ri[3];
+                    if (kr2 < K) A.rowsum[j][kr2] = rsel;
+                }
+            }
+        } else {
+            const int xi = item - n_gemv;
+            const int64_t c = xi / ncb, cb = xi - c * ncb;
+            float2 sx[4], sp[NJ][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                sx[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) sp[jj][q] = make_float2(0.f, 0.f);
+            }
+            const int nb = A.xr / kEsXRowsBox;
+            for (int bx = 0; bx < nb; ++bx) {
+                if (bx > 0) wait_own();
+                if (ok) {
+                    const uint8_t* st = ring + (k % kEsStages) * kEsStageBytes;
+                    const float* es = reinterpret_cast<const float*>(st + kEsEpsOff);   // zero past T
+#pragma unroll
+                    for (int i = 0; i < kEsXRowsBox / 8; ++i) {
+                        const int r = warp + 8 * i;
+                        const uint4 w = *reinterpret_cast<const uint4*>(st + (r * 256 + 8 * lane) * 2);
+                        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                        float e[NJ];
+#pragma unroll
+                        for (int jj = 0; jj < NJ; ++jj) e[jj] = es[jj * kEsXRowsBox + r];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
+                            sx[q] = f2_add(sx[q], x);
+#pragma unroll
+                            for (int jj = 0; jj < NJ; ++jj)
+                                sp[jj][q] = f2_fma(x, make_float2(e[jj], e[jj]), sp[jj][q]);
+                        }
+                    }
+                }
+                box_done();
+            }
+            // the chunk's column sums: warps meet in shared memory in warp order
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                red_x[warp][(2 * q) * P + lane] = sx[q].x;
+                red_x[warp][(2 * q + 1) * P + lane] = sx[q].y;
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
-                    A.xsum[jj][b * K + kcol] = xbi;
-                    pk[jj] += pb[jj];
+                    red_p[jj][warp][(2 * q) * P + lane] = sp[jj][q].x;
+                    red_p[jj][warp][(2 * q + 1) * P + lane] = sp[jj][q].y;
                 }
             }
+            // every wait of the chunk succeeded, or the CTA leaves before touching the counters
+            if (!__syncthreads_and(ok)) { failed = true; break; }
+            const int64_t kcol = cb * 256 + tid;
+            const int slot = (tid & 7) * P + (tid >> 3);
+            if (kcol < K) {
+                float xb = 0.0f;
+                float a[NJ];
 #pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) A.p[jj][kcol] = pk[jj];
+                for (int jj = 0; jj < NJ; ++jj) a[jj] = 0.0f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    xb += red_x[w][slot];
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][slot];
+                }
+                A.xs[c * K + kcol] = (int32_t)xb;
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) A.ps[(jj * A.nch + c) * K + kcol] = a[jj];
+            }
+            // red_x and red_p are rewritten only after the next item start's barrier
         }
-        if (last && threadIdx.x == 0) A.counter[cb] = 0;
-        __syncthreads();   // red_* and `last` are reused by the next item
+    }
+    if (failed && tid == 0 && A.d_status) *(volatile int*)A.d_status = S3R_ERR_TIMEOUT;
+    if (A.done) {
+        // Every CTA of the (cooperative, co-resident) grid has written its chunk
+        // partials: meet at a grid barrier (one counter, bounded wait), then the
+        // CTAs share out the column blocks and add the chunks up in a fixed
+        // order, one column per thread.
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(A.done, 1);
+            const uint64_t t0 = ec_gtime();
+            bool met = false;
+            while (!met) {
+                int v;
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(A.done) : "memory");
+                met = v >= (int)gridDim.x;
+                if (!met && ec_gtime() - t0 > 2000000000ull) break;
+            }
+            last = met;
+            if (!met && A.d_status) *(volatile int*)A.d_status = S3R_ERR_TIMEOUT;
+        }
+        __syncthreads();
+        if (last) {
+            __threadfence();
+            const int64_t cpe = B == 1 ? A.nch : A.S / A.xr;
+            for (int64_t cb = blockIdx.x; cb < A.ncb; cb += gridDim.x) {
+                const int64_t kcol = cb * 256 + tid;
+                if (kcol >= K) continue;
+                float pk[NJ];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
+                for (int64_t b = 0; b < B; ++b) {
+                    int xbi = 0;
+                    float pb[NJ];
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
+#pragma unroll 16
+                    for (int64_t cc = b * cpe; cc < (b + 1) * cpe; ++cc) {
+                        xbi += __ldcg(A.xs + cc * K + kcol);
+#pragma unroll
+                        for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * A.nch + cc) * K + kcol);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) {
+                        A.xsum[jj][b * K + kcol] = xbi;
+                        pk[jj] += pb[jj];
+                    }
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) A.p[jj][kcol] = pk[jj];
+            }
+        }
     }
     // an early exit may leave copies in flight: wait for them before leaving
-    if (threadIdx.x == 0)
-        for (int64_t q = kk; q < issued; ++q)
-            xs_wait((uint32_t)__cvta_generic_to_shared(full + (q % kXsStages)), (uint32_t)((q / kXsStages) & 1));
+    if (tid == 0)
+        for (int q = k; q < issued; ++q) xs_wait(bar0 + 8 * (q % kEsStages), (uint32_t)((q / kEsStages) & 1));
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 ec_encode_fn() {
@@ -692,46 +1022,128 @@ static int ec_sm_count() {
     return n;
 }
 
-template <int NJ, int ROWS>
-static int launch_xsum_tma_t(const CUtensorMap& map, const EcXsumArgs& X, int64_t ncb, int64_t nch, int* d_status,
-                             cudaStream_t stream) {
+template <int NJ, int BCH>
+static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, size_t smem, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e =
-            cudaFuncSetAttribute(ec_xsum_tma_kernel<NJ, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXsSmem);
+        cudaError_t e = cudaFuncSetAttribute(ec_stream_kernel<NJ, BCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kEsStages * kEsStageBytes + 128 + 128 + kMaxJobs * kEsMaxB * 4));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
-            return s3r_cuda_fail("ec column sums: cudaFuncSetAttribute", e);
+            return s3r_cuda_fail("ec stream: cudaFuncSetAttribute", e);
         }
         attr = true;
     }
-    const int64_t items = ncb * nch;
-    const int64_t grid = std::min<int64_t>(items, ec_sm_count());
-    ec_xsum_tma_kernel<NJ, ROWS><<<(unsigned)grid, 256, kXsSmem, stream>>>(map, X, ncb, nch, d_status);
-    S3R_CHECK_LAUNCH();
+    int64_t grid = std::min<int64_t>(S.n_items, ec_sm_count());
+    if (!S.done) {
+        ec_stream_kernel<NJ, BCH><<<(unsigned)grid, 256, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                                          maps[5], maps[6], S);
+        S3R_CHECK_LAUNCH();
+        return S3R_OK;
+    }
+    // the column-sum pass ends with a grid barrier: a cooperative launch keeps every CTA resident
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ec_stream_kernel<NJ, BCH>, 256, smem) != cudaSuccess ||
+        per_sm < 1) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    grid = std::min<int64_t>(grid, (int64_t)per_sm * ec_sm_count());
+    EcStreamArgs a = S;
+    CUtensorMap m[7];
+    for (int i = 0; i < 7; ++i) m[i] = maps[i];
+    void* args[8] = {&m[0], &m[1], &m[2], &m[3], &m[4], &m[5], &m[6], &a};
+    const cudaError_t e = cudaLaunchCooperativeKernel((const void*)ec_stream_kernel<NJ, BCH>, dim3((unsigned)grid),
+                                                      dim3(256), args, smem, stream);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail("ec stream: cudaLaunchCooperativeKernel", e);
+    }
+    s3r_count_launch();
     return S3R_OK;
 }
 
-// fp16 codes X8 [T, K] with 16-byte aligned rows: the TMA column-sum kernel.
-// Returns 1 when it does not apply (the caller falls back to ec_xsum_kernel).
-static int launch_xsum_tma(const EcXsumArgs& X, int nj, bool wide, int64_t ncb, int64_t nch, int* d_status,
-                           cudaStream_t stream) {
+// fp16 codes with 16-byte aligned rows: rowsum, v, mu (and, two-way, xsum and
+// p) in one streaming launch.  Returns 1 when it does not apply.
+static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
+                            bool two, int32_t* xs, float* ps, int* counter, int* d_status, cudaStream_t stream) {
+    const int64_t B = T / S;
+    if (B > kEsMaxB || T >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return 1;
+    if (N % 8 != 0 || (two && K % 8 != 0)) return 1;
+    for (int j = 0; j < nj; ++j)
+        if (!s3r_aligned16(jobs[j].W8) || !s3r_aligned16(jobs[j].colmean) || (two && !s3r_aligned16(jobs[j].eps)))
+            return 1;
+    if (two && !s3r_aligned16(X8)) return 1;
     auto fn = ec_encode_fn();
-    if (!fn || X.T >= (int64_t(1) << 31) || X.K >= (int64_t(1) << 31)) return 1;
-    CUtensorMap map;
-    const cuuint64_t dims[2] = {(cuuint64_t)X.K, (cuuint64_t)X.T};
-    const cuuint64_t strides[1] = {(cuuint64_t)X.K * 2};
-    const cuuint32_t box[2] = {256, (cuuint32_t)kXsBoxRows};
+    if (!fn) return 1;
+    const int bch = B == 1 ? 1 : (B <= 4 ? 4 : 8);
+    CUtensorMap maps[7];
     const cuuint32_t estr[2] = {1, 1};
-    // rows and columns past the end read as zero
-    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X.X8), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return 1;
-    if (wide) return nj == 2 ? launch_xsum_tma_t<2, 256>(map, X, ncb, nch, d_status, stream)
-                             : launch_xsum_tma_t<1, 256>(map, X, ncb, nch, d_status, stream);
-    return nj == 2 ? launch_xsum_tma_t<2, 128>(map, X, ncb, nch, d_status, stream)
-                   : launch_xsum_tma_t<1, 128>(map, X, ncb, nch, d_status, stream);
+    auto enc2 = [&](CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                    uint64_t pitch_bytes, uint32_t bc, uint32_t br) {
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+        const cuuint32_t box[2] = {bc, br};
+        return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    // a vector as one row of a 2-D map (entries past n read as zero)
+    auto enc1 = [&](CUtensorMap* m, const float* base, uint64_t n) {
+        return enc2(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, n, 1, (n * 4 + 15) / 16 * 16, kEsXRowsBox, 1);
+    };
+    for (int j = 0; j < nj; ++j) {
+        if (!enc2(&maps[1 + j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, jobs[j].W8, N, K, N * 2, 256, kEsWRows) ||
+            !enc2(&maps[3 + j], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, jobs[j].colmean, N, B, N * 4, 256, bch))
+            return 1;
+        if (two && !enc1(&maps[5 + j], jobs[j].eps, T)) return 1;
+    }
+    if (two) {
+        if (!enc2(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X8, K, T, K * 2, 256, kEsXRowsBox)) return 1;
+    } else {
+        maps[0] = maps[1];   // not read without input-side items
+        maps[5] = maps[1];
+    }
+    if (nj == 1) {
+        maps[2] = maps[1];
+        maps[4] = maps[3];
+        maps[6] = maps[5];
+    }
+    if (!two) maps[6] = maps[5];
+    EcStreamArgs A{};
+    A.T = T; A.K = K; A.N = N; A.S = S; A.B = B;
+    for (int j = 0; j < nj; ++j) {
+        A.eps[j] = jobs[j].eps;
+        A.mu[j] = jobs[j].mu;
+        A.rowsum[j] = jobs[j].rowsum;
+        A.v[j] = jobs[j].v;
+        A.xsum[j] = jobs[j].xsum;
+        A.p[j] = jobs[j].p;
+    }
+    A.xs = xs; A.ps = ps;
+    A.counter = two ? counter + s3r_cdiv(K, 256) : nullptr;   // after the column-block counters of the other path
+    A.done = two ? A.counter + 1 : nullptr;
+    A.xr = (B == 1 || S % 512 == 0) ? 512 : (S % 256 == 0 ? 256 : 128);
+    A.ncb = s3r_cdiv(K, 256);
+    A.nch = s3r_cdiv(T, A.xr);
+    A.ngr = s3r_cdiv(K, kEsWRows);
+    A.ngroups = (int)s3r_cdiv(B, bch);
+    A.nbn = s3r_cdiv(N, 256);
+    A.n_gemv = nj * A.ngr * A.ngroups;
+    A.n_items = A.n_gemv + (two ? A.ncb * A.nch : 0);
+    A.d_status = d_status;
+    A.mu_v4 = S % 4 == 0;
+    for (int j = 0; j < nj; ++j) A.mu_v4 = A.mu_v4 && s3r_aligned16(jobs[j].eps);
+    if (A.n_items >= (int64_t(1) << 30)) return 1;
+    const size_t smem = kEsStages * kEsStageBytes + 128 + 128 + (size_t)nj * B * 4;
+    if (nj == 2) {
+        if (bch == 1) return launch_ec_stream_t<2, 1>(maps, A, smem, stream);
+        if (bch == 4) return launch_ec_stream_t<2, 4>(maps, A, smem, stream);
+        return launch_ec_stream_t<2, 8>(maps, A, smem, stream);
+    }
+    if (bch == 1) return launch_ec_stream_t<1, 1>(maps, A, smem, stream);
+    if (bch == 4) return launch_ec_stream_t<1, 4>(maps, A, smem, stream);
+    return launch_ec_stream_t<1, 8>(maps, A, smem, stream);
 }
 
 // Workspace of the column-sum pass for `njobs` linears sharing X8 [T, K].
@@ -786,11 +1198,15 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
             M.colmean[j] = jobs[j].colmean;
         }
         M.T = T; M.N = N; M.S = S; M.ntc = ntc; M.ntr = ntr;
-        M.counter = (two && vec_x) ? counter : nullptr;
-        M.ncounter = (int)ncb;
+        M.counter = two ? counter : nullptr;
+        M.ncounter = (int)ncb + 2;   // the column blocks, then the streaming kernel's work queue and grid barrier
         dim3 grid((unsigned)s3r_cdiv(T + B * N, 256), (unsigned)nj);
         ec_means_kernel<<<grid, 256, 0, stream>>>(M);
         S3R_CHECK_LAUNCH();
+    }
+    if (ec_mode != S3R_EC_NONE && K > 0 && sizeof(CodeT) == 2) {
+        const int st = launch_ec_stream(jobs, nj, T, N, S, K, X8, two, xs, ps, counter, d_status, stream);
+        if (st <= 0) return st;   // launched (0) or failed (< 0); 1: the kernels below
     }
     if (ec_mode == S3R_EC_NONE || K == 0 || !vec_w) {
         for (int j = 0; j < nj; ++j) {
@@ -848,10 +1264,6 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
         // 256-row chunks where the examples allow it (chunks never straddle two)
         const bool wide = B == 1 || S % 256 == 0;
         const int64_t nchw = s3r_cdiv(T, wide ? 256 : 128);
-        if (sizeof(CodeT) == 2) {
-            int st = launch_xsum_tma(X, nj, wide, ncb, nchw, d_status, stream);
-            if (st <= 0) return st;   // launched (0) or failed (< 0); 1: fall through
-        }
         dim3 grid((unsigned)ncb, (unsigned)nchw);
         if (wide) {
             if (nj == 2) ec_xsum_kernel<CodeT, 2, 256><<<grid, 256, 0, stream>>>(X);

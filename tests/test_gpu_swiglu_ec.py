@@ -101,3 +101,27 @@ def test_ec_factors_repeat_bit_identical(s3r, fmt):
     for r in runs[1:]:
         for f in ("eps", "mu", "colmean", "rowsum", "v", "xsum", "p"):
             assert torch.equal(getattr(r, f), getattr(runs[0], f)), f
+
+
+def test_streaming_paths_are_taken(s3r):
+    """With fp16 codes and 16-byte aligned rows the quantizers run as one
+    persistent launch each and the correction factors as two (the means, then
+    one pass over W8 and X8); the counter sees every kernel the library starts."""
+    rng = np.random.default_rng(11)
+    T, N, K, S = 1024, 512, 264, 256
+    G = torch.from_numpy((rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)).to(torch.bfloat16).cuda()
+    W8 = torch.from_numpy(rng.integers(-127, 128, size=(K, N)).astype(np.float16)).cuda()
+    X8 = torch.from_numpy(rng.integers(-127, 128, size=(T, K)).astype(np.float16)).cuda()
+    n0 = s3r.kernel_launch_count()
+    q = s3r.s3r_quantize(G, seed=1, tensor_id=3, code_format=s3r.CODES_F16)
+    n1 = s3r.kernel_launch_count()
+    s3r.s3r_ec_correct(q, T, N, S, W8, X8, ec_mode=s3r.EC_TWO_WAY)
+    n2 = s3r.kernel_launch_count()
+    s3r.s3r_ec_correct(q, T, N, S, W8, X8, ec_mode=s3r.EC_DX_ONLY)
+    n3 = s3r.kernel_launch_count()
+    dA, h1, h3, s_x, s_w1, s_w3 = _swiglu_case(256, 384, 2)
+    c = lambda a: torch.from_numpy(a).cuda()
+    s3r.swiglu_quantize(c(dA), h1.cuda(), h3.cuda(), c(s_x), c(s_w1), c(s_w3), code_format=s3r.CODES_F16)
+    n4 = s3r.kernel_launch_count()
+    torch.cuda.synchronize()
+    assert (n1 - n0, n2 - n1, n3 - n2, n4 - n3) == (1, 2, 2, 1)
