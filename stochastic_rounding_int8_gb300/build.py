@@ -49,23 +49,38 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
     extra = list(extra or [])
 
+    def run(src, obj):
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+        return subprocess.run(cmd, capture_output=True, text=True)
+
+    def crashed(r):
+        return r.returncode < 0 or "Segmentation fault" in r.stderr
+
     def compile_one(pair):
         src, obj = pair
         if not force and not _stale(obj, src, headers):
             return None
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0 and (r.returncode < 0 or "Segmentation fault" in r.stderr):
-            # a compiler process that crashed (seen once under parallel builds) gets one more try
-            r = subprocess.run(cmd, capture_output=True, text=True)
+        return pair, run(src, obj)
+
+    retry = []
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        for res in ex.map(compile_one, zip(srcs, objs)):
+            if res is None:
+                continue
+            (src, obj), r = res
+            if r.returncode != 0 and crashed(r):
+                retry.append((src, obj))   # a compiler process that crashed under the parallel build
+            elif r.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+            elif verbose and r.stderr:
+                sys.stderr.write(r.stderr)
+    for src, obj in retry:   # one at a time, with nothing else compiling
+        for _ in range(2):
+            r = run(src, obj)
+            if r.returncode == 0 or not crashed(r):
+                break
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
-        return r.stderr if verbose else None
-
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        for msg in ex.map(compile_one, zip(srcs, objs)):
-            if msg:
-                sys.stderr.write(msg)
     if force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
