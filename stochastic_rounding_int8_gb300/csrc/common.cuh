@@ -156,6 +156,13 @@ __device__ __forceinline__ float lt_one(float a, float b) {
     asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
+// per bf16 half: a value whose magnitude is max(|a|, |b|) (NaN if either is NaN); the
+// sign bit is the xor of the inputs' and carries no meaning here
+__device__ __forceinline__ uint32_t bf16x2_absmax_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 // max(m, |a|, |b|), NaN if any of them is NaN
 __device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
     float d;

@@ -340,7 +340,8 @@ __device__ __forceinline__ void tile_scales(uint32_t amax_bits, float& d, float&
     inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amx);
 }
 
-// Round RPT rows of 8 values (rows RS apart) to codes and store them; with
+// Round RPT rows of 8 values (rows RS apart; gpair(j, q) gives values 2q and
+// 2q + 1 of row j) to codes and store them; with
 // ERR, add -e = g - delta*q (one rounding: the exact negation of delta*q - g)
 // into the row sums and the per-column sums.
 //   SR: q = floor(y) + [u < frac(y)] = ceil(y - u) for u in [0, 1).  y - u
@@ -348,10 +349,10 @@ __device__ __forceinline__ void tile_scales(uint32_t amax_bits, float& d, float&
 //   kMagic rounded up takes it: m = kMagic + q, exact.  RTNE: m = kMagic + y
 //   rounded to nearest.  The int8 code is the low byte of m's bits.
 // q0 points at my first row's 8 codes; rows_left: row j is stored iff RS j < rows_left.
-template <int MODE, int FMT, int RPT, int RS, bool ERR>
-__device__ __forceinline__ void round_rows(const float (&g)[RPT][8], float d, float inv, bool nonfinite,
-                                           const float* u0, int u_step, void* q0, int64_t row_step, int rows_left,
-                                           int64_t t_first, int nc0, int64_t N, uint32_t seed_lo, uint32_t tensor_id,
+template <int MODE, int FMT, int RPT, int RS, bool ERR, typename PairFn>
+__device__ __forceinline__ void round_rows(PairFn gpair, float d, float inv, bool nonfinite, const float* u0,
+                                           int u_step, void* q0, int64_t row_step, int rows_left, int64_t t_first,
+                                           int nc0, int64_t N, uint32_t seed_lo, uint32_t tensor_id,
                                            float (&rsum)[RPT], float2 (&colsum)[4]) {
     const float2 M2 = make_float2(kMagic, kMagic), inv2 = make_float2(inv, inv), nd2 = make_float2(-d, -d);
 #pragma unroll
@@ -385,7 +386,7 @@ __device__ __forceinline__ void round_rows(const float (&g)[RPT][8], float d, fl
         if (!nonfinite) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float2 g2 = make_float2(g[j][2 * q], g[j][2 * q + 1]);
+                const float2 g2 = gpair(j, q);   // values 8 c + 2 q, 8 c + 2 q + 1 of row j
                 const float2 y = f2_mul(g2, inv2);   // |y| <= 127
                 float2 m;
                 if (MODE == kRTNE) {
@@ -573,10 +574,25 @@ __global__ void __launch_bounds__(256, 2)
             if (tid == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
             break;
         }
-        // pass 1: fold g = (s_x * G) * s_w and absmax
-        float g[RPT][8];
+        // pass 1: fold g = (s_x * G) * s_w and absmax.  Unscaled input keeps the raw bf16
+        // pairs (half the registers) and takes the absmax two at a time in bf16: the
+        // magnitude max of a pair of bf16 values is exact, and bf16 -> fp32 is exact.
+        float g[FOLD ? RPT : 1][8];
+        uint32_t rw[FOLD ? 1 : RPT][4];
         float amax = 0.0f;   // NaN-propagating
-        {
+        if (!FOLD) {
+            const uint16_t* tb = reinterpret_cast<const uint16_t*>(qsmem + s * kQTileBytes);
+            uint32_t m2 = 0u;   // |max| per bf16 half (the sign bits are not used)
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(tb + (r0 + RS * j) * kTile + 8 * c);
+                rw[FOLD ? 0 : j][0] = raw.x; rw[FOLD ? 0 : j][1] = raw.y;
+                rw[FOLD ? 0 : j][2] = raw.z; rw[FOLD ? 0 : j][3] = raw.w;
+                m2 = bf16x2_absmax_nan(m2, bf16x2_absmax_nan(raw.x, raw.y));
+                m2 = bf16x2_absmax_nan(m2, bf16x2_absmax_nan(raw.z, raw.w));
+            }
+            amax = max3_abs_nan(0.0f, bf16_lo(m2), bf16_hi(m2));
+        } else {
             float sw[8];
             if (FOLD) {
                 const float4 w0 = *reinterpret_cast<const float4*>(&sw_s[sl][8 * c]);
@@ -599,8 +615,8 @@ __global__ void __launch_bounds__(256, 2)
                         v = f2_mul(v, make_float2(sx, sx));
                         v = f2_mul(v, make_float2(sw[2 * q], sw[2 * q + 1]));
                     }
-                    g[j][2 * q] = v.x;
-                    g[j][2 * q + 1] = v.y;
+                    g[FOLD ? j : 0][2 * q] = v.x;
+                    g[FOLD ? j : 0][2 * q + 1] = v.y;
                     amax = max3_abs_nan(amax, v.x, v.y);
                 }
             }
@@ -630,8 +646,13 @@ __global__ void __launch_bounds__(256, 2)
         float rsum[RPT];
         void* q0 = FMT == 0 ? (void*)(static_cast<int8_t*>(O.Q) + (t0 + r0) * C.N + nc0)
                             : (void*)(static_cast<__half*>(O.Q) + (t0 + r0) * C.N + nc0);
-        round_rows<MODE, FMT, RPT, RS, ERR>(g, d, inv, nonfinite, &xu_s[sl][r0].y, 2 * RS, q0, row_step, rows_left,
-                                            t0 + r0, nc0, C.N, C.seed_lo, O.tensor_id, rsum, colsum);
+        auto gpair = [&](int j, int q) -> float2 {
+            if (FOLD) return make_float2(g[FOLD ? j : 0][2 * q], g[FOLD ? j : 0][2 * q + 1]);
+            const uint32_t w = rw[FOLD ? 0 : j][q];
+            return make_float2(bf16_lo(w), bf16_hi(w));
+        };
+        round_rows<MODE, FMT, RPT, RS, ERR>(gpair, d, inv, nonfinite, &xu_s[sl][r0].y, 2 * RS, q0, row_step,
+                                            rows_left, t0 + r0, nc0, C.N, C.seed_lo, O.tensor_id, rsum, colsum);
         if (ERR && O.tok) {
             const float r = scatter_rows16<RPT>(rsum, c);   // row r0 + 16 (c >> 1)
             if ((c & 1) == 0 && RS * (c >> 1) < rows_left) O.tok[(t0 + r0 + RS * (c >> 1)) * ntc + cb] = -r;
@@ -1020,7 +1041,10 @@ __global__ void __launch_bounds__(512, 1)
             float2 colsum[4];
             float rsum[RPT];
             void* q0 = FMT == 0 ? (void*)(static_cast<int8_t*>(O.Q) + off) : (void*)(static_cast<__half*>(O.Q) + off);
-            round_rows<MODE, FMT, RPT, RS, ERR>(o ? g3 : g1, o ? d3s : d1s, o ? inv3 : inv1, o ? nf3 : nf1,
+            auto gpair = [&](int j, int q) -> float2 {
+                return o ? make_float2(g3[j][2 * q], g3[j][2 * q + 1]) : make_float2(g1[j][2 * q], g1[j][2 * q + 1]);
+            };
+            round_rows<MODE, FMT, RPT, RS, ERR>(gpair, o ? d3s : d1s, o ? inv3 : inv1, o ? nf3 : nf1,
                                                 o ? &xs_s[sl][r0].z : &xs_s[sl][r0].y, 4 * RS, q0, row_step,
                                                 rows_left, t0 + r0, nc0, C.N, C.seed_lo, O.tensor_id, rsum, colsum);
             if (ERR && O.tok) {
