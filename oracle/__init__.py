@@ -29,8 +29,9 @@ _LIB_PATH = os.path.join(_HERE, "liborc_s3r.so")
 _lock = threading.Lock()
 _lib = None
 
-RTNE, S3R, INDEP = 0, 1, 2
-EC_NONE, EC_DX_ONLY, EC_TWO_WAY, EC_DX_TOKEN_ONLY = 0, 1, 2, 3
+RTNE, S3R, INDEP, S3R7, BCAST = 0, 1, 2, 3, 4
+EC_NONE, EC_DX_ONLY, EC_TWO_WAY, EC_DX_TOKEN_ONLY, EC_DW_ONLY = 0, 1, 2, 3, 4
+SHARED = (S3R, S3R7, BCAST)   # modes with one threshold tensor for both products
 TILE = 128
 
 
@@ -56,6 +57,11 @@ def lib():
             L.orc_token_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
             L.orc_element_threshold.restype = C.c_float
             L.orc_element_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
+            L.orc_token_threshold7.restype = C.c_float
+            L.orc_token_threshold7.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
+            L.orc_example_threshold.restype = C.c_float
+            L.orc_example_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
+            L.orc_quantize_window_ex.restype = C.c_int
             L.orc_inv127_rz.restype = C.c_float
             L.orc_inv127_rz.argtypes = [C.c_float]
             L.orc_sr_step.restype = C.c_float
@@ -102,6 +108,16 @@ def token_threshold(t: int, seed: int, tensor_id: int) -> float:
     return lib().orc_token_threshold(int(t), int(seed), int(tensor_id))
 
 
+def token_threshold7(t: int, seed: int, tensor_id: int) -> float:
+    """[S3R] §III-B: 7-bit threshold of token t (byte t mod 4 of the word of t / 4, half-step shift)."""
+    return lib().orc_token_threshold7(int(t), int(seed), int(tensor_id))
+
+
+def example_threshold(b: int, seed: int, tensor_id: int) -> float:
+    """[S3R] §III-B, Phi_bcast: the threshold shared by every element of example b."""
+    return lib().orc_example_threshold(int(b), int(seed), int(tensor_id))
+
+
 def element_threshold(e: int, seed: int, tensor_id: int) -> float:
     return lib().orc_element_threshold(int(e), int(seed), int(tensor_id))
 
@@ -138,11 +154,12 @@ def sigmoidf(x: float) -> float:
     return lib().orc_sigmoidf(float(x))
 
 
-def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, TILE), window=None):
+def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, TILE), window=None, S=0):
     """Fold, tile-scale and round G (float32 [T, N]).
 
     window = (row_base, col_base, n_global) treats G as a tile-aligned window
-    of a larger tensor (thresholds use global indices).
+    of a larger tensor (thresholds use global indices).  S: tokens per example
+    (Phi_bcast; 0 = one example).  tile=(T, N) gives the paper's per-tensor step.
     Returns (Q int8 [T,N], delta f32 [ceil(T/tr), ceil(N/tc)], E f32 [T,N], status)."""
     G = _f32(G)
     T, N = G.shape
@@ -152,9 +169,9 @@ def quantize(G, s_x=None, s_w=None, mode=S3R, seed=0, tensor_id=0, tile=(TILE, T
     delta = np.zeros((ntr, ntc), dtype=np.float32)
     E = np.zeros((T, N), dtype=np.float32)
     rb, cb, ng = window if window is not None else (0, 0, N)
-    st = lib().orc_quantize_window(_p(G), _i64(T), _i64(N), _i64(N), _p(_f32(s_x)), _p(_f32(s_w)), C.c_int(mode),
-                                   C.c_uint64(seed), C.c_uint32(tensor_id), _i64(tr), _i64(tc), _p(Q), _p(delta),
-                                   _p(E), _i64(rb), _i64(cb), _i64(ng))
+    st = lib().orc_quantize_window_ex(_p(G), _i64(T), _i64(N), _i64(N), _p(_f32(s_x)), _p(_f32(s_w)),
+                                      C.c_int(mode), _i64(S), C.c_uint64(seed), C.c_uint32(tensor_id), _i64(tr),
+                                      _i64(tc), _p(Q), _p(delta), _p(E), _i64(rb), _i64(cb), _i64(ng))
     return Q, delta, E, st
 
 
@@ -311,16 +328,16 @@ def linear_backward(G, X8, s_x, W8, s_w, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0
     K = W8.shape[0]
     rows = np.arange(T) if rows is None else np.asarray(rows)
     krows = np.arange(K) if krows is None else np.asarray(krows)
-    Q, delta, E, st = quantize(G, s_x, s_w, mode, seed, tensor_id, tile)
+    Q, delta, E, st = quantize(G, s_x, s_w, mode, seed, tensor_id, tile, S=S)
     out = LinearBackward(Q=Q, delta=delta, E=E, status=st)
-    use_ec = mode == S3R and ec_mode != EC_NONE
+    use_ec = mode in SHARED and ec_mode != EC_NONE
     if mode == INDEP:
         Qr, dr, _, st2 = quantize(G, s_x, s_w, INDEP, seed, tensor_id + RHS_ID_OFFSET, tile)
         out.Q_rhs, out.delta_rhs, out.status = Qr, dr, st or st2
     if use_ec:
         out.eps, out.colmean, out.mu = error_stats(E, S)
         out.rowsum, out.v, out.xsum, out.p = ec_factors(out.eps, out.colmean, out.mu, S, W8,
-                                                        X8 if ec_mode == EC_TWO_WAY else None)
+                                                        X8 if ec_mode in (EC_TWO_WAY, EC_DW_ONLY) else None)
     em = ec_mode if use_ec else EC_NONE
     out.dX = dx(Q, delta, W8, s_x, em, out.eps, out.rowsum, out.v, S, rows, tile)
     Qw = out.Q_rhs if mode == INDEP else Q

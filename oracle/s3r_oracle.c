@@ -39,12 +39,15 @@
 #define ORC_RTNE 0
 #define ORC_S3R 1   /* one threshold per token, shared by its channels (Phi_2D) */
 #define ORC_INDEP 2 /* one threshold per element */
+#define ORC_S3R7 3  /* Phi_2D with 7-bit thresholds, four per word, shifted by half a step */
+#define ORC_BCAST 4 /* one threshold per example, shared by all its tokens and channels (Phi_bcast) */
 
 /* error-correction modes */
 #define ORC_EC_NONE 0
 #define ORC_EC_DX_ONLY 1     /* full activation-gradient term of the projection */
 #define ORC_EC_TWO_WAY 2     /* both products */
 #define ORC_EC_DX_TOKEN_ONLY 3 /* alternative reading: token-mean term eps*r only */
+#define ORC_EC_DW_ONLY 4     /* ablation: the weight-gradient term only */
 
 /* ------------------------------------------------------------------------- */
 /* Philox4x32-10 [PHX]: 10 rounds of the Philox S-box on a 4x32-bit counter   */
@@ -81,6 +84,34 @@ float orc_word_to_unit(uint32_t w) {
  * key = (low 32 bits of seed, tensor id); the threshold is output word 0. */
 float orc_token_threshold(uint64_t t, uint64_t seed, uint32_t tensor_id) {
     uint32_t ctr[4] = {(uint32_t)t, (uint32_t)(t >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, tensor_id};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return orc_word_to_unit(out[0]);
+}
+
+/* [S3R] §III-B "Structured subspace randomness": the paper's own thresholds
+ * are 7-bit values, four cut from each 32-bit word, on a grid shifted by half
+ * a step.  Token t takes byte (t mod 4) of output word 0 of Philox(counter =
+ * t / 4); of that byte the upper 7 bits k give u = (k + 1/2) / 128, so u takes
+ * the 128 values 1/256, 3/256, ..., 255/256 and P(u < p) differs from p by at
+ * most 1/256 (the pages' bound Delta/256 on the bias). */
+float orc_token_threshold7(uint64_t t, uint64_t seed, uint32_t tensor_id) {
+    uint64_t c = t >> 2;
+    uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, tensor_id};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    uint32_t byte = (out[0] >> (8u * (uint32_t)(t & 3u))) & 0xFFu;
+    return ((float)(byte >> 1) + 0.5f) / 128.0f;
+}
+
+/* [S3R] §III-B, Phi_bcast (the ablation): one threshold u_b per example b,
+ * shared by all its tokens and channels.  Counter = (b, 0, 1, 0) (counter
+ * word 2 = 1 keeps these draws apart from the per-token ones), same key and
+ * 24-bit grid as Phi_2D. */
+float orc_example_threshold(uint64_t b, uint64_t seed, uint32_t tensor_id) {
+    uint32_t ctr[4] = {(uint32_t)b, (uint32_t)(b >> 32), 1u, 0u};
     uint32_t key[2] = {(uint32_t)seed, tensor_id};
     uint32_t out[4];
     orc_philox4x32_10(ctr, key, out);
@@ -155,12 +186,15 @@ static float fold_one(const float* G, int64_t ldg, const float* s_x, const float
  * whose first row is global token row_base and first column is col_base, in a
  * tensor of n_global columns; only the threshold indices use these (token
  * t + row_base; element (t + row_base) * n_global + col_base + n). */
-int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
-                        const float* s_x, const float* s_w, int mode, uint64_t seed, uint32_t tensor_id,
-                        int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E,
-                        int64_t row_base, int64_t col_base, int64_t n_global) {
+/* S is the number of tokens per example (Phi_bcast: example of token t is
+ * t / S; S <= 0 means one example). */
+int orc_quantize_window_ex(const float* G, int64_t T, int64_t N, int64_t ldg,
+                           const float* s_x, const float* s_w, int mode, int64_t S, uint64_t seed,
+                           uint32_t tensor_id, int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E,
+                           int64_t row_base, int64_t col_base, int64_t n_global) {
     if (T < 0 || N < 0 || tr <= 0 || tc <= 0 || ldg < N) return ORC_ERR_ARG;
-    if (mode != ORC_RTNE && mode != ORC_S3R && mode != ORC_INDEP) return ORC_ERR_ARG;
+    if (mode != ORC_RTNE && mode != ORC_S3R && mode != ORC_INDEP && mode != ORC_S3R7 && mode != ORC_BCAST)
+        return ORC_ERR_ARG;
     int status = ORC_OK;
     int64_t ntr = (T + tr - 1) / tr, ntc = (N + tc - 1) / tc;
     for (int64_t i = 0; i < ntr; ++i) {
@@ -190,7 +224,11 @@ int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
             float inv = (amax > 0.0f) ? orc_inv127_rz(amax) : 0.0f;
             delta[i * ntc + j] = d;
             for (int64_t t = t0; t < t1; ++t) {
-                float u_tok = (mode == ORC_S3R) ? orc_token_threshold((uint64_t)(t + row_base), seed, tensor_id) : 0.0f;
+                const uint64_t tg = (uint64_t)(t + row_base);
+                float u_tok = 0.0f;
+                if (mode == ORC_S3R) u_tok = orc_token_threshold(tg, seed, tensor_id);
+                else if (mode == ORC_S3R7) u_tok = orc_token_threshold7(tg, seed, tensor_id);
+                else if (mode == ORC_BCAST) u_tok = orc_example_threshold(S > 0 ? tg / (uint64_t)S : 0u, seed, tensor_id);
                 for (int64_t n = n0; n < n1; ++n) {
                     float g = fold_one(G, ldg, s_x, s_w, t, n);
                     float y = g * inv;
@@ -198,7 +236,7 @@ int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
                     if (mode == ORC_RTNE) {
                         qf = nearbyintf(y);
                     } else {
-                        float u = (mode == ORC_S3R)
+                        float u = (mode != ORC_INDEP)
                                       ? u_tok
                                       : orc_element_threshold((uint64_t)((t + row_base) * n_global + col_base + n),
                                                               seed, tensor_id);
@@ -213,6 +251,14 @@ int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
         }
     }
     return status;
+}
+
+int orc_quantize_window(const float* G, int64_t T, int64_t N, int64_t ldg,
+                        const float* s_x, const float* s_w, int mode, uint64_t seed, uint32_t tensor_id,
+                        int64_t tr, int64_t tc, int8_t* Q, float* delta, float* E,
+                        int64_t row_base, int64_t col_base, int64_t n_global) {
+    return orc_quantize_window_ex(G, T, N, ldg, s_x, s_w, mode, 0, seed, tensor_id, tr, tc, Q, delta, E, row_base,
+                                  col_base, n_global);
 }
 
 int orc_quantize(const float* G, int64_t T, int64_t N, int64_t ldg,
@@ -395,7 +441,7 @@ void orc_dx(const int8_t* Q, const float* delta, const int8_t* W8, int64_t T, in
 
 /* Weight gradient ([S3R] §III-A, §III-D), for the requested rows k of dW [K, N]:
  *   acc[k,n] = sum_tb delta[tb, n/tc] * J[k, n, tb]
- *   corr     = sum_b xsum[b,k] (colmean[b,n] - mu[b]) + p[k]   (EC_TWO_WAY only)
+ *   corr     = sum_b xsum[b,k] (colmean[b,n] - mu[b]) + p[k]   (EC_TWO_WAY, EC_DW_ONLY)
  *   dW[k,n]  = (acc - corr) / s_w[n]                            (s_w NULL = 1)
  * The contraction blocks are the tile rows of Q (blk = tr).  dW is the sum
  * X^T G, not divided by the token count ([S3R] §III-A leaves 1/(BS) to the
@@ -412,7 +458,7 @@ void orc_dw(const int8_t* X8, const int8_t* Q, const float* delta, int64_t T, in
             double acc = 0.0;
             for (int64_t tb = 0; tb < ntb; ++tb) acc += (double)delta[tb * ntc + n / tc] * (double)J[n * ntb + tb];
             double corr = 0.0;
-            if (ec_mode == ORC_EC_TWO_WAY) {
+            if (ec_mode == ORC_EC_TWO_WAY || ec_mode == ORC_EC_DW_ONLY) {
                 for (int64_t b = 0; b < B; ++b) corr += (double)xsum[b * K + k] * (colmean[b * N + n] - mu[b]);
                 corr += p[k];
             }
