@@ -65,14 +65,23 @@ enum s3r_status {
 enum s3r_ec_mode {
     S3R_EC_NONE = 0,     /* plain S3R (or a baseline rounding) */
     S3R_EC_DX_ONLY = 1,  /* subtract P(E) W^T from the activation gradient only */
-    S3R_EC_TWO_WAY = 2   /* also subtract X^T P(E) from the weight gradient */
+    S3R_EC_TWO_WAY = 2,  /* also subtract X^T P(E) from the weight gradient */
+    S3R_EC_DW_ONLY = 3   /* ablation ([S3R] Table II): the weight-gradient term only */
 };
 
 /* How the upstream gradient is rounded ([S3R] §IV-B). */
 enum s3r_round_mode {
     S3R_ROUND_RTNE = 0,  /* deterministic round to nearest even */
     S3R_ROUND_S3R = 1,   /* one threshold per token shared by its channels (Phi_2D) */
-    S3R_ROUND_INDEP = 2  /* one threshold per element (conventional SR) */
+    S3R_ROUND_INDEP = 2, /* one threshold per element (conventional SR) */
+    /* [S3R] §III-B, the paper's own thresholds: Phi_2D with 7-bit values, four cut
+     * from each 32-bit word (token t: upper 7 bits k of byte t mod 4 of word 0 of
+     * Philox(counter = t / 4)), on the grid shifted by half a step, u = (k + 1/2)/128;
+     * the rounding bias is at most Delta/256. */
+    S3R_ROUND_S3R_7BIT = 3,
+    /* [S3R] §III-B, Phi_bcast (ablation): one threshold per example of S tokens,
+     * word 0 of Philox(counter = (b, 0, 1, 0)) on the 24-bit grid */
+    S3R_ROUND_BCAST = 4
 };
 
 /* Storage of the integer codes (values in [-127, 127]).  S8 is one byte per
@@ -135,6 +144,22 @@ int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* 
                  float* tok_err_part, float* col_err_part, int* d_status, cudaStream_t stream);
 
 /*
+ * s3r_quantize_ex -- s3r_quantize with the paper's own variants ([S3R] §III-A,
+ * §III-B): any `round_mode` (s3r_round_mode), S tokens per example (the
+ * examples of S3R_ROUND_BCAST; 0 = one example; T % S == 0 otherwise), and an
+ * optional per-tensor step.  With tensor_amax non-NULL (a device float) the
+ * call first sets *tensor_amax = max |g| over the whole tensor and then uses
+ * amax / 127 as the step of every tile: every tile_scale entry holds that
+ * step, which is [S3R]'s Delta = max|G'|/127.  The error partials are written
+ * for the shared-threshold modes (S3R, S3R_7BIT, BCAST) and left untouched
+ * otherwise.  Everything else is as in s3r_quantize.
+ */
+int s3r_quantize_ex(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x, const float* s_w,
+                    int round_mode, int64_t S, float* tensor_amax, uint64_t seed, uint32_t tensor_id, void* Q,
+                    int code_format, float* tile_scale, float* tok_err_part, float* col_err_part, int* d_status,
+                    cudaStream_t stream);
+
+/*
  * indep_sr_quantize -- conventional stochastic rounding with an independent
  * threshold per element ([S3R] §III-A, "Conventional QT implementations draw
  * independent full-size thresholds"; §IV-B "Independent SR").  Same fold, tile
@@ -169,8 +194,8 @@ int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, const float*
  * where exp is Cody-Waite reduction (ln 2 split in a 16-bit head and a tail)
  * with a degree-7 Taylor polynomial and the argument clamped to [-87, 88].
  * dh1 and dh3 are then quantized exactly as s3r_quantize would quantize them
- * (fold with s_x [T] and s_w1 / s_w3 [F]), with `round_mode` choosing S3R,
- * independent SR or RTNE and tensor ids tid1 / tid3.
+ * (fold with s_x [T] and s_w1 / s_w3 [F]), with `round_mode` choosing the
+ * rounding (s3r_round_mode) and tensor ids tid1 / tid3.
  * In : dA [T, F] fp32 (row stride ldd); h1, h3 [T, F] bf16 (row stride ldh).
  * Out: Q1, Q3 [T, F] codes in `code_format`; scale1, scale3 tile scales; tok1/col1/tok3/col3
  *      error partials as in s3r_quantize (NULL allowed).
@@ -180,6 +205,13 @@ int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3
                     int code_format, uint64_t seed, uint32_t tid1, uint32_t tid3, void* Q1, float* scale1,
                     float* tok1, float* col1, void* Q3, float* scale3, float* tok3, float* col3, int* d_status,
                     cudaStream_t stream);
+/* swiglu_quantize_ex -- the same with S tokens per example for S3R_ROUND_BCAST
+ * (0 = one example; T % S == 0 otherwise). */
+int swiglu_quantize_ex(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh, int64_t T,
+                       int64_t F, const float* s_x, const float* s_w1, const float* s_w3, int round_mode, int64_t S,
+                       int code_format, uint64_t seed, uint32_t tid1, uint32_t tid3, void* Q1, float* scale1,
+                       float* tok1, float* col1, void* Q3, float* scale3, float* tok3, float* col3, int* d_status,
+                       cudaStream_t stream);
 
 /*
  * s3r_ec_correct -- the error statistics and correction factors of S3R-EC
@@ -200,7 +232,7 @@ int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, const void* h3
  *      S % 128 == 0 or S == T.
  * Out: eps [T], mu [B], colmean [B, N], rowsum [K] int32, v [B, K];
  *      two-way: xsum [B, K] int32, p [K].
- * workspace: s3r_ec_workspace_size(T, K) bytes (two-way only; else may be NULL).
+ * workspace: s3r_ec_workspace_size(T, K) bytes (two-way and dW-only; else may be NULL).
  */
 size_t s3r_ec_workspace_size(int64_t T, int64_t K);
 int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,

@@ -31,8 +31,8 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "s3r.h")
 TILE = 128
 
 S3R_OK = 0
-ROUND_RTNE, ROUND_S3R, ROUND_INDEP = 0, 1, 2
-EC_NONE, EC_DX_ONLY, EC_TWO_WAY = 0, 1, 2
+ROUND_RTNE, ROUND_S3R, ROUND_INDEP, ROUND_S3R_7BIT, ROUND_BCAST = 0, 1, 2, 3, 4
+EC_NONE, EC_DX_ONLY, EC_TWO_WAY, EC_DW_ONLY = 0, 1, 2, 3
 AXIS_ROW, AXIS_COL, AXIS_TILE = 0, 1, 2
 TID_W2, TID_W1, TID_W3, RHS_ID_OFFSET = 0, 1, 2, 0x100
 MOE_TID_STRIDE = 16   # grouped mode: expert e uses tensor ids 16 e + (0, 1, 2)
@@ -50,10 +50,14 @@ _SIGS = {
     "s3r_kernel_launch_count": (C.c_uint64, []),
     "s3r_last_error": (C.c_char_p, []),
     "s3r_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _INT, _VP, _VP, _VP, _VP, _VP]),
+    "s3r_quantize_ex": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _I64, _VP, _U64, _U32, _VP, _INT, _VP, _VP,
+                               _VP, _VP, _VP]),
     "indep_sr_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _U64, _U32, _VP, _INT, _VP, _VP, _VP]),
     "rtne_quantize": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _INT, _VP, _VP, _VP]),
     "swiglu_quantize": (_INT, [_VP, _I64, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _INT, _INT, _U64, _U32, _U32,
                                _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "swiglu_quantize_ex": (_INT, [_VP, _I64, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _INT, _I64, _INT, _U64, _U32,
+                                  _U32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "s3r_ec_workspace_size": (_SZ, [_I64, _I64]),
     "s3r_ec_correct": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _I64, _VP, _INT, _INT, _VP, _VP, _VP, _VP, _VP, _VP,
                               _VP, _VP, _SZ, _VP, _VP]),
@@ -189,6 +193,26 @@ def s3r_quantize(G, s_x=None, s_w=None, seed=0, tensor_id=0, out: Quantized | No
     return out
 
 
+def s3r_quantize_ex(G, s_x=None, s_w=None, round_mode=ROUND_S3R, S=0, per_tensor=False, seed=0, tensor_id=0,
+                    out: Quantized | None = None, partials=True, status=None, stream=None,
+                    code_format=DEFAULT_CODES):
+    """s3r_quantize with a rounding mode, S tokens per example (Phi_bcast) and an
+    optional per-tensor step; returns (Quantized, tensor_amax or None)."""
+    T, N = G.shape
+    dev = G.device
+    if out is None:
+        out = Quantized(torch.empty((T, N), dtype=_CODE_DTYPE[code_format], device=dev),
+                        torch.empty((_cdiv(T, TILE), _cdiv(N, TILE)), dtype=torch.float32, device=dev),
+                        torch.empty((T, _cdiv(N, TILE)), dtype=torch.float32, device=dev) if partials else None,
+                        torch.empty((_cdiv(T, TILE), N), dtype=torch.float32, device=dev) if partials else None)
+    amax = torch.empty(1, dtype=torch.float32, device=dev) if per_tensor else None
+    _check(lib().s3r_quantize_ex(_ptr(_bits(G)), T, N, G.stride(0), _ptr(s_x), _ptr(s_w), round_mode, S, _ptr(amax),
+                                 seed, tensor_id, _ptr(out.Q), code_format_of(out.Q), _ptr(out.tile_scale),
+                                 _ptr(out.tok_err_part), _ptr(out.col_err_part), _ptr(status), _stream(stream)),
+           "s3r_quantize_ex")
+    return out, amax
+
+
 def indep_sr_quantize(G, s_x=None, s_w=None, seed=0, tensor_id=0, out: Quantized | None = None, status=None,
                       stream=None, code_format=DEFAULT_CODES) -> Quantized:
     T, N = G.shape
@@ -218,7 +242,7 @@ def rtne_quantize(A, scale_axis=AXIS_TILE, s_x=None, s_w=None, Q=None, scale=Non
 
 
 def swiglu_quantize(dA, h1, h3, s_x=None, s_w1=None, s_w3=None, round_mode=ROUND_S3R, seed=0, tid1=TID_W1,
-                    tid3=TID_W3, partials=True, status=None, stream=None, code_format=DEFAULT_CODES):
+                    tid3=TID_W3, partials=True, status=None, stream=None, code_format=DEFAULT_CODES, S=0):
     T, F = dA.shape
     dev = dA.device
 
@@ -230,11 +254,11 @@ def swiglu_quantize(dA, h1, h3, s_x=None, s_w1=None, s_w3=None, round_mode=ROUND
 
     o1, o3 = mk(), mk()
     assert dA.dtype == torch.float32 and h1.stride(0) == h3.stride(0)
-    _check(lib().swiglu_quantize(_ptr(dA), dA.stride(0), _ptr(_bits(h1)), _ptr(_bits(h3)), h1.stride(0), T, F,
-                                 _ptr(s_x), _ptr(s_w1), _ptr(s_w3), round_mode, code_format, seed, tid1, tid3,
-                                 _ptr(o1.Q), _ptr(o1.tile_scale), _ptr(o1.tok_err_part), _ptr(o1.col_err_part),
-                                 _ptr(o3.Q), _ptr(o3.tile_scale), _ptr(o3.tok_err_part), _ptr(o3.col_err_part),
-                                 _ptr(status), _stream(stream)), "swiglu_quantize")
+    _check(lib().swiglu_quantize_ex(_ptr(dA), dA.stride(0), _ptr(_bits(h1)), _ptr(_bits(h3)), h1.stride(0), T, F,
+                                    _ptr(s_x), _ptr(s_w1), _ptr(s_w3), round_mode, S, code_format, seed, tid1, tid3,
+                                    _ptr(o1.Q), _ptr(o1.tile_scale), _ptr(o1.tok_err_part), _ptr(o1.col_err_part),
+                                    _ptr(o3.Q), _ptr(o3.tile_scale), _ptr(o3.tok_err_part), _ptr(o3.col_err_part),
+                                    _ptr(status), _stream(stream)), "swiglu_quantize")
     return o1, o3
 
 
@@ -259,8 +283,9 @@ def s3r_ec_correct(q: Quantized, T, N, S, W8=None, X8=None, ec_mode=EC_TWO_WAY, 
     f = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)
     i = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)
     ec = ECFactors(f(T), f(B), f(B, N), i(K) if K else None, f(B, K) if K else None,
-                   i(B, K) if ec_mode == EC_TWO_WAY else None, f(K) if ec_mode == EC_TWO_WAY else None)
-    ws_bytes = lib().s3r_ec_workspace_size(T, K) if ec_mode == EC_TWO_WAY else 0
+                   i(B, K) if ec_mode in (EC_TWO_WAY, EC_DW_ONLY) else None,
+                   f(K) if ec_mode in (EC_TWO_WAY, EC_DW_ONLY) else None)
+    ws_bytes = lib().s3r_ec_workspace_size(T, K) if ec_mode in (EC_TWO_WAY, EC_DW_ONLY) else 0
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     fmt = code_format_of(W8 if W8 is not None else q.Q)
     _check(lib().s3r_ec_correct(_ptr(q.tok_err_part), _ptr(q.col_err_part), T, N, S, _ptr(W8), K, _ptr(X8), fmt, ec_mode,
@@ -333,7 +358,7 @@ def int8_gemm_dw(X8, Q, tile_scale, s_w=None, ec_mode=EC_NONE, ec: ECFactors | N
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
     S = T if S is None else S
-    two = ec_mode == EC_TWO_WAY and ec is not None
+    two = ec_mode in (EC_TWO_WAY, EC_DW_ONLY) and ec is not None
     _check(lib().int8_gemm_dw(_ptr(X8), _ptr(Q), _ptr(tile_scale), fmt, T, K, N, _ptr(s_w), ec_mode,
                               _ptr(ec.colmean if two else None), _ptr(ec.mu if two else None),
                               _ptr(ec.xsum if two else None), _ptr(ec.p if two else None), S, _ptr(dW),

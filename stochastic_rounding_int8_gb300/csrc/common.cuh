@@ -50,6 +50,21 @@ __device__ __forceinline__ float token_threshold(uint64_t t, uint32_t seed_lo, u
     return unit24(philox4x32_10((uint32_t)t, (uint32_t)(t >> 32), 0u, 0u, seed_lo, tensor_id).x);
 }
 
+// The paper's 7-bit per-token thresholds: four per word (token t takes byte t mod 4
+// of word 0 of Philox(counter = t / 4)); its upper 7 bits k give (k + 1/2) / 128,
+// the grid shifted by half a step.
+__device__ __forceinline__ float token_threshold7(uint64_t t, uint32_t seed_lo, uint32_t tensor_id) {
+    const uint64_t c = t >> 2;
+    const uint32_t w = philox4x32_10((uint32_t)c, (uint32_t)(c >> 32), 0u, 0u, seed_lo, tensor_id).x;
+    const uint32_t k = (w >> (8u * (uint32_t)(t & 3u) + 1u)) & 0x7Fu;
+    return ((float)k + 0.5f) * 0.0078125f;   // exact: k + 1/2 has at most 8 significant bits
+}
+
+// Phi_bcast: one threshold per example b, word 0 of Philox(counter = (b, 0, 1, 0)).
+__device__ __forceinline__ float example_threshold(uint64_t b, uint32_t seed_lo, uint32_t tensor_id) {
+    return unit24(philox4x32_10((uint32_t)b, (uint32_t)(b >> 32), 1u, 0u, seed_lo, tensor_id).x);
+}
+
 // ---------------------------------------------------------------------------
 // bf16 helpers
 // ---------------------------------------------------------------------------

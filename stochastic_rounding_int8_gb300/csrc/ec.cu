@@ -1065,13 +1065,16 @@ static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, si
 
 // fp16 codes with 16-byte aligned rows: rowsum, v, mu (and, two-way, xsum and
 // p) in one streaming launch.  Returns 1 when it does not apply.
+// weight: rowsum and v are wanted (weight-side items); two: xsum and p (input-side items).
 static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
-                            bool two, int32_t* xs, float* ps, int* counter, int* d_status, cudaStream_t stream) {
+                            bool weight, bool two, int32_t* xs, float* ps, int* counter, int* d_status,
+                            cudaStream_t stream) {
     const int64_t B = T / S;
     if (B > kEsMaxB || T >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return 1;
     if (N % 8 != 0 || (two && K % 8 != 0)) return 1;
     for (int j = 0; j < nj; ++j)
-        if (!s3r_aligned16(jobs[j].W8) || !s3r_aligned16(jobs[j].colmean) || (two && !s3r_aligned16(jobs[j].eps)))
+        if ((weight && (!s3r_aligned16(jobs[j].W8) || !s3r_aligned16(jobs[j].colmean))) ||
+            (two && !s3r_aligned16(jobs[j].eps)))
             return 1;
     if (two && !s3r_aligned16(X8)) return 1;
     auto fn = ec_encode_fn();
@@ -1093,8 +1096,9 @@ static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int
         return enc2(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, n, 1, (n * 4 + 15) / 16 * 16, kEsXRowsBox, 1);
     };
     for (int j = 0; j < nj; ++j) {
-        if (!enc2(&maps[1 + j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, jobs[j].W8, N, K, N * 2, 256, kEsWRows) ||
-            !enc2(&maps[3 + j], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, jobs[j].colmean, N, B, N * 4, 256, bch))
+        if (weight &&
+            (!enc2(&maps[1 + j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, jobs[j].W8, N, K, N * 2, 256, kEsWRows) ||
+             !enc2(&maps[3 + j], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, jobs[j].colmean, N, B, N * 4, 256, bch)))
             return 1;
         if (two && !enc1(&maps[5 + j], jobs[j].eps, T)) return 1;
     }
@@ -1104,6 +1108,11 @@ static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int
         maps[0] = maps[1];   // not read without input-side items
         maps[5] = maps[1];
     }
+    if (!weight)
+        for (int j = 0; j < 2; ++j) {   // not read without weight-side items
+            maps[1 + j] = maps[0];
+            maps[3 + j] = maps[0];
+        }
     if (nj == 1) {
         maps[2] = maps[1];
         maps[4] = maps[3];
@@ -1129,7 +1138,7 @@ static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int
     A.ngr = s3r_cdiv(K, kEsWRows);
     A.ngroups = (int)s3r_cdiv(B, bch);
     A.nbn = s3r_cdiv(N, 256);
-    A.n_gemv = nj * A.ngr * A.ngroups;
+    A.n_gemv = weight ? nj * A.ngr * A.ngroups : 0;
     A.n_items = A.n_gemv + (two ? A.ncb * A.nch : 0);
     A.d_status = d_status;
     A.mu_v4 = S % 4 == 0;
@@ -1158,7 +1167,8 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
                           int ec_mode, void* workspace, size_t workspace_bytes, int* d_status,
                           cudaStream_t stream) {
     const int64_t B = T / S, ntc = s3r_cdiv(N, kTile), ntr = s3r_cdiv(T, kTile);
-    const bool two = ec_mode == S3R_EC_TWO_WAY;
+    const bool two = ec_mode == S3R_EC_TWO_WAY || ec_mode == S3R_EC_DW_ONLY;     // input side: xsum, p
+    const bool weight = ec_mode == S3R_EC_DX_ONLY || ec_mode == S3R_EC_TWO_WAY;  // weight side: rowsum, v
     bool vec_w = N % 8 == 0;
     for (int j = 0; j < nj; ++j) vec_w = vec_w && s3r_aligned16(jobs[j].W8) && s3r_aligned16(jobs[j].colmean);
     const int64_t slab = std::min<int64_t>(N, kGemvSlabFloats / kGemvBch);   // multiple of 8 when N is
@@ -1205,17 +1215,18 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
         S3R_CHECK_LAUNCH();
     }
     if (ec_mode != S3R_EC_NONE && K > 0 && sizeof(CodeT) == 2) {
-        const int st = launch_ec_stream(jobs, nj, T, N, S, K, X8, two, xs, ps, counter, d_status, stream);
+        const int st = launch_ec_stream(jobs, nj, T, N, S, K, X8, weight, two, xs, ps, counter, d_status, stream);
         if (st <= 0) return st;   // launched (0) or failed (< 0); 1: the kernels below
     }
-    if (ec_mode == S3R_EC_NONE || K == 0 || !vec_w) {
+    if (ec_mode == S3R_EC_NONE || K == 0 || !vec_w || !weight) {
         for (int j = 0; j < nj; ++j) {
             ec_mu_kernel<<<(unsigned)s3r_cdiv(B, 8), kGemvThreads, 0, stream>>>(jobs[j].eps, S, B, jobs[j].mu);
             S3R_CHECK_LAUNCH();
         }
     }
     if (ec_mode == S3R_EC_NONE || K == 0) return S3R_OK;
-    if (vec_w) {
+    if (!weight) {
+    } else if (vec_w) {
         EcGemvArgs G{};
         for (int j = 0; j < nj; ++j) {
             G.W8[j] = jobs[j].W8;
@@ -1294,17 +1305,19 @@ static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int6
                            int* d_status, cudaStream_t stream) {
     if (T < 0 || N < 0 || K < 0 || S <= 0) return S3R_ERR_ARG;
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
-    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (ec_mode < S3R_EC_NONE || ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
+    const bool weight = ec_mode == S3R_EC_DX_ONLY || ec_mode == S3R_EC_TWO_WAY;   // rowsum and v
+    const bool input = ec_mode == S3R_EC_TWO_WAY || ec_mode == S3R_EC_DW_ONLY;    // xsum and p
     if (T == 0 || N == 0) return S3R_OK;
     if (T % S != 0) return S3R_ERR_SHAPE;
     if (S % kTile != 0 && S != T) return S3R_ERR_SHAPE;
     for (int j = 0; j < nj; ++j) {
         const EcJob& J = jobs[j];
         if (!J.tok || !J.col || !J.eps || !J.mu || !J.colmean) return S3R_ERR_ARG;
-        if (ec_mode != S3R_EC_NONE && K > 0 && (!J.W8 || !J.rowsum || !J.v)) return S3R_ERR_ARG;
-        if (ec_mode == S3R_EC_TWO_WAY && K > 0 && (!J.xsum || !J.p)) return S3R_ERR_ARG;
+        if (weight && K > 0 && (!J.W8 || !J.rowsum || !J.v)) return S3R_ERR_ARG;
+        if (input && K > 0 && (!J.xsum || !J.p)) return S3R_ERR_ARG;
     }
-    if (ec_mode == S3R_EC_TWO_WAY && K > 0 && !X8) return S3R_ERR_ARG;
+    if (input && K > 0 && !X8) return S3R_ERR_ARG;
     if (code_format == S3R_CODES_F16)
         return launch_factors<__half>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, d_status,
                                       stream);
@@ -1407,7 +1420,7 @@ extern "C" int s3r_ec_correct_static(const float* tok_err_part, const float* col
                                      int64_t S, const void* W8, int64_t K, const void* X8, int code_format,
                                      int ec_mode, float* eps, float* mu, float* colmean, int32_t* rowsum, float* v,
                                      int32_t* xsum, float* p, int* d_status, cudaStream_t stream) {
-    if (ec_mode != S3R_EC_TWO_WAY)   // only the two-way factors need scratch
+    if (ec_mode != S3R_EC_TWO_WAY && ec_mode != S3R_EC_DW_ONLY)   // only the column sums need scratch
         return s3r_ec_correct(tok_err_part, col_err_part, T, N, S, W8, K, X8, code_format, ec_mode, eps, mu, colmean,
                               rowsum, v, xsum, p, nullptr, 0, d_status, stream);
     const size_t need = s3r_ec_workspace_size(T, K);

@@ -143,7 +143,8 @@ int make_block(Block& b, const s3r_ffn_args& a, void* ws, size_t ws_bytes, uint3
     b.Lo = layout(ws, ws_bytes, a.T, a.d, a.F, a.S, a.round_mode, b.fmt);
     if (!b.Lo.ok) return S3R_ERR_WORKSPACE;
     b.rm = a.round_mode;
-    b.ec = b.rm == S3R_ROUND_S3R ? a.ec_mode : S3R_EC_NONE;
+    const bool shared = b.rm == S3R_ROUND_S3R || b.rm == S3R_ROUND_S3R_7BIT || b.rm == S3R_ROUND_BCAST;
+    b.ec = shared ? a.ec_mode : S3R_EC_NONE;
     b.indep = b.rm == S3R_ROUND_INDEP;
     b.tid2 = tid_base + S3R_TID_W2;
     b.tid1 = tid_base + S3R_TID_W1;
@@ -156,9 +157,9 @@ int step_quantize_dy(Block& b, cudaStream_t stream) {
     const s3r_ffn_args& a = b.a;
     LinearWs& L2 = b.Lo.w2;
     const int64_t T = a.T, d = a.d;
-    if (b.rm == S3R_ROUND_S3R)
-        return s3r_quantize(a.dY, T, d, d, a.s_a, a.s_w2, a.seed, b.tid2, L2.Q, b.fmt, L2.scale, L2.tok, L2.col,
-                            a.d_status, stream);
+    if (b.rm == S3R_ROUND_S3R || b.rm == S3R_ROUND_S3R_7BIT || b.rm == S3R_ROUND_BCAST)
+        return s3r_quantize_ex(a.dY, T, d, d, a.s_a, a.s_w2, b.rm, a.S, nullptr, a.seed, b.tid2, L2.Q, b.fmt,
+                               L2.scale, L2.tok, L2.col, a.d_status, stream);
     if (b.indep) {
         S3R_TRY(indep_sr_quantize(a.dY, T, d, d, a.s_a, a.s_w2, a.seed, b.tid2, L2.Q, b.fmt, L2.scale, a.d_status,
                                   stream));
@@ -194,7 +195,7 @@ int step_da(Block& b, cudaStream_t stream) {
 // 4. dW2 = A8^T Q2 / s_w2  [F, d]
 UmmaDwProblem dw_problem(const Block& b, const void* X8, const LinearWs& L, int64_t K, int64_t N, const float* s_w,
                          float* dW) {
-    const bool two = b.ec == S3R_EC_TWO_WAY;
+    const bool two = b.ec == S3R_EC_TWO_WAY || b.ec == S3R_EC_DW_ONLY;
     return UmmaDwProblem{X8, b.indep ? L.Qr : L.Q, b.indep ? L.scale_r : L.scale, b.a.T, K, N, s_w, b.ec,
                          two ? L.colmean : nullptr, two ? L.mu : nullptr, two ? L.xsum : nullptr,
                          two ? L.p : nullptr, b.a.S, dW, nullptr};
@@ -213,11 +214,11 @@ int step_swiglu(Block& b, cudaStream_t stream) {
     LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
     const int64_t T = a.T, F = a.F;
     const bool keep_err = b.ec != S3R_EC_NONE;
-    S3R_TRY(swiglu_quantize(b.Lo.dA, F, a.h1, a.h3, F, T, F, a.s_x, a.s_w1, a.s_w3, b.rm, b.fmt, a.seed, b.tid1,
+    S3R_TRY(swiglu_quantize_ex(b.Lo.dA, F, a.h1, a.h3, F, T, F, a.s_x, a.s_w1, a.s_w3, b.rm, a.S, b.fmt, a.seed, b.tid1,
                             b.tid3, L1.Q, L1.scale, keep_err ? L1.tok : nullptr, keep_err ? L1.col : nullptr, L3.Q,
                             L3.scale, keep_err ? L3.tok : nullptr, keep_err ? L3.col : nullptr, a.d_status, stream));
     if (b.indep)
-        S3R_TRY(swiglu_quantize(b.Lo.dA, F, a.h1, a.h3, F, T, F, a.s_x, a.s_w1, a.s_w3, b.rm, b.fmt, a.seed,
+        S3R_TRY(swiglu_quantize_ex(b.Lo.dA, F, a.h1, a.h3, F, T, F, a.s_x, a.s_w1, a.s_w3, b.rm, a.S, b.fmt, a.seed,
                                 b.tid1 + kRhsOffset, b.tid3 + kRhsOffset, L1.Qr, L1.scale_r, nullptr, nullptr, L3.Qr,
                                 L3.scale_r, nullptr, nullptr, a.d_status, stream));
     return S3R_OK;
@@ -399,8 +400,8 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     if (!a) return S3R_ERR_ARG;
     const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
     if (T <= 0 || d <= 0 || F <= 0) return S3R_ERR_ARG;
-    if (a->round_mode < S3R_ROUND_RTNE || a->round_mode > S3R_ROUND_INDEP) return S3R_ERR_ARG;
-    if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (a->round_mode < S3R_ROUND_RTNE || a->round_mode > S3R_ROUND_BCAST) return S3R_ERR_ARG;
+    if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
     if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     const int fmt = a->code_format;
     if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->A8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 ||
@@ -554,4 +555,4 @@ extern "C" const char* s3r_status_string(int status) {
     }
 }
 
-extern "C" int s3r_abi_version(void) { return 100; }
+extern "C" int s3r_abi_version(void) { return 101; }

@@ -305,7 +305,8 @@ extern "C" int int8_gemm_dx(const void* Qv, const float* tile_scale, const void*
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (T == 0 || K == 0) return S3R_OK;
     if (!Qv || !tile_scale || !W8v || !dX) return S3R_ERR_ARG;
-    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (ec_mode < S3R_EC_NONE || ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
+    if (ec_mode == S3R_EC_DW_ONLY) ec_mode = S3R_EC_NONE;   // the ablation corrects dW only
     if (ec_mode != S3R_EC_NONE && (!eps || !rowsum || !v || S <= 0 || T % S != 0)) return S3R_ERR_ARG;
     if (N == 0) return S3R_ERR_SHAPE;
     if (code_format == S3R_CODES_F16)
@@ -329,7 +330,8 @@ extern "C" int int8_gemm_dx_sum(const struct s3r_dx_term* terms, int n_terms, in
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (T == 0 || K == 0) return S3R_OK;
     if (!dX) return S3R_ERR_ARG;
-    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (ec_mode < S3R_EC_NONE || ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
+    if (ec_mode == S3R_EC_DW_ONLY) ec_mode = S3R_EC_NONE;   // the ablation corrects dW only
     for (int i = 0; i < n_terms; ++i) {
         const s3r_dx_term& t = terms[i];
         if (!t.Q || !t.tile_scale || !t.W8) return S3R_ERR_ARG;
@@ -362,7 +364,8 @@ extern "C" int int8_gemm_dw(const void* X8v, const void* Qv, const float* tile_s
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (K == 0 || N == 0) return S3R_OK;
     if (!X8v || !Qv || !tile_scale || !dW) return S3R_ERR_ARG;
-    if (ec_mode != S3R_EC_NONE && ec_mode != S3R_EC_DX_ONLY && ec_mode != S3R_EC_TWO_WAY) return S3R_ERR_ARG;
+    if (ec_mode < S3R_EC_NONE || ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
+    if (ec_mode == S3R_EC_DW_ONLY) ec_mode = S3R_EC_TWO_WAY;   // dW carries the whole correction
     if (ec_mode == S3R_EC_TWO_WAY && (!colmean || !mu || !xsum || !p || S <= 0 || T % S != 0)) return S3R_ERR_ARG;
     if (T == 0) return S3R_ERR_SHAPE;
     if (code_format == S3R_CODES_F16)

@@ -829,7 +829,8 @@ static int add_dx_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDxPr
     const bool two = q.Q3 != nullptr;
     if (!s3r_aligned16(q.Q) || !s3r_aligned16(q.W) || N % 8 != 0) return S3R_ERR_ALIGN;
     if (two && (!s3r_aligned16(q.Q3) || !s3r_aligned16(q.W3))) return S3R_ERR_ALIGN;
-    if (q.ec_mode && S < T && S % kTile != 0) {
+    const int ecm = q.ec_mode == S3R_EC_DW_ONLY ? S3R_EC_NONE : q.ec_mode;   // dX is uncorrected under dW-only
+    if (ecm && S < T && S % kTile != 0) {
         // the epilogue stages v for at most kNbX examples per 128-row tile
         int64_t nb = 0;
         for (int64_t m0 = 0; m0 < T; m0 += umma::BM) {
@@ -859,7 +860,7 @@ static int add_dx_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDxPr
     P.M = T; P.N = K; P.kind = umma::kDX;
     dx_segment(P.seg[0], q.tile_scale, N, q.eps, q.rowsum, q.v);
     if (two) dx_segment(P.seg[1], q.tile_scale3, N, q.eps3, q.rowsum3, q.v3);
-    P.C = q.dX; P.ldc = K; P.dump = q.dump; P.s_row = q.s_x; P.ec_mode = q.ec_mode; P.S = S;
+    P.C = q.dX; P.ldc = K; P.dump = q.dump; P.s_row = q.s_x; P.ec_mode = ecm; P.S = S;
     P.accumulate = q.accumulate;
     // bytes per row strip of A (BM rows of Q over the contraction) and per column strip of B (BN rows of W)
     const double kbytes = 2.0 * (double)N * (two ? 2 : 1);
@@ -884,7 +885,8 @@ static int add_dw_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDwPr
     umma::Segment& g = P.seg[0];
     g.scale = q.tile_scale; g.sm = 0; g.sn = 1; g.sk = s3r_cdiv(N, kTile); g.nt_limit = s3r_cdiv(N, kTile);
     g.K = T;
-    P.C = q.dW; P.ldc = N; P.dump = q.dump; P.s_col = q.s_w; P.ec_mode = q.ec_mode; P.S = S;
+    P.C = q.dW; P.ldc = N; P.dump = q.dump; P.s_col = q.s_w; P.S = S;
+    P.ec_mode = q.ec_mode == S3R_EC_DW_ONLY ? S3R_EC_TWO_WAY : q.ec_mode;   // dW carries the whole correction
     P.B = q.S > 0 ? T / q.S : 1; P.colmean = q.colmean; P.mu = q.mu; P.xsum = q.xsum; P.p = q.p;
     const double kbytes = 2.0 * (double)T;   // per output row / column over the contraction
     strip[0] = umma::BM * kbytes;

@@ -23,7 +23,11 @@
 
 namespace s3r {
 
-enum QMode { kRTNE = 0, kS3R = 1, kINDEP = 2 };
+enum QMode { kRTNE = 0, kS3R = 1, kINDEP = 2, kS3R7 = 3, kBCAST = 4 };
+
+// Modes with one threshold per row of the tensor (shared by its channels), one
+// threshold tensor for both products, and the S3R-EC error partials.
+__host__ __device__ constexpr bool row_mode(int m) { return m == kS3R || m == kS3R7 || m == kBCAST; }
 
 // Per-thread geometry of a 128x128 tile: chunk c (8 columns), rows r0 + j*RSTRIDE.
 template <int RPT>
@@ -48,7 +52,17 @@ struct QuantCommon {
     uint32_t seed_lo;
     int* d_status;
     bool vec_store;  // Q rows aligned for one vector store per 8-code chunk
+    int64_t S;       // tokens per example (Phi_bcast); 0: one example
+    const uint32_t* tensor_amax;   // per-tensor step: bits of max |g| over the tensor (null: per tile)
 };
+
+// The threshold of row t under a row-threshold mode.
+template <int MODE>
+__device__ __forceinline__ float row_threshold(uint64_t t, const QuantCommon& C, uint32_t tensor_id) {
+    if (MODE == kS3R7) return token_threshold7(t, C.seed_lo, tensor_id);
+    if (MODE == kBCAST) return example_threshold(C.S > 0 ? t / (uint64_t)C.S : 0u, C.seed_lo, tensor_id);
+    return token_threshold(t, C.seed_lo, tensor_id);
+}
 
 // Block-wide max of non-negative float bit patterns (NaN/Inf compare largest).
 template <int WARPS>
@@ -88,9 +102,9 @@ __device__ __forceinline__ void round_and_store(const float (&ng)[RPT][8], uint3
 
     // thresholds of my rows: lane (half*16 + j) draws the one of row r0 + j*RSTRIDE
     float u_row[RPT];
-    if (MODE == kS3R) {
+    if (row_mode(MODE)) {
         float mine = 0.0f;
-        if (c < RPT) mine = token_threshold((uint64_t)(t0 + r0 + c * Geo::kRowStride), C.seed_lo, O.tensor_id);
+        if (c < RPT) mine = row_threshold<MODE>((uint64_t)(t0 + r0 + c * Geo::kRowStride), C, O.tensor_id);
 #pragma unroll
         for (int j = 0; j < RPT; ++j) u_row[j] = __shfl_sync(0xFFFFFFFFu, mine, (lane & 16) + j);
     }
@@ -142,8 +156,8 @@ __device__ __forceinline__ void round_and_store(const float (&ng)[RPT][8], uint3
                     const float2 fm = f2_add_rm(y, M2);              // kMagic + floor(y)
                     const float2 f = f2_sub(fm, M2);                 // floor(y), exact
                     const float2 p = f2_sub(y, f);                   // residual in [0, 1), exact
-                    const float ua = (MODE == kS3R) ? u_row[j] : u8[2 * k];
-                    const float ub = (MODE == kS3R) ? u_row[j] : u8[2 * k + 1];
+                    const float ua = row_mode(MODE) ? u_row[j] : u8[2 * k];
+                    const float ub = row_mode(MODE) ? u_row[j] : u8[2 * k + 1];
                     m = f2_add(fm, make_float2(lt_one(ua, p.x), lt_one(ub, p.y)));   // + [u < p]
                 }
                 const float2 q = f2_sub(m, M2);                      // the code, exact
@@ -290,6 +304,7 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(TileQuantArgs A, Qua
         }
     }
     amax_bits = block_max_u32<Geo::kWarps>(amax_bits, red);
+    if (C.tensor_amax) amax_bits = __ldg(C.tensor_amax);   // one step for the whole tensor
     round_and_store<MODE, RPT>(g, amax_bits, t0, n0, r0, c, C, O, col_smem);
 }
 
@@ -380,7 +395,7 @@ __device__ __forceinline__ void round_rows(PairFn gpair, float d, float inv, boo
                 }
             }
         }
-        const float ut = MODE == kS3R ? u0[j * u_step] : 0.0f;
+        const float ut = row_mode(MODE) ? u0[j * u_step] : 0.0f;
         float qv[8], qm[8];
         float2 rs = make_float2(0.0f, 0.0f);
         if (!nonfinite) {
@@ -393,7 +408,7 @@ __device__ __forceinline__ void round_rows(PairFn gpair, float d, float inv, boo
                     // per lane: a packed add that is the product's only use would be fused into an fma
                     m = make_float2(__fadd_rn(y.x, kMagic), __fadd_rn(y.y, kMagic));
                 } else {
-                    const float2 uu = MODE == kS3R ? make_float2(ut, ut) : make_float2(u8[2 * q], u8[2 * q + 1]);
+                    const float2 uu = row_mode(MODE) ? make_float2(ut, ut) : make_float2(u8[2 * q], u8[2 * q + 1]);
                     m = f2_add_rp(f2_sub_rp(y, uu), M2);
                 }
                 const float2 qq = f2_sub(m, M2);   // the code, exact
@@ -501,8 +516,8 @@ __device__ __forceinline__ float2 q_side(const TileQuantArgs& A, const QuantComm
     if (threadIdx.x < kTile) {
         const int64_t t = (int64_t)rb * kTile + threadIdx.x;
         const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
-        if (MODE == kS3R && rb != u_rb) {
-            u_mine = token_threshold((uint64_t)t, C.seed_lo, tensor_id);
+        if (row_mode(MODE) && rb != u_rb) {
+            u_mine = row_threshold<MODE>((uint64_t)t, C, tensor_id);
             u_rb = rb;
         }
         return make_float2(sx, u_mine);
@@ -517,7 +532,7 @@ __global__ void __launch_bounds__(256, 2)
     quantize_tma_kernel(const __grid_constant__ CUtensorMap tmG, TileQuantArgs A, QuantCommon C, QuantOut O,
                         int64_t ntiles) {
     constexpr int RPT = 8, RS = 16;   // rows r0 + 16 j of the tile, 8 columns from 8 c
-    constexpr bool ERR = MODE == kS3R;   // error partials
+    constexpr bool ERR = row_mode(MODE);   // error partials
     extern __shared__ __align__(128) uint8_t qsmem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + kQStages * kQTileBytes);
     __shared__ __align__(16) float2 xu_s[2][kTile];   // (s_x, u) per tile row
@@ -633,7 +648,8 @@ __global__ void __launch_bounds__(256, 2)
             issue(issued);
             ++issued;
         }
-        const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, red[lane & 7]);
+        uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, red[lane & 7]);
+        if (C.tensor_amax) amax_bits = __ldg(C.tensor_amax);   // one step for the whole tensor
         const bool nonfinite = amax_bits >= 0x7F800000u;   // uniform across the CTA
         float d, inv;
         tile_scales(amax_bits, d, inv);
@@ -875,9 +891,9 @@ __device__ __forceinline__ void sw_side(const SwigluArgs& A, const QuantCommon& 
     if (threadIdx.x < kTile) {
         const int64_t t = (int64_t)rb * kTile + threadIdx.x;
         const float sx = (A.s_x && t < C.T) ? __ldg(A.s_x + t) : 1.0f;
-        if (MODE == kS3R && rb != u_rb) {
-            u1 = token_threshold((uint64_t)t, C.seed_lo, O1.tensor_id);
-            u3 = token_threshold((uint64_t)t, C.seed_lo, O3.tensor_id);
+        if (row_mode(MODE) && rb != u_rb) {
+            u1 = row_threshold<MODE>((uint64_t)t, C, O1.tensor_id);
+            u3 = row_threshold<MODE>((uint64_t)t, C, O3.tensor_id);
             u_rb = rb;
         }
         xs = make_float4(sx, u1, u3, 0.0f);
@@ -894,7 +910,7 @@ __global__ void __launch_bounds__(512, 1)
                       const __grid_constant__ CUtensorMap tmH3, SwigluArgs A, QuantCommon C, QuantOut O1, QuantOut O3,
                       int64_t ntiles) {
     constexpr int RPT = 4, RS = 32;
-    constexpr bool ERR = MODE == kS3R;
+    constexpr bool ERR = row_mode(MODE);
     extern __shared__ uint8_t swsm_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(swsm_raw) + 127) & ~(uintptr_t)127);
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kSwStages * kSwQuarterBytes);
@@ -1227,22 +1243,57 @@ static int try_quant_tma(int mode, const TileQuantArgs& A, const QuantCommon& C,
                                : launch_quant_tma<kRTNE, 0>(map, A, C, O, ntiles, stream);
         case kS3R: return f16 ? launch_quant_tma<kS3R, 1>(map, A, C, O, ntiles, stream)
                               : launch_quant_tma<kS3R, 0>(map, A, C, O, ntiles, stream);
+        case kS3R7: return f16 ? launch_quant_tma<kS3R7, 1>(map, A, C, O, ntiles, stream)
+                               : launch_quant_tma<kS3R7, 0>(map, A, C, O, ntiles, stream);
+        case kBCAST: return f16 ? launch_quant_tma<kBCAST, 1>(map, A, C, O, ntiles, stream)
+                                : launch_quant_tma<kBCAST, 0>(map, A, C, O, ntiles, stream);
         default: return f16 ? launch_quant_tma<kINDEP, 1>(map, A, C, O, ntiles, stream)
                             : launch_quant_tma<kINDEP, 0>(map, A, C, O, ntiles, stream);
     }
 }
 
+// Per-tensor step: max |g| of the folded gradient over the whole tensor, as a
+// bit pattern (non-negative floats and NaN order like their bits), combined
+// across CTAs with an atomic max (order-independent, so deterministic).
+__global__ void __launch_bounds__(256) tensor_absmax_kernel(const uint16_t* G, int64_t T, int64_t N, int64_t ldg,
+                                                            const float* s_x, const float* s_w, uint32_t* amax) {
+    __shared__ uint32_t red[8];
+    uint32_t m = 0u;
+    const int64_t total = T * N;
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (int64_t)gridDim.x * 256) {
+        const int64_t t = i / N, n = i - t * N;
+        float g = __uint_as_float((uint32_t)G[t * ldg + n] << 16);
+        if (s_x) g = __fmul_rn(s_x[t], g);
+        if (s_w) g = __fmul_rn(g, s_w[n]);
+        m = max(m, __float_as_uint(g) & 0x7FFFFFFFu);
+    }
+    m = block_max_u32<8>(m, red);
+    if (threadIdx.x == 0) atomicMax(amax, m);
+}
+
+// S: tokens per example (Phi_bcast; 0: one example).  tensor_amax: per-tensor
+// step (a device float that receives max |g|), or null for one step per tile.
 static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
                              const float* s_w, uint64_t seed, uint32_t tensor_id, void* Q, int fmt, float* scale,
-                             float* tok, float* col, int* d_status, cudaStream_t stream) {
-    if (T < 0 || N < 0 || !valid_fmt(fmt)) return S3R_ERR_ARG;
+                             float* tok, float* col, int* d_status, cudaStream_t stream, int64_t S = 0,
+                             float* tensor_amax = nullptr) {
+    if (T < 0 || N < 0 || !valid_fmt(fmt) || S < 0) return S3R_ERR_ARG;
     if (T == 0 || N == 0) return S3R_OK;
     if (!G || !Q || !scale) return S3R_ERR_ARG;
     if (ldg < N) return S3R_ERR_SHAPE;
     if (s3r_cdiv(T, kTile) > 65535) return S3R_ERR_UNSUPPORTED;
     TileQuantArgs A{static_cast<const uint16_t*>(G), ldg, s_x, s_w, s3r_aligned16(G) && (ldg % 8) == 0};
-    QuantCommon C{T, N, s3r_cdiv(N, kTile), (uint32_t)seed, d_status, s3r_aligned16(Q) && (N % 8) == 0};
+    QuantCommon C{T, N, s3r_cdiv(N, kTile), (uint32_t)seed, d_status, s3r_aligned16(Q) && (N % 8) == 0, S,
+                  reinterpret_cast<const uint32_t*>(tensor_amax)};
     QuantOut O{Q, fmt, scale, tok, col, tensor_id};
+    if (tensor_amax) {
+        cudaError_t e = cudaMemsetAsync(tensor_amax, 0, sizeof(float), stream);
+        if (e != cudaSuccess) return s3r_cuda_fail("quantize: cudaMemsetAsync", e);
+        const int64_t blocks = std::min<int64_t>(s3r_cdiv(T * N, 256), 8LL * sm_count());
+        tensor_absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(A.G, T, N, ldg, s_x, s_w,
+                                                                   reinterpret_cast<uint32_t*>(tensor_amax));
+        S3R_CHECK_LAUNCH();
+    }
     const int tma = try_quant_tma(mode, A, C, O, stream);
     if (tma <= 0) return tma;   // launched (0) or failed (< 0)
     dim3 grid((unsigned)s3r_cdiv(N, kTile), (unsigned)s3r_cdiv(T, kTile));
@@ -1250,6 +1301,8 @@ static int launch_tile_quant(int mode, const void* G, int64_t T, int64_t N, int6
         case kRTNE: quantize_tile_kernel<kRTNE><<<grid, 256, 0, stream>>>(A, C, O); break;
         case kS3R: quantize_tile_kernel<kS3R><<<grid, 256, 0, stream>>>(A, C, O); break;
         case kINDEP: quantize_tile_kernel<kINDEP><<<grid, 256, 0, stream>>>(A, C, O); break;
+        case kS3R7: quantize_tile_kernel<kS3R7><<<grid, 256, 0, stream>>>(A, C, O); break;
+        case kBCAST: quantize_tile_kernel<kBCAST><<<grid, 256, 0, stream>>>(A, C, O); break;
         default: return S3R_ERR_ARG;
     }
     S3R_CHECK_LAUNCH();
@@ -1261,6 +1314,27 @@ extern "C" int s3r_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, co
                             float* tok_err_part, float* col_err_part, int* d_status, cudaStream_t stream) {
     return launch_tile_quant(kS3R, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, code_format, tile_scale, tok_err_part,
                              col_err_part, d_status, stream);
+}
+
+extern "C" int s3r_quantize_ex(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
+                               const float* s_w, int round_mode, int64_t S, float* tensor_amax, uint64_t seed,
+                               uint32_t tensor_id, void* Q, int code_format, float* tile_scale, float* tok_err_part,
+                               float* col_err_part, int* d_status, cudaStream_t stream) {
+    int mode;
+    switch (round_mode) {
+        case S3R_ROUND_S3R: mode = kS3R; break;
+        case S3R_ROUND_S3R_7BIT: mode = kS3R7; break;
+        case S3R_ROUND_BCAST: mode = kBCAST; break;
+        case S3R_ROUND_RTNE: mode = kRTNE; break;
+        case S3R_ROUND_INDEP: mode = kINDEP; break;
+        default: return S3R_ERR_ARG;
+    }
+    if (round_mode == S3R_ROUND_BCAST && S > 0 && T % S != 0) return S3R_ERR_SHAPE;
+    const bool partials = round_mode == S3R_ROUND_S3R || round_mode == S3R_ROUND_S3R_7BIT ||
+                          round_mode == S3R_ROUND_BCAST;
+    return launch_tile_quant(mode, G, T, N, ldg, s_x, s_w, seed, tensor_id, Q, code_format, tile_scale,
+                             partials ? tok_err_part : nullptr, partials ? col_err_part : nullptr, d_status, stream,
+                             S, tensor_amax);
 }
 
 extern "C" int indep_sr_quantize(const void* G, int64_t T, int64_t N, int64_t ldg, const float* s_x,
@@ -1345,6 +1419,10 @@ static int try_swiglu_tma(int round_mode, const SwigluArgs& A, const QuantCommon
                                         : launch_swiglu_tma<kRTNE, 0>(maps, A, C, O1, O3, ntiles, stream);
         case S3R_ROUND_S3R: return f16 ? launch_swiglu_tma<kS3R, 1>(maps, A, C, O1, O3, ntiles, stream)
                                        : launch_swiglu_tma<kS3R, 0>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_S3R_7BIT: return f16 ? launch_swiglu_tma<kS3R7, 1>(maps, A, C, O1, O3, ntiles, stream)
+                                            : launch_swiglu_tma<kS3R7, 0>(maps, A, C, O1, O3, ntiles, stream);
+        case S3R_ROUND_BCAST: return f16 ? launch_swiglu_tma<kBCAST, 1>(maps, A, C, O1, O3, ntiles, stream)
+                                         : launch_swiglu_tma<kBCAST, 0>(maps, A, C, O1, O3, ntiles, stream);
         case S3R_ROUND_INDEP: return f16 ? launch_swiglu_tma<kINDEP, 1>(maps, A, C, O1, O3, ntiles, stream)
                                          : launch_swiglu_tma<kINDEP, 0>(maps, A, C, O1, O3, ntiles, stream);
         default: return S3R_ERR_ARG;
@@ -1356,7 +1434,17 @@ extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, con
                                int code_format, uint64_t seed, uint32_t tid1, uint32_t tid3, void* Q1, float* scale1,
                                float* tok1, float* col1, void* Q3, float* scale3, float* tok3, float* col3,
                                int* d_status, cudaStream_t stream) {
-    if (T < 0 || F < 0 || !valid_fmt(code_format)) return S3R_ERR_ARG;
+    return swiglu_quantize_ex(dA, ldd, h1, h3, ldh, T, F, s_x, s_w1, s_w3, round_mode, 0, code_format, seed, tid1,
+                              tid3, Q1, scale1, tok1, col1, Q3, scale3, tok3, col3, d_status, stream);
+}
+
+extern "C" int swiglu_quantize_ex(const float* dA, int64_t ldd, const void* h1, const void* h3, int64_t ldh,
+                                  int64_t T, int64_t F, const float* s_x, const float* s_w1, const float* s_w3,
+                                  int round_mode, int64_t S, int code_format, uint64_t seed, uint32_t tid1,
+                                  uint32_t tid3, void* Q1, float* scale1, float* tok1, float* col1, void* Q3,
+                                  float* scale3, float* tok3, float* col3, int* d_status, cudaStream_t stream) {
+    if (T < 0 || F < 0 || !valid_fmt(code_format) || S < 0) return S3R_ERR_ARG;
+    if (round_mode == S3R_ROUND_BCAST && S > 0 && T % S != 0) return S3R_ERR_SHAPE;
     if (T == 0 || F == 0) return S3R_OK;
     if (!dA || !h1 || !h3 || !Q1 || !Q3 || !scale1 || !scale3) return S3R_ERR_ARG;
     if (ldd < F || ldh < F) return S3R_ERR_SHAPE;
@@ -1364,7 +1452,7 @@ extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, con
     SwigluArgs A{dA, ldd, static_cast<const uint16_t*>(h1), static_cast<const uint16_t*>(h3), ldh, s_x, s_w1, s_w3,
                  s3r_aligned16(dA) && s3r_aligned16(h1) && s3r_aligned16(h3) && (ldd % 4) == 0 && (ldh % 8) == 0};
     QuantCommon C{T, F, s3r_cdiv(F, kTile), (uint32_t)seed, d_status,
-                  s3r_aligned16(Q1) && s3r_aligned16(Q3) && (F % 8) == 0};
+                  s3r_aligned16(Q1) && s3r_aligned16(Q3) && (F % 8) == 0, S, nullptr};
     QuantOut O1{Q1, code_format, scale1, tok1, col1, tid1}, O3{Q3, code_format, scale3, tok3, col3, tid3};
     const int tma = try_swiglu_tma(round_mode, A, C, O1, O3, stream);
     if (tma <= 0) return tma;   // launched (0) or failed (< 0)
@@ -1372,6 +1460,8 @@ extern "C" int swiglu_quantize(const float* dA, int64_t ldd, const void* h1, con
     switch (round_mode) {
         case S3R_ROUND_RTNE: swiglu_quantize_kernel<kRTNE><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
         case S3R_ROUND_S3R: swiglu_quantize_kernel<kS3R><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
+        case S3R_ROUND_S3R_7BIT: swiglu_quantize_kernel<kS3R7><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
+        case S3R_ROUND_BCAST: swiglu_quantize_kernel<kBCAST><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
         case S3R_ROUND_INDEP: swiglu_quantize_kernel<kINDEP><<<grid, 512, 0, stream>>>(A, C, O1, O3); break;
         default: return S3R_ERR_ARG;
     }

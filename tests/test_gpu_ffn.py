@@ -35,10 +35,12 @@ def _staged(s3r, ops, dY, S, rm, ec, seed, tid_base=0):
     F = ops.A8.shape[1]
     out = {}
     indep = rm == s3r.ROUND_INDEP
-    ecm = ec if rm == s3r.ROUND_S3R else s3r.EC_NONE
+    shared = rm in (s3r.ROUND_S3R, s3r.ROUND_S3R_7BIT, s3r.ROUND_BCAST)
+    ecm = ec if shared else s3r.EC_NONE
     cf = s3r.code_format_of(ops.X8)
-    if rm == s3r.ROUND_S3R:
-        q2 = s3r.s3r_quantize(dY, ops.s_a, ops.s_w2, seed, tid_base + s3r.TID_W2, code_format=cf)
+    if shared:
+        q2, _ = s3r.s3r_quantize_ex(dY, ops.s_a, ops.s_w2, rm, S, seed=seed, tensor_id=tid_base + s3r.TID_W2,
+                                    code_format=cf)
     elif indep:
         q2 = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, tid_base + s3r.TID_W2, code_format=cf)
         out["q2r"] = s3r.indep_sr_quantize(dY, ops.s_a, ops.s_w2, seed, tid_base + s3r.TID_W2 + s3r.RHS_ID_OFFSET,
@@ -51,7 +53,7 @@ def _staged(s3r, ops, dY, S, rm, ec, seed, tid_base=0):
     q2w = out.get("q2r", q2)
     dW2 = s3r.int8_gemm_dw(ops.A8, q2w.Q, q2w.tile_scale, ops.s_w2, ecm, ec2, S)
     q1, q3 = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed, tid_base + s3r.TID_W1,
-                                 tid_base + s3r.TID_W3, code_format=cf)
+                                 tid_base + s3r.TID_W3, code_format=cf, S=S)
     if indep:
         out["q1r"], out["q3r"] = s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3, rm, seed,
                                                      tid_base + s3r.TID_W1 + s3r.RHS_ID_OFFSET,
@@ -78,7 +80,13 @@ def _oracle_ops(orc, inp):
     return orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
 
 
-MODES = [("S3R", "EC_TWO_WAY"), ("S3R", "EC_DX_ONLY"), ("S3R", "EC_NONE"), ("INDEP", "EC_NONE"), ("RTNE", "EC_NONE")]
+MODES = [("S3R", "EC_TWO_WAY"), ("S3R", "EC_DX_ONLY"), ("S3R", "EC_NONE"), ("INDEP", "EC_NONE"), ("RTNE", "EC_NONE"),
+         ("S3R_7BIT", "EC_TWO_WAY"), ("BCAST", "EC_TWO_WAY"), ("S3R", "EC_DW_ONLY")]
+ORACLE_MODE = {"S3R_7BIT": "S3R7"}   # oracle constant names that differ from the library's
+
+
+def _omode(orc, mode):
+    return getattr(orc, ORACLE_MODE.get(mode, mode))
 
 
 @pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
@@ -106,15 +114,19 @@ def _forward_ops_bit_exact(ops_g, ops_o):
 def _flip_effect(D, W8, X8, s_x, s_w, S, ecm, orc):
     """Exact change of (dX, dW) when the dequantized operand changes by D."""
     Dx = D - projection(D, S) if ecm in (orc.EC_DX_ONLY, orc.EC_TWO_WAY) else D
-    Dw = D - projection(D, S) if ecm == orc.EC_TWO_WAY else D
+    Dw = D - projection(D, S) if ecm in (orc.EC_TWO_WAY, orc.EC_DW_ONLY) else D
     ddx = (Dx @ W8.astype(np.float64).T) / s_x[:, None].astype(np.float64)
     ddw = (X8.astype(np.float64).T @ Dw) / s_w[None, :].astype(np.float64)
     return ddx, ddw
 
 
-def _thresholds(orc, mode, T, N, seed, tid):
+def _thresholds(orc, mode, T, N, seed, tid, S=0):
     if mode == "S3R":
         return np.array([orc.token_threshold(t, seed, tid) for t in range(T)])[:, None]
+    if mode == "S3R_7BIT":
+        return np.array([orc.token_threshold7(t, seed, tid) for t in range(T)])[:, None]
+    if mode == "BCAST":
+        return np.array([orc.example_threshold(t // S if S else 0, seed, tid) for t in range(T)])[:, None]
     if mode == "INDEP":
         return np.array([[orc.element_threshold(t * N + n, seed, tid) for n in range(N)] for t in range(T)])
     return 0.5
@@ -137,19 +149,21 @@ def compare_block_with_oracle(s3r, orc, gpu, ops_o, h1, h3, dY, S, mode, ec, see
     near-tie code flips, whose exact linear effect is added to the oracle."""
     T = dY.shape[0]
     F = ops_o.A8.shape[1]
-    omode, oec = getattr(orc, mode), getattr(orc, ec)
+    omode, oec = _omode(orc, mode), getattr(orc, ec)
     ref = orc.ffn_backward(ops_o, h1, h3, dY, S, mode=omode, ec_mode=oec, seed=seed, tid_base=tid_base)
-    ecx = oec if omode == orc.S3R else orc.EC_NONE
+    ecx = oec if omode in orc.SHARED else orc.EC_NONE
+    dx_ec = ecx in (orc.EC_DX_ONLY, orc.EC_TWO_WAY)
+    dw_ec = ecx in (orc.EC_TWO_WAY, orc.EC_DW_ONLY)
     # stage 1: codes exact, dA and dW2 within the fp32 bound
     assert np.array_equal(codes(gpu["q2"].Q), ref.w2.Q)
     w2 = ref.w2
     mdx = dx_magnitude(w2.Q, w2.delta, ops_o.W2_8, ops_o.s_a,
-                       *( (w2.eps, w2.rowsum, w2.v, S) if ecx else (None, None, None, None)))
+                       *( (w2.eps, w2.rowsum, w2.v, S) if dx_ec else (None, None, None, None)))
     assert_close_mag(gpu["dA"].cpu().numpy(), w2.dX, mdx, "dA")
     Qw2 = w2.Q_rhs if omode == orc.INDEP else w2.Q
     dw2 = w2.delta_rhs if omode == orc.INDEP else w2.delta
     mdw = dw_magnitude(ops_o.A8, Qw2, dw2, ops_o.s_w2,
-                       *((w2.colmean, w2.mu, w2.xsum, w2.p) if ecx == orc.EC_TWO_WAY else (None,) * 4))
+                       *((w2.colmean, w2.mu, w2.xsum, w2.p) if dw_ec else (None,) * 4))
     assert_close_mag(gpu["dW2"].cpu().numpy(), w2.dW, mdw, "dW2")
     # stage 2: near-tie flips only; their exact effect added to the oracle
     exp_dX = ref.dX.copy()
@@ -163,7 +177,7 @@ def compare_block_with_oracle(s3r, orc, gpu, ops_o, h1, h3, dY, S, mode, ec, see
         g = ((ops_o.s_x[:, None] * dh).astype(np.float32) * s_w[None, :]).astype(np.float32)
         inv = np.vectorize(lambda a: np.float32(orc.inv127_rz(float(a))))(_tile_amax(g)).astype(np.float32)
         y = (g * expand_tiles(inv, T, F).astype(np.float32)).astype(np.float32)
-        near_tie_flips(Qg, lb.Q, y, _thresholds(orc, mode, T, F, seed, tid))
+        near_tie_flips(Qg, lb.Q, y, _thresholds(orc, mode, T, F, seed, tid, S))
         D = expand_tiles(dg, T, F) * Qg - expand_tiles(lb.delta, T, F) * lb.Q
         ddx, ddw = _flip_effect(D, W8, ops_o.X8, ops_o.s_x, s_w, S, ecx, orc)
         exp_dX += ddx
@@ -174,14 +188,14 @@ def compare_block_with_oracle(s3r, orc, gpu, ops_o, h1, h3, dY, S, mode, ec, see
             Dr = expand_tiles(dr, T, F) * Qr - expand_tiles(lb.delta_rhs, T, F) * lb.Q_rhs
             _, ddw = _flip_effect(Dr, W8, ops_o.X8, ops_o.s_x, s_w, S, ecx, orc)
         exp[name] += ddw
-        if ecx:
+        if dx_ec:
             mags_dx += dx_magnitude(lb.Q, lb.delta, W8, ops_o.s_x, lb.eps, lb.rowsum, lb.v, S)
         else:
             mags_dx += dx_magnitude(lb.Q, lb.delta, W8, ops_o.s_x)
         Qw = lb.Q_rhs if omode == orc.INDEP else lb.Q
         dw_ = lb.delta_rhs if omode == orc.INDEP else lb.delta
         mags[name] = dw_magnitude(ops_o.X8, Qw, dw_, s_w,
-                                  *((lb.colmean, lb.mu, lb.xsum, lb.p) if ecx == orc.EC_TWO_WAY else (None,) * 4))
+                                  *((lb.colmean, lb.mu, lb.xsum, lb.p) if dw_ec else (None,) * 4))
     assert_close_mag(gpu["dX"].cpu().numpy(), exp_dX, mags_dx, "dX")
     assert_close_mag(gpu["dW1"].cpu().numpy(), exp["dW1"], mags["dW1"], "dW1")
     assert_close_mag(gpu["dW3"].cpu().numpy(), exp["dW3"], mags["dW3"], "dW3")

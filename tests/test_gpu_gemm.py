@@ -70,27 +70,28 @@ def _linear(orc, T, K, N, S, seed):
 
 
 @FMTS
-@pytest.mark.parametrize("ec_name", ["EC_NONE", "EC_DX_ONLY", "EC_TWO_WAY"])
+@pytest.mark.parametrize("ec_name", ["EC_NONE", "EC_DX_ONLY", "EC_TWO_WAY", "EC_DW_ONLY"])
 @pytest.mark.parametrize("T,K,N,S", [(256, 512, 1024, 256), (512, 200, 384, 128), (300, 136, 264, 300)])
 def test_linear_backward_parity(s3r, orc, fmt, ec_name, T, K, N, S):
     """dX and dW of one linear layer (the tiny-linear workload and ragged
     variants) through quantize -> correction -> both GEMMs."""
     inp, G, X8, s_x, W8, s_w = _linear(orc, T, K, N, S, seed=T + K + N)
-    ec_mode = getattr(orc, ec_name)
+    ec_mode = getattr(orc, ec_name)      # the oracle's constant
+    ec_lib = getattr(s3r, ec_name)       # the library's
     ref = orc.linear_backward(G, X8, s_x, W8, s_w, S, mode=orc.S3R, ec_mode=ec_mode, seed=11, tensor_id=0)
     c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     q = s3r.s3r_quantize(inp.dY.cuda(), c(s_x), c(s_w), seed=11, tensor_id=0, code_format=fmt)
-    ec = s3r.s3r_ec_correct(q, T, N, S, _dev(W8, fmt), _dev(X8, fmt), ec_mode=ec_mode) if ec_mode else None
-    dX = s3r.int8_gemm_dx(q.Q, q.tile_scale, _dev(W8, fmt), c(s_x), ec_mode, ec, S)
-    dW = s3r.int8_gemm_dw(_dev(X8, fmt), q.Q, q.tile_scale, c(s_w), ec_mode, ec, S)
+    ec = s3r.s3r_ec_correct(q, T, N, S, _dev(W8, fmt), _dev(X8, fmt), ec_mode=ec_lib) if ec_lib else None
+    dX = s3r.int8_gemm_dx(q.Q, q.tile_scale, _dev(W8, fmt), c(s_x), ec_lib, ec, S)
+    dW = s3r.int8_gemm_dw(_dev(X8, fmt), q.Q, q.tile_scale, c(s_w), ec_lib, ec, S)
     torch.cuda.synchronize()
     assert np.array_equal(codes(q.Q), ref.Q)
-    if ec_mode:
+    if ec_mode in (orc.EC_DX_ONLY, orc.EC_TWO_WAY):
         mdx = dx_magnitude(ref.Q, ref.delta, W8, s_x, ref.eps, ref.rowsum, ref.v, S)
     else:
         mdx = dx_magnitude(ref.Q, ref.delta, W8, s_x)
     assert_close_mag(dX.cpu().numpy(), ref.dX, mdx, "dX")
-    if ec_mode == orc.EC_TWO_WAY:
+    if ec_mode in (orc.EC_TWO_WAY, orc.EC_DW_ONLY):
         mdw = dw_magnitude(X8, ref.Q, ref.delta, s_w, ref.colmean, ref.mu, ref.xsum, ref.p)
     else:
         mdw = dw_magnitude(X8, ref.Q, ref.delta, s_w)

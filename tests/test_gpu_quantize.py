@@ -142,3 +142,55 @@ def test_zero_tile(s3r):
     assert tok[150, 2] == np.float32(want)
     tok[150, 2] = 0.0
     assert not tok.any() and float(o.col_err_part.cpu()[0].abs().sum()) == 0.0
+
+
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
+@pytest.mark.parametrize("mode,S", [("S3R_7BIT", 0), ("BCAST", 0), ("BCAST", 128), ("BCAST", 256)])
+@pytest.mark.parametrize("T,N,fold", [(256, 1024, True), (300, 260, False), (512, 384, True), (129, 136, True)])
+def test_paper_modes_parity(s3r, orc, fmt, mode, S, T, N, fold):
+    """The paper's 7-bit thresholds and the per-example Phi_bcast: codes and
+    tile scales bit for bit, error partials within the fp32 bound."""
+    if S and T % S:
+        pytest.skip("examples must tile the rows")
+    Gb, s_x, s_w = _case(T, N, T * 5 + N + S)
+    sxd, swd = (s_x.cuda(), s_w.cuda()) if fold else (None, None)
+    seed, tid = 77, 9
+    o, amax = s3r.s3r_quantize_ex(Gb.cuda(), sxd, swd, getattr(s3r, "ROUND_" + mode), S, seed=seed, tensor_id=tid,
+                                  code_format=fmt)
+    torch.cuda.synchronize()
+    assert amax is None
+    G = orc.from_torch_bf16(Gb)
+    omode = orc.S3R7 if mode == "S3R_7BIT" else orc.BCAST
+    Qo, do, Eo, st = orc.quantize(G, s_x.numpy() if fold else None, s_w.numpy() if fold else None, mode=omode,
+                                  seed=seed, tensor_id=tid, S=S)
+    assert st == 0
+    assert np.array_equal(codes(o.Q), Qo), f"codes differ in {(codes(o.Q) != Qo).sum()} elements"
+    assert np.array_equal(o.tile_scale.cpu().numpy(), do)
+    tok_o, col_o = orc.error_partials(Eo)
+    tok_m, col_m = orc.error_partials(np.abs(Eo))
+    assert_close_mag(o.tok_err_part.cpu().numpy(), tok_o, tok_m, "tok_err_part")
+    assert_close_mag(o.col_err_part.cpu().numpy(), col_o, col_m, "col_err_part")
+
+
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
+@pytest.mark.parametrize("mode", ["S3R", "S3R_7BIT", "RTNE"])
+@pytest.mark.parametrize("T,N", [(384, 512), (300, 260)])
+def test_per_tensor_step_parity(s3r, orc, fmt, mode, T, N):
+    """[S3R]'s per-tensor step: one Delta = max|G'|/127 for every tile, codes
+    bit for bit against the oracle with one tile covering the tensor."""
+    Gb, s_x, s_w = _case(T, N, T + 3 * N, outliers=True)
+    o, amax = s3r.s3r_quantize_ex(Gb.cuda(), s_x.cuda(), s_w.cuda(), getattr(s3r, "ROUND_" + mode), 0,
+                                  per_tensor=True, seed=3, tensor_id=1, code_format=fmt)
+    torch.cuda.synchronize()
+    G = orc.from_torch_bf16(Gb)
+    omode = {"S3R": orc.S3R, "S3R_7BIT": orc.S3R7, "RTNE": orc.RTNE}[mode]
+    Qo, do, Eo, _ = orc.quantize(G, s_x.numpy(), s_w.numpy(), mode=omode, seed=3, tensor_id=1, tile=(T, N))
+    g = ((s_x.numpy()[:, None] * G).astype(np.float32) * s_w.numpy()[None, :]).astype(np.float32)
+    assert amax.item() == np.abs(g).max()
+    assert np.array_equal(codes(o.Q), Qo)
+    assert np.all(o.tile_scale.cpu().numpy() == do[0, 0])
+    if mode != "RTNE":
+        tok_o, col_o = orc.error_partials(Eo)
+        tok_m, col_m = orc.error_partials(np.abs(Eo))
+        assert_close_mag(o.tok_err_part.cpu().numpy(), tok_o, tok_m, "tok_err_part")
+        assert_close_mag(o.col_err_part.cpu().numpy(), col_o, col_m, "col_err_part")

@@ -27,22 +27,25 @@ def _swiglu_case(T, F, seed):
 
 
 @pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
-@pytest.mark.parametrize("mode", ["S3R", "INDEP", "RTNE"])
+@pytest.mark.parametrize("mode", ["S3R", "INDEP", "RTNE", "S3R_7BIT", "BCAST"])
 @pytest.mark.parametrize("T,F", [(256, 384), (300, 200), (129, 1000), (64, 8)])
 def test_swiglu_quantize_parity(s3r, orc, fmt, mode, T, F):
     dA, h1, h3, s_x, s_w1, s_w3 = _swiglu_case(T, F, T + F)
+    S = 128 if mode == "BCAST" and T % 128 == 0 else 0
     c = lambda a: torch.from_numpy(a).cuda()
     o1, o3 = s3r.swiglu_quantize(c(dA), h1.cuda(), h3.cuda(), c(s_x), c(s_w1), c(s_w3),
-                                 round_mode=getattr(s3r, "ROUND_" + mode), seed=42, tid1=1, tid3=2, code_format=fmt)
+                                 round_mode=getattr(s3r, "ROUND_" + mode), seed=42, tid1=1, tid3=2, code_format=fmt,
+                                 S=S)
     torch.cuda.synchronize()
     dh1, dh3 = orc.swiglu_bwd(dA, orc.from_torch_bf16(h1), orc.from_torch_bf16(h3))
+    omode = orc.S3R7 if mode == "S3R_7BIT" else getattr(orc, mode)
     for o, g, s_w, tid in ((o1, dh1, s_w1, 1), (o3, dh3, s_w3, 2)):
-        Qo, do, Eo, st = orc.quantize(g, s_x, s_w, mode=getattr(orc, mode), seed=42, tensor_id=tid)
+        Qo, do, Eo, st = orc.quantize(g, s_x, s_w, mode=omode, seed=42, tensor_id=tid, S=S)
         assert st == 0
         Qg = codes(o.Q)
         assert np.array_equal(Qg, Qo), f"{mode} tid {tid}: {(Qg != Qo).sum()} codes differ"
         assert np.array_equal(o.tile_scale.cpu().numpy(), do)
-        if mode == "S3R":
+        if omode in orc.SHARED:
             t_o, c_o = orc.error_partials(Eo)
             t_m, c_m = orc.error_partials(np.abs(Eo))
             assert_close_mag(o.tok_err_part.cpu().numpy(), t_o, t_m, "tok")
@@ -50,7 +53,7 @@ def test_swiglu_quantize_parity(s3r, orc, fmt, mode, T, F):
 
 
 @pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
-@pytest.mark.parametrize("ec_mode", ["EC_DX_ONLY", "EC_TWO_WAY"])
+@pytest.mark.parametrize("ec_mode", ["EC_DX_ONLY", "EC_TWO_WAY", "EC_DW_ONLY"])
 @pytest.mark.parametrize("T,N,K,S", [(256, 1024, 512, 256), (512, 384, 200, 128), (300, 260, 72, 300),
                                      (1024, 256, 130, 256), (1280, 256, 136, 128), (384, 5632, 264, 128),
                                      (512, 7000, 264, 128), (256, 512, 5008, 128)])
@@ -76,10 +79,11 @@ def test_ec_factors_parity(s3r, orc, fmt, ec_mode, T, N, K, S):
     assert_close_mag(ec.eps.cpu().numpy(), eps, eps_m, "eps")
     assert_close_mag(ec.colmean.cpu().numpy(), colmean, cm_m, "colmean")
     assert_close_mag(ec.mu.cpu().numpy(), mu, mu_m, "mu")
-    assert np.array_equal(ec.rowsum.cpu().numpy(), rowsum)
-    v_m = (np.abs(colmean) + np.abs(mu)[:, None]) @ np.abs(W8.astype(np.float64)).T
-    assert_close_mag(ec.v.cpu().numpy(), v, v_m + cm_m @ np.abs(W8.astype(np.float64)).T, "v")
-    if ec_mode == "EC_TWO_WAY":
+    if ec_mode != "EC_DW_ONLY":   # the weight-side factors are not needed by the dW-only ablation
+        assert np.array_equal(ec.rowsum.cpu().numpy(), rowsum)
+        v_m = (np.abs(colmean) + np.abs(mu)[:, None]) @ np.abs(W8.astype(np.float64)).T
+        assert_close_mag(ec.v.cpu().numpy(), v, v_m + cm_m @ np.abs(W8.astype(np.float64)).T, "v")
+    if ec_mode in ("EC_TWO_WAY", "EC_DW_ONLY"):
         assert np.array_equal(ec.xsum.cpu().numpy(), xsum)
         p_m = np.abs(X8.astype(np.float64)).T @ (np.abs(eps) + eps_m)
         assert_close_mag(ec.p.cpu().numpy(), p, p_m, "p")
