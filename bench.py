@@ -378,6 +378,11 @@ def time_quantize_sweep(s3r, steps=20):
         "s3r_f16_codes": (lambda i: s3r.s3r_quantize(G, seed=i, out=q16), 2 + 2 + part),
         "indep_sr_one_copy": (lambda i: s3r.indep_sr_quantize(G, seed=i, out=qi), 3.0),
         "rtne": (lambda i: s3r.rtne_quantize(G, Q=Qr, scale=sr), 3.0),
+        # the paper's thresholds (7-bit, four per word) and its per-tensor step (one extra read
+        # of the gradient for the global absmax before the quantization pass)
+        "s3r_7bit": (lambda i: s3r.s3r_quantize_ex(G, round_mode=s3r.ROUND_S3R_7BIT, seed=i, out=q8), 2 + 1 + part),
+        "s3r_7bit_per_tensor": (lambda i: s3r.s3r_quantize_ex(G, round_mode=s3r.ROUND_S3R_7BIT, per_tensor=True,
+                                                              seed=i, out=q8), 2 + 2 + 1 + part),
     }
     for name, (fn, bpe) in runs.items():
         for i in range(3):
@@ -393,6 +398,24 @@ def time_quantize_sweep(s3r, steps=20):
         out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(bpe * Tq * Nq / (ms * 1e-3) / 1e9, 1),
                      "alg_bytes_per_elem": round(bpe, 4)}
     out["shape"] = [Tq, Nq]
+    # the other row counts of the sweep, S3R with int8 codes
+    for Tx in (4096, 65536):
+        Gx = workloads.quantize_sweep_input(Tx, Nq, seed=workloads.DATA_SEED + 3).cuda()
+        qx = s3r.s3r_quantize(Gx, code_format=S8)
+        for i in range(3):
+            s3r.s3r_quantize(Gx, seed=i, out=qx)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(steps):
+            s3r.s3r_quantize(Gx, seed=i, out=qx)
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        out[f"s3r_T{Tx}"] = {"us": round(ms * 1e3, 2), "GB_s": round((3 + part) * Tx * Nq / (ms * 1e-3) / 1e9, 1),
+                             "alg_bytes_per_elem": round(3 + part, 4),
+                             "l2_note": "input 64 MB < L2: repeated calls partly hit L2" if Tx == 4096 else ""}
+        del Gx, qx
     return out
 
 
@@ -492,7 +515,11 @@ def run_ours(args, world, rank, local):
     if not args.no_context and rank == 0:
         ctx = {}
         for name, rm, ec in (("s3r_ec_dx_only", s3r.ROUND_S3R, s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE),
-                             ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE)):
+                             ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE),
+                             # the paper's own variants: 7-bit thresholds, Phi_bcast, the dW-only correction
+                             ("s3r_7bit_ec_two_way", s3r.ROUND_S3R_7BIT, s3r.EC_TWO_WAY),
+                             ("s3r_bcast_ec_two_way", s3r.ROUND_BCAST, s3r.EC_TWO_WAY),
+                             ("s3r_ec_dw_only", s3r.ROUND_S3R, s3r.EC_DW_ONLY)):
             m, _, _, _ = time_ffn(s3r, ops, dY, 10, 2, rm, ec, 1)
             ctx[name] = {"tokens_s": round(T * 10 / (m * 1e-3), 1), "ms": round(m / 10, 4)}
         _, ops8 = device_setup(s3r, rank, s3r.CODES_S8)
@@ -504,7 +531,8 @@ def run_ours(args, world, rank, local):
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / ms_step, 3)
         ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / ms_step, 3)
         qs = time_quantize_sweep(s3r)
-        for k in ("s3r", "s3r_f16_codes", "indep_sr_one_copy", "rtne"):
+        for k in ("s3r", "s3r_f16_codes", "indep_sr_one_copy", "rtne", "s3r_7bit", "s3r_7bit_per_tensor",
+                  "s3r_T4096", "s3r_T65536"):
             qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
         ctx["quantize_sweep"] = qs
         ctx["moe_e8_d4096_F1408_tok16384_top2"] = time_moe(s3r)

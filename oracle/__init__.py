@@ -62,6 +62,8 @@ def lib():
             L.orc_example_threshold.restype = C.c_float
             L.orc_example_threshold.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32]
             L.orc_quantize_window_ex.restype = C.c_int
+            L.orc_float_to_bf16.restype = C.c_uint16
+            L.orc_float_to_bf16.argtypes = [C.c_float]
             L.orc_inv127_rz.restype = C.c_float
             L.orc_inv127_rz.argtypes = [C.c_float]
             L.orc_sr_step.restype = C.c_float
@@ -365,6 +367,69 @@ class FFNForwardOperands:
     s_w3: np.ndarray
     W2_8: np.ndarray
     s_w2: np.ndarray
+
+
+def gemm_fwd(X8, s_x, W8, s_w):
+    """INT8 forward Y = diag(s_x) X8 W8 diag(s_w): exact int32 per 128-wide block,
+    blocks added in fp32 in order, then (acc * s_x) * s_w in fp32 ([S3R] §III-A)."""
+    X8 = np.ascontiguousarray(X8, dtype=np.int8)
+    W8 = np.ascontiguousarray(W8, dtype=np.int8)
+    T, K = X8.shape
+    N = W8.shape[1]
+    Y = np.zeros((T, N), dtype=np.float32)
+    lib().orc_gemm_fwd(_p(X8), _p(_f32(s_x)), _p(W8), _p(_f32(s_w)), _i64(T), _i64(K), _i64(N), _p(Y))
+    return Y
+
+
+def to_bf16_bits(x) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest even."""
+    x = _f32(x)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    for idx, v in np.ndenumerate(x):
+        out[idx] = lib().orc_float_to_bf16(float(v))
+    return out
+
+
+def swiglu_fwd(h1f, h3f):
+    """Forward gate: bf16 h1, h3 (bit patterns) and a = bf16(silu(h1) h3)."""
+    h1f, h3f = _f32(h1f), _f32(h3f)
+    h1b = np.zeros(h1f.shape, dtype=np.uint16)
+    h3b = np.zeros(h1f.shape, dtype=np.uint16)
+    ab = np.zeros(h1f.shape, dtype=np.uint16)
+    lib().orc_swiglu_fwd(_p(h1f), _p(h3f), _i64(h1f.size), _p(h1b), _p(h3b), _p(ab))
+    return h1b, h3b, ab
+
+
+@dataclass
+class FFNForward:
+    X8: np.ndarray
+    s_x: np.ndarray
+    W1_8: np.ndarray
+    s_w1: np.ndarray
+    W3_8: np.ndarray
+    s_w3: np.ndarray
+    W2_8: np.ndarray
+    s_w2: np.ndarray
+    h1: np.ndarray      # bf16 bit patterns [T, F]
+    h3: np.ndarray
+    a: np.ndarray
+    A8: np.ndarray
+    s_a: np.ndarray
+    Y: np.ndarray       # fp32 [T, d]
+
+
+def ffn_forward_int8(X, W1, W3, W2) -> FFNForward:
+    """The SwiGLU block forward with INT8 GEMMs: RTNE operands (per-token X and
+    a, per-output-channel weights), h1 = X W1 and h3 = X W3 saved as bf16,
+    a = silu(h1) h3 in bf16, then Y = a W2 (fp32)."""
+    X8, s_x = rtne_operand(X, 0)
+    W1_8, s_w1 = rtne_operand(W1, 1)
+    W3_8, s_w3 = rtne_operand(W3, 1)
+    W2_8, s_w2 = rtne_operand(W2, 1)
+    h1b, h3b, ab = swiglu_fwd(gemm_fwd(X8, s_x, W1_8, s_w1), gemm_fwd(X8, s_x, W3_8, s_w3))
+    A8, s_a = rtne_operand(bf16_to_f32(ab), 0)
+    Y = gemm_fwd(A8, s_a, W2_8, s_w2)
+    return FFNForward(X8, s_x, W1_8, s_w1, W3_8, s_w3, W2_8, s_w2, h1b, h3b, ab, A8, s_a, Y)
 
 
 def ffn_forward_operands(X, W1, W3, W2, a) -> FFNForwardOperands:

@@ -523,3 +523,50 @@ void orc_swiglu_bwd(const float* dA, const float* h1, const float* h3, int64_t n
         dh3[i] = dA[i] * silu;
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* INT8 forward ([S3R] §III-A: Y = diag(s_x) X_hat W_hat diag(s_w), with the  */
+/* RTNE operands of orc_rtne_operand).  The contraction runs in 128-wide      */
+/* blocks: each block's int32 sum is exact, the blocks are added in ascending */
+/* order in fp32, and the result is rescaled in fp32 as (acc * s_x[t]) *      */
+/* s_w[n].  X8 [T, K] int8, W8 [K, N] int8, Y [T, N] fp32.                    */
+/* ------------------------------------------------------------------------- */
+void orc_gemm_fwd(const int8_t* X8, const float* s_x, const int8_t* W8, const float* s_w, int64_t T, int64_t K,
+                  int64_t N, float* Y) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int64_t k0 = 0; k0 < K; k0 += 128) {
+                int32_t blk = 0;
+                for (int64_t k = k0; k < K && k < k0 + 128; ++k)
+                    blk += (int32_t)X8[t * K + k] * (int32_t)W8[k * N + n];
+                acc = acc + (float)blk;
+            }
+            float y = acc * s_x[t];
+            Y[t * N + n] = y * s_w[n];
+        }
+}
+
+/* fp32 to bf16 bits, rounded to nearest even (NaN kept quiet). */
+uint16_t orc_float_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* The SwiGLU gate of the forward (the FFN block of [S3R] §IV-A): the GEMM
+ * outputs are saved as bf16 (h1, h3: the activations the backward reads), and
+ * a = silu(h1) * h3 is formed from those bf16 values in fp32, in this order:
+ *   s = sigmoid(h1),  silu = h1 * s,  a = bf16(silu * h3). */
+void orc_swiglu_fwd(const float* h1f, const float* h3f, int64_t n, uint16_t* h1b, uint16_t* h3b, uint16_t* ab) {
+    for (int64_t i = 0; i < n; ++i) {
+        h1b[i] = orc_float_to_bf16(h1f[i]);
+        h3b[i] = orc_float_to_bf16(h3f[i]);
+        float x = orc_bf16_to_float(h1b[i]), z = orc_bf16_to_float(h3b[i]);
+        float s = orc_sigmoidf(x);
+        float silu = x * s;
+        ab[i] = orc_float_to_bf16(silu * z);
+    }
+}
