@@ -361,6 +361,54 @@ def time_ffn_large(s3r, steps=5, warmup=2):
     return out
 
 
+def _event_ms(fn, steps, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        fn()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
+def time_forward(s3r, inp, pk, steps=10, warmup=3):
+    """Context: the block's INT8 forward (ffn_forward: RTNE X and weights, the
+    gate/up GEMM with the SwiGLU gate in its epilogue, RTNE a, the down GEMM),
+    its two GEMMs alone, and the BF16 cuBLAS forward of the same block."""
+    c = lambda t: t.cuda()
+    X, W1, W3, W2 = c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2)
+    st = s3r.new_status()
+    out = s3r.alloc_ffn_forward(T, D, F)
+    fwd = lambda: s3r.ffn_forward(X, W1, W3, W2, out=out, status=st)
+    ms = _event_ms(fwd, steps, warmup)
+    o = out.ops
+    gate = lambda: s3r.int8_gemm_fwd_swiglu(o.X8, o.s_x, o.W1_8, o.s_w1, o.W3_8, o.s_w3, o.h1, o.h3, out.a,
+                                            status=st)
+    gms = _event_ms(gate, steps, warmup)
+    down = lambda: s3r.int8_gemm_fwd(o.A8, o.s_a, o.W2_8, o.s_w2, Y=out.Y, status=st)
+    dms = _event_ms(down, steps, warmup)
+    s3r.check_status(st)
+
+    def bf16():
+        h1, h3 = X @ W1, X @ W3
+        a = (torch.nn.functional.silu(h1.float()) * h3.float()).to(torch.bfloat16)
+        return a @ W2
+
+    bms = _event_ms(bf16, steps, warmup)
+    peak = pk.get("bf16_tflops")
+    tf = lambda flops, t: round(flops / (t * 1e-3) / 1e12, 1)
+    return {"ms": round(ms, 4), "tokens_s": round(T / (ms * 1e-3), 1), "tflops": tf(6.0 * T * D * F, ms),
+            "gate_up_gemm_swiglu": {"ms": round(gms, 4), "tflops": tf(4.0 * T * D * F, gms),
+                                    "frac_bf16_burst": round(4.0 * T * D * F / (gms * 1e-3) / 1e12 / peak, 3)},
+            "down_gemm": {"ms": round(dms, 4), "tflops": tf(2.0 * T * D * F, dms),
+                          "frac_bf16_burst": round(2.0 * T * D * F / (dms * 1e-3) / 1e12 / peak, 3)},
+            "bf16_cublas_forward": {"ms": round(bms, 4), "tokens_s": round(T / (bms * 1e-3), 1)},
+            "vs_bf16": round(bms / ms, 3)}
+
+
 def time_quantize_sweep(s3r, steps=20):
     """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100
     outliers; int8 codes (1 B) and fp16-carried codes (2 B)."""
@@ -530,6 +578,12 @@ def run_ours(args, world, rank, local):
         ctx["bf16_cublas_backward"] = {"tokens_s": round(T / (bms * 1e-3), 1), "ms": round(bms, 4)}
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / ms_step, 3)
         ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / ms_step, 3)
+        fw = time_forward(s3r, inp, pk)
+        ctx["forward_int8"] = fw
+        # one INT8 training step of the block: this forward + the timed backward
+        ctx["train_step_int8_vs_bf16"] = {
+            "int8_ms": round(fw["ms"] + ms_step, 4),
+            "bf16_ms": round(fw["bf16_cublas_forward"]["ms"] + ctx["bf16_cublas_backward"]["ms"], 4)}
         qs = time_quantize_sweep(s3r)
         for k in ("s3r", "s3r_f16_codes", "indep_sr_one_copy", "rtne", "s3r_7bit", "s3r_7bit_per_tensor",
                   "s3r_T4096", "s3r_T65536"):

@@ -330,6 +330,79 @@ int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int cod
                  int* d_status, cudaStream_t stream);
 
 /*
+ * int8_gemm_fwd -- the INT8 forward product of one linear ([S3R] §III-A:
+ * the forward operands are rounded to nearest with a per-token scale for the
+ * input and a per-output-channel scale for the weight, multiplied with S32
+ * accumulation and rescaled on both sides):
+ *   Y[t, n] = (acc[t, n] * s_x[t]) * s_w[n]            in fp32, in this order,
+ *   acc     = sum over 128-wide blocks kb (ascending) of the exact integer
+ *             block sum  sum_{k in kb} X8[t, k] W8[k, n], added in fp32.
+ * Each block sum is below 2^24 in magnitude, so it is exact; only the
+ * block-to-block additions and the two rescales round.
+ * In : X8 [T, K] codes (row stride K), s_x [T]; W8 [K, N] codes as stored
+ *      (row stride N), s_w [N].  code_format must be S3R_CODES_F16
+ *      (S3R_ERR_UNSUPPORTED otherwise); K and N multiples of 8 and X8, W8
+ *      16-byte aligned (S3R_ERR_ALIGN).
+ * Out: Y [T, N] fp32 (row stride N).  K == 0 gives Y = 0.
+ * One tcgen05 launch; d_status as for int8_gemm_dx.
+ */
+int int8_gemm_fwd(const void* X8, const float* s_x, const void* W8, const float* s_w, int code_format, int64_t T,
+                  int64_t K, int64_t N, float* Y, int* d_status, cudaStream_t stream);
+
+/*
+ * int8_gemm_fwd_swiglu -- the gate and up projections of the SwiGLU block
+ * (FFN block of [S3R] §IV-A) on one input, with the gate in the epilogue:
+ *   h1 = bf16(Y1), h3 = bf16(Y3)     Y1, Y3 as int8_gemm_fwd with (W1_8, s_w1)
+ *                                    and (W3_8, s_w3); bf16 = nearest even
+ *   a  = bf16((h1 * s) * h3),  s = 1 / (1 + exp(-h1))   in fp32 from the
+ *        bf16 h1 and h3, exp as in swiglu_quantize.
+ * h1 and h3 are the activations the backward reads; a feeds the next linear.
+ * In : X8 [T, K], s_x [T]; W1_8, W3_8 [K, F] (row stride F), s_w1, s_w3 [F];
+ *      same format and alignment rules as int8_gemm_fwd.
+ * Out: h1, h3, a [T, F] bf16 (row stride F).  One tcgen05 launch.
+ */
+int int8_gemm_fwd_swiglu(const void* X8, const float* s_x, const void* W1_8, const float* s_w1, const void* W3_8,
+                         const float* s_w3, int code_format, int64_t T, int64_t K, int64_t F, void* h1, void* h3,
+                         void* a, int* d_status, cudaStream_t stream);
+
+/*
+ * ffn_forward -- the SwiGLU FFN block forward with INT8 GEMMs, the operands
+ * of ffn_backward as its outputs:
+ *   1. X8, s_x   = rtne_quantize(X, per row)
+ *   2. W1_8, W3_8, W2_8 and their scales = rtne_quantize(W, per column)
+ *      (skipped when quantize_weights == 0: they are inputs then)
+ *   3. h1, h3, a = int8_gemm_fwd_swiglu(X8, W1_8, W3_8)
+ *   4. A8, s_a   = rtne_quantize(a, per row)
+ *   5. Y         = int8_gemm_fwd(A8, s_a, W2_8, s_w2)
+ * All on `stream`, no host synchronization, no workspace.
+ */
+struct s3r_ffn_fwd_args {
+    int64_t T, d, F;             /* tokens, model width, FFN width (d and F multiples of 8) */
+    const void* X;               /* bf16 [T, d] */
+    const void* W1;              /* bf16 [d, F] (read when quantize_weights) */
+    const void* W3;              /* bf16 [d, F] */
+    const void* W2;              /* bf16 [F, d] */
+    int quantize_weights;        /* 1: step 2 runs; 0: W*_8 and s_w* hold the weights' codes */
+    int code_format;             /* S3R_CODES_F16 */
+    void* X8;                    /* out [T, d] codes, s_x [T] */
+    float* s_x;
+    void* W1_8;                  /* out/in [d, F] codes, s_w1 [F] */
+    float* s_w1;
+    void* W3_8;                  /* out/in [d, F] codes, s_w3 [F] */
+    float* s_w3;
+    void* W2_8;                  /* out/in [F, d] codes, s_w2 [d] */
+    float* s_w2;
+    void* h1;                    /* out bf16 [T, F] */
+    void* h3;                    /* out bf16 [T, F] */
+    void* a;                     /* out bf16 [T, F] */
+    void* A8;                    /* out [T, F] codes, s_a [T] */
+    float* s_a;
+    float* Y;                    /* out fp32 [T, d] */
+    int* d_status;               /* device int or NULL */
+};
+int ffn_forward(const struct s3r_ffn_fwd_args* args, cudaStream_t stream);
+
+/*
  * ffn_backward -- the whole SwiGLU FFN block backward (FFN block of [S3R]
  * §IV-A, Table III), y = (silu(X W1) * (X W3)) W2:
  *   1. quantize dY (fold s_a, s_w2) -> Q2          [tensor id 0]

@@ -69,6 +69,10 @@ _SIGS = {
     "int8_gemm_dw_workspace_size": (_SZ, [_I64, _I64, _I64, _INT]),
     "int8_gemm_dw": (_INT, [_VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP, _VP,
                             _SZ, _VP, _VP]),
+    "int8_gemm_fwd": (_INT, [_VP, _VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _VP]),
+    "int8_gemm_fwd_swiglu": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _VP, _VP,
+                                    _VP]),
+    "ffn_forward": (_INT, [_VP, _VP]),
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
@@ -384,6 +388,77 @@ def debug_dw_blocks(X8, Q, stream=None):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
     _check(lib().s3r_debug_dw_blocks(_ptr(X8), _ptr(Q), fmt, T, K, N, _ptr(out), _ptr(ws), ws.numel(),
                                      _stream(stream)), "s3r_debug_dw_blocks")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# forward GEMMs
+# ---------------------------------------------------------------------------
+def int8_gemm_fwd(X8, s_x, W8, s_w, Y=None, status=None, stream=None):
+    """Y = (X8 W8 * s_x[t]) * s_w[n] in fp32; X8 [T, K], W8 [K, N] fp16 codes."""
+    T, K = X8.shape
+    N = W8.shape[1]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.float32, device=X8.device)
+    _check(lib().int8_gemm_fwd(_ptr(X8), _ptr(s_x), _ptr(W8), _ptr(s_w), _fmt2(X8, W8), T, K, N, _ptr(Y),
+                               _ptr(status), _stream(stream)), "int8_gemm_fwd")
+    return Y
+
+
+def int8_gemm_fwd_swiglu(X8, s_x, W1_8, s_w1, W3_8, s_w3, h1=None, h3=None, a=None, status=None, stream=None):
+    """The gate and up projections with the SwiGLU gate: returns bf16 (h1, h3, a)."""
+    T, K = X8.shape
+    F = W1_8.shape[1]
+    out = [t if t is not None else torch.empty((T, F), dtype=torch.bfloat16, device=X8.device) for t in (h1, h3, a)]
+    _check(lib().int8_gemm_fwd_swiglu(_ptr(X8), _ptr(s_x), _ptr(W1_8), _ptr(s_w1), _ptr(W3_8), _ptr(s_w3),
+                                      _fmt2(X8, W1_8), T, K, F, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                      _ptr(status), _stream(stream)), "int8_gemm_fwd_swiglu")
+    return tuple(out)
+
+
+class _FfnFwdArgs(C.Structure):
+    _fields_ = [("T", C.c_int64), ("d", C.c_int64), ("F", C.c_int64),
+                ("X", _VP), ("W1", _VP), ("W3", _VP), ("W2", _VP),
+                ("quantize_weights", C.c_int), ("code_format", C.c_int),
+                ("X8", _VP), ("s_x", _VP), ("W1_8", _VP), ("s_w1", _VP), ("W3_8", _VP), ("s_w3", _VP),
+                ("W2_8", _VP), ("s_w2", _VP), ("h1", _VP), ("h3", _VP), ("a", _VP), ("A8", _VP), ("s_a", _VP),
+                ("Y", _VP), ("d_status", _VP)]
+
+
+@dataclass
+class FFNForward:
+    """The block forward's outputs: the backward's operands, a and Y."""
+    ops: "FFNOperands"
+    a: torch.Tensor
+    Y: torch.Tensor
+
+
+def alloc_ffn_forward(T, d, F, device="cuda") -> FFNForward:
+    """Output buffers of ffn_forward (fp16 codes)."""
+    e = lambda *shape, dt=torch.float16: torch.empty(shape, dtype=dt, device=device)
+    f32, bf = torch.float32, torch.bfloat16
+    ops = FFNOperands(e(T, d), e(T, dt=f32), e(T, F), e(T, dt=f32), e(d, F), e(F, dt=f32), e(d, F), e(F, dt=f32),
+                      e(F, d), e(d, dt=f32), e(T, F, dt=bf), e(T, F, dt=bf))
+    return FFNForward(ops, e(T, F, dt=bf), e(T, d, dt=f32))
+
+
+def ffn_forward(X, W1=None, W3=None, W2=None, out: FFNForward | None = None, quantize_weights=True, status=None,
+                stream=None) -> FFNForward:
+    """The SwiGLU block forward with INT8 GEMMs (one C call, five launches):
+    RTNE X and (unless quantize_weights is False, in which case `out.ops`
+    already holds the weights' codes) the weights, h1/h3/a through the fused
+    gate, RTNE a, Y = a W2."""
+    T, d = X.shape
+    F = out.ops.W1_8.shape[1] if out is not None else W1.shape[1]
+    if out is None:
+        out = alloc_ffn_forward(T, d, F, X.device)
+    o = out.ops
+    args = _FfnFwdArgs(T, d, F, _ptr(_bits(X)), _ptr(_bits(W1) if W1 is not None else None),
+                       _ptr(_bits(W3) if W3 is not None else None), _ptr(_bits(W2) if W2 is not None else None),
+                       int(quantize_weights), CODES_F16, _ptr(o.X8), _ptr(o.s_x), _ptr(o.W1_8), _ptr(o.s_w1),
+                       _ptr(o.W3_8), _ptr(o.s_w3), _ptr(o.W2_8), _ptr(o.s_w2), _ptr(o.h1), _ptr(o.h3), _ptr(out.a),
+                       _ptr(o.A8), _ptr(o.s_a), _ptr(out.Y), _ptr(status))
+    _check(lib().ffn_forward(C.byref(args), _stream(stream)), "ffn_forward")
     return out
 
 

@@ -289,6 +289,12 @@ int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t
 // longest problems first
 int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, int* d_status,
                      cudaStream_t stream);
+// The INT8 forward on fp16-carried codes: Y = (X W * s_x) * s_w (W3 == NULL),
+// or with W3 the gate and up projections through the SwiGLU gate into bf16
+// h1, h3 and a (Y unused).  X [T, K], W and W3 [K, N] as stored.
+int umma_fwd(const void* X, const float* s_x, const void* W, const float* s_w, const void* W3, const float* s_w3,
+             int64_t T, int64_t K, int64_t N, float* Y, uint16_t* h1, uint16_t* h3, uint16_t* a, int* d_status,
+             cudaStream_t stream);
 
 // S3R-EC factors of the two linears that read the same input X (W1 and W3 of
 // the SwiGLU block) in one pass; bit-identical to two s3r_ec_correct calls

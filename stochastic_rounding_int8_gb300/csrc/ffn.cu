@@ -540,6 +540,41 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     return record(a, 8, stream);
 }
 
+// The block forward: RTNE operands (per-token X and a, per-output-channel
+// weights), the gate and up projections with the SwiGLU gate in their
+// epilogue (h1, h3, a in bf16), then Y = a W2 in fp32 ("Efficient Quantization
+// Training with Stochastic Rounding via Structured Subspace Randomness"
+// §III-A, §IV-A).  Five launches, or two fewer when the weights come
+// quantized.
+extern "C" int ffn_forward(const struct s3r_ffn_fwd_args* a, cudaStream_t stream) {
+    if (!a) return S3R_ERR_ARG;
+    const int64_t T = a->T, d = a->d, F = a->F;
+    if (T < 0 || d < 0 || F < 0) return S3R_ERR_ARG;
+    if (a->code_format != S3R_CODES_F16) {
+        s3r_record_error("ffn_forward", "the forward runs on fp16-carried codes (S3R_CODES_F16) only");
+        return S3R_ERR_UNSUPPORTED;
+    }
+    if (T == 0 || d == 0 || F == 0) return S3R_OK;
+    if (!a->X || !a->X8 || !a->s_x || !a->W1_8 || !a->s_w1 || !a->W3_8 || !a->s_w3 || !a->W2_8 || !a->s_w2 ||
+        !a->h1 || !a->h3 || !a->a || !a->A8 || !a->s_a || !a->Y)
+        return S3R_ERR_ARG;
+    if (a->quantize_weights && (!a->W1 || !a->W3 || !a->W2)) return S3R_ERR_ARG;
+    const int fmt = S3R_CODES_F16;
+    S3R_TRY(rtne_quantize(a->X, T, d, d, nullptr, nullptr, S3R_AXIS_ROW, a->X8, fmt, a->s_x, a->d_status, stream));
+    if (a->quantize_weights) {
+        S3R_TRY(rtne_quantize(a->W1, d, F, F, nullptr, nullptr, S3R_AXIS_COL, a->W1_8, fmt, a->s_w1, a->d_status,
+                              stream));
+        S3R_TRY(rtne_quantize(a->W3, d, F, F, nullptr, nullptr, S3R_AXIS_COL, a->W3_8, fmt, a->s_w3, a->d_status,
+                              stream));
+        S3R_TRY(rtne_quantize(a->W2, F, d, d, nullptr, nullptr, S3R_AXIS_COL, a->W2_8, fmt, a->s_w2, a->d_status,
+                              stream));
+    }
+    S3R_TRY(int8_gemm_fwd_swiglu(a->X8, a->s_x, a->W1_8, a->s_w1, a->W3_8, a->s_w3, fmt, T, d, F, a->h1, a->h3, a->a,
+                                 a->d_status, stream));
+    S3R_TRY(rtne_quantize(a->a, T, F, F, nullptr, nullptr, S3R_AXIS_ROW, a->A8, fmt, a->s_a, a->d_status, stream));
+    return int8_gemm_fwd(a->A8, a->s_a, a->W2_8, a->s_w2, fmt, T, F, d, a->Y, a->d_status, stream);
+}
+
 extern "C" const char* s3r_status_string(int status) {
     switch (status) {
         case S3R_OK: return "S3R_OK";
@@ -555,4 +590,4 @@ extern "C" const char* s3r_status_string(int status) {
     }
 }
 
-extern "C" int s3r_abi_version(void) { return 101; }
+extern "C" int s3r_abi_version(void) { return 102; }

@@ -38,6 +38,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -77,6 +78,14 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 // Epilogue kinds; a kMixed launch takes each problem's kind from the problem.
 enum Epi { kDX = 0, kDW = 1, kDump = 2, kMixed = 3 };
+// Problem kind of the INT8 forward (mixed launches only): A = X [M, K] K-major,
+// B = W [K, N] MN-major, unit block scales, epilogue (acc * s_x[m]) * s_w[n].
+constexpr int kFwd = 4;
+// Problem kind of the gate and up projections with the SwiGLU gate in the
+// epilogue (mixed launches only): one 128-column slice of W1 and the same
+// slice of W3 fill the 256 accumulator columns, and the epilogue writes
+// h1 = bf16(s_x s_w1 X W1), h3 = bf16(s_x s_w3 X W3) and a = bf16(silu(h1) h3).
+constexpr int kGate = 5;
 
 // One contraction segment: scale(mt, nt, kb) = scale[mt*sm + nt*sn + kb*sk],
 // and for the activation gradient its correction terms.
@@ -103,6 +112,10 @@ struct Problem {
     int32_t* dump;
     const float* s_row;          // dX: 1/s_x[row] rescale
     const float* s_col;          // dW: 1/s_w[col] rescale
+    const float* f_row;          // forward: s_x[row] multiplier (then f_col[col])
+    const float* f_col;
+    const float* f_col3;         // gate: s_w3
+    uint16_t* gate_out[3];       // gate: h1, h3, a (bf16, row stride ldc)
     int ec_mode;
     int64_t S, B;
     const float* colmean;
@@ -339,6 +352,28 @@ __device__ __forceinline__ void seed_tile(const Problem& P, float (&acc)[128], f
 template <int EPI>
 __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128], const float* cv, float* stage,
                                             int64_t row, int64_t c0, int lane) {
+    if (EPI == kDX && P.f_row) {
+        // forward: (acc * s_x[row]) * s_w[col], one rounding each, columns past N scaled by 1
+        const float fr = row < P.M ? __ldg(P.f_row + row) : 1.0f;
+        const float2 fr2 = make_float2(fr, fr);
+        const bool fvec = (reinterpret_cast<uintptr_t>(P.f_col) & 15u) == 0;
+#pragma unroll
+        for (int j4 = 0; j4 < 128; j4 += 4) {
+            const int64_t col = c0 + j4;
+            const float4 fc = (fvec && col + 4 <= P.N)
+                                  ? __ldg(reinterpret_cast<const float4*>(P.f_col + col))
+                                  : make_float4(col < P.N ? __ldg(P.f_col + col) : 1.0f,
+                                                col + 1 < P.N ? __ldg(P.f_col + col + 1) : 1.0f,
+                                                col + 2 < P.N ? __ldg(P.f_col + col + 2) : 1.0f,
+                                                col + 3 < P.N ? __ldg(P.f_col + col + 3) : 1.0f);
+            const float2 a = f2_mul(f2_mul(make_float2(acc[j4], acc[j4 + 1]), fr2), make_float2(fc.x, fc.y));
+            const float2 b = f2_mul(f2_mul(make_float2(acc[j4 + 2], acc[j4 + 3]), fr2), make_float2(fc.z, fc.w));
+            acc[j4] = a.x;
+            acc[j4 + 1] = a.y;
+            acc[j4 + 2] = b.x;
+            acc[j4 + 3] = b.y;
+        }
+    }
     if (EPI == kDX && P.s_row) {
         const float rinv = row < P.M ? __frcp_rn(__ldg(P.s_row + row)) : 1.0f;
         const float2 r2 = make_float2(rinv, rinv);
@@ -395,6 +430,59 @@ __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128],
             }
         }
         __syncwarp();
+    }
+}
+
+// Gate epilogue of the forward (thread = row, acc[0..63] = h1 and acc[64..127]
+// = h3 accumulators of output columns c0 .. c0 + 63): rescale in fp32 as
+// (acc * s_x) * s_w, round h1 and h3 to bf16 (nearest even), and from those
+// bf16 values a = bf16((h1 * sigmoid(h1)) * h3).  Each thread writes its
+// row's 64 columns of h1, h3 and a as 16-byte pieces (columns past N are not
+// written).
+__device__ __forceinline__ void finish_gate(const Problem& P, const float (&acc)[128], int64_t row, int64_t c0) {
+    if (row >= P.M) return;
+    const float fr = __ldg(P.f_row + row);
+    const bool vec = (P.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(P.gate_out[0]) |
+                                           reinterpret_cast<uintptr_t>(P.gate_out[1]) |
+                                           reinterpret_cast<uintptr_t>(P.gate_out[2])) & 15u) == 0;
+#pragma unroll
+    for (int j8 = 0; j8 < 64; j8 += 8) {
+        const int64_t col = c0 + j8;
+        if (col >= P.N) break;
+        uint32_t w1[4], w3[4], wa[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            uint16_t b1[2], b3[2], ba[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int64_t cc = col + j + e;
+                const float s1 = cc < P.N ? __ldg(P.f_col + cc) : 1.0f;
+                const float s3 = cc < P.N ? __ldg(P.f_col3 + cc) : 1.0f;
+                const float h1 = __fmul_rn(__fmul_rn(acc[j8 + j + e], fr), s1);
+                const float h3 = __fmul_rn(__fmul_rn(acc[64 + j8 + j + e], fr), s3);
+                b1[e] = __bfloat16_as_ushort(__float2bfloat16_rn(h1));
+                b3[e] = __bfloat16_as_ushort(__float2bfloat16_rn(h3));
+                const float x = __uint_as_float((uint32_t)b1[e] << 16), z = __uint_as_float((uint32_t)b3[e] << 16);
+                const float silu = __fmul_rn(x, sigmoid_cw(x));
+                ba[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(silu, z)));
+            }
+            w1[j / 2] = (uint32_t)b1[0] | ((uint32_t)b1[1] << 16);
+            w3[j / 2] = (uint32_t)b3[0] | ((uint32_t)b3[1] << 16);
+            wa[j / 2] = (uint32_t)ba[0] | ((uint32_t)ba[1] << 16);
+        }
+        const int64_t off = row * P.ldc + col;
+        if (vec && col + 8 <= P.N) {
+            *reinterpret_cast<uint4*>(P.gate_out[0] + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            *reinterpret_cast<uint4*>(P.gate_out[1] + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+            *reinterpret_cast<uint4*>(P.gate_out[2] + off) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        } else {
+            for (int j = 0; j < 8 && col + j < P.N; ++j) {
+                const int sh = 16 * (j & 1);
+                P.gate_out[0][off + j] = (uint16_t)(w1[j / 2] >> sh);
+                P.gate_out[1][off + j] = (uint16_t)(w3[j / 2] >> sh);
+                P.gate_out[2][off + j] = (uint16_t)(wa[j / 2] >> sh);
+            }
+        }
     }
 }
 
@@ -484,13 +572,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
                     const int nkb = nkb0 + nkb1;   // 128-wide blocks of this tile
                     if (pi != last_pi) {
-                        for (int j = 0; j < (nkb1 ? 4 : 2); ++j)
+                        for (int j = 0; j < (nkb1 || P.kind == kGate ? 4 : 2); ++j)
                             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)(mp + j)) : "memory");
                         last_pi = pi;
                     }
                     int tm, tn;
                     tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
-                    const int32_t m0 = tm * BM, n0 = tn * BN;
+                    const bool gate = EPI == kMixed && P.kind == kGate;
+                    const int32_t m0 = tm * BM, n0 = tn * (gate ? BN / 2 : BN);
                     for (int sl = 0; sl < 2 * nkb; ++sl, ++it) {
                         const int s = it % STAGES;
                         if (!mbar_wait(empty0 + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abrt)) {
@@ -506,14 +595,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const CUtensorMap* mB = mp + (second ? 3 : 1);
                         const int32_t k0 = (second ? sl - 2 * nkb0 : sl) * BKS;
                         const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
-                        if (!(EPI == kMixed ? P.kind == kDW : MN)) {
+                        const bool a_mn = EPI == kMixed ? P.kind == kDW : MN;
+                        const bool b_mn = EPI == kMixed ? (P.kind != kDX) : MN;
+                        if (!a_mn) {
                             tma_load(a_dst, mA, k0, m0, fb);
-                            tma_load(b_dst, mB, k0, n0, fb);
                         } else {
                             tma_load(a_dst, mA, m0, k0, fb);
                             tma_load(a_dst + MN_ATOM_BYTES, mA, m0 + 64, k0, fb);
+                        }
+                        if (!b_mn) {
+                            tma_load(b_dst, mB, k0, n0, fb);
+                        } else {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) tma_load(b_dst + j * MN_ATOM_BYTES, mB, n0 + 64 * j, k0, fb);
+                            for (int j = 0; j < 4; ++j)   // gate: W1 slice in atoms 0, 1 and W3 slice in 2, 3
+                                tma_load(b_dst + j * MN_ATOM_BYTES, gate && j >= 2 ? mp + 3 : mB,
+                                         n0 + 64 * (gate ? (j & 1) : j), k0, fb);
                         }
                     }
                 }
@@ -529,8 +625,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
                     const Problem& P = A.prob[problem_of(A, tile)];
                     const int nkb = (int)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128));
-                    const bool mn = EPI == kMixed ? P.kind == kDW : MN;
-                    const uint32_t idesc = mn ? idesc_f16(BM, BN, true, true) : idesc_f16(BM, BN, false, false);
+                    const bool a_mn = EPI == kMixed ? P.kind == kDW : MN;
+                    const bool b_mn = EPI == kMixed ? (P.kind != kDX) : MN;
+                    const uint32_t idesc = a_mn ? idesc_f16(BM, BN, true, true)
+                                                : (b_mn ? idesc_f16(BM, BN, false, true) : idesc_f16(BM, BN, false, false));
                     for (int kb = 0; kb < nkb; ++kb, ++gkb) {
                         const int buf = gkb & 1;
                         if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(gkb >> 1) & 1u) ^ 1u, abrt)) {
@@ -549,14 +647,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint32_t a0 = su32(sA + s * A_STAGE), b0 = su32(sB + s * B_STAGE);
 #pragma unroll
                             for (int k16 = 0; k16 < BKS / 16; ++k16) {
-                                uint64_t ad, bd;
-                                if (!mn) {
-                                    ad = sdesc(a0 + 32 * k16, 16, 1024);
-                                    bd = sdesc(b0 + 32 * k16, 16, 1024);
-                                } else {
-                                    ad = sdesc(a0 + 2048 * k16, MN_ATOM_BYTES, 1024);
-                                    bd = sdesc(b0 + 2048 * k16, MN_ATOM_BYTES, 1024);
-                                }
+                                const uint64_t ad = a_mn ? sdesc(a0 + 2048 * k16, MN_ATOM_BYTES, 1024)
+                                                         : sdesc(a0 + 32 * k16, 16, 1024);
+                                const uint64_t bd = b_mn ? sdesc(b0 + 2048 * k16, MN_ATOM_BYTES, 1024)
+                                                         : sdesc(b0 + 32 * k16, 16, 1024);
                                 umma_f16(d_tmem, ad, bd, idesc, (h | k16) != 0);
                             }
                             umma_commit(empty0 + 8 * s);
@@ -576,7 +670,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // warp w reads TMEM lanes 32 * (w % 4) ..; two warps per lane quarter
         // split the 256 accumulator columns into halves
         const int q = warp & 3, ew = warp - EPI_WARP0, half = ew >> 2;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * half);
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
         float* stage = sEpi + ew * (32 * STAGE_PITCH);
         float* cv = sCv + half * CV_FLOATS;
         const int ht = 32 * q + lane;   // thread index within the half
@@ -590,10 +684,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
             const int mt = tm, nt = tn * 2 + half;   // 128-wide tile indices
             const int64_t row = (int64_t)mt * BM + 32 * q + lane;
-            const int64_t c0 = (int64_t)nt * 128;
+            const bool gate = EPI == kMixed && P.kind == kGate;
+            // gate: this half owns output columns c0 .. c0 + 63, accumulators
+            // 0..63 = h1 (TMEM columns 64 half ..), 64..127 = h3 (128 + 64 half ..)
+            const int64_t c0 = gate ? (int64_t)tn * 128 + 64 * half : (int64_t)nt * 128;
+            const uint32_t col_base = (uint32_t)(gate ? 64 * half : 128 * half);
+            const uint32_t col_step = gate ? 128u - 64u : 0u;   // extra offset of chunks 4..7
             float acc[128];
             if (EPI == kMixed) {
-                if (P.kind == kDX) seed_tile<kDX>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
+                if (P.kind != kDW) seed_tile<kDX>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
                 else seed_tile<kDW>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
             } else if (EPI != kDump) {
                 seed_tile<EPI>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
@@ -604,6 +703,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool first = kb < nkb0;
                 const int64_t k = first ? kb : kb - nkb0;
                 const float* base = first ? P.seg[0].scale : P.seg[1].scale;
+                if (!base) return 1.0f;   // unit block scales (the forward)
                 const int64_t off = first ? mt * P.seg[0].sm + nt * P.seg[0].sn + k * P.seg[0].sk
                                           : mt * P.seg[1].sm + nt * P.seg[1].sn + k * P.seg[1].sk;
                 const int64_t lim = first ? P.seg[0].nt_limit : P.seg[1].nt_limit;
@@ -628,7 +728,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int c = 0; c < 8; c += 4) {
                     uint32_t r[4][16];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) tmem_ld16(lane_addr + (uint32_t)(buf * BN + 16 * (c + u)), r[u]);
+                    for (int u = 0; u < 4; ++u)
+                        tmem_ld16(lane_addr + col_base + (uint32_t)(buf * BN + 16 * (c + u)) + (c + u >= 4 ? col_step : 0u),
+                                  r[u]);
                     tmem_wait_ld();
                     if (EPI == kDump) {
                         if (row < P.M) {
@@ -663,7 +765,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (EPI == kDump || !ok) continue;
             if (EPI == kMixed) {
-                if (P.kind == kDX) finish_tile<kDX>(P, acc, cv, stage, row, c0, lane);
+                if (gate) finish_gate(P, acc, row, c0);
+                else if (P.kind != kDW) finish_tile<kDX>(P, acc, cv, stage, row, c0, lane);
                 else finish_tile<kDW>(P, acc, cv, stage, row, c0, lane);
             } else {
                 finish_tile<EPI>(P, acc, cv, stage, row, c0, lane);
@@ -790,7 +893,7 @@ static int launch(const Maps& maps, Args& A, const double (*strip)[2], cudaStrea
     int64_t total = 0;
     for (int i = 0; i < A.nprob; ++i) {
         Problem& P = A.prob[i];
-        const int64_t ntm = s3r_cdiv(P.M, BM), ntn = s3r_cdiv(P.N, BN);
+        const int64_t ntm = s3r_cdiv(P.M, BM), ntn = s3r_cdiv(P.N, P.kind == kGate ? BN / 2 : BN);
         if (ntm * ntn > (int64_t)1 << 30) return S3R_ERR_UNSUPPORTED;
         P.ntm = (int)ntm;
         P.ntn = (int)ntn;
@@ -894,6 +997,52 @@ static int add_dw_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDwPr
     return S3R_OK;
 }
 
+// Forward problems (fp16-carried codes): A = X [T, K] K-major, B = W [K, N]
+// MN-major (as stored), unit block scales.  kFwd writes Y [T, N] fp32 =
+// (acc * s_x[t]) * s_w[n]; kGate contracts X with W1 and W3 at once and writes
+// h1, h3 and a (bf16 [T, N], row stride N) through the SwiGLU gate.
+static int add_fwd_problem(umma::Maps& maps, umma::Args& A, int i, const void* X, const float* s_x, const void* W,
+                           const float* s_w, const void* W3, const float* s_w3, int64_t T, int64_t K, int64_t N,
+                           float* Y, uint16_t* const* gate_out, double (&strip)[2]) {
+    const bool gate = W3 != nullptr;
+    if (!s3r_aligned16(X) || !s3r_aligned16(W) || K % 8 != 0 || N % 8 != 0) return S3R_ERR_ALIGN;
+    if (gate && !s3r_aligned16(W3)) return S3R_ERR_ALIGN;
+    CUtensorMap* m = maps.m[i];
+    int st = umma::make_map(&m[0], X, K, T, K, umma::BM);
+    if (!st) st = umma::make_map(&m[1], W, N, K, N, 64);
+    if (!st && gate) st = umma::make_map(&m[3], W3, N, K, N, 64);
+    if (st) return st;
+    m[2] = m[0];
+    if (!gate) m[3] = m[1];
+    umma::Problem& P = A.prob[i];
+    P = umma::Problem{};
+    P.M = T; P.N = N; P.kind = gate ? umma::kGate : umma::kFwd;
+    umma::Segment& g = P.seg[0];
+    g.scale = nullptr; g.sm = g.sn = g.sk = 0; g.nt_limit = INT64_MAX; g.K = K;
+    P.f_row = s_x; P.f_col = s_w; P.f_col3 = s_w3;
+    P.C = Y; P.ldc = N; P.S = T;
+    if (gate)
+        for (int j = 0; j < 3; ++j) P.gate_out[j] = gate_out[j];
+    strip[0] = umma::BM * 2.0 * (double)K;
+    strip[1] = umma::BN * 2.0 * (double)K;
+    return S3R_OK;
+}
+
+int umma_fwd(const void* X, const float* s_x, const void* W, const float* s_w, const void* W3, const float* s_w3,
+             int64_t T, int64_t K, int64_t N, float* Y, uint16_t* h1, uint16_t* h3, uint16_t* a, int* d_status,
+             cudaStream_t stream) {
+    thread_local umma::Maps maps;
+    thread_local umma::Args A;
+    std::memset(&A, 0, sizeof(A));
+    double strip[1][2];
+    uint16_t* outs[3] = {h1, h3, a};
+    const int st = add_fwd_problem(maps, A, 0, X, s_x, W, s_w, W3, s_w3, T, K, N, Y, outs, strip[0]);
+    if (st) return st;
+    A.nprob = 1;
+    A.d_status = d_status;
+    return umma::launch<umma::kMixed, false>(maps, A, strip, stream);
+}
+
 int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream) {
     if (n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
     thread_local umma::Maps maps;   // host staging of the launch's parameters (copied at launch)
@@ -984,4 +1133,50 @@ int umma_gemm_dw(const void* X, const void* Q, const float* tile_scale, int64_t 
                  const float* p, int64_t S, float* dW, int32_t* dump, int* d_status, cudaStream_t stream) {
     const UmmaDwProblem q{X, Q, tile_scale, T, K, N, s_w, ec_mode, colmean, mu, xsum, p, S, dW, dump};
     return umma_dw_group(&q, 1, d_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// C ABI of the forward GEMMs
+// ---------------------------------------------------------------------------
+static int fwd_args(const void* X8, const float* s_x, const void* W8, const float* s_w, int code_format, int64_t T,
+                    int64_t K, int64_t N) {
+    if (T < 0 || K < 0 || N < 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_F16) {
+        s3r_record_error("int8_gemm_fwd", "the forward runs on fp16-carried codes (S3R_CODES_F16) only");
+        return S3R_ERR_UNSUPPORTED;
+    }
+    if (T > 0 && N > 0 && K > 0 && (!X8 || !s_x || !W8 || !s_w)) return S3R_ERR_ARG;
+    return S3R_OK;
+}
+
+extern "C" int int8_gemm_fwd(const void* X8, const float* s_x, const void* W8, const float* s_w, int code_format,
+                             int64_t T, int64_t K, int64_t N, float* Y, int* d_status, cudaStream_t stream) {
+    int st = fwd_args(X8, s_x, W8, s_w, code_format, T, K, N);
+    if (st) return st;
+    if (T == 0 || N == 0) return S3R_OK;
+    if (!Y) return S3R_ERR_ARG;
+    if (K == 0) {
+        const cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)(T * N) * sizeof(float), stream);
+        return e == cudaSuccess ? S3R_OK : s3r_cuda_fail("int8_gemm_fwd: cudaMemsetAsync", e);
+    }
+    return umma_fwd(X8, s_x, W8, s_w, nullptr, nullptr, T, K, N, Y, nullptr, nullptr, nullptr, d_status, stream);
+}
+
+extern "C" int int8_gemm_fwd_swiglu(const void* X8, const float* s_x, const void* W1_8, const float* s_w1,
+                                    const void* W3_8, const float* s_w3, int code_format, int64_t T, int64_t K,
+                                    int64_t F, void* h1, void* h3, void* a, int* d_status, cudaStream_t stream) {
+    int st = fwd_args(X8, s_x, W1_8, s_w1, code_format, T, K, F);
+    if (st) return st;
+    if (T == 0 || F == 0) return S3R_OK;
+    if (!h1 || !h3 || !a || (K > 0 && (!W3_8 || !s_w3))) return S3R_ERR_ARG;
+    if (K == 0) {   // h1 = h3 = 0, a = silu(0) * 0 = 0
+        for (void* p : {h1, h3, a}) {
+            const cudaError_t e = cudaMemsetAsync(p, 0, (size_t)(T * F) * 2, stream);
+            if (e != cudaSuccess) return s3r_cuda_fail("int8_gemm_fwd_swiglu: cudaMemsetAsync", e);
+        }
+        return S3R_OK;
+    }
+    return umma_fwd(X8, s_x, W1_8, s_w1, W3_8, s_w3, T, K, F, nullptr, static_cast<uint16_t*>(h1),
+                    static_cast<uint16_t*>(h3), static_cast<uint16_t*>(a), d_status, stream);
 }

@@ -33,7 +33,7 @@ def test_status_strings(L):
     for code in range(-1, -9, -1):
         assert s3r.status_string(code).startswith("S3R_ERR_")
     assert s3r.status_string(-99) == "S3R_ERR_UNKNOWN"
-    assert L.s3r_abi_version() == 101
+    assert L.s3r_abi_version() == 102
 
 
 def test_host_argument_checks_need_no_gpu(L):
