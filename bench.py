@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn",
-                                              "moe"],
+                                              "moe", "fwd", "fwd_gate", "fwd_gate_quantize", "fwd_down"],
                     help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
     return ap.parse_args()
 
@@ -381,13 +381,15 @@ def time_forward(s3r, inp, pk, steps=10, warmup=3):
     c = lambda t: t.cuda()
     X, W1, W3, W2 = c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2)
     st = s3r.new_status()
-    out = s3r.alloc_ffn_forward(T, D, F)
+    out = s3r.alloc_ffn_forward(T, D, F, keep_a=False)   # the backward reads a's codes only
     fwd = lambda: s3r.ffn_forward(X, W1, W3, W2, out=out, status=st)
     ms = _event_ms(fwd, steps, warmup)
     o = out.ops
-    gate = lambda: s3r.int8_gemm_fwd_swiglu(o.X8, o.s_x, o.W1_8, o.s_w1, o.W3_8, o.s_w3, o.h1, o.h3, out.a,
-                                            status=st)
+    gate = lambda: s3r.int8_gemm_fwd_swiglu(o.X8, o.s_x, o.W1_8, o.s_w1, o.W3_8, o.s_w3, o.h1, o.h3,
+                                            with_gate=False, status=st)
     gms = _event_ms(gate, steps, warmup)
+    gq = lambda: s3r.swiglu_fwd_quantize(o.h1, o.h3, keep_a=False, Q=o.A8, scale=o.s_a, status=st)
+    qms = _event_ms(gq, steps, warmup)
     down = lambda: s3r.int8_gemm_fwd(o.A8, o.s_a, o.W2_8, o.s_w2, Y=out.Y, status=st)
     dms = _event_ms(down, steps, warmup)
     s3r.check_status(st)
@@ -401,8 +403,11 @@ def time_forward(s3r, inp, pk, steps=10, warmup=3):
     peak = pk.get("bf16_tflops")
     tf = lambda flops, t: round(flops / (t * 1e-3) / 1e12, 1)
     return {"ms": round(ms, 4), "tokens_s": round(T / (ms * 1e-3), 1), "tflops": tf(6.0 * T * D * F, ms),
-            "gate_up_gemm_swiglu": {"ms": round(gms, 4), "tflops": tf(4.0 * T * D * F, gms),
-                                    "frac_bf16_burst": round(4.0 * T * D * F / (gms * 1e-3) / 1e12 / peak, 3)},
+            "gate_up_gemm": {"ms": round(gms, 4), "tflops": tf(4.0 * T * D * F, gms),
+                             "frac_bf16_burst": round(4.0 * T * D * F / (gms * 1e-3) / 1e12 / peak, 3)},
+            "swiglu_gate_rtne_a": {"ms": round(qms, 4),
+                                   "GB_s": round(6.0 * T * F / (qms * 1e-3) / 1e9, 1),
+                                   "frac_hbm": round(6.0 * T * F / (qms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)},
             "down_gemm": {"ms": round(dms, 4), "tflops": tf(2.0 * T * D * F, dms),
                           "frac_bf16_burst": round(2.0 * T * D * F / (dms * 1e-3) / 1e12 / peak, 3)},
             "bf16_cublas_forward": {"ms": round(bms, 4), "tokens_s": round(T / (bms * 1e-3), 1)},
@@ -622,6 +627,16 @@ def run_kernel_case(args):
         mops = s3r.moe_forward_operands(c(mi.X), c(mi.W1), c(mi.W3), c(mi.W2), c(mi.a), c(mi.h1), c(mi.h3))
         mdY = mi.dY.cuda()
         fns["moe"] = lambda: s3r.ffn_backward(mops, mdY, 0, group_offsets=mi.offsets)
+    if args.kernel_case.startswith("fwd"):
+        c = lambda t: t.cuda()
+        X, W1, W3, W2 = c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2)
+        fo = s3r.ffn_forward(X, W1, W3, W2, keep_a=False)
+        o = fo.ops
+        fns["fwd"] = lambda: s3r.ffn_forward(X, W1, W3, W2, out=fo)
+        fns["fwd_gate"] = lambda: s3r.int8_gemm_fwd_swiglu(o.X8, o.s_x, o.W1_8, o.s_w1, o.W3_8, o.s_w3, o.h1, o.h3,
+                                                           with_gate=False)
+        fns["fwd_gate_quantize"] = lambda: s3r.swiglu_fwd_quantize(o.h1, o.h3, keep_a=False, Q=o.A8, scale=o.s_a)
+        fns["fwd_down"] = lambda: s3r.int8_gemm_fwd(o.A8, o.s_a, o.W2_8, o.s_w2, Y=fo.Y)
     if args.kernel_case == "quantize_sweep":
         Gs = workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).cuda()
         qs = s3r.s3r_quantize(Gs, code_format=s3r.CODES_S8)

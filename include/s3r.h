@@ -359,11 +359,28 @@ int int8_gemm_fwd(const void* X8, const float* s_x, const void* W8, const float*
  * h1 and h3 are the activations the backward reads; a feeds the next linear.
  * In : X8 [T, K], s_x [T]; W1_8, W3_8 [K, F] (row stride F), s_w1, s_w3 [F];
  *      same format and alignment rules as int8_gemm_fwd.
- * Out: h1, h3, a [T, F] bf16 (row stride F).  One tcgen05 launch.
+ * Out: h1, h3 [T, F] bf16 (row stride F); a [T, F] bf16, or NULL to skip the
+ *      gate (swiglu_fwd_quantize then forms a together with its codes, the
+ *      faster split).  One tcgen05 launch.
  */
 int int8_gemm_fwd_swiglu(const void* X8, const float* s_x, const void* W1_8, const float* s_w1, const void* W3_8,
                          const float* s_w3, int code_format, int64_t T, int64_t K, int64_t F, void* h1, void* h3,
                          void* a, int* d_status, cudaStream_t stream);
+
+/*
+ * swiglu_fwd_quantize -- the forward SwiGLU gate fused into the per-token
+ * RTNE of its output (FFN block of [S3R] §IV-A; §III-A for the operand):
+ *   a[t, f] = bf16((h1 * s) * h3),  s = 1 / (1 + exp(-h1))   as in
+ *             int8_gemm_fwd_swiglu, from the bf16 h1 and h3;
+ *   then Q, scale = rtne_quantize(a, S3R_AXIS_ROW) exactly.
+ * In : h1, h3 [T, F] bf16 (row stride ldh).  F and ldh multiples of 8, h1,
+ *      h3, a and Q 16-byte aligned (S3R_ERR_ALIGN).
+ * Out: a [T, F] bf16 (row stride F) or NULL (not written); Q [T, F] codes in
+ *      `code_format`; scale [T].  A row holding a non-finite a gets a NaN
+ *      scale, zero codes and *d_status = S3R_ERR_NONFINITE.  One launch.
+ */
+int swiglu_fwd_quantize(const void* h1, const void* h3, int64_t T, int64_t F, int64_t ldh, void* a, void* Q,
+                        int code_format, float* scale, int* d_status, cudaStream_t stream);
 
 /*
  * ffn_forward -- the SwiGLU FFN block forward with INT8 GEMMs, the operands
@@ -371,8 +388,8 @@ int int8_gemm_fwd_swiglu(const void* X8, const float* s_x, const void* W1_8, con
  *   1. X8, s_x   = rtne_quantize(X, per row)
  *   2. W1_8, W3_8, W2_8 and their scales = rtne_quantize(W, per column)
  *      (skipped when quantize_weights == 0: they are inputs then)
- *   3. h1, h3, a = int8_gemm_fwd_swiglu(X8, W1_8, W3_8)
- *   4. A8, s_a   = rtne_quantize(a, per row)
+ *   3. h1, h3    = int8_gemm_fwd_swiglu(X8, W1_8, W3_8)  (a = NULL)
+ *   4. a, A8, s_a = swiglu_fwd_quantize(h1, h3)
  *   5. Y         = int8_gemm_fwd(A8, s_a, W2_8, s_w2)
  * All on `stream`, no host synchronization, no workspace.
  */
@@ -394,7 +411,7 @@ struct s3r_ffn_fwd_args {
     float* s_w2;
     void* h1;                    /* out bf16 [T, F] */
     void* h3;                    /* out bf16 [T, F] */
-    void* a;                     /* out bf16 [T, F] */
+    void* a;                     /* out bf16 [T, F], or NULL (not kept) */
     void* A8;                    /* out [T, F] codes, s_a [T] */
     float* s_a;
     float* Y;                    /* out fp32 [T, d] */

@@ -72,6 +72,7 @@ _SIGS = {
     "int8_gemm_fwd": (_INT, [_VP, _VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _VP]),
     "int8_gemm_fwd_swiglu": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _VP, _VP,
                                     _VP]),
+    "swiglu_fwd_quantize": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _VP, _VP]),
     "ffn_forward": (_INT, [_VP, _VP]),
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
@@ -405,15 +406,37 @@ def int8_gemm_fwd(X8, s_x, W8, s_w, Y=None, status=None, stream=None):
     return Y
 
 
-def int8_gemm_fwd_swiglu(X8, s_x, W1_8, s_w1, W3_8, s_w3, h1=None, h3=None, a=None, status=None, stream=None):
-    """The gate and up projections with the SwiGLU gate: returns bf16 (h1, h3, a)."""
+def int8_gemm_fwd_swiglu(X8, s_x, W1_8, s_w1, W3_8, s_w3, h1=None, h3=None, a=None, with_gate=True, status=None,
+                         stream=None):
+    """The gate and up projections (and, with_gate, the SwiGLU gate in the
+    epilogue): returns bf16 (h1, h3, a or None)."""
     T, K = X8.shape
     F = W1_8.shape[1]
-    out = [t if t is not None else torch.empty((T, F), dtype=torch.bfloat16, device=X8.device) for t in (h1, h3, a)]
+    new = lambda: torch.empty((T, F), dtype=torch.bfloat16, device=X8.device)
+    out = [h1 if h1 is not None else new(), h3 if h3 is not None else new(),
+           (a if a is not None else new()) if with_gate else None]
     _check(lib().int8_gemm_fwd_swiglu(_ptr(X8), _ptr(s_x), _ptr(W1_8), _ptr(s_w1), _ptr(W3_8), _ptr(s_w3),
                                       _fmt2(X8, W1_8), T, K, F, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
                                       _ptr(status), _stream(stream)), "int8_gemm_fwd_swiglu")
     return tuple(out)
+
+
+def swiglu_fwd_quantize(h1, h3, a=None, keep_a=True, Q=None, scale=None, status=None, stream=None,
+                        code_format=DEFAULT_CODES):
+    """a = bf16(silu(h1) h3) fused into its per-token RTNE: returns (a or None, Q, scale)."""
+    T, F = h1.shape
+    assert h1.shape == h3.shape and h1.stride(0) == h3.stride(0)
+    dev = h1.device
+    if keep_a and a is None:
+        a = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+    if Q is None:
+        Q = torch.empty((T, F), dtype=_CODE_DTYPE[code_format], device=dev)
+    if scale is None:
+        scale = torch.empty((T,), dtype=torch.float32, device=dev)
+    _check(lib().swiglu_fwd_quantize(_ptr(_bits(h1)), _ptr(_bits(h3)), T, F, h1.stride(0),
+                                     _ptr(a if keep_a else None), _ptr(Q), code_format_of(Q), _ptr(scale),
+                                     _ptr(status), _stream(stream)), "swiglu_fwd_quantize")
+    return (a if keep_a else None), Q, scale
 
 
 class _FfnFwdArgs(C.Structure):
@@ -427,23 +450,24 @@ class _FfnFwdArgs(C.Structure):
 
 @dataclass
 class FFNForward:
-    """The block forward's outputs: the backward's operands, a and Y."""
+    """The block forward's outputs: the backward's operands, a (or None: the
+    backward reads only its codes) and Y."""
     ops: "FFNOperands"
-    a: torch.Tensor
+    a: torch.Tensor | None
     Y: torch.Tensor
 
 
-def alloc_ffn_forward(T, d, F, device="cuda") -> FFNForward:
+def alloc_ffn_forward(T, d, F, device="cuda", keep_a=True) -> FFNForward:
     """Output buffers of ffn_forward (fp16 codes)."""
     e = lambda *shape, dt=torch.float16: torch.empty(shape, dtype=dt, device=device)
     f32, bf = torch.float32, torch.bfloat16
     ops = FFNOperands(e(T, d), e(T, dt=f32), e(T, F), e(T, dt=f32), e(d, F), e(F, dt=f32), e(d, F), e(F, dt=f32),
                       e(F, d), e(d, dt=f32), e(T, F, dt=bf), e(T, F, dt=bf))
-    return FFNForward(ops, e(T, F, dt=bf), e(T, d, dt=f32))
+    return FFNForward(ops, e(T, F, dt=bf) if keep_a else None, e(T, d, dt=f32))
 
 
 def ffn_forward(X, W1=None, W3=None, W2=None, out: FFNForward | None = None, quantize_weights=True, status=None,
-                stream=None) -> FFNForward:
+                stream=None, keep_a=True) -> FFNForward:
     """The SwiGLU block forward with INT8 GEMMs (one C call, five launches):
     RTNE X and (unless quantize_weights is False, in which case `out.ops`
     already holds the weights' codes) the weights, h1/h3/a through the fused
@@ -451,7 +475,7 @@ def ffn_forward(X, W1=None, W3=None, W2=None, out: FFNForward | None = None, qua
     T, d = X.shape
     F = out.ops.W1_8.shape[1] if out is not None else W1.shape[1]
     if out is None:
-        out = alloc_ffn_forward(T, d, F, X.device)
+        out = alloc_ffn_forward(T, d, F, X.device, keep_a)
     o = out.ops
     args = _FfnFwdArgs(T, d, F, _ptr(_bits(X)), _ptr(_bits(W1) if W1 is not None else None),
                        _ptr(_bits(W3) if W3 is not None else None), _ptr(_bits(W2) if W2 is not None else None),

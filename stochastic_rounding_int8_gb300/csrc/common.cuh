@@ -189,11 +189,10 @@ __device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
 // rounding mode) and the low byte of the sum's bits is that integer mod 256.
 constexpr float kMagic = 12582912.0f;
 
-// The SwiGLU derivative terms of two lanes at once, per lane bit-identical to
-//   s = sigmoid_cw(x); silu = x * s; dsilu = s * (1 + x * (1 - s))
-// (exp_cw of -x with the negation folded into the reduction constants, the
-// correctly rounded reciprocal standing for the IEEE quotient 1 / (1 + e)).
-__device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& dsilu) {
+// sigmoid_cw of two lanes at once, per lane bit-identical to sigmoid_cw (exp_cw
+// of -x, the correctly rounded reciprocal standing for the IEEE quotient
+// 1 / (1 + e)).
+__device__ __forceinline__ float2 sigmoid2(float2 x) {
     // exp_cw(-x): clamp, n = rint(-x log2 e), r = -x - n ln2 (two parts), Taylor
     const float a0 = fminf(fmaxf(-x.x, -87.0f), 88.0f), a1 = fminf(fmaxf(-x.y, -87.0f), 88.0f);
     const float2 a = make_float2(a0, a1);
@@ -216,15 +215,21 @@ __device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& ds
     const int bm = (int)__float_as_uint(kMagic) - 127;
     const float2 two_n = make_float2(__int_as_float(((int)__float_as_uint(tm0) - bm) << 23),
                                      __int_as_float(((int)__float_as_uint(tm1) - bm) << 23));
+    // (1 + poly 2^n may fuse into an fma: a product with a power of two is exact.)
     const float2 e = f2_mul(poly, two_n);
     const float2 den = f2_add(make_float2(1.0f, 1.0f), e);
-    const float2 s = make_float2(__frcp_rn(den.x), __frcp_rn(den.y));
+    return make_float2(__frcp_rn(den.x), __frcp_rn(den.y));
+}
+
+// The SwiGLU derivative terms of two lanes at once, per lane bit-identical to
+//   s = sigmoid_cw(x); silu = x * s; dsilu = s * (1 + x * (1 - s))
+__device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& dsilu) {
+    const float2 s = sigmoid2(x);
     silu = f2_mul(x, s);
     const float2 one = make_float2(1.0f, 1.0f);
     // ptxas contracts a packed multiply whose only use is a packed add into a
     // packed fma, .rn or not; the scalar __fadd_rn is never contracted, so the
     // product x (1 - s) is rounded on its own as the documented order requires.
-    // (1 + poly 2^n above may fuse: a product with a power of two is exact.)
     const float2 xt = f2_mul(x, f2_sub(one, s));
     dsilu = f2_mul(s, make_float2(__fadd_rn(1.0f, xt.x), __fadd_rn(1.0f, xt.y)));
 }

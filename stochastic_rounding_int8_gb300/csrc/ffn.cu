@@ -541,11 +541,10 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
 }
 
 // The block forward: RTNE operands (per-token X and a, per-output-channel
-// weights), the gate and up projections with the SwiGLU gate in their
-// epilogue (h1, h3, a in bf16), then Y = a W2 in fp32 ("Efficient Quantization
-// Training with Stochastic Rounding via Structured Subspace Randomness"
-// §III-A, §IV-A).  Five launches, or two fewer when the weights come
-// quantized.
+// weights), the gate and up projections in one launch (h1, h3 in bf16), the
+// SwiGLU gate fused into the RTNE of a, then Y = a W2 in fp32 ("Efficient
+// Quantization Training with Stochastic Rounding via Structured Subspace
+// Randomness" §III-A, §IV-A).
 extern "C" int ffn_forward(const struct s3r_ffn_fwd_args* a, cudaStream_t stream) {
     if (!a) return S3R_ERR_ARG;
     const int64_t T = a->T, d = a->d, F = a->F;
@@ -556,7 +555,7 @@ extern "C" int ffn_forward(const struct s3r_ffn_fwd_args* a, cudaStream_t stream
     }
     if (T == 0 || d == 0 || F == 0) return S3R_OK;
     if (!a->X || !a->X8 || !a->s_x || !a->W1_8 || !a->s_w1 || !a->W3_8 || !a->s_w3 || !a->W2_8 || !a->s_w2 ||
-        !a->h1 || !a->h3 || !a->a || !a->A8 || !a->s_a || !a->Y)
+        !a->h1 || !a->h3 || !a->A8 || !a->s_a || !a->Y)
         return S3R_ERR_ARG;
     if (a->quantize_weights && (!a->W1 || !a->W3 || !a->W2)) return S3R_ERR_ARG;
     const int fmt = S3R_CODES_F16;
@@ -569,9 +568,9 @@ extern "C" int ffn_forward(const struct s3r_ffn_fwd_args* a, cudaStream_t stream
         S3R_TRY(rtne_quantize(a->W2, F, d, d, nullptr, nullptr, S3R_AXIS_COL, a->W2_8, fmt, a->s_w2, a->d_status,
                               stream));
     }
-    S3R_TRY(int8_gemm_fwd_swiglu(a->X8, a->s_x, a->W1_8, a->s_w1, a->W3_8, a->s_w3, fmt, T, d, F, a->h1, a->h3, a->a,
-                                 a->d_status, stream));
-    S3R_TRY(rtne_quantize(a->a, T, F, F, nullptr, nullptr, S3R_AXIS_ROW, a->A8, fmt, a->s_a, a->d_status, stream));
+    S3R_TRY(int8_gemm_fwd_swiglu(a->X8, a->s_x, a->W1_8, a->s_w1, a->W3_8, a->s_w3, fmt, T, d, F, a->h1, a->h3,
+                                 nullptr, a->d_status, stream));
+    S3R_TRY(swiglu_fwd_quantize(a->h1, a->h3, T, F, F, a->a, a->A8, fmt, a->s_a, a->d_status, stream));
     return int8_gemm_fwd(a->A8, a->s_a, a->W2_8, a->s_w2, fmt, T, F, d, a->Y, a->d_status, stream);
 }
 

@@ -435,52 +435,72 @@ __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128],
 
 // Gate epilogue of the forward (thread = row, acc[0..63] = h1 and acc[64..127]
 // = h3 accumulators of output columns c0 .. c0 + 63): rescale in fp32 as
-// (acc * s_x) * s_w, round h1 and h3 to bf16 (nearest even), and from those
-// bf16 values a = bf16((h1 * sigmoid(h1)) * h3).  Each thread writes its
-// row's 64 columns of h1, h3 and a as 16-byte pieces (columns past N are not
-// written).
+// (acc * s_x) * s_w and round to bf16 (nearest even).  With an `a` output the
+// gate follows from those bf16 values: a = bf16((h1 * sigmoid(h1)) * h3).
+// Each thread writes its row's 64 columns as 16-byte pieces; N is a multiple
+// of 8, so a group of 8 columns lies wholly inside or outside.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
 __device__ __forceinline__ void finish_gate(const Problem& P, const float (&acc)[128], int64_t row, int64_t c0) {
     if (row >= P.M) return;
     const float fr = __ldg(P.f_row + row);
-    const bool vec = (P.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(P.gate_out[0]) |
-                                           reinterpret_cast<uintptr_t>(P.gate_out[1]) |
-                                           reinterpret_cast<uintptr_t>(P.gate_out[2])) & 15u) == 0;
+    const float2 fr2 = make_float2(fr, fr);
+    uint16_t* const out_a = P.gate_out[2];
+    const bool vec = (P.ldc % 8 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(P.gate_out[0]) | reinterpret_cast<uintptr_t>(P.gate_out[1]) |
+                       reinterpret_cast<uintptr_t>(out_a) | reinterpret_cast<uintptr_t>(P.f_col) |
+                       reinterpret_cast<uintptr_t>(P.f_col3)) & 15u) == 0;
 #pragma unroll
     for (int j8 = 0; j8 < 64; j8 += 8) {
         const int64_t col = c0 + j8;
         if (col >= P.N) break;
+        float s1[8], s3[8];
+        if (vec) {
+            const float4* p1 = reinterpret_cast<const float4*>(P.f_col + col);
+            const float4* p3 = reinterpret_cast<const float4*>(P.f_col3 + col);
+            const float4 a0 = __ldg(p1), a1 = __ldg(p1 + 1), b0 = __ldg(p3), b1 = __ldg(p3 + 1);
+            s1[0] = a0.x; s1[1] = a0.y; s1[2] = a0.z; s1[3] = a0.w; s1[4] = a1.x; s1[5] = a1.y; s1[6] = a1.z; s1[7] = a1.w;
+            s3[0] = b0.x; s3[1] = b0.y; s3[2] = b0.z; s3[3] = b0.w; s3[4] = b1.x; s3[5] = b1.y; s3[6] = b1.z; s3[7] = b1.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                s1[j] = __ldg(P.f_col + col + j);
+                s3[j] = __ldg(P.f_col3 + col + j);
+            }
+        }
         uint32_t w1[4], w3[4], wa[4];
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
-            uint16_t b1[2], b3[2], ba[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int64_t cc = col + j + e;
-                const float s1 = cc < P.N ? __ldg(P.f_col + cc) : 1.0f;
-                const float s3 = cc < P.N ? __ldg(P.f_col3 + cc) : 1.0f;
-                const float h1 = __fmul_rn(__fmul_rn(acc[j8 + j + e], fr), s1);
-                const float h3 = __fmul_rn(__fmul_rn(acc[64 + j8 + j + e], fr), s3);
-                b1[e] = __bfloat16_as_ushort(__float2bfloat16_rn(h1));
-                b3[e] = __bfloat16_as_ushort(__float2bfloat16_rn(h3));
-                const float x = __uint_as_float((uint32_t)b1[e] << 16), z = __uint_as_float((uint32_t)b3[e] << 16);
-                const float silu = __fmul_rn(x, sigmoid_cw(x));
-                ba[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(silu, z)));
-            }
-            w1[j / 2] = (uint32_t)b1[0] | ((uint32_t)b1[1] << 16);
-            w3[j / 2] = (uint32_t)b3[0] | ((uint32_t)b3[1] << 16);
-            wa[j / 2] = (uint32_t)ba[0] | ((uint32_t)ba[1] << 16);
+            const float2 h1 = f2_mul(f2_mul(make_float2(acc[j8 + j], acc[j8 + j + 1]), fr2), make_float2(s1[j], s1[j + 1]));
+            const float2 h3 =
+                f2_mul(f2_mul(make_float2(acc[64 + j8 + j], acc[64 + j8 + j + 1]), fr2), make_float2(s3[j], s3[j + 1]));
+            w1[j / 2] = bf16x2_bits(h1.x, h1.y);
+            w3[j / 2] = bf16x2_bits(h3.x, h3.y);
         }
         const int64_t off = row * P.ldc + col;
-        if (vec && col + 8 <= P.N) {
+        if (out_a) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 x = make_float2(__uint_as_float(w1[k] << 16), __uint_as_float(w1[k] & 0xFFFF0000u));
+                const float2 z = make_float2(__uint_as_float(w3[k] << 16), __uint_as_float(w3[k] & 0xFFFF0000u));
+                const float2 av = f2_mul(f2_mul(x, sigmoid2(x)), z);
+                wa[k] = bf16x2_bits(av.x, av.y);
+            }
+        }
+        if (vec) {
             *reinterpret_cast<uint4*>(P.gate_out[0] + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
             *reinterpret_cast<uint4*>(P.gate_out[1] + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
-            *reinterpret_cast<uint4*>(P.gate_out[2] + off) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            if (out_a) *reinterpret_cast<uint4*>(out_a + off) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
         } else {
-            for (int j = 0; j < 8 && col + j < P.N; ++j) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
                 const int sh = 16 * (j & 1);
                 P.gate_out[0][off + j] = (uint16_t)(w1[j / 2] >> sh);
                 P.gate_out[1][off + j] = (uint16_t)(w3[j / 2] >> sh);
-                P.gate_out[2][off + j] = (uint16_t)(wa[j / 2] >> sh);
+                if (out_a) out_a[off + j] = (uint16_t)(wa[j / 2] >> sh);
             }
         }
     }
@@ -1169,9 +1189,10 @@ extern "C" int int8_gemm_fwd_swiglu(const void* X8, const float* s_x, const void
     int st = fwd_args(X8, s_x, W1_8, s_w1, code_format, T, K, F);
     if (st) return st;
     if (T == 0 || F == 0) return S3R_OK;
-    if (!h1 || !h3 || !a || (K > 0 && (!W3_8 || !s_w3))) return S3R_ERR_ARG;
+    if (!h1 || !h3 || (K > 0 && (!W3_8 || !s_w3))) return S3R_ERR_ARG;
     if (K == 0) {   // h1 = h3 = 0, a = silu(0) * 0 = 0
         for (void* p : {h1, h3, a}) {
+            if (!p) continue;
             const cudaError_t e = cudaMemsetAsync(p, 0, (size_t)(T * F) * 2, stream);
             if (e != cudaSuccess) return s3r_cuda_fail("int8_gemm_fwd_swiglu: cudaMemsetAsync", e);
         }

@@ -15,6 +15,7 @@
 // reduced with shuffles and a small shared-memory pass, in a fixed order.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <cstdio>
@@ -1159,6 +1160,235 @@ __global__ void __launch_bounds__(256) rtne_cols_kernel(const uint16_t* A, int64
     }
 }
 
+// Vectorized forms for 16-byte aligned rows (C and lda multiples of 8): the
+// same arithmetic element by element, on 8 bf16 values per 16-byte access.
+
+// max of |x| over 8 bf16 as a float bit pattern (NaN/Inf compare largest)
+__device__ __forceinline__ uint32_t absmax8_bits(const uint4& v) {
+    uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16) << 16;
+}
+
+// 8 codes of one 16-byte group: q = clamp(rint(a * inv[i]), -127, 127)
+template <int FMT>
+__device__ __forceinline__ void store_codes8(void* Q, int64_t idx, const uint4& v, const float (&inv)[8],
+                                             bool zero) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float a = __uint_as_float(i & 1 ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
+        q[i] = zero ? 0.0f : fminf(fmaxf(rintf(a * inv[i]), -127.0f), 127.0f);
+    }
+    if (FMT == S3R_CODES_F16) {
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 p = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
+            h[i] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        *reinterpret_cast<uint4*>(static_cast<__half*>(Q) + idx) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+        uint32_t b[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i >> 2] |= ((uint32_t)(int)q[i] & 0xFFu) << (8 * (i & 3));
+        *reinterpret_cast<uint2*>(static_cast<int8_t*>(Q) + idx) = make_uint2(b[0], b[1]);
+    }
+}
+
+// Block-wide max over a block of `blockDim.x / 32` warps (at most 8).
+__device__ __forceinline__ uint32_t block_max_dyn(uint32_t v, uint32_t* smem) {
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    uint32_t m = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, smem[w]);
+    return m;
+}
+
+// Rows of 16-byte groups: one row per block of 32 * ceil(groups / 128) threads
+// (at most 256), so that each thread holds up to kRowRegs groups between the
+// max and the rounding; longer rows are read again (or recomputed).
+constexpr int kRowRegs = 4;
+
+static inline unsigned row_block_threads(int64_t groups) {
+    const int64_t w = (groups + 32 * kRowRegs - 1) / (32 * kRowRegs);
+    return (unsigned)(32 * (w < 1 ? 1 : (w > 8 ? 8 : w)));
+}
+
+// The row's step and 1/step from its max bits; a non-finite row gets a NaN
+// step, zero codes and the status flag.
+__device__ __forceinline__ float row_scale_finish(uint32_t m, int64_t r, float* scale, int* d_status, bool& bad) {
+    bad = m >= 0x7F800000u;
+    const float amax = __uint_as_float(m);
+    if (threadIdx.x == 0) {
+        scale[r] = bad ? __uint_as_float(0x7FC00000u) : (m ? amax / 127.0f : 1.0f);
+        if (bad) set_status(d_status, S3R_ERR_NONFINITE);
+    }
+    return bad ? 0.0f : (m ? __fdiv_rz(127.0f, amax) : 1.0f);   // |a * inv| <= 127
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) rtne_rows_vec_kernel(const uint16_t* A, int64_t C, int64_t lda, void* Q,
+                                                            float* scale, int* d_status) {
+    __shared__ uint32_t red[8];
+    const int64_t r = (int64_t)blockIdx.x;
+    const int nt = (int)blockDim.x;
+    const uint4* row = reinterpret_cast<const uint4*>(A + r * lda);
+    const int64_t nv = C / 8;
+    uint4 v[kRowRegs];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < kRowRegs; ++i) {
+        const int64_t j = threadIdx.x + (int64_t)nt * i;
+        v[i] = j < nv ? __ldg(row + j) : make_uint4(0u, 0u, 0u, 0u);
+        m = max(m, absmax8_bits(v[i]));
+    }
+    for (int64_t j = threadIdx.x + (int64_t)nt * kRowRegs; j < nv; j += nt) m = max(m, absmax8_bits(__ldg(row + j)));
+    bool bad;
+    const float iv = row_scale_finish(block_max_dyn(m, red), r, scale, d_status, bad);
+    const float inv[8] = {iv, iv, iv, iv, iv, iv, iv, iv};
+#pragma unroll
+    for (int i = 0; i < kRowRegs; ++i) {
+        const int64_t j = threadIdx.x + (int64_t)nt * i;
+        if (j < nv) store_codes8<FMT>(Q, r * C + 8 * j, v[i], inv, bad);
+    }
+    for (int64_t j = threadIdx.x + (int64_t)nt * kRowRegs; j < nv; j += nt)
+        store_codes8<FMT>(Q, r * C + 8 * j, __ldg(row + j), inv, bad);
+}
+
+// The forward SwiGLU gate fused into the per-row RTNE of its output: from
+// bf16 h1 and h3, a = bf16((h1 * sigmoid(h1)) * h3) element by element (fp32,
+// that order), then the row's step max|a| / 127 and codes exactly as
+// rtne_rows_vec_kernel on a.
+__device__ __forceinline__ uint4 swiglu_gate8(const uint4& h1, const uint4& h3) {
+    const uint32_t x2[4] = {h1.x, h1.y, h1.z, h1.w}, z2[4] = {h3.x, h3.y, h3.z, h3.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 x = make_float2(__uint_as_float(x2[k] << 16), __uint_as_float(x2[k] & 0xFFFF0000u));
+        const float2 z = make_float2(__uint_as_float(z2[k] << 16), __uint_as_float(z2[k] & 0xFFFF0000u));
+        const float2 a = f2_mul(f2_mul(x, sigmoid2(x)), z);
+        const __nv_bfloat162 p = __floats2bfloat162_rn(a.x, a.y);
+        w[k] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) swiglu_fwd_rows_kernel(const uint16_t* H1, const uint16_t* H3, int64_t F,
+                                                              int64_t ldh, uint16_t* Aout, void* Q, float* scale,
+                                                              int* d_status) {
+    __shared__ uint32_t red[8];
+    const int64_t r = (int64_t)blockIdx.x;
+    const int nt = (int)blockDim.x;
+    const uint4* h1 = reinterpret_cast<const uint4*>(H1 + r * ldh);
+    const uint4* h3 = reinterpret_cast<const uint4*>(H3 + r * ldh);
+    const int64_t nv = F / 8;
+    uint4 v[kRowRegs];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < kRowRegs; ++i) {
+        const int64_t j = threadIdx.x + (int64_t)nt * i;
+        v[i] = j < nv ? swiglu_gate8(__ldg(h1 + j), __ldg(h3 + j)) : make_uint4(0u, 0u, 0u, 0u);
+        m = max(m, absmax8_bits(v[i]));
+        if (Aout && j < nv) *reinterpret_cast<uint4*>(Aout + r * F + 8 * j) = v[i];
+    }
+    for (int64_t j = threadIdx.x + (int64_t)nt * kRowRegs; j < nv; j += nt) {
+        const uint4 a = swiglu_gate8(__ldg(h1 + j), __ldg(h3 + j));
+        m = max(m, absmax8_bits(a));
+        if (Aout) *reinterpret_cast<uint4*>(Aout + r * F + 8 * j) = a;
+    }
+    bool bad;
+    const float iv = row_scale_finish(block_max_dyn(m, red), r, scale, d_status, bad);
+    const float inv[8] = {iv, iv, iv, iv, iv, iv, iv, iv};
+#pragma unroll
+    for (int i = 0; i < kRowRegs; ++i) {
+        const int64_t j = threadIdx.x + (int64_t)nt * i;
+        if (j < nv) store_codes8<FMT>(Q, r * F + 8 * j, v[i], inv, bad);
+    }
+    for (int64_t j = threadIdx.x + (int64_t)nt * kRowRegs; j < nv; j += nt)
+        store_codes8<FMT>(Q, r * F + 8 * j, swiglu_gate8(__ldg(h1 + j), __ldg(h3 + j)), inv, bad);
+}
+
+// Per-column scales in three stream-ordered launches: the column maxima
+// (atomicMax of the bit patterns into `bits`, zeroed before), the rounding
+// with 1/step from those maxima, then bits -> scale.  Blocks take 64 columns
+// x 256 rows: thread t reads 8 columns (16 bytes) of rows t/8, t/8 + 32, ...
+constexpr int kColStrip = 64, kColChunk = 256;
+
+__global__ void __launch_bounds__(256) rtne_colmax_kernel(const uint16_t* A, int64_t R, int64_t C, int64_t lda,
+                                                          uint32_t* bits) {
+    __shared__ uint32_t part[32][33];
+    const int g = threadIdx.x & 7, rr = threadIdx.x >> 3;
+    const int64_t c0 = (int64_t)blockIdx.x * kColStrip + 8 * g;
+    const int64_t r0 = (int64_t)blockIdx.y * kColChunk;
+    uint32_t m[4] = {0u, 0u, 0u, 0u};
+    if (c0 < C) {
+#pragma unroll 4
+        for (int k = 0; k < kColChunk / 32; ++k) {
+            const int64_t r = r0 + rr + 32 * k;
+            if (r < R) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(A + r * lda + c0));
+                m[0] = __vmaxu2(m[0], v.x & 0x7FFF7FFFu);
+                m[1] = __vmaxu2(m[1], v.y & 0x7FFF7FFFu);
+                m[2] = __vmaxu2(m[2], v.z & 0x7FFF7FFFu);
+                m[3] = __vmaxu2(m[3], v.w & 0x7FFF7FFFu);
+            }
+        }
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) part[rr][4 * g + w] = m[w];
+    __syncthreads();
+    if (threadIdx.x < 32) {   // one word (two columns) per thread, over the 32 row slots
+        uint32_t x = 0u;
+        for (int k = 0; k < 32; ++k) x = __vmaxu2(x, part[k][threadIdx.x]);
+        const int64_t c = (int64_t)blockIdx.x * kColStrip + 2 * threadIdx.x;
+        if (c < C) atomicMax(bits + c, (x & 0xFFFFu) << 16);
+        if (c + 1 < C) atomicMax(bits + c + 1, x & 0xFFFF0000u);
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) rtne_cols_vec_kernel(const uint16_t* A, int64_t R, int64_t C, int64_t lda,
+                                                            void* Q, const uint32_t* bits, int* d_status) {
+    const int g = threadIdx.x & 7, rr = threadIdx.x >> 3;
+    const int64_t c0 = (int64_t)blockIdx.x * kColStrip + 8 * g;
+    const int64_t r0 = (int64_t)blockIdx.y * kColChunk;
+    if (c0 >= C) return;
+    float inv[8];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t m = __ldg(bits + c0 + i);
+        bad = bad || m >= 0x7F800000u;
+        inv[i] = m >= 0x7F800000u ? 0.0f : (m ? __fdiv_rz(127.0f, __uint_as_float(m)) : 1.0f);
+    }
+    if (bad && blockIdx.y == 0 && rr == 0) set_status(d_status, S3R_ERR_NONFINITE);
+#pragma unroll 4
+    for (int k = 0; k < kColChunk / 32; ++k) {
+        const int64_t r = r0 + rr + 32 * k;
+        if (r < R) {
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(A + r * lda + c0));
+            if (bad) {   // a non-finite column codes to 0: mask its values (inv = 0 would give NaN * 0)
+                uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (inv[i] == 0.0f) w[i >> 1] &= (i & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            }
+            store_codes8<FMT>(Q, r * C + c0, v, inv, false);
+        }
+    }
+}
+
+__global__ void rtne_col_scale_kernel(const uint32_t* bits, int64_t C, float* scale) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    const uint32_t m = bits[c];
+    scale[c] = m >= 0x7F800000u ? __uint_as_float(0x7FC00000u) : (m ? __uint_as_float(m) / 127.0f : 1.0f);
+}
+
 }  // namespace s3r
 
 using namespace s3r;
@@ -1356,6 +1586,30 @@ extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, c
     if (lda < C) return S3R_ERR_SHAPE;
     if (s_x || s_w) return S3R_ERR_ARG;  // forward operands are not folded
     const uint16_t* a = static_cast<const uint16_t*>(A);
+    const bool vec = s3r_aligned16(A) && s3r_aligned16(Q) && C % 8 == 0 && lda % 8 == 0;
+    const bool f16 = code_format == S3R_CODES_F16;
+    if (vec && scale_axis == S3R_AXIS_ROW && R <= 0x7FFFFFFF) {
+        const unsigned nt = row_block_threads(C / 8);
+        if (f16) rtne_rows_vec_kernel<S3R_CODES_F16><<<(unsigned)R, nt, 0, stream>>>(a, C, lda, Q, scale, d_status);
+        else rtne_rows_vec_kernel<S3R_CODES_S8><<<(unsigned)R, nt, 0, stream>>>(a, C, lda, Q, scale, d_status);
+        S3R_CHECK_LAUNCH();
+        return S3R_OK;
+    }
+    if (vec && scale_axis == S3R_AXIS_COL && s3r_cdiv(R, kColChunk) <= 65535) {
+        // the column maxima are gathered in `scale` itself (as bit patterns), then converted
+        uint32_t* bits = reinterpret_cast<uint32_t*>(scale);
+        const cudaError_t e = cudaMemsetAsync(bits, 0, (size_t)C * 4, stream);
+        if (e != cudaSuccess) return s3r_cuda_fail("rtne_quantize: cudaMemsetAsync", e);
+        const dim3 grid((unsigned)s3r_cdiv(C, kColStrip), (unsigned)s3r_cdiv(R, kColChunk));
+        rtne_colmax_kernel<<<grid, 256, 0, stream>>>(a, R, C, lda, bits);
+        S3R_CHECK_LAUNCH();
+        if (f16) rtne_cols_vec_kernel<S3R_CODES_F16><<<grid, 256, 0, stream>>>(a, R, C, lda, Q, bits, d_status);
+        else rtne_cols_vec_kernel<S3R_CODES_S8><<<grid, 256, 0, stream>>>(a, R, C, lda, Q, bits, d_status);
+        S3R_CHECK_LAUNCH();
+        rtne_col_scale_kernel<<<(unsigned)s3r_cdiv(C, 256), 256, 0, stream>>>(bits, C, scale);
+        S3R_CHECK_LAUNCH();
+        return S3R_OK;
+    }
     if (scale_axis == S3R_AXIS_ROW) {
         if (R > 0x7FFFFFFF) return S3R_ERR_UNSUPPORTED;
         rtne_rows_kernel<<<(unsigned)R, 256, 0, stream>>>(a, R, C, lda, Q, code_format, scale, d_status);
@@ -1365,6 +1619,28 @@ extern "C" int rtne_quantize(const void* A, int64_t R, int64_t C, int64_t lda, c
     } else {
         return S3R_ERR_ARG;
     }
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+extern "C" int swiglu_fwd_quantize(const void* h1, const void* h3, int64_t T, int64_t F, int64_t ldh, void* a,
+                                   void* Q, int code_format, float* scale, int* d_status, cudaStream_t stream) {
+    if (T < 0 || F < 0 || !valid_fmt(code_format)) return S3R_ERR_ARG;
+    if (T == 0 || F == 0) return S3R_OK;
+    if (!h1 || !h3 || !Q || !scale) return S3R_ERR_ARG;
+    if (ldh < F) return S3R_ERR_SHAPE;
+    if (T > 0x7FFFFFFF) return S3R_ERR_UNSUPPORTED;
+    if (F % 8 != 0 || ldh % 8 != 0 || !s3r_aligned16(h1) || !s3r_aligned16(h3) || !s3r_aligned16(Q) ||
+        (a && !s3r_aligned16(a)))
+        return S3R_ERR_ALIGN;
+    const uint16_t* p1 = static_cast<const uint16_t*>(h1);
+    const uint16_t* p3 = static_cast<const uint16_t*>(h3);
+    uint16_t* pa = static_cast<uint16_t*>(a);
+    const unsigned nt = row_block_threads(F / 8);
+    if (code_format == S3R_CODES_F16)
+        swiglu_fwd_rows_kernel<S3R_CODES_F16><<<(unsigned)T, nt, 0, stream>>>(p1, p3, F, ldh, pa, Q, scale, d_status);
+    else
+        swiglu_fwd_rows_kernel<S3R_CODES_S8><<<(unsigned)T, nt, 0, stream>>>(p1, p3, F, ldh, pa, Q, scale, d_status);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
 }

@@ -87,6 +87,58 @@ def test_gemm_fwd_swiglu_bit_exact(s3r, orc, T, K, F):
     assert np.array_equal(_bits(a), ra)
 
 
+@pytest.mark.parametrize("T,F,pad", [(64, 5632, 0), (37, 8, 0), (300, 13000, 8), (5, 136, 24)])
+@pytest.mark.parametrize("fmt", ["f16", "s8"])
+def test_swiglu_fwd_quantize_matches_oracle(s3r, orc, T, F, pad, fmt):
+    """The gate fused into the RTNE of a: a bit for bit as the oracle's
+    swiglu_fwd, codes and scales as its RTNE operand of a; rows longer than
+    the register-resident part recompute the gate for the codes."""
+    rng = np.random.default_rng(T + F)
+    std = 0.02 * np.sqrt(2048)
+    full1 = torch.from_numpy((rng.standard_normal((T, F + pad)) * std).astype(np.float32)).to(torch.bfloat16)
+    full3 = torch.from_numpy((rng.standard_normal((T, F + pad)) * std).astype(np.float32)).to(torch.bfloat16)
+    full1[min(2, T - 1), :] = 0   # an all-zero row: a = 0, scale 1
+    h1, h3 = full1[:, :F], full3[:, :F]
+    cf = s3r.CODES_F16 if fmt == "f16" else s3r.CODES_S8
+    a, Q, sc = s3r.swiglu_fwd_quantize(h1.cuda(), h3.cuda(), code_format=cf)
+    f = lambda t: orc.bf16_to_f32(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    _, _, ra = orc.swiglu_fwd(f(h1), f(h3))
+    assert np.array_equal(_bits(a), ra)
+    rq, rs = orc.rtne_operand(orc.bf16_to_f32(ra), 0)
+    got = Q.cpu().float().numpy().astype(np.int8) if fmt == "f16" else Q.cpu().numpy()
+    assert np.array_equal(got, rq)
+    assert np.array_equal(sc.cpu().numpy(), rs)
+    none, Q2, sc2 = s3r.swiglu_fwd_quantize(h1.cuda(), h3.cuda(), keep_a=False, code_format=cf)
+    assert none is None and torch.equal(Q2, Q) and torch.equal(sc2, sc)
+
+
+def test_swiglu_fwd_quantize_nonfinite_and_alignment(s3r):
+    h1 = torch.randn(4, 64).to(torch.bfloat16).cuda()
+    h3 = torch.randn(4, 64).to(torch.bfloat16).cuda()
+    h1[1, 7] = float("inf")
+    st = s3r.new_status()
+    a, Q, sc = s3r.swiglu_fwd_quantize(h1, h3, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == -4   # S3R_ERR_NONFINITE
+    assert torch.isnan(sc[1]).item() and torch.count_nonzero(Q[1]).item() == 0
+    assert not torch.isnan(sc[[0, 2, 3]]).any()
+    with pytest.raises(s3r.S3RError, match="ALIGN"):
+        s3r.swiglu_fwd_quantize(h1[:, :60], h3[:, :60])
+
+
+def test_gemm_fwd_pair_without_gate(s3r):
+    """With a = NULL the launch writes the same h1, h3 and leaves a alone."""
+    rng = np.random.default_rng(11)
+    T, K, F = 192, 384, 264
+    X8, W1, W3 = _codes(rng, (T, K)), _codes(rng, (K, F)), _codes(rng, (K, F))
+    c = lambda a: torch.from_numpy(a).cuda()
+    s_x, s_w1, s_w3 = (c((rng.random(n) * 0.01 + 1e-4).astype(np.float32)) for n in (T, F, F))
+    h1, h3, a = s3r.int8_gemm_fwd_swiglu(_dev_codes(X8), s_x, _dev_codes(W1), s_w1, _dev_codes(W3), s_w3)
+    g1, g3, none = s3r.int8_gemm_fwd_swiglu(_dev_codes(X8), s_x, _dev_codes(W1), s_w1, _dev_codes(W3), s_w3,
+                                            with_gate=False)
+    assert none is None and torch.equal(g1, h1) and torch.equal(g3, h3)
+
+
 def _block(T, d, F, seed=0):
     inp = workloads.ffn_inputs(T, d, F, S=T, seed=workloads.DATA_SEED + seed)
     return inp.X, inp.W1, inp.W3, inp.W2
@@ -125,6 +177,9 @@ def test_ffn_forward_matches_oracle(s3r, orc, T, d, F):
         getattr(again.ops, name).copy_(getattr(out.ops, name))
     s3r.ffn_forward(X.cuda(), out=again, quantize_weights=False)
     assert torch.equal(again.Y, out.Y) and torch.equal(again.a, out.a)
+    # without keeping a (the backward reads only its codes)
+    lean = s3r.ffn_forward(X.cuda(), W1.cuda(), W3.cuda(), W2.cuda(), keep_a=False)
+    assert lean.a is None and torch.equal(lean.Y, out.Y) and torch.equal(lean.ops.A8, out.ops.A8)
 
 
 def test_ffn_forward_full_size_sampled_rows(s3r, orc):
@@ -163,3 +218,47 @@ def test_forward_edge_cases(s3r):
     with pytest.raises(s3r.S3RError, match="UNSUPPORTED"):
         s3r.int8_gemm_fwd(torch.ones((8, 16), dtype=torch.int8, device=dev), s[:8],
                           torch.ones((16, 16), dtype=torch.int8, device=dev), s)
+
+
+@pytest.mark.parametrize("R,C,pad", [(300, 264, 0), (77, 13000, 8), (2048, 5632, 0), (5632, 2048, 0), (33, 12, 0),
+                                     (19, 100, 3), (600, 8, 0)])
+@pytest.mark.parametrize("fmt", ["f16", "s8"])
+def test_rtne_operand_row_and_column_scales(s3r, orc, R, C, pad, fmt):
+    """rtne_quantize per row and per column against the oracle's RTNE operand:
+    16-byte rows (vector kernels, rows longer than the register-resident
+    part included) and odd widths or strides (element kernels); an all-zero
+    row and column, and a row and a column holding an Inf."""
+    rng = np.random.default_rng(R + C + pad)
+    full = torch.from_numpy((rng.standard_normal((R, C + pad)) * 0.02).astype(np.float32)).to(torch.bfloat16)
+    full[1, :] = 0
+    full[:, 2] = 0
+    A = full[:, :C]
+    cf = s3r.CODES_F16 if fmt == "f16" else s3r.CODES_S8
+    f = lambda t: orc.bf16_to_f32(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    for axis in (s3r.AXIS_ROW, s3r.AXIS_COL):
+        Q, sc = s3r.rtne_quantize(A.cuda(), axis, code_format=cf)
+        rq, rs = orc.rtne_operand(f(A), 0 if axis == s3r.AXIS_ROW else 1)
+        got = Q.cpu().float().numpy().astype(np.int8) if fmt == "f16" else Q.cpu().numpy()
+        assert np.array_equal(got, rq)
+        assert np.array_equal(sc.cpu().numpy(), rs)
+    # a non-finite value: its row (column) codes to 0 with a NaN scale and the status flag
+    B = A.clone()
+    B[3, 5] = float("inf")
+    for axis, idx in ((s3r.AXIS_ROW, 3), (s3r.AXIS_COL, 5)):
+        st = s3r.new_status()
+        Q, sc = s3r.rtne_quantize(B.cuda(), axis, code_format=cf, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == -4   # S3R_ERR_NONFINITE
+        q = Q.cpu().float()
+        line = q[idx] if axis == s3r.AXIS_ROW else q[:, idx]
+        assert torch.count_nonzero(line).item() == 0 and torch.isnan(sc[idx]).item()
+        clean = torch.ones(sc.numel(), dtype=torch.bool)
+        clean[idx] = False
+        ref_q, ref_s = s3r.rtne_quantize(A.cuda(), axis, code_format=cf)
+        assert torch.equal(sc.cpu()[clean], ref_s.cpu()[clean])
+        keep = (q != ref_q.cpu().float())
+        if axis == s3r.AXIS_ROW:
+            keep[idx] = False
+        else:
+            keep[:, idx] = False
+        assert not keep.any()
