@@ -64,6 +64,9 @@ def lib():
             L.orc_quantize_window_ex.restype = C.c_int
             L.orc_float_to_bf16.restype = C.c_uint16
             L.orc_float_to_bf16.argtypes = [C.c_float]
+            L.orc_sr_bf16.restype = C.c_uint16
+            L.orc_sr_bf16.argtypes = [C.c_float, C.c_uint32]
+            L.orc_sr_bf16_matrix.restype = C.c_int
             L.orc_inv127_rz.restype = C.c_float
             L.orc_inv127_rz.argtypes = [C.c_float]
             L.orc_sr_step.restype = C.c_float
@@ -398,6 +401,24 @@ def swiglu_fwd(h1f, h3f):
     ab = np.zeros(h1f.shape, dtype=np.uint16)
     lib().orc_swiglu_fwd(_p(h1f), _p(h3f), _i64(h1f.size), _p(h1b), _p(h3b), _p(ab))
     return h1b, h3b, ab
+
+
+def sr_bf16_scalar(x: float, v: int) -> int:
+    """bf16 bits of x rounded stochastically with the 16-bit threshold v."""
+    return int(lib().orc_sr_bf16(float(x), int(v)))
+
+
+def sr_bf16(X, mode=S3R, seed=0, tensor_id=0) -> np.ndarray:
+    """fp32 [T, N] -> bf16 bit patterns [T, N]: S3R (one 16-bit threshold per
+    token), INDEP (one per element) or RTNE ([S3R] §II, §III-B)."""
+    X = _f32(X)
+    T, N = X.shape
+    Y = np.zeros((T, N), dtype=np.uint16)
+    st = lib().orc_sr_bf16_matrix(_p(X), _i64(T), _i64(N), _i64(N), C.c_int(mode), C.c_uint64(seed),
+                                  C.c_uint32(tensor_id), _p(Y))
+    if st != 0:
+        raise ValueError(f"orc_sr_bf16_matrix status {st}")
+    return Y
 
 
 @dataclass

@@ -570,3 +570,62 @@ void orc_swiglu_fwd(const float* h1f, const float* h3f, int64_t n, uint16_t* h1b
         ab[i] = orc_float_to_bf16(silu * z);
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Stochastic rounding of fp32 to bf16 with 16-bit thresholds.  [S3R] §II:   */
+/* the hardware conversion to floating-point formats rounds stochastically    */
+/* from random bits the program supplies; §III-B: one threshold per token,    */
+/* shared by all its channels.  On the magnitude: bf16 keeps the upper 16     */
+/* bits of the fp32 pattern.  With L the 16 dropped bits and v a 16-bit       */
+/* threshold, the magnitude moves up one bf16 step iff L > v; for v uniform   */
+/* on 0..65535 that has probability L / 2^16, the distance to the lower       */
+/* neighbour over the spacing ([SRB] "The probability formula").  Values      */
+/* beyond the largest finite bf16 (infinities included) saturate to it, NaN   */
+/* becomes 0x7FFF: the saturating rule of the conversion the kernels use.     */
+/* ------------------------------------------------------------------------- */
+uint16_t orc_sr_bf16(float x, uint32_t v) {
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    uint32_t sign = (u >> 16) & 0x8000u, mag = u & 0x7FFFFFFFu;
+    if (mag > 0x7F800000u) return 0x7FFFu;
+    uint32_t hi = mag >> 16, low = mag & 0xFFFFu;
+    if (low > (v & 0xFFFFu)) hi += 1u;
+    if (hi >= 0x7F80u) hi = 0x7F7Fu;
+    return (uint16_t)(sign | hi);
+}
+
+/* X [T, N] fp32 (row stride ldx) -> Y [T, N] bf16 bits (row stride N).
+ *   ORC_S3R:   v = the upper 16 bits of token t's word (word 0 of
+ *              Philox(counter = (t, t >> 32, 0, 0)), the word of
+ *              orc_token_threshold: its 24-bit threshold truncated to 16 bits);
+ *   ORC_INDEP: v = the upper 16 bits of element e = t N + n's word
+ *              (word e mod 4 of Philox(counter = e / 4));
+ *   ORC_RTNE:  round to nearest even (orc_float_to_bf16). */
+int orc_sr_bf16_matrix(const float* X, int64_t T, int64_t N, int64_t ldx, int mode, uint64_t seed,
+                       uint32_t tensor_id, uint16_t* Y) {
+    if (T < 0 || N < 0 || ldx < N) return ORC_ERR_ARG;
+    if (mode != ORC_S3R && mode != ORC_INDEP && mode != ORC_RTNE) return ORC_ERR_ARG;
+    uint32_t key[2] = {(uint32_t)seed, tensor_id};
+    for (int64_t t = 0; t < T; ++t) {
+        uint32_t out[4];
+        uint32_t ctr[4] = {(uint32_t)t, (uint32_t)((uint64_t)t >> 32), 0u, 0u};
+        orc_philox4x32_10(ctr, key, out);
+        uint32_t v_tok = out[0] >> 16;
+        for (int64_t n = 0; n < N; ++n) {
+            float x = X[t * ldx + n];
+            if (mode == ORC_RTNE) {
+                Y[t * N + n] = orc_float_to_bf16(x);
+                continue;
+            }
+            uint32_t v = v_tok;
+            if (mode == ORC_INDEP) {
+                uint64_t e = (uint64_t)t * (uint64_t)N + (uint64_t)n, c = e >> 2;
+                uint32_t ce[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u}, w[4];
+                orc_philox4x32_10(ce, key, w);
+                v = w[e & 3u] >> 16;
+            }
+            Y[t * N + n] = orc_sr_bf16(x, v);
+        }
+    }
+    return ORC_OK;
+}
