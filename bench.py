@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn",
-                                              "moe", "fwd", "fwd_gate", "fwd_gate_quantize", "fwd_down"],
+                                              "moe", "fwd", "fwd_gate", "fwd_gate_quantize", "fwd_down",
+                                              "sr_bf16"],
                     help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
     return ap.parse_args()
 
@@ -414,6 +415,23 @@ def time_forward(s3r, inp, pk, steps=10, warmup=3):
             "vs_bf16": round(bms / ms, 3)}
 
 
+def time_sr_bf16(s3r, pk, steps=20, warmup=3):
+    """Context: stochastic rounding of fp32 to bf16 on the hardware conversion
+    with S3R's per-token thresholds, per-element thresholds, and RTNE, at
+    [16384, 8192] (fp32 in, bf16 out: 6 algorithmic bytes per element; 805 MB
+    per call, larger than L2)."""
+    Tq, Nq = 16384, 8192
+    G = (workloads.quantize_sweep_input(Tq, Nq, seed=workloads.DATA_SEED + 3).float() * 1e3).cuda()
+    Y = torch.empty((Tq, Nq), dtype=torch.bfloat16, device="cuda")
+    out = {"shape": [Tq, Nq]}
+    for name, rm in (("s3r", s3r.ROUND_S3R), ("indep_sr", s3r.ROUND_INDEP), ("rtne", s3r.ROUND_RTNE)):
+        ms = _event_ms(lambda: s3r.s3r_sr_bf16(G, rm, seed=1, Y=Y), steps, warmup)
+        gbs = 6.0 * Tq * Nq / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
+    del G, Y
+    return out
+
+
 def time_quantize_sweep(s3r, steps=20):
     """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100
     outliers; int8 codes (1 B) and fp16-carried codes (2 B)."""
@@ -594,6 +612,7 @@ def run_ours(args, world, rank, local):
                   "s3r_T4096", "s3r_T65536"):
             qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
         ctx["quantize_sweep"] = qs
+        ctx["sr_bf16_sweep"] = time_sr_bf16(s3r, pk)
         ctx["moe_e8_d4096_F1408_tok16384_top2"] = time_moe(s3r)
         ctx["swiglu_ffn_d4096_F14336_T16384"] = time_ffn_large(s3r)
         line["context"] = ctx
@@ -637,6 +656,10 @@ def run_kernel_case(args):
                                                            with_gate=False)
         fns["fwd_gate_quantize"] = lambda: s3r.swiglu_fwd_quantize(o.h1, o.h3, keep_a=False, Q=o.A8, scale=o.s_a)
         fns["fwd_down"] = lambda: s3r.int8_gemm_fwd(o.A8, o.s_a, o.W2_8, o.s_w2, Y=fo.Y)
+    if args.kernel_case == "sr_bf16":
+        Gb = (workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).float() * 1e3).cuda()
+        Yb = torch.empty((16384, 8192), dtype=torch.bfloat16, device="cuda")
+        fns["sr_bf16"] = lambda: s3r.s3r_sr_bf16(Gb, s3r.ROUND_S3R, seed=1, Y=Yb)
     if args.kernel_case == "quantize_sweep":
         Gs = workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).cuda()
         qs = s3r.s3r_quantize(Gs, code_format=s3r.CODES_S8)

@@ -383,6 +383,30 @@ int swiglu_fwd_quantize(const void* h1, const void* h3, int64_t T, int64_t F, in
                         int code_format, float* scale, int* d_status, cudaStream_t stream);
 
 /*
+ * s3r_sr_bf16 -- stochastic rounding of fp32 to bf16 with S3R's shared
+ * thresholds on the hardware stochastic-rounding conversion ([S3R] §II:
+ * Blackwell rounds to floating-point formats stochastically from random bits
+ * the program supplies; §III-B: one threshold per token).  Per element, on
+ * the magnitude: bf16 keeps the upper 16 bits of the fp32 pattern, and moves
+ * up one bf16 step iff the 16 dropped bits exceed the 16-bit threshold v
+ * (probability = distance to the lower neighbour over the spacing); the sign
+ * is kept; beyond the largest finite bf16 (infinities included) saturates to
+ * it, NaN becomes 0x7FFF.
+ *   round_mode S3R_ROUND_S3R:   v = (w >> 16), w = token t's word as in
+ *                               s3r_quantize (Philox4x32-10, counter
+ *                               (t mod 2^32, t >> 32, 0, 0), key (seed mod
+ *                               2^32, tensor_id)): all channels share it;
+ *              S3R_ROUND_INDEP: v = (w_e >> 16), w_e = word (e mod 4) of
+ *                               Philox(counter e / 4), e = t N + n;
+ *              S3R_ROUND_RTNE:  round to nearest even (no saturation).
+ * In : X [T, N] fp32 (row stride ldx).  Out: Y [T, N] bf16 (row stride ldy).
+ * 16-byte aligned X, Y with ldx % 4 == 0 and ldy % 8 == 0 take the vector
+ * path; any other layout is converted element by element (same results).
+ */
+int s3r_sr_bf16(const float* X, int64_t T, int64_t N, int64_t ldx, int round_mode, uint64_t seed, uint32_t tensor_id,
+                void* Y, int64_t ldy, cudaStream_t stream);
+
+/*
  * ffn_forward -- the SwiGLU FFN block forward with INT8 GEMMs, the operands
  * of ffn_backward as its outputs:
  *   1. X8, s_x   = rtne_quantize(X, per row)

@@ -408,13 +408,14 @@ def sr_bf16_scalar(x: float, v: int) -> int:
     return int(lib().orc_sr_bf16(float(x), int(v)))
 
 
-def sr_bf16(X, mode=S3R, seed=0, tensor_id=0) -> np.ndarray:
+def sr_bf16(X, mode=S3R, seed=0, tensor_id=0, t0=0) -> np.ndarray:
     """fp32 [T, N] -> bf16 bit patterns [T, N]: S3R (one 16-bit threshold per
-    token), INDEP (one per element) or RTNE ([S3R] §II, §III-B)."""
+    token), INDEP (one per element) or RTNE ([S3R] §II, §III-B).  Row i is
+    token t0 + i."""
     X = _f32(X)
     T, N = X.shape
     Y = np.zeros((T, N), dtype=np.uint16)
-    st = lib().orc_sr_bf16_matrix(_p(X), _i64(T), _i64(N), _i64(N), C.c_int(mode), C.c_uint64(seed),
+    st = lib().orc_sr_bf16_matrix(_p(X), _i64(T), _i64(N), _i64(N), _i64(t0), C.c_int(mode), C.c_uint64(seed),
                                   C.c_uint32(tensor_id), _p(Y))
     if st != 0:
         raise ValueError(f"orc_sr_bf16_matrix status {st}")

@@ -594,27 +594,29 @@ uint16_t orc_sr_bf16(float x, uint32_t v) {
     return (uint16_t)(sign | hi);
 }
 
-/* X [T, N] fp32 (row stride ldx) -> Y [T, N] bf16 bits (row stride N).
+/* X [T, N] fp32 (row stride ldx) -> Y [T, N] bf16 bits (row stride N); row i
+ * is token t = t0 + i (t0 > 0 evaluates a window of a larger tensor).
  *   ORC_S3R:   v = the upper 16 bits of token t's word (word 0 of
  *              Philox(counter = (t, t >> 32, 0, 0)), the word of
  *              orc_token_threshold: its 24-bit threshold truncated to 16 bits);
  *   ORC_INDEP: v = the upper 16 bits of element e = t N + n's word
  *              (word e mod 4 of Philox(counter = e / 4));
  *   ORC_RTNE:  round to nearest even (orc_float_to_bf16). */
-int orc_sr_bf16_matrix(const float* X, int64_t T, int64_t N, int64_t ldx, int mode, uint64_t seed,
+int orc_sr_bf16_matrix(const float* X, int64_t T, int64_t N, int64_t ldx, int64_t t0, int mode, uint64_t seed,
                        uint32_t tensor_id, uint16_t* Y) {
-    if (T < 0 || N < 0 || ldx < N) return ORC_ERR_ARG;
+    if (T < 0 || N < 0 || ldx < N || t0 < 0) return ORC_ERR_ARG;
     if (mode != ORC_S3R && mode != ORC_INDEP && mode != ORC_RTNE) return ORC_ERR_ARG;
     uint32_t key[2] = {(uint32_t)seed, tensor_id};
-    for (int64_t t = 0; t < T; ++t) {
+    for (int64_t i = 0; i < T; ++i) {
+        int64_t t = t0 + i;
         uint32_t out[4];
         uint32_t ctr[4] = {(uint32_t)t, (uint32_t)((uint64_t)t >> 32), 0u, 0u};
         orc_philox4x32_10(ctr, key, out);
         uint32_t v_tok = out[0] >> 16;
         for (int64_t n = 0; n < N; ++n) {
-            float x = X[t * ldx + n];
+            float x = X[i * ldx + n];
             if (mode == ORC_RTNE) {
-                Y[t * N + n] = orc_float_to_bf16(x);
+                Y[i * N + n] = orc_float_to_bf16(x);
                 continue;
             }
             uint32_t v = v_tok;
@@ -624,7 +626,7 @@ int orc_sr_bf16_matrix(const float* X, int64_t T, int64_t N, int64_t ldx, int mo
                 orc_philox4x32_10(ce, key, w);
                 v = w[e & 3u] >> 16;
             }
-            Y[t * N + n] = orc_sr_bf16(x, v);
+            Y[i * N + n] = orc_sr_bf16(x, v);
         }
     }
     return ORC_OK;

@@ -74,6 +74,7 @@ _SIGS = {
                                     _VP]),
     "swiglu_fwd_quantize": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _VP, _VP]),
     "ffn_forward": (_INT, [_VP, _VP]),
+    "s3r_sr_bf16": (_INT, [_VP, _I64, _I64, _I64, _INT, _U64, _U32, _VP, _I64, _VP]),
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
@@ -437,6 +438,18 @@ def swiglu_fwd_quantize(h1, h3, a=None, keep_a=True, Q=None, scale=None, status=
                                      _ptr(a if keep_a else None), _ptr(Q), code_format_of(Q), _ptr(scale),
                                      _ptr(status), _stream(stream)), "swiglu_fwd_quantize")
     return (a if keep_a else None), Q, scale
+
+
+def s3r_sr_bf16(X, round_mode=ROUND_S3R, seed=0, tensor_id=0, Y=None, stream=None):
+    """fp32 [T, N] -> bf16 [T, N], stochastically rounded with one 16-bit
+    threshold per token (ROUND_S3R), per element (ROUND_INDEP), or RTNE."""
+    assert X.dtype == torch.float32 and X.dim() == 2
+    T, N = X.shape
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
+    _check(lib().s3r_sr_bf16(_ptr(X), T, N, X.stride(0), round_mode, seed, tensor_id, _ptr(Y), Y.stride(0),
+                             _stream(stream)), "s3r_sr_bf16")
+    return Y
 
 
 class _FfnFwdArgs(C.Structure):

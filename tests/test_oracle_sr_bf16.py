@@ -88,6 +88,10 @@ def test_matrix_s3r_shares_one_threshold_per_token(orc):
     for t in range(T):
         v = int(orc.philox4x32_10([t, 0, 0, 0], [7, 5])[0]) >> 16
         assert np.array_equal(up[t], lows[t] > v)
+    # a window of rows starting at token 10 equals those rows of the whole
+    assert np.array_equal(orc.sr_bf16(X[10:14], orc.S3R, seed=7, tensor_id=5, t0=10), Y[10:14])
+    assert np.array_equal(orc.sr_bf16(X[10:14], orc.INDEP, seed=7, tensor_id=5, t0=10),
+                          orc.sr_bf16(X, orc.INDEP, seed=7, tensor_id=5)[10:14])
     Yi = orc.sr_bf16(X, orc.INDEP, seed=7, tensor_id=5)
     upi = (Yi & 0x7FFF) != ((np.abs(X).view(np.uint32) >> 16) & 0x7FFF)
     for t in (0, 5, 23):
