@@ -373,8 +373,9 @@ class FFNForwardOperands:
 
 
 def gemm_fwd(X8, s_x, W8, s_w):
-    """INT8 forward Y = diag(s_x) X8 W8 diag(s_w): exact int32 per 128-wide block,
-    blocks added in fp32 in order, then (acc * s_x) * s_w in fp32 ([S3R] §III-A)."""
+    """INT8 forward Y = diag(s_x) X8 W8 diag(s_w): the exact integer sum (S32
+    accumulation), one rounding to fp32, then (acc * s_x) * s_w in fp32
+    ([S3R] §III-A)."""
     X8 = np.ascontiguousarray(X8, dtype=np.int8)
     W8 = np.ascontiguousarray(W8, dtype=np.int8)
     T, K = X8.shape

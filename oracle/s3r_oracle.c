@@ -526,23 +526,18 @@ void orc_swiglu_bwd(const float* dA, const float* h1, const float* h3, int64_t n
 
 /* ------------------------------------------------------------------------- */
 /* INT8 forward ([S3R] §III-A: Y = diag(s_x) X_hat W_hat diag(s_w), with the  */
-/* RTNE operands of orc_rtne_operand).  The contraction runs in 128-wide      */
-/* blocks: each block's int32 sum is exact, the blocks are added in ascending */
-/* order in fp32, and the result is rescaled in fp32 as (acc * s_x[t]) *      */
+/* RTNE operands of orc_rtne_operand).  S8 x S8 products accumulate exactly  */
+/* as integers (the section's S32 accumulation), the sum is converted to fp32 */
+/* once (round to nearest even) and rescaled in fp32 as (acc * s_x[t]) *      */
 /* s_w[n].  X8 [T, K] int8, W8 [K, N] int8, Y [T, N] fp32.                    */
 /* ------------------------------------------------------------------------- */
 void orc_gemm_fwd(const int8_t* X8, const float* s_x, const int8_t* W8, const float* s_w, int64_t T, int64_t K,
                   int64_t N, float* Y) {
     for (int64_t t = 0; t < T; ++t)
         for (int64_t n = 0; n < N; ++n) {
-            float acc = 0.0f;
-            for (int64_t k0 = 0; k0 < K; k0 += 128) {
-                int32_t blk = 0;
-                for (int64_t k = k0; k < K && k < k0 + 128; ++k)
-                    blk += (int32_t)X8[t * K + k] * (int32_t)W8[k * N + n];
-                acc = acc + (float)blk;
-            }
-            float y = acc * s_x[t];
+            int64_t acc = 0;
+            for (int64_t k = 0; k < K; ++k) acc += (int64_t)X8[t * K + k] * (int64_t)W8[k * N + n];
+            float y = (float)acc * s_x[t];
             Y[t * N + n] = y * s_w[n];
         }
 }

@@ -3,7 +3,7 @@
 Source: "Efficient Quantization Training with Stochastic Rounding via
 Structured Subspace Randomness" -- §III-A (forward operands rounded to
 nearest with per-token and per-output-channel scales, Y = diag(s_x) X_hat
-W_hat diag(s_w) from S32 accumulation), §IV-A (GEMM outputs rounded to bf16;
+W_hat diag(s_w) from S32 (exact integer) accumulation), §IV-A (GEMM outputs rounded to bf16;
 the SwiGLU FFN block).
 """
 import numpy as np
@@ -11,10 +11,11 @@ import pytest
 import torch
 
 
-def test_gemm_fwd_single_block_closed_form(orc):
-    """K <= 128: one exact int32 block, then (I * s_x) * s_w in fp32."""
-    rng = np.random.default_rng(0)
-    T, K, N = 37, 128, 53
+@pytest.mark.parametrize("T,K,N", [(37, 128, 53), (16, 1000, 24), (5, 4096, 7), (64, 300, 64)])
+def test_gemm_fwd_is_the_exact_integer_product_rescaled(orc, T, K, N):
+    """Against numpy: the int64 matrix product, converted to float32 (round to
+    nearest), then times s_x and s_w in float32."""
+    rng = np.random.default_rng(T + K)
     X8 = rng.integers(-127, 128, size=(T, K)).astype(np.int8)
     W8 = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
     s_x = (rng.random(T) * 0.1 + 0.01).astype(np.float32)
@@ -24,10 +25,22 @@ def test_gemm_fwd_single_block_closed_form(orc):
     assert np.array_equal(orc.gemm_fwd(X8, s_x, W8, s_w), exp)
 
 
+def test_gemm_fwd_saturated_sum_rounds_once(orc):
+    """All codes +127 over K = 8192: the sum 8192 * 127^2 = 132,128,768 needs
+    27 bits; it is rounded to fp32 once (a blockwise fp32 sum would round on
+    the way)."""
+    K = 8192
+    X8 = np.full((1, K), 127, np.int8)
+    W8 = np.full((K, 1), 127, np.int8)
+    one = np.ones(1, np.float32)
+    y = orc.gemm_fwd(X8, one, W8, one)[0, 0]
+    assert y == np.float32(K * 127 * 127)
+
+
 @pytest.mark.parametrize("T,K,N", [(16, 1000, 24), (5, 4096, 7), (64, 300, 64)])
 def test_gemm_fwd_equals_exact_product_within_fp32_bound(orc, T, K, N):
-    """Brute force: the exact int64 product scaled in fp64, within the fp32
-    rounding of the block sums and the two rescales."""
+    """Brute force: the exact int64 product scaled in fp64, within three fp32
+    roundings (the conversion and the two rescales)."""
     rng = np.random.default_rng(T + K)
     X8 = rng.integers(-127, 128, size=(T, K)).astype(np.int8)
     W8 = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
@@ -35,9 +48,7 @@ def test_gemm_fwd_equals_exact_product_within_fp32_bound(orc, T, K, N):
     s_w = (rng.random(N) + 0.5).astype(np.float32)
     I = X8.astype(np.int64) @ W8.astype(np.int64)
     exact = I.astype(np.float64) * s_x[:, None].astype(np.float64) * s_w[None, :].astype(np.float64)
-    mag = (np.abs(X8.astype(np.float64)) @ np.abs(W8.astype(np.float64))) * s_x[:, None] * s_w[None, :]
-    nblk = -(-K // 128)
-    bound = (nblk + 2) * 2.0 ** -24 * mag + 1e-30
+    bound = 3 * 2.0 ** -24 * np.abs(exact) + 1e-30
     assert np.all(np.abs(orc.gemm_fwd(X8, s_x, W8, s_w) - exact) <= bound)
 
 
