@@ -334,11 +334,9 @@ int int8_gemm_dw(const void* X8, const void* Q, const float* tile_scale, int cod
  * the forward operands are rounded to nearest with a per-token scale for the
  * input and a per-output-channel scale for the weight, multiplied with S32
  * accumulation and rescaled on both sides):
- *   Y[t, n] = (acc[t, n] * s_x[t]) * s_w[n]            in fp32, in this order,
- *   acc     = sum over 128-wide blocks kb (ascending) of the exact integer
- *             block sum  sum_{k in kb} X8[t, k] W8[k, n], added in fp32.
- * Each block sum is below 2^24 in magnitude, so it is exact; only the
- * block-to-block additions and the two rescales round.
+ *   Y[t, n] = (fp32(acc[t, n]) * s_x[t]) * s_w[n]      in fp32, in this order,
+ *   acc     = sum_k X8[t, k] W8[k, n]                   exact (S32; K * 127^2 < 2^31)
+ * fp32() rounds to nearest even; only it and the two rescales round.
  * In : X8 [T, K] codes (row stride K), s_x [T]; W8 [K, N] codes as stored
  *      (row stride N), s_w [N].  code_format must be S3R_CODES_F16
  *      (S3R_ERR_UNSUPPORTED otherwise); K and N multiples of 8 and X8, W8

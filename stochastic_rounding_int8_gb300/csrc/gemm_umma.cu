@@ -86,6 +86,11 @@ constexpr int kFwd = 4;
 // slice of W3 fill the 256 accumulator columns, and the epilogue writes
 // h1 = bf16(s_x s_w1 X W1), h3 = bf16(s_x s_w3 X W3) and a = bf16(silu(h1) h3).
 constexpr int kGate = 5;
+// Forward problems have unit block scales, so their accumulator is drained once
+// per kFwdUnit 128-wide blocks: the TMEM partial over 1024 products of codes is
+// below 1024 * 127^2 < 2^24 in magnitude, an exact integer in fp32; the
+// epilogue adds the units as int32 (the exact S32 sum) and converts once.
+constexpr int kFwdUnit = 8;
 
 // One contraction segment: scale(mt, nt, kb) = scale[mt*sm + nt*sn + kb*sk],
 // and for the activation gradient its correction terms.
@@ -353,7 +358,10 @@ template <int EPI>
 __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128], const float* cv, float* stage,
                                             int64_t row, int64_t c0, int lane) {
     if (EPI == kDX && P.f_row) {
-        // forward: (acc * s_x[row]) * s_w[col], one rounding each, columns past N scaled by 1
+        // forward: the exact int32 sum converted once, then (acc * s_x[row]) * s_w[col], one
+        // rounding each, columns past N scaled by 1
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = __int2float_rn(__float_as_int(acc[j]));
         const float fr = row < P.M ? __ldg(P.f_row + row) : 1.0f;
         const float2 fr2 = make_float2(fr, fr);
         const bool fvec = (reinterpret_cast<uintptr_t>(P.f_col) & 15u) == 0;
@@ -434,8 +442,9 @@ __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128],
 }
 
 // Gate epilogue of the forward (thread = row, acc[0..63] = h1 and acc[64..127]
-// = h3 accumulators of output columns c0 .. c0 + 63): rescale in fp32 as
-// (acc * s_x) * s_w and round to bf16 (nearest even).  With an `a` output the
+// = h3 accumulators of output columns c0 .. c0 + 63, as exact int32 sums):
+// convert to fp32 once, rescale in fp32 as (acc * s_x) * s_w and round to
+// bf16 (nearest even).  With an `a` output the
 // gate follows from those bf16 values: a = bf16((h1 * sigmoid(h1)) * h3).
 // Each thread writes its row's 64 columns as 16-byte pieces; N is a multiple
 // of 8, so a group of 8 columns lies wholly inside or outside.
@@ -444,8 +453,10 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-__device__ __forceinline__ void finish_gate(const Problem& P, const float (&acc)[128], int64_t row, int64_t c0) {
+__device__ __forceinline__ void finish_gate(const Problem& P, float (&acc)[128], int64_t row, int64_t c0) {
     if (row >= P.M) return;
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] = __int2float_rn(__float_as_int(acc[j]));   // the exact int32 sums
     const float fr = __ldg(P.f_row + row);
     const float2 fr2 = make_float2(fr, fr);
     uint16_t* const out_a = P.gate_out[2];
@@ -649,7 +660,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const bool b_mn = EPI == kMixed ? (P.kind != kDX) : MN;
                     const uint32_t idesc = a_mn ? idesc_f16(BM, BN, true, true)
                                                 : (b_mn ? idesc_f16(BM, BN, false, true) : idesc_f16(BM, BN, false, false));
-                    for (int kb = 0; kb < nkb; ++kb, ++gkb) {
+                    // one accumulator per drain unit: a 128-wide block, or kFwdUnit of them (forward)
+                    const int bpu = (EPI == kMixed && P.kind >= kFwd) ? kFwdUnit : 1;
+                    for (int kb = 0; kb < nkb; kb += bpu, ++gkb) {
                         const int buf = gkb & 1;
                         if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(gkb >> 1) & 1u) ^ 1u, abrt)) {
                             ok = false;
@@ -657,23 +670,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         tc_after();
                         const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
-                        for (int h = 0; h < 2 && ok; ++h, ++it) {
-                            const int s = it % STAGES;
-                            if (!mbar_wait(full0 + 8 * s, (uint32_t)(it / STAGES) & 1u, abrt)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_after();
-                            const uint32_t a0 = su32(sA + s * A_STAGE), b0 = su32(sB + s * B_STAGE);
+                        const int kend = kb + bpu < nkb ? kb + bpu : nkb;
+                        for (int b = kb; b < kend && ok; ++b) {
+                            for (int h = 0; h < 2 && ok; ++h, ++it) {
+                                const int s = it % STAGES;
+                                if (!mbar_wait(full0 + 8 * s, (uint32_t)(it / STAGES) & 1u, abrt)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_after();
+                                const uint32_t a0 = su32(sA + s * A_STAGE), b0 = su32(sB + s * B_STAGE);
 #pragma unroll
-                            for (int k16 = 0; k16 < BKS / 16; ++k16) {
-                                const uint64_t ad = a_mn ? sdesc(a0 + 2048 * k16, MN_ATOM_BYTES, 1024)
-                                                         : sdesc(a0 + 32 * k16, 16, 1024);
-                                const uint64_t bd = b_mn ? sdesc(b0 + 2048 * k16, MN_ATOM_BYTES, 1024)
-                                                         : sdesc(b0 + 32 * k16, 16, 1024);
-                                umma_f16(d_tmem, ad, bd, idesc, (h | k16) != 0);
+                                for (int k16 = 0; k16 < BKS / 16; ++k16) {
+                                    const uint64_t ad = a_mn ? sdesc(a0 + 2048 * k16, MN_ATOM_BYTES, 1024)
+                                                             : sdesc(a0 + 32 * k16, 16, 1024);
+                                    const uint64_t bd = b_mn ? sdesc(b0 + 2048 * k16, MN_ATOM_BYTES, 1024)
+                                                             : sdesc(b0 + 32 * k16, 16, 1024);
+                                    umma_f16(d_tmem, ad, bd, idesc, (b != kb || h != 0 || k16 != 0) ? 1u : 0u);
+                                }
+                                umma_commit(empty0 + 8 * s);
                             }
-                            umma_commit(empty0 + 8 * s);
                         }
                         if (!ok) break;
                         umma_commit(tfull0 + 8 * buf);
@@ -729,11 +745,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t lim = first ? P.seg[0].nt_limit : P.seg[1].nt_limit;
                 return nt < lim ? __ldg(base + off) : 0.0f;
             };
-            float sc_next = nkb > 0 ? scale_of(0) : 0.0f;
-            for (int kb = 0; kb < nkb; ++kb, ++gkb) {
+            // forward problems: one drain per kFwdUnit blocks, summed as int32 (see kFwdUnit)
+            const bool fwd = EPI == kMixed && P.kind >= kFwd;
+            const int nun = fwd ? (nkb + kFwdUnit - 1) / kFwdUnit : nkb;
+            float sc_next = (!fwd && nkb > 0) ? scale_of(0) : 0.0f;
+            for (int kb = 0; kb < nun; ++kb, ++gkb) {
                 const int buf = gkb & 1;
                 const float sc = sc_next;
-                if (kb + 1 < nkb) sc_next = scale_of(kb + 1);
+                if (!fwd && kb + 1 < nkb) sc_next = scale_of(kb + 1);
                 // warp-uniform outcome: the tcgen05.ld below needs the whole warp
                 const bool got =
                     __all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * buf, (uint32_t)(gkb >> 1) & 1u, abrt));
@@ -764,6 +783,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             __float2int_rn(__uint_as_float(r[u][j]));
                                 }
                         }
+                    } else if (fwd) {
+                        // exact integer partials: acc holds int32 bits
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                float& a = acc[16 * (c + u) + j];
+                                a = __int_as_float(__float_as_int(a) + __float2int_rn(__uint_as_float(r[u][j])));
+                            }
                     } else {
                         // acc = fma(scale, block, acc), two lanes per packed instruction
                         const float2 sc2 = make_float2(sc, sc);
