@@ -771,6 +771,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tmem_ld16(lane_addr + col_base + (uint32_t)(buf * BN + 16 * (c + u)) + (c + u >= 4 ? col_step : 0u),
                                   r[u]);
                     tmem_wait_ld();
+                    if (c == 4) {
+                        // every load of this accumulator has landed: hand it back to the MMA
+                        // issuer before the last folds
+                        tc_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                    }
                     if (EPI == kDump) {
                         if (row < P.M) {
 #pragma unroll
@@ -807,9 +814,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                     }
                 }
-                tc_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
             }
             if (EPI == kDump || !ok) continue;
             if (EPI == kMixed) {
