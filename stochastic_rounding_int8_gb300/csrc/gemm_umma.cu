@@ -76,8 +76,11 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + CV_BYTES + 1
 static_assert(SMEM_BYTES + 64 <= 232448, "shared memory budget of one sm_103a CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
-// Epilogue kinds; a kMixed launch takes each problem's kind from the problem.
-enum Epi { kDX = 0, kDW = 1, kDump = 2, kMixed = 3 };
+// Epilogue kinds; a kMixed launch takes each problem's kind (kDX or kDW) from
+// the problem, a kFwdE launch (forward problems only) too (kFwd or kGate).
+// The forward gets its own instantiation so that the backward kernels carry
+// none of its code.
+enum Epi { kDX = 0, kDW = 1, kDump = 2, kMixed = 3, kFwdE = 4 };
 // Problem kind of the INT8 forward (mixed launches only): A = X [M, K] K-major,
 // B = W [K, N] MN-major, unit block scales, epilogue (acc * s_x[m]) * s_w[n].
 constexpr int kFwd = 4;
@@ -354,10 +357,10 @@ __device__ __forceinline__ void seed_tile(const Problem& P, float (&acc)[128], f
 // staged 1/s_w[n]), then 16-column rounds through the warp's staging buffer
 // so that every global access is a 64-byte row segment (accumulate reads
 // included).
-template <int EPI>
+template <int EPI, bool FWD = false>
 __device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128], const float* cv, float* stage,
                                             int64_t row, int64_t c0, int lane) {
-    if (EPI == kDX && P.f_row) {
+    if (FWD) {
         // forward: the exact int32 sum converted once, then (acc * s_x[row]) * s_w[col], one
         // rounding each, columns past N scaled by 1
 #pragma unroll
@@ -603,13 +606,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
                     const int nkb = nkb0 + nkb1;   // 128-wide blocks of this tile
                     if (pi != last_pi) {
-                        for (int j = 0; j < (nkb1 || P.kind == kGate ? 4 : 2); ++j)
+                        for (int j = 0; j < (nkb1 || (EPI == kFwdE && P.kind == kGate) ? 4 : 2); ++j)
                             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)(mp + j)) : "memory");
                         last_pi = pi;
                     }
                     int tm, tn;
                     tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
-                    const bool gate = EPI == kMixed && P.kind == kGate;
+                    const bool gate = EPI == kFwdE && P.kind == kGate;
                     const int32_t m0 = tm * BM, n0 = tn * (gate ? BN / 2 : BN);
                     for (int sl = 0; sl < 2 * nkb; ++sl, ++it) {
                         const int s = it % STAGES;
@@ -626,8 +629,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const CUtensorMap* mB = mp + (second ? 3 : 1);
                         const int32_t k0 = (second ? sl - 2 * nkb0 : sl) * BKS;
                         const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
-                        const bool a_mn = EPI == kMixed ? P.kind == kDW : MN;
-                        const bool b_mn = EPI == kMixed ? (P.kind != kDX) : MN;
+                        // forward: A K-major, B MN-major as stored
+                        const bool a_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? false : MN);
+                        const bool b_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? true : MN);
                         if (!a_mn) {
                             tma_load(a_dst, mA, k0, m0, fb);
                         } else {
@@ -656,12 +660,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
                     const Problem& P = A.prob[problem_of(A, tile)];
                     const int nkb = (int)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128));
-                    const bool a_mn = EPI == kMixed ? P.kind == kDW : MN;
-                    const bool b_mn = EPI == kMixed ? (P.kind != kDX) : MN;
+                    const bool a_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? false : MN);
+                    const bool b_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? true : MN);
                     const uint32_t idesc = a_mn ? idesc_f16(BM, BN, true, true)
                                                 : (b_mn ? idesc_f16(BM, BN, false, true) : idesc_f16(BM, BN, false, false));
                     // one accumulator per drain unit: a 128-wide block, or kFwdUnit of them (forward)
-                    const int bpu = (EPI == kMixed && P.kind >= kFwd) ? kFwdUnit : 1;
+                    const int bpu = EPI == kFwdE ? kFwdUnit : 1;
                     for (int kb = 0; kb < nkb; kb += bpu, ++gkb) {
                         const int buf = gkb & 1;
                         if (!mbar_wait(tempty0 + 8 * buf, ((uint32_t)(gkb >> 1) & 1u) ^ 1u, abrt)) {
@@ -720,14 +724,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
             const int mt = tm, nt = tn * 2 + half;   // 128-wide tile indices
             const int64_t row = (int64_t)mt * BM + 32 * q + lane;
-            const bool gate = EPI == kMixed && P.kind == kGate;
+            const bool gate = EPI == kFwdE && P.kind == kGate;
             // gate: this half owns output columns c0 .. c0 + 63, accumulators
             // 0..63 = h1 (TMEM columns 64 half ..), 64..127 = h3 (128 + 64 half ..)
             const int64_t c0 = gate ? (int64_t)tn * 128 + 64 * half : (int64_t)nt * 128;
             const uint32_t col_base = (uint32_t)(gate ? 64 * half : 128 * half);
             const uint32_t col_step = gate ? 128u - 64u : 0u;   // extra offset of chunks 4..7
             float acc[128];
-            if (EPI == kMixed) {
+            if (EPI == kFwdE) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) acc[j] = 0.0f;   // int32 zero
+            } else if (EPI == kMixed) {
                 if (P.kind != kDW) seed_tile<kDX>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
                 else seed_tile<kDW>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
             } else if (EPI != kDump) {
@@ -739,14 +746,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool first = kb < nkb0;
                 const int64_t k = first ? kb : kb - nkb0;
                 const float* base = first ? P.seg[0].scale : P.seg[1].scale;
-                if (!base) return 1.0f;   // unit block scales (the forward)
                 const int64_t off = first ? mt * P.seg[0].sm + nt * P.seg[0].sn + k * P.seg[0].sk
                                           : mt * P.seg[1].sm + nt * P.seg[1].sn + k * P.seg[1].sk;
                 const int64_t lim = first ? P.seg[0].nt_limit : P.seg[1].nt_limit;
                 return nt < lim ? __ldg(base + off) : 0.0f;
             };
             // forward problems: one drain per kFwdUnit blocks, summed as int32 (see kFwdUnit)
-            const bool fwd = EPI == kMixed && P.kind >= kFwd;
+            constexpr bool fwd = EPI == kFwdE;
             const int nun = fwd ? (nkb + kFwdUnit - 1) / kFwdUnit : nkb;
             float sc_next = (!fwd && nkb > 0) ? scale_of(0) : 0.0f;
             for (int kb = 0; kb < nun; ++kb, ++gkb) {
@@ -771,13 +777,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tmem_ld16(lane_addr + col_base + (uint32_t)(buf * BN + 16 * (c + u)) + (c + u >= 4 ? col_step : 0u),
                                   r[u]);
                     tmem_wait_ld();
-                    if (c == 4) {
-                        // every load of this accumulator has landed: hand it back to the MMA
-                        // issuer before the last folds
-                        tc_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-                    }
                     if (EPI == kDump) {
                         if (row < P.M) {
 #pragma unroll
@@ -814,11 +813,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                     }
                 }
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
             }
             if (EPI == kDump || !ok) continue;
-            if (EPI == kMixed) {
+            if (EPI == kFwdE) {
                 if (gate) finish_gate(P, acc, row, c0);
-                else if (P.kind != kDW) finish_tile<kDX>(P, acc, cv, stage, row, c0, lane);
+                else finish_tile<kDX, true>(P, acc, cv, stage, row, c0, lane);
+            } else if (EPI == kMixed) {
+                if (P.kind != kDW) finish_tile<kDX>(P, acc, cv, stage, row, c0, lane);
                 else finish_tile<kDW>(P, acc, cv, stage, row, c0, lane);
             } else {
                 finish_tile<EPI>(P, acc, cv, stage, row, c0, lane);
@@ -1092,7 +1096,7 @@ int umma_fwd(const void* X, const float* s_x, const void* W, const float* s_w, c
     if (st) return st;
     A.nprob = 1;
     A.d_status = d_status;
-    return umma::launch<umma::kMixed, false>(maps, A, strip, stream);
+    return umma::launch<umma::kFwdE, false>(maps, A, strip, stream);
 }
 
 int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream) {
