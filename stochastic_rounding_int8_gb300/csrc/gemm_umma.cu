@@ -1,5 +1,8 @@
-// gemm_umma.cu -- the INT8 backward GEMMs on the 5th-generation tensor cores
-// (tcgen05, sm_103a), with the codes carried exactly in fp16.
+// gemm_umma.cu -- the INT8 GEMMs on the 5th-generation tensor cores (tcgen05,
+// sm_103a), with the codes carried exactly in fp16: the backward's dX and dW
+// (per-block promotion, correction in the epilogue) and, in a kernel
+// instantiation of their own, the forward's Y = X W and gate/up projections
+// (exact integer accumulation, see kFwdUnit).
 //
 // Paper: "Efficient Quantization Training with Stochastic Rounding via
 // Structured Subspace Randomness" §III-A: S8 x S8 GEMM with S32 accumulation,
