@@ -71,21 +71,47 @@ def test_workspace_sizes_are_host_only(L):
     assert L.s3r_ec_workspace_size(0, 5) == 0
 
 
-def test_ffn_args_struct_layout_matches_header():
-    """The ctypes mirror of struct s3r_ffn_args has one field per header field."""
+def _header_struct_fields(name):
     import re
     txt = open(s3r.HEADER).read()
-    body = re.search(r"struct s3r_ffn_args \{(.*?)\};", txt, re.S).group(1)
+    body = re.search(r"struct " + name + r" \{(.*?)\};", txt, re.S).group(1)
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = []
     for decl in body.split(";"):
         decl = decl.strip()
         if not decl:
             continue
-        names = decl.split()[-1] if "," not in decl else decl
         for part in re.split(r",", decl):
             fields.append(re.findall(r"\w+", part)[-1])
-    assert fields == [f for f, _ in s3r._FfnArgs._fields_]
+    return fields
+
+
+def test_ffn_args_struct_layout_matches_header():
+    """The ctypes mirrors of struct s3r_ffn_args and struct s3r_ffn_fwd_args
+    have one field per header field, in order."""
+    assert _header_struct_fields("s3r_ffn_args") == [f for f, _ in s3r._FfnArgs._fields_]
+    assert _header_struct_fields("s3r_ffn_fwd_args") == [f for f, _ in s3r._FfnFwdArgs._fields_]
+
+
+def test_forward_and_sr_bf16_arguments_checked_on_host(L):
+    """Host-side checks of the forward and SR-to-bf16 entries (fake,
+    never-dereferenced pointers; no launch happens)."""
+    import ctypes as C
+    fake = C.c_void_p(0x1000)
+    S3R_ERR_ARG, S3R_ERR_SHAPE, S3R_ERR_UNSUPPORTED = -1, -3, -8
+    # int8-carried codes are not taken by the forward
+    assert L.int8_gemm_fwd(fake, fake, fake, fake, s3r.CODES_S8, 8, 16, 16, fake, None, None) == S3R_ERR_UNSUPPORTED
+    assert L.int8_gemm_fwd(fake, fake, fake, fake, s3r.CODES_F16, -1, 16, 16, fake, None, None) == S3R_ERR_ARG
+    assert L.int8_gemm_fwd(fake, fake, fake, fake, s3r.CODES_F16, 0, 16, 16, fake, None, None) == 0
+    assert L.int8_gemm_fwd_swiglu(fake, fake, fake, fake, None, None, s3r.CODES_F16, 8, 16, 16, fake, fake, None,
+                                  None, None) == S3R_ERR_ARG   # W3 missing
+    assert L.swiglu_fwd_quantize(fake, fake, 4, 16, 8, None, fake, s3r.CODES_F16, fake, None, None) == S3R_ERR_SHAPE
+    assert L.swiglu_fwd_quantize(fake, fake, 4, 16, 16, None, fake, 7, fake, None, None) == S3R_ERR_ARG
+    assert L.s3r_sr_bf16(fake, 4, 16, 8, s3r.ROUND_S3R, 0, 0, fake, 16, None) == S3R_ERR_SHAPE
+    assert L.s3r_sr_bf16(fake, 4, 16, 16, s3r.ROUND_S3R_7BIT, 0, 0, fake, 16, None) == S3R_ERR_ARG
+    assert L.s3r_sr_bf16(fake, 0, 16, 16, s3r.ROUND_S3R, 0, 0, fake, 16, None) == 0
+    args = s3r._FfnFwdArgs(8, 16, 16, fake, fake, fake, fake, 1, s3r.CODES_S8)
+    assert L.ffn_forward(C.byref(args), None) == S3R_ERR_UNSUPPORTED
 
 
 def test_grouped_args_rejected_on_host():
