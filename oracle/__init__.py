@@ -67,6 +67,11 @@ def lib():
             L.orc_sr_bf16.restype = C.c_uint16
             L.orc_sr_bf16.argtypes = [C.c_float, C.c_uint32]
             L.orc_sr_bf16_matrix.restype = C.c_int
+            L.orc_sr_e4m3.restype = C.c_uint8
+            L.orc_sr_e4m3.argtypes = [C.c_float, C.c_uint32]
+            L.orc_rn_e4m3.restype = C.c_uint8
+            L.orc_rn_e4m3.argtypes = [C.c_float]
+            L.orc_sr_fp8_matrix.restype = C.c_int
             L.orc_inv127_rz.restype = C.c_float
             L.orc_inv127_rz.argtypes = [C.c_float]
             L.orc_sr_step.restype = C.c_float
@@ -420,6 +425,29 @@ def sr_bf16(X, mode=S3R, seed=0, tensor_id=0, t0=0) -> np.ndarray:
                                   C.c_uint32(tensor_id), _p(Y))
     if st != 0:
         raise ValueError(f"orc_sr_bf16_matrix status {st}")
+    return Y
+
+
+def sr_e4m3_scalar(y: float, v: int) -> int:
+    """e4m3 code of y rounded stochastically with the 16-bit threshold v."""
+    return int(lib().orc_sr_e4m3(float(y), int(v)))
+
+
+def rn_e4m3_scalar(y: float) -> int:
+    return int(lib().orc_rn_e4m3(float(y)))
+
+
+def sr_fp8(X, inv_scale=1.0, mode=S3R, seed=0, tensor_id=0, t0=0) -> np.ndarray:
+    """fp32 [T, N] -> e4m3 codes [T, N] of y = x * inv_scale (fp32): S3R (one
+    16-bit threshold per token), INDEP (one per element) or RTNE ([S3R] §II,
+    §III-B).  Row i is token t0 + i."""
+    X = _f32(X)
+    T, N = X.shape
+    Y = np.zeros((T, N), dtype=np.uint8)
+    st = lib().orc_sr_fp8_matrix(_p(X), _i64(T), _i64(N), _i64(N), _i64(t0), C.c_float(inv_scale), C.c_int(mode),
+                                 C.c_uint64(seed), C.c_uint32(tensor_id), _p(Y))
+    if st != 0:
+        raise ValueError(f"orc_sr_fp8_matrix status {st}")
     return Y
 
 

@@ -626,3 +626,81 @@ int orc_sr_bf16_matrix(const float* X, int64_t T, int64_t N, int64_t ldx, int64_
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Stochastic rounding of fp32 to FP8 e4m3 (1 sign, 4 exponent bits with     */
+/* bias 7, 3 mantissa bits; no infinity, largest finite 448, 0x7F NaN), the   */
+/* FP8 form of the same hardware conversion ([S3R] §II).  y = x * inv_scale   */
+/* in fp32 first (the caller's scale).  On the magnitude m = |y|: the e4m3    */
+/* spacing is s = 2^(e-3) for m in [2^e, 2^(e+1)), e >= -6, and 2^-9 below    */
+/* 2^-6; with k = floor(m / s) and p = m / s - k, the magnitude becomes       */
+/* (k + 1) s iff floor(p 2^16) > v for the 16-bit threshold v (probability    */
+/* floor(p 2^16) / 2^16, [SRB] "The probability formula" to 2^-16).  m >= 448 */
+/* (infinities included) saturates to 448; NaN gives 0x7F.  RTNE rounds to    */
+/* nearest even and saturates the same way.                                   */
+/* ------------------------------------------------------------------------- */
+static uint8_t orc_e4m3_round(float y, int mode, uint32_t v) {
+    uint32_t u;
+    memcpy(&u, &y, 4);
+    uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    uint32_t mag = u & 0x7FFFFFFFu;
+    if (mag > 0x7F800000u) return 0x7Fu;
+    double m = fabs((double)y);
+    if (m >= 448.0) return (uint8_t)(sign | 0x7Eu);
+    int e = 0;
+    if (m > 0.0) {
+        (void)frexp(m, &e);   /* m = f 2^e, f in [0.5, 1): the binade is 2^(e-1) */
+        e -= 1;
+    }
+    int sub = (m < ldexp(1.0, -6));
+    double s = sub ? ldexp(1.0, -9) : ldexp(1.0, e - 3);
+    double q = m / s;                          /* exact: s is a power of two */
+    int64_t k = (int64_t)floor(q);
+    double p = q - (double)k;                  /* exact */
+    if (mode == ORC_RTNE) {
+        if (p > 0.5 || (p == 0.5 && (k & 1))) k += 1;
+    } else {
+        uint32_t f16 = (uint32_t)floor(p * 65536.0);
+        if (f16 > (v & 0xFFFFu)) k += 1;
+    }
+    uint32_t bits;
+    if (sub) {
+        bits = (uint32_t)k;                    /* k <= 8: subnormal codes, 8 = 2^-6 */
+    } else {
+        bits = (uint32_t)(((e + 7) << 3) + (int)(k - 8));   /* k = 16 carries into the exponent */
+    }
+    if (bits > 0x7Eu) bits = 0x7Eu;            /* beyond 448: saturate */
+    return (uint8_t)(sign | bits);
+}
+
+uint8_t orc_sr_e4m3(float y, uint32_t v) { return orc_e4m3_round(y, ORC_S3R, v); }
+uint8_t orc_rn_e4m3(float y) { return orc_e4m3_round(y, ORC_RTNE, 0u); }
+
+/* X [T, N] fp32 (row stride ldx) -> Y [T, N] e4m3 codes (row stride N):
+ * y = x * inv_scale in fp32, then per mode as orc_sr_bf16_matrix (S3R: the
+ * token word's upper 16 bits; INDEP: element e's word; RTNE). Row i is token t0 + i. */
+int orc_sr_fp8_matrix(const float* X, int64_t T, int64_t N, int64_t ldx, int64_t t0, float inv_scale, int mode,
+                      uint64_t seed, uint32_t tensor_id, uint8_t* Y) {
+    if (T < 0 || N < 0 || ldx < N || t0 < 0) return ORC_ERR_ARG;
+    if (mode != ORC_S3R && mode != ORC_INDEP && mode != ORC_RTNE) return ORC_ERR_ARG;
+    uint32_t key[2] = {(uint32_t)seed, tensor_id};
+    for (int64_t i = 0; i < T; ++i) {
+        int64_t t = t0 + i;
+        uint32_t out[4];
+        uint32_t ctr[4] = {(uint32_t)t, (uint32_t)((uint64_t)t >> 32), 0u, 0u};
+        orc_philox4x32_10(ctr, key, out);
+        uint32_t v_tok = out[0] >> 16;
+        for (int64_t n = 0; n < N; ++n) {
+            float y = X[i * ldx + n] * inv_scale;
+            uint32_t v = v_tok;
+            if (mode == ORC_INDEP) {
+                uint64_t e = (uint64_t)t * (uint64_t)N + (uint64_t)n, c = e >> 2;
+                uint32_t ce[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u}, w[4];
+                orc_philox4x32_10(ce, key, w);
+                v = w[e & 3u] >> 16;
+            }
+            Y[i * N + n] = orc_e4m3_round(y, mode, v);
+        }
+    }
+    return ORC_OK;
+}
