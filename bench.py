@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn",
                                               "moe", "fwd", "fwd_gate", "fwd_gate_quantize", "fwd_down",
-                                              "sr_bf16"],
+                                              "sr_bf16", "sr_fp8"],
                     help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
     return ap.parse_args()
 
@@ -428,7 +428,13 @@ def time_sr_bf16(s3r, pk, steps=20, warmup=3):
         ms = _event_ms(lambda: s3r.s3r_sr_bf16(G, rm, seed=1, Y=Y), steps, warmup)
         gbs = 6.0 * Tq * Nq / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
-    del G, Y
+    # the same rounding to FP8 e4m3 after a scale (fp32 in, one byte out: 5 B per element)
+    Y8 = torch.empty((Tq, Nq), dtype=torch.uint8, device="cuda")
+    for name, rm in (("fp8_s3r", s3r.ROUND_S3R), ("fp8_indep_sr", s3r.ROUND_INDEP), ("fp8_rtne", s3r.ROUND_RTNE)):
+        ms = _event_ms(lambda: s3r.s3r_sr_fp8(G, 0.01, rm, seed=1, Y=Y8), steps, warmup)
+        gbs = 5.0 * Tq * Nq / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
+    del G, Y, Y8
     return out
 
 
@@ -656,10 +662,12 @@ def run_kernel_case(args):
                                                            with_gate=False)
         fns["fwd_gate_quantize"] = lambda: s3r.swiglu_fwd_quantize(o.h1, o.h3, keep_a=False, Q=o.A8, scale=o.s_a)
         fns["fwd_down"] = lambda: s3r.int8_gemm_fwd(o.A8, o.s_a, o.W2_8, o.s_w2, Y=fo.Y)
-    if args.kernel_case == "sr_bf16":
+    if args.kernel_case in ("sr_bf16", "sr_fp8"):
         Gb = (workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).float() * 1e3).cuda()
         Yb = torch.empty((16384, 8192), dtype=torch.bfloat16, device="cuda")
         fns["sr_bf16"] = lambda: s3r.s3r_sr_bf16(Gb, s3r.ROUND_S3R, seed=1, Y=Yb)
+        Y8b = torch.empty((16384, 8192), dtype=torch.uint8, device="cuda")
+        fns["sr_fp8"] = lambda: s3r.s3r_sr_fp8(Gb, 0.01, s3r.ROUND_S3R, seed=1, Y=Y8b)
     if args.kernel_case == "quantize_sweep":
         Gs = workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).cuda()
         qs = s3r.s3r_quantize(Gs, code_format=s3r.CODES_S8)

@@ -405,6 +405,23 @@ int s3r_sr_bf16(const float* X, int64_t T, int64_t N, int64_t ldx, int round_mod
                 void* Y, int64_t ldy, cudaStream_t stream);
 
 /*
+ * s3r_sr_fp8 -- the same rounding to FP8 e4m3 (1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits; no infinity, largest finite 448), after a scale:
+ *   y = x * inv_scale                 fp32, one rounding
+ *   e4m3 spacing s = 2^(e-3) for |y| in [2^e, 2^(e+1)), e >= -6, and 2^-9
+ *   below 2^-6; with k = floor(|y| / s) and p = |y| / s - k, the magnitude
+ *   becomes (k + 1) s iff floor(p 2^16) > v (S3R / INDEP, v as in
+ *   s3r_sr_bf16), or rounds to nearest even (RTNE).  The sign is kept;
+ *   |y| >= 448 (infinities included) gives +-448, NaN gives 0x7F.
+ * In : X [T, N] fp32 (row stride ldx).  Out: Y [T, N] e4m3 codes, one byte
+ * each (row stride ldy).  16-byte aligned X with ldx % 4 == 0 and 8-byte
+ * aligned Y with ldy % 8 == 0 take the vector path; other layouts are
+ * converted element by element (same results).
+ */
+int s3r_sr_fp8(const float* X, int64_t T, int64_t N, int64_t ldx, float inv_scale, int round_mode, uint64_t seed,
+               uint32_t tensor_id, void* Y, int64_t ldy, cudaStream_t stream);
+
+/*
  * ffn_forward -- the SwiGLU FFN block forward with INT8 GEMMs, the operands
  * of ffn_backward as its outputs:
  *   1. X8, s_x   = rtne_quantize(X, per row)

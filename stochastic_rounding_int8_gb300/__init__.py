@@ -75,6 +75,7 @@ _SIGS = {
     "swiglu_fwd_quantize": (_INT, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _INT, _VP, _VP, _VP]),
     "ffn_forward": (_INT, [_VP, _VP]),
     "s3r_sr_bf16": (_INT, [_VP, _I64, _I64, _I64, _INT, _U64, _U32, _VP, _I64, _VP]),
+    "s3r_sr_fp8": (_INT, [_VP, _I64, _I64, _I64, C.c_float, _INT, _U64, _U32, _VP, _I64, _VP]),
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
@@ -449,6 +450,19 @@ def s3r_sr_bf16(X, round_mode=ROUND_S3R, seed=0, tensor_id=0, Y=None, stream=Non
         Y = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
     _check(lib().s3r_sr_bf16(_ptr(X), T, N, X.stride(0), round_mode, seed, tensor_id, _ptr(Y), Y.stride(0),
                              _stream(stream)), "s3r_sr_bf16")
+    return Y
+
+
+def s3r_sr_fp8(X, inv_scale=1.0, round_mode=ROUND_S3R, seed=0, tensor_id=0, Y=None, stream=None):
+    """fp32 [T, N] -> e4m3 codes [T, N] (uint8) of X * inv_scale, stochastically
+    rounded with one 16-bit threshold per token (ROUND_S3R), per element
+    (ROUND_INDEP), or RTNE; saturating at +-448."""
+    assert X.dtype == torch.float32 and X.dim() == 2
+    T, N = X.shape
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.uint8, device=X.device)
+    _check(lib().s3r_sr_fp8(_ptr(X), T, N, X.stride(0), float(inv_scale), round_mode, seed, tensor_id, _ptr(Y),
+                            Y.stride(0), _stream(stream)), "s3r_sr_fp8")
     return Y
 
 

@@ -1,5 +1,5 @@
-// sr_bf16.cu -- stochastic rounding of fp32 to bf16 with S3R's shared
-// thresholds, on the hardware stochastic-rounding conversion.
+// sr_bf16.cu -- stochastic rounding of fp32 to bf16 and to FP8 e4m3 with
+// S3R's shared thresholds, on the hardware stochastic-rounding conversions.
 //
 // Paper: "Efficient Quantization Training with Stochastic Rounding via
 // Structured Subspace Randomness" §II (Blackwell converts to floating-point
@@ -14,8 +14,16 @@
 // v is the upper 16 bits of the token's Philox word (the INT8 quantizer's
 // 24-bit threshold, truncated), so all channels of a token share it.
 //
-// Streaming kernel: a block takes (row, 8192-column chunk) units; each thread
-// converts four groups of 8 values (two 16-byte loads, one 16-byte store).
+// cvt.rs.satfinite.e4m3x4.f32 d, {a, b, c, e}, rbits puts a in byte 3 ... e
+// in byte 0; b takes rbits[31:16] and e rbits[15:0] the same way (the e4m3
+// magnitude moves up one step iff floor(p 2^16) + r >= 2^16, p its position
+// between the two neighbours), while a and c take those 16 bits reversed.
+// One threshold per token therefore goes through lanes b and e only (a and
+// c carry zeros): two values per conversion.
+//
+// Streaming kernels: a block takes (row, 8192-column chunk) units; each
+// thread converts four groups of 8 values (two 16-byte loads, one 16- or
+// 8-byte store).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -32,6 +40,22 @@ __device__ __forceinline__ uint32_t cvt_rs_pair(float lo, float hi, uint32_t v_l
     const uint32_t rbits = ((0xFFFFu - v_hi) << 16) | (0xFFFFu - v_lo);
     uint32_t d;
     asm("cvt.rs.satfinite.bf16x2.f32 %0, %1, %2, %3;" : "=r"(d) : "f"(hi), "f"(lo), "r"(rbits));
+    return d;
+}
+
+// e4m3: lo -> byte 0 (lane e), hi -> byte 2 (lane b) of the result.
+__device__ __forceinline__ uint32_t cvt_rs_e4m3_pair(float lo, float hi, uint32_t v_lo, uint32_t v_hi) {
+    const uint32_t rbits = ((0xFFFFu - v_hi) << 16) | (0xFFFFu - v_lo);
+    uint32_t d;
+    asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=r"(d)
+        : "f"(0.0f), "f"(hi), "f"(0.0f), "f"(lo), "r"(rbits));
+    return d;
+}
+// e4m3 round to nearest even: lo -> byte 0, hi -> byte 1.
+__device__ __forceinline__ uint32_t rn_e4m3_pair(float lo, float hi) {
+    unsigned short d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
     return d;
 }
 
@@ -104,6 +128,53 @@ __global__ void __launch_bounds__(kSrThreads) sr_bf16_kernel(const float* X, int
     }
 }
 
+// Four e4m3 codes (values 4 p .. 4 p + 3 of the group) in one 32-bit word.
+template <int MODE>
+__device__ __forceinline__ uint32_t e4m3_quad(const float (&y)[8], const uint32_t (&v)[8], int p) {
+    if (MODE == kSrRTNE)
+        return rn_e4m3_pair(y[4 * p], y[4 * p + 1]) | (rn_e4m3_pair(y[4 * p + 2], y[4 * p + 3]) << 16);
+    const uint32_t d0 = cvt_rs_e4m3_pair(y[4 * p], y[4 * p + 1], v[4 * p], v[4 * p + 1]);
+    const uint32_t d1 = cvt_rs_e4m3_pair(y[4 * p + 2], y[4 * p + 3], v[4 * p + 2], v[4 * p + 3]);
+    return __byte_perm(d0, d1, 0x6420);   // bytes 0, 2 of d0, then bytes 0, 2 of d1
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kSrThreads) sr_fp8_kernel(const float* X, int64_t N, int64_t ldx, float inv_scale,
+                                                            uint8_t* Y, int64_t ldy, uint32_t seed_lo, uint32_t tid,
+                                                            int64_t units, int64_t upr, bool vec) {
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int64_t t = u / upr, c_base = (u - t * upr) * kSrChunk;
+        uint32_t vt = 0u;
+        if (MODE == kSrS3R) vt = philox4x32_10((uint32_t)t, (uint32_t)(t >> 32), 0u, 0u, seed_lo, tid).x >> 16;
+        const float* xr = X + t * ldx;
+        uint8_t* yr = Y + t * ldy;
+#pragma unroll
+        for (int k = 0; k < kSrGroups; ++k) {
+            const int64_t c = c_base + 8 * ((int64_t)threadIdx.x + kSrThreads * k);
+            if (c >= N) break;
+            uint32_t v[8];
+            if (MODE == kSrINDEP) element_v8((uint64_t)t * (uint64_t)N + (uint64_t)c, seed_lo, tid, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (MODE != kSrINDEP) v[i] = vt;
+            if (vec && c + 8 <= N) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(xr + c));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(xr + c + 4));
+                const float y[8] = {__fmul_rn(a.x, inv_scale), __fmul_rn(a.y, inv_scale), __fmul_rn(a.z, inv_scale),
+                                    __fmul_rn(a.w, inv_scale), __fmul_rn(b.x, inv_scale), __fmul_rn(b.y, inv_scale),
+                                    __fmul_rn(b.z, inv_scale), __fmul_rn(b.w, inv_scale)};
+                *reinterpret_cast<uint2*>(yr + c) = make_uint2(e4m3_quad<MODE>(y, v, 0), e4m3_quad<MODE>(y, v, 1));
+            } else {
+                for (int i = 0; i < 8 && c + i < N; ++i) {
+                    const float y = __fmul_rn(xr[c + i], inv_scale);
+                    const uint32_t w = MODE == kSrRTNE ? rn_e4m3_pair(y, 0.0f) : cvt_rs_e4m3_pair(y, 0.0f, v[i], 0u);
+                    yr[c + i] = (uint8_t)(w & 0xFFu);
+                }
+            }
+        }
+    }
+}
+
 int sm_count_sr() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -141,6 +212,37 @@ extern "C" int s3r_sr_bf16(const float* X, int64_t T, int64_t N, int64_t ldx, in
             break;
         default:
             sr_bf16_kernel<kSrRTNE><<<grid, kSrThreads, 0, stream>>>(X, N, ldx, y, ldy, s, tensor_id, units, upr, vec);
+    }
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
+
+extern "C" int s3r_sr_fp8(const float* X, int64_t T, int64_t N, int64_t ldx, float inv_scale, int round_mode,
+                          uint64_t seed, uint32_t tensor_id, void* Y, int64_t ldy, cudaStream_t stream) {
+    if (T < 0 || N < 0) return S3R_ERR_ARG;
+    if (round_mode != S3R_ROUND_S3R && round_mode != S3R_ROUND_INDEP && round_mode != S3R_ROUND_RTNE)
+        return S3R_ERR_ARG;
+    if (T == 0 || N == 0) return S3R_OK;
+    if (!X || !Y) return S3R_ERR_ARG;
+    if (ldx < N || ldy < N) return S3R_ERR_SHAPE;
+    const bool vec = s3r_aligned16(X) && ((uintptr_t)Y & 7u) == 0 && ldx % 4 == 0 && ldy % 8 == 0;
+    const int64_t upr = s3r_cdiv(N, kSrChunk), units = T * upr;
+    const int64_t cap = (int64_t)sm_count_sr() * 8;
+    const unsigned grid = (unsigned)(units < cap ? units : cap);
+    uint8_t* y = static_cast<uint8_t*>(Y);
+    const uint32_t s = (uint32_t)seed;
+    switch (round_mode) {
+        case S3R_ROUND_S3R:
+            sr_fp8_kernel<kSrS3R><<<grid, kSrThreads, 0, stream>>>(X, N, ldx, inv_scale, y, ldy, s, tensor_id, units,
+                                                                    upr, vec);
+            break;
+        case S3R_ROUND_INDEP:
+            sr_fp8_kernel<kSrINDEP><<<grid, kSrThreads, 0, stream>>>(X, N, ldx, inv_scale, y, ldy, s, tensor_id,
+                                                                      units, upr, vec);
+            break;
+        default:
+            sr_fp8_kernel<kSrRTNE><<<grid, kSrThreads, 0, stream>>>(X, N, ldx, inv_scale, y, ldy, s, tensor_id, units,
+                                                                     upr, vec);
     }
     S3R_CHECK_LAUNCH();
     return S3R_OK;

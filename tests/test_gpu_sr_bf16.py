@@ -1,5 +1,5 @@
-"""GPU parity: stochastic rounding of fp32 to bf16 with S3R's shared
-thresholds on the hardware conversion.
+"""GPU parity: stochastic rounding of fp32 to bf16, and to FP8 e4m3 after a
+scale, with S3R's shared thresholds on the hardware conversions.
 
 Source: "Efficient Quantization Training with Stochastic Rounding via
 Structured Subspace Randomness" -- §II (hardware SR to floating-point formats
@@ -79,3 +79,36 @@ def test_sr_bf16_rejects_bad_arguments(s3r):
         s3r.s3r_sr_bf16(X, s3r.ROUND_S3R_7BIT)
     with pytest.raises(AssertionError):
         s3r.s3r_sr_bf16(X.to(torch.bfloat16))
+
+
+# --- FP8 e4m3 ------------------------------------------------------------
+@pytest.mark.parametrize("T,N,pad", [(64, 8192, 0), (33, 8200, 0), (17, 1000, 4), (9, 77, 3), (3, 16385, 1)])
+@pytest.mark.parametrize("mode", ["s3r", "indep", "rtne"])
+@pytest.mark.parametrize("inv", [1.0, 0.37])
+def test_sr_fp8_matches_oracle(s3r, orc, T, N, pad, mode, inv):
+    """y = x * inv_scale, then e4m3 codes bit for bit: vector and element
+    paths, ragged widths and strides, subnormal to saturated magnitudes."""
+    rng = np.random.default_rng(T * 13 + N + pad)
+    mag = 10.0 ** rng.uniform(-4.0, 3.0, size=(T, N + pad))
+    full = (np.sign(rng.standard_normal((T, N + pad))) * mag).astype(np.float32)
+    X = full[:, :N]
+    sm, om = _MODES[mode]
+    Y = s3r.s3r_sr_fp8(torch.from_numpy(full).cuda()[:, :N], inv, getattr(s3r, sm), seed=3, tensor_id=9)
+    ref = orc.sr_fp8(np.ascontiguousarray(X), inv, getattr(orc, om), seed=3, tensor_id=9)
+    assert np.array_equal(Y.cpu().numpy(), ref)
+
+
+def test_sr_fp8_special_values_and_full_size_rows(s3r, orc):
+    X = np.array([[448.0, -448.0, 1e9, -np.inf, np.inf, 0.0, -0.0, 2.0 ** -12]] * 2, dtype=np.float32)
+    Y = s3r.s3r_sr_fp8(torch.from_numpy(X).cuda(), 1.0, s3r.ROUND_S3R, seed=1).cpu().numpy()
+    assert np.array_equal(Y, orc.sr_fp8(X, 1.0, orc.S3R, seed=1))
+    assert list(Y[0, :5]) == [0x7E, 0xFE, 0x7E, 0xFE, 0x7E]
+    nan = s3r.s3r_sr_fp8(torch.full((1, 8), float("nan"), device="cuda"))
+    assert torch.all((nan & 0x7F) == 0x7F)
+    # [16384, 8192] at the sweep size: sampled rows equal the oracle's window
+    T, N = 16384, 8192
+    G = workloads.quantize_sweep_input(T, N, seed=workloads.DATA_SEED + 3).float() * 1e3
+    Yf = s3r.s3r_sr_fp8(G.cuda(), 2.0, s3r.ROUND_S3R, seed=5, tensor_id=1).cpu().numpy()
+    for t in (0, 4097, T - 1):
+        ref = orc.sr_fp8(np.ascontiguousarray(G.numpy()[t:t + 1]), 2.0, orc.S3R, seed=5, tensor_id=1, t0=t)
+        assert np.array_equal(Yf[t:t + 1], ref)
