@@ -1,6 +1,15 @@
 /*
  * s3r.h -- C ABI of libs3r, a GB300 (sm_103a) implementation of the S3R /
- * S3R-EC INT8 backward pass of a linear or SwiGLU FFN layer.
+ * S3R-EC INT8 backward pass of a linear or SwiGLU FFN layer, the INT8
+ * forward of the same block, and stochastic rounding of fp32 to bf16 / FP8
+ * with the same shared thresholds.
+ *
+ * Entry points: quantizers (s3r_quantize, s3r_quantize_ex, indep_sr_quantize,
+ * rtne_quantize, swiglu_quantize, swiglu_quantize_ex, swiglu_fwd_quantize),
+ * correction factors (s3r_ec_correct, s3r_ec_correct_static), products
+ * (int8_gemm_dx, int8_gemm_dx_sum, int8_gemm_dw, int8_gemm_fwd,
+ * int8_gemm_fwd_swiglu), whole block (ffn_backward, ffn_forward), SR to
+ * floating point (s3r_sr_bf16, s3r_sr_fp8), status and debug helpers.
  *
  * Method: "Efficient Quantization Training with Stochastic Rounding via
  * Structured Subspace Randomness" (cited below as [S3R] with its sections:
