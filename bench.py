@@ -4,8 +4,10 @@
 One step = one pass of the whole backward hot path (quantize dY, correction
 factors, both INT8 GEMMs of W2, SwiGLU glue fused into the quantization of the
 gate/up gradients, their correction factors, both GEMMs of W1 and W3) over one
-batch: the d=2048, F=5632, T=8192 (4 x 2048 tokens) Llama-style block, inputs
-resident in HBM.  Prints ONE JSON line (rank 0).
+batch: the d=4096, F=14336, T=16384 (8 x 2048 tokens) Llama-style block (the
+shape of the paper's Table III row W7, the largest FFN block of the workloads),
+inputs resident in HBM.  The d=2048, F=5632, T=8192 block and the other
+workloads are timed as context.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
 
@@ -34,16 +36,23 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 METRIC = "FFN backward tokens/s, S3R-EC INT8 vs BF16, 1 GB300; quantize GB/s vs HBM peak"
-WORKLOAD = "swiglu_ffn_d2048_F5632_T8192"
+WORKLOAD = "swiglu_ffn_d4096_F14336_T16384"
+SMALL_BLOCK = "swiglu_ffn_d2048_F5632_T8192"
 CFG = workloads.WORKLOADS[WORKLOAD]
 T, D, F, S = CFG["T"], CFG["d"], CFG["F"], CFG["S"]
 L2_BYTES = 129 * 2 ** 20
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM launches of one
+# ffn_backward step of the timed block, per GEMM product, from one ncu capture of the step's
+# launch list on a GB300 (the command is in the design notes); keyed by the sha256 of the GEMM
+# source it was taken on, so that it is reported only while that kernel is unchanged.
+GEMM_TRAFFIC = {}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-context", action="store_true", help="skip the BF16 / baseline-mode context timings")
@@ -51,7 +60,9 @@ def parse():
     ap.add_argument("--kernel-case", choices=["gemm_dx", "gemm_dw", "quantize", "quantize_sweep", "swiglu", "ec", "ffn",
                                               "moe", "fwd", "fwd_gate", "fwd_gate_quantize", "fwd_down",
                                               "sr_bf16", "sr_fp8"],
-                    help="profiling helper: run one kernel of the benchmark's block --steps times, print a short line")
+                    help="profiling helper: run one kernel of a block --steps times, print a short line")
+    ap.add_argument("--block", choices=[WORKLOAD, SMALL_BLOCK], default=SMALL_BLOCK,
+                    help="--kernel-case: which FFN block (default: the smaller one, for ncu captures)")
     return ap.parse_args()
 
 
@@ -153,21 +164,41 @@ def peaks():
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def device_setup(s3r, rank, code_format=None):
-    inp = workloads.ffn_inputs(T, D, F, S, seed=workloads.DATA_SEED + 1 + 1000 * rank)
+class Block:
+    """One SwiGLU FFN block workload: its sizes and its seeded inputs."""
+
+    def __init__(self, name, data_seed):
+        w = workloads.WORKLOADS[name]
+        self.name = name
+        self.T, self.d, self.F, self.S = w["T"], w["d"], w["F"], w["S"]
+        self.data_seed = data_seed
+        self.flops_per_product = 2.0 * self.T * self.d * self.F   # each of the six GEMM products of a step
+
+    def inputs(self, rank=0):
+        return workloads.ffn_inputs(self.T, self.d, self.F, self.S, seed=self.data_seed + 1000 * rank)
+
+
+HEAD = Block(WORKLOAD, workloads.DATA_SEED + 2)
+SMALL = Block(SMALL_BLOCK, workloads.DATA_SEED + 1)
+
+
+def device_ops(s3r, inp, code_format=None):
     c = lambda t: t.cuda()
     cf = s3r.DEFAULT_CODES if code_format is None else code_format
     ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3),
                                    code_format=cf)
     torch.cuda.synchronize()
-    return inp, ops
+    return ops
 
 
-def time_ffn(s3r, ops, dY, steps, warmup, rm, ec, world, events=False):
-    """Device time of `steps` ffn_backward calls on resident inputs."""
-    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S, rm, ec, s3r.code_format_of(ops.X8)), dtype=torch.uint8,
+def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False):
+    """Device time of `steps` ffn_backward calls on resident inputs: total ms
+    between two events around the loop, launches counted by the library, and
+    (events=True) each step's per-step-boundary event times [steps, 8]."""
+    T, d, F, S = blk.T, blk.d, blk.F, blk.S
+    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, rm, ec, s3r.code_format_of(ops.X8)), dtype=torch.uint8,
                      device="cuda")
-    grads = s3r.alloc_ffn_grads(T, D, F)
+    grads = s3r.alloc_ffn_grads(T, d, F)
     st = s3r.new_status()
     for i in range(warmup):
         s3r.ffn_backward(ops, dY, S, rm, ec, seed=i, grads=grads, workspace=ws, status=st)
@@ -194,22 +225,24 @@ def time_ffn(s3r, ops, dY, steps, warmup, rm, ec, world, events=False):
     seg = None
     if events:
         seg = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(s3r.FFN_NUM_EVENTS - 1)] for evs in step_ev])
-    return max_over_ranks(ms, world), launches, seg, grads
+    del ws, grads
+    return max_over_ranks(ms, world), launches, seg
 
 
-def time_e2e(s3r, inp, ops, steps, warmup, world):
+def time_e2e(s3r, blk, inp, ops, steps, warmup, world):
     """Same step through the C ABI with HOST buffers: pinned host -> device
     copies of every input of the step, the backward, device -> host copies of
     all four gradients, inside the timed region."""
+    T, d, F, S = blk.T, blk.d, blk.F, blk.S
     host_in = {k: getattr(ops, k).cpu().pin_memory() for k in
                ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2", "h1", "h3")}
     host_in["dY"] = inp.dY.pin_memory()
     dev_in = {k: torch.empty_like(v, device="cuda") for k, v in host_in.items()}
     dops = s3r.FFNOperands(**{k: dev_in[k] for k in host_in if k != "dY"})
-    grads = s3r.alloc_ffn_grads(T, D, F)
+    grads = s3r.alloc_ffn_grads(T, d, F)
     host_out = {k: torch.empty(getattr(grads, k).shape, dtype=torch.float32).pin_memory()
                 for k in ("dX", "dW1", "dW3", "dW2")}
-    ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S, code_format=s3r.code_format_of(ops.X8)), dtype=torch.uint8,
+    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, code_format=s3r.code_format_of(ops.X8)), dtype=torch.uint8,
                      device="cuda")
     bi = sum(v.numel() * v.element_size() for v in host_in.values())
     bo = sum(v.numel() * v.element_size() for v in host_out.values())
@@ -233,6 +266,7 @@ def time_e2e(s3r, inp, ops, steps, warmup, world):
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     barrier(world)
+    del dev_in, dops, grads, ws, host_in, host_out
     return ms, bi, bo
 
 
@@ -252,16 +286,85 @@ def time_bf16_backward(inp, steps, warmup):
         dW3 = X.t() @ dh3
         return dX, dW1, dW2, dW3
 
+    return _event_ms(step, steps, warmup)
+
+
+def _event_ms(fn, steps, warmup):
     for _ in range(warmup):
-        step()
+        fn()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(steps):
-        step()
+        fn()
     t1.record()
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / steps
+
+
+def gemm_roofline(blk, seg, pk, pk_kind):
+    """The GEMM class of ffn_backward (dA + dW2 and dX1 + dX3 + dW1 + dW3, two
+    mixed tcgen05 launches carrying the six products of a step) from the step
+    events: algorithmic flops per product over the class's mean time per
+    product, against the measured dense bf16 peak (burst: the GEMMs are timed
+    in a step-long region at full clock, not in a seconds-long loop)."""
+    segm = seg.mean(0)
+    gemm_ms = float(segm[2] + segm[3] + segm[6] + segm[7])
+    achieved = blk.flops_per_product / (gemm_ms / 6 * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    return {"kernel": "umma_gemm_kernel (dA + dW2 and dX1 + dX3 + dW1 + dW3 as two mixed launches)",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_note": f"dense bf16 burst ({pk_kind}); the codes run on the tensor cores as fp16 (kind::f16, "
+                         f"the same nominal rate as bf16)",
+            "frac_of_sustained_peak": round(achieved / pk.get("bf16_tflops_sustained", peak), 4),
+            "flops_per_product": blk.flops_per_product, "products_per_step": 6,
+            "avg_us_per_product": round(gemm_ms / 6 * 1e3, 1)}
+
+
+def gemm_traffic():
+    """DRAM bytes per GEMM product from the recorded ncu capture, or None when
+    the GEMM source changed since it was taken."""
+    import hashlib
+    src = os.path.join(ROOT, "stochastic_rounding_int8_gb300", "csrc", "gemm_umma.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return GEMM_TRAFFIC.get(h)
+
+
+def block_line(s3r, blk, inp, ops, dY, steps, warmup, world, pk, pk_kind):
+    """Timed S3R-EC two-way steps of one block: throughput, mean and median step
+    time, the step split and the GEMM class's roofline."""
+    ms, launches, seg = time_ffn(s3r, blk, ops, dY, steps, warmup, s3r.ROUND_S3R, s3r.EC_TWO_WAY, world,
+                                 events=True)
+    per_step = seg.sum(1)
+    return {"tokens_s": world * blk.T * steps / (ms * 1e-3), "ms_per_step": ms / steps,
+            "ms_per_step_median": float(np.median(per_step)), "launches": launches,
+            "step_breakdown_ms": {n: round(float(v), 4) for n, v in zip(s3r.FFN_STEPS, seg.mean(0))},
+            "roofline": gemm_roofline(blk, seg, pk, pk_kind)}
+
+
+def mode_context(s3r, blk, ops, dY, inp, steps=8, warmup=2):
+    """The same block under the other rounding / correction modes, int8 code
+    storage (mma.sync path) and the BF16 cuBLAS backward."""
+    ctx = {}
+    for name, rm, ec in (("s3r_ec_dx_only", s3r.ROUND_S3R, s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE),
+                         ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE),
+                         # the paper's own variants: 7-bit thresholds, Phi_bcast, the dW-only correction
+                         ("s3r_7bit_ec_two_way", s3r.ROUND_S3R_7BIT, s3r.EC_TWO_WAY),
+                         ("s3r_bcast_ec_two_way", s3r.ROUND_BCAST, s3r.EC_TWO_WAY),
+                         ("s3r_ec_dw_only", s3r.ROUND_S3R, s3r.EC_DW_ONLY)):
+        m, _, _ = time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, 1)
+        ctx[name] = {"tokens_s": round(blk.T * steps / (m * 1e-3), 1), "ms": round(m / steps, 4)}
+    ops8 = device_ops(s3r, inp, s3r.CODES_S8)
+    m, _, _ = time_ffn(s3r, blk, ops8, dY, 3, 1, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1)
+    ctx["s3r_ec_two_way_int8_storage_mma_sync"] = {"tokens_s": round(blk.T * 3 / (m * 1e-3), 1), "ms": round(m / 3, 4)}
+    del ops8
+    bms = time_bf16_backward(inp, steps, warmup)
+    ctx["bf16_cublas_backward"] = {"tokens_s": round(blk.T / (bms * 1e-3), 1), "ms": round(bms, 4)}
+    return ctx
 
 
 def time_moe(s3r, steps=5, warmup=2):
@@ -307,16 +410,7 @@ def time_moe(s3r, steps=5, warmup=2):
     torch.cuda.synchronize()
     out["step_breakdown_ms"] = {n: round(ev[j].elapsed_time(ev[j + 1]), 4) for j, n in enumerate(s3r.FFN_STEPS)}
     for name, fn in (("s3r_ec_two_way_grouped", ours), ("bf16_cublas_per_expert", bf16)):
-        for _ in range(warmup):
-            fn()
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(steps):
-            fn()
-        t1.record()
-        torch.cuda.synchronize()
-        ms = t0.elapsed_time(t1) / steps
+        ms = _event_ms(fn, steps, warmup)
         out[name] = {"tokens_s": round(w["tokens"] / (ms * 1e-3), 1), "ms": round(ms, 4)}
     s3r.check_status(st)
     out["group_rows"] = [b - a for a, b in zip(offs[:-1], offs[1:])]
@@ -324,61 +418,12 @@ def time_moe(s3r, steps=5, warmup=2):
     return out
 
 
-def time_ffn_large(s3r, steps=5, warmup=2):
-    """Context: the larger SwiGLU block (d=4096, F=14336, T=16384 = 8 x 2048,
-    Table III's W7 shape): S3R-EC two-way, S3R-EC dX-only, S3R, independent SR
-    and the BF16 cuBLAS backward of the same block."""
-    w = workloads.WORKLOADS["swiglu_ffn_d4096_F14336_T16384"]
-    Tl, dl, Fl, Sl = w["T"], w["d"], w["F"], w["S"]
-    inp = workloads.ffn_inputs(Tl, dl, Fl, Sl, seed=workloads.DATA_SEED + 2)
-    c = lambda t: t.cuda()
-    ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
-    dY = inp.dY.cuda()
-    st = s3r.new_status()
-    out = {}
-    for name, rm, ec in (("s3r_ec_two_way", s3r.ROUND_S3R, s3r.EC_TWO_WAY), ("s3r_ec_dx_only", s3r.ROUND_S3R,
-                         s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE), ("indep_sr_int8", s3r.ROUND_INDEP,
-                         s3r.EC_NONE)):
-        ws = torch.empty(s3r.ffn_workspace_size(Tl, dl, Fl, Sl, rm, ec), dtype=torch.uint8, device="cuda")
-        grads = s3r.alloc_ffn_grads(Tl, dl, Fl)
-        for i in range(warmup):
-            s3r.ffn_backward(ops, dY, Sl, rm, ec, seed=i, grads=grads, workspace=ws, status=st)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for i in range(steps):
-            s3r.ffn_backward(ops, dY, Sl, rm, ec, seed=100 + i, grads=grads, workspace=ws, status=st)
-        t1.record()
-        torch.cuda.synchronize()
-        ms = t0.elapsed_time(t1) / steps
-        out[name] = {"tokens_s": round(Tl / (ms * 1e-3), 1), "ms": round(ms, 4),
-                     "gemm_tflops_if_all_gemm": round(12.0 * Tl * dl * Fl / (ms * 1e-3) / 1e12, 1)}
-        del ws, grads
-    s3r.check_status(st)
-    bms = time_bf16_backward(inp, steps, warmup)
-    out["bf16_cublas_backward"] = {"tokens_s": round(Tl / (bms * 1e-3), 1), "ms": round(bms, 4)}
-    out["s3r_ec_two_way_vs_bf16"] = round(bms / out["s3r_ec_two_way"]["ms"], 3)
-    out["s3r_ec_two_way_vs_indep_sr"] = round(out["indep_sr_int8"]["ms"] / out["s3r_ec_two_way"]["ms"], 3)
-    return out
-
-
-def _event_ms(fn, steps, warmup):
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        fn()
-    t1.record()
-    torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / steps
-
-
-def time_forward(s3r, inp, pk, steps=10, warmup=3):
+def time_forward(s3r, blk, inp, pk, steps=10, warmup=3):
     """Context: the block's INT8 forward (ffn_forward: RTNE X and weights, the
-    gate/up GEMM with the SwiGLU gate in its epilogue, RTNE a, the down GEMM),
-    its two GEMMs alone, and the BF16 cuBLAS forward of the same block."""
+    gate/up GEMM, the SwiGLU gate fused into the RTNE of a, the down GEMM),
+    its two GEMMs and the gate kernel alone, and the BF16 cuBLAS forward of the
+    same block."""
+    T, D, F = blk.T, blk.d, blk.F
     c = lambda t: t.cuda()
     X, W1, W3, W2 = c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2)
     st = s3r.new_status()
@@ -401,7 +446,7 @@ def time_forward(s3r, inp, pk, steps=10, warmup=3):
         return a @ W2
 
     bms = _event_ms(bf16, steps, warmup)
-    peak = pk.get("bf16_tflops")
+    peak = pk["bf16_tflops"]
     tf = lambda flops, t: round(flops / (t * 1e-3) / 1e12, 1)
     return {"ms": round(ms, 4), "tokens_s": round(T / (ms * 1e-3), 1), "tflops": tf(6.0 * T * D * F, ms),
             "gate_up_gemm": {"ms": round(gms, 4), "tflops": tf(4.0 * T * D * F, gms),
@@ -438,8 +483,8 @@ def time_sr_bf16(s3r, pk, steps=20, warmup=3):
     return out
 
 
-def time_quantize_sweep(s3r, steps=20):
-    """S3R / independent SR / RTNE quantizers on dY [16384, 8192] bf16 with 1% x100
+def time_quantize_sweep(s3r, pk, steps=20):
+    """S3R / independent SR / RTNE quantizers on dY [T, 8192] bf16 with 1% x100
     outliers; int8 codes (1 B) and fp16-carried codes (2 B)."""
     Tq, Nq = 16384, 8192
     G = workloads.quantize_sweep_input(Tq, Nq, seed=workloads.DATA_SEED + 3).cuda()
@@ -462,177 +507,153 @@ def time_quantize_sweep(s3r, steps=20):
                                                               seed=i, out=q8), 2 + 2 + 1 + part),
     }
     for name, (fn, bpe) in runs.items():
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for i in range(steps):
-            fn(i)
-        t1.record()
-        torch.cuda.synchronize()
-        ms = t0.elapsed_time(t1) / steps
-        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(bpe * Tq * Nq / (ms * 1e-3) / 1e9, 1),
-                     "alg_bytes_per_elem": round(bpe, 4)}
+        it = iter(range(10 ** 9))
+        ms = _event_ms(lambda: fn(next(it)), steps, 3)
+        gbs = bpe * Tq * Nq / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "alg_bytes_per_elem": round(bpe, 4),
+                     "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
     out["shape"] = [Tq, Nq]
     # the other row counts of the sweep, S3R with int8 codes
     for Tx in (4096, 65536):
         Gx = workloads.quantize_sweep_input(Tx, Nq, seed=workloads.DATA_SEED + 3).cuda()
         qx = s3r.s3r_quantize(Gx, code_format=S8)
-        for i in range(3):
-            s3r.s3r_quantize(Gx, seed=i, out=qx)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for i in range(steps):
-            s3r.s3r_quantize(Gx, seed=i, out=qx)
-        t1.record()
-        torch.cuda.synchronize()
-        ms = t0.elapsed_time(t1) / steps
-        out[f"s3r_T{Tx}"] = {"us": round(ms * 1e3, 2), "GB_s": round((3 + part) * Tx * Nq / (ms * 1e-3) / 1e9, 1),
-                             "alg_bytes_per_elem": round(3 + part, 4),
+        it = iter(range(10 ** 9))
+        ms = _event_ms(lambda: s3r.s3r_quantize(Gx, seed=next(it), out=qx), steps, 3)
+        gbs = (3 + part) * Tx * Nq / (ms * 1e-3) / 1e9
+        out[f"s3r_T{Tx}"] = {"us": round(ms * 1e3, 2), "GB_s": round(gbs, 1), "alg_bytes_per_elem": round(3 + part, 4),
+                             "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
                              "l2_note": "input 64 MB < L2: repeated calls partly hit L2" if Tx == 4096 else ""}
         del Gx, qx
     return out
 
 
-def cpu_baseline(tokens=128):
-    """The plain CPU oracle (single thread) on a bounded sample of the same
-    block: `tokens` tokens (one example) of the d=2048, F=5632 FFN."""
+def host_cpu():
+    """The host's logical core count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"^Model name:\s*(.+)$", out, re.M)
+        model = m.group(1).strip() if m else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            m = re.search(r"^model name\s*:\s*(.+)$", open("/proc/cpuinfo").read(), re.M)
+            model = m.group(1).strip() if m else None
+        except OSError:
+            pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model or "unknown"}
+
+
+def _oracle_block_sample(blk, tokens):
+    """The oracle's operands for `tokens` tokens (one example) of a block."""
     import oracle as orc
-    inp = workloads.ffn_inputs(tokens, D, F, tokens, seed=workloads.DATA_SEED + 1)
+    inp = workloads.ffn_inputs(tokens, blk.d, blk.F, tokens, seed=blk.data_seed)
     f = orc.from_torch_bf16
     ops = orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
     h1, h3, dY = f(inp.h1), f(inp.h3), f(inp.dY)
+    return lambda: orc.ffn_backward(ops, h1, h3, dY, tokens, mode=orc.S3R, ec_mode=orc.EC_TWO_WAY, seed=0)
+
+
+def cpu_baseline(blk, tokens=64):
+    """The plain CPU oracle (single thread, as it stands) on a bounded sample of
+    the timed block: `tokens` tokens (one example) of its backward."""
+    run = _oracle_block_sample(blk, tokens)
     t0 = time.perf_counter()
-    orc.ffn_backward(ops, h1, h3, dY, tokens, mode=orc.S3R, ec_mode=orc.EC_TWO_WAY, seed=0)
+    run()
     dt = time.perf_counter() - t0
     return {"value": round(tokens / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{tokens} tokens (one example) of the d=2048, F=5632 SwiGLU block, S3R-EC two-way, "
-                      f"{dt:.1f} s single-threaded"}
+            "sample": f"{tokens} tokens (one example) of the d={blk.d}, F={blk.F} SwiGLU block backward, S3R-EC "
+                      f"two-way, {dt:.1f} s on one thread of the host", **host_cpu()}
 
 
-def profiled_traffic(kernel: str):
-    """DRAM bytes per GEMM product of `kernel` from the committed ncu summary
-    of this workload, or None when the GEMM source changed since the capture."""
-    import hashlib
-    root = os.path.dirname(os.path.abspath(__file__))
-    try:
-        txt = open(os.path.join(root, "profiles", "ffn_d2048_F5632_T8192_launches.md")).read()
-        src = open(os.path.join(root, "stochastic_rounding_int8_gb300", "csrc", "gemm_umma.cu"), "rb").read()
-    except OSError:
-        return None
-    m = re.search(r"gemm_umma\.cu sha256: ([0-9a-f]{64})", txt)
-    t = re.search(rf"{re.escape(kernel)}=(\d+)", txt)
-    if not m or not t or m.group(1) != hashlib.sha256(src).hexdigest():
-        return None
-    return int(t.group(1))
+def config_of(blk, world):
+    return {"workload": blk.name, "T": blk.T, "d": blk.d, "F": blk.F, "examples": blk.T // blk.S, "seq": blk.S,
+            "rounding": "S3R Phi_2D", "ec": "two-way", "tile": 128,
+            "codes": "int8 values carried in fp16 (tcgen05 kind::f16, fp32 accumulate per 128-K block)",
+            "l2": "working set of a step several GB > 129 MB L2 (no flush needed)", "parallelism": f"replica x{world}"}
 
 
 def run_ours(args, world, rank, local):
     import stochastic_rounding_int8_gb300 as s3r
     s3r.lib()
     pk, pk_kind = peaks()
-    inp, ops = device_setup(s3r, rank)
+    blk = HEAD
+    inp = blk.inputs(rank)
+    ops = device_ops(s3r, inp)
     dY = inp.dY.cuda()
     clocks = Clocks(local)
     # main timed region: S3R-EC two-way, step events for the per-kernel roofline
     clocks.start()
-    ms, launches, seg, _ = time_ffn(s3r, ops, dY, args.steps, args.warmup, s3r.ROUND_S3R, s3r.EC_TWO_WAY, world,
-                                    events=True)
+    r = block_line(s3r, blk, inp, ops, dY, args.steps, args.warmup, world, pk, pk_kind)
     clk = clocks.stop()
-    ms_step = ms / args.steps
-    value = world * T * args.steps / (ms * 1e-3)
-    # per-step segments -> dominant kernel class
-    segm = seg.mean(0)
-    names = s3r.FFN_STEPS
-    # second field: GEMM products of 2*T*d*F flops per step; with fp16 codes dA + dW2 and
-    # dX1 + dX3 + dW1 + dW3 are one mixed launch each, so all six products form one class
-    classes = {"int8_gemm": (segm[2] + segm[3] + segm[6] + segm[7], 6),
-               "quantize (dY + SwiGLU-fused)": (segm[0] + segm[4], 2), "s3r_ec_correct": (segm[1] + segm[5], 3)}
-    dom = max(classes, key=lambda k: classes[k][0])
-    dom_ms, dom_n = classes[dom]
-    flops_per_launch = 2.0 * T * D * F
-    if dom.startswith("int8_gemm"):
-        achieved = flops_per_launch / (dom_ms / dom_n * 1e-3) / 1e12
-        peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
-        roof = {"kernel": "umma_gemm_kernel (int8_gemm_dx / int8_gemm_dw: dA + dW2 and dX1 + dX3 + dW1 + dW3 "
-                          "as two mixed launches)", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom),
-                "traffic_note": "DRAM read + write bytes per GEMM product from the committed ncu capture "
-                                "(profiles/ffn_d2048_F5632_T8192_launches.md); null once the GEMM source changed",
-                "peak_note": f"dense bf16 sustained ({pk_kind}); the s8 codes run on the tensor cores at the "
-                             f"16-bit rate or below on sm_103a",
-                "flops_per_product": flops_per_launch, "products_per_step": dom_n,
-                "avg_us_per_product": round(dom_ms / dom_n * 1e3, 1)}
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": None, "traffic": None}
-    steps_ms = {n: round(float(v), 4) for n, v in zip(names, segm)}
+    roof = r["roofline"]
+    roof["traffic"] = gemm_traffic()
+    roof["traffic_note"] = ("DRAM read + write bytes per GEMM product of this block from an ncu capture of the "
+                            "step's launch list; null when the GEMM source changed since")
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": round(r["tokens_s"], 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4),
+        "ms_per_step_median": round(r["ms_per_step_median"], 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "s8", "data": "synthetic (seeded; shapes/distributions of the paper's FFN "
-                                                  "block workload)",
-        "config": {"workload": WORKLOAD, "T": T, "d": D, "F": F, "examples": T // S, "seq": S,
-                   "rounding": "S3R Phi_2D", "ec": "two-way", "tile": 128,
-                   "codes": "int8 values carried in fp16 (tcgen05 kind::f16, fp32 accumulate per 128-K block)",
-                   "l2": "working set ~1 GB > 129 MB L2 (no flush needed)", "parallelism": f"replica x{world}"},
+                                                    "block workload)",
+        "config": config_of(blk, world),
         "clocks": clk,
-        "gpu_launches": int(launches),
+        "gpu_launches": int(r["launches"]),
         "roofline": roof,
-        "step_breakdown_ms": steps_ms,
+        "step_breakdown_ms": r["step_breakdown_ms"],
     }
     # e2e through the C ABI with host buffers
-    e2e_steps = max(3, min(args.steps, 20))
-    ems, bi, bo = time_e2e(s3r, inp, ops, e2e_steps, min(args.warmup, 3), world)
-    line["e2e"] = {"value": round(world * T * e2e_steps / (ems * 1e-3), 1), "unit": "tokens/s",
+    e2e_steps = max(3, min(args.steps, 10))
+    ems, bi, bo = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world)
+    line["e2e"] = {"value": round(world * blk.T * e2e_steps / (ems * 1e-3), 1), "unit": "tokens/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
     if not args.no_context and rank == 0:
-        ctx = {}
-        for name, rm, ec in (("s3r_ec_dx_only", s3r.ROUND_S3R, s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE),
-                             ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE),
-                             # the paper's own variants: 7-bit thresholds, Phi_bcast, the dW-only correction
-                             ("s3r_7bit_ec_two_way", s3r.ROUND_S3R_7BIT, s3r.EC_TWO_WAY),
-                             ("s3r_bcast_ec_two_way", s3r.ROUND_BCAST, s3r.EC_TWO_WAY),
-                             ("s3r_ec_dw_only", s3r.ROUND_S3R, s3r.EC_DW_ONLY)):
-            m, _, _, _ = time_ffn(s3r, ops, dY, 10, 2, rm, ec, 1)
-            ctx[name] = {"tokens_s": round(T * 10 / (m * 1e-3), 1), "ms": round(m / 10, 4)}
-        _, ops8 = device_setup(s3r, rank, s3r.CODES_S8)
-        m, _, _, _ = time_ffn(s3r, ops8, dY, 5, 1, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1)
-        ctx["s3r_ec_two_way_int8_storage_mma_sync"] = {"tokens_s": round(T * 5 / (m * 1e-3), 1), "ms": round(m / 5, 4)}
-        del ops8
-        bms = time_bf16_backward(inp, 10, 3)
-        ctx["bf16_cublas_backward"] = {"tokens_s": round(T / (bms * 1e-3), 1), "ms": round(bms, 4)}
-        ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / ms_step, 3)
-        ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / ms_step, 3)
-        fw = time_forward(s3r, inp, pk)
+        ctx = mode_context(s3r, blk, ops, dY, inp)
+        ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / r["ms_per_step"], 3)
+        ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / r["ms_per_step"], 3)
+        fw = time_forward(s3r, blk, inp, pk)
         ctx["forward_int8"] = fw
         # one INT8 training step of the block: this forward + the timed backward
         ctx["train_step_int8_vs_bf16"] = {
-            "int8_ms": round(fw["ms"] + ms_step, 4),
+            "int8_ms": round(fw["ms"] + r["ms_per_step"], 4),
             "bf16_ms": round(fw["bf16_cublas_forward"]["ms"] + ctx["bf16_cublas_backward"]["ms"], 4)}
-        qs = time_quantize_sweep(s3r)
-        for k in ("s3r", "s3r_f16_codes", "indep_sr_one_copy", "rtne", "s3r_7bit", "s3r_7bit_per_tensor",
-                  "s3r_T4096", "s3r_T65536"):
-            qs[k]["frac_hbm"] = round(qs[k]["GB_s"] / pk["hbm_gbs"], 3)
-        ctx["quantize_sweep"] = qs
+        del ops, dY, inp
+        torch.cuda.empty_cache()
+        # the smaller block as its own line (the round's earlier headline shape)
+        sb = SMALL
+        sinp = sb.inputs()
+        sops = device_ops(s3r, sinp)
+        sdY = sinp.dY.cuda()
+        rs = block_line(s3r, sb, sinp, sops, sdY, 20, 3, 1, pk, pk_kind)
+        sctx = {"tokens_s": round(rs["tokens_s"], 1), "ms_per_step": round(rs["ms_per_step"], 4),
+                "ms_per_step_median": round(rs["ms_per_step_median"], 4),
+                "step_breakdown_ms": rs["step_breakdown_ms"], "roofline": rs["roofline"]}
+        sctx.update(mode_context(s3r, sb, sops, sdY, sinp))
+        sctx["s3r_ec_two_way_vs_bf16"] = round(sctx["bf16_cublas_backward"]["ms"] / rs["ms_per_step"], 3)
+        sctx["s3r_ec_two_way_vs_indep_sr"] = round(sctx["indep_sr_int8"]["ms"] / rs["ms_per_step"], 3)
+        sctx["forward_int8"] = time_forward(s3r, sb, sinp, pk)
+        ctx[sb.name] = sctx
+        del sops, sdY, sinp
+        torch.cuda.empty_cache()
+        ctx["quantize_sweep"] = time_quantize_sweep(s3r, pk)
         ctx["sr_bf16_sweep"] = time_sr_bf16(s3r, pk)
         ctx["moe_e8_d4096_F1408_tok16384_top2"] = time_moe(s3r)
-        ctx["swiglu_ffn_d4096_F14336_T16384"] = time_ffn_large(s3r)
         line["context"] = ctx
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"] = cpu_baseline(blk)
     return line
 
 
 def run_kernel_case(args):
-    """Launch one kernel class of the benchmark's FFN block (the W2 / W1 linear
-    shapes) --steps times after --warmup, for ncu captures; prints its time."""
+    """Launch one kernel class of an FFN block (its W2 / W1 linear shapes)
+    --steps times after --warmup, for ncu captures; prints its time."""
     import stochastic_rounding_int8_gb300 as s3r
     s3r.lib()
-    inp, ops = device_setup(s3r, 0)
+    blk = HEAD if args.block == WORKLOAD else SMALL
+    T, D, F, S = blk.T, blk.d, blk.F, blk.S
+    inp = blk.inputs()
+    ops = device_ops(s3r, inp)
     dY = inp.dY.cuda()
     q2 = s3r.s3r_quantize(dY, ops.s_a, ops.s_w2)
     ec2 = s3r.s3r_ec_correct(q2, T, D, S, ops.W2_8, ops.A8, s3r.EC_TWO_WAY)
@@ -643,8 +664,11 @@ def run_kernel_case(args):
         "quantize": lambda: s3r.s3r_quantize(dY, ops.s_a, ops.s_w2, out=q2),
         "swiglu": lambda: s3r.swiglu_quantize(dA, ops.h1, ops.h3, ops.s_x, ops.s_w1, ops.s_w3),
         "ec": lambda: s3r.s3r_ec_correct(q2, T, D, S, ops.W2_8, ops.A8, s3r.EC_TWO_WAY),
-        "ffn": lambda: s3r.ffn_backward(ops, dY, S),
     }
+    if args.kernel_case == "ffn":
+        ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S), dtype=torch.uint8, device="cuda")
+        grads = s3r.alloc_ffn_grads(T, D, F)
+        fns["ffn"] = lambda: s3r.ffn_backward(ops, dY, S, grads=grads, workspace=ws)
     if args.kernel_case == "moe":
         w = workloads.WORKLOADS["moe_e8_d4096_F1408_tok16384_top2"]
         mi = workloads.moe_inputs(w["tokens"], w["topk"], w["experts"], w["d"], w["F"], seed=workloads.DATA_SEED + 5)
@@ -672,31 +696,18 @@ def run_kernel_case(args):
         Gs = workloads.quantize_sweep_input(16384, 8192, seed=workloads.DATA_SEED + 3).cuda()
         qs = s3r.s3r_quantize(Gs, code_format=s3r.CODES_S8)
         fns["quantize_sweep"] = lambda: s3r.s3r_quantize(Gs, out=qs)
-    fn = fns[args.kernel_case]
-    for _ in range(args.warmup):
-        fn()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(args.steps):
-        fn()
-    t1.record()
-    torch.cuda.synchronize()
-    print(json.dumps({"kernel_case": args.kernel_case, "ms_per_call": round(t0.elapsed_time(t1) / args.steps, 4)}))
+    ms = _event_ms(fns[args.kernel_case], args.steps, args.warmup)
+    print(json.dumps({"kernel_case": args.kernel_case, "block": blk.name, "ms_per_call": round(ms, 4)}))
 
 
 def run_reference(args, world, rank):
-    """The oracle as the reference arm: each step a bounded sample (8 tokens of
-    the d=2048, F=5632 block, ~1-3 s) on the host cores."""
+    """The oracle as the reference arm: each step a bounded sample (4 tokens of
+    the timed block, one example; a few seconds) on one host thread."""
     if rank != 0:
         return None
-    import oracle as orc
-    tok = 8
-    inp = workloads.ffn_inputs(tok, D, F, tok, seed=workloads.DATA_SEED + 1)
-    f = orc.from_torch_bf16
-    ops = orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
-    h1, h3, dY = f(inp.h1), f(inp.h3), f(inp.dY)
-    run = lambda: orc.ffn_backward(ops, h1, h3, dY, tok, mode=orc.S3R, ec_mode=orc.EC_TWO_WAY, seed=0)
+    blk = HEAD
+    tok = 4
+    run = _oracle_block_sample(blk, tok)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -704,13 +715,14 @@ def run_reference(args, world, rank):
         run()
     dt = time.perf_counter() - t0
     value = tok * args.steps / dt
-    sample = f"{tok} tokens (one example) of the d=2048, F=5632 SwiGLU block per step, single-threaded C oracle"
+    sample = (f"{tok} tokens (one example) of the d={blk.d}, F={blk.F} SwiGLU block backward per step, "
+              f"single-threaded C oracle")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": T, "d": D, "F": F, "rounding": "S3R Phi_2D", "ec": "two-way"},
+            "config": config_of(blk, world),
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_cpu()},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

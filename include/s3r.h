@@ -251,9 +251,9 @@ int s3r_ec_correct(const float* tok_err_part, const float* col_err_part, int64_t
 
 /*
  * s3r_ec_correct_static -- s3r_ec_correct without a caller workspace, for
- * callers that cannot allocate device memory when they run it (inside a
- * stream capture that must not allocate, from a host callback or a real-time
- * loop, or under a device memory budget fixed before the first step).  The
+ * callers that cannot allocate device memory when they run it (from a host
+ * callback or a real-time loop, where an allocation may block or fail, or
+ * under a device memory budget fixed before the first step).  The
  * paper has no counterpart: this is a deployment convenience of this library.
  * Arguments and results are those of s3r_ec_correct.  The two-way column sums
  * use a scratch array of 8 MiB that lives in the library (every GPU that loads
@@ -422,7 +422,9 @@ int s3r_sr_bf16(const float* X, int64_t T, int64_t N, int64_t ldx, int round_mod
  *   becomes (k + 1) s iff floor(p 2^16) > v (S3R / INDEP, v as in
  *   s3r_sr_bf16), or rounds to nearest even (RTNE).  The sign is kept;
  *   |y| >= 448 (infinities included) gives +-448, NaN gives 0x7F.
- * In : X [T, N] fp32 (row stride ldx).  Out: Y [T, N] e4m3 codes, one byte
+ * In : X [T, N] fp32 (row stride ldx); inv_scale finite and > 0 (S3R_ERR_ARG
+ * otherwise: zero, negative, NaN and infinite scales are rejected before any
+ * launch).  Out: Y [T, N] e4m3 codes, one byte
  * each (row stride ldy).  16-byte aligned X with ldx % 4 == 0 and 8-byte
  * aligned Y with ldy % 8 == 0 take the vector path; other layouts are
  * converted element by element (same results).
@@ -550,6 +552,27 @@ size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int ro
 size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, int64_t num_groups, int64_t d, int64_t F,
                                       int round_mode, int ec_mode, int code_format);
 int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
+
+/*
+ * s3r_ffn_workspace_offsets -- inspection hook: where ffn_backward keeps its
+ * intermediates inside the caller's workspace, so that a test can compare
+ * them with a reference after the call.  Writes to `out` (a HOST array of
+ * S3R_FFN_WS_VIEWS entries) the byte offsets, from a workspace base aligned
+ * to 256 bytes, of
+ *   [0] Q2 codes [T, d]   [1] Q2 tile scales [ceil(T/128), ceil(d/128)]
+ *   [2] Q1 codes [T, F]   [3] Q1 tile scales [ceil(T/128), ceil(F/128)]
+ *   [4] Q3 codes [T, F]   [5] Q3 tile scales
+ *   [6] dA [T, F] fp32 (the activation gradient of W2, input of the glue)
+ * codes in `code_format`, all row-major with the listed widths.  num_groups
+ * = 0: the dense block (T, S as in ffn_backward).  num_groups = E > 0: the
+ * block of expert `group` (0 <= group < E) under the HOST group_offsets of
+ * the grouped call (T and S ignored; the shapes use the group's row count).
+ * S3R_ERR_ARG for invalid sizes, an empty group or a NULL `out`.
+ * Host-only: launches nothing.
+ */
+#define S3R_FFN_WS_VIEWS 7
+int s3r_ffn_workspace_offsets(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int code_format,
+                              const int64_t* group_offsets, int64_t num_groups, int64_t group, size_t* out);
 
 /*
  * Test hooks: the exact int32 per-block partial products computed by the

@@ -291,6 +291,98 @@ def dw(X8, Q, delta, s_w, ec_mode, colmean, mu, xsum, p, S, krows, tile=(TILE, T
     return out
 
 
+def block_sums(A, B):
+    """Exact integer sums of one contraction block, sum_j A[i, j] B[j, k], for
+    code matrices A [m, <=128] and B [<=128, n] (|code| <= 127), through a
+    library matmul in float32: every product is an integer of magnitude
+    <= 127^2 and every partial sum of at most 128 of them stays below
+    128 * 127^2 < 2^24, so it is an integer float32 holds exactly whatever
+    the order of summation (and whatever the input rounding, since the codes
+    are exact in any format with 7 significant bits).  A guard checks the row
+    sums against integer arithmetic.  Returns a float64 torch tensor [m, n]."""
+    import torch
+    a = torch.from_numpy(np.ascontiguousarray(A, dtype=np.float32))
+    b = torch.from_numpy(np.ascontiguousarray(B, dtype=np.float32))
+    assert a.shape[1] == b.shape[0] <= TILE
+    out = (a @ b).double()
+    ref = np.asarray(A, dtype=np.int64) @ np.asarray(B, dtype=np.int64).sum(1)
+    assert np.array_equal(out.sum(1).numpy(), ref.astype(np.float64)), "block sums are not exact"
+    return out
+
+
+def dx_matmul(Q, delta, W8, s_x, ec_mode, eps, rowsum, v, S, rows=None, tile=(TILE, TILE), chunk=2048):
+    """The activation gradient of `dx` ([S3R] §III-A, §III-D) with each
+    128-wide block's integer sum taken by `block_sums` (a library matmul)
+    instead of nested loops.  The float64 promotion repeats `dx`'s order
+    operation for operation -- blocks in ascending order, acc += delta *
+    block, then eps * rowsum + v, then (acc - corr) / s_x, each a separately
+    rounded IEEE operation -- so the result equals `dx` bit for bit; only the
+    integer sums are formed differently."""
+    import torch
+    Q = np.asarray(Q, dtype=np.int8)
+    W8 = np.asarray(W8, dtype=np.int8)
+    T, N = Q.shape
+    K = W8.shape[0]
+    tr, tc = tile
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    nkb = -(-N // tc)
+    delta = torch.from_numpy(np.asarray(delta, dtype=np.float32).astype(np.float64))
+    out = np.zeros((rows.size, K), dtype=np.float64)
+    Wt = [np.ascontiguousarray(W8[:, kb * tc:(kb + 1) * tc].T) for kb in range(nkb)]
+    t64 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+    for c0 in range(0, rows.size, chunk):
+        r = rows[c0:c0 + chunk]
+        tile_row = torch.from_numpy(r // tr)
+        acc = torch.zeros((r.size, K), dtype=torch.float64)
+        for kb in range(nkb):
+            blk = block_sums(Q[r, kb * tc:(kb + 1) * tc], Wt[kb])
+            acc += delta[tile_row, kb][:, None] * blk
+        corr = torch.zeros_like(acc)
+        if ec_mode in (EC_DX_ONLY, EC_TWO_WAY):
+            corr = t64(eps)[r][:, None] * t64(rowsum)[None, :] + t64(v)[r // S]
+        elif ec_mode == EC_DX_TOKEN_ONLY:
+            corr = t64(eps)[r][:, None] * t64(rowsum)[None, :]
+        sx = torch.ones(r.size, dtype=torch.float64) if s_x is None else \
+            t64(np.asarray(s_x, dtype=np.float32)[r].astype(np.float64))
+        out[c0:c0 + r.size] = ((acc - corr) / sx[:, None]).numpy()
+    return out
+
+
+def dw_matmul(X8, Q, delta, s_w, ec_mode, colmean, mu, xsum, p, S, krows=None, tile=(TILE, TILE)):
+    """The weight gradient of `dw` ([S3R] §III-A, §III-D) with each 128-token
+    block's integer sum taken by `block_sums`; the float64 promotion and the
+    correction repeat `dw`'s order operation for operation (blocks in
+    ascending order, then the per-example terms in example order, then p),
+    so the result equals `dw` bit for bit."""
+    import torch
+    X8 = np.asarray(X8, dtype=np.int8)
+    Q = np.asarray(Q, dtype=np.int8)
+    T, K = X8.shape
+    N = Q.shape[1]
+    tr, tc = tile
+    krows = np.arange(K) if krows is None else np.asarray(krows, dtype=np.int64)
+    ntb = -(-T // tr)
+    delta = np.asarray(delta, dtype=np.float32).astype(np.float64)
+    acc = torch.zeros((krows.size, N), dtype=torch.float64)
+    Xk = X8[:, krows]
+    for tb in range(ntb):
+        blk = block_sums(np.ascontiguousarray(Xk[tb * tr:(tb + 1) * tr].T), Q[tb * tr:(tb + 1) * tr])
+        dcol = torch.from_numpy(np.repeat(delta[tb], tc)[:N])
+        acc += dcol[None, :] * blk
+    corr = torch.zeros_like(acc)
+    t64 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+    if ec_mode in (EC_TWO_WAY, EC_DW_ONLY):
+        B = T // S
+        xs, cm, m = t64(xsum), t64(colmean), t64(mu)
+        kr = torch.from_numpy(krows)
+        for b in range(B):
+            corr += xs[b, kr][:, None] * (cm[b] - m[b])[None, :]
+        corr += t64(p)[kr][:, None]
+    sw = torch.ones(N, dtype=torch.float64) if s_w is None else \
+        t64(np.asarray(s_w, dtype=np.float32).astype(np.float64))
+    return ((acc - corr) / sw[None, :]).numpy()
+
+
 def swiglu_bwd(dA, h1, h3):
     dA, h1, h3 = _f32(dA), _f32(h1), _f32(h3)
     dh1 = np.empty_like(dA)
@@ -326,12 +418,14 @@ RHS_ID_OFFSET = 0x100   # tensor-id offset of the second (dW) copy under indepen
 
 
 def linear_backward(G, X8, s_x, W8, s_w, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0, tensor_id=0,
-                    rows=None, krows=None, tile=(TILE, TILE)) -> LinearBackward:
+                    rows=None, krows=None, tile=(TILE, TILE), matmul=False) -> LinearBackward:
     """Backward of Y = X W given the saved forward operands.
 
     G: float32 [T, N] upstream gradient (exact widening of bf16).
     X8 [T, K] int8 with s_x [T]; W8 [K, N] int8 with s_w [N].
     rows / krows: which rows of dX / dW to produce (default: all).
+    matmul: form the products' integer block sums with a library matmul
+    (dx_matmul / dw_matmul, equal bit for bit) instead of nested loops.
     """
     G = _f32(G)
     T, N = G.shape
@@ -349,10 +443,11 @@ def linear_backward(G, X8, s_x, W8, s_w, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0
         out.rowsum, out.v, out.xsum, out.p = ec_factors(out.eps, out.colmean, out.mu, S, W8,
                                                         X8 if ec_mode in (EC_TWO_WAY, EC_DW_ONLY) else None)
     em = ec_mode if use_ec else EC_NONE
-    out.dX = dx(Q, delta, W8, s_x, em, out.eps, out.rowsum, out.v, S, rows, tile)
+    fdx, fdw = (dx_matmul, dw_matmul) if matmul else (dx, dw)
+    out.dX = fdx(Q, delta, W8, s_x, em, out.eps, out.rowsum, out.v, S, rows, tile)
     Qw = out.Q_rhs if mode == INDEP else Q
     dw_delta = out.delta_rhs if mode == INDEP else delta
-    out.dW = dw(X8, Qw, dw_delta, s_w, em, out.colmean, out.mu, out.xsum, out.p, S, krows, tile)
+    out.dW = fdw(X8, Qw, dw_delta, s_w, em, out.colmean, out.mu, out.xsum, out.p, S, krows, tile)
     return out
 
 
@@ -509,12 +604,13 @@ class FFNBackward:
 
 
 def ffn_backward(ops: FFNForwardOperands, h1, h3, dY, S, mode=S3R, ec_mode=EC_TWO_WAY, seed=0,
-                 rows=None, krows_d=None, krows_f=None, tid_base=0) -> FFNBackward:
+                 rows=None, krows_d=None, krows_f=None, tid_base=0, matmul=False) -> FFNBackward:
     """SwiGLU FFN block backward: W2 linear, then the SwiGLU glue, then W1 and
     W3 (dX = dX1 + dX3).  dA is needed for every token (the glue feeds the
     second quantization), so the W2 activation gradient is computed in full
     and rounded to fp32 before the glue, the precision the kernels hand on.
-    The three linears use tensor ids tid_base + (0, 1, 2)."""
+    The three linears use tensor ids tid_base + (0, 1, 2).  matmul: see
+    linear_backward (the same results, fast enough for full-size blocks)."""
     T = dY.shape[0]
     F = ops.A8.shape[1]
     d = ops.X8.shape[1]
@@ -522,13 +618,13 @@ def ffn_backward(ops: FFNForwardOperands, h1, h3, dY, S, mode=S3R, ec_mode=EC_TW
     krows_d = np.arange(d) if krows_d is None else np.asarray(krows_d)
     krows_f = np.arange(F) if krows_f is None else np.asarray(krows_f)
     w2 = linear_backward(dY, ops.A8, ops.s_a, ops.W2_8, ops.s_w2, S, mode, ec_mode, seed, tid_base + TID_W2,
-                         rows=np.arange(T), krows=krows_f)
+                         rows=np.arange(T), krows=krows_f, matmul=matmul)
     dA = w2.dX.astype(np.float32)
     dh1, dh3 = swiglu_bwd(dA, h1, h3)
     w1 = linear_backward(dh1, ops.X8, ops.s_x, ops.W1_8, ops.s_w1, S, mode, ec_mode, seed, tid_base + TID_W1,
-                         rows=rows, krows=krows_d)
+                         rows=rows, krows=krows_d, matmul=matmul)
     w3 = linear_backward(dh3, ops.X8, ops.s_x, ops.W3_8, ops.s_w3, S, mode, ec_mode, seed, tid_base + TID_W3,
-                         rows=rows, krows=krows_d)
+                         rows=rows, krows=krows_d, matmul=matmul)
     return FFNBackward(w2=w2, w1=w1, w3=w3, dA=dA, dh1=dh1, dh3=dh3,
                        dX=w1.dX + w3.dX, dW1=w1.dW, dW2=w2.dW, dW3=w3.dW)
 
@@ -579,7 +675,7 @@ class MoEBackward:
 
 
 def moe_ffn_backward(ops: MoEForwardOperands, h1, h3, dY, offsets, mode=S3R, ec_mode=EC_TWO_WAY,
-                     seed=0) -> MoEBackward:
+                     seed=0, matmul=False) -> MoEBackward:
     """Grouped SwiGLU FFN backward over expert-sorted routed rows ([S3R] §IV,
     MoE models): expert e owns rows offsets[e] .. offsets[e+1] and runs the
     whole block backward on them as one example, with its own weights; tiles
@@ -597,7 +693,7 @@ def moe_ffn_backward(ops: MoEForwardOperands, h1, h3, dY, offsets, mode=S3R, ec_
             per.append(None)
             continue
         b = ffn_backward(ops.expert(e, r0, r1), h1[r0:r1], h3[r0:r1], dY[r0:r1], r1 - r0, mode, ec_mode, seed,
-                         tid_base=MOE_TID_STRIDE * e)
+                         tid_base=MOE_TID_STRIDE * e, matmul=matmul)
         dX[r0:r1] = b.dX
         dW1[e], dW3[e], dW2[e] = b.dW1, b.dW3, b.dW2
         per.append(b)

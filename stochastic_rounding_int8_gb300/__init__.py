@@ -79,6 +79,7 @@ _SIGS = {
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
+    "s3r_ffn_workspace_offsets": (_INT, [_I64, _I64, _I64, _I64, _INT, _INT, _VP, _I64, _I64, _VP]),
     "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP]),
     "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
 }
@@ -648,3 +649,38 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
         args.step_events = C.cast(handles, C.POINTER(C.c_void_p))
     _check(lib().ffn_backward(C.byref(args), _stream(stream)), "ffn_backward")
     return grads
+
+
+FFN_WS_VIEWS = ("Q2", "scale2", "Q1", "scale1", "Q3", "scale3", "dA")
+
+
+def ffn_workspace_views(workspace, T, d, F, S, round_mode=ROUND_S3R, code_format=DEFAULT_CODES, group_offsets=None,
+                        group=0) -> dict:
+    """Views into an ffn_backward workspace (after the call): the codes and tile
+    scales of the three quantized gradients and dA, as laid out by the library
+    (s3r_ffn_workspace_offsets).  Grouped mode: the block of expert `group`."""
+    assert workspace.dtype == torch.uint8 and workspace.data_ptr() % 256 == 0
+    out = (C.c_size_t * 7)()
+    if group_offsets is not None:
+        offs = [int(o) for o in group_offsets]
+        arr = (C.c_int64 * len(offs))(*offs)
+        T = offs[group + 1] - offs[group]
+        S = T
+        _check(lib().s3r_ffn_workspace_offsets(0, d, F, 0, round_mode, code_format, C.cast(arr, _VP), len(offs) - 1,
+                                               group, C.cast(out, _VP)), "s3r_ffn_workspace_offsets")
+    else:
+        _check(lib().s3r_ffn_workspace_offsets(T, d, F, S, round_mode, code_format, None, 0, 0, C.cast(out, _VP)),
+               "s3r_ffn_workspace_offsets")
+    cdt = _CODE_DTYPE[code_format]
+    shapes = {"Q2": ((T, d), cdt), "scale2": ((_cdiv(T, TILE), _cdiv(d, TILE)), torch.float32),
+              "Q1": ((T, F), cdt), "scale1": ((_cdiv(T, TILE), _cdiv(F, TILE)), torch.float32),
+              "Q3": ((T, F), cdt), "scale3": ((_cdiv(T, TILE), _cdiv(F, TILE)), torch.float32),
+              "dA": ((T, F), torch.float32)}
+    views = {}
+    for i, name in enumerate(FFN_WS_VIEWS):
+        shape, dt = shapes[name]
+        nbytes = shape[0] * shape[1] * torch.empty(0, dtype=dt).element_size()
+        off = int(out[i])
+        assert off + nbytes <= workspace.numel(), name
+        views[name] = workspace[off:off + nbytes].view(dt).view(shape)
+    return views

@@ -248,6 +248,12 @@ __device__ __forceinline__ void set_status(int* d_status, int code) {
 void s3r_count_launch();
 void s3r_record_error(const char* where, const char* what);
 int s3r_cuda_fail(const char* where, cudaError_t err);
+// Streaming multiprocessors of the current device (looked up once per device).
+int s3r_sm_count();
+// Raises the dynamic shared-memory limit of kernel `func` to `bytes` on the
+// current device, once per (kernel, device) pair (the attribute is per
+// device); thread-safe.  Returns S3R_OK or S3R_ERR_CUDA (described under `what`).
+int s3r_kernel_smem(const void* func, int bytes, const char* what);
 
 // Grouped tcgen05 GEMMs on fp16-carried codes (gemm_umma.cu): up to 24
 // problems in one persistent launch, each computed exactly as a

@@ -1009,31 +1009,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 ec_encode_fn() {
     return fn;
 }
 
-static int ec_sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            (void)cudaGetLastError();
-            n = 148;
-        }
-    }
-    return n;
-}
+static int ec_sm_count() { return s3r_sm_count(); }
 
 template <int NJ, int BCH>
 static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, size_t smem, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(ec_stream_kernel<NJ, BCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(kEsStages * kEsStageBytes + 128 + 128 + kMaxJobs * kEsMaxB * 4));
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return s3r_cuda_fail("ec stream: cudaFuncSetAttribute", e);
-        }
-        attr = true;
-    }
+    const int st = s3r_kernel_smem((const void*)ec_stream_kernel<NJ, BCH>,
+                                   (int)(kEsStages * kEsStageBytes + 128 + 128 + kMaxJobs * kEsMaxB * 4),
+                                   "ec stream: cudaFuncSetAttribute");
+    if (st) return st;
     int64_t grid = std::min<int64_t>(S.n_items, ec_sm_count());
     if (!S.done) {
         ec_stream_kernel<NJ, BCH><<<(unsigned)grid, 256, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
@@ -1175,15 +1158,7 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
     const size_t gsm = gemv_smem_bytes(slab, B);
     vec_w = vec_w && gsm <= 200 * 1024;
     // every warp holds at most kGemvPairs row pairs: one CTA per SM gives sms * kGemvWarps warps per launch
-    int gsms = 148;
-    {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&gsms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            (void)cudaGetLastError();
-            gsms = 148;
-        }
-    }
+    const int gsms = s3r_sm_count();
     const int64_t per_job = std::max<int64_t>(1, gsms / nj);
     vec_w = vec_w && s3r_cdiv(K, kGemvRows) <= per_job * kGemvWarps * kGemvPairs;
     const bool vec_x = K % 8 == 0 && s3r_aligned16(X8);
@@ -1242,16 +1217,8 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
         const int64_t per = std::min<int64_t>(need, per_job);
         G.ctas0 = (int)per;
         G.ctas1 = nj > 1 ? (int)per : 0;
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(ec_gemv_kernel<CodeT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 200 * 1024);
-            if (e != cudaSuccess) {
-                (void)cudaGetLastError();
-                return s3r_cuda_fail("ec gemv: cudaFuncSetAttribute", e);
-            }
-            attr = true;
-        }
+        const int st = s3r_kernel_smem((const void*)ec_gemv_kernel<CodeT>, 200 * 1024, "ec gemv: cudaFuncSetAttribute");
+        if (st) return st;
         ec_gemv_kernel<CodeT><<<(unsigned)(per * nj), kGemvThreads, gsm, stream>>>(G);
         S3R_CHECK_LAUNCH();
     } else {
@@ -1365,8 +1332,7 @@ int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, 
 // Allocation-free variant of s3r_ec_correct.
 //
 // Some callers cannot allocate device memory at the moment they run the
-// backward: code that must not call cudaMalloc while a stream is being
-// captured, code running from a host callback or a real-time loop where an
+// backward: code running from a host callback or a real-time loop, where an
 // allocation would block or fail, or deployments that fix their whole device
 // memory budget before the first step.  For them the two-way column sums use a
 // scratch array that lives in this library's module, not a caller workspace.

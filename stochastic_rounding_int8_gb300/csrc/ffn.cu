@@ -7,6 +7,9 @@
 // synchronization; every intermediate lives in the caller's workspace.
 #include <algorithm>
 #include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -28,6 +31,45 @@ int s3r_cuda_fail(const char* where, cudaError_t err) {
     return S3R_ERR_CUDA;
 }
 extern "C" const char* s3r_last_error(void) { return g_last_error; }
+
+static std::mutex g_setup_mutex;
+
+int s3r_sm_count() {
+    constexpr int kMaxDev = 64;
+    static int counts[kMaxDev] = {};
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (dev < kMaxDev && counts[dev]) return counts[dev];
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    if (dev < kMaxDev) counts[dev] = n;
+    return n;
+}
+
+int s3r_kernel_smem(const void* func, int bytes, const char* what) {
+    static std::set<std::pair<const void*, int>> done;   // (kernel, device) pairs already raised
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail(what, e);
+    }
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (done.count({func, dev})) return S3R_OK;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s3r_cuda_fail(what, e);
+    }
+    done.insert({func, dev});
+    return S3R_OK;
+}
 
 namespace {
 
@@ -394,6 +436,34 @@ extern "C" size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, i
     for (int64_t e = 0; e < num_groups; ++e)
         if (group_offsets[e + 1] < group_offsets[e]) return 0;
     return grouped_bytes(group_offsets, num_groups, d, F, round_mode, code_format);
+}
+
+extern "C" int s3r_ffn_workspace_offsets(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode,
+                                         int code_format, const int64_t* group_offsets, int64_t num_groups,
+                                         int64_t group, size_t* out) {
+    if (!out || d <= 0 || F <= 0) return S3R_ERR_ARG;
+    if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
+    uintptr_t base = 0;   // offsets from a 256-byte aligned workspace base
+    if (num_groups > 0) {
+        if (!group_offsets || group < 0 || group >= num_groups || group_offsets[0] != 0) return S3R_ERR_ARG;
+        for (int64_t e = 0; e < num_groups; ++e)
+            if (group_offsets[e + 1] < group_offsets[e]) return S3R_ERR_ARG;
+        // the same walk as ffn_backward's grouped carve: one block per non-empty expert
+        for (int64_t e = 0; e < group; ++e) {
+            const int64_t Tg = group_offsets[e + 1] - group_offsets[e];
+            if (Tg == 0) continue;
+            base = (base + 255) & ~(uintptr_t)255;
+            base += layout(nullptr, 0, Tg, d, F, Tg, round_mode, code_format).total;
+        }
+        base = (base + 255) & ~(uintptr_t)255;
+        T = group_offsets[group + 1] - group_offsets[group];
+        S = T;
+    }
+    if (T <= 0 || S <= 0 || T % S != 0) return S3R_ERR_ARG;
+    const FfnLayout Lo = layout(nullptr, 0, T, d, F, S, round_mode, code_format);
+    const void* views[S3R_FFN_WS_VIEWS] = {Lo.w2.Q, Lo.w2.scale, Lo.w1.Q, Lo.w1.scale, Lo.w3.Q, Lo.w3.scale, Lo.dA};
+    for (int i = 0; i < S3R_FFN_WS_VIEWS; ++i) out[i] = (size_t)(base + reinterpret_cast<uintptr_t>(views[i]));
+    return S3R_OK;
 }
 
 extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {

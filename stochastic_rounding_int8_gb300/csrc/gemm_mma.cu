@@ -246,21 +246,12 @@ int umma_gemm_dw(const void* X, const void* Q, const float* tile_scale, int64_t 
                  const float* s_w, int ec_mode, const float* colmean, const float* mu, const int32_t* xsum,
                  const float* p, int64_t S, float* dW, int32_t* dump, int* d_status, cudaStream_t stream);
 
-static bool gemm_smem_ready = false;
-
 static int ensure_gemm_smem() {
-    if (gemm_smem_ready) return S3R_OK;
-    if (cudaFuncSetAttribute(gemm_tn_s8_kernel<kEpiDX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tn_s8_kernel<kEpiDW>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tn_s8_kernel<kEpiDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
-            cudaSuccess) {
-        cudaError_t e = cudaGetLastError();
-        return s3r_cuda_fail("mma.sync gemm: cudaFuncSetAttribute", e);
-    }
-    gemm_smem_ready = true;
-    return S3R_OK;
+    const char* what = "mma.sync gemm: cudaFuncSetAttribute";
+    int st = s3r_kernel_smem((const void*)gemm_tn_s8_kernel<kEpiDX>, kGemmSmem, what);
+    if (!st) st = s3r_kernel_smem((const void*)gemm_tn_s8_kernel<kEpiDW>, kGemmSmem, what);
+    if (!st) st = s3r_kernel_smem((const void*)gemm_tn_s8_kernel<kEpiDump>, kGemmSmem, what);
+    return st;
 }
 
 template <int EPI>

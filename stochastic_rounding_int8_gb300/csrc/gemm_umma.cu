@@ -36,6 +36,7 @@
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <vector>
 
@@ -884,15 +885,7 @@ static int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t out
     return S3R_OK;
 }
 
-static int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 148;
-    }
-    return n;
-}
+static int sm_count() { return s3r_sm_count(); }
 
 // Band height whose first wave of `wave` tiles touches the fewest operand
 // bytes: distinct row strips x a_strip + distinct column strips x b_strip.
@@ -916,16 +909,11 @@ static int pick_band_rows(int ntm, int ntn, int wave, double a_strip, double b_s
 
 template <int EPI, bool MN>
 static int ensure_kernel() {
-    static bool attr = false;
-    if (attr) return S3R_OK;
-    cudaError_t e =
-        cudaFuncSetAttribute(umma_gemm_kernel<EPI, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return s3r_cuda_fail("umma gemm: cudaFuncSetAttribute", e);
-    }
+    static std::atomic<bool> checked{false};   // the register count is a property of the build, not the device
+    const int st = s3r_kernel_smem((const void*)umma_gemm_kernel<EPI, MN>, SMEM_BYTES, "umma gemm: cudaFuncSetAttribute");
+    if (st || checked.load()) return st;
     cudaFuncAttributes fa{};
-    e = cudaFuncGetAttributes(&fa, umma_gemm_kernel<EPI, MN>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, umma_gemm_kernel<EPI, MN>);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return s3r_cuda_fail("umma gemm: cudaFuncGetAttributes", e);
@@ -937,7 +925,7 @@ static int ensure_kernel() {
         s3r_record_error("umma gemm", buf);
         return S3R_ERR_UNSUPPORTED;
     }
-    attr = true;
+    checked.store(true);
     return S3R_OK;
 }
 

@@ -1410,33 +1410,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
     return fn;
 }
 
-static int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess) {
-            (void)cudaGetLastError();
-            n = 148;
-        }
-    }
-    return n;
-}
+static int sm_count() { return s3r_sm_count(); }
 
 
 template <int MODE, int FMT, bool FOLD>
 static int launch_quant_tma(const CUtensorMap& map, const TileQuantArgs& A, const QuantCommon& C, const QuantOut& O,
                             int64_t ntiles, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(quantize_tma_kernel<MODE, FMT, FOLD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantTmaSmem);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return s3r_cuda_fail("quantize: cudaFuncSetAttribute", e);
-        }
-        attr = true;
-    }
+    const int st = s3r_kernel_smem((const void*)quantize_tma_kernel<MODE, FMT, FOLD>, kQuantTmaSmem,
+                                   "quantize: cudaFuncSetAttribute");
+    if (st) return st;
     const int64_t grid = ntiles < 2LL * sm_count() ? ntiles : 2LL * sm_count();
     quantize_tma_kernel<MODE, FMT, FOLD><<<(unsigned)grid, 256, kQuantTmaSmem, stream>>>(map, A, C, O, ntiles);
     S3R_CHECK_LAUNCH();
@@ -1648,16 +1630,9 @@ extern "C" int swiglu_fwd_quantize(const void* h1, const void* h3, int64_t T, in
 template <int MODE, int FMT>
 static int launch_swiglu_tma(const CUtensorMap* maps, const SwigluArgs& A, const QuantCommon& C, const QuantOut& O1,
                              const QuantOut& O3, int64_t ntiles, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(swiglu_tma_kernel<MODE, FMT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSwigluTmaSmem);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return s3r_cuda_fail("swiglu_quantize: cudaFuncSetAttribute", e);
-        }
-        attr = true;
-    }
+    const int st = s3r_kernel_smem((const void*)swiglu_tma_kernel<MODE, FMT>, kSwigluTmaSmem,
+                                   "swiglu_quantize: cudaFuncSetAttribute");
+    if (st) return st;
     const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
     swiglu_tma_kernel<MODE, FMT><<<(unsigned)grid, 512, kSwigluTmaSmem, stream>>>(maps[0], maps[1], maps[2], A, C,
                                                                                    O1, O3, ntiles);

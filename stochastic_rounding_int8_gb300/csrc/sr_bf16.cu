@@ -175,14 +175,7 @@ __global__ void __launch_bounds__(kSrThreads) sr_fp8_kernel(const float* X, int6
     }
 }
 
-int sm_count_sr() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 148;
-    }
-    return n;
-}
+int sm_count_sr() { return s3r_sm_count(); }
 
 }  // namespace
 }  // namespace s3r
@@ -222,6 +215,10 @@ extern "C" int s3r_sr_fp8(const float* X, int64_t T, int64_t N, int64_t ldx, flo
     if (T < 0 || N < 0) return S3R_ERR_ARG;
     if (round_mode != S3R_ROUND_S3R && round_mode != S3R_ROUND_INDEP && round_mode != S3R_ROUND_RTNE)
         return S3R_ERR_ARG;
+    if (!(inv_scale > 0.0f) || !(inv_scale <= 3.402823466e38f)) {   // rejects 0, negatives, NaN and infinity
+        s3r_record_error("s3r_sr_fp8", "inv_scale must be finite and greater than zero");
+        return S3R_ERR_ARG;
+    }
     if (T == 0 || N == 0) return S3R_OK;
     if (!X || !Y) return S3R_ERR_ARG;
     if (ldx < N || ldy < N) return S3R_ERR_SHAPE;

@@ -48,13 +48,20 @@ def expand_tiles(delta, T, N, tr=TILE, tc=TILE):
     return np.repeat(np.repeat(np.asarray(delta, dtype=np.float64), tr, 0), tc, 1)[:T, :N]
 
 
+def _mm(a, b):
+    """float64 matrix product (torch's CPU matmul: multi-threaded)."""
+    import torch
+    return (torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)) @
+            torch.from_numpy(np.ascontiguousarray(b, dtype=np.float64))).numpy()
+
+
 def dx_magnitude(Q, delta, W8, s_x, eps=None, rowsum=None, v=None, S=None, rows=None):
     """sum_kb |delta| * |sum_n Q W8| bounded above by |Delta Q| |W8|^T, plus the
     correction terms, over |s_x|: an upper bound of the terms' absolute sum."""
     T, N = Q.shape
     rows = np.arange(T) if rows is None else np.asarray(rows)
     G = np.abs(expand_tiles(delta, T, N)[rows] * Q[rows].astype(np.float64))
-    mag = G @ np.abs(W8.astype(np.float64)).T
+    mag = _mm(G, np.abs(W8.astype(np.float64)).T)
     if eps is not None:
         mag = mag + np.abs(eps[rows])[:, None] * np.abs(rowsum.astype(np.float64))[None, :]
         mag = mag + np.abs(v[rows // S])
@@ -67,7 +74,7 @@ def dw_magnitude(X8, Q, delta, s_w, colmean=None, mu=None, xsum=None, p=None, kr
     N = Q.shape[1]
     krows = np.arange(K) if krows is None else np.asarray(krows)
     G = np.abs(expand_tiles(delta, T, N) * Q.astype(np.float64))
-    mag = np.abs(X8[:, krows].astype(np.float64)).T @ G
+    mag = _mm(np.abs(X8[:, krows].astype(np.float64)).T, G)
     if colmean is not None:
         cm = np.abs(colmean - mu[:, None])
         mag = mag + np.abs(xsum[:, krows].astype(np.float64)).T @ cm + np.abs(p[krows])[:, None]
@@ -102,3 +109,57 @@ def near_tie_flips(Q_gpu, Q_orc, y_orc, u, max_frac=1e-3, margin=1e-3):
     close = np.minimum(np.abs(p - u), np.minimum(p, 1 - p)) < margin
     assert close[mask].all(), "a code differs where the oracle's decision was not a near tie"
     return mask
+
+
+def tile_amax(g, tile=TILE):
+    """Per-128x128-tile absmax of g [T, N] (ragged edges included), float32."""
+    T, N = g.shape
+    nt, nn = -(-T // tile), -(-N // tile)
+    pad = np.zeros((nt * tile, nn * tile), dtype=np.float32)
+    pad[:T, :N] = np.abs(g)
+    return pad.reshape(nt, tile, nn, tile).max(axis=(1, 3))
+
+
+def flip_effect(Qg, dg, Qo, do, W8, X8, s_x, s_w, S, dx_ec, dw_ec, rows, krows, chunk=2048):
+    """Exact change of dX[rows] and dW[krows] of one linear when the oracle's
+    dequantized gradient Delta_o Q_o is replaced by Delta_g Q_g, i.e. by
+    D = Delta_g Q_g - Delta_o Q_o: through the correction (D - P(D), P the
+    per-example projection onto row- and column-constant matrices) where the
+    mode applies it, then both products and the rescales.  Streams D in
+    chunks of rows, so it never holds the whole [T, N] difference."""
+    T, N = Qg.shape
+    assert chunk % TILE == 0
+    rows = np.asarray(rows, dtype=np.int64)
+    krows = np.asarray(krows, dtype=np.int64)
+    B = T // S
+    rowsum = np.zeros(T)
+    colsum = np.zeros((B, N))
+    XD = np.zeros((krows.size, N))
+    Drows = np.zeros((rows.size, N))
+    pos = {int(r): i for i, r in enumerate(rows)}
+    X8k = X8[:, krows].astype(np.float64)
+    for t0 in range(0, T, chunk):
+        t1 = min(T, t0 + chunk)
+        tr = t0 // TILE   # chunk is a multiple of the tile height
+        Dc = (expand_tiles(dg[tr:], t1 - t0, N) * Qg[t0:t1].astype(np.float64)
+              - expand_tiles(do[tr:], t1 - t0, N) * Qo[t0:t1].astype(np.float64))
+        rowsum[t0:t1] = Dc.sum(1)
+        for b in range(t0 // S, (t1 - 1) // S + 1):
+            a0, a1 = max(t0, b * S), min(t1, (b + 1) * S)
+            colsum[b] += Dc[a0 - t0:a1 - t0].sum(0)
+        XD += _mm(X8k[t0:t1].T, Dc)
+        sel = rows[(rows >= t0) & (rows < t1)]
+        for r in sel:
+            Drows[pos[int(r)]] = Dc[r - t0]
+    rowmean = rowsum / N
+    colmean = colsum / S
+    mu = rowsum.reshape(B, S).sum(1) / (S * N)
+    b_of = rows // S
+    if dx_ec:
+        Drows = Drows - rowmean[rows][:, None] - colmean[b_of] + mu[b_of][:, None]
+    ddx = _mm(Drows, W8.astype(np.float64).T) / np.asarray(s_x, dtype=np.float64)[rows][:, None]
+    if dw_ec:
+        xs = X8k.reshape(B, S, krows.size).sum(1)                  # [B, nk]
+        XD = XD - (X8k.T @ rowmean)[:, None] - xs.T @ colmean + (xs.T @ mu)[:, None]
+    ddw = XD / np.asarray(s_w, dtype=np.float64)[None, :]
+    return ddx, ddw

@@ -125,3 +125,38 @@ def test_grouped_args_rejected_on_host():
                          s3r.ROUND_S3R, s3r.EC_TWO_WAY, s3r.CODES_F16, 0, fake, fake, fake, fake, fake, 1 << 30,
                          None, None, len(offs) - 1, C.cast(arr, C.POINTER(C.c_int64)))
         assert s3r.lib().ffn_backward(C.byref(a), None) == -1
+
+
+def test_sr_fp8_rejects_bad_scales_on_host(L):
+    """s3r_sr_fp8 takes only a finite scale above zero; zero, negative, NaN and
+    infinite scales are rejected before any launch (fake pointers)."""
+    fake = C.c_void_p(0x1000)
+    for bad in (0.0, -1.0, -0.0, float("nan"), float("inf"), float("-inf")):
+        assert L.s3r_sr_fp8(fake, 4, 16, 16, bad, s3r.ROUND_S3R, 0, 0, fake, 16, None) == -1, bad
+        assert "inv_scale" in L.s3r_last_error().decode()
+    assert L.s3r_sr_fp8(fake, 0, 16, 16, 0.5, s3r.ROUND_S3R, 0, 0, fake, 16, None) == 0   # empty: no launch
+
+
+def test_ffn_workspace_offsets(L):
+    """The inspection hook lays its views inside the workspace, without overlap,
+    in dense and grouped mode; grouped blocks follow each other."""
+    out = (C.c_size_t * 7)()
+    T, d, F, S = 512, 136, 392, 256
+    assert L.s3r_ffn_workspace_offsets(T, d, F, S, 1, 1, None, 0, 0, C.cast(out, C.c_void_p)) == 0
+    cd = 2
+    sizes = [T * d * cd, 4 * 2 * 2, T * F * cd, 4 * 4 * 4, T * F * cd, 4 * 4 * 4, T * F * 4]
+    spans = sorted((int(o), int(o) + n) for o, n in zip(out, sizes))
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+    assert spans[-1][1] <= L.s3r_ffn_workspace_size(T, d, F, S, 1, 2, 1)
+    assert all(int(o) % 256 == 0 for o in out)
+    offs = [0, 300, 300, 812]
+    arr = (C.c_int64 * 4)(*offs)
+    g0 = (C.c_size_t * 7)()
+    g2 = (C.c_size_t * 7)()
+    assert L.s3r_ffn_workspace_offsets(0, d, F, 0, 1, 1, C.cast(arr, C.c_void_p), 3, 0, C.cast(g0, C.c_void_p)) == 0
+    assert L.s3r_ffn_workspace_offsets(0, d, F, 0, 1, 1, C.cast(arr, C.c_void_p), 3, 2, C.cast(g2, C.c_void_p)) == 0
+    first = L.s3r_ffn_workspace_size(300, d, F, 300, 1, 2, 1)
+    assert int(g2[0]) - int(g0[0]) >= first - 256
+    assert int(g2[6]) + 512 * F * 4 <= L.s3r_ffn_grouped_workspace_size(C.cast(arr, C.c_void_p), 3, d, F, 1, 2, 1)
+    # the empty expert has no block
+    assert L.s3r_ffn_workspace_offsets(0, d, F, 0, 1, 1, C.cast(arr, C.c_void_p), 3, 1, C.cast(g0, C.c_void_p)) == -1

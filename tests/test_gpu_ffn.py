@@ -7,9 +7,8 @@
    one step where the oracle's decision was a near tie; the test checks that
    every such difference is a near tie and adds its exact linear effect
    (through the correction and both products) before comparing dX, dW1, dW3.
-3. At the full d=2048 / F=5632 / T=8192 size the block's outputs are finite,
-   stage 1 matches the oracle on sampled rows, and every gradient lies within
-   quantization noise of fp64 autograd through the dequantized operands.
+ffn_backward itself at full size, element by element against the oracle, is
+in test_gpu_ffn_oracle.py.
 """
 import numpy as np
 import pytest
@@ -215,82 +214,3 @@ def test_ffn_staged_matches_oracle(s3r, orc, fmt, mode, ec):
     torch.cuda.synchronize()
     h1, h3, dY = (orc.from_torch_bf16(t) for t in (inp.h1, inp.h3, inp.dY))
     compare_block_with_oracle(s3r, orc, gpu, ops_o, h1, h3, dY, S, mode, ec, seed)
-
-
-def test_ffn_full_size_block(s3r, orc):
-    """d=2048, F=5632, T=8192 (4 x 2048), S3R-EC two-way, as the benchmark runs it."""
-    T, d, F, S = 8192, 2048, 5632, 2048
-    inp = workloads.ffn_inputs(T, d, F, S, seed=workloads.DATA_SEED + 1)
-    ops = _device_ops(s3r, inp)
-    st = s3r.new_status()
-    g = s3r.ffn_backward(ops, inp.dY.cuda(), S, s3r.ROUND_S3R, s3r.EC_TWO_WAY, seed=0, status=st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
-    for k in ("dX", "dW1", "dW3", "dW2"):
-        assert torch.isfinite(getattr(g, k)).all(), k
-    # stage 1 exact on sampled rows of dW2 (oracle)
-    A8, s_a = codes(ops.A8), ops.s_a.cpu().numpy()
-    W8, s_w2 = codes(ops.W2_8), ops.s_w2.cpu().numpy()
-    krows = np.array([0, 17, 2900, F - 1])
-    ref = orc.linear_backward(orc.from_torch_bf16(inp.dY), A8, s_a, W8, s_w2, S, mode=orc.S3R,
-                              ec_mode=orc.EC_TWO_WAY, seed=0, tensor_id=orc.TID_W2, rows=np.array([0, T - 1]),
-                              krows=krows)
-    mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w2, ref.colmean, ref.mu, ref.xsum, ref.p, krows=krows)
-    assert_close_mag(g.dW2.cpu().numpy()[krows], ref.dW, mdw, "dW2 rows")
-    # every gradient within quantization noise of fp64 autograd (sampled rows)
-    f64 = lambda q, s, ax: q.double() * s.double().unsqueeze(1 - ax)   # fp16/int8 codes are exact in fp64
-    Xd, Ad = f64(ops.X8.cpu(), ops.s_x.cpu(), 0), f64(ops.A8.cpu(), ops.s_a.cpu(), 0)
-    W1d, W3d = f64(ops.W1_8.cpu(), ops.s_w1.cpu(), 1), f64(ops.W3_8.cpu(), ops.s_w3.cpu(), 1)
-    W2d = f64(ops.W2_8.cpu(), ops.s_w2.cpu(), 1)
-    G = inp.dY.double()
-    dA = G @ W2d.T
-    t1 = inp.h1.double().requires_grad_(True)
-    t3 = inp.h3.double().requires_grad_(True)
-    (torch.nn.functional.silu(t1) * t3).backward(dA)
-    dh1, dh3 = t1.grad, t3.grad
-    rows = torch.arange(0, T, 97)
-    cols = torch.arange(0, F, 89)
-    rel = lambda a, b: float((a - b).norm() / b.norm())
-    assert rel(g.dX.cpu().double()[rows], (dh1[rows] @ W1d.T + dh3[rows] @ W3d.T)) < 0.15
-    assert rel(g.dW2.cpu().double()[cols], (Ad[:, cols].T @ G)) < 0.15
-    assert rel(g.dW1.cpu().double()[:, cols], (Xd.T @ dh1[:, cols])) < 0.15
-    assert rel(g.dW3.cpu().double()[:, cols], (Xd.T @ dh3[:, cols])) < 0.15
-
-
-def test_ffn_large_block_sampled(s3r, orc):
-    """The larger block, d=4096, F=14336, T=16384 (8 x 2048), S3R-EC two-way:
-    finite outputs, stage 1 against the oracle on sampled rows of dW2 and of
-    dA, and every gradient within quantization noise of fp64 autograd on
-    sampled rows and columns."""
-    T, d, F, S = 16384, 4096, 14336, 2048
-    inp = workloads.ffn_inputs(T, d, F, S, seed=workloads.DATA_SEED + 2)
-    ops = _device_ops(s3r, inp)
-    st = s3r.new_status()
-    g = s3r.ffn_backward(ops, inp.dY.cuda(), S, s3r.ROUND_S3R, s3r.EC_TWO_WAY, seed=0, status=st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
-    for k in ("dX", "dW1", "dW3", "dW2"):
-        assert torch.isfinite(getattr(g, k)).all(), k
-    A8, s_a = codes(ops.A8), ops.s_a.cpu().numpy()
-    W8, s_w2 = codes(ops.W2_8), ops.s_w2.cpu().numpy()
-    krows = np.array([0, 5000, F - 1])
-    ref = orc.linear_backward(orc.from_torch_bf16(inp.dY), A8, s_a, W8, s_w2, S, mode=orc.S3R,
-                              ec_mode=orc.EC_TWO_WAY, seed=0, tensor_id=orc.TID_W2, rows=np.array([0]), krows=krows)
-    mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w2, ref.colmean, ref.mu, ref.xsum, ref.p, krows=krows)
-    assert_close_mag(g.dW2.cpu().numpy()[krows], ref.dW, mdw, "dW2 rows")
-    f64 = lambda q, s, ax: q.double() * s.double().unsqueeze(1 - ax)
-    rows = torch.arange(0, T, 1021)
-    cols = torch.arange(0, F, 997)
-    G = inp.dY.double()
-    Xd = f64(ops.X8.cpu(), ops.s_x.cpu(), 0)
-    W1d, W3d = f64(ops.W1_8.cpu(), ops.s_w1.cpu(), 1), f64(ops.W3_8.cpu(), ops.s_w3.cpu(), 1)
-    W2d = f64(ops.W2_8.cpu(), ops.s_w2.cpu(), 1)
-    dA = G @ W2d.T
-    t1 = inp.h1.double().requires_grad_(True)
-    t3 = inp.h3.double().requires_grad_(True)
-    (torch.nn.functional.silu(t1) * t3).backward(dA)
-    dh1, dh3 = t1.grad, t3.grad
-    rel = lambda a, b: float((a - b).norm() / b.norm())
-    assert rel(g.dX.cpu().double()[rows], (dh1[rows] @ W1d.T + dh3[rows] @ W3d.T)) < 0.15
-    assert rel(g.dW1.cpu().double()[:, cols], (Xd.T @ dh1[:, cols])) < 0.15
-    assert rel(g.dW3.cpu().double()[:, cols], (Xd.T @ dh3[:, cols])) < 0.15

@@ -162,8 +162,10 @@ def test_dx_sum_accumulate_and_single_term(s3r):
 @pytest.mark.parametrize("fmt,ec_name", [(1, "EC_DX_ONLY"), (1, "EC_TWO_WAY"), (0, "EC_TWO_WAY")])
 def test_ffn_w2_gemms_full_size_sampled(s3r, orc, fmt, ec_name):
     """The W2 linear of the d=2048, F=5632, T=8192 (4 x 2048) SwiGLU block at
-    full size: dA = dX of W2 [8192, 5632] and dW2 [5632, 2048] in the launch
-    configuration the benchmark times, checked on 48 sampled rows each."""
+    full size through the standalone int8_gemm_dx / int8_gemm_dw launches
+    (ffn_backward's own mixed launches are compared in
+    test_gpu_ffn_oracle.py): dA = dX of W2 [8192, 5632] and dW2 [5632, 2048],
+    checked on 48 sampled rows each."""
     T, d, F, S = 8192, 2048, 5632, 2048
     inp = workloads.ffn_inputs(T, d, F, S, seed=workloads.DATA_SEED + 1)
     A = orc.from_torch_bf16(inp.a)

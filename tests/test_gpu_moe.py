@@ -5,16 +5,15 @@
    (0, 1, 2); empty experts get zero weight gradients.
 2. Each expert's staged backward matches the oracle's grouped backward (the
    same near-tie rules as the dense block).
-3. The MoE workload at full size (8 experts, d=4096, F=1408, 16384 tokens
-   top-2, Zipf(1.1) loads): finite outputs, sampled rows of the smallest
-   expert's W2 gradient against the oracle.
+The MoE workload at full size is compared with the oracle, expert by expert,
+in test_gpu_ffn_oracle.py.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads
-from parity_util import assert_close_mag, codes, dw_magnitude
+from parity_util import codes
 from test_gpu_ffn import MODES, _staged, compare_block_with_oracle
 
 pytestmark = pytest.mark.gpu
@@ -90,30 +89,3 @@ def test_staged_experts_match_oracle(s3r, orc, fmt, mode, ec):
         torch.cuda.synchronize()
         compare_block_with_oracle(s3r, orc, gpu, ops_o.expert(e, r0, r1), h1[r0:r1], h3[r0:r1], dY[r0:r1],
                                   r1 - r0, mode, ec, 4, tid_base=orc.MOE_TID_STRIDE * e)
-
-
-def test_moe_workload_full_size(s3r, orc):
-    """8 experts, d=4096, F=1408, 16384 tokens top-2 (32768 routed rows),
-    S3R-EC two-way, as the benchmark runs it."""
-    w = workloads.WORKLOADS["moe_e8_d4096_F1408_tok16384_top2"]
-    inp = workloads.moe_inputs(w["tokens"], w["topk"], w["experts"], w["d"], w["F"],
-                               seed=workloads.DATA_SEED + 5)
-    ops = _device_ops(s3r, inp, s3r.CODES_F16)
-    st = s3r.new_status()
-    g = s3r.ffn_backward(ops, inp.dY.cuda(), 0, s3r.ROUND_S3R, s3r.EC_TWO_WAY, seed=0, status=st,
-                         group_offsets=inp.offsets)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
-    for k in ("dX", "dW1", "dW3", "dW2"):
-        assert torch.isfinite(getattr(g, k)).all(), k
-    # the smallest expert's W2 gradient on sampled rows against the oracle
-    e = w["experts"] - 1
-    r0, r1 = inp.offsets[e], inp.offsets[e + 1]
-    A8, s_a = codes(ops.A8[r0:r1]), ops.s_a[r0:r1].cpu().numpy()
-    W8, s_w2 = codes(ops.W2_8[e]), ops.s_w2[e].cpu().numpy()
-    krows = np.array([0, 11, 700, w["F"] - 1])
-    ref = orc.linear_backward(orc.from_torch_bf16(inp.dY[r0:r1]), A8, s_a, W8, s_w2, r1 - r0, mode=orc.S3R,
-                              ec_mode=orc.EC_TWO_WAY, seed=0, tensor_id=orc.MOE_TID_STRIDE * e + orc.TID_W2,
-                              rows=np.array([0]), krows=krows)
-    mdw = dw_magnitude(A8, ref.Q, ref.delta, s_w2, ref.colmean, ref.mu, ref.xsum, ref.p, krows=krows)
-    assert_close_mag(g.dW2[e].cpu().numpy()[krows], ref.dW, mdw, "dW2 rows of the smallest expert")

@@ -55,3 +55,67 @@ def test_rescale_equals_dequantize_then_contract(orc):
     dW = orc.dw(X8, Q, delta, s_w, orc.EC_NONE, None, None, None, None, T, np.arange(K))
     assert np.allclose(dX, (Gt @ W8.T.astype(np.float64)) / s_x[:, None], rtol=1e-12)
     assert np.allclose(dW, (X8.T.astype(np.float64) @ Gt) / s_w[None, :], rtol=1e-12)
+
+
+@pytest.mark.parametrize("T,N,K,S", [(260, 300, 24, 130), (128, 128, 1, 128), (1, 129, 3, 1), (300, 257, 40, 150)])
+@pytest.mark.parametrize("ec_name", ["EC_NONE", "EC_DX_ONLY", "EC_TWO_WAY", "EC_DX_TOKEN_ONLY", "EC_DW_ONLY"])
+def test_matmul_products_equal_loop_products(orc, T, N, K, S, ec_name):
+    """dx_matmul / dw_matmul (integer block sums by a library matmul) equal the
+    nested-loop dx / dw bit for bit, corrections and rescales included, on
+    ragged shapes; rows and krows subsets too."""
+    rng = np.random.default_rng(T + 3 * N + 7 * K)
+    ec = getattr(orc, ec_name)
+    Q = rng.integers(-127, 128, size=(T, N)).astype(np.int8)
+    Q[0, :min(N, 5)] = 127                      # extremes of the block sums
+    W8 = rng.integers(-127, 128, size=(K, N)).astype(np.int8)
+    W8[0, :min(N, 5)] = -127
+    X8 = rng.integers(-127, 128, size=(T, K)).astype(np.int8)
+    delta = (rng.random((-(-T // 128), -(-N // 128))) + 0.1).astype(np.float32) * np.float32(1e-3)
+    s_x = (rng.random(T) + 0.5).astype(np.float32)
+    s_w = (rng.random(N) + 0.5).astype(np.float32)
+    B = T // S
+    eps = rng.standard_normal(T) * 1e-4
+    colmean = rng.standard_normal((B, N)) * 1e-4
+    mu = rng.standard_normal(B) * 1e-5
+    rowsum, v, xsum, p = orc.ec_factors(eps, colmean, mu, S, W8, X8)
+    rows = np.arange(T)
+    krows = np.arange(K)
+    a = orc.dx(Q, delta, W8, s_x, ec, eps, rowsum, v, S, rows)
+    b = orc.dx_matmul(Q, delta, W8, s_x, ec, eps, rowsum, v, S, rows, chunk=97)
+    assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+    a = orc.dw(X8, Q, delta, s_w, ec, colmean, mu, xsum, p, S, krows)
+    b = orc.dw_matmul(X8, Q, delta, s_w, ec, colmean, mu, xsum, p, S, krows)
+    assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+    sub = np.array([T - 1, 0]) if T > 1 else np.array([0])
+    assert np.array_equal(orc.dx(Q, delta, W8, None, ec, eps, rowsum, v, S, sub),
+                          orc.dx_matmul(Q, delta, W8, None, ec, eps, rowsum, v, S, sub))
+    ksub = np.array([K - 1, 0]) if K > 1 else np.array([0])
+    assert np.array_equal(orc.dw(X8, Q, delta, None, ec, colmean, mu, xsum, p, S, ksub),
+                          orc.dw_matmul(X8, Q, delta, None, ec, colmean, mu, xsum, p, S, ksub))
+
+
+def test_block_sums_exact_at_the_extremes(orc):
+    """A 128-long block of +-127 * +-127 products (the largest block sum) is
+    exact through the library matmul; a wrong sum trips the guard."""
+    A = np.full((3, 128), 127, dtype=np.int8)
+    A[1] = -127
+    B = np.full((128, 4), 127, dtype=np.int8)
+    B[:, 2] = -127
+    out = orc.block_sums(A, B)
+    assert np.array_equal(out, (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64))
+    assert out[0, 0] == 128 * 127 * 127
+
+
+def test_ffn_backward_matmul_equals_loops(orc):
+    """The FFN block composed with the matmul products equals the loop version
+    bit for bit (every intermediate and output)."""
+    import workloads
+    inp = workloads.ffn_inputs(256, 128, 384, 128, seed=21)
+    f = orc.from_torch_bf16
+    ops = orc.ffn_forward_operands(f(inp.X), f(inp.W1), f(inp.W3), f(inp.W2), f(inp.a))
+    h1, h3, dY = f(inp.h1), f(inp.h3), f(inp.dY)
+    a = orc.ffn_backward(ops, h1, h3, dY, 128, orc.S3R, orc.EC_TWO_WAY, seed=3)
+    b = orc.ffn_backward(ops, h1, h3, dY, 128, orc.S3R, orc.EC_TWO_WAY, seed=3, matmul=True)
+    for k in ("dA", "dX", "dW1", "dW2", "dW3"):
+        assert np.array_equal(getattr(a, k), getattr(b, k)), k
+    assert np.array_equal(a.w1.Q, b.w1.Q) and np.array_equal(a.w3.Q, b.w3.Q)
