@@ -23,14 +23,21 @@
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (M=128, N=256, K=16) into one of two 256-column fp32
 //               accumulators (double buffer) and commits to mbarriers;
-//   warps 2, 3  idle (they complete warpgroup 0 for the register split);
+//   warps 2, 3  helpers: copy each tile's epilogue vectors (rescale factors,
+//               correction terms) into a shared-memory side buffer with
+//               cp.async while the tile's first blocks run;
 //   warps 4..11 epilogue: per 128-K block, tcgen05.ld their 32 TMEM lanes x
-//               128 columns, acc = fma(scale, block, acc) in registers (acc
-//               seeded with minus the correction); at the end of the tile the
-//               1/s rescale and coalesced fp32 stores, while the producer and
-//               the MMA issuer already run the next tile.
+//               128 columns, acc = fma(scale, block, acc) in registers; after
+//               block kCorrBlock they subtract the correction (from the side
+//               buffer), at the end of the tile rescale by 1/s and hand the
+//               tile to the TMA engine (bulk tensor stores from small
+//               swizzled staging buffers), while the producer and the MMA
+//               issuer already run the next tile.
 // Warpgroup 0 gives registers to the epilogue warpgroups (setmaxnreg), so a
 // drain keeps four TMEM loads in flight next to the 128 accumulators.
+// The tile boundary is what the two TMEM accumulators must hide (about two
+// blocks of MMA time), so nothing on it waits for global memory: the side
+// data is already in shared memory and the stores are asynchronous.
 // The activation gradient may contract two operand pairs into one
 // accumulator (dX = Q1 W1^T + Q3 W3^T), each with its own scales.
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
@@ -57,26 +64,41 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int MN_ATOM_BYTES = BKS * 128;    // one 64-wide MN atom column over a 64-deep K slice: 8 KiB
 constexpr int THREADS = 384;               // three warpgroups
 constexpr int EPI_WARP0 = 4;                // epilogue warps 4..11 (warpgroups 1 and 2)
-// Register split (setmaxnreg): warpgroup 0 (producer, MMA issuer, two idle
-// warps) drops to kRegsLow, the epilogue warpgroups rise to kRegsHigh.  The
+// Register split (setmaxnreg): warpgroup 0 (producer, MMA issuer, two
+// helpers) drops to kRegsLow, the epilogue warpgroups rise to kRegsHigh.  The
 // launch holds regs_per_thread * 384 registers; the split needs
 // kRegsLow * 128 + kRegsHigh * 256 of them, so the host refuses to launch a
 // build whose per-thread count is below kMinLaunchRegs (an increase that the
 // pool cannot satisfy would wait forever).
-constexpr int kRegsLow = 40, kRegsHigh = 216;
+constexpr int kRegsLow = 56, kRegsHigh = 216;
 constexpr int kMinLaunchRegs = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
 constexpr int EPI_WARPS = 8;
-constexpr int CHUNK = 16;                   // columns per epilogue staging round
-constexpr int STAGE_PITCH = 20;             // floats per staged row: conflict-free 16-byte writes
-constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * STAGE_PITCH * 4;   // 20 KiB
+// Output staging of the TMA stores: per epilogue warp two buffers of 32 rows x
+// 8 fp32 columns (1 KiB each, 32-byte swizzle), so the warp fills one while
+// the TMA engine still reads the other.
+constexpr int OUT_COLS = 8;
+constexpr int OUT_BUF_BYTES = 32 * OUT_COLS * 4;
+constexpr int OUT_STAGE_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;   // 16 KiB
 constexpr int kNbX = 4;                     // dX: examples one 128-row tile may span (S >= 43)
-constexpr int kBch = 8;                     // dW: examples staged per pass
-constexpr int CV_FLOATS = 256 + 2 * kNbX * 128;   // per half; the dW layout (128 + kBch * 128) fits too
-static_assert(128 + kBch * 128 <= CV_FLOATS, "dW column staging fits the dX layout's size");
-constexpr int CV_BYTES = 2 * CV_FLOATS * 4;        // 10 KiB
+constexpr int kBch = 8;                     // dW: examples whose correction vectors are staged per round
+// Side data of one tile, copied into shared memory by the two helper warps
+// while the tile's first blocks run (offsets in floats; rows of the tile are
+// its 128 output rows, columns its 256 output columns):
+//   dX: 1/s_x[row] | eps_g[row] (g < 2) | rowsum_g[col] | v_g[b_lo + i][col] (i < kNbX)
+//   dW: 1/s_w[col] | p[row] | xsum[b][row] | colmean[b][col] - mu[b] for a round
+//       of kBch examples (B > kBch takes several rounds, each refilling the
+//       last two arrays)
+constexpr int SX_ROWSC = 0, SX_EPS = 128, SX_RS = SX_EPS + 2 * 128, SX_V = SX_RS + 2 * 256;
+constexpr int SX_END = SX_V + 2 * kNbX * 256;
+constexpr int SW_COLSC = 0, SW_P = 256, SW_XS = SW_P + 128, SW_CM = SW_XS + kBch * 128;
+constexpr int SW_END = SW_CM + kBch * 256;
+constexpr int SIDE_FLOATS = SX_END > SW_END ? SX_END : SW_END;
+// The correction enters the accumulators after block kCorrBlock of a tile,
+// which leaves the helpers a few blocks to bring the tile's side data in.
+constexpr int kCorrBlock = 3;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + CV_BYTES + 1024 + NUM_BARS * 8 + 16;
+constexpr int NUM_BARS = 2 * STAGES + 7;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGE_BYTES + SIDE_FLOATS * 4 + 1024 + NUM_BARS * 8 + 16;
 static_assert(SMEM_BYTES + 64 <= 232448, "shared memory budget of one sm_103a CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
@@ -134,12 +156,13 @@ struct Problem {
     const float* mu;
     const int32_t* xsum;
     const float* p;
-    int accumulate;
+    int accumulate;              // C += result (an add-reduction store)
+    int c_tma;                   // C is addressable by the TMA engine (map 4 of the problem)
 };
 
 // A launch: up to kMaxProb problems (of one kind, or mixed), their tiles numbered one
-// after another; each problem has up to four tensor maps (A and B of each
-// segment).  Both live in the constant parameter space (__grid_constant__),
+// after another; each problem has up to five tensor maps (A and B of each
+// segment, and the output C).  Both live in the constant parameter space (__grid_constant__),
 // so indexing them with a run-time problem number costs no copy.
 constexpr int kMaxProb = 24;
 struct Args {
@@ -149,7 +172,7 @@ struct Args {
     int* d_status;
 };
 struct Maps {
-    CUtensorMap m[kMaxProb][4];
+    CUtensorMap m[kMaxProb][5];
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -246,205 +269,283 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Per-tile column vectors, staged in shared memory by the four epilogue warps
-// of each 128-column half (one column per thread, coalesced), so that the
-// per-thread seed and rescale below are branch-free broadcast smem reads:
-//   dX: rowsum_g[128] for g < 2, then v_g[b_lo + i][128] for i < kNbX;
-//   dW: 1/s_w[128], then colmean[b][128] - mu[b] for a chunk of kBch examples.
-// Columns past N are staged as 0.
-__device__ __forceinline__ void half_bar(int half) {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + half), "r"(128) : "memory");
-}
-
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// Seeds the thread's 128 accumulators (row `row`, columns c0..c0+127) with
-// minus the correction, which does not depend on the contraction:
-//   dX: -(eps_g[t] rowsum_g[k] + v_g[t/S, k]) summed over the terms g;
-//   dW: -(p[k] + sum_b xsum[b, k] (colmean[b, n] - mu[b])).
-// The dW pass also stages 1/s_w for the final rescale.
-template <int EPI>
-__device__ __forceinline__ void seed_tile(const Problem& P, float (&acc)[128], float* cv, int64_t row, int64_t m0,
-                                          int64_t c0, int half, int ht) {
-    const bool in = row < P.M;
-    const int64_t cc = c0 + ht;   // the column this thread stages
-    const bool cin = cc < P.N;
-    if (EPI == kDX) {
-        if (!P.ec_mode) {
-#pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-            return;
+// ---------------------------------------------------------------------------
+// Side data.  The two helper warps (64 threads) copy a tile's epilogue vectors
+// from global memory into the side buffer with cp.async (no registers held,
+// zero fill past the tensor ends), then convert them in place: reciprocals of
+// the rescale factors, int32 sums to float, colmean - mu.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(float* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src) : "memory");
+}
+// 4 bytes, or zeros when `valid` is false (nothing is read then; src is a valid address regardless)
+__device__ __forceinline__ void cp_async4(float* dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(su32(dst)), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// the 64 helper threads (warps 2 and 3)
+__device__ __forceinline__ void helper_bar() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// the same barrier, returning whether `ok` holds for all 64 (one outcome for all)
+__device__ __forceinline__ bool helper_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 64, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+// dst[0 .. n) = src[0 .. n) (32-bit elements), elements at index >= valid zero
+// filled; 16-byte copies when the whole run is valid and aligned.  ht: helper thread 0..63.
+__device__ __forceinline__ void side_copy(float* dst, const void* src, int n, int64_t valid, int ht) {
+    const char* s = static_cast<const char*>(src);
+    if (valid >= n && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        for (int i = 4 * ht; i < n; i += 4 * 64) cp_async16(dst + i, s + 4 * (size_t)i);
+    } else {
+        for (int i = ht; i < n; i += 64) cp_async4(dst + i, i < valid ? s + 4 * (size_t)i : s, i < valid);
+    }
+}
+
+// Copies and converts the side data of one tile (rows m0 .., columns n0 .. of
+// problem P) into `sd`.  All 64 helper threads call it; it ends with their
+// shared barrier passed, so every value is in place when they arrive.
+// Rounds of side data a tile takes: the dW two-way correction stages kBch
+// examples per round; everything else fits one.
+__device__ __forceinline__ int side_rounds(const Problem& P, bool dw) {
+    if (!dw || P.ec_mode != S3R_EC_TWO_WAY || P.B <= kBch) return 1;
+    return (int)((P.B + kBch - 1) / kBch);
+}
+
+template <int KIND>
+__device__ __forceinline__ void load_side(const Problem& P, float* sd, int64_t m0, int64_t n0, int ht, int round) {
+    const int64_t rows = P.M - m0 < BM ? P.M - m0 : BM;      // valid rows of the tile
+    const int64_t cols = P.N - n0 < BN ? P.N - n0 : BN;      // valid columns
+    if (KIND == kDX) {
+        if (P.s_row) side_copy(sd + SX_ROWSC, P.s_row + m0, BM, rows, ht);
+        const int nseg = P.seg[1].K > 0 ? 2 : 1;
+        int64_t b_lo = 0, b_hi = 0;
+        if (P.ec_mode) {
+            b_lo = m0 / P.S;
+            b_hi = (m0 + rows - 1) / P.S;
+            for (int g = 0; g < nseg; ++g) {
+                side_copy(sd + SX_EPS + g * 128, P.seg[g].eps + m0, BM, rows, ht);
+                side_copy(sd + SX_RS + g * 256, P.seg[g].rowsum + n0, BN, cols, ht);
+                for (int64_t i = 0; i < kNbX && b_lo + i <= b_hi; ++i)
+                    side_copy(sd + SX_V + (g * kNbX + (int)i) * 256, P.seg[g].v + (b_lo + i) * P.N + n0, BN, cols, ht);
+            }
         }
-        const int64_t b_lo = m0 / P.S;
-        const int64_t b_hi = ((m0 + BM - 1 < P.M ? m0 + BM - 1 : P.M - 1)) / P.S;
-        half_bar(half);   // every thread of the half is past its previous use of cv
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            const bool on = g == 0 || P.seg[1].K > 0;
-            cv[g * 128 + ht] = (on && cin) ? (float)__ldg(P.seg[g].rowsum + cc) : 0.0f;
-            for (int i = 0; i < kNbX; ++i)   // staged negated: the seed below is one fma per pair
-                cv[256 + (g * kNbX + i) * 128 + ht] =
-                    (on && cin && b_lo + i <= b_hi) ? -__ldg(P.seg[g].v + (b_lo + i) * P.N + cc) : 0.0f;
-        }
-        half_bar(half);
-        const float ep0 = in ? __ldg(P.seg[0].eps + row) : 0.0f;
-        const float ep1 = (in && P.seg[1].K > 0) ? __ldg(P.seg[1].eps + row) : 0.0f;
-        const int i_row = in ? (int)(row / P.S - b_lo) : 0;
-        // -(ep rowsum + v) = fma(-ep, rowsum, -v) exactly (v is staged negated)
-        const float* rs0 = cv;
-        const float* nv0 = cv + 256 + i_row * 128;
-        const float2 nep0 = make_float2(-ep0, -ep0);
-#pragma unroll
-        for (int j4 = 0; j4 < 128; j4 += 4) {
-            const float4 r = lds4(rs0 + j4), w = lds4(nv0 + j4);
-            const float2 a = f2_fma(nep0, make_float2(r.x, r.y), make_float2(w.x, w.y));
-            const float2 b = f2_fma(nep0, make_float2(r.z, r.w), make_float2(w.z, w.w));
-            acc[j4 + 0] = a.x;
-            acc[j4 + 1] = a.y;
-            acc[j4 + 2] = b.x;
-            acc[j4 + 3] = b.y;
-        }
-        if (P.seg[1].K > 0) {
-            const float* rs1 = cv + 128;
-            const float* nv1 = cv + 256 + (kNbX + i_row) * 128;
-            const float2 nep1 = make_float2(-ep1, -ep1);
-#pragma unroll
-            for (int j4 = 0; j4 < 128; j4 += 4) {
-                const float4 r = lds4(rs1 + j4), w = lds4(nv1 + j4);
-                const float2 a = f2_add(make_float2(acc[j4], acc[j4 + 1]),
-                                        f2_fma(nep1, make_float2(r.x, r.y), make_float2(w.x, w.y)));
-                const float2 b = f2_add(make_float2(acc[j4 + 2], acc[j4 + 3]),
-                                        f2_fma(nep1, make_float2(r.z, r.w), make_float2(w.z, w.w)));
-                acc[j4 + 0] = a.x;
-                acc[j4 + 1] = a.y;
-                acc[j4 + 2] = b.x;
-                acc[j4 + 3] = b.y;
+        cp_async_wait_all();
+        helper_bar();
+        for (int i = ht; i < BM; i += 64)
+            sd[SX_ROWSC + i] = P.s_row ? __frcp_rn(sd[SX_ROWSC + i]) : 1.0f;   // 1/s of a zero-filled row is unused
+        if (P.ec_mode) {
+            for (int g = 0; g < 2; ++g) {
+                for (int j = ht; j < BN; j += 64)
+                    sd[SX_RS + g * 256 + j] = g < nseg ? (float)__float_as_int(sd[SX_RS + g * 256 + j]) : 0.0f;
+                if (g >= nseg)
+                    for (int i = ht; i < BM; i += 64) sd[SX_EPS + g * 128 + i] = 0.0f;
             }
         }
     } else {
         const bool two = P.ec_mode == S3R_EC_TWO_WAY;
-        const float pr = (two && in) ? __ldg(P.p + row) : 0.0f;
+        const int64_t b0 = (int64_t)round * kBch;
+        const int nb = two ? (int)(P.B - b0 < kBch ? P.B - b0 : kBch) : 0;
+        if (round == 0) {
+            if (P.s_col) side_copy(sd + SW_COLSC, P.s_col + n0, BN, cols, ht);
+            if (two) side_copy(sd + SW_P, P.p + m0, BM, rows, ht);
+        }
+        for (int b = 0; b < nb; ++b) {
+            side_copy(sd + SW_XS + b * 128, P.xsum + (b0 + b) * P.M + m0, BM, rows, ht);
+            side_copy(sd + SW_CM + b * 256, P.colmean + (b0 + b) * P.N + n0, BN, cols, ht);
+        }
+        cp_async_wait_all();
+        helper_bar();
+        if (round == 0)
+            for (int j = ht; j < BN; j += 64) sd[SW_COLSC + j] = P.s_col ? __frcp_rn(sd[SW_COLSC + j]) : 1.0f;
+        for (int b = 0; b < nb; ++b) {
+            const float mb = __ldg(P.mu + b0 + b);
+            for (int i = ht; i < BM; i += 64) sd[SW_XS + b * 128 + i] = (float)__float_as_int(sd[SW_XS + b * 128 + i]);
+            for (int j = ht; j < BN; j += 64) sd[SW_CM + b * 256 + j] = sd[SW_CM + b * 256 + j] - mb;
+        }
+    }
+    helper_bar();
+}
+
+// Subtracts the correction (or, for dW, one round of it) from the thread's
+// accumulators (row `row`, local row rl of the tile, its 128 columns of half
+// `half`), from the side data:
+//   dX: acc -= eps_g[t] rowsum_g[k] + v_g[t/S, k] for each term g;
+//   dW: acc -= sum_b xsum[b, k] (colmean[b, n] - mu[b]) over the round's
+//       examples, and p[k] in round 0 (two-way).
+template <int KIND>
+__device__ __forceinline__ void apply_correction(const Problem& P, float (&acc)[128], const float* sd, int64_t row,
+                                                 int64_t m0, int rl, int half, int round) {
+    if (KIND == kDX) {
+        if (!P.ec_mode) return;
+        const int i_row = row < P.M ? (int)(row / P.S - m0 / P.S) : 0;
+        const int nseg = P.seg[1].K > 0 ? 2 : 1;
+        for (int g = 0; g < nseg; ++g) {
+            const float ep = sd[SX_EPS + g * 128 + rl];
+            const float2 ep2 = make_float2(ep, ep);
+            const float* rs = sd + SX_RS + g * 256 + 128 * half;
+            const float* vv = sd + SX_V + (g * kNbX + i_row) * 256 + 128 * half;
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = pr;
-        const int64_t nb = two ? P.B : 0;
-        for (int64_t b0 = 0; b0 == 0 || b0 < nb; b0 += kBch) {
-            half_bar(half);   // every thread of the half is past its previous use of cv
-            if (b0 == 0) cv[ht] = (P.s_col && cin) ? __frcp_rn(__ldg(P.s_col + cc)) : 1.0f;
-            for (int i = 0; i < kBch; ++i)
-                cv[128 + i * 128 + ht] =
-                    (cin && b0 + i < nb) ? __ldg(P.colmean + (b0 + i) * P.N + cc) - __ldg(P.mu + b0 + i) : 0.0f;
-            half_bar(half);
-            const int64_t nbi = nb - b0 < kBch ? nb - b0 : kBch;
-            for (int64_t i = 0; i < nbi; ++i) {
-                const float xs = in ? (float)__ldg(P.xsum + (b0 + i) * P.M + row) : 0.0f;
-                const float* cm = cv + 128 + i * 128;
-                const float2 xs2 = make_float2(xs, xs);
-#pragma unroll
-                for (int j4 = 0; j4 < 128; j4 += 4) {
-                    const float4 c4 = lds4(cm + j4);
-                    const float2 a = f2_fma(xs2, make_float2(c4.x, c4.y), make_float2(acc[j4], acc[j4 + 1]));
-                    const float2 b = f2_fma(xs2, make_float2(c4.z, c4.w), make_float2(acc[j4 + 2], acc[j4 + 3]));
-                    acc[j4 + 0] = a.x;
-                    acc[j4 + 1] = a.y;
-                    acc[j4 + 2] = b.x;
-                    acc[j4 + 3] = b.y;
-                }
+            for (int j4 = 0; j4 < 128; j4 += 4) {
+                const float4 r = lds4(rs + j4), w = lds4(vv + j4);
+                const float2 a = f2_fma(ep2, make_float2(r.x, r.y), make_float2(w.x, w.y));
+                const float2 b = f2_fma(ep2, make_float2(r.z, r.w), make_float2(w.z, w.w));
+                const float2 x = f2_sub(make_float2(acc[j4], acc[j4 + 1]), a);
+                const float2 y = f2_sub(make_float2(acc[j4 + 2], acc[j4 + 3]), b);
+                acc[j4 + 0] = x.x;
+                acc[j4 + 1] = x.y;
+                acc[j4 + 2] = y.x;
+                acc[j4 + 3] = y.y;
             }
         }
+    } else {
+        if (P.ec_mode != S3R_EC_TWO_WAY) return;
+        const int64_t b0 = (int64_t)round * kBch;
+        const int nb = (int)(P.B - b0 < kBch ? P.B - b0 : kBch);
+        for (int b = 0; b < nb; ++b) {
+            const float nx = -sd[SW_XS + b * 128 + rl];
+            const float2 nx2 = make_float2(nx, nx);
+            const float* cm = sd + SW_CM + b * 256 + 128 * half;
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = -acc[j];
+            for (int j4 = 0; j4 < 128; j4 += 4) {
+                const float4 c4 = lds4(cm + j4);
+                const float2 x = f2_fma(nx2, make_float2(c4.x, c4.y), make_float2(acc[j4], acc[j4 + 1]));
+                const float2 y = f2_fma(nx2, make_float2(c4.z, c4.w), make_float2(acc[j4 + 2], acc[j4 + 3]));
+                acc[j4 + 0] = x.x;
+                acc[j4 + 1] = x.y;
+                acc[j4 + 2] = y.x;
+                acc[j4 + 3] = y.y;
+            }
+        }
+        if (round) return;
+        const float pr = sd[SW_P + rl];
+        const float2 pr2 = make_float2(pr, pr);
+#pragma unroll
+        for (int j = 0; j < 128; j += 2) {
+            const float2 x = f2_sub(make_float2(acc[j], acc[j + 1]), pr2);
+            acc[j] = x.x;
+            acc[j + 1] = x.y;
+        }
     }
 }
 
-// Final epilogue of one warp's 32 x 128 block (thread = row, acc = its 128
-// columns from c0, already corrected): the rescale (times 1/s_x[t] or the
-// staged 1/s_w[n]), then 16-column rounds through the warp's staging buffer
-// so that every global access is a 64-byte row segment (accumulate reads
-// included).
-template <int EPI, bool FWD = false>
-__device__ __forceinline__ void finish_tile(const Problem& P, float (&acc)[128], const float* cv, float* stage,
-                                            int64_t row, int64_t c0, int lane) {
-    if (FWD) {
-        // forward: the exact int32 sum converted once, then (acc * s_x[row]) * s_w[col], one
-        // rounding each, columns past N scaled by 1
-#pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = __int2float_rn(__float_as_int(acc[j]));
-        const float fr = row < P.M ? __ldg(P.f_row + row) : 1.0f;
-        const float2 fr2 = make_float2(fr, fr);
-        const bool fvec = (reinterpret_cast<uintptr_t>(P.f_col) & 15u) == 0;
-#pragma unroll
-        for (int j4 = 0; j4 < 128; j4 += 4) {
-            const int64_t col = c0 + j4;
-            const float4 fc = (fvec && col + 4 <= P.N)
-                                  ? __ldg(reinterpret_cast<const float4*>(P.f_col + col))
-                                  : make_float4(col < P.N ? __ldg(P.f_col + col) : 1.0f,
-                                                col + 1 < P.N ? __ldg(P.f_col + col + 1) : 1.0f,
-                                                col + 2 < P.N ? __ldg(P.f_col + col + 2) : 1.0f,
-                                                col + 3 < P.N ? __ldg(P.f_col + col + 3) : 1.0f);
-            const float2 a = f2_mul(f2_mul(make_float2(acc[j4], acc[j4 + 1]), fr2), make_float2(fc.x, fc.y));
-            const float2 b = f2_mul(f2_mul(make_float2(acc[j4 + 2], acc[j4 + 3]), fr2), make_float2(fc.z, fc.w));
-            acc[j4] = a.x;
-            acc[j4 + 1] = a.y;
-            acc[j4 + 2] = b.x;
-            acc[j4 + 3] = b.y;
-        }
-    }
-    if (EPI == kDX && P.s_row) {
-        const float rinv = row < P.M ? __frcp_rn(__ldg(P.s_row + row)) : 1.0f;
-        const float2 r2 = make_float2(rinv, rinv);
+// The final rescale: times 1/s_x[t] (dX) or 1/s_w[n] (dW), from the side data.
+template <int KIND>
+__device__ __forceinline__ void rescale(const Problem& P, float (&acc)[128], const float* sd, int rl, int half) {
+    if (KIND == kDX) {
+        if (!P.s_row) return;
+        const float r = sd[SX_ROWSC + rl];
+        const float2 r2 = make_float2(r, r);
 #pragma unroll
         for (int j = 0; j < 128; j += 2) {
-            const float2 a = f2_mul(make_float2(acc[j], acc[j + 1]), r2);
-            acc[j] = a.x;
-            acc[j + 1] = a.y;
+            const float2 x = f2_mul(make_float2(acc[j], acc[j + 1]), r2);
+            acc[j] = x.x;
+            acc[j + 1] = x.y;
         }
-    }
-    if (EPI == kDW && P.s_col) {
+    } else {
+        if (!P.s_col) return;
+        const float* cs = sd + SW_COLSC + 128 * half;
 #pragma unroll
         for (int j4 = 0; j4 < 128; j4 += 4) {
-            const float4 r = lds4(cv + j4);
-            const float2 a = f2_mul(make_float2(acc[j4], acc[j4 + 1]), make_float2(r.x, r.y));
-            const float2 b = f2_mul(make_float2(acc[j4 + 2], acc[j4 + 3]), make_float2(r.z, r.w));
-            acc[j4 + 0] = a.x;
-            acc[j4 + 1] = a.y;
-            acc[j4 + 2] = b.x;
-            acc[j4 + 3] = b.y;
+            const float4 r = lds4(cs + j4);
+            const float2 x = f2_mul(make_float2(acc[j4], acc[j4 + 1]), make_float2(r.x, r.y));
+            const float2 y = f2_mul(make_float2(acc[j4 + 2], acc[j4 + 3]), make_float2(r.z, r.w));
+            acc[j4 + 0] = x.x;
+            acc[j4 + 1] = x.y;
+            acc[j4 + 2] = y.x;
+            acc[j4 + 3] = y.y;
         }
     }
-    const bool cvec = (P.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(P.C) & 15u) == 0);
-    const bool accum = EPI == kDX && P.accumulate;
-    const int srow = lane >> 2, scol = 4 * (lane & 3);   // store mapping: 8 rows x 4 float4 per instruction
-    const int64_t row0 = row - lane;
-    float* mine = stage + lane * STAGE_PITCH;
+}
+
+// Forward scaling: the exact int32 sum converted once, then (acc * s_x[row]) *
+// s_w[col], one rounding each; columns past N are scaled by 1.
+__device__ __forceinline__ void fwd_scale(const Problem& P, float (&acc)[128], int64_t row, int64_t c0) {
 #pragma unroll
-    for (int c = 0; c < 128 / CHUNK; ++c) {
+    for (int j = 0; j < 128; ++j) acc[j] = __int2float_rn(__float_as_int(acc[j]));
+    const float fr = row < P.M ? __ldg(P.f_row + row) : 1.0f;
+    const float2 fr2 = make_float2(fr, fr);
+    const bool fvec = (reinterpret_cast<uintptr_t>(P.f_col) & 15u) == 0;
 #pragma unroll
-        for (int j4 = 0; j4 < CHUNK; j4 += 4)
-            *reinterpret_cast<float4*>(mine + j4) = make_float4(acc[CHUNK * c + j4], acc[CHUNK * c + j4 + 1],
-                                                                acc[CHUNK * c + j4 + 2], acc[CHUNK * c + j4 + 3]);
-        __syncwarp();
-        const int64_t col = c0 + CHUNK * c + scol;
-#pragma unroll 1
-        for (int r8 = 0; r8 < 4; ++r8) {
-            const int lr = 8 * r8 + srow;
-            const int64_t grow = row0 + lr;
-            if (grow < P.M && col < P.N) {
-                const float4 v4 = lds4(stage + lr * STAGE_PITCH + scol);
-                float w[4] = {v4.x, v4.y, v4.z, v4.w};
-                float* dst = P.C + grow * P.ldc + col;
-                if (cvec && col + 4 <= P.N) {
-                    if (accum) {
-                        const float4 t = *reinterpret_cast<const float4*>(dst);
-                        w[0] += t.x; w[1] += t.y; w[2] += t.z; w[3] += t.w;
-                    }
-                    *reinterpret_cast<float4*>(dst) = make_float4(w[0], w[1], w[2], w[3]);
-                } else {
-                    for (int j = 0; j < 4; ++j)
-                        if (col + j < P.N) dst[j] = accum ? w[j] + dst[j] : w[j];
-                }
+    for (int j4 = 0; j4 < 128; j4 += 4) {
+        const int64_t col = c0 + j4;
+        const float4 fc = (fvec && col + 4 <= P.N)
+                              ? __ldg(reinterpret_cast<const float4*>(P.f_col + col))
+                              : make_float4(col < P.N ? __ldg(P.f_col + col) : 1.0f,
+                                            col + 1 < P.N ? __ldg(P.f_col + col + 1) : 1.0f,
+                                            col + 2 < P.N ? __ldg(P.f_col + col + 2) : 1.0f,
+                                            col + 3 < P.N ? __ldg(P.f_col + col + 3) : 1.0f);
+        const float2 a = f2_mul(f2_mul(make_float2(acc[j4], acc[j4 + 1]), fr2), make_float2(fc.x, fc.y));
+        const float2 b = f2_mul(f2_mul(make_float2(acc[j4 + 2], acc[j4 + 3]), fr2), make_float2(fc.z, fc.w));
+        acc[j4] = a.x;
+        acc[j4 + 1] = a.y;
+        acc[j4 + 2] = b.x;
+        acc[j4 + 3] = b.y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Output: the warp's 32 rows x 128 columns (thread = row) leave through the
+// TMA engine, 8 columns per bulk store: each lane writes its row of 32 bytes
+// into a staging buffer in the 32-byte swizzled layout of the tensor map (the
+// second 16-byte half first on rows 4..7 of every 8), so the writes are free
+// of bank conflicts; lane 0 then issues the store (or an add-reduction when
+// the result accumulates into C).  The TMA engine drops what lies outside C.
+// Two buffers per warp alternate; a buffer is rewritten only after the store
+// that read it has finished reading (bulk async-group wait).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void tma_store(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, bool add) {
+    if (add)
+        asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                         (uint64_t)map),
+                     "r"(x), "r"(y), "r"(src)
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
+                     "r"(x), "r"(y), "r"(src)
+                     : "memory");
+}
+
+// x0: first column of the thread's 128; y0 = row - lane: first row of the warp's 32.
+__device__ __forceinline__ void store_tile(const Problem& P, const CUtensorMap* cmap, const float (&acc)[128],
+                                           uint8_t* obuf, int64_t row, int64_t x0, int lane) {
+    const bool accum = P.accumulate != 0;
+    if (P.c_tma) {
+        const int64_t y0 = row - lane;
+        const int sw = (lane >> 2) & 1;
+#pragma unroll
+        for (int c = 0; c < 128 / OUT_COLS; ++c) {
+            uint8_t* b = obuf + (c & 1) * OUT_BUF_BYTES;
+            if (lane == 0) bulk_wait_read1();   // the store that last read b has read it
+            __syncwarp();
+            float4* r = reinterpret_cast<float4*>(b + lane * 32);
+            r[sw] = make_float4(acc[8 * c + 0], acc[8 * c + 1], acc[8 * c + 2], acc[8 * c + 3]);
+            r[sw ^ 1] = make_float4(acc[8 * c + 4], acc[8 * c + 5], acc[8 * c + 6], acc[8 * c + 7]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int64_t x = x0 + OUT_COLS * c;
+                if (x < P.N && y0 < P.M) tma_store(cmap, su32(b), (int32_t)x, (int32_t)y0, accum);
+                bulk_commit();
             }
         }
-        __syncwarp();
+    } else if (row < P.M) {   // C not addressable by the TMA engine: plain stores
+        float* dst = P.C + row * P.ldc + x0;
+#pragma unroll
+        for (int j = 0; j < 128; ++j)
+            if (x0 + j < P.N) dst[j] = accum ? dst[j] + acc[j] : acc[j];
     }
 }
 
@@ -548,21 +649,24 @@ __device__ __forceinline__ int problem_of(const Args& A, int tile) {
 
 // 12 warps: one SM sub-partition hosts three of them, one per warpgroup, so the
 // launch is capped at 168 registers per thread; after the split a
-// sub-partition holds (40 + 216 + 216) * 32 = 15104 of its 16384.
+// sub-partition holds (56 + 216 + 216) * 32 = 15616 of its 16384.
 template <int EPI, bool MN>
 __global__ void __launch_bounds__(THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args A) {
+    // the side-data protocol (helper warps, correction inside the tile) serves the backward kinds
+    constexpr bool SIDE = EPI == kDX || EPI == kDW || EPI == kMixed;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_STAGE;
-    float* sEpi = reinterpret_cast<float*>(sB + STAGES * B_STAGE);
-    float* sCv = sEpi + EPI_STAGE_BYTES / 4;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sCv) + CV_BYTES);
+    uint8_t* sOut = sB + STAGES * B_STAGE;   // 1024-byte aligned: the swizzle atoms start on it
+    float* sSide = reinterpret_cast<float*>(sOut + OUT_STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sSide + SIDE_FLOATS);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     const uint32_t full0 = su32(bars), empty0 = su32(bars + STAGES), tfull0 = su32(bars + 2 * STAGES),
-                   tempty0 = su32(bars + 2 * STAGES + 2), done_bar = su32(bars + 2 * STAGES + 4);
+                   tempty0 = su32(bars + 2 * STAGES + 2), done_bar = su32(bars + 2 * STAGES + 4),
+                   side_full = su32(bars + 2 * STAGES + 5), side_empty = su32(bars + 2 * STAGES + 6);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = A.total_tiles;   // tile counts fit 32 bits (checked by the host)
@@ -577,6 +681,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(tempty0 + 8 * b, EPI_WARPS);
         }
         mbar_init(done_bar, 1);
+        mbar_init(side_full, 64);          // the 64 helper threads
+        mbar_init(side_empty, EPI_WARPS);  // lane 0 of each epilogue warp
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -707,6 +813,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                 umma_commit(done_bar);
                 mbar_wait_drain(done_bar, 0);
             }
+        } else if (SIDE) {
+            // ------------------------------ helpers (warps 2, 3) ------------------------------
+            // Bring each tile's epilogue vectors into the side buffer as soon as the
+            // epilogue has finished with the previous tile's.
+            const int ht = threadIdx.x - 64;
+            uint32_t sph = 0;   // side-buffer cycles so far (the same count on the epilogue side)
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const Problem& P = A.prob[problem_of(A, tile)];
+                int tm, tn;
+                tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
+                const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
+                const bool dw = EPI == kMixed ? P.kind == kDW : EPI == kDW;
+                const int nr = side_rounds(P, dw);
+                for (int r = 0; r < nr; ++r, ++sph) {
+                    // one outcome for both helper warps: they meet at named barriers below
+                    if (!helper_all(mbar_wait(side_empty, (sph & 1u) ^ 1u, abrt))) {
+                        *abrt = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (dw) load_side<kDW>(P, sSide, m0, n0, ht, r);
+                    else load_side<kDX>(P, sSide, m0, n0, ht, r);
+                    mbar_arrive(side_full);
+                }
+            }
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
@@ -715,43 +847,56 @@ __global__ void __launch_bounds__(THREADS, 1)
         // split the 256 accumulator columns into halves
         const int q = warp & 3, ew = warp - EPI_WARP0, half = ew >> 2;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-        float* stage = sEpi + ew * (32 * STAGE_PITCH);
-        float* cv = sCv + half * CV_FLOATS;
-        const int ht = 32 * q + lane;   // thread index within the half
+        uint8_t* obuf = sOut + ew * (2 * OUT_BUF_BYTES);
+        const int rl = 32 * q + lane;   // row within the tile
         int gkb = 0;
+        uint32_t sph = 0;   // side-buffer cycles so far (the same count on the helper side)
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const Problem& P = A.prob[problem_of(A, tile)];
+            const int pi = problem_of(A, tile);
+            const Problem& P = A.prob[pi];
             const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
             const int nkb = nkb0 + nkb1;
             int tm, tn;
             tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
             const int mt = tm, nt = tn * 2 + half;   // 128-wide tile indices
-            const int64_t row = (int64_t)mt * BM + 32 * q + lane;
+            const int64_t m0 = (int64_t)mt * BM;
+            const int64_t row = m0 + rl;
             const bool gate = EPI == kFwdE && P.kind == kGate;
+            const bool is_dw = EPI == kMixed ? P.kind == kDW : EPI == kDW;
             // gate: this half owns output columns c0 .. c0 + 63, accumulators
             // 0..63 = h1 (TMEM columns 64 half ..), 64..127 = h3 (128 + 64 half ..)
             const int64_t c0 = gate ? (int64_t)tn * 128 + 64 * half : (int64_t)nt * 128;
             const uint32_t col_base = (uint32_t)(gate ? 64 * half : 128 * half);
             const uint32_t col_step = gate ? 128u - 64u : 0u;   // extra offset of chunks 4..7
             float acc[128];
-            if (EPI == kFwdE) {
 #pragma unroll
-                for (int j = 0; j < 128; ++j) acc[j] = 0.0f;   // int32 zero
-            } else if (EPI == kMixed) {
-                if (P.kind != kDW) seed_tile<kDX>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
-                else seed_tile<kDW>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
-            } else if (EPI != kDump) {
-                seed_tile<EPI>(P, acc, cv, row, (int64_t)mt * BM, c0, half, ht);
-            }
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;   // (int32 zero for the forward)
+            // the correction enters after block kc (all its rounds); the last
+            // round's side data stays for the final rescale
+            const int kc = nkb - 1 < kCorrBlock ? nkb - 1 : kCorrBlock;
+            const int nr = SIDE ? side_rounds(P, is_dw) : 0;
+            auto correct = [&]() -> bool {
+                for (int r = 0; r < nr; ++r) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(side_full, sph & 1u, abrt))) return false;
+                    if (is_dw) apply_correction<kDW>(P, acc, sSide, row, m0, rl, half, r);
+                    else apply_correction<kDX>(P, acc, sSide, row, m0, rl, half, r);
+                    if (r + 1 < nr) {   // hand the buffer back for the next round
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(side_empty);
+                        ++sph;
+                    }
+                }
+                return true;
+            };
             // scale of block kb, loaded one block ahead
             auto scale_of = [&](int kb) -> float {
                 if (EPI == kDump) return 0.0f;
                 const bool first = kb < nkb0;
-                const int64_t k = first ? kb : kb - nkb0;
+                const int64_t kk = first ? kb : kb - nkb0;
                 const float* base = first ? P.seg[0].scale : P.seg[1].scale;
-                const int64_t off = first ? mt * P.seg[0].sm + nt * P.seg[0].sn + k * P.seg[0].sk
-                                          : mt * P.seg[1].sm + nt * P.seg[1].sn + k * P.seg[1].sk;
+                const int64_t off = first ? mt * P.seg[0].sm + nt * P.seg[0].sn + kk * P.seg[0].sk
+                                          : mt * P.seg[1].sm + nt * P.seg[1].sn + kk * P.seg[1].sk;
                 const int64_t lim = first ? P.seg[0].nt_limit : P.seg[1].nt_limit;
                 return nt < lim ? __ldg(base + off) : 0.0f;
             };
@@ -820,18 +965,36 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                if (SIDE && kb == kc && !correct()) {   // after the TMEM hand-back: the MMA runs on meanwhile
+                    ok = false;
+                    *abrt = 1;
+                    break;
+                }
             }
             if (EPI == kDump || !ok) continue;
-            if (EPI == kFwdE) {
-                if (gate) finish_gate(P, acc, row, c0);
-                else finish_tile<kDX, true>(P, acc, cv, stage, row, c0, lane);
-            } else if (EPI == kMixed) {
-                if (P.kind != kDW) finish_tile<kDX>(P, acc, cv, stage, row, c0, lane);
-                else finish_tile<kDW>(P, acc, cv, stage, row, c0, lane);
-            } else {
-                finish_tile<EPI>(P, acc, cv, stage, row, c0, lane);
+            if (SIDE) {
+                if (nkb == 0 && !correct()) {   // no block ran: the correction alone
+                    ok = false;
+                    *abrt = 1;
+                    continue;
+                }
+                if (is_dw) rescale<kDW>(P, acc, sSide, rl, half);
+                else rescale<kDX>(P, acc, sSide, rl, half);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(side_empty);   // the helpers may refill the side buffer
+                ++sph;
+                store_tile(P, &maps.m[pi][4], acc, obuf, row, c0, lane);
+            } else if (EPI == kFwdE) {
+                if (gate) {
+                    finish_gate(P, acc, row, c0);
+                } else {
+                    fwd_scale(P, acc, row, c0);
+                    store_tile(P, &maps.m[pi][4], acc, obuf, row, c0, lane);
+                }
             }
         }
+        // every bulk store has finished before the CTA (and its staging buffers) goes away
+        if (lane == 0) bulk_wait_all();
     }
     __syncthreads();
     if (warp == 1) {
@@ -882,6 +1045,34 @@ static int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t out
         s3r_record_error("tensor map", buf);
         return S3R_ERR_CUDA;
     }
+    return S3R_OK;
+}
+
+// The output C [rows, cols] fp32 (row stride ldc elements) for the TMA stores
+// of the epilogue: box 8 columns x 32 rows, 32-byte swizzle.  Leaves
+// P.c_tma = 0 (plain stores) when C cannot be described (row stride or base
+// not 16-byte aligned).
+static int make_out_map(CUtensorMap* m, Problem& P) {
+    P.c_tma = 0;
+    if (!P.C || P.M <= 0 || P.N <= 0 || P.ldc % 4 != 0 || (reinterpret_cast<uintptr_t>(P.C) & 15u) != 0)
+        return S3R_OK;
+    auto fn = encode_fn();
+    if (!fn) return S3R_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)P.N, (cuuint64_t)P.M};
+    cuuint64_t strides[1] = {(cuuint64_t)P.ldc * 4};
+    cuuint32_t box[2] = {(cuuint32_t)OUT_COLS, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.C, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[200];
+        snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled returned %d for the output (%lld x %lld, stride %lld)",
+                 (int)r, (long long)P.M, (long long)P.N, (long long)P.ldc);
+        s3r_record_error("tensor map", buf);
+        return S3R_ERR_CUDA;
+    }
+    P.c_tma = 1;
     return S3R_OK;
 }
 
@@ -1012,6 +1203,8 @@ static int add_dx_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDxPr
     if (two) dx_segment(P.seg[1], q.tile_scale3, N, q.eps3, q.rowsum3, q.v3);
     P.C = q.dX; P.ldc = K; P.dump = q.dump; P.s_row = q.s_x; P.ec_mode = ecm; P.S = S;
     P.accumulate = q.accumulate;
+    st = q.dump ? S3R_OK : umma::make_out_map(&m[4], P);
+    if (st) return st;
     // bytes per row strip of A (BM rows of Q over the contraction) and per column strip of B (BN rows of W)
     const double kbytes = 2.0 * (double)N * (two ? 2 : 1);
     strip[0] = umma::BM * kbytes;
@@ -1038,6 +1231,8 @@ static int add_dw_problem(umma::Maps& maps, umma::Args& A, int i, const UmmaDwPr
     P.C = q.dW; P.ldc = N; P.dump = q.dump; P.s_col = q.s_w; P.S = S;
     P.ec_mode = q.ec_mode == S3R_EC_DW_ONLY ? S3R_EC_TWO_WAY : q.ec_mode;   // dW carries the whole correction
     P.B = q.S > 0 ? T / q.S : 1; P.colmean = q.colmean; P.mu = q.mu; P.xsum = q.xsum; P.p = q.p;
+    st = q.dump ? S3R_OK : umma::make_out_map(&m[4], P);
+    if (st) return st;
     const double kbytes = 2.0 * (double)T;   // per output row / column over the contraction
     strip[0] = umma::BM * kbytes;
     strip[1] = umma::BN * kbytes;
@@ -1068,6 +1263,10 @@ static int add_fwd_problem(umma::Maps& maps, umma::Args& A, int i, const void* X
     g.scale = nullptr; g.sm = g.sn = g.sk = 0; g.nt_limit = INT64_MAX; g.K = K;
     P.f_row = s_x; P.f_col = s_w; P.f_col3 = s_w3;
     P.C = Y; P.ldc = N; P.S = T;
+    if (!gate) {
+        st = umma::make_out_map(&m[4], P);
+        if (st) return st;
+    }
     if (gate)
         for (int j = 0; j < 3; ++j) P.gate_out[j] = gate_out[j];
     strip[0] = umma::BM * 2.0 * (double)K;
