@@ -505,18 +505,28 @@ __device__ __forceinline__ bool xs_wait(uint32_t bar, uint32_t parity) {
 // workspace (gemv items first, the larger ones), else strided over the CTAs:
 //   gemv (linear j, examples BCH g .. BCH g + BCH - 1, weight rows 32 rb ..
 //     32 rb + 31): boxes of 32 rows x 256 channels of W8_j, each with the
-//     matching BCH x 256 slab of colmean_j; warp w keeps rows w + 8 i (i < 4), lane l channels
-//     8 l .. 8 l + 7, and after the last box the lanes meet in a butterfly.
-//     The sums of codes are exact in fp32 (|sum| <= 127 N < 2^24).
+//     matching BCH x 256 slab of colmean_j; consumer warp w keeps rows w and
+//     w + 16, lane l channels 8 l .. 8 l + 7, and after the last box the
+//     lanes meet in a reduce-scatter and the warp stores its two rows.  The
+//     sums of codes are exact in fp32 (|sum| <= 127 N < 2^24).
 //   xsum (256-column block cb, chunk c of XR rows of X8): XR / 64 boxes of
 //     64 rows x 256 columns, each with the matching 64 entries of eps_j; warp
-//     w takes rows w + 8 i, lane l columns 8 l .. 8 l + 7; chunk partials go
-//     to the workspace and the last chunk of a column block (a counter, no
-//     waiting) adds them in a fixed order, one column per thread.
-// A TMA engine keeps kEsStages boxes in flight; a box's stage is refilled
-// once every thread has passed the next box's wait.  mu_b of every linear is
-// computed by each CTA in the same fixed order (the same bits everywhere).
+//     w takes rows w + 16 i, lane l columns 8 l .. 8 l + 7; after the last
+//     box the 16 warps meet in shared memory (a written / read mbarrier pair)
+//     and add their partials in warp order into the chunk's workspace row.
+// Warp 16 is the producer.  One lane takes item ids from the queue one item
+// ahead (the atomic's latency hides behind the copies), posts each id in a
+// small ring before the item's first copy, and keeps kEsStages boxes in
+// flight; a stage is refilled once all 16 consumer warps have released it.
+// Consumer warps wait for every box on their own and never meet the producer
+// in a CTA barrier.  Every wait is bounded and gives up early once another
+// warp has raised the CTA's abort flag.  After a grid barrier (bounded) every
+// thread of the grid takes a share of the fixed-order sums over the chunks.
+// mu_b of every linear is computed by each CTA in the same fixed order (the
+// same bits everywhere) while the first copies land.
 // ---------------------------------------------------------------------------
+constexpr int kEsConsumers = 16;                              // consumer warps
+constexpr int kEsThreads = 32 * (kEsConsumers + 1);           // plus the producer warp
 constexpr int kEsStages = 5;
 constexpr int kEsXRowsBox = 64, kEsWRows = 32;
 constexpr int kEsCmOff = kEsWRows * 256 * 2;             // colmean slab after the 16 KiB of weight codes
@@ -524,6 +534,14 @@ constexpr int kEsEpsOff = kEsXRowsBox * 256 * 2;         // eps slices after the
 constexpr int kEsStageBytes = kEsEpsOff + kMaxJobs * kEsXRowsBox * 4;
 constexpr int kEsQueue = 8;                              // item ids in flight per CTA
 constexpr int kEsMaxB = 1024;                            // examples whose mu a CTA holds
+
+// Dynamic shared memory: ring (128-byte aligned) | full and empty barriers of
+// the stages, the exchange's two barriers | the exchange [16][(1 + nj) 256]
+// floats | mu [nj][B].
+static size_t es_smem_bytes(int nj, int64_t B) {
+    return 128 + (size_t)kEsStages * kEsStageBytes + (2 * kEsStages + 2) * 8 +
+           (size_t)kEsConsumers * 256 * (1 + nj) * 4 + (size_t)nj * (size_t)B * 4;
+}
 
 struct EcStreamArgs {
     int64_t T, K, N, S, B;
@@ -540,7 +558,7 @@ struct EcStreamArgs {
     int64_t ncb, nch;  // column blocks and chunks of the input-side pass
     int xr;            // rows per chunk (128, 256 or 512)
     int64_t ngr;       // weight row blocks per linear
-    int ngroups;       // example groups of kEsBch
+    int ngroups;       // example groups of BCH
     int64_t nbn;       // channel boxes per weight row block
     int64_t n_gemv, n_items;
     int mu_v4;         // eps 16-byte aligned and S % 4 == 0: vector loads for mu
@@ -557,36 +575,72 @@ __device__ __forceinline__ void es_tma(uint32_t dst, const CUtensorMap* map, int
 __device__ __forceinline__ void es_tma1(uint32_t dst, const CUtensorMap* map, int32_t x, uint32_t bar) {
     es_tma(dst, map, x, 0, bar);
 }
+__device__ __forceinline__ void es_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// the consumer warps' named barrier (the producer warp never takes part)
+__device__ __forceinline__ void es_consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEsConsumers) : "memory");
+}
+// Bounded wait (2 s of %globaltimer) that also gives up once the CTA's abort flag is up.
+__device__ __forceinline__ bool es_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    const uint64_t t0 = ec_gtime();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (*abort_flag || ec_gtime() - t0 > 2000000000ull) return false;
+    }
+}
 
-// mu[b] = (1/S) sum_{t < S} e[b S + t] for every b < B over a 256-thread CTA
-// in a fixed order: per-thread strided sums, a butterfly in each warp, then
-// the eight warps in order.  red holds 64 floats.
-__device__ void cta_mu256(const float* e, int64_t S, int64_t B, float* red, float* out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// mu[b] = (1/S) sum_{t < S} e[b S + t] for every b < B over the 512 consumer
+// threads in a fixed order: per-thread strided sums (float4 loads when V4),
+// a butterfly in each warp, then the 16 warps in order.  red holds 8 x 16 floats.
+template <bool V4>
+__device__ void es_mu(const float* e, int64_t S, int64_t B, float* red, float* out) {
+    constexpr int NT = 32 * kEsConsumers;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int64_t b0 = 0; b0 < B; b0 += 8) {
         float s[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) s[q] = 0.0f;
-#pragma unroll 4
-        for (int64_t t = threadIdx.x; t < S; t += 256) {
+        if (V4) {
+#pragma unroll 2
+            for (int64_t i = 4 * tid; i < S; i += 4 * NT) {
+                float4 v[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (b0 + q < B) s[q] += e[(b0 + q) * S + t];
+                for (int q = 0; q < 8; ++q)
+                    v[q] = b0 + q < B ? __ldg(reinterpret_cast<const float4*>(e + (b0 + q) * S + i))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) s[q] += (v[q].x + v[q].y) + (v[q].z + v[q].w);
+            }
+        } else {
+#pragma unroll 4
+            for (int64_t t = tid; t < S; t += NT) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (b0 + q < B) s[q] += e[(b0 + q) * S + t];
+            }
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) s[q] += __shfl_xor_sync(0xFFFFFFFFu, s[q], o);
-            if (lane == 0) red[q * 8 + warp] = s[q];
+            if (lane == 0) red[q * kEsConsumers + warp] = s[q];
         }
-        __syncthreads();
-        if (threadIdx.x < 8 && b0 + threadIdx.x < B) {
+        es_consumers_sync();
+        if (tid < 8 && b0 + tid < B) {
             float m = 0.0f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) m += red[threadIdx.x * 8 + w];
-            out[b0 + threadIdx.x] = m / (float)S;
+            for (int w = 0; w < kEsConsumers; ++w) m += red[tid * kEsConsumers + w];
+            out[b0 + tid] = m / (float)S;
         }
-        __syncthreads();
+        es_consumers_sync();
     }
 }
 
@@ -620,202 +674,175 @@ __device__ __forceinline__ float warp_scatter(const float (&v)[V]) {
     return a[0];
 }
 
-// The same means from float4 loads (e 16-byte aligned, S a multiple of 4):
-// every load of eight examples is in flight at once.
-__device__ void cta_mu256_v4(const float* e, int64_t S, int64_t B, float* red, float* out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int64_t b0 = 0; b0 < B; b0 += 8) {
-        float s[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) s[q] = 0.0f;
-#pragma unroll 2
-        for (int64_t i = 4 * threadIdx.x; i < S; i += 1024) {
-            float4 v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                v[q] = b0 + q < B ? __ldg(reinterpret_cast<const float4*>(e + (b0 + q) * S + i))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) s[q] += (v[q].x + v[q].y) + (v[q].z + v[q].w);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s[q] += __shfl_xor_sync(0xFFFFFFFFu, s[q], o);
-            if (lane == 0) red[q * 8 + warp] = s[q];
-        }
-        __syncthreads();
-        if (threadIdx.x < 8 && b0 + threadIdx.x < B) {
-            float m = 0.0f;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) m += red[threadIdx.x * 8 + w];
-            out[b0 + threadIdx.x] = m / (float)S;
-        }
-        __syncthreads();
-    }
-}
-
 template <int NJ, int BCH>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kEsThreads, 1)
     ec_stream_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                      const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmC0,
                      const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmE0,
                      const __grid_constant__ CUtensorMap tmE1, EcStreamArgs A) {
-    constexpr int P = 33;
+    constexpr int NA = 1 + NJ;   // column-sum arrays: xs, then ps of each linear
     extern __shared__ uint8_t es_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(es_raw) + 127) & ~(uintptr_t)127);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + kEsStages * kEsStageBytes);   // copies landed
-    uint64_t* empty = full + kEsStages;                                                // all warps done
-    float* mu_s = reinterpret_cast<float*>(empty + kEsStages);   // [NJ][B]
-    __shared__ float red_p[NJ][8][8 * P];
-    __shared__ float red_x[8][8 * P];
-    __shared__ float mred[64];
+    uint64_t* empty = full + kEsStages;                                                // consumers done
+    uint64_t* xbar = empty + kEsStages;   // exchange: [0] partials written, [1] partials read
+    float* red = reinterpret_cast<float*>(xbar + 2);              // [16][NA][256]
+    float* mu_s = red + kEsConsumers * NA * 256;                  // [NJ][B]
+    __shared__ float mred[8 * kEsConsumers];
     __shared__ int q_item[kEsQueue];
     __shared__ int last;
+    __shared__ int abort_s;
+    volatile int* abort_flag = &abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t K = A.K, B = A.B;
-    int* queue = A.counter;
     const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(full);
     const uint32_t ebar0 = (uint32_t)__cvta_generic_to_shared(empty);
-    // producer state (thread 0): the next item id (fetched one item ahead, so the
-    // queue's latency hides behind the copies), the current item decoded once,
-    // and the box of the next copy
+    const uint32_t xbar0 = (uint32_t)__cvta_generic_to_shared(xbar);
     const int n_items = (int)A.n_items, n_gemv = (int)A.n_gemv, ngr = (int)A.ngr, ncb = (int)A.ncb;
     const int per_j = ngr * A.ngroups;
-    int p_fetched = 0;
-    auto fetch = [&]() -> int {
-        const int it = queue ? atomicAdd(queue, 1) : (int)blockIdx.x + p_fetched * (int)gridDim.x;
-        ++p_fetched;
-        return it < n_items ? it : -1;
-    };
-    int p_next = -1, p_box = 0, p_nbox = 0, p_ord = 0;
-    bool p_done = false, p_gemv = false;
-    const CUtensorMap *p_m0 = nullptr, *p_m1 = nullptr;
-    int32_t p_x = 0, p_y = 0, p_y1 = 0;
-    int issued = 0;   // boxes (and end marks) issued
-    auto issue_next = [&]() {
-        const int s = issued % kEsStages;
-        const uint32_t bar = bar0 + 8 * s;
-        uint8_t* dst = ring + s * kEsStageBytes;
-        if (p_box == p_nbox) {   // the next item, or the end mark
-            const int item = p_next;
-            q_item[p_ord % kEsQueue] = item;
-            ++p_ord;
-            p_box = 0;
-            if (item < 0) {
-                p_done = true;
-                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-                ++issued;
-                return;
-            }
-            p_next = fetch();
-            p_gemv = item < n_gemv;
-            if (p_gemv) {
-                const int j = item / per_j, rem = item - j * per_j;
-                const int g = rem / ngr, rb = rem - g * ngr;
-                p_m0 = j ? &tmW1 : &tmW0;
-                p_m1 = j ? &tmC1 : &tmC0;
-                p_y = rb * kEsWRows;
-                p_y1 = g * BCH;
-                p_nbox = (int)A.nbn;
-            } else {
-                const int xi = item - n_gemv, c = xi / ncb, cb = xi - c * ncb;
-                p_x = cb * 256;
-                p_y = c * A.xr;
-                p_nbox = A.xr / kEsXRowsBox;
-            }
-        }
-        if (p_gemv) {
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kEsCmOff + BCH * 256 * 4)
-                         : "memory");
-            es_tma((uint32_t)__cvta_generic_to_shared(dst), p_m0, p_box * 256, p_y, bar);
-            es_tma((uint32_t)__cvta_generic_to_shared(dst + kEsCmOff), p_m1, p_box * 256, p_y1, bar);
-        } else {
-            const int32_t y = p_y + p_box * kEsXRowsBox;
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                         "r"(kEsEpsOff + NJ * kEsXRowsBox * 4)
-                         : "memory");
-            es_tma((uint32_t)__cvta_generic_to_shared(dst), &tmX, p_x, y, bar);
-            es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff), &tmE0, y, bar);
-            if (NJ > 1) es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff + kEsXRowsBox * 4), &tmE1, y, bar);
-        }
-        ++p_box;
-        ++issued;
-    };
     if (tid == 0) {
         for (int i = 0; i < kEsStages; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * i) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(ebar0 + 8 * i) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ebar0 + 8 * i), "n"(kEsConsumers) : "memory");
         }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(xbar0), "n"(kEsConsumers) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(xbar0 + 8), "n"(kEsConsumers) : "memory");
+        abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const CUtensorMap* maps[7] = {&tmX, &tmW0, &tmW1, &tmC0, &tmC1, &tmE0, &tmE1};
-        for (int i = 0; i < 7; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)maps[i]) : "memory");
-        p_next = fetch();
     }
-    // mu_b of every linear (fixed order, the same bits in every CTA) while the first copies land
-    for (int j = 0; j < NJ; ++j) {
-        if (A.mu_v4) cta_mu256_v4(A.eps[j], A.S, B, mred, mu_s + j * B);
-        else cta_mu256(A.eps[j], A.S, B, mred, mu_s + j * B);
-    }
-    if (blockIdx.x == 0)
-        for (int j = 0; j < NJ; ++j)
-            for (int64_t b = tid; b < B; b += 256) A.mu[j][b] = mu_s[j * B + b];
-    // the ring fills once the means' loads are back (they would queue behind the copies)
-    if (tid == 0)
-        for (int i = 0; i < kEsStages && !p_done; ++i) issue_next();
     __syncthreads();
-    int k = 0;        // boxes consumed
-    int ord = 0;      // items consumed
-    bool ok = true;   // every wait of this thread so far succeeded (after a failure it waits no more)
-    // Thread 0 refills the stage of box k - 1 as soon as every warp has left it
-    // (its empty barrier); then each thread waits for box k itself, so warps
-    // run ahead of each other within an item.  The CTA agrees on success at
-    // every item start (and before the column-sum counters).
-    auto wait_own = [&]() {
-        if (tid == 0 && k > 0 && !p_done && ok) {
-            const int q = k - 1;
-            if (xs_wait(ebar0 + 8 * (q % kEsStages), (uint32_t)((q / kEsStages) & 1))) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue_next();
-            } else {
-                ok = false;
+    bool failed = false;
+    int issued = 0;   // boxes (and the end mark) issued: the producer lane's count
+    if (warp == kEsConsumers) {
+        // ---- producer (one lane) ----
+        if (lane == 0) {
+            const CUtensorMap* maps[7] = {&tmX, &tmW0, &tmW1, &tmC0, &tmC1, &tmE0, &tmE1};
+            for (int i = 0; i < 7; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)maps[i]) : "memory");
+            int p_fetched = 0;
+            auto fetch = [&]() -> int {
+                const int it = A.counter ? atomicAdd(A.counter, 1) : (int)blockIdx.x + p_fetched * (int)gridDim.x;
+                ++p_fetched;
+                return it < n_items ? it : -1;
+            };
+            int p_next = fetch(), p_box = 0, p_nbox = 0, p_ord = 0;
+            bool p_gemv = false;
+            const CUtensorMap *p_m0 = nullptr, *p_m1 = nullptr;
+            int32_t p_x = 0, p_y = 0, p_y1 = 0;
+            while (true) {
+                const int s = issued % kEsStages;
+                if (issued >= kEsStages) {
+                    if (!es_wait(ebar0 + 8 * s, (uint32_t)(((issued / kEsStages) - 1) & 1), abort_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                const uint32_t bar = bar0 + 8 * s;
+                uint8_t* dst = ring + s * kEsStageBytes;
+                if (p_box == p_nbox) {   // the next item, or the end mark
+                    const int item = p_next;
+                    q_item[p_ord % kEsQueue] = item;
+                    ++p_ord;
+                    p_box = 0;
+                    if (item < 0) {
+                        es_arrive(bar);
+                        ++issued;
+                        break;
+                    }
+                    p_next = fetch();
+                    p_gemv = item < n_gemv;
+                    if (p_gemv) {
+                        const int j = item / per_j, rem = item - j * per_j;
+                        const int g = rem / ngr, rb = rem - g * ngr;
+                        p_m0 = j ? &tmW1 : &tmW0;
+                        p_m1 = j ? &tmC1 : &tmC0;
+                        p_y = rb * kEsWRows;
+                        p_y1 = g * BCH;
+                        p_nbox = (int)A.nbn;
+                    } else {
+                        const int xi = item - n_gemv, c = xi / ncb, cb = xi - c * ncb;
+                        p_x = cb * 256;
+                        p_y = c * A.xr;
+                        p_nbox = A.xr / kEsXRowsBox;
+                    }
+                }
+                if (p_gemv) {
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                                 "r"(kEsCmOff + BCH * 256 * 4)
+                                 : "memory");
+                    es_tma((uint32_t)__cvta_generic_to_shared(dst), p_m0, p_box * 256, p_y, bar);
+                    es_tma((uint32_t)__cvta_generic_to_shared(dst + kEsCmOff), p_m1, p_box * 256, p_y1, bar);
+                } else {
+                    const int32_t y = p_y + p_box * kEsXRowsBox;
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                                 "r"(kEsEpsOff + NJ * kEsXRowsBox * 4)
+                                 : "memory");
+                    es_tma((uint32_t)__cvta_generic_to_shared(dst), &tmX, p_x, y, bar);
+                    es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff), &tmE0, y, bar);
+                    if (NJ > 1)
+                        es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff + kEsXRowsBox * 4), &tmE1, y, bar);
+                }
+                ++p_box;
+                ++issued;
             }
         }
-        if (ok) ok = xs_wait(bar0 + 8 * (k % kEsStages), (uint32_t)((k / kEsStages) & 1));
-    };
-    // every warp marks the box it finished
-    auto box_done = [&]() {
-        __syncwarp();
-        if (lane == 0)
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ebar0 + 8 * (k % kEsStages)) : "memory");
-        ++k;
-    };
-    bool failed = false;
-    while (true) {
-        wait_own();
-        if (!__syncthreads_and(ok)) { failed = true; break; }
-        const int item = q_item[ord % kEsQueue];
-        if (item < 0) { ++k; break; }   // the end mark (no copy behind it, no refill after it)
-        ++ord;
-        if (item < n_gemv) {
-            const int j = item / per_j, rem = item - j * per_j;
-            const int g = rem / ngr;
-            const int64_t rb = rem - g * ngr;
-            const float* mu_j = mu_s + j * B;
-            // accumulators over channel pairs (2e, 2e + 1), one per row and example
-            float2 acc[4][BCH], rs[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                rs[i] = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int q = 0; q < BCH; ++q) acc[i][q] = make_float2(0.0f, 0.0f);
+    } else {
+        // ---- consumers ----
+        for (int j = 0; j < NJ; ++j) {
+            if (A.mu_v4) es_mu<true>(A.eps[j], A.S, B, mred, mu_s + j * B);
+            else es_mu<false>(A.eps[j], A.S, B, mred, mu_s + j * B);
+        }
+        if (blockIdx.x == 0)
+            for (int j = 0; j < NJ; ++j)
+                for (int64_t b = tid; b < B; b += 32 * kEsConsumers) A.mu[j][b] = mu_s[j * B + b];
+        int k = 0;    // boxes consumed
+        int ord = 0;  // items consumed
+        int nx = 0;   // input-side items consumed (phases of the exchange)
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) es_arrive(ebar0 + 8 * (k % kEsStages));
+            ++k;
+        };
+        while (!failed) {
+            if (!es_wait(bar0 + 8 * (k % kEsStages), (uint32_t)((k / kEsStages) & 1), abort_flag)) {
+                failed = true;
+                break;
             }
-            for (int bx = 0; bx < (int)A.nbn; ++bx) {
-                if (bx > 0) wait_own();
-                if (ok) {
+            const int item = q_item[ord % kEsQueue];
+            if (item < 0) break;   // the end mark (no copy behind it, no refill after it)
+            ++ord;
+            if (item < n_gemv) {
+                const int j = item / per_j, rem = item - j * per_j;
+                const int g = rem / ngr;
+                const int64_t rb = rem - g * ngr;
+                const float* mu_j = mu_s + j * B;
+                // accumulators over channel pairs (2e, 2e + 1), one per row and example
+                float2 acc[2][BCH], rs[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    rs[i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int q = 0; q < BCH; ++q) acc[i][q] = make_float2(0.0f, 0.0f);
+                }
+                for (int bx = 0; bx < (int)A.nbn; ++bx) {
+                    if (bx > 0 && !es_wait(bar0 + 8 * (k % kEsStages), (uint32_t)((k / kEsStages) & 1), abort_flag)) {
+                        failed = true;
+                        break;
+                    }
                     const uint8_t* st = ring + (k % kEsStages) * kEsStageBytes;
-                    // centered channel means of my 8 channels (past N and past B the copies read zero)
-                    float2 cm2[BCH][4];
+                    float2 x2[2][4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(st + ((warp + 16 * i) * 256 + 8 * lane) * 2);
+                        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            x2[i][e] = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
+                            rs[i] = f2_add(rs[i], x2[i][e]);
+                        }
+                    }
+                    // centered channel means of my 8 channels, one example at a time (past N and
+                    // past B the copies read zero)
 #pragma unroll
                     for (int q = 0; q < BCH; ++q) {
                         const int64_t b = (int64_t)g * BCH + q;
@@ -824,68 +851,57 @@ __global__ void __launch_bounds__(256, 1)
                         const float4 c0 = *reinterpret_cast<const float4*>(st + kEsCmOff + (q * 256 + 8 * lane) * 4);
                         const float4 c1 =
                             *reinterpret_cast<const float4*>(st + kEsCmOff + (q * 256 + 8 * lane + 4) * 4);
-                        cm2[q][0] = f2_sub(make_float2(c0.x, c0.y), m2);
-                        cm2[q][1] = f2_sub(make_float2(c0.z, c0.w), m2);
-                        cm2[q][2] = f2_sub(make_float2(c1.x, c1.y), m2);
-                        cm2[q][3] = f2_sub(make_float2(c1.z, c1.w), m2);
+                        const float2 cm2[4] = {f2_sub(make_float2(c0.x, c0.y), m2), f2_sub(make_float2(c0.z, c0.w), m2),
+                                               f2_sub(make_float2(c1.x, c1.y), m2), f2_sub(make_float2(c1.z, c1.w), m2)};
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[i][q] = f2_fma(cm2[e], x2[i][e], acc[i][q]);
                     }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(st + ((warp + 8 * i) * 256 + 8 * lane) * 2);
-                        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 x2 = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
-                            rs[i] = f2_add(rs[i], x2);
-#pragma unroll
-                            for (int q = 0; q < BCH; ++q) acc[i][q] = f2_fma(cm2[q][e], x2, acc[i][q]);
-                        }
-                    }
+                    release();
                 }
-                box_done();
-            }
-            // row sums: integers, one reduction each; v: a reduce-scatter of the 4 x BCH values,
-            // after which lane l holds value l / (32 / (4 BCH)) = (row, example) in row-major order
-            {
-                int ri[4];
+                if (failed) break;
+                // row sums: integers, one reduction each; v: a reduce-scatter of the 2 x BCH values,
+                // after which lane l holds value l / (32 / (2 BCH)) = (row, example) in row-major order
+                int ri[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) ri[i] = __reduce_add_sync(0xFFFFFFFFu, (int)(rs[i].x + rs[i].y));
-                float vv[4 * BCH];
+                for (int i = 0; i < 2; ++i) ri[i] = __reduce_add_sync(0xFFFFFFFFu, (int)(rs[i].x + rs[i].y));
+                float vv[2 * BCH];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
                     for (int q = 0; q < BCH; ++q) vv[i * BCH + q] = acc[i][q].x + acc[i][q].y;
-                const float vsum = warp_scatter<4 * BCH>(vv);
-                constexpr int G = 32 / (4 * BCH);   // lanes per value
+                const float vsum = warp_scatter<2 * BCH>(vv);
+                constexpr int G = 32 / (2 * BCH);   // lanes per value
                 const int vi = lane / G, i = vi / BCH, q = vi - i * BCH;
-                const int64_t kr = rb * kEsWRows + warp + 8 * i;
+                const int64_t kr = rb * kEsWRows + warp + 16 * i;
                 const int64_t b = (int64_t)g * BCH + q;
-                if (ok && lane % G == 0 && kr < K && b < B) A.v[j][b * K + kr] = vsum;
-                if (ok && lane < 4 && g == 0) {
-                    const int64_t kr2 = rb * kEsWRows + warp + 8 * lane;
-                    const int rsel = lane == 0 ? ri[0] : lane == 1 ? ri[1] : lane == 2 ? ri[2] : ri[3];
-                    if (kr2 < K) A.rowsum[j][kr2] = rsel;
+                if (lane % G == 0 && kr < K && b < B) A.v[j][b * K + kr] = vsum;
+                if (lane < 2 && g == 0) {
+                    const int64_t kr2 = rb * kEsWRows + warp + 16 * lane;
+                    if (kr2 < K) A.rowsum[j][kr2] = lane ? ri[1] : ri[0];
                 }
-            }
-        } else {
-            const int xi = item - n_gemv;
-            const int64_t c = xi / ncb, cb = xi - c * ncb;
-            float2 sx[4], sp[NJ][4];
+            } else {
+                const int xi = item - n_gemv;
+                const int64_t c = xi / ncb, cb = xi - c * ncb;
+                float2 sx[4], sp[NJ][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                sx[q] = make_float2(0.f, 0.f);
+                for (int q = 0; q < 4; ++q) {
+                    sx[q] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) sp[jj][q] = make_float2(0.f, 0.f);
-            }
-            const int nb = A.xr / kEsXRowsBox;
-            for (int bx = 0; bx < nb; ++bx) {
-                if (bx > 0) wait_own();
-                if (ok) {
+                    for (int jj = 0; jj < NJ; ++jj) sp[jj][q] = make_float2(0.f, 0.f);
+                }
+                const int nb = A.xr / kEsXRowsBox;
+                for (int bx = 0; bx < nb; ++bx) {
+                    if (bx > 0 && !es_wait(bar0 + 8 * (k % kEsStages), (uint32_t)((k / kEsStages) & 1), abort_flag)) {
+                        failed = true;
+                        break;
+                    }
                     const uint8_t* st = ring + (k % kEsStages) * kEsStageBytes;
                     const float* es = reinterpret_cast<const float*>(st + kEsEpsOff);   // zero past T
 #pragma unroll
-                    for (int i = 0; i < kEsXRowsBox / 8; ++i) {
-                        const int r = warp + 8 * i;
+                    for (int i = 0; i < kEsXRowsBox / kEsConsumers; ++i) {
+                        const int r = warp + kEsConsumers * i;
                         const uint4 w = *reinterpret_cast<const uint4*>(st + (r * 256 + 8 * lane) * 2);
                         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
                         float e[NJ];
@@ -900,49 +916,58 @@ __global__ void __launch_bounds__(256, 1)
                                 sp[jj][q] = f2_fma(x, make_float2(e[jj], e[jj]), sp[jj][q]);
                         }
                     }
+                    release();
                 }
-                box_done();
-            }
-            // the chunk's column sums: warps meet in shared memory in warp order
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                red_x[warp][(2 * q) * P + lane] = sx[q].x;
-                red_x[warp][(2 * q + 1) * P + lane] = sx[q].y;
-#pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) {
-                    red_p[jj][warp][(2 * q) * P + lane] = sp[jj][q].x;
-                    red_p[jj][warp][(2 * q + 1) * P + lane] = sp[jj][q].y;
+                if (failed) break;
+                // the chunk's column sums: the 16 warps meet in shared memory and add up in warp order
+                if (nx > 0 && !es_wait(xbar0 + 8, (uint32_t)((nx - 1) & 1), abort_flag)) {   // last item's sums read
+                    failed = true;
+                    break;
                 }
-            }
-            // every wait of the chunk succeeded, or the CTA leaves before touching the counters
-            if (!__syncthreads_and(ok)) { failed = true; break; }
-            const int64_t kcol = cb * 256 + tid;
-            const int slot = (tid & 7) * P + (tid >> 3);
-            if (kcol < K) {
-                float xb = 0.0f;
-                float a[NJ];
+                {
+                    float* mine = red + warp * NA * 256 + 8 * lane;
+                    *reinterpret_cast<float4*>(mine) = make_float4(sx[0].x, sx[0].y, sx[1].x, sx[1].y);
+                    *reinterpret_cast<float4*>(mine + 4) = make_float4(sx[2].x, sx[2].y, sx[3].x, sx[3].y);
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) a[jj] = 0.0f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    xb += red_x[w][slot];
-#pragma unroll
-                    for (int jj = 0; jj < NJ; ++jj) a[jj] += red_p[jj][w][slot];
+                    for (int jj = 0; jj < NJ; ++jj) {
+                        float* pj = mine + (1 + jj) * 256;
+                        *reinterpret_cast<float4*>(pj) = make_float4(sp[jj][0].x, sp[jj][0].y, sp[jj][1].x, sp[jj][1].y);
+                        *reinterpret_cast<float4*>(pj + 4) =
+                            make_float4(sp[jj][2].x, sp[jj][2].y, sp[jj][3].x, sp[jj][3].y);
+                    }
                 }
-                A.xs[c * K + kcol] = (int32_t)xb;
+                __syncwarp();
+                if (lane == 0) es_arrive(xbar0);
+                if (!es_wait(xbar0, (uint32_t)(nx & 1), abort_flag)) {   // every warp's partials written
+                    failed = true;
+                    break;
+                }
+                for (int vi = tid; vi < NA * 256; vi += 32 * kEsConsumers) {
+                    const int a = vi >> 8, col = vi & 255;
+                    float sum = 0.0f;
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) A.ps[(jj * A.nch + c) * K + kcol] = a[jj];
+                    for (int w = 0; w < kEsConsumers; ++w) sum += red[(w * NA + a) * 256 + col];
+                    const int64_t kcol = cb * 256 + col;
+                    if (kcol < K) {
+                        if (a == 0) A.xs[c * K + kcol] = (int32_t)sum;
+                        else A.ps[((int64_t)(a - 1) * A.nch + c) * K + kcol] = sum;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) es_arrive(xbar0 + 8);
+                ++nx;
             }
-            // red_x and red_p are rewritten only after the next item start's barrier
         }
     }
-    if (failed && tid == 0 && A.d_status) *(volatile int*)A.d_status = S3R_ERR_TIMEOUT;
+    if (failed) {
+        *abort_flag = 1;
+        if (A.d_status) *(volatile int*)A.d_status = S3R_ERR_TIMEOUT;
+    }
+    __syncthreads();
     if (A.done) {
         // Every CTA of the (cooperative, co-resident) grid has written its chunk
-        // partials: meet at a grid barrier (one counter, bounded wait), then the
-        // CTAs share out the column blocks and add the chunks up in a fixed
-        // order, one column per thread.
-        __syncthreads();
+        // partials: meet at a grid barrier (one counter, bounded wait), then
+        // every thread of the grid adds up its share of the chunks in a fixed order.
         if (tid == 0) {
             __threadfence();
             atomicAdd(A.done, 1);
@@ -954,44 +979,77 @@ __global__ void __launch_bounds__(256, 1)
                 met = v >= (int)gridDim.x;
                 if (!met && ec_gtime() - t0 > 2000000000ull) break;
             }
-            last = met;
+            last = met && !*abort_flag;
             if (!met && A.d_status) *(volatile int*)A.d_status = S3R_ERR_TIMEOUT;
         }
         __syncthreads();
         if (last) {
             __threadfence();
-            const int64_t cpe = B == 1 ? A.nch : A.S / A.xr;
-            for (int64_t cb = blockIdx.x; cb < A.ncb; cb += gridDim.x) {
-                const int64_t kcol = cb * 256 + tid;
-                if (kcol >= K) continue;
-                float pk[NJ];
-#pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
-                for (int64_t b = 0; b < B; ++b) {
-                    int xbi = 0;
+            const int64_t cpe = B == 1 ? A.nch : A.S / A.xr;   // chunks per example
+            const int64_t gthreads = (int64_t)gridDim.x * kEsThreads;
+            const int64_t gtid = (int64_t)blockIdx.x * kEsThreads + tid;
+            if (B <= 32 && (B & (B - 1)) == 0) {
+                // a warp takes 32 / B columns, one lane per (column, example): the example's
+                // chunks in order, then p over the B lanes of the column in a butterfly
+                const int cpw = 32 / (int)B;
+                const int64_t nwarps = gthreads >> 5;
+                const int b = lane % (int)B;
+                for (int64_t base = (gtid >> 5) * cpw; base < K; base += nwarps * cpw) {
+                    const int64_t kcol = base + lane / (int)B;
+                    const bool on = kcol < K;
+                    int xb = 0;
                     float pb[NJ];
 #pragma unroll
                     for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
-#pragma unroll 16
-                    for (int64_t cc = b * cpe; cc < (b + 1) * cpe; ++cc) {
-                        xbi += __ldcg(A.xs + cc * K + kcol);
+                    if (on) {
+#pragma unroll 8
+                        for (int64_t cc = b * cpe; cc < (b + 1) * cpe; ++cc) {
+                            xb += __ldcg(A.xs + cc * K + kcol);
 #pragma unroll
-                        for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * A.nch + cc) * K + kcol);
-                    }
+                            for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * A.nch + cc) * K + kcol);
+                        }
 #pragma unroll
-                    for (int jj = 0; jj < NJ; ++jj) {
-                        A.xsum[jj][b * K + kcol] = xbi;
-                        pk[jj] += pb[jj];
+                        for (int jj = 0; jj < NJ; ++jj) A.xsum[jj][b * K + kcol] = xb;
                     }
+                    for (int o = (int)B / 2; o >= 1; o >>= 1)
+#pragma unroll
+                        for (int jj = 0; jj < NJ; ++jj) pb[jj] += __shfl_xor_sync(0xFFFFFFFFu, pb[jj], o);
+                    if (on && b == 0)
+#pragma unroll
+                        for (int jj = 0; jj < NJ; ++jj) A.p[jj][kcol] = pb[jj];
                 }
+            } else {
+                for (int64_t kcol = gtid; kcol < K; kcol += gthreads) {
+                    float pk[NJ];
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) A.p[jj][kcol] = pk[jj];
+                    for (int jj = 0; jj < NJ; ++jj) pk[jj] = 0.0f;
+                    for (int64_t b2 = 0; b2 < B; ++b2) {
+                        int xbi = 0;
+                        float pb[NJ];
+#pragma unroll
+                        for (int jj = 0; jj < NJ; ++jj) pb[jj] = 0.0f;
+#pragma unroll 8
+                        for (int64_t cc = b2 * cpe; cc < (b2 + 1) * cpe; ++cc) {
+                            xbi += __ldcg(A.xs + cc * K + kcol);
+#pragma unroll
+                            for (int jj = 0; jj < NJ; ++jj) pb[jj] += __ldcg(A.ps + (jj * A.nch + cc) * K + kcol);
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < NJ; ++jj) {
+                            A.xsum[jj][b2 * K + kcol] = xbi;
+                            pk[jj] += pb[jj];
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) A.p[jj][kcol] = pk[jj];
+                }
             }
         }
     }
-    // an early exit may leave copies in flight: wait for them before leaving
-    if (tid == 0)
-        for (int q = k; q < issued; ++q) xs_wait(bar0 + 8 * (q % kEsStages), (uint32_t)((q / kEsStages) & 1));
+    // an early exit may leave copies in flight: the producer waits for them before leaving
+    if (*abort_flag && warp == kEsConsumers && lane == 0)
+        for (int q = issued > kEsStages ? issued - kEsStages : 0; q < issued; ++q)
+            xs_wait(bar0 + 8 * (q % kEsStages), (uint32_t)((q / kEsStages) & 1));
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 ec_encode_fn() {
@@ -1013,20 +1071,20 @@ static int ec_sm_count() { return s3r_sm_count(); }
 
 template <int NJ, int BCH>
 static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, size_t smem, cudaStream_t stream) {
-    const int st = s3r_kernel_smem((const void*)ec_stream_kernel<NJ, BCH>,
-                                   (int)(kEsStages * kEsStageBytes + 128 + 128 + kMaxJobs * kEsMaxB * 4),
+    const int st = s3r_kernel_smem((const void*)ec_stream_kernel<NJ, BCH>, (int)es_smem_bytes(NJ, kEsMaxB),
                                    "ec stream: cudaFuncSetAttribute");
     if (st) return st;
     int64_t grid = std::min<int64_t>(S.n_items, ec_sm_count());
     if (!S.done) {
-        ec_stream_kernel<NJ, BCH><<<(unsigned)grid, 256, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                                          maps[5], maps[6], S);
+        ec_stream_kernel<NJ, BCH><<<(unsigned)grid, kEsThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                                 maps[4], maps[5], maps[6], S);
         S3R_CHECK_LAUNCH();
         return S3R_OK;
     }
     // the column-sum pass ends with a grid barrier: a cooperative launch keeps every CTA resident
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ec_stream_kernel<NJ, BCH>, 256, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ec_stream_kernel<NJ, BCH>, kEsThreads, smem) !=
+            cudaSuccess ||
         per_sm < 1) {
         (void)cudaGetLastError();
         return 1;
@@ -1037,7 +1095,7 @@ static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, si
     for (int i = 0; i < 7; ++i) m[i] = maps[i];
     void* args[8] = {&m[0], &m[1], &m[2], &m[3], &m[4], &m[5], &m[6], &a};
     const cudaError_t e = cudaLaunchCooperativeKernel((const void*)ec_stream_kernel<NJ, BCH>, dim3((unsigned)grid),
-                                                      dim3(256), args, smem, stream);
+                                                      dim3(kEsThreads), args, smem, stream);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return s3r_cuda_fail("ec stream: cudaLaunchCooperativeKernel", e);
@@ -1046,9 +1104,6 @@ static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, si
     return S3R_OK;
 }
 
-// fp16 codes with 16-byte aligned rows: rowsum, v, mu (and, two-way, xsum and
-// p) in one streaming launch.  Returns 1 when it does not apply.
-// weight: rowsum and v are wanted (weight-side items); two: xsum and p (input-side items).
 static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
                             bool weight, bool two, int32_t* xs, float* ps, int* counter, int* d_status,
                             cudaStream_t stream) {
@@ -1127,7 +1182,7 @@ static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int
     A.mu_v4 = S % 4 == 0;
     for (int j = 0; j < nj; ++j) A.mu_v4 = A.mu_v4 && s3r_aligned16(jobs[j].eps);
     if (A.n_items >= (int64_t(1) << 30)) return 1;
-    const size_t smem = kEsStages * kEsStageBytes + 128 + 128 + (size_t)nj * B * 4;
+    const size_t smem = es_smem_bytes(nj, B);
     if (nj == 2) {
         if (bch == 1) return launch_ec_stream_t<2, 1>(maps, A, smem, stream);
         if (bch == 4) return launch_ec_stream_t<2, 4>(maps, A, smem, stream);
