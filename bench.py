@@ -42,11 +42,17 @@ CFG = workloads.WORKLOADS[WORKLOAD]
 T, D, F, S = CFG["T"], CFG["d"], CFG["F"], CFG["S"]
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM launches of one
-# ffn_backward step of the timed block, per GEMM product, from one ncu capture of the step's
-# launch list on a GB300 (the command is in the design notes); keyed by the sha256 of the GEMM
-# source it was taken on, so that it is reported only while that kernel is unchanged.
-GEMM_TRAFFIC = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the two GEMM launches of one
+# ffn_backward step, divided by the step's six products, from a one-pass ncu capture of
+#   python bench.py --kernel-case ffn --block <block> --steps 1 --warmup 1
+# on a GB300; keyed by the sha256 of the GEMM source it was taken on, so that it is reported
+# only while that kernel is unchanged, then by block.
+GEMM_TRAFFIC = {
+    "c3099914d96ba9add3d5578b0e1215e73f418bf866539570108f4d7ec566a124": {
+        "swiglu_ffn_d4096_F14336_T16384": 2331.5e6,   # dA + dW2 4643 MB, dX1 + dX3 + dW1 + dW3 9346 MB
+        "swiglu_ffn_d2048_F5632_T8192": 208.2e6,      # 428.5 MB and 820.8 MB
+    },
+}
 
 
 def parse():
@@ -173,6 +179,12 @@ class Block:
         self.T, self.d, self.F, self.S = w["T"], w["d"], w["F"], w["S"]
         self.data_seed = data_seed
         self.flops_per_product = 2.0 * self.T * self.d * self.F   # each of the six GEMM products of a step
+        # algorithmic bytes of the six products (each reads its two code operands once and writes its
+        # fp32 output once; dX1 and dX3 share one dX), averaged per product
+        T, d, F = self.T, self.d, self.F
+        step = ((2 * T * d + 2 * F * d + 4 * T * F) + (2 * T * F + 2 * T * d + 4 * F * d)
+                + 2 * (2 * T * F + 2 * F * d) + 4 * T * d + 2 * (2 * T * d + 2 * T * F + 4 * d * F))
+        self.gemm_bytes_per_product = step / 6.0
 
     def inputs(self, rank=0):
         return workloads.ffn_inputs(self.T, self.d, self.F, self.S, seed=self.data_seed + 1000 * rank)
@@ -322,16 +334,26 @@ def gemm_roofline(blk, seg, pk, pk_kind):
             "avg_us_per_product": round(gemm_ms / 6 * 1e3, 1)}
 
 
-def gemm_traffic():
-    """DRAM bytes per GEMM product from the recorded ncu capture, or None when
-    the GEMM source changed since it was taken."""
+def gemm_traffic(blk):
+    """DRAM bytes per GEMM product of block `blk` from the recorded ncu capture,
+    or None when the GEMM source changed since it was taken."""
     import hashlib
     src = os.path.join(ROOT, "stochastic_rounding_int8_gb300", "csrc", "gemm_umma.cu")
     try:
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
-    return GEMM_TRAFFIC.get(h)
+    return GEMM_TRAFFIC.get(h, {}).get(blk.name)
+
+
+def add_traffic(roof, blk):
+    """The GEMM class's recorded DRAM traffic per product next to its algorithmic bytes."""
+    tr = gemm_traffic(blk)
+    roof["traffic"] = tr
+    roof["algorithmic_bytes_per_product"] = round(blk.gemm_bytes_per_product)
+    roof["traffic_over_algorithmic"] = round(tr / blk.gemm_bytes_per_product, 3) if tr else None
+    roof["traffic_note"] = ("DRAM read + write bytes per GEMM product of this block from a one-pass ncu capture of "
+                            "the step's two GEMM launches; null when the GEMM source changed since")
 
 
 def block_line(s3r, blk, inp, ops, dY, steps, warmup, world, pk, pk_kind):
@@ -588,9 +610,7 @@ def run_ours(args, world, rank, local):
     r = block_line(s3r, blk, inp, ops, dY, args.steps, args.warmup, world, pk, pk_kind)
     clk = clocks.stop()
     roof = r["roofline"]
-    roof["traffic"] = gemm_traffic()
-    roof["traffic_note"] = ("DRAM read + write bytes per GEMM product of this block from an ncu capture of the "
-                            "step's launch list; null when the GEMM source changed since")
+    add_traffic(roof, blk)
     line = {
         "metric": METRIC, "value": round(r["tokens_s"], 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4),
@@ -620,12 +640,13 @@ def run_ours(args, world, rank, local):
             "bf16_ms": round(fw["bf16_cublas_forward"]["ms"] + ctx["bf16_cublas_backward"]["ms"], 4)}
         del ops, dY, inp
         torch.cuda.empty_cache()
-        # the smaller block as its own line (the round's earlier headline shape)
+        # the smaller block as its own line
         sb = SMALL
         sinp = sb.inputs()
         sops = device_ops(s3r, sinp)
         sdY = sinp.dY.cuda()
         rs = block_line(s3r, sb, sinp, sops, sdY, 20, 3, 1, pk, pk_kind)
+        add_traffic(rs["roofline"], sb)
         sctx = {"tokens_s": round(rs["tokens_s"], 1), "ms_per_step": round(rs["ms_per_step"], 4),
                 "ms_per_step_median": round(rs["ms_per_step_median"], 4),
                 "step_breakdown_ms": rs["step_breakdown_ms"], "roofline": rs["roofline"]}

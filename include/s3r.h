@@ -585,6 +585,19 @@ int s3r_debug_dx_blocks(const void* Q, const void* W8, int code_format, int64_t 
 int s3r_debug_dw_blocks(const void* X8, const void* Q, int code_format, int64_t T, int64_t K, int64_t N,
                         int32_t* out_dw, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Test hook for the reciprocal inside the SwiGLU glue (sigma = 1 / (1 + e)
+ * of the SwiGLU block, [S3R] section IV-A), which must equal the IEEE
+ * quotient bit for bit so that the codes downstream of the glue match an
+ * implementation that divides: counts the floats
+ * whose bit patterns lie in [lo_bits, hi_bits) (positive, finite, lo_bits <
+ * hi_bits <= 0x7F800000) for which the kernels' reciprocal differs from the
+ * correctly rounded IEEE reciprocal, adding the count into *d_count (device
+ * memory, caller-owned, one unsigned 64-bit integer).  Asynchronous on
+ * `stream`.  S3R_ERR_ARG for an invalid range or a NULL d_count.
+ */
+int s3r_check_reciprocal(uint32_t lo_bits, uint32_t hi_bits, unsigned long long* d_count, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -81,6 +81,7 @@ _SIGS = {
     "ffn_backward": (_INT, [_VP, _VP]),
     "s3r_ffn_workspace_offsets": (_INT, [_I64, _I64, _I64, _I64, _INT, _INT, _VP, _I64, _I64, _VP]),
     "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP]),
+    "s3r_check_reciprocal": (_INT, [_U32, _U32, _VP, _VP]),
     "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
 }
 
@@ -372,6 +373,14 @@ def int8_gemm_dw(X8, Q, tile_scale, s_w=None, ec_mode=EC_NONE, ec: ECFactors | N
                               _ptr(ec.xsum if two else None), _ptr(ec.p if two else None), S, _ptr(dW),
                               _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)), "int8_gemm_dw")
     return dW
+
+
+def check_reciprocal(lo_bits, hi_bits, device="cuda", stream=None) -> int:
+    """Floats with bit patterns in [lo_bits, hi_bits) whose reciprocal in the
+    SwiGLU glue differs from the IEEE one (test hook)."""
+    count = torch.zeros(1, dtype=torch.int64, device=device)
+    _check(lib().s3r_check_reciprocal(lo_bits, hi_bits, _ptr(count), _stream(stream)), "s3r_check_reciprocal")
+    return int(count.item())
 
 
 def debug_dx_blocks(Q, W8, stream=None):

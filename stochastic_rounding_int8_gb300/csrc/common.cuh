@@ -189,6 +189,22 @@ __device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
 // rounding mode) and the low byte of the sum's bits is that integer mod 256.
 constexpr float kMagic = 12582912.0f;
 
+// 1 / d correctly rounded for d in [1, 2^126): the hardware approximation
+// (within one ulp) refined by one Newton-Raphson step on the residual,
+// y + y (1 - d y) with both operations fused (Markstein's correction).  An
+// exhaustive GPU comparison over every float in [1, 2^126) found it equal to
+// the IEEE reciprocal; larger d (a result below the normal range, where the
+// approximation flushes) takes the IEEE reciprocal itself.
+static __device__ __noinline__ float2 rcp2_ieee(float2 d) { return make_float2(__frcp_rn(d.x), __frcp_rn(d.y)); }
+__device__ __forceinline__ float2 rcp2_den(float2 d) {
+    if (fmaxf(d.x, d.y) >= 0x1p126f) return rcp2_ieee(d);
+    float2 y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.x) : "f"(d.x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.y) : "f"(d.y));
+    const float2 e = f2_fma(make_float2(-d.x, -d.y), y, make_float2(1.0f, 1.0f));
+    return f2_fma(e, y, y);
+}
+
 // sigmoid_cw of two lanes at once, per lane bit-identical to sigmoid_cw (exp_cw
 // of -x, the correctly rounded reciprocal standing for the IEEE quotient
 // 1 / (1 + e)).
@@ -212,13 +228,15 @@ __device__ __forceinline__ float2 sigmoid2(float2 x) {
     poly = f2_fma(poly, r, make_float2(0.5f, 0.5f));
     poly = f2_fma(poly, r, make_float2(1.0f, 1.0f));
     poly = f2_fma(poly, r, make_float2(1.0f, 1.0f));
-    const int bm = (int)__float_as_uint(kMagic) - 127;
-    const float2 two_n = make_float2(__int_as_float(((int)__float_as_uint(tm0) - bm) << 23),
-                                     __int_as_float(((int)__float_as_uint(tm1) - bm) << 23));
+    // 2^n = (bits(tm) - bits(kMagic) + 127) << 23 (0x4B400000 = bits of kMagic), as one multiply-add
+    // on the bits (mod 2^32)
+    constexpr uint32_t kExpBias = (uint32_t)(127 - (int)0x4B400000) << 23;
+    const float2 two_n = make_float2(__uint_as_float(__float_as_uint(tm0) * 8388608u + kExpBias),
+                                     __uint_as_float(__float_as_uint(tm1) * 8388608u + kExpBias));
     // (1 + poly 2^n may fuse into an fma: a product with a power of two is exact.)
     const float2 e = f2_mul(poly, two_n);
     const float2 den = f2_add(make_float2(1.0f, 1.0f), e);
-    return make_float2(__frcp_rn(den.x), __frcp_rn(den.y));
+    return rcp2_den(den);
 }
 
 // The SwiGLU derivative terms of two lanes at once, per lane bit-identical to

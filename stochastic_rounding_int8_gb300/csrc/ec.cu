@@ -58,29 +58,46 @@ struct EcMeansArgs {
 };
 
 // eps[t] = (sum_j tok[t, j]) / N ;  colmean[b, n] = (sum_{tile rows i of b} col[i, n]) / S
-// (blockIdx.y selects the linear).
-__global__ void ec_means_kernel(EcMeansArgs A) {
+// (blockIdx.y selects the linear).  The first kMeansTokBlocks(T) blocks take
+// eight tokens each, one warp per token: lane-strided sums over the token's
+// tile partials (coalesced), then a butterfly; the rest take one (b, n) each,
+// summing the example's tile rows in order.
+constexpr int kMeansTokPerBlock = 8;
+__host__ __device__ inline int64_t means_tok_blocks(int64_t T) { return (T + kMeansTokPerBlock - 1) / kMeansTokPerBlock; }
+__global__ void __launch_bounds__(256) ec_means_kernel(EcMeansArgs A) {
     const int j = blockIdx.y;
     const float* tok = j ? A.tok[1] : A.tok[0];
     const float* col = j ? A.col[1] : A.col[0];
     float* eps = j ? A.eps[1] : A.eps[0];
     float* colmean = j ? A.colmean[1] : A.colmean[0];
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t T = A.T, N = A.N, S = A.S, B = T / S;
     if (A.counter && blockIdx.x == 0 && j == 0)
         for (int c = threadIdx.x; c < A.ncounter; c += blockDim.x) A.counter[c] = 0;
-    if (i < T) {
-        float s = 0.0f;
-        for (int64_t c = 0; c < A.ntc; ++c) s += tok[i * A.ntc + c];
-        eps[i] = s / (float)N;
-    } else if (i < T + B * N) {
-        const int64_t k = i - T, b = k / N, n = k % N;
-        int64_t r_begin, r_end;
-        if (B == 1) { r_begin = 0; r_end = A.ntr; }
-        else { r_begin = b * (S / kTile); r_end = (b + 1) * (S / kTile); }
-        float s = 0.0f;
-        for (int64_t r = r_begin; r < r_end; ++r) s += col[r * N + n];
-        colmean[b * N + n] = s / (float)S;
+    const int64_t tb = means_tok_blocks(T);
+    if ((int64_t)blockIdx.x < tb) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int64_t t = (int64_t)blockIdx.x * kMeansTokPerBlock + warp;
+        if (t < T) {
+            const float* row = tok + t * A.ntc;
+            float s = 0.0f;
+#pragma unroll 4
+            for (int64_t c = lane; c < A.ntc; c += 32) s += row[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            if (lane == 0) eps[t] = s / (float)N;
+        }
+    } else {
+        const int64_t k = ((int64_t)blockIdx.x - tb) * blockDim.x + threadIdx.x;
+        if (k < B * N) {
+            const int64_t b = k / N, n = k % N;
+            int64_t r_begin, r_end;
+            if (B == 1) { r_begin = 0; r_end = A.ntr; }
+            else { r_begin = b * (S / kTile); r_end = (b + 1) * (S / kTile); }
+            float s = 0.0f;
+#pragma unroll 8
+            for (int64_t r = r_begin; r < r_end; ++r) s += col[r * N + n];
+            colmean[b * N + n] = s / (float)S;
+        }
     }
 }
 
@@ -575,6 +592,16 @@ __device__ __forceinline__ void es_tma(uint32_t dst, const CUtensorMap* map, int
 __device__ __forceinline__ void es_tma1(uint32_t dst, const CUtensorMap* map, int32_t x, uint32_t bar) {
     es_tma(dst, map, x, 0, bar);
 }
+// A copy of streamed codes, read once: marked first to leave L2, so the chunk
+// partials written meanwhile (and read back after the grid barrier) stay.
+__device__ __forceinline__ void es_tma_stream(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void es_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -724,6 +751,8 @@ __global__ void __launch_bounds__(kEsThreads, 1)
                 ++p_fetched;
                 return it < n_items ? it : -1;
             };
+            uint64_t evict_first;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
             int p_next = fetch(), p_box = 0, p_nbox = 0, p_ord = 0;
             bool p_gemv = false;
             const CUtensorMap *p_m0 = nullptr, *p_m1 = nullptr;
@@ -770,14 +799,14 @@ __global__ void __launch_bounds__(kEsThreads, 1)
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                                  "r"(kEsCmOff + BCH * 256 * 4)
                                  : "memory");
-                    es_tma((uint32_t)__cvta_generic_to_shared(dst), p_m0, p_box * 256, p_y, bar);
+                    es_tma_stream((uint32_t)__cvta_generic_to_shared(dst), p_m0, p_box * 256, p_y, bar, evict_first);
                     es_tma((uint32_t)__cvta_generic_to_shared(dst + kEsCmOff), p_m1, p_box * 256, p_y1, bar);
                 } else {
                     const int32_t y = p_y + p_box * kEsXRowsBox;
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                                  "r"(kEsEpsOff + NJ * kEsXRowsBox * 4)
                                  : "memory");
-                    es_tma((uint32_t)__cvta_generic_to_shared(dst), &tmX, p_x, y, bar);
+                    es_tma_stream((uint32_t)__cvta_generic_to_shared(dst), &tmX, p_x, y, bar, evict_first);
                     es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff), &tmE0, y, bar);
                     if (NJ > 1)
                         es_tma1((uint32_t)__cvta_generic_to_shared(dst + kEsEpsOff + kEsXRowsBox * 4), &tmE1, y, bar);
@@ -1240,7 +1269,7 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
         M.T = T; M.N = N; M.S = S; M.ntc = ntc; M.ntr = ntr;
         M.counter = two ? counter : nullptr;
         M.ncounter = (int)ncb + 2;   // the column blocks, then the streaming kernel's work queue and grid barrier
-        dim3 grid((unsigned)s3r_cdiv(T + B * N, 256), (unsigned)nj);
+        dim3 grid((unsigned)(means_tok_blocks(T) + s3r_cdiv(B * N, 256)), (unsigned)nj);
         ec_means_kernel<<<grid, 256, 0, stream>>>(M);
         S3R_CHECK_LAUNCH();
     }

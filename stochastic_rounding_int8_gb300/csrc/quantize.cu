@@ -1719,3 +1719,32 @@ extern "C" int swiglu_quantize_ex(const float* dA, int64_t ldd, const void* h1, 
     S3R_CHECK_LAUNCH();
     return S3R_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Test hook: the glue's reciprocal against the IEEE one over a range of bit
+// patterns (grid-stride, one atomic per thread with a mismatch).
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void __launch_bounds__(256) check_reciprocal_kernel(uint32_t lo, uint32_t hi, unsigned long long* count) {
+    const uint64_t n = (uint64_t)(hi - lo);
+    unsigned long long bad = 0;
+    for (uint64_t i = 2 * ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x); i < n;
+         i += 2 * (uint64_t)gridDim.x * blockDim.x) {
+        const float a = __uint_as_float(lo + (uint32_t)i);
+        const float b = i + 1 < n ? __uint_as_float(lo + (uint32_t)i + 1) : a;
+        const float2 r = s3r::rcp2_den(make_float2(a, b));
+        bad += __float_as_uint(r.x) != __float_as_uint(__frcp_rn(a));
+        bad += __float_as_uint(r.y) != __float_as_uint(__frcp_rn(b));
+    }
+    if (bad) atomicAdd(count, bad);
+}
+}  // namespace
+
+extern "C" int s3r_check_reciprocal(uint32_t lo_bits, uint32_t hi_bits, unsigned long long* d_count,
+                                    cudaStream_t stream) {
+    if (!d_count || lo_bits >= hi_bits || hi_bits > 0x7F800000u || lo_bits == 0u) return S3R_ERR_ARG;
+    const int grid = s3r_sm_count() * 8;
+    check_reciprocal_kernel<<<grid, 256, 0, stream>>>(lo_bits, hi_bits, d_count);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}

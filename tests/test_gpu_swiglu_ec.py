@@ -129,3 +129,14 @@ def test_streaming_paths_are_taken(s3r):
     n4 = s3r.kernel_launch_count()
     torch.cuda.synchronize()
     assert (n1 - n0, n2 - n1, n3 - n2, n4 - n3) == (1, 2, 2, 1)
+
+
+def test_glue_reciprocal_equals_ieee_everywhere(s3r):
+    """sigma = 1 / (1 + e) in the glue ([S3R] section IV-A's SwiGLU block) uses
+    the hardware reciprocal approximation refined by one Newton-Raphson step,
+    with the IEEE reciprocal for results below the normal range.  1 + e lies in
+    [1, 1 + e^88], so every float from 1.0 to the largest finite one is checked
+    against the correctly rounded reciprocal: no difference anywhere."""
+    one, two126, top = 0x3F800000, 0x7E800000, 0x7F800000
+    assert s3r.check_reciprocal(one, two126) == 0
+    assert s3r.check_reciprocal(two126, top) == 0
