@@ -69,6 +69,8 @@ def parse():
                     help="profiling helper: run one kernel of a block --steps times, print a short line")
     ap.add_argument("--block", choices=[WORKLOAD, SMALL_BLOCK], default=SMALL_BLOCK,
                     help="--kernel-case: which FFN block (default: the smaller one, for ncu captures)")
+    ap.add_argument("--fuse-glue", action="store_true",
+                    help="--kernel-case ffn: the SwiGLU glue inside the dA GEMM's epilogue (S3R_FFN_FUSE_GLUE)")
     return ap.parse_args()
 
 
@@ -203,17 +205,18 @@ def device_ops(s3r, inp, code_format=None):
     return ops
 
 
-def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False):
+def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse=False):
     """Device time of `steps` ffn_backward calls on resident inputs: total ms
     between two events around the loop, launches counted by the library, and
-    (events=True) each step's per-step-boundary event times [steps, 8]."""
+    (events=True) each step's per-step-boundary event times [steps, 8].
+    fuse: the SwiGLU glue inside the dA GEMM's epilogue."""
     T, d, F, S = blk.T, blk.d, blk.F, blk.S
     ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, rm, ec, s3r.code_format_of(ops.X8)), dtype=torch.uint8,
                      device="cuda")
     grads = s3r.alloc_ffn_grads(T, d, F)
     st = s3r.new_status()
     for i in range(warmup):
-        s3r.ffn_backward(ops, dY, S, rm, ec, seed=i, grads=grads, workspace=ws, status=st)
+        s3r.ffn_backward(ops, dY, S, rm, ec, seed=i, grads=grads, workspace=ws, status=st, fuse_glue=fuse)
     step_ev = None
     if events:
         step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(s3r.FFN_NUM_EVENTS)] for _ in range(steps)]
@@ -227,7 +230,7 @@ def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False):
     t0.record()
     for i in range(steps):
         s3r.ffn_backward(ops, dY, S, rm, ec, seed=1000 + i, grads=grads, workspace=ws, status=st,
-                         step_events=step_ev[i] if events else None)
+                         step_events=step_ev[i] if events else None, fuse_glue=fuse)
     t1.record()
     torch.cuda.synchronize()
     launches = s3r.kernel_launch_count() - n0
@@ -380,6 +383,10 @@ def mode_context(s3r, blk, ops, dY, inp, steps=8, warmup=2):
                          ("s3r_ec_dw_only", s3r.ROUND_S3R, s3r.EC_DW_ONLY)):
         m, _, _ = time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, 1)
         ctx[name] = {"tokens_s": round(blk.T * steps / (m * 1e-3), 1), "ms": round(m / steps, 4)}
+    # the SwiGLU glue inside the dA GEMM's epilogue (S3R_FFN_FUSE_GLUE) against the separate kernel
+    m, _, seg = time_ffn(s3r, blk, ops, dY, steps, warmup, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1, events=True, fuse=True)
+    ctx["s3r_ec_two_way_fused_glue"] = {"tokens_s": round(blk.T * steps / (m * 1e-3), 1), "ms": round(m / steps, 4),
+                                        "dA_dW2_launch_ms": round(float(seg[:, 2].mean()), 4)}
     ops8 = device_ops(s3r, inp, s3r.CODES_S8)
     m, _, _ = time_ffn(s3r, blk, ops8, dY, 3, 1, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1)
     ctx["s3r_ec_two_way_int8_storage_mma_sync"] = {"tokens_s": round(blk.T * 3 / (m * 1e-3), 1), "ms": round(m / 3, 4)}
@@ -689,7 +696,7 @@ def run_kernel_case(args):
     if args.kernel_case == "ffn":
         ws = torch.empty(s3r.ffn_workspace_size(T, D, F, S), dtype=torch.uint8, device="cuda")
         grads = s3r.alloc_ffn_grads(T, D, F)
-        fns["ffn"] = lambda: s3r.ffn_backward(ops, dY, S, grads=grads, workspace=ws)
+        fns["ffn"] = lambda: s3r.ffn_backward(ops, dY, S, grads=grads, workspace=ws, fuse_glue=args.fuse_glue)
     if args.kernel_case == "moe":
         w = workloads.WORKLOADS["moe_e8_d4096_F1408_tok16384_top2"]
         mi = workloads.moe_inputs(w["tokens"], w["topk"], w["experts"], w["d"], w["F"], seed=workloads.DATA_SEED + 5)

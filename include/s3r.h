@@ -485,6 +485,16 @@ int ffn_forward(const struct s3r_ffn_fwd_args* args, cudaStream_t stream);
  * events 4 and 8 then follow 3 and 7 directly.
  * Independent SR quantizes each gradient twice (tensor ids + 0x100 for the
  * dW copy) and applies no correction; RTNE applies no correction either.
+ *
+ * flags & S3R_FFN_FUSE_GLUE (dense block, fp16 codes, round_mode S3R,
+ * S3R_7BIT, BCAST or RTNE; ignored otherwise): step 5 runs inside the
+ * epilogue of step 3 ([S3R] §III-B: the threshold broadcast and the rounding
+ * live inside the fusion that produces the gradient; §IV-A: the SwiGLU
+ * block) -- each 128 x 128 tile of dA is turned into dh1 and dh3, folded and
+ * quantized where the GEMM holds it, so dA never reaches memory (the
+ * workspace's dA is left unwritten).  Q1, Q3 and their tile scales are the
+ * same bit for bit as with the separate step 5; the error partials are the
+ * same sums in another order.  Step event 5 then follows 4 directly.
  * All buffers are device pointers owned by the caller; `args` itself is a
  * HOST pointer read during the call only.
  *
@@ -543,8 +553,10 @@ struct s3r_ffn_args {
                                     after steps 1, 2, 3, 4, 5, 6, 7, 8 above (for timing) */
     int64_t num_groups;          /* 0: one dense block; E > 0: grouped mode (above) */
     const int64_t* group_offsets; /* grouped mode: HOST [E + 1] row offsets */
+    int flags;                   /* 0, or S3R_FFN_FUSE_GLUE (above) */
 };
 #define S3R_FFN_NUM_EVENTS 9
+#define S3R_FFN_FUSE_GLUE 1
 size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
                               int code_format);
 /* grouped mode: group_offsets is the HOST [num_groups + 1] array of the call;

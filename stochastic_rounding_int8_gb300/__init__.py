@@ -535,10 +535,11 @@ class _FfnArgs(C.Structure):
                 ("dX", _VP), ("dW1", _VP), ("dW3", _VP), ("dW2", _VP),
                 ("workspace", _VP), ("workspace_bytes", C.c_size_t), ("d_status", _VP),
                 ("step_events", C.POINTER(C.c_void_p)), ("num_groups", C.c_int64),
-                ("group_offsets", C.POINTER(C.c_int64))]
+                ("group_offsets", C.POINTER(C.c_int64)), ("flags", C.c_int)]
 
 
 FFN_NUM_EVENTS = 9
+FFN_FUSE_GLUE = 1   # S3R_FFN_FUSE_GLUE
 FFN_STEPS = ["quantize dY", "EC W2", "GEMM dA (dX of W2)", "GEMM dW2", "SwiGLU + quantize dh1/dh3", "EC W1/W3",
              "GEMM dX (W1 + W3)", "GEMM dW1 + dW3"]
 # with fp16 codes, steps 3 + 4 and 7 + 8 are one launch each (their time lands on 3 and 7)
@@ -620,11 +621,13 @@ def alloc_moe_grads(R, E, d, F, device="cuda") -> FFNGrads:
 
 def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, seed=0,
                  grads: FFNGrads | None = None, workspace=None, status=None, stream=None,
-                 step_events=None, group_offsets=None) -> FFNGrads:
+                 step_events=None, group_offsets=None, fuse_glue=False) -> FFNGrads:
     """step_events: optional list of FFN_NUM_EVENTS torch.cuda.Event (timing).
     group_offsets: grouped (mixture-of-experts) mode, a list of E + 1 row
     offsets of the expert-sorted rows; the weights in `ops` are then stacked
-    per expert and S is ignored."""
+    per expert and S is ignored.  fuse_glue: run the SwiGLU glue and the
+    quantization of dh1, dh3 inside the dA GEMM's epilogue (S3R_FFN_FUSE_GLUE;
+    dense block with fp16 codes, not independent SR; dA is then not kept)."""
     T, d = dY.shape
     F = ops.A8.shape[1]
     dev = dY.device
@@ -648,6 +651,7 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
                     p(ops.s_a), p(ops.W1_8), p(ops.s_w1), p(ops.W3_8), p(ops.s_w3), p(ops.W2_8), p(ops.s_w2),
                     round_mode, ec_mode, fmt, seed, p(grads.dX), p(grads.dW1), p(grads.dW3), p(grads.dW2),
                     p(workspace), workspace.numel(), p(status), None)
+    args.flags = FFN_FUSE_GLUE if fuse_glue else 0
     if group_offsets is not None:
         off_arr = (C.c_int64 * len(offs))(*offs)   # kept alive until the call returns
         args.num_groups = len(offs) - 1

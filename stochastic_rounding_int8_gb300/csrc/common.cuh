@@ -252,6 +252,16 @@ __device__ __forceinline__ void swiglu_terms2(float2 x, float2& silu, float2& ds
     dsilu = f2_mul(s, make_float2(__fadd_rn(1.0f, xt.x), __fadd_rn(1.0f, xt.y)));
 }
 
+// Tile scale delta = amax / 127 and inv = 127 / amax rounded toward zero (so
+// |g * inv| <= 127 and no code leaves [-127, 127]) from the tile absmax bits
+// (non-negative floats; NaN and infinity order last).
+__device__ __forceinline__ void tile_scales(uint32_t amax_bits, float& d, float& inv) {
+    const bool nonfinite = amax_bits >= 0x7F800000u;
+    const float amx = __uint_as_float(amax_bits);
+    d = nonfinite ? __uint_as_float(0x7FC00000u) : amx / 127.0f;
+    inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amx);
+}
+
 // Record a device-side error (first writer wins is not needed: any error code
 // tells the caller to look; all writers write a negative constant).
 __device__ __forceinline__ void set_status(int* d_status, int code) {
@@ -318,6 +328,36 @@ int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t
 // longest problems first
 int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, int* d_status,
                      cudaStream_t stream);
+// The SwiGLU glue and the quantization of its two outputs run in the epilogue
+// of one dX problem of a mixed launch (the activation gradient dA of the
+// block's down projection, one contraction term): instead of storing dA, each
+// 128 x 128 quarter-tile becomes dh1 = (dA h3) sigma'(h1), dh3 = dA silu(h1),
+// folded with s_x and s_w1 / s_w3, rounded to fp16-carried codes Q1, Q3 with
+// their tile scales and error partials -- the same values, bit for bit, as
+// swiglu_quantize_ex on the stored dA (the partials up to summation order).
+struct UmmaGlue {
+    int dx_index;                // which dX problem of the launch carries the glue
+    int round_mode;              // S3R_ROUND_S3R, _S3R_7BIT, _BCAST or _RTNE
+    uint64_t seed;
+    uint32_t tid1, tid3;
+    int64_t S;                   // tokens per example (S3R_ROUND_BCAST)
+    const void* h1;              // bf16 [T, F], row stride ldh
+    const void* h3;
+    int64_t ldh;
+    const float* s_x;            // folds (NULL: 1)
+    const float* s_w1;
+    const float* s_w3;
+    void* Q1;                    // fp16 codes [T, F]
+    void* Q3;
+    float* scale1;               // tile scales [ceil(T/128), ceil(F/128)]
+    float* scale3;
+    float* tok1;                 // per-token error partials [T, ceil(F/128)] (NULL: none)
+    float* tok3;
+    float* col1;                 // per-channel error partials [ceil(T/128), F]
+    float* col3;
+};
+int umma_mixed_group_glue(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, const UmmaGlue* glue,
+                          int* d_status, cudaStream_t stream);
 // The INT8 forward on fp16-carried codes: Y = (X W * s_x) * s_w (W3 == NULL),
 // or with W3 the gate and up projections through the SwiGLU gate into bf16
 // h1, h3 and a (Y unused).  X [T, K], W and W3 [K, N] as stored.

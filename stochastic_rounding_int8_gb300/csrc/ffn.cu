@@ -266,6 +266,36 @@ int step_swiglu(Block& b, cudaStream_t stream) {
     return S3R_OK;
 }
 
+// 3 + 4 + 5 with the glue in the dA epilogue (fp16 codes; not independent SR):
+// the glue's description for the dA problem of the mixed launch
+UmmaGlue glue_of(const Block& b) {
+    const s3r_ffn_args& a = b.a;
+    const LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
+    const bool keep_err = b.ec != S3R_EC_NONE;
+    UmmaGlue g{};
+    g.dx_index = 0;
+    g.round_mode = b.rm;
+    g.seed = a.seed;
+    g.tid1 = b.tid1;
+    g.tid3 = b.tid3;
+    g.S = a.S;
+    g.h1 = a.h1;
+    g.h3 = a.h3;
+    g.ldh = a.F;
+    g.s_x = a.s_x;
+    g.s_w1 = a.s_w1;
+    g.s_w3 = a.s_w3;
+    g.Q1 = L1.Q;
+    g.Q3 = L3.Q;
+    g.scale1 = L1.scale;
+    g.scale3 = L3.scale;
+    g.tok1 = keep_err ? L1.tok : nullptr;
+    g.tok3 = keep_err ? L3.tok : nullptr;
+    g.col1 = keep_err ? L1.col : nullptr;
+    g.col3 = keep_err ? L3.col : nullptr;
+    return g;
+}
+
 // 6. correction factors of W1 and W3 (W8 [d, F], X8 [T, d]), one pass over X8
 int step_ec_w13(Block& b, cudaStream_t stream) {
     if (b.ec == S3R_EC_NONE) return S3R_OK;
@@ -489,19 +519,31 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
         S3R_TRY(record(a, 1, stream));
         S3R_TRY(step_ec_w2(b, stream));
         S3R_TRY(record(a, 2, stream));
-        if (fmt == S3R_CODES_F16) {
+        const bool fuse = (a->flags & S3R_FFN_FUSE_GLUE) && fmt == S3R_CODES_F16 && !b.indep;
+        if (fuse) {
+            // dA (never stored: the SwiGLU glue and the quantization of dh1, dh3 run in its
+            // epilogue) and dW2 in one launch; steps 4 and 5 are then empty
+            UmmaDxProblem qx = dx_problem_da(b);
+            qx.dX = nullptr;
+            const UmmaDwProblem qw = dw_problem(b, b.a.A8, b.Lo.w2, b.a.F, b.a.d, b.a.s_w2, b.a.dW2);
+            const UmmaGlue gl = glue_of(b);
+            S3R_TRY(umma_mixed_group_glue(&qx, 1, &qw, 1, &gl, a->d_status, stream));
+            S3R_TRY(record(a, 3, stream));
+            S3R_TRY(record(a, 4, stream));
+        } else if (fmt == S3R_CODES_F16) {
             // dA and dW2 in one mixed launch (their tiles share the grid); step 4 is then empty
             const UmmaDxProblem qx = dx_problem_da(b);
             const UmmaDwProblem qw = dw_problem(b, b.a.A8, b.Lo.w2, b.a.F, b.a.d, b.a.s_w2, b.a.dW2);
             S3R_TRY(umma_mixed_group(&qx, 1, &qw, 1, a->d_status, stream));
             S3R_TRY(record(a, 3, stream));
+            S3R_TRY(record(a, 4, stream));
         } else {
             S3R_TRY(step_da(b, stream));
             S3R_TRY(record(a, 3, stream));
             S3R_TRY(step_dw2(b, stream));
+            S3R_TRY(record(a, 4, stream));
         }
-        S3R_TRY(record(a, 4, stream));
-        S3R_TRY(step_swiglu(b, stream));
+        if (!fuse) S3R_TRY(step_swiglu(b, stream));
         S3R_TRY(record(a, 5, stream));
         S3R_TRY(step_ec_w13(b, stream));
         S3R_TRY(record(a, 6, stream));

@@ -40,6 +40,9 @@
 // data is already in shared memory and the stores are asynchronous.
 // The activation gradient may contract two operand pairs into one
 // accumulator (dX = Q1 W1^T + Q3 W3^T), each with its own scales.
+// A third instantiation (kMixedG) can end one dX problem -- the activation
+// gradient dA of the SwiGLU block's down projection -- with the SwiGLU glue
+// and the quantization of dh1 and dh3 instead of a store (glue_tile below).
 // Every mbarrier wait is bounded (S3R_ERR_TIMEOUT in d_status, clean exit).
 #include <cstdio>
 #include <algorithm>
@@ -71,7 +74,11 @@ constexpr int EPI_WARP0 = 4;                // epilogue warps 4..11 (warpgroups 
 // build whose per-thread count is below kMinLaunchRegs (an increase that the
 // pool cannot satisfy would wait forever).
 constexpr int kRegsLow = 56, kRegsHigh = 216;
-constexpr int kMinLaunchRegs = (kRegsLow * 128 + kRegsHigh * 256 + 383) / 384;
+// The glue instantiation gives warpgroup 0 the whole remainder of a
+// 168-register launch (its helpers also bring the glue's side data in).
+constexpr int kRegsLowGlue = 72;
+constexpr int kMinLaunchRegs = (kRegsLowGlue * 128 + kRegsHigh * 256 + 383) / 384;
+static_assert(kRegsLow <= kRegsLowGlue, "the launch check covers both splits");
 constexpr int EPI_WARPS = 8;
 // Output staging of the TMA stores: per epilogue warp two buffers of 32 rows x
 // 8 fp32 columns (1 KiB each, 32-byte swizzle), so the warp fills one while
@@ -93,11 +100,17 @@ constexpr int SX_END = SX_V + 2 * kNbX * 256;
 constexpr int SW_COLSC = 0, SW_P = 256, SW_XS = SW_P + 128, SW_CM = SW_XS + kBch * 128;
 constexpr int SW_END = SW_CM + kBch * 256;
 constexpr int SIDE_FLOATS = SX_END > SW_END ? SX_END : SW_END;
+// The glue problem has one contraction term, so the second term's v slab holds
+// the glue's side data instead: s_x[row] (the fold, not its reciprocal) and
+// s_w1, s_w3 of the tile's 256 columns.
+constexpr int SG_SX = SX_V + kNbX * 256, SG_SW1 = SG_SX + 128, SG_SW3 = SG_SW1 + 256, SG_END = SG_SW3 + 256;
+static_assert(SG_END <= SX_END, "glue side data inside the dX side layout");
 // The correction enters the accumulators after block kCorrBlock of a tile,
 // which leaves the helpers a few blocks to bring the tile's side data in.
 constexpr int kCorrBlock = 3;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * STAGES + 7;
+// + three exchange barriers per epilogue warpgroup for the glue epilogue
+constexpr int NUM_BARS = 2 * STAGES + 7 + 6;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGE_BYTES + SIDE_FLOATS * 4 + 1024 + NUM_BARS * 8 + 16;
 static_assert(SMEM_BYTES + 64 <= 232448, "shared memory budget of one sm_103a CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
@@ -106,7 +119,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 // the problem, a kFwdE launch (forward problems only) too (kFwd or kGate).
 // The forward gets its own instantiation so that the backward kernels carry
 // none of its code.
-enum Epi { kDX = 0, kDW = 1, kDump = 2, kMixed = 3, kFwdE = 4 };
+enum Epi { kDX = 0, kDW = 1, kDump = 2, kMixed = 3, kFwdE = 4, kMixedG = 6 };
 // Problem kind of the INT8 forward (mixed launches only): A = X [M, K] K-major,
 // B = W [K, N] MN-major, unit block scales, epilogue (acc * s_x[m]) * s_w[n].
 constexpr int kFwd = 4;
@@ -165,15 +178,41 @@ struct Problem {
 // segment, and the output C).  Both live in the constant parameter space (__grid_constant__),
 // so indexing them with a run-time problem number costs no copy.
 constexpr int kMaxProb = 24;
+// The SwiGLU glue of a kMixedG launch (see UmmaGlue): problem `prob` stores
+// no dA; its epilogue writes the codes of dh1 and dh3 instead.
+struct Glue {
+    int prob;                    // launch problem carrying the glue (-1: none)
+    int rtne;                    // 1: round to nearest even; 0: SR with one threshold per row
+    int thr;                     // row thresholds: 0 per token, 1 per token (7-bit), 2 per example
+    uint32_t seed_lo, tid1, tid3;
+    int64_t S;                   // tokens per example (thr == 2)
+    const uint16_t* h1;
+    const uint16_t* h3;
+    int64_t ldh;
+    const float* s_x;
+    const float* s_w1;
+    const float* s_w3;
+    uint16_t* Q1;
+    uint16_t* Q3;
+    float* scale1;
+    float* scale3;
+    float* tok1;
+    float* tok3;
+    float* col1;
+    float* col3;
+    int64_t ntc;                 // 128-wide column tiles of dh1 (ceil(F / 128))
+};
 struct Args {
     Problem prob[kMaxProb];
     int nprob;
     int total_tiles;
     int* d_status;
+    Glue glue;
 };
 struct Maps {
     CUtensorMap m[kMaxProb][5];
 };
+static_assert(sizeof(Maps) + sizeof(Args) <= 32764, "kernel parameters beyond the 32764-byte limit");
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -268,6 +307,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// thread i writes 16 consecutive 32-bit columns of lane (base + i)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
@@ -320,8 +374,17 @@ __device__ __forceinline__ int side_rounds(const Problem& P, bool dw) {
     return (int)((P.B + kBch - 1) / kBch);
 }
 
+// The row threshold of token t under the glue's rounding (as the quantizers draw it).
+__device__ __forceinline__ float glue_threshold(const Glue& G, uint64_t t, uint32_t tid) {
+    if (G.thr == 1) return token_threshold7(t, G.seed_lo, tid);
+    if (G.thr == 2) return example_threshold(G.S > 0 ? t / (uint64_t)G.S : 0u, G.seed_lo, tid);
+    return token_threshold(t, G.seed_lo, tid);
+}
+
+// G: the glue of this tile's problem, or null.
 template <int KIND>
-__device__ __forceinline__ void load_side(const Problem& P, float* sd, int64_t m0, int64_t n0, int ht, int round) {
+__device__ __forceinline__ void load_side(const Problem& P, float* sd, int64_t m0, int64_t n0, int ht, int round,
+                                          const Glue* G) {
     const int64_t rows = P.M - m0 < BM ? P.M - m0 : BM;      // valid rows of the tile
     const int64_t cols = P.N - n0 < BN ? P.N - n0 : BN;      // valid columns
     if (KIND == kDX) {
@@ -338,8 +401,21 @@ __device__ __forceinline__ void load_side(const Problem& P, float* sd, int64_t m
                     side_copy(sd + SX_V + (g * kNbX + (int)i) * 256, P.seg[g].v + (b_lo + i) * P.N + n0, BN, cols, ht);
             }
         }
+        if (G) {
+            if (G->s_x) side_copy(sd + SG_SX, G->s_x + m0, BM, rows, ht);
+            if (G->s_w1) side_copy(sd + SG_SW1, G->s_w1 + n0, BN, cols, ht);
+            if (G->s_w3) side_copy(sd + SG_SW3, G->s_w3 + n0, BN, cols, ht);
+        }
         cp_async_wait_all();
         helper_bar();
+        if (G) {
+            if (!G->s_x)
+                for (int i = ht; i < BM; i += 64) sd[SG_SX + i] = 1.0f;
+            for (int j = ht; j < BN; j += 64) {
+                if (!G->s_w1) sd[SG_SW1 + j] = 1.0f;
+                if (!G->s_w3) sd[SG_SW3 + j] = 1.0f;
+            }
+        }
         for (int i = ht; i < BM; i += 64)
             sd[SX_ROWSC + i] = P.s_row ? __frcp_rn(sd[SX_ROWSC + i]) : 1.0f;   // 1/s of a zero-filled row is unused
         if (P.ec_mode) {
@@ -549,6 +625,220 @@ __device__ __forceinline__ void store_tile(const Problem& P, const CUtensorMap* 
     }
 }
 
+// ---------------------------------------------------------------------------
+// The SwiGLU glue epilogue (kMixedG launches, the glue problem's tiles).  A
+// warpgroup's 128 rows x 128 columns of dA (thread = row, acc after the
+// correction and the 1/s_x rescale) are exactly one 128 x 128 tile of dh1
+// and of dh3, so the whole quantization of both happens here:
+//   pass 1: h1, h3 of the thread's row (16-byte loads, prefetched to L2 a few
+//           blocks earlier), the glue and the folds in the order of the
+//           separate SwiGLU quantizer (two lanes per packed instruction);
+//           the folded dh1 replaces dA in acc, the folded dh3 goes into the
+//           tile's own TMEM accumulator (still held back from the MMA
+//           issuer), and the two absmaxes meet across the warpgroup;
+//   pass 2: per output the tile scale, the codes (16-byte stores of fp16
+//           codes), the per-token error sum of the row and the per-channel
+//           sums over the warp's 32 rows (a reduce-scatter), which meet
+//           across the warpgroup in a fixed order through the warps' staging
+//           buffers.
+// The exchanges use three mbarriers per warpgroup (count 4, lane 0 of each
+// warp), waited on with the bounded wait; returns false if one ran out.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// v[0..16): one value per column of a 16-column chunk, the thread's row.
+// Returns the sum over the warp's 32 lanes (rows) of column (lane >> 1); the
+// pairs are added in a fixed order (halving exchanges on lane bits 4..1,
+// then bit 0).
+__device__ __forceinline__ float colsum16(const float (&v)[16], int lane) {
+    float a[8], b[4], c[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (b4 ? v[i + 8] : v[i]) + __shfl_xor_sync(0xFFFFFFFFu, b4 ? v[i] : v[i + 8], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = (b3 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? a[i] : a[i + 4], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i] = (b2 ? b[i + 2] : b[i]) + __shfl_xor_sync(0xFFFFFFFFu, b2 ? b[i] : b[i + 2], 4);
+    float d = (b1 ? c[1] : c[0]) + __shfl_xor_sync(0xFFFFFFFFu, b1 ? c[0] : c[1], 2);
+    d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
+    return d;
+}
+
+// Rounds the folded values in acc (the thread's row, columns c0 ..) to codes
+// with step d and normalizer inv, stores them (fp16) into Q and the error
+// partials: returns the row's sum of g - d q; the warp's column sums of it go
+// to xc[0..128).
+__device__ __forceinline__ float glue_round(const Glue& G, const float (&acc)[128], float d, float inv, bool nonfinite,
+                                            float u, bool vrow, int64_t row, int64_t c0, int64_t F, uint16_t* Q,
+                                            bool err, float* xc, int lane) {
+    const float2 M2 = make_float2(kMagic, kMagic), inv2 = make_float2(inv, inv), nd2 = make_float2(-d, -d);
+    const float2 uu = make_float2(u, u);
+    float2 rs = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        float ne[16];
+        uint32_t hw[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const float2 g2 = make_float2(acc[16 * cc + i], acc[16 * cc + i + 1]);
+            float2 qq = make_float2(0.0f, 0.0f), e = make_float2(0.0f, 0.0f);
+            if (!nonfinite) {
+                const float2 y = f2_mul(g2, inv2);   // |y| <= 127
+                float2 m;
+                if (G.rtne)   // per lane: a packed add that is the product's only use would be fused into an fma
+                    m = make_float2(__fadd_rn(y.x, kMagic), __fadd_rn(y.y, kMagic));
+                else
+                    m = f2_add_rp(f2_sub_rp(y, uu), M2);   // kMagic + ceil(y - u) = kMagic + floor(y) + [u < frac(y)]
+                qq = f2_sub(m, M2);
+                e = f2_fma(nd2, qq, g2);   // g - delta q
+            }
+            ne[i] = e.x;
+            ne[i + 1] = e.y;
+            rs = f2_add(rs, e);
+            const __half2 h2 = __floats2half2_rn(qq.x, qq.y);
+            hw[i / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t col = c0 + 16 * cc + 8 * h;
+            if (vrow && col < F)
+                *reinterpret_cast<uint4*>(Q + row * F + col) = make_uint4(hw[4 * h], hw[4 * h + 1], hw[4 * h + 2],
+                                                                          hw[4 * h + 3]);
+        }
+        if (err) {
+            const float cs = colsum16(ne, lane);
+            if ((lane & 1) == 0) xc[16 * cc + (lane >> 1)] = cs;
+        }
+    }
+    return rs.x + rs.y;
+}
+
+// tcol: TMEM address of the thread's lane, its 128 columns, in the tile's last
+// accumulator; xbase: the staging area of this warpgroup's four warps (2 KiB
+// each, as float[2][128] for the column exchange); gam: absmax exchange
+// [warp][output]; ph: glue tiles this warpgroup has finished.
+__device__ __forceinline__ bool glue_tile(const Glue& G, const Problem& P, float (&acc)[128], const float* sd,
+                                          uint32_t tcol, int64_t row, int rl, int64_t mt, int64_t nt, int64_t c0,
+                                          int half, int q, int lane, uint8_t* xbase, uint32_t (*gam)[2],
+                                          uint32_t barA, uint32_t barB, uint32_t barC, uint32_t ph,
+                                          volatile int* abrt, int* d_status) {
+    const int64_t F = P.N;
+    const bool vrow = row < P.M;
+    const float sx = sd[SG_SX + rl];
+    const float2 sx2 = make_float2(sx, sx);
+    const float* sw1 = sd + SG_SW1 + 128 * half;
+    const float* sw3 = sd + SG_SW3 + 128 * half;
+    const uint16_t* p1 = G.h1 + row * G.ldh + c0;   // read only for valid rows and columns
+    const uint16_t* p3 = G.h3 + row * G.ldh + c0;
+    // ---- pass 1: glue, folds, absmax; dh1 into acc, dh3 into TMEM (8 columns at a time) ----
+    float am1 = 0.0f, am3 = 0.0f;   // NaN-propagating
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc) {
+        const bool okg = vrow && c0 + 8 * cc < F;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
+        if (okg) {
+            a = __ldg(reinterpret_cast<const uint4*>(p1 + 8 * cc));
+            b = __ldg(reinterpret_cast<const uint4*>(p3 + 8 * cc));
+        }
+        const uint32_t w1[4] = {a.x, a.y, a.z, a.w}, w3[4] = {b.x, b.y, b.z, b.w};
+        uint32_t v3[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const int j = 8 * cc + i;
+            // glue, in the documented order, two lanes per packed instruction
+            // (no contraction: built with -fmad=false)
+            const float2 x = make_float2(bf16_lo(w1[i >> 1]), bf16_hi(w1[i >> 1]));
+            const float2 x3 = make_float2(bf16_lo(w3[i >> 1]), bf16_hi(w3[i >> 1]));
+            const float2 d2 = okg ? make_float2(acc[j], acc[j + 1]) : make_float2(0.0f, 0.0f);
+            float2 silu, dsilu;
+            swiglu_terms2(x, silu, dsilu);
+            const float2 dh1 = f2_mul(f2_mul(d2, x3), dsilu);
+            const float2 dh3 = f2_mul(d2, silu);
+            // folds (s_x * dh) * s_w
+            const float2 g1 = f2_mul(f2_mul(sx2, dh1), make_float2(sw1[j], sw1[j + 1]));
+            const float2 g3 = f2_mul(f2_mul(sx2, dh3), make_float2(sw3[j], sw3[j + 1]));
+            acc[j] = g1.x;
+            acc[j + 1] = g1.y;
+            v3[i] = __float_as_uint(g3.x);
+            v3[i + 1] = __float_as_uint(g3.y);
+            am1 = max3_abs_nan(am1, g1.x, g1.y);
+            am3 = max3_abs_nan(am3, g3.x, g3.y);
+        }
+        tmem_st8(tcol + 8 * cc, v3);
+    }
+    tmem_wait_st();   // the loads of pass 2 read what these stores wrote
+    {
+        const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am1));
+        const uint32_t m3 = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am3));
+        if (lane == 0) {
+            gam[q][0] = m1;
+            gam[q][1] = m3;
+        }
+    }
+    // the column exchange reuses the warp's staging buffers: the stores that read them are done first
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(barA);
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(barA, ph & 1u, abrt))) return false;
+    const uint32_t amax1 = max(max(gam[0][0], gam[1][0]), max(gam[2][0], gam[3][0]));
+    const uint32_t amax3 = max(max(gam[0][1], gam[1][1]), max(gam[2][1], gam[3][1]));
+    float d1, inv1, d3, inv3;
+    tile_scales(amax1, d1, inv1);
+    tile_scales(amax3, d3, inv3);
+    const bool nf1 = amax1 >= 0x7F800000u, nf3 = amax3 >= 0x7F800000u;
+    if (q == 0 && lane == 0) {
+        G.scale1[mt * G.ntc + nt] = d1;
+        G.scale3[mt * G.ntc + nt] = d3;
+        if (nf1 || nf3) set_status(d_status, S3R_ERR_NONFINITE);
+    }
+    // ---- pass 2: codes and error partials, dh1 from acc, then dh3 from TMEM ----
+    const bool err = G.tok1 != nullptr;
+    float* xc = reinterpret_cast<float*>(xbase + q * (2 * OUT_BUF_BYTES));   // this warp's [2][128]
+    // the row's thresholds (one Philox draw each, as the quantizers draw them)
+    const float u1 = G.rtne ? 0.0f : glue_threshold(G, (uint64_t)row, G.tid1);
+    const float u3 = G.rtne ? 0.0f : glue_threshold(G, (uint64_t)row, G.tid3);
+    const float r1 = glue_round(G, acc, d1, inv1, nf1, u1, vrow, row, c0, F, G.Q1, err, xc, lane);
+#pragma unroll
+    for (int c = 0; c < 8; c += 4) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) tmem_ld16(tcol + 16 * (c + u), r[u]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[16 * (c + u) + j] = __uint_as_float(r[u][j]);
+    }
+    const float r3 = glue_round(G, acc, d3, inv3, nf3, u3, vrow, row, c0, F, G.Q3, err, xc + 128, lane);
+    if (err && vrow) {
+        G.tok1[row * G.ntc + nt] = -r1;
+        G.tok3[row * G.ntc + nt] = -r3;
+    }
+    if (err) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barB);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(barB, ph & 1u, abrt))) return false;
+        // thread 32 q + lane adds its column over the four warps, in warp order
+        const int tix = 32 * q + lane;
+        if (c0 + tix < F) {
+            float s1 = 0.0f, s3 = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float* xw = reinterpret_cast<const float*>(xbase + w * (2 * OUT_BUF_BYTES));
+                s1 += xw[tix];
+                s3 += xw[128 + tix];
+            }
+            G.col1[mt * F + c0 + tix] = -s1;
+            G.col3[mt * F + c0 + tix] = -s3;
+        }
+        // every warp has read the staging buffers before any of them is written again
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barC);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(barC, ph & 1u, abrt))) return false;
+    }
+    return true;
+}
+
 // Gate epilogue of the forward (thread = row, acc[0..63] = h1 and acc[64..127]
 // = h3 accumulators of output columns c0 .. c0 + 63, as exact int32 sums):
 // convert to fp32 once, rescale in fp32 as (acc * s_x) * s_w and round to
@@ -654,9 +944,11 @@ template <int EPI, bool MN>
 __global__ void __launch_bounds__(THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args A) {
     // the side-data protocol (helper warps, correction inside the tile) serves the backward kinds
-    constexpr bool SIDE = EPI == kDX || EPI == kDW || EPI == kMixed;
+    constexpr bool SIDE = EPI == kDX || EPI == kDW || EPI == kMixed || EPI == kMixedG;
+    constexpr bool MIXED = EPI == kMixed || EPI == kMixedG;   // each problem has its own kind (kDX or kDW)
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
+    __shared__ uint32_t glue_amax[2][4][2];   // glue epilogue: absmax exchange [warpgroup][warp][output]
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_STAGE;
@@ -666,7 +958,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
     const uint32_t full0 = su32(bars), empty0 = su32(bars + STAGES), tfull0 = su32(bars + 2 * STAGES),
                    tempty0 = su32(bars + 2 * STAGES + 2), done_bar = su32(bars + 2 * STAGES + 4),
-                   side_full = su32(bars + 2 * STAGES + 5), side_empty = su32(bars + 2 * STAGES + 6);
+                   side_full = su32(bars + 2 * STAGES + 5), side_empty = su32(bars + 2 * STAGES + 6),
+                   glue_bar0 = su32(bars + 2 * STAGES + 7);   // [A, B, C] x [warpgroup]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = A.total_tiles;   // tile counts fit 32 bits (checked by the host)
@@ -683,6 +976,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(done_bar, 1);
         mbar_init(side_full, 64);          // the 64 helper threads
         mbar_init(side_empty, EPI_WARPS);  // lane 0 of each epilogue warp
+        for (int b = 0; b < 6; ++b) mbar_init(glue_bar0 + 8 * b, 4);   // lane 0 of each warp of a warpgroup
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -703,7 +997,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // their phases across tiles, so the next tile's copies and MMAs start while
     // the epilogue still stores the previous tile.
     if (warp < EPI_WARP0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI == kMixedG ? kRegsLowGlue : kRegsLow));
         if (warp == 0) {
             if (lane == 0) {
                 int it = 0;   // slice counter over the whole persistent run
@@ -716,7 +1010,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
                     const int nkb = nkb0 + nkb1;   // 128-wide blocks of this tile
                     if (pi != last_pi) {
-                        for (int j = 0; j < (nkb1 || (EPI == kFwdE && P.kind == kGate) ? 4 : 2); ++j)
+                        for (int j = 0; j < (nkb1 || (EPI == kFwdE && P.kind == kGate) || (EPI == kMixedG && pi == A.glue.prob)
+                                                 ? 4 : 2); ++j)
                             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)(mp + j)) : "memory");
                         last_pi = pi;
                     }
@@ -724,7 +1019,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
                     const bool gate = EPI == kFwdE && P.kind == kGate;
                     const int32_t m0 = tm * BM, n0 = tn * (gate ? BN / 2 : BN);
+                    // glue tile: its h1 and h3 boxes into L2 a few blocks before the tile ends
+                    // (maps 2 and 3 of the one-term glue problem)
+                    const int pf_sl = EPI == kMixedG && pi == A.glue.prob ? 2 * (nkb > 4 ? nkb - 4 : 0) : -1;
                     for (int sl = 0; sl < 2 * nkb; ++sl, ++it) {
+                        if (sl == pf_sl) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                                                 (uint64_t)(mp + 2 + (j >> 2))),
+                                             "r"(n0 + 64 * (j & 3)), "r"(m0)
+                                             : "memory");
+                        }
                         const int s = it % STAGES;
                         if (!mbar_wait(empty0 + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abrt)) {
                             *abrt = 1;
@@ -740,8 +1046,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const int32_t k0 = (second ? sl - 2 * nkb0 : sl) * BKS;
                         const uint32_t a_dst = su32(sA + s * A_STAGE), b_dst = su32(sB + s * B_STAGE);
                         // forward: A K-major, B MN-major as stored
-                        const bool a_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? false : MN);
-                        const bool b_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? true : MN);
+                        const bool a_mn = MIXED ? P.kind == kDW : (EPI == kFwdE ? false : MN);
+                        const bool b_mn = MIXED ? P.kind == kDW : (EPI == kFwdE ? true : MN);
                         if (!a_mn) {
                             tma_load(a_dst, mA, k0, m0, fb);
                         } else {
@@ -770,8 +1076,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
                     const Problem& P = A.prob[problem_of(A, tile)];
                     const int nkb = (int)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128));
-                    const bool a_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? false : MN);
-                    const bool b_mn = EPI == kMixed ? P.kind == kDW : (EPI == kFwdE ? true : MN);
+                    const bool a_mn = MIXED ? P.kind == kDW : (EPI == kFwdE ? false : MN);
+                    const bool b_mn = MIXED ? P.kind == kDW : (EPI == kFwdE ? true : MN);
                     const uint32_t idesc = a_mn ? idesc_f16(BM, BN, true, true)
                                                 : (b_mn ? idesc_f16(BM, BN, false, true) : idesc_f16(BM, BN, false, false));
                     // one accumulator per drain unit: a 128-wide block, or kFwdUnit of them (forward)
@@ -825,7 +1131,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int tm, tn;
                 tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
                 const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
-                const bool dw = EPI == kMixed ? P.kind == kDW : EPI == kDW;
+                const bool dw = MIXED ? P.kind == kDW : EPI == kDW;
                 const int nr = side_rounds(P, dw);
                 for (int r = 0; r < nr; ++r, ++sph) {
                     // one outcome for both helper warps: they meet at named barriers below
@@ -834,8 +1140,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if (dw) load_side<kDW>(P, sSide, m0, n0, ht, r);
-                    else load_side<kDX>(P, sSide, m0, n0, ht, r);
+                    const Glue* G = (EPI == kMixedG && problem_of(A, tile) == A.glue.prob) ? &A.glue : nullptr;
+                    if (dw) load_side<kDW>(P, sSide, m0, n0, ht, r, nullptr);
+                    else load_side<kDX>(P, sSide, m0, n0, ht, r, G);
                     mbar_arrive(side_full);
                 }
             }
@@ -851,6 +1158,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int rl = 32 * q + lane;   // row within the tile
         int gkb = 0;
         uint32_t sph = 0;   // side-buffer cycles so far (the same count on the helper side)
+        uint32_t gph = 0;   // glue tiles this warpgroup has finished (phase of its exchange barriers)
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             const int pi = problem_of(A, tile);
@@ -863,7 +1171,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t m0 = (int64_t)mt * BM;
             const int64_t row = m0 + rl;
             const bool gate = EPI == kFwdE && P.kind == kGate;
-            const bool is_dw = EPI == kMixed ? P.kind == kDW : EPI == kDW;
+            const bool is_dw = MIXED ? P.kind == kDW : EPI == kDW;
+            // glue tile: the last block's accumulator is held back from the MMA
+            // issuer until the glue has used it for dh3
+            const bool glue = EPI == kMixedG && pi == A.glue.prob;
             // gate: this half owns output columns c0 .. c0 + 63, accumulators
             // 0..63 = h1 (TMEM columns 64 half ..), 64..127 = h3 (128 + 64 half ..)
             const int64_t c0 = gate ? (int64_t)tn * 128 + 64 * half : (int64_t)nt * 128;
@@ -964,7 +1275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                if (lane == 0 && !(glue && kb + 1 == nun)) mbar_arrive(tempty0 + 8 * buf);
                 if (SIDE && kb == kc && !correct()) {   // after the TMEM hand-back: the MMA runs on meanwhile
                     ok = false;
                     *abrt = 1;
@@ -980,6 +1291,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (is_dw) rescale<kDW>(P, acc, sSide, rl, half);
                 else rescale<kDX>(P, acc, sSide, rl, half);
+                if (EPI == kMixedG && glue) {
+                    // acc is this warpgroup's 128 x 128 tile of dA: the glue and both quantizations
+                    const uint32_t lb = (uint32_t)((gkb - 1) & 1);   // the held accumulator
+                    if (c0 < P.N) {
+                        if (!glue_tile(A.glue, P, acc, sSide, lane_addr + lb * BN + col_base, row, rl, mt, nt, c0,
+                                       half, q, lane, sOut + (4 * half) * (2 * OUT_BUF_BYTES), glue_amax[half],
+                                       glue_bar0 + 8 * half, glue_bar0 + 8 * (2 + half), glue_bar0 + 8 * (4 + half),
+                                       gph, abrt, A.d_status)) {
+                            ok = false;
+                            *abrt = 1;
+                            continue;
+                        }
+                        ++gph;
+                    }
+                    tmem_wait_st();
+                    tc_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(tempty0 + 8 * lb);   // the accumulator goes back to the MMA issuer
+                        mbar_arrive(side_empty);
+                    }
+                    ++sph;
+                    continue;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(side_empty);   // the helpers may refill the side buffer
                 ++sph;
@@ -1325,16 +1660,65 @@ int umma_dw_group(const UmmaDwProblem* probs, int n, int* d_status, cudaStream_t
     return umma::launch<umma::kDW, true>(maps, A, strip, stream);
 }
 
+// The glue of a kMixedG launch from its C-level description, for launch
+// problem `prob` (a one-term dX problem of width F = P.N).
+static int make_glue(umma::Glue& G, const UmmaGlue& g, const umma::Problem& P, int prob) {
+    if (P.seg[1].K > 0) return S3R_ERR_ARG;   // dA has one contraction term
+    const int64_t F = P.N;
+    if (!g.h1 || !g.h3 || !g.Q1 || !g.Q3 || !g.scale1 || !g.scale3) return S3R_ERR_ARG;
+    if ((g.tok1 == nullptr) != (g.col1 == nullptr) || (g.tok1 == nullptr) != (g.tok3 == nullptr) ||
+        (g.tok3 == nullptr) != (g.col3 == nullptr))
+        return S3R_ERR_ARG;
+    if (g.ldh < F || F % 8 != 0 || g.ldh % 8 != 0 || !s3r_aligned16(g.h1) || !s3r_aligned16(g.h3) ||
+        !s3r_aligned16(g.Q1) || !s3r_aligned16(g.Q3))
+        return S3R_ERR_ALIGN;
+    G = umma::Glue{};
+    G.prob = prob;
+    switch (g.round_mode) {
+        case S3R_ROUND_S3R: G.thr = 0; break;
+        case S3R_ROUND_S3R_7BIT: G.thr = 1; break;
+        case S3R_ROUND_BCAST: G.thr = 2; break;
+        case S3R_ROUND_RTNE: G.rtne = 1; break;
+        default: return S3R_ERR_ARG;
+    }
+    if (G.rtne && g.tok1) return S3R_ERR_ARG;   // RTNE keeps no error partials
+    G.seed_lo = (uint32_t)g.seed;
+    G.tid1 = g.tid1;
+    G.tid3 = g.tid3;
+    G.S = g.S;
+    G.h1 = static_cast<const uint16_t*>(g.h1);
+    G.h3 = static_cast<const uint16_t*>(g.h3);
+    G.ldh = g.ldh;
+    G.s_x = g.s_x;
+    G.s_w1 = g.s_w1;
+    G.s_w3 = g.s_w3;
+    G.Q1 = static_cast<uint16_t*>(g.Q1);
+    G.Q3 = static_cast<uint16_t*>(g.Q3);
+    G.scale1 = g.scale1;
+    G.scale3 = g.scale3;
+    G.tok1 = g.tok1;
+    G.tok3 = g.tok3;
+    G.col1 = g.col1;
+    G.col3 = g.col3;
+    G.ntc = s3r_cdiv(F, kTile);
+    return S3R_OK;
+}
+
 // dX and dW problems in one launch (no dumps).  Problems run in the order of
 // their per-tile contraction length, longest first, so the short tiles at the
-// end of the round-robin fill in behind the long ones.
-int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, int* d_status,
-                     cudaStream_t stream) {
+// end of the round-robin fill in behind the long ones.  With a glue, dX
+// problem glue->dx_index ends in the SwiGLU glue instead of a store.
+static int mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, const UmmaGlue* glue,
+                       int* d_status, cudaStream_t stream) {
     const int n = ndx + ndw;
     if (ndx < 0 || ndw < 0 || n < 1 || n > umma::kMaxProb) return S3R_ERR_ARG;
+    if (glue && (glue->dx_index < 0 || glue->dx_index >= ndx || dx[glue->dx_index].dX != nullptr ||
+                 dx[glue->dx_index].accumulate))
+        return S3R_ERR_ARG;
     thread_local umma::Maps maps;
     thread_local umma::Args A;
     std::memset(&A, 0, sizeof(A));
+    A.glue.prob = -1;
     double strip[umma::kMaxProb][2];
     // order: per-tile 128-blocks descending (stable)
     int order[umma::kMaxProb];
@@ -1348,13 +1732,31 @@ int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, 
         const int i = order[k];
         if (i < ndx && dx[i].dump) return S3R_ERR_ARG;
         if (i >= ndx && dw[i - ndx].dump) return S3R_ERR_ARG;
-        const int st = i < ndx ? add_dx_problem(maps, A, k, dx[i], strip[k])
-                               : add_dw_problem(maps, A, k, dw[i - ndx], strip[k]);
+        int st = i < ndx ? add_dx_problem(maps, A, k, dx[i], strip[k])
+                         : add_dw_problem(maps, A, k, dw[i - ndx], strip[k]);
+        if (!st && glue && i == glue->dx_index) {
+            // maps 2 and 3 of the one-term glue problem describe h1 and h3 (L2 prefetches of the glue's boxes)
+            st = make_glue(A.glue, *glue, A.prob[k], k);
+            if (!st) st = umma::make_map(&maps.m[k][2], glue->h1, A.prob[k].N, A.prob[k].M, glue->ldh, umma::BM);
+            if (!st) st = umma::make_map(&maps.m[k][3], glue->h3, A.prob[k].N, A.prob[k].M, glue->ldh, umma::BM);
+        }
         if (st) return st;
     }
     A.nprob = n;
     A.d_status = d_status;
+    if (glue) return umma::launch<umma::kMixedG, false>(maps, A, strip, stream);
     return umma::launch<umma::kMixed, false>(maps, A, strip, stream);
+}
+
+int umma_mixed_group(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, int* d_status,
+                     cudaStream_t stream) {
+    return mixed_group(dx, ndx, dw, ndw, nullptr, d_status, stream);
+}
+
+int umma_mixed_group_glue(const UmmaDxProblem* dx, int ndx, const UmmaDwProblem* dw, int ndw, const UmmaGlue* glue,
+                          int* d_status, cudaStream_t stream) {
+    if (!glue) return S3R_ERR_ARG;
+    return mixed_group(dx, ndx, dw, ndw, glue, d_status, stream);
 }
 
 int umma_gemm_dx2(const void* Q, const float* tile_scale, const void* W, const float* eps, const int32_t* rowsum,

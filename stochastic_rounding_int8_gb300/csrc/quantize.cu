@@ -347,15 +347,6 @@ __device__ __forceinline__ void q_issue_tile(uint32_t dst, const CUtensorMap* ma
         : "memory");
 }
 
-// Tile scale delta = amax / 127 and inv = 127 / amax rounded toward zero (so
-// |g * inv| <= 127 and no code leaves [-127, 127]) from the tile absmax bits.
-__device__ __forceinline__ void tile_scales(uint32_t amax_bits, float& d, float& inv) {
-    const bool nonfinite = amax_bits >= 0x7F800000u;
-    const float amx = __uint_as_float(amax_bits);
-    d = nonfinite ? __uint_as_float(0x7FC00000u) : amx / 127.0f;
-    inv = (amax_bits == 0u || nonfinite) ? 0.0f : __fdiv_rz(127.0f, amx);
-}
-
 // Round RPT rows of 8 values (rows RS apart; gpair(j, q) gives values 2q and
 // 2q + 1 of row j) to codes and store them; with
 // ERR, add -e = g - delta*q (one rounding: the exact negation of delta*q - g)

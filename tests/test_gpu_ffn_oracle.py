@@ -43,12 +43,13 @@ def _host(t):
     return t.detach().cpu().numpy()
 
 
-def check_block(orc, views, g, ops_o, h1, h3, dY, S, seed, tid_base, rows, krows_d, krows_f):
+def check_block(orc, views, g, ops_o, h1, h3, dY, S, seed, tid_base, rows, krows_d, krows_f, check_dA=True):
     """One block's (or expert's) ffn_backward results against the oracle.
     views: the block's workspace views (codes, tile scales, dA); g: its output
     gradients as host arrays (dX [T, d], dW1 / dW3 [d, F], dW2 [F, d]); rows:
     token rows of dA and dX to compare; krows_d / krows_f: rows of dW1, dW3
-    and of dW2."""
+    and of dW2; check_dA: False when the glue ran in the dA epilogue (dA is
+    not kept)."""
     T = dY.shape[0]
     F = ops_o.A8.shape[1]
     # stage 1: W2
@@ -57,8 +58,9 @@ def check_block(orc, views, g, ops_o, h1, h3, dY, S, seed, tid_base, rows, krows
     assert w2.status == 0
     assert np.array_equal(codes(views["Q2"]), w2.Q), "codes of dY"
     assert np.array_equal(_host(views["scale2"]), w2.delta), "tile scales of dY"
-    mdx = dx_magnitude(w2.Q, w2.delta, ops_o.W2_8, ops_o.s_a, w2.eps, w2.rowsum, w2.v, S, rows=rows)
-    assert_close_mag(_host(views["dA"])[rows], w2.dX[rows], mdx, "dA")
+    if check_dA:
+        mdx = dx_magnitude(w2.Q, w2.delta, ops_o.W2_8, ops_o.s_a, w2.eps, w2.rowsum, w2.v, S, rows=rows)
+        assert_close_mag(_host(views["dA"])[rows], w2.dX[rows], mdx, "dA")
     mdw = dw_magnitude(ops_o.A8, w2.Q, w2.delta, ops_o.s_w2, w2.colmean, w2.mu, w2.xsum, w2.p, krows=krows_f)
     assert_close_mag(g["dW2"][krows_f], w2.dW, mdw, "dW2")
     # stage 2: the glue on the oracle's own dA, then W1 and W3
@@ -92,13 +94,14 @@ def check_block(orc, views, g, ops_o, h1, h3, dY, S, seed, tid_base, rows, krows
     assert_close_mag(g["dX"][rows], exp_dx, mag_dx, "dX")
 
 
-def _run_dense(s3r, orc, T, d, F, S, seed_data, seed, rows=None, krows_d=None, krows_f=None):
+def _run_dense(s3r, orc, T, d, F, S, seed_data, seed, rows=None, krows_d=None, krows_f=None, fuse_glue=False):
     inp = workloads.ffn_inputs(T, d, F, S, seed=seed_data)
     c = lambda t: t.cuda()
     ops = s3r.ffn_forward_operands(c(inp.X), c(inp.W1), c(inp.W3), c(inp.W2), c(inp.a), c(inp.h1), c(inp.h3))
     ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S), dtype=torch.uint8, device="cuda")
     st = s3r.new_status()
-    grads = s3r.ffn_backward(ops, c(inp.dY), S, s3r.ROUND_S3R, s3r.EC_TWO_WAY, seed=seed, workspace=ws, status=st)
+    grads = s3r.ffn_backward(ops, c(inp.dY), S, s3r.ROUND_S3R, s3r.EC_TWO_WAY, seed=seed, workspace=ws, status=st,
+                             fuse_glue=fuse_glue)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     views = s3r.ffn_workspace_views(ws, T, d, F, S)
@@ -115,7 +118,8 @@ def _run_dense(s3r, orc, T, d, F, S, seed_data, seed, rows=None, krows_d=None, k
     rows = np.arange(T) if rows is None else rows
     krows_d = np.arange(d) if krows_d is None else krows_d
     krows_f = np.arange(F) if krows_f is None else krows_f
-    check_block(orc, views, g, ops_o, f(inp.h1), f(inp.h3), f(inp.dY), S, seed, 0, rows, krows_d, krows_f)
+    check_block(orc, views, g, ops_o, f(inp.h1), f(inp.h3), f(inp.dY), S, seed, 0, rows, krows_d, krows_f,
+                check_dA=not fuse_glue)
 
 
 def test_ffn_backward_block_in_full(s3r, orc):
@@ -130,6 +134,20 @@ def test_ffn_backward_ragged_block_in_full(s3r, orc):
     """A mid-size block with ragged tiles on every GEMM edge (T = 3 x 640,
     d = 520, F = 1416: neither width a multiple of 128 or 256)."""
     _run_dense(s3r, orc, 1920, 520, 1416, 640, 77, seed=3)
+
+
+def test_ffn_backward_fused_glue_block_in_full(s3r, orc):
+    """The same d=2048 block with the SwiGLU glue and the quantization of dh1,
+    dh3 inside the dA GEMM's epilogue (fuse_glue): every code of Q1, Q3
+    judged against the oracle's glue on its own dA, and every element of dX,
+    dW1, dW3, dW2."""
+    _run_dense(s3r, orc, 8192, 2048, 5632, 2048, workloads.DATA_SEED + 1, seed=0, fuse_glue=True)
+
+
+def test_ffn_backward_fused_glue_ragged_block_in_full(s3r, orc):
+    """The ragged mid-size block with the fused glue (the last 256-wide dA tile
+    keeps 8 valid columns in its second half: F = 1416)."""
+    _run_dense(s3r, orc, 1920, 520, 1416, 640, 77, seed=3, fuse_glue=True)
 
 
 def test_ffn_backward_large_block_sampled(s3r, orc):
