@@ -494,8 +494,13 @@ __device__ __forceinline__ float scatter_rows16(const float (&v)[RPT], int c) {
 // consecutive tiles mostly share a row block and reuse that block's
 // thresholds.  A TMA engine keeps up to kQStages 128 x 128 bf16 tiles in
 // flight in a shared-memory ring.  The side data of a tile -- the row scales
-// with the row thresholds, and the column scales -- is fetched one tile
-// ahead (threads 0..127 own a row, 128..255 a column) into a second slot.
+// with the row thresholds, and the column scales -- is fetched two tiles
+// ahead (threads 0..127 own a row, 128..255 a column) into a three-slot ring.
+// One CTA barrier per tile: every thread waits for the tile's copy itself;
+// the barrier after the absmax hands the stage back to the TMA engine, makes
+// the warps' maxima visible, and also orders the exchanges around it -- the
+// previous tile's column sums (double-buffered) are added after it, and the
+// side-data slot that the previous tile used is refilled after it.
 constexpr int kQStages = 3;
 constexpr int kQTileBytes = kTile * kTile * 2;
 constexpr int kQuantTmaSmem = kQStages * kQTileBytes + 8 * kQStages;
@@ -527,10 +532,10 @@ __global__ void __launch_bounds__(256, 2)
     constexpr bool ERR = row_mode(MODE);   // error partials
     extern __shared__ __align__(128) uint8_t qsmem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(qsmem + kQStages * kQTileBytes);
-    __shared__ __align__(16) float2 xu_s[2][kTile];   // (s_x, u) per tile row
-    __shared__ __align__(16) float sw_s[2][kTile];    // s_w per tile column
-    __shared__ uint32_t red[8];
-    __shared__ __align__(16) float col_smem[8 * kTile];
+    __shared__ __align__(16) float2 xu_s[3][kTile];   // (s_x, u) per tile row; tile k in slot k % 3
+    __shared__ __align__(16) float sw_s[3][kTile];    // s_w per tile column
+    __shared__ uint32_t red[2][8];                    // the warps' absmax, tile k in [k & 1]
+    __shared__ __align__(16) float col_smem[2][8 * kTile];   // per-warp column sums, tile k in [k & 1]
     const int tid = threadIdx.x, c = tid & 15, r0 = tid >> 4, lane = tid & 31, warp = tid >> 5;
     // tile indices fit 32 bits (checked on the host) and advance incrementally
     const int ntc = (int)C.ntc;
@@ -545,15 +550,17 @@ __global__ void __launch_bounds__(256, 2)
                      bar0 + 8 * s);
         if (++icb == ntc) { icb = 0; ++irb; }
     };
-    int rb = beg / ntc, cb = beg - (beg / ntc) * ntc;   // current tile
-    int nrb = rb, ncb = cb;                             // tile after the current one
-    if (++ncb == ntc) { ncb = 0; ++nrb; }
+    int rb = beg / ntc, cb = beg - (beg / ntc) * ntc;      // current tile
+    int srb = rb, scb = cb;                                // next tile whose side data is fetched
     float u_mine = 0.0f;
     int u_rb = -1;
-    if (count > 0) {
-        const float2 sd = q_side<MODE>(A, C, O.tensor_id, rb, cb, u_mine, u_rb);
-        if (tid < kTile) xu_s[0][tid] = sd;
-        else sw_s[0][tid - kTile] = sd.x;
+    auto put_side = [&](int slot, float2 sd) {
+        if (tid < kTile) xu_s[slot][tid] = sd;
+        else sw_s[slot][tid - kTile] = sd.x;
+    };
+    for (int i = 0; i < 2 && i < count; ++i) {   // tiles 0 and 1
+        put_side(i, q_side<MODE>(A, C, O.tensor_id, srb, scb, u_mine, u_rb));
+        if (++scb == ntc) { scb = 0; ++srb; }
     }
     if (tid == 0) {
         for (int i = 0; i < kQStages; ++i)
@@ -567,20 +574,23 @@ __global__ void __launch_bounds__(256, 2)
         for (; issued < kQStages && issued < count; ++issued) issue(issued);
     int k = 0, s = 0;
     uint32_t phase = 0;
+    int prb = 0, pcb = 0;   // the previous tile (its column sums are added one tile later)
+    bool done = true;       // false: the CTA left early (a wait ran out)
     for (; k < count; ++k) {
-        const int sl = k & 1;
+        const int sl = k % 3;
         const int64_t t0 = (int64_t)rb * kTile, n0 = (int64_t)cb * kTile;
         const int nc0 = (int)n0 + 8 * c;
         const int64_t rl = C.T - t0 - r0;
         const int rows_left = rl < kTile ? (int)rl : kTile;   // my row j is valid iff RS j < rows_left
-        // the next tile's side data: loads (and thresholds) in flight during this tile
+        // side data two tiles ahead: loads (and thresholds) in flight during this tile
+        const bool more = k + 2 < count;
         float2 side = make_float2(0.0f, 0.0f);
-        if (k + 1 < count) side = q_side<MODE>(A, C, O.tensor_id, nrb, ncb, u_mine, u_rb);
-        // every thread waits; the CTA leaves together if any wait ran out
-        if (!__syncthreads_and(q_wait(bar0 + 8 * s, phase))) {
-            if (tid == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
-            break;
+        if (more) {
+            side = q_side<MODE>(A, C, O.tensor_id, srb, scb, u_mine, u_rb);
+            if (++scb == ntc) { scb = 0; ++srb; }
         }
+        // every thread waits for the tile itself; a wait that ran out is settled at the barrier
+        const bool ok = q_wait(bar0 + 8 * s, phase);
         // pass 1: fold g = (s_x * G) * s_w and absmax.  Unscaled input keeps the raw bf16
         // pairs (half the registers) and takes the absmax two at a time in bf16: the
         // magnitude max of a pair of bf16 values is exact, and bf16 -> fp32 is exact.
@@ -628,19 +638,32 @@ __global__ void __launch_bounds__(256, 2)
                 }
             }
         }
-        // block absmax (non-negative floats and NaN order like their bit patterns); after the
-        // barrier every thread is done with this stage, which is refilled at once
+        // block absmax (non-negative floats and NaN order like their bit patterns)
         {
             const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
-            if (lane == 0) red[warp] = wm;
+            if (lane == 0) red[k & 1][warp] = wm;
         }
-        __syncthreads();
+        // the one barrier of the tile: every thread is done with this stage (refilled at once),
+        // the maxima and the previous tile's column sums are visible, and the CTA leaves
+        // together if any wait ran out
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) set_status(C.d_status, S3R_ERR_TIMEOUT);
+            done = false;
+            break;
+        }
         if (tid == 0 && issued < count) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(issued);
             ++issued;
         }
-        uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, red[lane & 7]);
+        if (ERR && O.col && k > 0 && tid < kTile) {   // the previous tile's column sums, in warp order
+            const float* cs = col_smem[(k - 1) & 1];
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) sum += cs[w * kTile + tid];
+            if ((int64_t)pcb * kTile + tid < C.N) O.col[(int64_t)prb * C.N + (int64_t)pcb * kTile + tid] = -sum;
+        }
+        uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, red[k & 1][lane & 7]);
         if (C.tensor_amax) amax_bits = __ldg(C.tensor_amax);   // one step for the whole tensor
         const bool nonfinite = amax_bits >= 0x7F800000u;   // uniform across the CTA
         float d, inv;
@@ -673,26 +696,28 @@ __global__ void __launch_bounds__(256, 2)
                 cs[2 * q + 1] = colsum[q].y + __shfl_xor_sync(0xFFFFFFFFu, colsum[q].y, 16);
             }
             if (lane < 16) {
-                *reinterpret_cast<float4*>(&col_smem[warp * kTile + 8 * c]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
-                *reinterpret_cast<float4*>(&col_smem[warp * kTile + 8 * c + 4]) =
-                    make_float4(cs[4], cs[5], cs[6], cs[7]);
+                float* dst = &col_smem[k & 1][warp * kTile + 8 * c];
+                *reinterpret_cast<float4*>(dst) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(cs[4], cs[5], cs[6], cs[7]);
             }
         }
-        if (k + 1 < count) {
-            if (tid < kTile) xu_s[sl ^ 1][tid] = side;
-            else sw_s[sl ^ 1][tid - kTile] = side.x;
-        }
+        // slot (k + 2) % 3 held the previous tile's side data, which every thread finished
+        // reading before this tile's barrier
+        if (more) put_side((k + 2) % 3, side);
+        prb = rb;
+        pcb = cb;
+        if (++cb == ntc) { cb = 0; ++rb; }
+        if (++s == kQStages) { s = 0; phase ^= 1u; }
+    }
+    if (done && count > 0 && ERR && O.col) {   // the last tile's column sums
         __syncthreads();
-        if (ERR && O.col && tid < kTile) {
+        if (tid < kTile) {
+            const float* cs = col_smem[(count - 1) & 1];
             float sum = 0.0f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) sum += col_smem[w * kTile + tid];
-            if (n0 + tid < C.N) O.col[(int64_t)rb * C.N + n0 + tid] = -sum;
+            for (int w = 0; w < 8; ++w) sum += cs[w * kTile + tid];
+            if ((int64_t)pcb * kTile + tid < C.N) O.col[(int64_t)prb * C.N + (int64_t)pcb * kTile + tid] = -sum;
         }
-        rb = nrb;
-        cb = ncb;
-        if (++ncb == ntc) { ncb = 0; ++nrb; }
-        if (++s == kQStages) { s = 0; phase ^= 1u; }
     }
     // an early exit may leave copies in flight: wait for them before leaving
     if (tid == 0)
