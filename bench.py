@@ -48,12 +48,11 @@ L2_BYTES = 129 * 2 ** 20
 # on a GB300; keyed by the sha256 of the GEMM source it was taken on, so that it is reported
 # only while that kernel is unchanged, then by block.
 GEMM_TRAFFIC = {
-    "c3099914d96ba9add3d5578b0e1215e73f418bf866539570108f4d7ec566a124": {
-        "swiglu_ffn_d4096_F14336_T16384": 2331.5e6,   # dA + dW2 4643 MB, dX1 + dX3 + dW1 + dW3 9346 MB
-        "swiglu_ffn_d2048_F5632_T8192": 208.2e6,      # 428.5 MB and 820.8 MB
+    "980cc34aa950177fa76fb1f55e8c2eeff42c37874320f44c42f29711e4f54799": {
+        "swiglu_ffn_d4096_F14336_T16384": 2368.4e6,   # dA + dW2 4669 MB, dX1 + dX3 + dW1 + dW3 9541 MB
+        "swiglu_ffn_d2048_F5632_T8192": 208.1e6,      # 441.9 MB and 806.5 MB
     },
 }
-
 
 def parse():
     ap = argparse.ArgumentParser()
