@@ -41,6 +41,7 @@ SMALL_BLOCK = "swiglu_ffn_d2048_F5632_T8192"
 CFG = workloads.WORKLOADS[WORKLOAD]
 T, D, F, S = CFG["T"], CFG["d"], CFG["F"], CFG["S"]
 L2_BYTES = 129 * 2 ** 20
+E2E_IN_STREAMS = 3   # streams carrying the e2e input copies (one stream: 0.55 M tokens/s on one box, 1.33 M with 2-4)
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the two GEMM launches of one
 # ffn_backward step, divided by the step's six products, from a one-pass ncu capture of
@@ -244,39 +245,77 @@ def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse
 
 
 def time_e2e(s3r, blk, inp, ops, steps, warmup, world):
-    """Same step through the C ABI with HOST buffers: pinned host -> device
-    copies of every input of the step, the backward, device -> host copies of
-    all four gradients, inside the timed region."""
+    """Same step through the C ABI with HOST buffers: every step copies all of
+    its inputs from pinned host memory to the device, runs the backward, and
+    copies all four gradients back, inside the timed region.  The copies run
+    on their own streams, double-buffered, so step i's input copy and step
+    i - 1's gradient copy overlap step i - 1's and step i's backward (the
+    way a training loop feeds a device); events order the buffers' reuse."""
     T, d, F, S = blk.T, blk.d, blk.F, blk.S
     host_in = {k: getattr(ops, k).cpu().pin_memory() for k in
                ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2", "h1", "h3")}
     host_in["dY"] = inp.dY.pin_memory()
-    dev_in = {k: torch.empty_like(v, device="cuda") for k, v in host_in.items()}
-    dops = s3r.FFNOperands(**{k: dev_in[k] for k in host_in if k != "dY"})
-    grads = s3r.alloc_ffn_grads(T, d, F)
-    host_out = {k: torch.empty(getattr(grads, k).shape, dtype=torch.float32).pin_memory()
-                for k in ("dX", "dW1", "dW3", "dW2")}
+    dev_in = [{k: torch.empty_like(v, device="cuda") for k, v in host_in.items()} for _ in range(2)]
+    dops = [s3r.FFNOperands(**{k: di[k] for k in host_in if k != "dY"}) for di in dev_in]
+    grads = [s3r.alloc_ffn_grads(T, d, F) for _ in range(2)]
+    host_out = [{k: torch.empty(getattr(grads[0], k).shape, dtype=torch.float32).pin_memory()
+                 for k in ("dX", "dW1", "dW3", "dW2")} for _ in range(2)]
     ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, code_format=s3r.code_format_of(ops.X8)), dtype=torch.uint8,
                      device="cuda")
     bi = sum(v.numel() * v.element_size() for v in host_in.values())
-    bo = sum(v.numel() * v.element_size() for v in host_out.values())
+    bo = sum(v.numel() * v.element_size() for v in host_out[0].values())
+    # the input copies spread over N_IN streams (balanced by bytes), so several copy engines share them
+    N_IN = E2E_IN_STREAMS
+    s_ins = [torch.cuda.Stream() for _ in range(N_IN)]
+    s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    load = [0] * N_IN
+    lane_of = {}
+    for k, v in sorted(host_in.items(), key=lambda kv: -kv[1].numel() * kv[1].element_size()):
+        j = load.index(min(load))
+        lane_of[k] = j
+        load[j] += v.numel() * v.element_size()
+    ev = lambda: torch.cuda.Event()
+    in_done = [[ev() for _ in range(N_IN)] for _ in range(2)]
+    comp_done, out_done = [ev(), ev()], [ev(), ev()]
+    used = [False, False]
 
     def step(i):
-        for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        s3r.ffn_backward(dops, dev_in["dY"], S, seed=i, grads=grads, workspace=ws)
-        for k, v in host_out.items():
-            v.copy_(getattr(grads, k), non_blocking=True)
+        b = i % 2
+        for j, s_in in enumerate(s_ins):
+            with torch.cuda.stream(s_in):
+                if used[b]:
+                    s_in.wait_event(comp_done[b])    # the backward of step i - 2 has read these inputs
+                for k, v in host_in.items():
+                    if lane_of[k] == j:
+                        dev_in[b][k].copy_(v, non_blocking=True)
+                in_done[b][j].record(s_in)
+        with torch.cuda.stream(s_comp):
+            for j in range(N_IN):
+                s_comp.wait_event(in_done[b][j])
+            if used[b]:
+                s_comp.wait_event(out_done[b])   # step i - 2's gradients have left the device
+            s3r.ffn_backward(dops[b], dev_in[b]["dY"], S, seed=i, grads=grads[b], workspace=ws, stream=s_comp)
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            for k, v in host_out[b].items():
+                v.copy_(getattr(grads[b], k), non_blocking=True)
+            out_done[b].record(s_out)
+        used[b] = True
 
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     barrier(world)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
+    t0.record(s_ins[0])
+    for s_in in s_ins[1:]:
+        s_in.wait_event(t0)
     for i in range(steps):
-        step(i)
-    t1.record()
+        step(warmup + i)
+    s_out.wait_event(out_done[(warmup + steps - 1) % 2])
+    s_out.wait_event(comp_done[(warmup + steps - 1) % 2])
+    t1.record(s_out)
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     barrier(world)
@@ -633,7 +672,9 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(3, min(args.steps, 10))
     ems, bi, bo = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world)
     line["e2e"] = {"value": round(world * blk.T * e2e_steps / (ems * 1e-3), 1), "unit": "tokens/s",
-                   "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
+                   "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+                   "copies": "every step copies all inputs in and all four gradients out; the copies run on their "
+                             "own streams, double-buffered, overlapping the neighbouring steps' backward"}
     if not args.no_context and rank == 0:
         ctx = mode_context(s3r, blk, ops, dY, inp)
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / r["ms_per_step"], 3)
