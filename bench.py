@@ -679,6 +679,11 @@ def run_ours(args, world, rank, local):
         ctx = mode_context(s3r, blk, ops, dY, inp)
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / r["ms_per_step"], 3)
         ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / r["ms_per_step"], 3)
+        # what keeping the activation gradient dA in fp32 costs: written by the dA GEMM, read by the
+        # SwiGLU quantizer (the fused-glue variant above avoids it but stalls the GEMM instead)
+        da_bytes = 2 * 4 * blk.T * blk.F
+        ctx["dA_fp32_intermediate"] = {"bytes_per_step": da_bytes,
+                                       "ms_at_measured_hbm": round(da_bytes / (pk["hbm_gbs"] * 1e9) * 1e3, 4)}
         fw = time_forward(s3r, blk, inp, pk)
         ctx["forward_int8"] = fw
         # one INT8 training step of the block: this forward + the timed backward
