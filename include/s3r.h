@@ -610,6 +610,26 @@ int s3r_debug_dw_blocks(const void* X8, const void* Q, int code_format, int64_t 
  */
 int s3r_check_reciprocal(uint32_t lo_bits, uint32_t hi_bits, unsigned long long* d_count, cudaStream_t stream);
 
+/*
+ * Test hook for failure detection (no counterpart on the pages): every wait
+ * inside the kernels is bounded -- it gives up after its limit (2 s) or, where
+ * the kernel has one, as soon as another role of the CTA raised its abort
+ * flag -- and a kernel whose wait gave up writes S3R_ERR_TIMEOUT to d_status
+ * and exits cleanly, leaving the context usable.  This runs the wait routine
+ * of one kernel family (family: S3R_WAIT_GEMM, S3R_WAIT_QUANTIZE or
+ * S3R_WAIT_EC) in a one-CTA launch on an mbarrier that nothing arrives on,
+ * with the limit limit_ns (0 < limit_ns <= 2e9); raise_abort != 0 (GEMM and
+ * EC families only) has a second warp raise the abort flag after about 1 ms
+ * instead.  The waiter writes the nanoseconds it waited to *d_waited_ns and
+ * S3R_ERR_TIMEOUT to *d_status (both device memory).  Asynchronous on `stream`.
+ * S3R_ERR_ARG for a bad family, limit or pointer.
+ */
+#define S3R_WAIT_GEMM 0
+#define S3R_WAIT_QUANTIZE 1
+#define S3R_WAIT_EC 2
+int s3r_debug_wait_timeout(int family, uint64_t limit_ns, int raise_abort, int* d_status,
+                           unsigned long long* d_waited_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

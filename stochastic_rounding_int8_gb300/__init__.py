@@ -82,6 +82,7 @@ _SIGS = {
     "s3r_ffn_workspace_offsets": (_INT, [_I64, _I64, _I64, _I64, _INT, _INT, _VP, _I64, _I64, _VP]),
     "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP]),
     "s3r_check_reciprocal": (_INT, [_U32, _U32, _VP, _VP]),
+    "s3r_debug_wait_timeout": (_INT, [_INT, _U64, _INT, _VP, _VP, _VP]),
     "s3r_debug_dw_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
 }
 
@@ -381,6 +382,20 @@ def check_reciprocal(lo_bits, hi_bits, device="cuda", stream=None) -> int:
     count = torch.zeros(1, dtype=torch.int64, device=device)
     _check(lib().s3r_check_reciprocal(lo_bits, hi_bits, _ptr(count), _stream(stream)), "s3r_check_reciprocal")
     return int(count.item())
+
+
+WAIT_GEMM, WAIT_QUANTIZE, WAIT_EC = 0, 1, 2
+
+
+def debug_wait_timeout(family, limit_ns, raise_abort=False, device="cuda", stream=None):
+    """Run one kernel family's bounded wait on a barrier that nothing arrives
+    on (test hook): returns (device status, nanoseconds waited)."""
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    waited = torch.zeros(1, dtype=torch.int64, device=device)
+    _check(lib().s3r_debug_wait_timeout(family, limit_ns, int(bool(raise_abort)), _ptr(st), _ptr(waited),
+                                        _stream(stream)), "s3r_debug_wait_timeout")
+    torch.cuda.synchronize()
+    return int(st.item()), int(waited.item())
 
 
 def debug_dx_blocks(Q, W8, stream=None):

@@ -365,6 +365,14 @@ int umma_fwd(const void* X, const float* s_x, const void* W, const float* s_w, c
              int64_t T, int64_t K, int64_t N, float* Y, uint16_t* h1, uint16_t* h3, uint16_t* a, int* d_status,
              cudaStream_t stream);
 
+// Test hooks of the bounded waits (see s3r_debug_wait_timeout): each runs its
+// kernel family's own wait routine on a barrier that nothing arrives on.
+int umma_wait_probe(uint64_t limit_ns, int raise_abort, int* d_status, unsigned long long* waited_ns,
+                    cudaStream_t stream);
+int quant_wait_probe(uint64_t limit_ns, int* d_status, unsigned long long* waited_ns, cudaStream_t stream);
+int ec_wait_probe(uint64_t limit_ns, int raise_abort, int* d_status, unsigned long long* waited_ns,
+                  cudaStream_t stream);
+
 // S3R-EC factors of the two linears that read the same input X (W1 and W3 of
 // the SwiGLU block) in one pass; bit-identical to two s3r_ec_correct calls
 // (ec.cu).

@@ -610,7 +610,8 @@ __device__ __forceinline__ void es_consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kEsConsumers) : "memory");
 }
 // Bounded wait (2 s of %globaltimer) that also gives up once the CTA's abort flag is up.
-__device__ __forceinline__ bool es_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+__device__ __forceinline__ bool es_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                        uint64_t limit_ns = 2000000000ull) {
     const uint64_t t0 = ec_gtime();
     while (true) {
         uint32_t ok;
@@ -620,9 +621,37 @@ __device__ __forceinline__ bool es_wait(uint32_t bar, uint32_t parity, const vol
             : "r"(bar), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (*abort_flag || ec_gtime() - t0 > 2000000000ull) return false;
+        if (*abort_flag || ec_gtime() - t0 > limit_ns) return false;
     }
 }
+
+// Test hook: es_wait on a barrier that nothing arrives on, with a short limit;
+// with raise_abort a second warp raises the CTA's abort flag after about a
+// millisecond instead.  The waiter records how long it waited and sets
+// S3R_ERR_TIMEOUT.
+__global__ void __launch_bounds__(64) es_wait_probe_kernel(uint64_t limit_ns, int raise_abort, int* d_status,
+                                                           unsigned long long* waited_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_s;
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+        abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 32 && raise_abort) {
+        const uint64_t t0 = ec_gtime();
+        while (ec_gtime() - t0 < 1000000ull) {}
+        *reinterpret_cast<volatile int*>(&abort_s) = 1;
+    } else if (threadIdx.x == 0) {
+        const uint64_t t0 = ec_gtime();
+        const bool ok = es_wait(b, 0u, &abort_s, limit_ns);
+        *waited_ns = ec_gtime() - t0;
+        if (!ok) set_status(d_status, S3R_ERR_TIMEOUT);
+    }
+}
+
 
 // mu[b] = (1/S) sum_{t < S} e[b S + t] for every b < B over the 512 consumer
 // threads in a fixed order: per-thread strided sums (float4 loads when V4),
@@ -1378,6 +1407,13 @@ static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int6
 }  // namespace s3r
 
 using namespace s3r;
+
+int ec_wait_probe(uint64_t limit_ns, int raise_abort, int* d_status, unsigned long long* waited_ns,
+                  cudaStream_t stream) {
+    es_wait_probe_kernel<<<1, 64, 0, stream>>>(limit_ns, raise_abort, d_status, waited_ns);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
 
 extern "C" size_t s3r_ec_workspace_size(int64_t T, int64_t K) {
     if (T <= 0 || K <= 0) return 0;

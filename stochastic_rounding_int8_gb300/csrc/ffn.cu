@@ -32,6 +32,19 @@ int s3r_cuda_fail(const char* where, cudaError_t err) {
 }
 extern "C" const char* s3r_last_error(void) { return g_last_error; }
 
+extern "C" int s3r_debug_wait_timeout(int family, uint64_t limit_ns, int raise_abort, int* d_status,
+                                      unsigned long long* d_waited_ns, cudaStream_t stream) {
+    if (!d_status || !d_waited_ns || limit_ns == 0 || limit_ns > 2000000000ull) return S3R_ERR_ARG;
+    switch (family) {
+        case S3R_WAIT_GEMM: return umma_wait_probe(limit_ns, raise_abort, d_status, d_waited_ns, stream);
+        case S3R_WAIT_QUANTIZE:
+            if (raise_abort) return S3R_ERR_ARG;   // the quantizers' waits have no abort flag
+            return quant_wait_probe(limit_ns, d_status, d_waited_ns, stream);
+        case S3R_WAIT_EC: return ec_wait_probe(limit_ns, raise_abort, d_status, d_waited_ns, stream);
+        default: return S3R_ERR_ARG;
+    }
+}
+
 static std::mutex g_setup_mutex;
 
 int s3r_sm_count() {

@@ -241,15 +241,43 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait for the phase of the given parity to complete; gives up (false) after
-// kWaitNs or as soon as another role raised the abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// limit_ns or as soon as another role raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitNs) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = gtime();
     while (!mbar_try(bar, parity)) {
         if (*abort_flag) return false;
-        if (gtime() - t0 > kWaitNs) return false;
+        if (gtime() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// Test hook: mbar_wait on a barrier that nothing arrives on, with a short
+// limit; with raise_abort a second warp raises the abort flag after about a
+// millisecond instead.  The waiter records how long it waited and, having
+// given up, sets S3R_ERR_TIMEOUT as the kernels do.
+__global__ void __launch_bounds__(64) wait_probe_kernel(uint64_t limit_ns, int raise_abort, int* d_status,
+                                                        unsigned long long* waited_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_s;
+    const uint32_t b = su32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 32 && raise_abort) {
+        const uint64_t t0 = gtime();
+        while (gtime() - t0 < 1000000ull) {}
+        *reinterpret_cast<volatile int*>(&abort_s) = 1;
+    } else if (threadIdx.x == 0) {
+        const uint64_t t0 = gtime();
+        const bool ok = mbar_wait(b, 0u, &abort_s, limit_ns);
+        *waited_ns = gtime() - t0;
+        if (!ok) set_status(d_status, S3R_ERR_TIMEOUT);
+    }
 }
 // Bounded wait that ignores the abort flag: used before teardown, where the
 // copies or MMAs still in flight must land whatever the other roles did.
@@ -1622,6 +1650,13 @@ int umma_fwd(const void* X, const float* s_x, const void* W, const float* s_w, c
     A.nprob = 1;
     A.d_status = d_status;
     return umma::launch<umma::kFwdE, false>(maps, A, strip, stream);
+}
+
+int umma_wait_probe(uint64_t limit_ns, int raise_abort, int* d_status, unsigned long long* waited_ns,
+                    cudaStream_t stream) {
+    umma::wait_probe_kernel<<<1, 64, 0, stream>>>(limit_ns, raise_abort, d_status, waited_ns);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
 }
 
 int umma_dx_group(const UmmaDxProblem* probs, int n, int* d_status, cudaStream_t stream) {

@@ -323,7 +323,7 @@ __device__ __forceinline__ uint64_t q_gtime() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-__device__ __forceinline__ bool q_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool q_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kQuantWaitNs) {
     uint32_t ok = 0;
     const uint64_t t0 = q_gtime();
     while (true) {
@@ -333,7 +333,23 @@ __device__ __forceinline__ bool q_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (q_gtime() - t0 > kQuantWaitNs) return false;
+        if (q_gtime() - t0 > limit_ns) return false;
+    }
+}
+
+// Test hook: q_wait on a barrier that nothing arrives on, with a short limit;
+// the waiter records how long it waited and sets S3R_ERR_TIMEOUT.
+__global__ void __launch_bounds__(32) q_wait_probe_kernel(uint64_t limit_ns, int* d_status,
+                                                          unsigned long long* waited_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const uint64_t t0 = q_gtime();
+        const bool ok = q_wait(b, 0u, limit_ns);
+        *waited_ns = q_gtime() - t0;
+        if (!ok) set_status(d_status, S3R_ERR_TIMEOUT);
     }
 }
 __device__ __forceinline__ void q_issue_tile(uint32_t dst, const CUtensorMap* map, int32_t col, int32_t row,
@@ -1430,6 +1446,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
 }
 
 static int sm_count() { return s3r_sm_count(); }
+
+int quant_wait_probe(uint64_t limit_ns, int* d_status, unsigned long long* waited_ns, cudaStream_t stream) {
+    q_wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, d_status, waited_ns);
+    S3R_CHECK_LAUNCH();
+    return S3R_OK;
+}
 
 
 template <int MODE, int FMT, bool FOLD>
