@@ -377,12 +377,20 @@ int ec_wait_probe(uint64_t limit_ns, int raise_abort, int* d_status, unsigned lo
 // the SwiGLU block) in one pass; bit-identical to two s3r_ec_correct calls
 // (ec.cu).
 size_t s3r_ec_pair_workspace_size(int64_t T, int64_t K);
+// max_ctas > 0 caps the grid of the streaming pass (several calls sharing the
+// GPU on side streams); 0: all SMs.
 int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, float* eps1, float* mu1,
                         float* colmean1, int32_t* rowsum1, float* v1, int32_t* xsum1, float* p1, const float* tok3,
                         const float* col3, const void* W3_8, float* eps3, float* mu3, float* colmean3,
                         int32_t* rowsum3, float* v3, int32_t* xsum3, float* p3, int64_t T, int64_t N, int64_t S,
                         int64_t K, const void* X8, int code_format, int ec_mode, void* workspace,
-                        size_t workspace_bytes, int* d_status, cudaStream_t stream);
+                        size_t workspace_bytes, int max_ctas, int* d_status, cudaStream_t stream);
+// s3r_ec_correct with that cap.
+int s3r_ec_correct_capped(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
+                          const void* W8, int64_t K, const void* X8, int code_format, int ec_mode, float* eps,
+                          float* mu, float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p,
+                          void* workspace, size_t workspace_bytes, int max_ctas, int* d_status,
+                          cudaStream_t stream);
 #define S3R_CHECK_LAUNCH()                                               \
     do {                                                                 \
         s3r_count_launch();                                              \

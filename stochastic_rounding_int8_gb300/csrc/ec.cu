@@ -1127,12 +1127,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 ec_encode_fn() {
 
 static int ec_sm_count() { return s3r_sm_count(); }
 
+// max_ctas > 0 caps the grid (a call that shares the GPU with other such calls
+// on other streams takes its share of the SMs instead of all of them).
 template <int NJ, int BCH>
-static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, size_t smem, cudaStream_t stream) {
+static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, size_t smem, int max_ctas,
+                              cudaStream_t stream) {
     const int st = s3r_kernel_smem((const void*)ec_stream_kernel<NJ, BCH>, (int)es_smem_bytes(NJ, kEsMaxB),
                                    "ec stream: cudaFuncSetAttribute");
     if (st) return st;
     int64_t grid = std::min<int64_t>(S.n_items, ec_sm_count());
+    if (max_ctas > 0) grid = std::min<int64_t>(grid, max_ctas);
     if (!S.done) {
         ec_stream_kernel<NJ, BCH><<<(unsigned)grid, kEsThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
                                                                                  maps[4], maps[5], maps[6], S);
@@ -1163,8 +1167,8 @@ static int launch_ec_stream_t(const CUtensorMap* maps, const EcStreamArgs& S, si
 }
 
 static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
-                            bool weight, bool two, int32_t* xs, float* ps, int* counter, int* d_status,
-                            cudaStream_t stream) {
+                            bool weight, bool two, int32_t* xs, float* ps, int* counter, int max_ctas,
+                            int* d_status, cudaStream_t stream) {
     const int64_t B = T / S;
     if (B > kEsMaxB || T >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return 1;
     if (N % 8 != 0 || (two && K % 8 != 0)) return 1;
@@ -1242,13 +1246,13 @@ static int launch_ec_stream(const EcJob* jobs, int nj, int64_t T, int64_t N, int
     if (A.n_items >= (int64_t(1) << 30)) return 1;
     const size_t smem = es_smem_bytes(nj, B);
     if (nj == 2) {
-        if (bch == 1) return launch_ec_stream_t<2, 1>(maps, A, smem, stream);
-        if (bch == 4) return launch_ec_stream_t<2, 4>(maps, A, smem, stream);
-        return launch_ec_stream_t<2, 8>(maps, A, smem, stream);
+        if (bch == 1) return launch_ec_stream_t<2, 1>(maps, A, smem, max_ctas, stream);
+        if (bch == 4) return launch_ec_stream_t<2, 4>(maps, A, smem, max_ctas, stream);
+        return launch_ec_stream_t<2, 8>(maps, A, smem, max_ctas, stream);
     }
-    if (bch == 1) return launch_ec_stream_t<1, 1>(maps, A, smem, stream);
-    if (bch == 4) return launch_ec_stream_t<1, 4>(maps, A, smem, stream);
-    return launch_ec_stream_t<1, 8>(maps, A, smem, stream);
+    if (bch == 1) return launch_ec_stream_t<1, 1>(maps, A, smem, max_ctas, stream);
+    if (bch == 4) return launch_ec_stream_t<1, 4>(maps, A, smem, max_ctas, stream);
+    return launch_ec_stream_t<1, 8>(maps, A, smem, max_ctas, stream);
 }
 
 // Workspace of the column-sum pass for `njobs` linears sharing X8 [T, K].
@@ -1260,7 +1264,7 @@ static size_t xsum_workspace_bytes(int64_t T, int64_t K, int njobs) {
 
 template <typename CodeT>
 static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
-                          int ec_mode, void* workspace, size_t workspace_bytes, int* d_status,
+                          int ec_mode, void* workspace, size_t workspace_bytes, int max_ctas, int* d_status,
                           cudaStream_t stream) {
     const int64_t B = T / S, ntc = s3r_cdiv(N, kTile), ntr = s3r_cdiv(T, kTile);
     const bool two = ec_mode == S3R_EC_TWO_WAY || ec_mode == S3R_EC_DW_ONLY;     // input side: xsum, p
@@ -1303,7 +1307,8 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
         S3R_CHECK_LAUNCH();
     }
     if (ec_mode != S3R_EC_NONE && K > 0 && sizeof(CodeT) == 2) {
-        const int st = launch_ec_stream(jobs, nj, T, N, S, K, X8, weight, two, xs, ps, counter, d_status, stream);
+        const int st =
+            launch_ec_stream(jobs, nj, T, N, S, K, X8, weight, two, xs, ps, counter, max_ctas, d_status, stream);
         if (st <= 0) return st;   // launched (0) or failed (< 0); 1: the kernels below
     }
     if (ec_mode == S3R_EC_NONE || K == 0 || !vec_w || !weight) {
@@ -1382,7 +1387,7 @@ static int launch_factors(const EcJob* jobs, int nj, int64_t T, int64_t N, int64
 // two-linear path of the FFN block.
 static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int64_t S, int64_t K, const void* X8,
                            int code_format, int ec_mode, void* workspace, size_t workspace_bytes,
-                           int* d_status, cudaStream_t stream) {
+                           int* d_status, cudaStream_t stream, int max_ctas = 0) {
     if (T < 0 || N < 0 || K < 0 || S <= 0) return S3R_ERR_ARG;
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     if (ec_mode < S3R_EC_NONE || ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
@@ -1399,9 +1404,10 @@ static int ec_correct_jobs(const EcJob* jobs, int nj, int64_t T, int64_t N, int6
     }
     if (input && K > 0 && !X8) return S3R_ERR_ARG;
     if (code_format == S3R_CODES_F16)
-        return launch_factors<__half>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, d_status,
-                                      stream);
-    return launch_factors<int8_t>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, d_status, stream);
+        return launch_factors<__half>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, max_ctas,
+                                      d_status, stream);
+    return launch_factors<int8_t>(jobs, nj, T, N, S, K, X8, ec_mode, workspace, workspace_bytes, max_ctas, d_status,
+                                  stream);
 }
 
 }  // namespace s3r
@@ -1429,6 +1435,16 @@ extern "C" int s3r_ec_correct(const float* tok_err_part, const float* col_err_pa
                            stream);
 }
 
+int s3r_ec_correct_capped(const float* tok_err_part, const float* col_err_part, int64_t T, int64_t N, int64_t S,
+                          const void* W8, int64_t K, const void* X8, int code_format, int ec_mode, float* eps,
+                          float* mu, float* colmean, int32_t* rowsum, float* v, int32_t* xsum, float* p,
+                          void* workspace, size_t workspace_bytes, int max_ctas, int* d_status,
+                          cudaStream_t stream) {
+    const EcJob job{tok_err_part, col_err_part, W8, eps, mu, colmean, rowsum, v, xsum, p};
+    return ec_correct_jobs(&job, 1, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, d_status,
+                           stream, max_ctas);
+}
+
 // The two linears of the SwiGLU block that read the same input X (W1 and W3):
 // the same factors as two s3r_ec_correct calls, bit for bit, in one pass.
 size_t s3r_ec_pair_workspace_size(int64_t T, int64_t K) {
@@ -1441,11 +1457,11 @@ int s3r_ec_correct_pair(const float* tok1, const float* col1, const void* W1_8, 
                         const float* col3, const void* W3_8, float* eps3, float* mu3, float* colmean3,
                         int32_t* rowsum3, float* v3, int32_t* xsum3, float* p3, int64_t T, int64_t N, int64_t S,
                         int64_t K, const void* X8, int code_format, int ec_mode, void* workspace,
-                        size_t workspace_bytes, int* d_status, cudaStream_t stream) {
+                        size_t workspace_bytes, int max_ctas, int* d_status, cudaStream_t stream) {
     const EcJob jobs[2] = {{tok1, col1, W1_8, eps1, mu1, colmean1, rowsum1, v1, xsum1, p1},
                            {tok3, col3, W3_8, eps3, mu3, colmean3, rowsum3, v3, xsum3, p3}};
     return ec_correct_jobs(jobs, 2, T, N, S, K, X8, code_format, ec_mode, workspace, workspace_bytes, d_status,
-                           stream);
+                           stream, max_ctas);
 }
 
 // ---------------------------------------------------------------------------

@@ -190,6 +190,7 @@ struct Block {
     int rm, ec, fmt;
     bool indep;
     uint32_t tid2, tid1, tid3;
+    int ec2_ctas = 0, ec13_ctas = 0;   // grid caps of the EC streaming passes (0: all SMs)
 };
 
 int make_block(Block& b, const s3r_ffn_args& a, void* ws, size_t ws_bytes, uint32_t tid_base) {
@@ -229,8 +230,9 @@ int step_ec_w2(Block& b, cudaStream_t stream) {
     if (b.ec == S3R_EC_NONE) return S3R_OK;
     const s3r_ffn_args& a = b.a;
     LinearWs& L2 = b.Lo.w2;
-    return s3r_ec_correct(L2.tok, L2.col, a.T, a.d, a.S, a.W2_8, a.F, a.A8, b.fmt, b.ec, L2.eps, L2.mu, L2.colmean,
-                          L2.rowsum, L2.v, L2.xsum, L2.p, b.Lo.ec_ws, b.Lo.ec_ws_bytes, a.d_status, stream);
+    return s3r_ec_correct_capped(L2.tok, L2.col, a.T, a.d, a.S, a.W2_8, a.F, a.A8, b.fmt, b.ec, L2.eps, L2.mu,
+                                 L2.colmean, L2.rowsum, L2.v, L2.xsum, L2.p, b.Lo.ec_ws, b.Lo.ec_ws_bytes, b.ec2_ctas,
+                                 a.d_status, stream);
 }
 
 // 3. dA = Q2 W2_8^T (rescaled, corrected, / s_a)  [T, F]
@@ -316,7 +318,7 @@ int step_ec_w13(Block& b, cudaStream_t stream) {
     LinearWs &L1 = b.Lo.w1, &L3 = b.Lo.w3;
     return s3r_ec_correct_pair(L1.tok, L1.col, a.W1_8, L1.eps, L1.mu, L1.colmean, L1.rowsum, L1.v, L1.xsum, L1.p,
                                L3.tok, L3.col, a.W3_8, L3.eps, L3.mu, L3.colmean, L3.rowsum, L3.v, L3.xsum, L3.p,
-                               a.T, a.F, a.S, a.d, a.X8, b.fmt, b.ec, b.Lo.ec_ws, b.Lo.ec_ws_bytes,
+                               a.T, a.F, a.S, a.d, a.X8, b.fmt, b.ec, b.Lo.ec_ws, b.Lo.ec_ws_bytes, b.ec13_ctas,
                                a.d_status, stream);
 }
 
@@ -611,6 +613,26 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     }
     const bool f16 = fmt == S3R_CODES_F16;
     const size_t nb = blocks.size();
+    // The experts' EC passes on the side streams: blocks i and i + kSideStreams share a stream, so the
+    // blocks of round i / kSideStreams run side by side; each takes a share of the SMs in proportion
+    // to the codes it streams (weight side + its rows' input side), instead of all of them.
+    {
+        const int sms = s3r_sm_count();
+        for (size_t r0 = 0; r0 < nb; r0 += kSideStreams) {
+            const size_t r1 = std::min(nb, r0 + (size_t)kSideStreams);
+            double w2 = 0.0, w13 = 0.0;
+            for (size_t i = r0; i < r1; ++i) {
+                w2 += (double)F * d + (double)blocks[i].a.T * F;
+                w13 += 2.0 * d * F + (double)blocks[i].a.T * d;
+            }
+            for (size_t i = r0; i < r1; ++i) {
+                const double my2 = (double)F * d + (double)blocks[i].a.T * F;
+                const double my13 = 2.0 * d * F + (double)blocks[i].a.T * d;
+                blocks[i].ec2_ctas = std::max(8, (int)(sms * my2 / w2));
+                blocks[i].ec13_ctas = std::max(8, (int)(sms * my13 / w13));
+            }
+        }
+    }
     S3R_TRY(record(a, 0, stream));
     S3R_TRY(run_on_side_streams(blocks, step_quantize_dy, stream));
     S3R_TRY(record(a, 1, stream));
