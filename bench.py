@@ -46,12 +46,12 @@ E2E_IN_STREAMS = 3   # streams carrying the e2e input copies (one stream: 0.55 M
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the two GEMM launches of one
 # ffn_backward step, divided by the step's six products, from a one-pass ncu capture of
 #   python bench.py --kernel-case ffn --block <block> --steps 1 --warmup 1
-# on a GB300; keyed by the sha256 of the GEMM source it was taken on, so that it is reported
-# only while that kernel is unchanged, then by block.
+# on a GB300; keyed by the sha256 of the GEMM sources it was taken on (the kernel, then the tile
+# deal), so that it is reported only while they are unchanged, then by block.
 GEMM_TRAFFIC = {
-    "2008acc8d0099cce946586c468362841c378116f1db29f704f85ba68f8d3f668": {
-        "swiglu_ffn_d4096_F14336_T16384": 2368.3e6,   # dA + dW2 4625 MB, dX1 + dX3 + dW1 + dW3 9584 MB
-        "swiglu_ffn_d2048_F5632_T8192": 209.1e6,      # 444.7 MB and 809.7 MB
+    "8e8c1dafe7b0a96ca2b0f918c7f71b02e0250f042eb21bfbbf09ccee94839d98": {
+        "swiglu_ffn_d4096_F14336_T16384": 2237.7e6,   # dA + dW2 4398 MB, dX1 + dX3 + dW1 + dW3 9028 MB
+        "swiglu_ffn_d2048_F5632_T8192": 209.5e6,      # 441.5 MB and 815.4 MB
     },
 }
 
@@ -380,12 +380,14 @@ def gemm_traffic(blk):
     """DRAM bytes per GEMM product of block `blk` from the recorded ncu capture,
     or None when the GEMM source changed since it was taken."""
     import hashlib
-    src = os.path.join(ROOT, "stochastic_rounding_int8_gb300", "csrc", "gemm_umma.cu")
+    csrc = os.path.join(ROOT, "stochastic_rounding_int8_gb300", "csrc")
+    h = hashlib.sha256()
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        for f in ("gemm_umma.cu", "deal_plan.h"):   # the kernel and the tile deal it walks
+            h.update(open(os.path.join(csrc, f), "rb").read())
     except OSError:
         return None
-    return GEMM_TRAFFIC.get(h, {}).get(blk.name)
+    return GEMM_TRAFFIC.get(h.hexdigest(), {}).get(blk.name)
 
 
 def add_traffic(roof, blk):

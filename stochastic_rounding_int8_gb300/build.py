@@ -44,7 +44,8 @@ def _stale(obj: str, src: str, headers: list[str]) -> bool:
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    headers = glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "s3r.h")]
+    headers = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+               + [os.path.join(ROOT, "include", "s3r.h")])
     srcs = sources()
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
     extra = list(extra or [])

@@ -56,6 +56,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "deal_plan.h"
 
 namespace s3r {
 namespace umma {
@@ -208,6 +209,10 @@ struct Args {
     int total_tiles;
     int* d_status;
     Glue glue;
+    // How problem i's tiles are dealt to the CTAs of a mixed launch (next_tile):
+    // first deal_m[i] rounds over the deal_w[i] CTAs deal_s[i], deal_s[i] + 1, ...
+    // (cyclic), then round robin over all CTAs from deal_s[i].
+    int deal_s[kMaxProb], deal_w[kMaxProb], deal_m[kMaxProb];
 };
 struct Maps {
     CUtensorMap m[kMaxProb][5];
@@ -957,12 +962,60 @@ __host__ __device__ __forceinline__ void tile_coords(int tile, int ntm, int ntn,
     tn = in / rows;
 }
 
-// The problem that owns launch tile `tile` (tiles of problem i start at
+// The next tile of CTA b (of G) in the launch: problems in order, within a
+// problem the CTA's tiles of the deal (Args::deal_s) in increasing
+// order.  (p, k): the caller's position, zero-initialized.  Every role of the
+// CTA walks the same sequence.
+__device__ __forceinline__ bool next_tile(const Args& A, int b, int G, int& p, int& k, int& tile) {
+    while (p < A.nprob) {
+        const Problem& P = A.prob[p];
+        int t;
+        if (deal::kth_tile(P.ntm * P.ntn, A.deal_s[p], A.deal_w[p], A.deal_m[p], b, G, k, t)) {
+            tile = P.tile_base + t;
+            ++k;
+            return true;
+        }
+        ++p;
+        k = 0;
+    }
+    return false;
+}
+
+// The launch problem that owns launch tile `tile` (tiles of problem i start at
 // prob[i].tile_base, in increasing order).
 __device__ __forceinline__ int problem_of(const Args& A, int tile) {
     int i = 0;
     while (i + 1 < A.nprob && tile >= A.prob[i + 1].tile_base) ++i;
     return i;
+}
+
+// A CTA's walk over its tiles, as launch tile indices (ntiles: past the last).
+// Mixed launches (problems with tiles of different lengths) walk the host's
+// deal, (p, k) holding the current tile's problem and its place in the deal;
+// the others, whose deal is plain round robin, step the index by the grid.
+template <bool DEAL>
+__device__ __forceinline__ int first_tile(const Args& A, int ntiles, int& p, int& k) {
+    if constexpr (DEAL) {
+        int t;
+        return next_tile(A, (int)blockIdx.x, (int)gridDim.x, p, k, t) ? t : ntiles;
+    } else {
+        return (int)blockIdx.x;
+    }
+}
+template <bool DEAL>
+__device__ __forceinline__ int following_tile(const Args& A, int ntiles, int& p, int& k, int tile) {
+    if constexpr (DEAL) {
+        int t;
+        return next_tile(A, (int)blockIdx.x, (int)gridDim.x, p, k, t) ? t : ntiles;
+    } else {
+        return tile + (int)gridDim.x;
+    }
+}
+// The problem of the walk's current tile.
+template <bool DEAL>
+__device__ __forceinline__ int tile_problem(const Args& A, int p, int tile) {
+    if constexpr (DEAL) return p;
+    else return problem_of(A, tile);
 }
 
 // 12 warps: one SM sub-partition hosts three of them, one per warpgroup, so the
@@ -1020,10 +1073,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     volatile int* abrt = &abort_flag;
 
-    // Persistent: this CTA owns tiles blockIdx.x, blockIdx.x + gridDim.x, ...;
-    // tiles run along N first.  The smem ring and the TMEM double buffer keep
-    // their phases across tiles, so the next tile's copies and MMAs start while
-    // the epilogue still stores the previous tile.
+    // Persistent: this CTA walks the tiles the host's deal gives it (next_tile).
+    // The smem ring and the TMEM double buffer keep their phases across tiles,
+    // so the next tile's copies and MMAs start while the epilogue still stores
+    // the previous tile.
     if (warp < EPI_WARP0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI == kMixedG ? kRegsLowGlue : kRegsLow));
         if (warp == 0) {
@@ -1031,8 +1084,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int it = 0;   // slice counter over the whole persistent run
                 int last_pi = -1;
                 bool ok = true;
-                for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                    const int pi = problem_of(A, tile);
+                int sp = 0, sk = 0;
+                for (int tile = first_tile<MIXED>(A, ntiles, sp, sk); tile < ntiles && ok;
+                     tile = following_tile<MIXED>(A, ntiles, sp, sk, tile)) {
+                    const int pi = tile_problem<MIXED>(A, sp, tile);
                     const Problem& P = A.prob[pi];
                     const CUtensorMap* mp = &maps.m[pi][0];
                     const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
@@ -1101,8 +1156,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) {
                 int it = 0, gkb = 0;   // slice and block counters over the whole run
                 bool ok = true;
-                for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                    const Problem& P = A.prob[problem_of(A, tile)];
+                int sp = 0, sk = 0;
+                for (int tile = first_tile<MIXED>(A, ntiles, sp, sk); tile < ntiles && ok;
+                     tile = following_tile<MIXED>(A, ntiles, sp, sk, tile)) {
+                    const Problem& P = A.prob[tile_problem<MIXED>(A, sp, tile)];
                     const int nkb = (int)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128));
                     const bool a_mn = MIXED ? P.kind == kDW : (EPI == kFwdE ? false : MN);
                     const bool b_mn = MIXED ? P.kind == kDW : (EPI == kFwdE ? true : MN);
@@ -1154,8 +1211,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int ht = threadIdx.x - 64;
             uint32_t sph = 0;   // side-buffer cycles so far (the same count on the epilogue side)
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const Problem& P = A.prob[problem_of(A, tile)];
+            int sp = 0, sk = 0;
+            for (int tile = first_tile<MIXED>(A, ntiles, sp, sk); tile < ntiles && ok;
+                 tile = following_tile<MIXED>(A, ntiles, sp, sk, tile)) {
+                const Problem& P = A.prob[tile_problem<MIXED>(A, sp, tile)];
                 int tm, tn;
                 tile_coords(tile - P.tile_base, P.ntm, P.ntn, P.band_rows, tm, tn);
                 const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
@@ -1168,7 +1227,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const Glue* G = (EPI == kMixedG && problem_of(A, tile) == A.glue.prob) ? &A.glue : nullptr;
+                    const Glue* G = (EPI == kMixedG && tile_problem<MIXED>(A, sp, tile) == A.glue.prob) ? &A.glue : nullptr;
                     if (dw) load_side<kDW>(P, sSide, m0, n0, ht, r, nullptr);
                     else load_side<kDX>(P, sSide, m0, n0, ht, r, G);
                     mbar_arrive(side_full);
@@ -1188,8 +1247,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t sph = 0;   // side-buffer cycles so far (the same count on the helper side)
         uint32_t gph = 0;   // glue tiles this warpgroup has finished (phase of its exchange barriers)
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const int pi = problem_of(A, tile);
+        int sp = 0, sk = 0;
+        for (int tile = first_tile<MIXED>(A, ntiles, sp, sk); tile < ntiles && ok;
+             tile = following_tile<MIXED>(A, ntiles, sp, sk, tile)) {
+            const int pi = tile_problem<MIXED>(A, sp, tile);
             const Problem& P = A.prob[pi];
             const int nkb0 = (int)s3r_cdiv(P.seg[0].K, 128), nkb1 = (int)s3r_cdiv(P.seg[1].K, 128);
             const int nkb = nkb0 + nkb1;
@@ -1509,6 +1570,31 @@ static int launch(const Maps& maps, Args& A, const double (*strip)[2], cudaStrea
     A.total_tiles = (int)total;
     if (total == 0) return S3R_OK;
     const int64_t grid = total < sms ? total : sms;   // persistent: one CTA per SM
+    if (EPI == kMixed || EPI == kMixedG) {
+        // the static deal of a mixed launch: a tile costs its 128-wide blocks plus about six
+        // blocks' worth of tile end
+        int64_t n[kMaxProb];
+        double c[kMaxProb];
+        deal::Plan plan[kMaxProb];
+        for (int i = 0; i < A.nprob; ++i) {
+            const Problem& P = A.prob[i];
+            n[i] = (int64_t)P.ntm * P.ntn;
+            c[i] = (double)(s3r_cdiv(P.seg[0].K, 128) + s3r_cdiv(P.seg[1].K, 128)) + 6.0;
+        }
+        deal::plan(A.nprob, n, c, (int)grid, plan);
+        for (int i = 0; i < A.nprob; ++i) {
+            A.deal_s[i] = plan[i].s;
+            A.deal_w[i] = plan[i].w;
+            A.deal_m[i] = plan[i].m;
+        }
+    } else {
+        // the other kernels step the launch-wide tile index by the grid (walk<false>)
+        for (int i = 0; i < A.nprob; ++i) {
+            A.deal_s[i] = (int)(A.prob[i].tile_base % grid);
+            A.deal_w[i] = (int)grid;
+            A.deal_m[i] = 0;
+        }
+    }
     umma_gemm_kernel<EPI, MN><<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(maps, A);
     S3R_CHECK_LAUNCH();
     return S3R_OK;
