@@ -245,15 +245,22 @@ def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse
     return max_over_ranks(ms, world), launches, seg
 
 
-def time_e2e(s3r, blk, inp, ops, steps, warmup, world):
+E2E_CODES = ("X8", "A8", "W1_8", "W3_8", "W2_8")
+
+
+def time_e2e(s3r, blk, inp, ops, steps, warmup, world, int8_at_rest=True):
     """Same step through the C ABI with HOST buffers: every step copies all of
     its inputs from pinned host memory to the device, runs the backward, and
     copies all four gradients back, inside the timed region.  The copies run
     on their own streams, double-buffered, so step i's input copy and step
     i - 1's gradient copy overlap step i - 1's and step i's backward (the
-    way a training loop feeds a device); events order the buffers' reuse."""
+    way a training loop feeds a device); events order the buffers' reuse.
+    int8_at_rest: the operand codes live in host memory as int8 (half the
+    bytes over the host link) and the call widens them on the device
+    (S3R_CODES_S8_F16); otherwise they are copied as fp16 codes."""
     T, d, F, S = blk.T, blk.d, blk.F, blk.S
-    host_in = {k: getattr(ops, k).cpu().pin_memory() for k in
+    conv = (lambda k, t: t.to(torch.int8) if k in E2E_CODES else t) if int8_at_rest else (lambda k, t: t)
+    host_in = {k: conv(k, getattr(ops, k)).cpu().pin_memory() for k in
                ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2", "h1", "h3")}
     host_in["dY"] = inp.dY.pin_memory()
     dev_in = [{k: torch.empty_like(v, device="cuda") for k, v in host_in.items()} for _ in range(2)]
@@ -261,8 +268,8 @@ def time_e2e(s3r, blk, inp, ops, steps, warmup, world):
     grads = [s3r.alloc_ffn_grads(T, d, F) for _ in range(2)]
     host_out = [{k: torch.empty(getattr(grads[0], k).shape, dtype=torch.float32).pin_memory()
                  for k in ("dX", "dW1", "dW3", "dW2")} for _ in range(2)]
-    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, code_format=s3r.code_format_of(ops.X8)), dtype=torch.uint8,
-                     device="cuda")
+    fmt = s3r.CODES_S8_F16 if int8_at_rest else s3r.code_format_of(ops.X8)
+    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, code_format=fmt), dtype=torch.uint8, device="cuda")
     bi = sum(v.numel() * v.element_size() for v in host_in.values())
     bo = sum(v.numel() * v.element_size() for v in host_out[0].values())
     # the input copies spread over N_IN streams (balanced by bytes), so several copy engines share them
@@ -295,7 +302,8 @@ def time_e2e(s3r, blk, inp, ops, steps, warmup, world):
                 s_comp.wait_event(in_done[b][j])
             if used[b]:
                 s_comp.wait_event(out_done[b])   # step i - 2's gradients have left the device
-            s3r.ffn_backward(dops[b], dev_in[b]["dY"], S, seed=i, grads=grads[b], workspace=ws, stream=s_comp)
+            s3r.ffn_backward(dops[b], dev_in[b]["dY"], S, seed=i, grads=grads[b], workspace=ws, stream=s_comp,
+                             widen_codes=int8_at_rest)
             comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -677,10 +685,14 @@ def run_ours(args, world, rank, local):
     line["e2e"] = {"value": round(world * blk.T * e2e_steps / (ems * 1e-3), 1), "unit": "tokens/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
                    "copies": "every step copies all inputs in and all four gradients out; the copies run on their "
-                             "own streams, double-buffered, overlapping the neighbouring steps' backward"}
+                             "own streams, double-buffered, overlapping the neighbouring steps' backward",
+                   "operand_codes_at_rest": "int8 (ffn_backward widens them on the device, S3R_CODES_S8_F16)"}
     if not args.no_context and rank == 0:
         ctx = mode_context(s3r, blk, ops, dY, inp)
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / r["ms_per_step"], 3)
+        ems16, bi16, bo16 = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world, int8_at_rest=False)
+        ctx["e2e_fp16_codes_at_rest"] = {"tokens_s": round(world * blk.T * e2e_steps / (ems16 * 1e-3), 1),
+                                         "h2d_bytes_per_step": bi16, "d2h_bytes_per_step": bo16}
         ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / r["ms_per_step"], 3)
         # what keeping the activation gradient dA in fp32 costs: written by the dA GEMM, read by the
         # SwiGLU quantizer (the fused-glue variant above avoids it but stalls the GEMM instead)

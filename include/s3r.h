@@ -100,8 +100,10 @@ enum s3r_round_mode {
  * (TMA straight into the MMA's shared-memory layout, no conversion pass).
  * Both products of one layer must use the same format. */
 enum s3r_code_format {
-    S3R_CODES_S8 = 0,   /* int8_t [rows, cols] */
-    S3R_CODES_F16 = 1   /* IEEE fp16 [rows, cols], integer valued; cols % 8 == 0 for the GEMMs */
+    S3R_CODES_S8 = 0,     /* int8_t [rows, cols] */
+    S3R_CODES_F16 = 1,    /* IEEE fp16 [rows, cols], integer valued; cols % 8 == 0 for the GEMMs */
+    S3R_CODES_S8_F16 = 2  /* ffn_backward only: the operand codes at rest as int8_t (half the bytes
+                             of F16), widened to fp16 inside the call; computed as F16 */
 };
 
 /* Scale granularity of rtne_quantize. */
@@ -498,6 +500,17 @@ int ffn_forward(const struct s3r_ffn_fwd_args* args, cudaStream_t stream);
  * All buffers are device pointers owned by the caller; `args` itself is a
  * HOST pointer read during the call only.
  *
+ * code_format S3R_CODES_S8_F16: X8, A8, W1_8, W3_8 and W2_8 hold int8_t codes
+ * (any alignment); the call first copies them, widened to fp16 (exact: every
+ * int8 value is an fp16 integer), into the tail of the workspace, then runs
+ * the S3R_CODES_F16 block on the copies.  Every result, and every
+ * intermediate s3r_ffn_workspace_offsets points at (fp16 codes), equals the
+ * S3R_CODES_F16 call on the same codes bit for bit; d and F must be
+ * multiples of 8 (S3R_ERR_ALIGN).  The widening runs before the first step
+ * event.  The workspace functions take the same
+ * code_format and add 2 bytes per operand code (plus alignment) to the
+ * S3R_CODES_F16 size.
+ *
  * Grouped (mixture-of-experts) mode, num_groups = E > 0 (the MoE models of
  * [S3R] §IV; the pages give no grouping rule, so the plain one): the T rows
  * of dY, h1, h3, X8/s_x, A8/s_a and dX are routed rows sorted by expert, and
@@ -575,7 +588,8 @@ int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
  *   [2] Q1 codes [T, F]   [3] Q1 tile scales [ceil(T/128), ceil(F/128)]
  *   [4] Q3 codes [T, F]   [5] Q3 tile scales
  *   [6] dA [T, F] fp32 (the activation gradient of W2, input of the glue)
- * codes in `code_format`, all row-major with the listed widths.  num_groups
+ * codes in `code_format` (fp16 for S3R_CODES_S8_F16, whose block runs on
+ * fp16 codes), all row-major with the listed widths.  num_groups
  * = 0: the dense block (T, S as in ffn_backward).  num_groups = E > 0: the
  * block of expert `group` (0 <= group < E) under the HOST group_offsets of
  * the grouped call (T and S ignored; the shapes use the group's row count).

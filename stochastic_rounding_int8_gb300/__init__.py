@@ -37,8 +37,9 @@ AXIS_ROW, AXIS_COL, AXIS_TILE = 0, 1, 2
 TID_W2, TID_W1, TID_W3, RHS_ID_OFFSET = 0, 1, 2, 0x100
 MOE_TID_STRIDE = 16   # grouped mode: expert e uses tensor ids 16 e + (0, 1, 2)
 CODES_S8, CODES_F16 = 0, 1
+CODES_S8_F16 = 2   # ffn_backward only: int8 operand codes widened to fp16 inside the call
 DEFAULT_CODES = CODES_F16
-_CODE_DTYPE = {CODES_S8: torch.int8, CODES_F16: torch.float16}
+_CODE_DTYPE = {CODES_S8: torch.int8, CODES_F16: torch.float16, CODES_S8_F16: torch.float16}
 
 _lib = None
 
@@ -636,17 +637,23 @@ def alloc_moe_grads(R, E, d, F, device="cuda") -> FFNGrads:
 
 def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, seed=0,
                  grads: FFNGrads | None = None, workspace=None, status=None, stream=None,
-                 step_events=None, group_offsets=None, fuse_glue=False) -> FFNGrads:
+                 step_events=None, group_offsets=None, fuse_glue=False, widen_codes=False) -> FFNGrads:
     """step_events: optional list of FFN_NUM_EVENTS torch.cuda.Event (timing).
     group_offsets: grouped (mixture-of-experts) mode, a list of E + 1 row
     offsets of the expert-sorted rows; the weights in `ops` are then stacked
     per expert and S is ignored.  fuse_glue: run the SwiGLU glue and the
     quantization of dh1, dh3 inside the dA GEMM's epilogue (S3R_FFN_FUSE_GLUE;
-    dense block with fp16 codes, not independent SR; dA is then not kept)."""
+    dense block with fp16 codes, not independent SR; dA is then not kept).
+    widen_codes: int8 operand codes in `ops` run as fp16 codes (S3R_CODES_S8_F16:
+    widened inside the call, results equal to the fp16-code call)."""
     T, d = dY.shape
     F = ops.A8.shape[1]
     dev = dY.device
     fmt = code_format_of(ops.X8)
+    if widen_codes:
+        if fmt != CODES_S8:
+            raise ValueError("widen_codes takes int8 operand codes")
+        fmt = CODES_S8_F16
     if group_offsets is not None:
         offs = [int(o) for o in group_offsets]
         E = len(offs) - 1

@@ -173,10 +173,19 @@ FfnLayout layout(void* base, size_t bytes, int64_t T, int64_t d, int64_t F, int6
 
 }  // namespace
 
+// S3R_CODES_S8_F16: the fp16 copies of the five operand code tensors follow the
+// fp16 block's workspace (E experts' stacked weights in grouped mode).
+size_t widen_bytes(int64_t T, int64_t d, int64_t F, int64_t E) {
+    auto r = [](int64_t b) { return (size_t)((b + 255) / 256 * 256); };
+    return 255 + r(2 * T * d) + r(2 * T * F) + 2 * r(2 * E * d * F) + r(2 * E * F * d);
+}
+
 extern "C" size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
                                          int code_format) {
     (void)ec_mode;
     if (T <= 0 || d <= 0 || F <= 0 || S <= 0 || T % S != 0) return 0;
+    if (code_format == S3R_CODES_S8_F16)
+        return layout(nullptr, 0, T, d, F, S, round_mode, S3R_CODES_F16).total + widen_bytes(T, d, F, 1);
     return layout(nullptr, 0, T, d, F, S, round_mode, code_format).total;
 }
 
@@ -480,6 +489,9 @@ extern "C" size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, i
     if (!group_offsets || num_groups <= 0 || d <= 0 || F <= 0) return 0;
     for (int64_t e = 0; e < num_groups; ++e)
         if (group_offsets[e + 1] < group_offsets[e]) return 0;
+    if (code_format == S3R_CODES_S8_F16)
+        return grouped_bytes(group_offsets, num_groups, d, F, round_mode, S3R_CODES_F16) +
+               widen_bytes(group_offsets[num_groups] - group_offsets[0], d, F, num_groups);
     return grouped_bytes(group_offsets, num_groups, d, F, round_mode, code_format);
 }
 
@@ -487,6 +499,7 @@ extern "C" int s3r_ffn_workspace_offsets(int64_t T, int64_t d, int64_t F, int64_
                                          int code_format, const int64_t* group_offsets, int64_t num_groups,
                                          int64_t group, size_t* out) {
     if (!out || d <= 0 || F <= 0) return S3R_ERR_ARG;
+    if (code_format == S3R_CODES_S8_F16) code_format = S3R_CODES_F16;   // the widened block runs on fp16 codes
     if (code_format != S3R_CODES_S8 && code_format != S3R_CODES_F16) return S3R_ERR_ARG;
     uintptr_t base = 0;   // offsets from a 256-byte aligned workspace base
     if (num_groups > 0) {
@@ -511,20 +524,124 @@ extern "C" int s3r_ffn_workspace_offsets(int64_t T, int64_t d, int64_t F, int64_
     return S3R_OK;
 }
 
-extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
+namespace {
+
+// The host checks of ffn_backward that need no workspace carve: sizes, modes,
+// pointers, the example split (dense) or the row offsets (grouped).
+int check_block_args(const s3r_ffn_args* a) {
     if (!a) return S3R_ERR_ARG;
     const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
     if (T <= 0 || d <= 0 || F <= 0) return S3R_ERR_ARG;
     if (a->round_mode < S3R_ROUND_RTNE || a->round_mode > S3R_ROUND_BCAST) return S3R_ERR_ARG;
     if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
-    if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16) return S3R_ERR_ARG;
-    const int fmt = a->code_format;
+    if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16 && a->code_format != S3R_CODES_S8_F16)
+        return S3R_ERR_ARG;
     if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->A8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 ||
         !a->dW2 || !a->dW3)
         return S3R_ERR_ARG;
     if (a->num_groups == 0) {
         if (S <= 0) return S3R_ERR_ARG;
         if (T % S != 0 || (S % S3R_TILE != 0 && S != T)) return S3R_ERR_SHAPE;
+        return S3R_OK;
+    }
+    const int64_t E = a->num_groups;
+    const int64_t* off = a->group_offsets;
+    if (E < 0 || !off || off[0] != 0 || off[E] != T) return S3R_ERR_ARG;
+    for (int64_t e = 0; e < E; ++e)
+        if (off[e + 1] < off[e]) return S3R_ERR_ARG;
+    if (E > (int64_t)(0xFFFFFFFFu / S3R_MOE_TID_STRIDE)) return S3R_ERR_ARG;
+    return S3R_OK;
+}
+
+// int8 codes to the same integers in fp16, four at a time: the bytes, offset
+// by 128, become the low mantissa bits of 0x6400 (1024 + u exactly), and one
+// subtraction of 1152 leaves u - 128, the code, without rounding.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+struct WidenJob {
+    const int8_t* src;
+    uint16_t* dst;   // 16-byte aligned
+    int64_t n;
+};
+struct WidenJobs {
+    WidenJob j[5];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) widen_codes_kernel(const WidenJobs J) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nth = (int64_t)gridDim.x * blockDim.x;
+    for (int s = 0; s < J.n; ++s) {
+        const WidenJob w = J.j[s];
+        const int64_t n16 = ((uintptr_t)w.src & 15u) == 0 ? w.n / 16 : 0;
+        const uint4* src = reinterpret_cast<const uint4*>(w.src);
+        uint4* dst = reinterpret_cast<uint4*>(w.dst);
+        for (int64_t i = tid; i < n16; i += nth) {
+            const uint4 v = __ldcs(src + i);
+            uint4 a, b;
+            widen4(v.x, a.x, a.y);
+            widen4(v.y, a.z, a.w);
+            widen4(v.z, b.x, b.y);
+            widen4(v.w, b.z, b.w);
+            dst[2 * i] = a;
+            dst[2 * i + 1] = b;
+        }
+        for (int64_t i = n16 * 16 + tid; i < w.n; i += nth) {
+            uint32_t lo, hi;
+            widen4((uint32_t)(uint8_t)w.src[i], lo, hi);
+            w.dst[i] = (uint16_t)(lo & 0xFFFFu);
+        }
+    }
+}
+
+// S3R_CODES_S8_F16: widens X8, A8, W1_8, W3_8 and W2_8 into the tail of the
+// workspace, then runs the fp16-code block on the copies.
+int ffn_backward_widened(const s3r_ffn_args* a, cudaStream_t stream) {
+    const int64_t T = a->T, d = a->d, F = a->F;   // the arguments passed check_block_args
+    const bool grouped = a->num_groups > 0;
+    const int64_t E = grouped ? a->num_groups : 1;
+    if (d % 8 != 0 || F % 8 != 0) return S3R_ERR_ALIGN;   // the fp16-code GEMMs' rows
+    const size_t base = grouped ? s3r_ffn_grouped_workspace_size(a->group_offsets, E, d, F, a->round_mode,
+                                                                  a->ec_mode, S3R_CODES_F16)
+                                : s3r_ffn_workspace_size(T, d, F, a->S, a->round_mode, a->ec_mode, S3R_CODES_F16);
+    if (base == 0) return S3R_ERR_ARG;
+    if (!a->workspace || a->workspace_bytes < base + widen_bytes(T, d, F, E)) return S3R_ERR_WORKSPACE;
+    s3r_ffn_args w = *a;
+    w.code_format = S3R_CODES_F16;
+    w.workspace_bytes = base;
+    uintptr_t p = ((uintptr_t)a->workspace + base + 255) & ~(uintptr_t)255;
+    WidenJobs J{};
+    const void* src[5] = {a->X8, a->A8, a->W1_8, a->W3_8, a->W2_8};
+    const int64_t n[5] = {T * d, T * F, E * d * F, E * d * F, E * F * d};
+    const void** dst[5] = {&w.X8, &w.A8, &w.W1_8, &w.W3_8, &w.W2_8};
+    for (int i = 0; i < 5; ++i) {
+        J.j[i] = WidenJob{static_cast<const int8_t*>(src[i]), reinterpret_cast<uint16_t*>(p), n[i]};
+        *dst[i] = reinterpret_cast<const void*>(p);
+        p += (uintptr_t)((2 * n[i] + 255) / 256 * 256);
+    }
+    J.n = 5;
+    const int64_t total16 = (T * (d + F) + 3 * E * d * F) / 16;
+    const int64_t cap = (int64_t)s3r_sm_count() * 8;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(cap, (total16 + 255) / 256));
+    widen_codes_kernel<<<grid, 256, 0, stream>>>(J);
+    S3R_CHECK_LAUNCH();
+    return ffn_backward(&w, stream);
+}
+
+}  // namespace
+
+extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
+    S3R_TRY(check_block_args(a));
+    if (a->code_format == S3R_CODES_S8_F16) return ffn_backward_widened(a, stream);
+    const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
+    const int fmt = a->code_format;
+    if (a->num_groups == 0) {
         if (!a->workspace || a->workspace_bytes < s3r_ffn_workspace_size(T, d, F, S, a->round_mode, a->ec_mode, fmt))
             return S3R_ERR_WORKSPACE;
         Block b;
@@ -582,10 +699,6 @@ extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     // one multi-problem launch over the experts.
     const int64_t E = a->num_groups;
     const int64_t* off = a->group_offsets;
-    if (E < 0 || !off || off[0] != 0 || off[E] != T) return S3R_ERR_ARG;
-    for (int64_t e = 0; e < E; ++e)
-        if (off[e + 1] < off[e]) return S3R_ERR_ARG;
-    if (E > (int64_t)(0xFFFFFFFFu / S3R_MOE_TID_STRIDE)) return S3R_ERR_ARG;
     if (!a->workspace || a->workspace_bytes < grouped_bytes(off, E, d, F, a->round_mode, fmt))
         return S3R_ERR_WORKSPACE;
     std::vector<Block> blocks;
@@ -736,4 +849,4 @@ extern "C" const char* s3r_status_string(int status) {
     }
 }
 
-extern "C" int s3r_abi_version(void) { return 102; }
+extern "C" int s3r_abi_version(void) { return 103; }

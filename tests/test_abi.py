@@ -33,7 +33,7 @@ def test_status_strings(L):
     for code in range(-1, -9, -1):
         assert s3r.status_string(code).startswith("S3R_ERR_")
     assert s3r.status_string(-99) == "S3R_ERR_UNKNOWN"
-    assert L.s3r_abi_version() == 102
+    assert L.s3r_abi_version() == 103
 
 
 def test_host_argument_checks_need_no_gpu(L):
@@ -160,3 +160,35 @@ def test_ffn_workspace_offsets(L):
     assert int(g2[6]) + 512 * F * 4 <= L.s3r_ffn_grouped_workspace_size(C.cast(arr, C.c_void_p), 3, d, F, 1, 2, 1)
     # the empty expert has no block
     assert L.s3r_ffn_workspace_offsets(0, d, F, 0, 1, 1, C.cast(arr, C.c_void_p), 3, 1, C.cast(g0, C.c_void_p)) == -1
+
+
+def test_widened_codes_workspace_and_checks(L):
+    """S3R_CODES_S8_F16 (int8 operand codes widened inside ffn_backward): its
+    workspace is the fp16 block's plus the five fp16 copies, its intermediates
+    sit where the fp16 block keeps them, and its own checks run before any
+    launch (fake, never-dereferenced pointers)."""
+    r = lambda b: (b + 255) // 256 * 256
+    T, d, F, S = 512, 136, 392, 256
+    f16 = L.s3r_ffn_workspace_size(T, d, F, S, 1, 2, s3r.CODES_F16)
+    wide = L.s3r_ffn_workspace_size(T, d, F, S, 1, 2, s3r.CODES_S8_F16)
+    assert wide == f16 + 255 + r(2 * T * d) + r(2 * T * F) + 3 * r(2 * d * F)
+    offs = [0, 300, 300, 812]
+    arr = (C.c_int64 * 4)(*offs)
+    g16 = L.s3r_ffn_grouped_workspace_size(C.cast(arr, C.c_void_p), 3, d, F, 1, 2, s3r.CODES_F16)
+    gw = L.s3r_ffn_grouped_workspace_size(C.cast(arr, C.c_void_p), 3, d, F, 1, 2, s3r.CODES_S8_F16)
+    assert gw == g16 + 255 + r(2 * 812 * d) + r(2 * 812 * F) + 3 * r(2 * 3 * d * F)
+    a, b = (C.c_size_t * 7)(), (C.c_size_t * 7)()
+    assert L.s3r_ffn_workspace_offsets(T, d, F, S, 1, s3r.CODES_F16, None, 0, 0, C.cast(a, C.c_void_p)) == 0
+    assert L.s3r_ffn_workspace_offsets(T, d, F, S, 1, s3r.CODES_S8_F16, None, 0, 0, C.cast(b, C.c_void_p)) == 0
+    assert list(a) == list(b)
+    fake = C.c_void_p(0x1000)
+
+    def call(d_, F_, ws_bytes):
+        args = s3r._FfnArgs(T, d_, F_, S, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                            fake, s3r.ROUND_S3R, s3r.EC_TWO_WAY, s3r.CODES_S8_F16, 0, fake, fake, fake, fake, fake,
+                            ws_bytes, None, None)
+        return L.ffn_backward(C.byref(args), None)
+    before = L.s3r_kernel_launch_count()
+    assert call(132, F, 1 << 40) == -2                # d not a multiple of 8: the fp16 GEMMs' rows
+    assert call(d, F, wide - 1) == -7                 # the widened copies do not fit
+    assert L.s3r_kernel_launch_count() == before

@@ -81,3 +81,42 @@ def test_static_scratch_rejects_oversized_problem():
     out = _outputs(T, N, K, S, dev)
     assert _call(L, "s3r_ec_correct_static", q, T, N, S, W, X, 1, out) == -8
     assert "static array holds" in L.s3r_last_error().decode()
+
+
+@pytest.mark.parametrize("fmt", [0, 1], ids=["s8", "f16"])
+def test_static_scratch_in_a_captured_graph(fmt):
+    """The call inside a CUDA graph capture (the global capture mode, which
+    refuses calls that could allocate or synchronize), then replayed over new
+    gradients written into the captured partials: every replay must equal the
+    workspace version on the same inputs bit for bit."""
+    import stochastic_rounding_int8_gb300 as s3r
+    L = s3r.lib()
+    T, N, K, S = 4096, 1024, 2816, 1024
+    dev = "cuda"
+    rng = np.random.default_rng(7)
+    dt = torch.float16 if fmt else torch.int8
+    W = torch.from_numpy(rng.integers(-127, 128, size=(K, N)).astype(np.int8)).to(dt).to(dev)
+    X = torch.from_numpy(rng.integers(-127, 128, size=(T, K)).astype(np.int8)).to(dt).to(dev)
+    grad = lambda: torch.from_numpy((rng.standard_t(3, size=(T, N)) * 1e-3).astype(np.float32)).to(
+        torch.bfloat16).to(dev)
+    q = s3r.s3r_quantize(grad(), seed=0, tensor_id=3, code_format=fmt)
+    st = s3r.new_status()
+    got = _outputs(T, N, K, S, dev)
+    assert _call(L, "s3r_ec_correct_static", q, T, N, S, W, X, fmt, got, status=st) == 0   # warm-up, eager
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rc = _call(L, "s3r_ec_correct_static", q, T, N, S, W, X, fmt, got, status=st)
+    assert rc == 0, L.s3r_last_error().decode()
+    ws = torch.empty(L.s3r_ec_workspace_size(T, K), dtype=torch.uint8, device=dev)
+    for rep in range(3):
+        s3r.s3r_quantize(grad(), seed=10 + rep, tensor_id=3, code_format=fmt, out=q)
+        for v in got.values():
+            v.fill_(-1)
+        g.replay()
+        ref = _outputs(T, N, K, S, dev)
+        assert _call(L, "s3r_ec_correct", q, T, N, S, W, X, fmt, ref, ws=ws) == 0
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for k in ("rowsum", "xsum", "eps", "mu", "colmean", "v", "p"):
+            assert torch.equal(got[k], ref[k]), (rep, k)
