@@ -206,18 +206,20 @@ def device_ops(s3r, inp, code_format=None):
     return ops
 
 
-def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse=False):
+def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse=False, widen=False):
     """Device time of `steps` ffn_backward calls on resident inputs: total ms
     between two events around the loop, launches counted by the library, and
     (events=True) each step's per-step-boundary event times [steps, 8].
-    fuse: the SwiGLU glue inside the dA GEMM's epilogue."""
+    fuse: the SwiGLU glue inside the dA GEMM's epilogue.  widen: int8 operand
+    codes widened inside the call (S3R_CODES_S8_F16)."""
     T, d, F, S = blk.T, blk.d, blk.F, blk.S
-    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, rm, ec, s3r.code_format_of(ops.X8)), dtype=torch.uint8,
-                     device="cuda")
+    fmt = s3r.CODES_S8_F16 if widen else s3r.code_format_of(ops.X8)
+    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, rm, ec, fmt), dtype=torch.uint8, device="cuda")
     grads = s3r.alloc_ffn_grads(T, d, F)
     st = s3r.new_status()
     for i in range(warmup):
-        s3r.ffn_backward(ops, dY, S, rm, ec, seed=i, grads=grads, workspace=ws, status=st, fuse_glue=fuse)
+        s3r.ffn_backward(ops, dY, S, rm, ec, seed=i, grads=grads, workspace=ws, status=st, fuse_glue=fuse,
+                         widen_codes=widen)
     step_ev = None
     if events:
         step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(s3r.FFN_NUM_EVENTS)] for _ in range(steps)]
@@ -231,7 +233,7 @@ def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse
     t0.record()
     for i in range(steps):
         s3r.ffn_backward(ops, dY, S, rm, ec, seed=1000 + i, grads=grads, workspace=ws, status=st,
-                         step_events=step_ev[i] if events else None, fuse_glue=fuse)
+                         step_events=step_ev[i] if events else None, fuse_glue=fuse, widen_codes=widen)
     t1.record()
     torch.cuda.synchronize()
     launches = s3r.kernel_launch_count() - n0
@@ -422,7 +424,8 @@ def block_line(s3r, blk, inp, ops, dY, steps, warmup, world, pk, pk_kind):
 
 def mode_context(s3r, blk, ops, dY, inp, steps=8, warmup=2):
     """The same block under the other rounding / correction modes, int8 code
-    storage (mma.sync path) and the BF16 cuBLAS backward."""
+    storage (the mma.sync path, and widened to fp16 inside the call) and the
+    BF16 cuBLAS backward."""
     ctx = {}
     for name, rm, ec in (("s3r_ec_dx_only", s3r.ROUND_S3R, s3r.EC_DX_ONLY), ("s3r", s3r.ROUND_S3R, s3r.EC_NONE),
                          ("indep_sr_int8", s3r.ROUND_INDEP, s3r.EC_NONE), ("rtne_int8", s3r.ROUND_RTNE, s3r.EC_NONE),
@@ -439,6 +442,10 @@ def mode_context(s3r, blk, ops, dY, inp, steps=8, warmup=2):
     ops8 = device_ops(s3r, inp, s3r.CODES_S8)
     m, _, _ = time_ffn(s3r, blk, ops8, dY, 3, 1, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1)
     ctx["s3r_ec_two_way_int8_storage_mma_sync"] = {"tokens_s": round(blk.T * 3 / (m * 1e-3), 1), "ms": round(m / 3, 4)}
+    # the same int8 operand codes widened to fp16 inside the call, then the tcgen05 block
+    m, _, _ = time_ffn(s3r, blk, ops8, dY, steps, warmup, s3r.ROUND_S3R, s3r.EC_TWO_WAY, 1, widen=True)
+    ctx["s3r_ec_two_way_int8_codes_widened"] = {"tokens_s": round(blk.T * steps / (m * 1e-3), 1),
+                                                "ms": round(m / steps, 4)}
     del ops8
     bms = time_bf16_backward(inp, steps, warmup)
     ctx["bf16_cublas_backward"] = {"tokens_s": round(blk.T / (bms * 1e-3), 1), "ms": round(bms, 4)}
