@@ -250,7 +250,7 @@ def time_ffn(s3r, blk, ops, dY, steps, warmup, rm, ec, world, events=False, fuse
 E2E_CODES = ("X8", "A8", "W1_8", "W3_8", "W2_8")
 
 
-def time_e2e(s3r, blk, inp, ops, steps, warmup, world, int8_at_rest=True):
+def time_e2e(s3r, blk, inp, ops, steps, warmup, world, int8_at_rest=True, recompute_a=True):
     """Same step through the C ABI with HOST buffers: every step copies all of
     its inputs from pinned host memory to the device, runs the backward, and
     copies all four gradients back, inside the timed region.  The copies run
@@ -259,19 +259,24 @@ def time_e2e(s3r, blk, inp, ops, steps, warmup, world, int8_at_rest=True):
     way a training loop feeds a device); events order the buffers' reuse.
     int8_at_rest: the operand codes live in host memory as int8 (half the
     bytes over the host link) and the call widens them on the device
-    (S3R_CODES_S8_F16); otherwise they are copied as fp16 codes."""
+    (S3R_CODES_S8_F16); otherwise they are copied as fp16 codes.  recompute_a:
+    the codes of a and their scales are not kept by the forward; the call forms
+    them from h1 and h3 (S3R_FFN_RECOMPUTE_A)."""
     T, d, F, S = blk.T, blk.d, blk.F, blk.S
     conv = (lambda k, t: t.to(torch.int8) if k in E2E_CODES else t) if int8_at_rest else (lambda k, t: t)
-    host_in = {k: conv(k, getattr(ops, k)).cpu().pin_memory() for k in
-               ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2", "h1", "h3")}
+    keys = ("X8", "s_x", "A8", "s_a", "W1_8", "s_w1", "W3_8", "s_w3", "W2_8", "s_w2", "h1", "h3")
+    host_in = {k: conv(k, getattr(ops, k)).cpu().pin_memory() for k in keys
+               if not (recompute_a and k in ("A8", "s_a"))}
     host_in["dY"] = inp.dY.pin_memory()
     dev_in = [{k: torch.empty_like(v, device="cuda") for k, v in host_in.items()} for _ in range(2)]
-    dops = [s3r.FFNOperands(**{k: di[k] for k in host_in if k != "dY"}) for di in dev_in]
+    dops = [s3r.FFNOperands(**{k: di.get(k) for k in keys}) for di in dev_in]
     grads = [s3r.alloc_ffn_grads(T, d, F) for _ in range(2)]
     host_out = [{k: torch.empty(getattr(grads[0], k).shape, dtype=torch.float32).pin_memory()
                  for k in ("dX", "dW1", "dW3", "dW2")} for _ in range(2)]
     fmt = s3r.CODES_S8_F16 if int8_at_rest else s3r.code_format_of(ops.X8)
-    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, code_format=fmt), dtype=torch.uint8, device="cuda")
+    flags = s3r.FFN_RECOMPUTE_A if recompute_a else 0
+    ws = torch.empty(s3r.ffn_workspace_size(T, d, F, S, code_format=fmt, flags=flags), dtype=torch.uint8,
+                     device="cuda")
     bi = sum(v.numel() * v.element_size() for v in host_in.values())
     bo = sum(v.numel() * v.element_size() for v in host_out[0].values())
     # the input copies spread over N_IN streams (balanced by bytes), so several copy engines share them
@@ -305,7 +310,7 @@ def time_e2e(s3r, blk, inp, ops, steps, warmup, world, int8_at_rest=True):
             if used[b]:
                 s_comp.wait_event(out_done[b])   # step i - 2's gradients have left the device
             s3r.ffn_backward(dops[b], dev_in[b]["dY"], S, seed=i, grads=grads[b], workspace=ws, stream=s_comp,
-                             widen_codes=int8_at_rest)
+                             widen_codes=int8_at_rest, recompute_a=recompute_a)
             comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -690,16 +695,24 @@ def run_ours(args, world, rank, local):
     # as many steps as the device-timed leg: the timed region includes filling the copy pipeline
     # (the first step's inputs) and draining it (the last step's gradients)
     e2e_steps = max(3, args.steps)
-    ems, bi, bo = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world)
-    line["e2e"] = {"value": round(world * blk.T * e2e_steps / (ems * 1e-3), 1), "unit": "tokens/s",
+    # the host link is shared with the machine's other work and its rate swings between runs:
+    # three runs, the median reported, all three listed
+    runs = []
+    for _ in range(3):
+        ems, bi, bo = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world)
+        runs.append(world * blk.T * e2e_steps / (ems * 1e-3))
+    line["e2e"] = {"value": round(sorted(runs)[1], 1), "unit": "tokens/s",
                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+                   "runs": [round(v, 1) for v in runs], "statistic": "median of the runs",
                    "copies": "every step copies all inputs in and all four gradients out; the copies run on their "
                              "own streams, double-buffered, overlapping the neighbouring steps' backward",
-                   "operand_codes_at_rest": "int8 (ffn_backward widens them on the device, S3R_CODES_S8_F16)"}
+                   "operand_codes_at_rest": "int8 (ffn_backward widens them on the device, S3R_CODES_S8_F16)",
+                   "codes_of_a": "formed by the call from h1 and h3 (S3R_FFN_RECOMPUTE_A), not copied"}
     if not args.no_context and rank == 0:
         ctx = mode_context(s3r, blk, ops, dY, inp)
         ctx["s3r_ec_two_way_vs_bf16"] = round(ctx["bf16_cublas_backward"]["ms"] / r["ms_per_step"], 3)
-        ems16, bi16, bo16 = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world, int8_at_rest=False)
+        ems16, bi16, bo16 = time_e2e(s3r, blk, inp, ops, e2e_steps, min(args.warmup, 2), world, int8_at_rest=False,
+                                     recompute_a=False)
         ctx["e2e_fp16_codes_at_rest"] = {"tokens_s": round(world * blk.T * e2e_steps / (ems16 * 1e-3), 1),
                                          "h2d_bytes_per_step": bi16, "d2h_bytes_per_step": bo16}
         ctx["s3r_ec_two_way_vs_indep_sr"] = round(ctx["indep_sr_int8"]["ms"] / r["ms_per_step"], 3)

@@ -511,6 +511,17 @@ int ffn_forward(const struct s3r_ffn_fwd_args* args, cudaStream_t stream);
  * code_format and add 2 bytes per operand code (plus alignment) to the
  * S3R_CODES_F16 size.
  *
+ * flags & S3R_FFN_RECOMPUTE_A (A8 and s_a NULL, S3R_ERR_ARG otherwise): the
+ * call forms the codes of a and their scales itself, from h1 and h3, with the
+ * forward's own kernel (swiglu_fwd_quantize: a = bf16(silu(h1) h3), per-token
+ * RTNE codes in the format the block computes in), into the tail of the
+ * workspace, and then runs the block on them.  The results equal a call
+ * given the A8 and s_a that swiglu_fwd_quantize makes from the same h1 and
+ * h3, bit for bit; the forward then need not keep A8 (T F codes) at all, and
+ * a backward fed from host memory moves that much less.  Workspace:
+ * s3r_ffn_workspace_size_flags / s3r_ffn_grouped_workspace_size_flags with
+ * the same flags.
+ *
  * Grouped (mixture-of-experts) mode, num_groups = E > 0 (the MoE models of
  * [S3R] §IV; the pages give no grouping rule, so the plain one): the T rows
  * of dY, h1, h3, X8/s_x, A8/s_a and dX are routed rows sorted by expert, and
@@ -566,16 +577,23 @@ struct s3r_ffn_args {
                                     after steps 1, 2, 3, 4, 5, 6, 7, 8 above (for timing) */
     int64_t num_groups;          /* 0: one dense block; E > 0: grouped mode (above) */
     const int64_t* group_offsets; /* grouped mode: HOST [E + 1] row offsets */
-    int flags;                   /* 0, or S3R_FFN_FUSE_GLUE (above) */
+    int flags;                   /* 0, or S3R_FFN_FUSE_GLUE | S3R_FFN_RECOMPUTE_A (above) */
 };
 #define S3R_FFN_NUM_EVENTS 9
 #define S3R_FFN_FUSE_GLUE 1
+#define S3R_FFN_RECOMPUTE_A 2
 size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
                               int code_format);
 /* grouped mode: group_offsets is the HOST [num_groups + 1] array of the call;
    0 for invalid offsets */
 size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, int64_t num_groups, int64_t d, int64_t F,
                                       int round_mode, int ec_mode, int code_format);
+/* the workspace of a call with these flags (S3R_FFN_RECOMPUTE_A adds the
+   recomputed codes of a and their scales); 0 for invalid sizes */
+size_t s3r_ffn_workspace_size_flags(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
+                                    int code_format, int flags);
+size_t s3r_ffn_grouped_workspace_size_flags(const int64_t* group_offsets, int64_t num_groups, int64_t d, int64_t F,
+                                            int round_mode, int ec_mode, int code_format, int flags);
 int ffn_backward(const struct s3r_ffn_args* args, cudaStream_t stream);
 
 /*

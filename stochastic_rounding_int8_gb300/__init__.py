@@ -79,6 +79,8 @@ _SIGS = {
     "s3r_sr_fp8": (_INT, [_VP, _I64, _I64, _I64, C.c_float, _INT, _U64, _U32, _VP, _I64, _VP]),
     "s3r_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT]),
     "s3r_ffn_grouped_workspace_size": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT]),
+    "s3r_ffn_workspace_size_flags": (_SZ, [_I64, _I64, _I64, _I64, _INT, _INT, _INT, _INT]),
+    "s3r_ffn_grouped_workspace_size_flags": (_SZ, [_VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT]),
     "ffn_backward": (_INT, [_VP, _VP]),
     "s3r_ffn_workspace_offsets": (_INT, [_I64, _I64, _I64, _I64, _INT, _INT, _VP, _I64, _I64, _VP]),
     "s3r_debug_dx_blocks": (_INT, [_VP, _VP, _INT, _I64, _I64, _I64, _VP, _VP]),
@@ -556,6 +558,7 @@ class _FfnArgs(C.Structure):
 
 FFN_NUM_EVENTS = 9
 FFN_FUSE_GLUE = 1   # S3R_FFN_FUSE_GLUE
+FFN_RECOMPUTE_A = 2   # S3R_FFN_RECOMPUTE_A
 FFN_STEPS = ["quantize dY", "EC W2", "GEMM dA (dX of W2)", "GEMM dW2", "SwiGLU + quantize dh1/dh3", "EC W1/W3",
              "GEMM dX (W1 + W3)", "GEMM dW1 + dW3"]
 # with fp16 codes, steps 3 + 4 and 7 + 8 are one launch each (their time lands on 3 and 7)
@@ -590,16 +593,17 @@ def ffn_forward_operands(X, W1, W3, W2, a, h1, h3, stream=None, code_format=DEFA
     return FFNOperands(X8, s_x, A8, s_a, W1_8, s_w1, W3_8, s_w3, W2_8, s_w2, h1, h3)
 
 
-def ffn_workspace_size(T, d, F, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, code_format=DEFAULT_CODES) -> int:
-    return int(lib().s3r_ffn_workspace_size(T, d, F, S, round_mode, ec_mode, code_format))
+def ffn_workspace_size(T, d, F, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, code_format=DEFAULT_CODES,
+                       flags=0) -> int:
+    return int(lib().s3r_ffn_workspace_size_flags(T, d, F, S, round_mode, ec_mode, code_format, flags))
 
 
 def grouped_workspace_size(group_offsets, d, F, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY,
-                           code_format=DEFAULT_CODES) -> int:
+                           code_format=DEFAULT_CODES, flags=0) -> int:
     offs = [int(o) for o in group_offsets]
     arr = (C.c_int64 * len(offs))(*offs)
-    return int(lib().s3r_ffn_grouped_workspace_size(C.cast(arr, _VP), len(offs) - 1, d, F, round_mode, ec_mode,
-                                                    code_format))
+    return int(lib().s3r_ffn_grouped_workspace_size_flags(C.cast(arr, _VP), len(offs) - 1, d, F, round_mode,
+                                                          ec_mode, code_format, flags))
 
 
 @dataclass
@@ -637,7 +641,8 @@ def alloc_moe_grads(R, E, d, F, device="cuda") -> FFNGrads:
 
 def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_WAY, seed=0,
                  grads: FFNGrads | None = None, workspace=None, status=None, stream=None,
-                 step_events=None, group_offsets=None, fuse_glue=False, widen_codes=False) -> FFNGrads:
+                 step_events=None, group_offsets=None, fuse_glue=False, widen_codes=False,
+                 recompute_a=False) -> FFNGrads:
     """step_events: optional list of FFN_NUM_EVENTS torch.cuda.Event (timing).
     group_offsets: grouped (mixture-of-experts) mode, a list of E + 1 row
     offsets of the expert-sorted rows; the weights in `ops` are then stacked
@@ -645,11 +650,15 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
     quantization of dh1, dh3 inside the dA GEMM's epilogue (S3R_FFN_FUSE_GLUE;
     dense block with fp16 codes, not independent SR; dA is then not kept).
     widen_codes: int8 operand codes in `ops` run as fp16 codes (S3R_CODES_S8_F16:
-    widened inside the call, results equal to the fp16-code call)."""
+    widened inside the call, results equal to the fp16-code call).
+    recompute_a: the call forms the codes of a and their scales from h1 and h3
+    (S3R_FFN_RECOMPUTE_A); ops.A8 and ops.s_a are then not used (may be None)."""
     T, d = dY.shape
-    F = ops.A8.shape[1]
+    F = ops.h1.shape[1]
     dev = dY.device
     fmt = code_format_of(ops.X8)
+    flags = (FFN_FUSE_GLUE if fuse_glue else 0) | (FFN_RECOMPUTE_A if recompute_a else 0)
+    a8, s_a = (None, None) if recompute_a else (ops.A8, ops.s_a)
     if widen_codes:
         if fmt != CODES_S8:
             raise ValueError("widen_codes takes int8 operand codes")
@@ -660,20 +669,20 @@ def ffn_backward(ops: FFNOperands, dY, S, round_mode=ROUND_S3R, ec_mode=EC_TWO_W
         tmax = max([b - a for a, b in zip(offs[:-1], offs[1:])] + [1])
         if grads is None:
             grads = alloc_moe_grads(T, E, d, F, dev)
-        need = grouped_workspace_size(offs, d, F, round_mode, ec_mode, fmt)
+        need = grouped_workspace_size(offs, d, F, round_mode, ec_mode, fmt, flags)
         S = 0
     else:
         if grads is None:
             grads = alloc_ffn_grads(T, d, F, dev)
-        need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode, fmt)
+        need = ffn_workspace_size(T, d, F, S, round_mode, ec_mode, fmt, flags)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     p = lambda t: None if t is None else t.data_ptr()
-    args = _FfnArgs(T, d, F, S, p(_bits(dY)), p(_bits(ops.h1)), p(_bits(ops.h3)), p(ops.X8), p(ops.s_x), p(ops.A8),
-                    p(ops.s_a), p(ops.W1_8), p(ops.s_w1), p(ops.W3_8), p(ops.s_w3), p(ops.W2_8), p(ops.s_w2),
+    args = _FfnArgs(T, d, F, S, p(_bits(dY)), p(_bits(ops.h1)), p(_bits(ops.h3)), p(ops.X8), p(ops.s_x), p(a8),
+                    p(s_a), p(ops.W1_8), p(ops.s_w1), p(ops.W3_8), p(ops.s_w3), p(ops.W2_8), p(ops.s_w2),
                     round_mode, ec_mode, fmt, seed, p(grads.dX), p(grads.dW1), p(grads.dW3), p(grads.dW2),
                     p(workspace), workspace.numel(), p(status), None)
-    args.flags = FFN_FUSE_GLUE if fuse_glue else 0
+    args.flags = flags
     if group_offsets is not None:
         off_arr = (C.c_int64 * len(offs))(*offs)   # kept alive until the call returns
         args.num_groups = len(offs) - 1

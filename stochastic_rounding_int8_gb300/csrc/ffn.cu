@@ -180,6 +180,13 @@ size_t widen_bytes(int64_t T, int64_t d, int64_t F, int64_t E) {
     return 255 + r(2 * T * d) + r(2 * T * F) + 2 * r(2 * E * d * F) + r(2 * E * F * d);
 }
 
+// S3R_FFN_RECOMPUTE_A: the recomputed codes of a [T, F] (in the format the block computes in)
+// and their scales [T] follow everything else.
+size_t recompute_bytes(int64_t T, int64_t F, int fmt) {
+    auto r = [](int64_t b) { return (size_t)((b + 255) / 256 * 256); };
+    return 255 + r(T * F * (fmt == S3R_CODES_S8 ? 1 : 2)) + r(4 * T);
+}
+
 extern "C" size_t s3r_ffn_workspace_size(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode, int ec_mode,
                                          int code_format) {
     (void)ec_mode;
@@ -483,6 +490,12 @@ size_t grouped_bytes(const int64_t* off, int64_t E, int64_t d, int64_t F, int ro
 
 }  // namespace
 
+extern "C" size_t s3r_ffn_workspace_size_flags(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode,
+                                               int ec_mode, int code_format, int flags) {
+    const size_t n = s3r_ffn_workspace_size(T, d, F, S, round_mode, ec_mode, code_format);
+    return n && (flags & S3R_FFN_RECOMPUTE_A) ? n + recompute_bytes(T, F, code_format) : n;
+}
+
 extern "C" size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, int64_t num_groups, int64_t d,
                                                  int64_t F, int round_mode, int ec_mode, int code_format) {
     (void)ec_mode;
@@ -493,6 +506,14 @@ extern "C" size_t s3r_ffn_grouped_workspace_size(const int64_t* group_offsets, i
         return grouped_bytes(group_offsets, num_groups, d, F, round_mode, S3R_CODES_F16) +
                widen_bytes(group_offsets[num_groups] - group_offsets[0], d, F, num_groups);
     return grouped_bytes(group_offsets, num_groups, d, F, round_mode, code_format);
+}
+
+extern "C" size_t s3r_ffn_grouped_workspace_size_flags(const int64_t* group_offsets, int64_t num_groups, int64_t d,
+                                                       int64_t F, int round_mode, int ec_mode, int code_format,
+                                                       int flags) {
+    const size_t n = s3r_ffn_grouped_workspace_size(group_offsets, num_groups, d, F, round_mode, ec_mode, code_format);
+    if (!n || !(flags & S3R_FFN_RECOMPUTE_A)) return n;
+    return n + recompute_bytes(group_offsets[num_groups] - group_offsets[0], F, code_format);
 }
 
 extern "C" int s3r_ffn_workspace_offsets(int64_t T, int64_t d, int64_t F, int64_t S, int round_mode,
@@ -536,9 +557,11 @@ int check_block_args(const s3r_ffn_args* a) {
     if (a->ec_mode < S3R_EC_NONE || a->ec_mode > S3R_EC_DW_ONLY) return S3R_ERR_ARG;
     if (a->code_format != S3R_CODES_S8 && a->code_format != S3R_CODES_F16 && a->code_format != S3R_CODES_S8_F16)
         return S3R_ERR_ARG;
-    if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->A8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 ||
-        !a->dW2 || !a->dW3)
+    if (!a->dY || !a->h1 || !a->h3 || !a->X8 || !a->W1_8 || !a->W3_8 || !a->W2_8 || !a->dX || !a->dW1 || !a->dW2 ||
+        !a->dW3)
         return S3R_ERR_ARG;
+    // A8 and s_a come from the caller, or (S3R_FFN_RECOMPUTE_A) from the call itself
+    if ((a->flags & S3R_FFN_RECOMPUTE_A) ? (a->A8 || a->s_a) : !a->A8) return S3R_ERR_ARG;
     if (a->num_groups == 0) {
         if (S <= 0) return S3R_ERR_ARG;
         if (T % S != 0 || (S % S3R_TILE != 0 && S != T)) return S3R_ERR_SHAPE;
@@ -602,7 +625,7 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const WidenJobs J) {
 
 // S3R_CODES_S8_F16: widens X8, A8, W1_8, W3_8 and W2_8 into the tail of the
 // workspace, then runs the fp16-code block on the copies.
-int ffn_backward_widened(const s3r_ffn_args* a, cudaStream_t stream) {
+int ffn_backward_widened(const s3r_ffn_args* a, cudaStream_t stream, const void* A8_f16 = nullptr) {
     const int64_t T = a->T, d = a->d, F = a->F;   // the arguments passed check_block_args
     const bool grouped = a->num_groups > 0;
     const int64_t E = grouped ? a->num_groups : 1;
@@ -620,13 +643,18 @@ int ffn_backward_widened(const s3r_ffn_args* a, cudaStream_t stream) {
     const void* src[5] = {a->X8, a->A8, a->W1_8, a->W3_8, a->W2_8};
     const int64_t n[5] = {T * d, T * F, E * d * F, E * d * F, E * F * d};
     const void** dst[5] = {&w.X8, &w.A8, &w.W1_8, &w.W3_8, &w.W2_8};
+    J.n = 0;
     for (int i = 0; i < 5; ++i) {
-        J.j[i] = WidenJob{static_cast<const int8_t*>(src[i]), reinterpret_cast<uint16_t*>(p), n[i]};
-        *dst[i] = reinterpret_cast<const void*>(p);
+        if (i == 1 && A8_f16) {   // the codes of a are fp16 already (recomputed by the call)
+            w.A8 = A8_f16;
+        } else {
+            J.j[J.n++] = WidenJob{static_cast<const int8_t*>(src[i]), reinterpret_cast<uint16_t*>(p), n[i]};
+            *dst[i] = reinterpret_cast<const void*>(p);
+        }
         p += (uintptr_t)((2 * n[i] + 255) / 256 * 256);
     }
-    J.n = 5;
-    const int64_t total16 = (T * (d + F) + 3 * E * d * F) / 16;
+    int64_t total16 = 0;
+    for (int i = 0; i < J.n; ++i) total16 += J.j[i].n / 16;
     const int64_t cap = (int64_t)s3r_sm_count() * 8;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(cap, (total16 + 255) / 256));
     widen_codes_kernel<<<grid, 256, 0, stream>>>(J);
@@ -634,10 +662,38 @@ int ffn_backward_widened(const s3r_ffn_args* a, cudaStream_t stream) {
     return ffn_backward(&w, stream);
 }
 
+// S3R_FFN_RECOMPUTE_A: the codes of a and their scales from h1 and h3 with the
+// forward's own kernel (swiglu_fwd_quantize: a = bf16(silu(h1) h3), per-token
+// RTNE), into the tail of the workspace, then the block on them.
+int ffn_backward_recompute(const s3r_ffn_args* a, cudaStream_t stream) {
+    const int64_t T = a->T, d = a->d, F = a->F;   // the arguments passed check_block_args
+    const int fmt = a->code_format, ifmt = fmt == S3R_CODES_S8 ? S3R_CODES_S8 : S3R_CODES_F16;
+    const size_t base = a->num_groups > 0
+                            ? s3r_ffn_grouped_workspace_size(a->group_offsets, a->num_groups, d, F, a->round_mode,
+                                                             a->ec_mode, fmt)
+                            : s3r_ffn_workspace_size(T, d, F, a->S, a->round_mode, a->ec_mode, fmt);
+    if (base == 0) return S3R_ERR_ARG;
+    if (!a->workspace || a->workspace_bytes < base + recompute_bytes(T, F, fmt)) return S3R_ERR_WORKSPACE;
+    if (F % 8 != 0 || !s3r_aligned16(a->h1) || !s3r_aligned16(a->h3)) return S3R_ERR_ALIGN;
+    uintptr_t p = ((uintptr_t)a->workspace + base + 255) & ~(uintptr_t)255;
+    void* A8 = reinterpret_cast<void*>(p);
+    p += (uintptr_t)((T * F * (ifmt == S3R_CODES_S8 ? 1 : 2) + 255) / 256 * 256);
+    float* s_a = reinterpret_cast<float*>(p);
+    S3R_TRY(swiglu_fwd_quantize(a->h1, a->h3, T, F, F, nullptr, A8, ifmt, s_a, a->d_status, stream));
+    s3r_ffn_args w = *a;
+    w.flags &= ~S3R_FFN_RECOMPUTE_A;
+    w.workspace_bytes = base;
+    w.s_a = s_a;
+    if (fmt == S3R_CODES_S8_F16) return ffn_backward_widened(&w, stream, A8);
+    w.A8 = A8;
+    return ffn_backward(&w, stream);
+}
+
 }  // namespace
 
 extern "C" int ffn_backward(const struct s3r_ffn_args* a, cudaStream_t stream) {
     S3R_TRY(check_block_args(a));
+    if (a->flags & S3R_FFN_RECOMPUTE_A) return ffn_backward_recompute(a, stream);
     if (a->code_format == S3R_CODES_S8_F16) return ffn_backward_widened(a, stream);
     const int64_t T = a->T, d = a->d, F = a->F, S = a->S;
     const int fmt = a->code_format;
@@ -849,4 +905,4 @@ extern "C" const char* s3r_status_string(int status) {
     }
 }
 
-extern "C" int s3r_abi_version(void) { return 103; }
+extern "C" int s3r_abi_version(void) { return 104; }

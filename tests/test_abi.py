@@ -33,7 +33,7 @@ def test_status_strings(L):
     for code in range(-1, -9, -1):
         assert s3r.status_string(code).startswith("S3R_ERR_")
     assert s3r.status_string(-99) == "S3R_ERR_UNKNOWN"
-    assert L.s3r_abi_version() == 103
+    assert L.s3r_abi_version() == 104
 
 
 def test_host_argument_checks_need_no_gpu(L):
@@ -191,4 +191,37 @@ def test_widened_codes_workspace_and_checks(L):
     before = L.s3r_kernel_launch_count()
     assert call(132, F, 1 << 40) == -2                # d not a multiple of 8: the fp16 GEMMs' rows
     assert call(d, F, wide - 1) == -7                 # the widened copies do not fit
+    assert L.s3r_kernel_launch_count() == before
+
+
+def test_recompute_a_workspace_and_checks(L):
+    """S3R_FFN_RECOMPUTE_A: the workspace adds the recomputed codes of a and
+    their scales; A8 and s_a must be NULL with the flag and A8 given without
+    it, all checked before any launch (fake, never-dereferenced pointers)."""
+    r = lambda b: (b + 255) // 256 * 256
+    T, d, F, S = 512, 136, 392, 256
+    R = s3r.FFN_RECOMPUTE_A
+    for fmt, cs in ((s3r.CODES_F16, 2), (s3r.CODES_S8_F16, 2), (s3r.CODES_S8, 1)):
+        base = L.s3r_ffn_workspace_size(T, d, F, S, 1, 2, fmt)
+        assert L.s3r_ffn_workspace_size_flags(T, d, F, S, 1, 2, fmt, 0) == base
+        assert L.s3r_ffn_workspace_size_flags(T, d, F, S, 1, 2, fmt, R) == base + 255 + r(cs * T * F) + r(4 * T)
+    offs = [0, 300, 300, 812]
+    arr = (C.c_int64 * 4)(*offs)
+    g = L.s3r_ffn_grouped_workspace_size(C.cast(arr, C.c_void_p), 3, d, F, 1, 2, s3r.CODES_F16)
+    assert L.s3r_ffn_grouped_workspace_size_flags(C.cast(arr, C.c_void_p), 3, d, F, 1, 2, s3r.CODES_F16, R) == \
+        g + 255 + r(2 * 812 * F) + r(4 * 812)
+    fake = C.c_void_p(0x1000)
+    need = L.s3r_ffn_workspace_size_flags(T, d, F, S, 1, 2, s3r.CODES_F16, R)
+
+    def call(a8, s_a, flags, ws_bytes):
+        args = s3r._FfnArgs(T, d, F, S, fake, fake, fake, fake, fake, a8, s_a, fake, fake, fake, fake, fake, fake,
+                            s3r.ROUND_S3R, s3r.EC_TWO_WAY, s3r.CODES_F16, 0, fake, fake, fake, fake, fake,
+                            ws_bytes, None, None)
+        args.flags = flags
+        return L.ffn_backward(C.byref(args), None)
+    before = L.s3r_kernel_launch_count()
+    assert call(fake, None, R, need) == -1        # A8 given with the flag
+    assert call(None, fake, R, need) == -1        # s_a given with the flag
+    assert call(None, None, 0, need) == -1        # no A8 and no flag
+    assert call(None, None, R, need - 1) == -7    # the recomputed codes do not fit
     assert L.s3r_kernel_launch_count() == before
